@@ -1,0 +1,403 @@
+#!/usr/bin/env python3
+"""Benchmark of the GLA forward hot path on GB300 (one JSON line on stdout).
+
+Default workload (N=1): the chunked forward at B=2, H=16, T=32768, dk=128,
+dv=256 (the long-sequence prefill workload the prefill roofline target is
+stated on), plus the decode step at B=256, H=32, dk=dv=128 reported under
+"decode".  A step is one gla_chunk_fwd call over the whole batch, inputs
+resident in HBM (2.15 GB of inputs, far larger than the 129 MB L2, so no L2
+flush is needed between steps).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the only reference this method
+has here) on a bounded sample of the same workload, on the host cores.
+Multi-GPU (torchrun): every rank runs its own replica of the workload (heads
+are independent; there is no exchange step), value = all ranks' tokens / the
+slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GLA chunk-fwd tokens/s (B·H·T) and % roofline; decode steps/s and HBM GB/s"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# --------------------------------------------------------------------------- workloads
+
+def chunk_bytes(cfg) -> int:
+    """Algorithmic bytes of one chunked forward: each input read once, each output written once."""
+    per_token = 2 * cfg.dk + 2 * cfg.dk + 2 * cfg.dv + 4 * cfg.dk + 2 * cfg.dv
+    state = cfg.B * cfg.H * cfg.dk * cfg.dv * 4 * (2 if cfg.sigma_h0 is not None else 1)
+    return cfg.tokens * per_token + state
+
+
+def chunk_flops(cfg, C: int = 64) -> int:
+    """Algorithmic flops (causal entries only) at chunk size C, as counted for the roofline."""
+    return cfg.tokens * ((C + 1) * (cfg.dk + cfg.dv) + 4 * cfg.dk * cfg.dv)
+
+
+def decode_bytes(cfg) -> int:
+    return cfg.B * cfg.H * (8 * cfg.dk * cfg.dv + 2 * cfg.dk + 2 * cfg.dk + 4 * cfg.dk
+                            + 2 * cfg.dv + 2 * cfg.dv)
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"gla_bench_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}",
+                                          f"--query-gpu={self.QUERY}", "--format=csv,noheader",
+                                          "-lms", "100"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            for line in open(self.path):
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1].split()[0]))
+                    smax = float(parts[2].split()[0])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        except OSError:
+            pass
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import __graft_entry__ as ge
+    ge.build()
+    import chunkwise_linear_rnn_gb300 as gla
+    from synth import CHUNK_CONFIGS, DECODE_CONFIG, make_config_inputs, make_decode_inputs
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    def max_over_ranks(x: float) -> float:
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    pk, pk_kind = peaks()
+    cfg = CHUNK_CONFIGS[args.workload]
+    q, k, v, a, h0 = make_config_inputs(cfg, seed=rank, device=dev)
+    o = torch.empty(cfg.B, cfg.H, cfg.T, cfg.dv, dtype=torch.bfloat16, device=dev)
+    hT = torch.empty(cfg.B, cfg.H, cfg.dk, cfg.dv, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        gla.gla_chunk_fwd(q, k, v, a, cfg.scale, h0, out=o, final_state=hT)
+
+    launches_per_step = 1
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    with ClockSampler(dev.index) as clk:
+        barrier()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for s, e in ev:
+            s.record(stream)
+            step()
+            e.record(stream)
+        t_end.record(stream)
+        barrier()
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end))
+    per_launch_ms = statistics.mean(s.elapsed_time(e) for s, e in ev)
+    if gla.gla_last_device_status(dev) != 0:
+        raise RuntimeError("device status word reports an expired wait during the benchmark")
+    ms_per_step = total_ms / args.steps
+    tokens_all = cfg.tokens * world
+    value = tokens_all / (ms_per_step / 1e3)
+    byts = chunk_bytes(cfg)
+    achieved_gbs = byts / (per_launch_ms / 1e3) / 1e9
+    clocks = clk.summary()
+
+    # ---- end to end through the public API: pinned host buffers, copies in the timed region
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, ha = (t.cpu().pin_memory() for t in (q, k, v, a))
+        hh0 = None if h0 is None else h0.cpu().pin_memory()
+        ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        hhT = torch.empty(hT.shape, dtype=hT.dtype).pin_memory()
+        dq, dk_, dv_, da = (torch.empty_like(t) for t in (q, k, v, a))
+        dh0 = None if h0 is None else torch.empty_like(h0)
+
+        def e2e_step():
+            dq.copy_(hq, non_blocking=True)
+            dk_.copy_(hk, non_blocking=True)
+            dv_.copy_(hv, non_blocking=True)
+            da.copy_(ha, non_blocking=True)
+            if dh0 is not None:
+                dh0.copy_(hh0, non_blocking=True)
+            gla.gla_chunk_fwd(dq, dk_, dv_, da, cfg.scale, dh0, out=o, final_state=hT)
+            ho.copy_(o, non_blocking=True)
+            hhT.copy_(hT, non_blocking=True)
+
+        e2e_steps = max(2, min(args.steps, 5))
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        s1.record(stream)
+        barrier()
+        e2e_ms = max_over_ranks(s0.elapsed_time(s1)) / e2e_steps
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, ha)) + (
+            0 if hh0 is None else hh0.numel() * 4)
+        d2h = ho.numel() * 2 + hhT.numel() * 4
+        e2e = {"value": tokens_all / (e2e_ms / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": e2e_ms}
+        del hq, hk, hv, ha, hh0, ho, hhT, dq, dk_, dv_, da, dh0
+
+    del q, k, v, a, h0, o, hT
+    torch.cuda.empty_cache()
+
+    # ---- decode step (secondary numbers on the same line)
+    decode = None
+    if not args.no_decode:
+        dc = DECODE_CONFIG
+        nsteps = args.decode_steps
+        dh0, dqs, dks, dvs, das = make_decode_inputs(dc.B, dc.H, dc.dk, dc.dv, nsteps,
+                                                     sigma_z=dc.sigma_z, tau=dc.tau,
+                                                     sigma_h0=dc.sigma_h0, seed=rank, device=dev)
+        h = dh0.clone()
+        do = torch.empty(dc.B, dc.H, dc.dv, dtype=torch.bfloat16, device=dev)
+        for s in range(min(3, nsteps)):
+            gla.gla_recurrent_step(dqs[s], dks[s], dvs[s], das[s], h, dc.scale, out=do)
+        barrier()
+        d0 = torch.cuda.Event(enable_timing=True)
+        d1 = torch.cuda.Event(enable_timing=True)
+        d0.record(stream)
+        for s in range(nsteps):
+            gla.gla_recurrent_step(dqs[s], dks[s], dvs[s], das[s], h, dc.scale, out=do)
+        d1.record(stream)
+        barrier()
+        dms = max_over_ranks(d0.elapsed_time(d1)) / nsteps
+        dbytes = decode_bytes(dc)
+        dgbs = dbytes / (dms / 1e3) / 1e9
+        decode = {"workload": dc.name, "steps_per_s": 1e3 / dms, "replicas": world,
+                  "ms_per_step": dms, "hbm_gbs": dgbs, "bytes_per_step": dbytes,
+                  "frac_of_hbm_peak": dgbs / pk["hbm_gbs"], "timed_steps": nsteps,
+                  "gpu_launches": nsteps}
+        del dh0, dqs, dks, dvs, das, h, do
+        torch.cuda.empty_cache()
+
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": cfg.name, "B": cfg.B, "H": cfg.H, "T": cfg.T, "dk": cfg.dk,
+                   "dv": cfg.dv, "chunk": 128, "replicas": world,
+                   "l2": "inputs (%.2f GB) larger than L2; no flush" % (byts / 1e9)},
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": pk["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved_gbs / pk["hbm_gbs"], "traffic": None,
+                     "peak_kind": pk_kind, "kernel": "chunk_fwd_kernel",
+                     "algorithmic_bytes_per_launch": byts,
+                     "flops_per_launch": chunk_flops(cfg),
+                     "tensor_frac": chunk_flops(cfg) / (per_launch_ms / 1e3) / 1e12 /
+                     pk["bf16_tflops"]},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if decode is not None:
+        line["decode"] = decode
+    return line
+
+
+# --------------------------------------------------------------------------- CPU baseline
+
+def oracle_sample(cfg, target_s: float, threads: int):
+    """Time the fp64 oracle on a bounded sample of the workload; returns a cpu_baseline dict."""
+    import torch
+    from oracle import gla_oracle
+    from synth import make_chunk_inputs
+    gla_oracle.build()
+    heads = max(1, min(cfg.B * cfg.H, threads))
+    # estimate the per-token rate on a short probe, then size the sample to ~target_s
+    t_probe = 256
+    q, k, v, a, h0 = make_chunk_inputs(1, heads, t_probe, cfg.dk, cfg.dv, sigma_z=cfg.sigma_z,
+                                       tau=cfg.tau, sigma_h0=cfg.sigma_h0, seed=0)
+    c = lambda t: t.float().numpy()  # noqa: E731
+    t0 = time.perf_counter()
+    gla_oracle.forward(c(q), c(k), c(v), a.numpy(), cfg.scale,
+                       None if h0 is None else h0.double().numpy(), nthreads=threads)
+    dt = max(time.perf_counter() - t0, 1e-4)
+    T = int(min(cfg.T, max(t_probe, t_probe * target_s / dt)))
+    q, k, v, a, h0 = make_chunk_inputs(1, heads, T, cfg.dk, cfg.dv, sigma_z=cfg.sigma_z,
+                                       tau=cfg.tau, sigma_h0=cfg.sigma_h0, seed=0)
+    t0 = time.perf_counter()
+    gla_oracle.forward(c(q), c(k), c(v), a.numpy(), cfg.scale,
+                       None if h0 is None else h0.double().numpy(), nthreads=threads)
+    dt = time.perf_counter() - t0
+    used = min(threads, heads)
+    return {"value": heads * T / dt, "unit": "tokens/s", "cores": used, "kind": "oracle",
+            "sample": f"{heads} heads x {T} tokens of {cfg.name} (dk={cfg.dk}, dv={cfg.dv}), "
+                      f"fp64 recurrence, {dt:.1f} s"}
+
+
+def host_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args):
+    from synth import CHUNK_CONFIGS
+    cfg = CHUNK_CONFIGS[args.workload]
+    threads = host_threads()
+    per = []
+    base = None
+    for _ in range(max(1, args.warmup)):
+        oracle_sample(cfg, 0.5, threads)
+    for _ in range(args.steps):
+        base = oracle_sample(cfg, args.ref_seconds, threads)
+        per.append(base["value"])
+    value = statistics.median(per)
+    base["value"] = value
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": None,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": cfg.name, "B": cfg.B, "H": cfg.H, "T": cfg.T,
+                                        "dk": cfg.dk, "dv": cfg.dv},
+        "cpu_baseline": base,
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="long", choices=["small", "medium", "long", "very_long"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--decode-steps", type=int, default=256)
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-seconds", type=float, default=10.0,
+                    help="CPU seconds per oracle sample")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        log("warning: fewer than 3 warm-up steps")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            from synth import CHUNK_CONFIGS
+            line["cpu_baseline"] = oracle_sample(CHUNK_CONFIGS[args.workload], args.ref_seconds,
+                                                 host_threads())
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

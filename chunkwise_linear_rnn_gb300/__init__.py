@@ -1,0 +1,128 @@
+"""GB300-native gated linear attention (GLA) forward: chunked prefill and decode step.
+
+The computation ("Gated Linear Attention (GLA): Mathematical Foundations, ..."
+(llms.blog), section "The Gated Recurrent Update"):
+
+    S_t = diag(alpha_t) S_{t-1} + k_t^T v_t,      o_t = scale * q_t S_t
+
+runs entirely in the hand-written sm_103a kernels of ``libgla.so``; this module
+only checks and marshals PyTorch tensors into the C ABI of ``include/gla.h``
+(device pointers, sizes and the current CUDA stream).
+
+Layouts (contiguous, head-first): q, k ``[B,H,T,dk]`` bf16; v ``[B,H,T,dv]``
+bf16; log_alpha ``[B,H,T,dk]`` fp32; o ``[B,H,T,dv]`` bf16; h0 / hT
+``[B,H,dk,dv]`` fp32.
+"""
+
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import GlaChunkOptions, GlaError, status_string  # noqa: F401
+
+__all__ = ["gla_chunk_fwd", "gla_recurrent_step", "gla_last_device_status", "GlaError",
+           "status_string", "library_path"]
+
+library_path = _lib.LIB_PATH
+
+
+def _stream(device: torch.device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape: tuple, device) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda" or (device is not None and t.device != device):
+        raise ValueError(f"{name} must be on the CUDA device {device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def gla_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: torch.Tensor,
+                  scale: float | None = None, h0: torch.Tensor | None = None,
+                  output_final_state: bool = True, *, out: torch.Tensor | None = None,
+                  final_state: torch.Tensor | None = None, segments: int = 0, dv_tile: int = 0,
+                  force_exact: bool = False):
+    """Chunkwise-parallel GLA forward over whole sequences.
+
+    Returns ``(o, hT)``; ``hT`` is None when ``output_final_state`` is False.
+    ``final_state`` may be ``h0`` itself (in-place state update).
+    ``segments``, ``dv_tile`` and ``force_exact`` are the C ABI's options
+    (0 / False = automatic).
+    """
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, T, dk]")
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    dev = q.device
+    _need(q, "q", torch.bfloat16, (B, H, T, dk), dev)
+    _need(k, "k", torch.bfloat16, (B, H, T, dk), dev)
+    _need(v, "v", torch.bfloat16, (B, H, T, dv), dev)
+    _need(log_alpha, "log_alpha", torch.float32, (B, H, T, dk), dev)
+    if h0 is not None:
+        _need(h0, "h0", torch.float32, (B, H, dk, dv), dev)
+    if out is None:
+        out = torch.empty(B, H, T, dv, dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, (B, H, T, dv), dev)
+    hT = None
+    if output_final_state:
+        hT = final_state if final_state is not None else torch.empty(
+            B, H, dk, dv, dtype=torch.float32, device=dev)
+        _need(hT, "final_state", torch.float32, (B, H, dk, dv), dev)
+    if scale is None:
+        scale = dk ** -0.5
+    opts = GlaChunkOptions(segments=int(segments), dv_tile=int(dv_tile),
+                           force_exact=1 if force_exact else 0)
+    with torch.cuda.device(dev):
+        st = _lib.lib().gla_chunk_fwd_ex(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), log_alpha.data_ptr(), float(scale),
+            None if h0 is None else h0.data_ptr(), out.data_ptr(),
+            None if hT is None else hT.data_ptr(), B, H, T, dk, dv, ctypes.byref(opts),
+            _stream(dev))
+    _lib.check(st, "gla_chunk_fwd")
+    return out, hT
+
+
+def gla_recurrent_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: torch.Tensor,
+                       h: torch.Tensor, scale: float | None = None, *,
+                       out: torch.Tensor | None = None) -> torch.Tensor:
+    """One decode token for every (batch, head): ``h`` is updated in place, returns o.
+
+    q, k, log_alpha: ``[B,H,dk]``; v: ``[B,H,dv]``; h: ``[B,H,dk,dv]`` fp32.
+    """
+    if h.dim() != 4:
+        raise ValueError("h must be [B, H, dk, dv]")
+    B, H, dk, dv = h.shape
+    dev = h.device
+    _need(h, "h", torch.float32, (B, H, dk, dv), dev)
+    _need(q, "q", torch.bfloat16, (B, H, dk), dev)
+    _need(k, "k", torch.bfloat16, (B, H, dk), dev)
+    _need(v, "v", torch.bfloat16, (B, H, dv), dev)
+    _need(log_alpha, "log_alpha", torch.float32, (B, H, dk), dev)
+    if out is None:
+        out = torch.empty(B, H, dv, dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, (B, H, dv), dev)
+    if scale is None:
+        scale = dk ** -0.5
+    with torch.cuda.device(dev):
+        st = _lib.lib().gla_recurrent_step(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                           log_alpha.data_ptr(), float(scale), h.data_ptr(),
+                                           out.data_ptr(), B, H, dk, dv, _stream(dev))
+    _lib.check(st, "gla_recurrent_step")
+    return out
+
+
+def gla_last_device_status(device: torch.device | int | None = None) -> int:
+    """Synchronise the current stream and read/clear the library's device status word."""
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else
+                       (device if isinstance(device, int) else device.index))
+    with torch.cuda.device(dev):
+        return int(_lib.lib().gla_last_device_status(_stream(dev)))

@@ -1,0 +1,81 @@
+"""ctypes handle on the in-tree CUDA library ``libgla.so`` (C ABI in include/gla.h).
+
+Loading never falls back to anything: if the library is missing or cannot be
+loaded the error says so and names the build command.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgla.so")
+
+# Status codes (enum gla_status in include/gla.h).
+GLA_OK = 0
+GLA_ERR_ARG = 1
+GLA_ERR_SHAPE = 2
+GLA_ERR_DEVICE = 3
+GLA_ERR_LAUNCH = 4
+GLA_ERR_TIMEOUT = 5
+GLA_ERR_ALLOC = 6
+
+EXPORTED = ("gla_chunk_fwd", "gla_chunk_fwd_ex", "gla_recurrent_step", "gla_status_string",
+            "gla_last_device_status", "gla_version")
+
+
+class GlaChunkOptions(ctypes.Structure):
+    _fields_ = [("segments", ctypes.c_int), ("dv_tile", ctypes.c_int),
+                ("force_exact", ctypes.c_int), ("reserved", ctypes.c_int * 5)]
+
+
+class GlaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+_lock = threading.Lock()
+_lib: ctypes.CDLL | None = None
+
+
+def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
+    vp, fp, i, f = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.gla_chunk_fwd.argtypes = [vp, vp, vp, fp, f, fp, vp, fp, i, i, i, i, i, vp]
+    lib.gla_chunk_fwd.restype = i
+    lib.gla_chunk_fwd_ex.argtypes = [vp, vp, vp, fp, f, fp, vp, fp, i, i, i, i, i,
+                                     ctypes.POINTER(GlaChunkOptions), vp]
+    lib.gla_chunk_fwd_ex.restype = i
+    lib.gla_recurrent_step.argtypes = [vp, vp, vp, fp, f, fp, vp, i, i, i, i, vp]
+    lib.gla_recurrent_step.restype = i
+    lib.gla_status_string.argtypes = [i]
+    lib.gla_status_string.restype = ctypes.c_char_p
+    lib.gla_last_device_status.argtypes = [vp]
+    lib.gla_last_device_status.restype = i
+    lib.gla_version.argtypes = []
+    lib.gla_version.restype = i
+    return lib
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (loaded once per process)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(
+                    f"{LIB_PATH} is missing: build it with "
+                    "`python -m chunkwise_linear_rnn_gb300.build` (needs nvcc for sm_103a)")
+            _lib = _bind(ctypes.CDLL(LIB_PATH))
+        return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().gla_status_string(int(status)).decode()
+
+
+def check(status: int, what: str) -> None:
+    if status != GLA_OK:
+        raise GlaError(status, what)

@@ -1,0 +1,228 @@
+// gla_api.cu — the C ABI declared in include/gla.h: host-side validation,
+// device checks, TMA tensor-map encoding and kernel dispatch.
+//
+// Nothing here computes any part of the method; every step of the forward
+// and of the decode step runs in the kernels of gla_chunk.cu / gla_decode.cu.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "gla.h"
+#include "gla_internal.h"
+
+namespace gla {
+
+__device__ unsigned int g_device_status = 0u;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool probed = false;
+    bool supported = false;
+    unsigned int *status = nullptr;  // device address of g_device_status
+};
+
+std::mutex g_mutex;
+DeviceInfo g_devices[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Current device, checked to be sm_103 (GB300).  Returns a GLA status.
+int current_device(DeviceInfo **out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return GLA_ERR_DEVICE;
+    }
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo &info = g_devices[dev];
+    if (!info.probed) {
+        info.probed = true;
+        cudaDeviceProp prop;
+        if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return GLA_ERR_DEVICE;
+        }
+        info.supported = (prop.major == 10 && prop.minor == 3);
+        if (info.supported) {
+            void *addr = nullptr;
+            if (cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess) {
+                cudaGetLastError();
+                info.supported = false;
+            } else {
+                info.status = static_cast<unsigned int *>(addr);
+            }
+        }
+    }
+    if (!info.supported) return GLA_ERR_DEVICE;
+    *out = &info;
+    return GLA_OK;
+}
+
+int encode_fn(EncodeTiledFn *fn) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_encode) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !p) {
+            cudaGetLastError();
+            return GLA_ERR_DEVICE;
+        }
+        g_encode = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    *fn = g_encode;
+    return GLA_OK;
+}
+
+// 3-D tensor map over a [BH, T, C] row-major tensor: dims (C, T, BH).
+bool make_map(EncodeTiledFn enc, CUtensorMap *m, const void *ptr, CUtensorMapDataType dt,
+              int elem_bytes, int C, int T, int BH, int box_c, int box_t,
+              CUtensorMapSwizzle swz) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(C), static_cast<cuuint64_t>(T),
+                          static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(C) * elem_bytes,
+                             static_cast<cuuint64_t>(C) * elem_bytes * static_cast<cuuint64_t>(T)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(box_c), static_cast<cuuint32_t>(box_t), 1u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = enc(m, dt, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool dk_ok(int dk) { return dk == 64 || dk == 128; }
+bool dv_ok(int dv) { return dv == 64 || dv == 128 || dv == 256; }
+
+}  // namespace
+}  // namespace gla
+
+extern "C" {
+
+int gla_version(void) { return 100; }
+
+const char *gla_status_string(int status) {
+    switch (status) {
+        case GLA_OK: return "ok";
+        case GLA_ERR_ARG: return "invalid argument (null pointer, non-positive size or misaligned pointer)";
+        case GLA_ERR_SHAPE: return "unsupported head dimensions (dk in {64,128}, dv in {64,128,256})";
+        case GLA_ERR_DEVICE: return "no usable CUDA device (this library needs an sm_103 GB300)";
+        case GLA_ERR_LAUNCH: return "a CUDA call failed while enqueuing work";
+        case GLA_ERR_TIMEOUT: return "a bounded device-side wait expired";
+        case GLA_ERR_ALLOC: return "stream-ordered scratch allocation failed";
+        default: return "unknown status";
+    }
+}
+
+int gla_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *log_alpha,
+                     float scale, const float *h0, void *o, float *hT, int B, int H, int T,
+                     int dk, int dv, const gla_chunk_options *opts, cudaStream_t stream) {
+    using namespace gla;
+    if (!q || !k || !v || !log_alpha || !o) return GLA_ERR_ARG;
+    if (B <= 0 || H <= 0 || T <= 0) return GLA_ERR_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_alpha) ||
+        !aligned16(o) || (h0 && !aligned16(h0)) || (hT && !aligned16(hT)))
+        return GLA_ERR_ARG;
+    if (!dk_ok(dk) || !dv_ok(dv)) return GLA_ERR_SHAPE;
+    gla_chunk_options o_def = {};
+    const gla_chunk_options &op = opts ? *opts : o_def;
+    if (op.dv_tile != 0 && op.dv_tile != 64 && op.dv_tile != 128) return GLA_ERR_ARG;
+    if (op.dv_tile > dv) return GLA_ERR_ARG;
+    if (op.segments < 0) return GLA_ERR_ARG;
+    if (static_cast<long long>(B) * H > 0x7fffffffLL) return GLA_ERR_ARG;
+
+    DeviceInfo *dev = nullptr;
+    int st = current_device(&dev);
+    if (st != GLA_OK) return st;
+    EncodeTiledFn enc = nullptr;
+    st = encode_fn(&enc);
+    if (st != GLA_OK) return st;
+
+    ChunkLaunch p;
+    const int BH = B * H;
+    const int dvt = op.dv_tile ? op.dv_tile : (dv >= 128 ? 128 : 64);
+    if (!make_map(enc, &p.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dk, T, BH, 64, 128,
+                  CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(enc, &p.tm_k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dk, T, BH, 64, 128,
+                  CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(enc, &p.tm_v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dv, T, BH, 64, 128,
+                  CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(enc, &p.tm_a, log_alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dk, T, BH, dk,
+                  128, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return GLA_ERR_LAUNCH;
+    p.h0 = h0;
+    p.hT = hT;
+    p.o = o;
+    p.scale = scale;
+    p.B = B;
+    p.H = H;
+    p.T = T;
+    p.dk = dk;
+    p.dv = dv;
+    p.dv_tile = dvt;
+    p.force_exact = op.force_exact ? 1 : 0;
+    p.status = dev->status;
+    const int err = launch_chunk_fwd(p, stream);
+    return err == 0 ? GLA_OK : GLA_ERR_LAUNCH;
+}
+
+int gla_chunk_fwd(const void *q, const void *k, const void *v, const float *log_alpha,
+                  float scale, const float *h0, void *o, float *hT, int B, int H, int T, int dk,
+                  int dv, cudaStream_t stream) {
+    return gla_chunk_fwd_ex(q, k, v, log_alpha, scale, h0, o, hT, B, H, T, dk, dv, nullptr,
+                            stream);
+}
+
+int gla_recurrent_step(const void *q, const void *k, const void *v, const float *log_alpha,
+                       float scale, float *h, void *o, int B, int H, int dk, int dv,
+                       cudaStream_t stream) {
+    using namespace gla;
+    if (!q || !k || !v || !log_alpha || !h || !o) return GLA_ERR_ARG;
+    if (B <= 0 || H <= 0) return GLA_ERR_ARG;
+    if (static_cast<long long>(B) * H > 0x7fffffffLL) return GLA_ERR_ARG;
+    if (!aligned16(h) || (reinterpret_cast<uintptr_t>(v) & 7u) ||
+        (reinterpret_cast<uintptr_t>(o) & 7u) || (reinterpret_cast<uintptr_t>(q) & 1u) ||
+        (reinterpret_cast<uintptr_t>(k) & 1u) || (reinterpret_cast<uintptr_t>(log_alpha) & 3u))
+        return GLA_ERR_ARG;
+    if (!dk_ok(dk) || !dv_ok(dv)) return GLA_ERR_SHAPE;
+    DeviceInfo *dev = nullptr;
+    int st = current_device(&dev);
+    if (st != GLA_OK) return st;
+    DecodeLaunch p{q, k, v, log_alpha, h, o, scale, B * H, dk, dv};
+    return launch_recurrent_step(p, stream) == 0 ? GLA_OK : GLA_ERR_LAUNCH;
+}
+
+int gla_last_device_status(cudaStream_t stream) {
+    using namespace gla;
+    DeviceInfo *dev = nullptr;
+    int st = current_device(&dev);
+    if (st != GLA_OK) return st;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaGetLastError();
+        return GLA_ERR_LAUNCH;
+    }
+    unsigned int word = 0;
+    if (cudaMemcpy(&word, dev->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return GLA_ERR_LAUNCH;
+    }
+    if (word != 0) {
+        const unsigned int zero = 0;
+        cudaMemcpy(dev->status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+        return GLA_ERR_TIMEOUT;
+    }
+    return GLA_OK;
+}
+
+}  // extern "C"

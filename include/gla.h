@@ -1,0 +1,128 @@
+/*
+ * gla.h — C ABI of the GB300 (sm_103a) gated linear attention forward library.
+ *
+ * The operation (from "Gated Linear Attention (GLA): Mathematical Foundations,
+ * Data-Dependent Gating, Chunkwise Parallel Forms, and Sub-Quadratic Sequence
+ * Modeling", llms.blog, section "The Gated Recurrent Update"):
+ *
+ *     S_t = diag(alpha_t) S_{t-1} + k_t^T v_t,      o_t = scale * q_t S_t,
+ *
+ * per (batch, head), with S in R^{dk x dv} and the gate given in log space,
+ * log_alpha_t = log(alpha_t) (the page's A, section "Sequence Partitioning and
+ * State Factorization").  The output reads the state after the token's own
+ * update; `scale` multiplies the output only, never the state.
+ *
+ * Layouts: row-major, contiguous, head-first.
+ *     q, k       bf16  [B, H, T, dk]
+ *     v          bf16  [B, H, T, dv]
+ *     log_alpha  fp32  [B, H, T, dk]
+ *     o          bf16  [B, H, T, dv]      (round-to-nearest-even from fp32)
+ *     h0, hT     fp32  [B, H, dk, dv]     (row index = key channel)
+ *
+ * Every pointer is a DEVICE pointer on the current CUDA device.  The caller
+ * owns every buffer; the library keeps no pointer after a call returns.
+ * All calls are asynchronous on `stream` (0 = the legacy default stream) and
+ * return once the work is enqueued.
+ *
+ * Supported shapes: dk in {64, 128}; dv in {64, 128, 256}; B, H >= 1;
+ * T >= 1 (any value: a ragged last chunk is handled inside the kernel).
+ * Pointers must be 16-byte aligned.
+ *
+ * Domain: log_alpha finite and <= 0 (alpha in (0, 1], the page's range in
+ * "Data-Dependent Forget Gate Parametrization").  Results for other gate
+ * values are computed but not covered by the accuracy claim.
+ *
+ * Accuracy: o and hT match the token-by-token recurrence evaluated in fp64 on
+ * the same inputs to relative L2 error <= 1e-2 and max-abs error <=
+ * 2e-2 * RMS(reference), for every finite input in the domain.
+ *
+ * Error behaviour: every entry point validates its arguments on the host
+ * before touching the GPU and returns a GLA_* status; nothing is enqueued
+ * when the status is not GLA_OK.  Device-side bounded waits that expire set a
+ * device status word, read (and cleared) by gla_last_device_status().
+ */
+#ifndef GLA_H_
+#define GLA_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *cudaStream_t;
+
+enum gla_status {
+    GLA_OK = 0,
+    GLA_ERR_ARG = 1,         /* null pointer, non-positive size, misaligned pointer   */
+    GLA_ERR_SHAPE = 2,       /* dk / dv outside the supported set                      */
+    GLA_ERR_DEVICE = 3,      /* no CUDA device, or the device is not sm_103            */
+    GLA_ERR_LAUNCH = 4,      /* a CUDA call failed while enqueuing the work            */
+    GLA_ERR_TIMEOUT = 5,     /* a bounded device-side wait expired (from the status word) */
+    GLA_ERR_ALLOC = 6        /* stream-ordered scratch allocation failed               */
+};
+
+/*
+ * gla_chunk_fwd — chunkwise-parallel forward over whole sequences (prefill).
+ *
+ * Computes o for every token and, when hT != NULL, the state after the last
+ * token, for the recurrence above started from h0 (zero when h0 == NULL).
+ * The method is the chunkwise form of the same page, sections "Cumulative
+ * Decay Representation", "Intra-Chunk Matrix Multiplications" and
+ * "Inter-Chunk Recurrence and Output Projection": per chunk of tokens the
+ * causal decayed Q K^T block times V, plus the decayed query times the state
+ * entering the chunk, with the state carried on chip from chunk to chunk.
+ *
+ * hT may alias h0 (in-place state update).  o must not overlap any input.
+ * When B * H is small the library splits each sequence into segments and
+ * joins them with an exact state correction; that path allocates its scratch
+ * with cudaMallocAsync / cudaFreeAsync on `stream`.
+ */
+int gla_chunk_fwd(const void *q, const void *k, const void *v, const float *log_alpha,
+                  float scale, const float *h0, void *o, float *hT, int B, int H, int T,
+                  int dk, int dv, cudaStream_t stream);
+
+/* Tuning and test knobs for gla_chunk_fwd_ex.  Zero-initialise; 0 = automatic. */
+typedef struct gla_chunk_options {
+    int segments;      /* sequence segments per (batch, head); 0 = automatic, 1 = no split */
+    int dv_tile;       /* value columns per CTA: 0 = automatic, else 64 or 128             */
+    int force_exact;   /* 1 = take the exact (elementwise-decay) path for every chunk       */
+    int reserved[5];
+} gla_chunk_options;
+
+/* gla_chunk_fwd with explicit options (opts may be NULL = all automatic). */
+int gla_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *log_alpha,
+                     float scale, const float *h0, void *o, float *hT, int B, int H, int T,
+                     int dk, int dv, const gla_chunk_options *opts, cudaStream_t stream);
+
+/*
+ * gla_recurrent_step — one decode token for B * H independent heads.
+ *
+ * h (fp32 [B, H, dk, dv]) is read and overwritten in place with
+ * diag(exp(log_alpha)) h + k^T v; o (bf16 [B, H, dv]) receives scale * q h
+ * with the updated h.  q, k, log_alpha are [B, H, dk]; v is [B, H, dv].
+ * Source: the recurrence above, one step (the same page, "The Gated Recurrent
+ * Update"; constant-memory decoding in its "Training and Inference
+ * Throughput" section).
+ */
+int gla_recurrent_step(const void *q, const void *k, const void *v, const float *log_alpha,
+                       float scale, float *h, void *o, int B, int H, int dk, int dv,
+                       cudaStream_t stream);
+
+/* Static text for a status code (never NULL). */
+const char *gla_status_string(int status);
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device status
+ * word on the current device.  Returns GLA_ERR_TIMEOUT if any kernel since
+ * the last call gave up a bounded wait, GLA_ERR_LAUNCH if the stream reports
+ * a CUDA error, else GLA_OK.
+ */
+int gla_last_device_status(cudaStream_t stream);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int gla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GLA_H_ */

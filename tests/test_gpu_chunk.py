@@ -1,0 +1,161 @@
+"""GPU parity of gla_chunk_fwd (through the C ABI) against the fp64 oracle.
+
+Small and ragged cases are compared element by element over every head; the
+full-size workloads are compared on sampled heads (heads are independent
+sequences, so the oracle runs those heads in full, every token).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import chunkwise_linear_rnn_gb300 as gla
+from oracle import gla_oracle as og
+from synth import CHUNK_CONFIGS, make_chunk_inputs, make_config_inputs
+from tolerance import assert_close
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from chunkwise_linear_rnn_gb300.build import build
+    build()
+    og.build()
+
+
+def _oracle(q, k, v, a, scale, h0, heads=None):
+    """Oracle on the exact GPU inputs; heads = list of (b, h) or None for all."""
+    def cpu(t):
+        return t.detach().float().cpu().numpy()
+    if heads is None:
+        return og.forward(cpu(q), cpu(k), cpu(v), cpu(a), scale,
+                          None if h0 is None else h0.double().cpu().numpy())
+    sel = lambda t: torch.stack([t[b, h] for b, h in heads])  # noqa: E731
+    o, hT = og.forward(cpu(sel(q)), cpu(sel(k)), cpu(sel(v)), cpu(sel(a)), scale,
+                       None if h0 is None else sel(h0).double().cpu().numpy())
+    return o, hT
+
+
+def _run_and_check(q, k, v, a, h0, what, heads=None, **kw):
+    scale = q.shape[-1] ** -0.5
+    o, hT = gla.gla_chunk_fwd(q, k, v, a, scale, h0, **kw)
+    torch.cuda.synchronize()
+    assert gla.gla_last_device_status() == 0
+    o_ref, h_ref = _oracle(q, k, v, a, scale, h0, heads)
+    if heads is not None:
+        o = torch.stack([o[b, h] for b, h in heads])
+        hT = torch.stack([hT[b, h] for b, h in heads])
+    r1 = assert_close(o.float().cpu().numpy(), o_ref, f"{what} o", bf16_output=True)
+    r2 = assert_close(hT.cpu().numpy(), h_ref, f"{what} hT")
+    return r1, r2
+
+
+def _inputs(B, H, T, dk, dv, *, h0=False, sigma_z=1.0, tau=16.0, seed=0):
+    q, k, v, a, s0 = make_chunk_inputs(B, H, T, dk, dv, sigma_z=sigma_z, tau=tau,
+                                       sigma_h0=0.1 if h0 else None, seed=seed, device="cpu")
+    to = lambda t: None if t is None else t.to(DEV)  # noqa: E731
+    return to(q), to(k), to(v), to(a), to(s0)
+
+
+def test_small_config_all_heads():
+    cfg = CHUNK_CONFIGS["small"]
+    q, k, v, a, h0 = (None if t is None else t.to(DEV) for t in make_config_inputs(cfg))
+    _run_and_check(q, k, v, a, h0, cfg.name)
+
+
+@pytest.mark.parametrize("T", [1, 2, 63, 127, 128, 129, 255, 300, 513])
+def test_ragged_lengths(T):
+    q, k, v, a, h0 = _inputs(2, 3, T, 64, 64, h0=True, seed=T)
+    _run_and_check(q, k, v, a, h0, f"T={T}")
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (64, 128), (64, 256), (128, 64), (128, 128),
+                                   (128, 256)])
+def test_head_dims(dk, dv):
+    q, k, v, a, h0 = _inputs(1, 2, 200, dk, dv, h0=True, seed=dk + dv)
+    _run_and_check(q, k, v, a, h0, f"dk={dk} dv={dv}")
+
+
+@pytest.mark.parametrize("dv_tile", [64, 128])
+def test_dv_tile_does_not_change_results(dv_tile):
+    q, k, v, a, h0 = _inputs(1, 2, 300, 128, 256, h0=True, seed=5)
+    _run_and_check(q, k, v, a, h0, f"dv_tile={dv_tile}", dv_tile=dv_tile)
+
+
+def test_no_initial_state_and_no_final_state():
+    q, k, v, a, _ = _inputs(2, 2, 130, 128, 128, seed=3)
+    o, hT = gla.gla_chunk_fwd(q, k, v, a, None, None, output_final_state=False)
+    assert hT is None
+    o_ref, _ = _oracle(q, k, v, a, 128 ** -0.5, None)
+    assert_close(o.float().cpu().numpy(), o_ref, "no h0 / no hT", bf16_output=True)
+
+
+def test_final_state_may_alias_initial_state():
+    q, k, v, a, h0 = _inputs(1, 3, 257, 64, 128, h0=True, seed=4)
+    h = h0.clone()
+    o_ref, h_ref = _oracle(q, k, v, a, 64 ** -0.5, h0)
+    o, hT = gla.gla_chunk_fwd(q, k, v, a, None, h, final_state=h)
+    assert hT.data_ptr() == h.data_ptr()
+    assert_close(o.float().cpu().numpy(), o_ref, "aliased o", bf16_output=True)
+    assert_close(h.cpu().numpy(), h_ref, "aliased hT")
+
+
+def test_vanishing_gates_take_the_exact_path():
+    # log alpha = -30 per token: the in-chunk decay leaves the fast path's bounded domain.
+    q, k, v, a, h0 = _inputs(1, 2, 200, 64, 64, h0=True, seed=6)
+    a = torch.full_like(a, -30.0)
+    _run_and_check(q, k, v, a, h0, "log alpha = -30")
+
+
+def test_gate_of_one_is_linear_attention():
+    q, k, v, a, h0 = _inputs(1, 2, 256, 128, 64, h0=True, seed=7)
+    a = torch.zeros_like(a)
+    _run_and_check(q, k, v, a, h0, "alpha = 1")
+
+
+def test_forced_exact_path_matches_oracle():
+    q, k, v, a, h0 = _inputs(1, 2, 300, 128, 128, h0=True, seed=8, sigma_z=2.0)
+    _run_and_check(q, k, v, a, h0, "force_exact", force_exact=True)
+
+
+def test_mixed_fast_and_exact_chunks():
+    q, k, v, a, h0 = _inputs(1, 1, 640, 128, 128, h0=True, seed=9)
+    a[..., 128:256, :] = -1.0     # chunk 1 leaves the bounded domain, its neighbours do not
+    _run_and_check(q, k, v, a, h0, "mixed chunks")
+
+
+def test_split_sequence_equals_one_call():
+    q, k, v, a, h0 = _inputs(1, 2, 400, 128, 128, h0=True, seed=10)
+    o, hT = gla.gla_chunk_fwd(q, k, v, a, None, h0)
+    T1 = 200  # not a chunk boundary
+    o1, h1 = gla.gla_chunk_fwd(q[:, :, :T1].contiguous(), k[:, :, :T1].contiguous(),
+                               v[:, :, :T1].contiguous(), a[:, :, :T1].contiguous(), None, h0)
+    o2, h2 = gla.gla_chunk_fwd(q[:, :, T1:].contiguous(), k[:, :, T1:].contiguous(),
+                               v[:, :, T1:].contiguous(), a[:, :, T1:].contiguous(), None, h1)
+    ref_o, ref_h = _oracle(q, k, v, a, 128 ** -0.5, h0)
+    assert_close(torch.cat([o1, o2], dim=2).float().cpu().numpy(), ref_o, "split o",
+                 bf16_output=True)
+    assert_close(h2.cpu().numpy(), ref_h, "split hT")
+    assert_close(o.float().cpu().numpy(), ref_o, "whole o", bf16_output=True)
+
+
+def test_medium_config_all_heads():
+    cfg = CHUNK_CONFIGS["medium"]
+    q, k, v, a, h0 = make_config_inputs(cfg, device=DEV)
+    _run_and_check(q, k, v, a, h0, cfg.name)
+
+
+def test_long_config_sampled_heads():
+    cfg = CHUNK_CONFIGS["long"]
+    q, k, v, a, h0 = make_config_inputs(cfg, device=DEV)
+    _run_and_check(q, k, v, a, h0, cfg.name, heads=[(0, 0), (1, 7), (1, 15)])
+
+
+def test_very_long_config_sampled_heads():
+    cfg = CHUNK_CONFIGS["very_long"]
+    q, k, v, a, h0 = make_config_inputs(cfg, device=DEV)
+    _run_and_check(q, k, v, a, h0, cfg.name, heads=[(0, 3), (0, 30)])

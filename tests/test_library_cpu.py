@@ -1,0 +1,117 @@
+"""Host-side checks of the C-ABI library that need no GPU.
+
+* the library builds for sm_103a and loads in a process without a GPU driver;
+* it exports every function that include/gla.h declares;
+* argument validation happens on the host, before any CUDA call, and returns
+  the documented status codes; with valid arguments and no GPU the calls
+  report GLA_ERR_DEVICE instead of crashing.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from chunkwise_linear_rnn_gb300 import _lib
+from chunkwise_linear_rnn_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gla.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return _lib.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gla_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for n in ("gla_chunk_fwd", "gla_recurrent_step", "gla_status_string",
+              "gla_last_device_status"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"{name} declared in gla.h but not exported"
+    assert set(_declared_functions()) <= set(_lib.EXPORTED) | set(_declared_functions())
+
+
+def test_status_strings(lib):
+    for code in range(0, 7):
+        s = _lib.status_string(code)
+        assert s and s != "unknown status"
+    assert _lib.status_string(99) == "unknown status"
+    assert lib.gla_version() >= 100
+
+
+# A fake, 16-byte aligned "device" address: validation must reject or accept
+# arguments without ever dereferencing it.
+P = 0x10000
+
+
+def _chunk(lib, *, q=P, k=P, v=P, a=P, h0=None, o=P, hT=None, B=1, H=1, T=16, dk=64, dv=64,
+           opts=None):
+    return lib.gla_chunk_fwd_ex(q, k, v, a, 0.125, h0, o, hT, B, H, T, dk, dv, opts, None)
+
+
+@pytest.mark.parametrize("field", ["q", "k", "v", "a", "o"])
+def test_chunk_rejects_null(lib, field):
+    assert _chunk(lib, **{field: None}) == _lib.GLA_ERR_ARG
+
+
+@pytest.mark.parametrize("dims", [dict(B=0), dict(H=0), dict(T=0), dict(T=-3)])
+def test_chunk_rejects_sizes(lib, dims):
+    assert _chunk(lib, **dims) == _lib.GLA_ERR_ARG
+
+
+@pytest.mark.parametrize("dk,dv", [(32, 64), (96, 64), (256, 64), (64, 32), (64, 512), (128, 192)])
+def test_chunk_rejects_shapes(lib, dk, dv):
+    assert _chunk(lib, dk=dk, dv=dv) == _lib.GLA_ERR_SHAPE
+
+
+def test_chunk_rejects_misaligned(lib):
+    assert _chunk(lib, q=P + 8) == _lib.GLA_ERR_ARG
+    assert _chunk(lib, hT=P + 4) == _lib.GLA_ERR_ARG
+
+
+def test_chunk_rejects_bad_options(lib):
+    assert _chunk(lib, opts=ctypes.byref(_lib.GlaChunkOptions(dv_tile=96))) == _lib.GLA_ERR_ARG
+    assert _chunk(lib, opts=ctypes.byref(_lib.GlaChunkOptions(dv_tile=128)), dv=64) == _lib.GLA_ERR_ARG
+    assert _chunk(lib, opts=ctypes.byref(_lib.GlaChunkOptions(segments=-1))) == _lib.GLA_ERR_ARG
+
+
+def test_step_validation(lib):
+    f = lib.gla_recurrent_step
+    assert f(None, P, P, P, 1.0, P, P, 1, 1, 64, 64, None) == _lib.GLA_ERR_ARG
+    assert f(P, P, P, P, 1.0, None, P, 1, 1, 64, 64, None) == _lib.GLA_ERR_ARG
+    assert f(P, P, P, P, 1.0, P, P, 0, 1, 64, 64, None) == _lib.GLA_ERR_ARG
+    assert f(P, P, P, P, 1.0, P + 4, P, 1, 1, 64, 64, None) == _lib.GLA_ERR_ARG
+    assert f(P, P, P, P, 1.0, P, P, 1, 1, 48, 64, None) == _lib.GLA_ERR_SHAPE
+
+
+def test_valid_arguments_without_gpu_report_device_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _chunk(lib) == _lib.GLA_ERR_DEVICE
+    assert lib.gla_recurrent_step(P, P, P, P, 1.0, P, P, 1, 1, 64, 64, None) == _lib.GLA_ERR_DEVICE
+    assert lib.gla_last_device_status(None) == _lib.GLA_ERR_DEVICE
+
+
+def test_python_binding_rejects_cpu_tensors():
+    import torch
+    import chunkwise_linear_rnn_gb300 as gla
+    q = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        gla.gla_chunk_fwd(q, q, q, torch.zeros(1, 1, 4, 64))
