@@ -23,6 +23,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
     bool probed = false;
     bool supported = false;
+    int sm_count = 1;
     unsigned int *status = nullptr;  // device address of g_device_status
 };
 
@@ -52,6 +53,7 @@ int current_device(DeviceInfo **out) {
             return GLA_ERR_DEVICE;
         }
         info.supported = (prop.major == 10 && prop.minor == 3);
+        info.sm_count = prop.multiProcessorCount;
         if (info.supported) {
             void *addr = nullptr;
             if (cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess) {
@@ -149,21 +151,41 @@ int gla_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *l
     st = encode_fn(&enc);
     if (st != GLA_OK) return st;
 
-    ChunkLaunch p;
     const int BH = B * H;
     const int dvt = op.dv_tile ? op.dv_tile : (dv >= 128 ? 128 : 64);
+    const int n_chunks = (T + 127) / 128;
+    // Sequence segments: enough (batch, head, tile, segment) units to fill the
+    // SMs once, each segment long enough (>= 8 chunks) to amortise its
+    // correction window.
+    int n_seg = op.segments;
+    if (n_seg == 0) {
+        const int units = BH * (dv / dvt);
+        n_seg = units > 0 ? dev->sm_count / units : 1;
+        n_seg = n_seg < n_chunks / 8 ? n_seg : n_chunks / 8;
+        if (n_seg < 1) n_seg = 1;
+    }
+    if (n_seg > n_chunks) n_seg = n_chunks;
+    const int seg_chunks = (n_chunks + n_seg - 1) / n_seg;
+    n_seg = (n_chunks + seg_chunks - 1) / seg_chunks;
+
+    ChunkLaunch p;
     if (!make_map(enc, &p.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dk, T, BH, 64, 128,
                   CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(enc, &p.tm_k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dk, T, BH, 64, 128,
                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(enc, &p.tm_a, log_alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dk, T, BH, dk, 128,
+                  CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_map(enc, &p.tm_v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dv, T, BH, 64, 128,
-                  CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(enc, &p.tm_a, log_alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dk, T, BH, dk,
-                  128, CU_TENSOR_MAP_SWIZZLE_NONE))
+                  CU_TENSOR_MAP_SWIZZLE_128B))
         return GLA_ERR_LAUNCH;
+    p.q = q;
+    p.k = k;
+    p.log_alpha = log_alpha;
     p.h0 = h0;
     p.hT = hT;
     p.o = o;
+    p.ws_state = nullptr;
+    p.ws_decay = nullptr;
     p.scale = scale;
     p.B = B;
     p.H = H;
@@ -171,9 +193,23 @@ int gla_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *l
     p.dk = dk;
     p.dv = dv;
     p.dv_tile = dvt;
+    p.n_seg = n_seg;
+    p.seg_chunks = seg_chunks;
     p.force_exact = op.force_exact ? 1 : 0;
     p.status = dev->status;
+    void *ws = nullptr;
+    if (n_seg > 1) {
+        const size_t state_bytes = static_cast<size_t>(n_seg) * BH * dk * dv * sizeof(float);
+        const size_t decay_bytes = static_cast<size_t>(n_seg) * BH * dk * sizeof(float);
+        if (cudaMallocAsync(&ws, state_bytes + decay_bytes, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return GLA_ERR_ALLOC;
+        }
+        p.ws_state = static_cast<float *>(ws);
+        p.ws_decay = reinterpret_cast<float *>(static_cast<char *>(ws) + state_bytes);
+    }
     const int err = launch_chunk_fwd(p, stream);
+    if (ws) cudaFreeAsync(ws, stream);
     return err == 0 ? GLA_OK : GLA_ERR_LAUNCH;
 }
 

@@ -11,29 +11,49 @@
 //     S_new = diag(e^Gamma_C) S_prev + (K * e^(Gamma_C - Gamma))^T V,
 // with the state S held on chip (TMEM, fp32) across the whole chunk loop.
 //
-// GB300 mapping (one CTA per (batch, head, value-column tile); C = 128 so that
-// every product is a 128-row tcgen05 MMA whose TMEM row i is lane i):
-//   * TMA streams the chunk's Q, K (bf16, 128-byte swizzle, directly in the
-//     K-major operand layout), V (bf16, MN-major operand layout) and A (fp32).
-//   * Fast path (every |Gamma| <= kExpBound in the chunk): thread d scans
-//     channel d and rescales with the chunk-start reference,
-//     Qh = Q e^Gamma (<= |Q|) and Kh = K e^-Gamma.  The decay then factorises:
-//     the whole decayed score block is P = Qh Kh^T, and the state update is
-//     S_new = diag(e^Gamma_C) (S_prev + Kh^T V): MMAs accumulating into TMEM
-//     plus a per-lane scale (TMEM lane = key channel).  Every exponent is
-//     bounded by kExpBound, so no factor overflows; masked entries of P are
-//     selected away, never multiplied by zero.
-//   * Exact path (a chunk whose decay leaves that bound, e.g. alpha -> 0): the
-//     score block is built elementwise from e^(Gamma_i - Gamma_j) <= 1 and the
-//     state factor from e^(Gamma_C - Gamma_j) <= 1; no exponent is positive.
-//   * Precision: bf16 operands carry 8 significant bits.  The two roundings
-//     that dominate the error of o and hT are removed by splitting the value
-//     into a bf16 pair x = hi + lo (16 significant bits): Kh (used by the
-//     score MMA and by the state MMA) and P (the A operand of P V, kept in
-//     TMEM).  Q-side operands and the bf16 copy of S stay single.
-//   * O = Qh S_prev + P V accumulates in TMEM; the epilogue scales, rounds to
-//     bf16 and stores.  S_prev is fed to the MMA as a bf16 copy in shared
-//     memory, refreshed from TMEM after each chunk.
+// Rescaling (bounded exponents).  With a reference r (the Gamma value just
+// before the first token of a block of tokens), Qh = Q e^(Gamma - r) <= |Q| and
+// Kh = K e^(r - Gamma): the decayed score block factorises as P = Qh Kh^T and
+// the state update as S_new = diag(e^(Gamma_end - r)) (S_prev + Kh^T V).  Both
+// are plain tensor-core products.  A chunk is processed as one block when
+// every |Gamma - r| <= kExpBound over it (the common case); otherwise it is
+// cut into equal power-of-two sub-chunks, each with its own reference, small
+// enough that the bound holds in each (sub-chunk rescaling).  A single token
+// whose own |log alpha| exceeds the bound is clamped to it: the state term
+// that changes is below e^-30 ~ 9e-14 of the state, under fp32 resolution.
+// Masked score entries are selected away, never multiplied by zero.
+//
+// Precision.  bf16 operands carry 8 significant bits; the two roundings that
+// dominate the output error are removed by splitting the operand into a bf16
+// pair x = hi + lo: the rescaled keys Kh (score and state products) and the
+// score block P (the A operand of P V, kept in TMEM).
+//
+// CTA organisation (one CTA per (batch, head, value-column tile, sequence
+// segment); 320 threads):
+//   warp 9 "tma": streams each chunk's A (fp32), Q, K (bf16, 128-byte swizzle,
+//     already in the K-major operand layout) and V (MN-major) tiles with TMA,
+//     each as soon as the tile it replaces has been consumed.
+//   warps 0-3 "prep": run the fp32 prefix sum of A (two channels x 64 tokens
+//     per thread, 8-byte shared-memory vectors), rescale Q and K in place to Qh
+//     and Kh_hi, write Kh_lo, and decide the item sequence (one block, or
+//     rescaled sub-chunks) and the correction window of each chunk.
+//   warp 8 "mma": one thread issues every tcgen05.mma and commit.
+//   warps 4-7 "tmem": thread i owns TMEM lane i — causal mask and hi/lo split
+//     of P, the per-row state scale and its bf16 copy for the next chunk's
+//     Qh S product, and the output epilogue.
+// The O accumulator is double-buffered so the next chunk's products overlap
+// the current chunk's epilogue; the next chunk's Q/K/A loads overlap the
+// current chunk's P V product and epilogue.
+//
+// Sequence segments (when B*H*tiles is too small to fill the GPU): segment
+// s > 0 first runs from a zero state (FULL mode), storing its end state and
+// total decay.  Its outputs depend on the true start state only through
+// (Q * e^Gamma_seg) S_start, where Gamma_seg is the decay since the segment
+// start; once every channel has decayed past e^-41.6 = 2^-60 that term is
+// below 2^-60 of the read-out and the FULL outputs are stored as they are.
+// The chunks before that point are recomputed by a second launch (CORRECT
+// mode) from the exact start state, obtained by scanning the segment summaries
+// S_start(s+1) = diag(e^G_s) S_start(s) + S*_s.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -46,74 +66,119 @@
 namespace gla {
 namespace {
 
-constexpr int kChunk = 128;       // tokens per chunk = MMA M
-constexpr int kThreads = 128;     // one thread per TMEM lane
-constexpr float kExpBound = 30.f; // fast path needs |Gamma| <= kExpBound per chunk
-constexpr uint32_t kTileRowBytes = 128;               // one swizzled row
-constexpr uint32_t kBlk = kChunk * kTileRowBytes;     // 64-column block of a 128-row tile
+constexpr int kChunk = 128;
+constexpr int kThreads = 320;           // 10 warps
+constexpr int kMmaWarp = 8;
+constexpr int kTmaWarp = 9;
+constexpr float kExpBound = 30.f;
+constexpr float kWindowCut = 41.58883083f;  // 60 ln 2
+constexpr uint32_t kBlk = kChunk * 128;     // one 64-column block of a 128-row tile
+
+constexpr int kItemLast = 1;   // last item of its chunk: releases the chunk's V stage
+constexpr int kItemStore = 2;  // store this item's output rows
+constexpr int kItemEnd = 4;    // end of the item stream
+
+constexpr int kModeFull = 0, kModeCorrect = 1;
+
+struct ItemInfo {
+    int t0, r0, r1, flags, lc, pad[3];
+};
+
+struct ChunkReq {
+    int t0, first_item, end, pad;
+};
+
+enum Bar {
+    kBarQkFull = 0, kBarQkEmpty, kBarItem, kBarPFull, kBarPSplit, kBarSDone, kBarSReady,
+    kBarOFull0, kBarOFull1, kBarOFree0, kBarOFree1, kBarVFull, kBarVEmpty, kBarAFull,
+    kBarQkRaw, kBarReq, kNumBars
+};
+// arrival counts, in enum order
+__device__ constexpr uint32_t kBarCounts[kNumBars] = {4, 1, 1, 1, 4, 1, 4, 1, 1, 4, 4, 1, 1, 1, 1, 1};
 
 template <int DK, int DVT>
 struct Smem {
-    static constexpr uint32_t kQ = 0;
     static constexpr uint32_t kQBytes = kChunk * DK * 2;
-    static constexpr uint32_t kK = kQ + kQBytes;          // Kh (high part)
-    static constexpr uint32_t kKlo = kK + kQBytes;        // Kh low part
-    static constexpr uint32_t kV = kKlo + kQBytes;
-    static constexpr uint32_t kVBytes = kChunk * DVT * 2;
-    static constexpr uint32_t kS = kV + kVBytes;
-    static constexpr uint32_t kSBlk = DK * kTileRowBytes;  // 64-column block of the state copy
-    static constexpr uint32_t kSBytes = DK * DVT * 2;
-    static constexpr uint32_t kA = kS + kSBytes;
+    static constexpr uint32_t kQ = 0;                     // Q, rescaled in place to Qh
+    static constexpr uint32_t kK = kQ + kQBytes;          // K, rescaled in place to Kh_hi
+    static constexpr uint32_t kKlo = kK + kQBytes;        // Kh_lo
+    static constexpr uint32_t kA = kKlo + kQBytes;        // fp32 log gates [128][DK]
     static constexpr uint32_t kABytes = kChunk * DK * 4;
-    static constexpr uint32_t kBar = kA + kABytes;
-    static constexpr uint32_t kTotal = kBar + 64;
-    static constexpr uint32_t kAlloc = kTotal + 1024;     // slack for 1024-byte alignment
+    static constexpr uint32_t kVBytes = kChunk * DVT * 2;
+    static constexpr uint32_t kV = kA + kABytes;
+    static constexpr uint32_t kSBlk = DK * 128;
+    static constexpr uint32_t kSBytes = DK * DVT * 2;
+    static constexpr uint32_t kS = kV + kVBytes;
+    static constexpr uint32_t kG = kS + kSBytes;          // float [2][DK]: state scale per item
+    static constexpr uint32_t kItem = kG + 2 * DK * 4;    // ItemInfo[2]
+    static constexpr uint32_t kReq = kItem + 64;          // ChunkReq
+    static constexpr uint32_t kBar = kReq + 16;           // mbarriers
+    static constexpr uint32_t kMisc = kBar + 8 * kNumBars;  // tmem slot
+    static constexpr uint32_t kTotal = kMisc + 16;
+    // At least 120 KB so that only one CTA fits on an SM: each CTA allocates
+    // all 512 TMEM columns.
+    static constexpr uint32_t kAlloc = (kTotal + 1024) > 122880u ? (kTotal + 1024) : 122880u;
     static_assert(kAlloc <= 232448, "shared memory budget exceeded");
 };
 
-// TMEM columns: P [0,128) (fp32 scores, then its bf16 hi/lo pair in place),
-// O [128,128+DVT), S [256,256+DVT).
-constexpr uint32_t kTmemP = 0, kTmemO = 128, kTmemS = 256, kTmemCols = 512;
+// TMEM columns: P [0,128) (fp32 scores, then the bf16 hi/lo pair in place),
+// O0 [128,128+DVT), O1, S after them.
+template <int DVT>
+struct Tmem {
+    static constexpr uint32_t kP = 0, kO0 = 128, kO1 = 128 + DVT, kS = 128 + 2 * DVT;
+    static constexpr uint32_t kCols = 512;
+};
 
-__device__ __forceinline__ float bf16_at(const uint8_t *base, uint32_t off) {
-    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(base + off));
-}
-__device__ __forceinline__ void bf16_put(uint8_t *base, uint32_t off, float x) {
-    *reinterpret_cast<__nv_bfloat16 *>(base + off) = __float2bfloat16_rn(x);
-}
-// x = hi + lo with hi = bf16(x), lo = bf16(x - hi); writes both, returns nothing.
-__device__ __forceinline__ void bf16_split_put(uint8_t *hi_base, uint8_t *lo_base, uint32_t off,
-                                               float x) {
-    const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-    *reinterpret_cast<__nv_bfloat16 *>(hi_base + off) = hi;
-    *reinterpret_cast<__nv_bfloat16 *>(lo_base + off) = __float2bfloat16_rn(x - __bfloat162float(hi));
+struct KParams {
+    CUtensorMap tm_q, tm_k, tm_a, tm_v;
+    const uint32_t *q;  // bf16 pairs
+    const uint32_t *k;
+    const float2 *a;
+    const float *h0;
+    float *hT;
+    __nv_bfloat16 *o;
+    float *ws_state;    // [n_seg][BH][DK][dv]
+    float *ws_decay;    // [n_seg][BH][DK]
+    float scale;
+    int H, T, dv, n_seg, seg_chunks, mode, force_sub;
+    unsigned int *status;
+};
+
+__device__ __forceinline__ bool bar_or(int id, int n, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(pred ? 1u : 0u), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
 }
 
-// Row i (= lane) of P, 32 consecutive columns starting at column 32*q, held in
-// x[]: store its bf16 hi/lo pair in place as the TMEM A operand of P V —
-// hi words at columns [32q, 32q+16), lo words at [32q+16, 32q+32).
-__device__ __forceinline__ void store_p_split(uint32_t t_P, int q, const float (&x)[32]) {
-    uint32_t hi[16], lo[16];
-#pragma unroll
-    for (int w = 0; w < 16; ++w) {
-        const __nv_bfloat16 h0 = __float2bfloat16_rn(x[2 * w]);
-        const __nv_bfloat16 h1 = __float2bfloat16_rn(x[2 * w + 1]);
-        hi[w] = static_cast<uint32_t>(__bfloat16_as_ushort(h0)) |
-                (static_cast<uint32_t>(__bfloat16_as_ushort(h1)) << 16);
-        lo[w] = pack_bf16x2(x[2 * w] - __bfloat162float(h0), x[2 * w + 1] - __bfloat162float(h1));
-    }
-    tmem_st16(t_P + 32 * q, hi);
-    tmem_st16(t_P + 32 * q + 16, lo);
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) { return pack_bf16x2(lo, hi); }
+
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// Split (x, y) into bf16 hi pair and bf16 lo pair.
+__device__ __forceinline__ void split_pair(float x, float y, uint32_t &hi, uint32_t &lo) {
+    const __nv_bfloat16 hx = __float2bfloat16_rn(x), hy = __float2bfloat16_rn(y);
+    hi = static_cast<uint32_t>(__bfloat16_as_ushort(hx)) |
+         (static_cast<uint32_t>(__bfloat16_as_ushort(hy)) << 16);
+    lo = pack_bf16x2(x - __bfloat162float(hx), y - __bfloat162float(hy));
+}
+
+__device__ __forceinline__ float clamp_gate(float a) {
+    return fminf(fmaxf(a, -kExpBound), kExpBound);
 }
 
 template <int DK, int DVT>
-__global__ void __launch_bounds__(kThreads, 1)
-    chunk_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_a,
-                     const float *__restrict__ h0, float *__restrict__ hT,
-                     __nv_bfloat16 *__restrict__ o, float scale, int H, int T, int dv,
-                     int force_exact, unsigned int *status) {
+__global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_constant__ KParams p) {
     using L = Smem<DK, DVT>;
+    using TM = Tmem<DVT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -123,366 +188,543 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *sV = smem + L::kV;
     uint8_t *sS = smem + L::kS;
     float *sA = reinterpret_cast<float *>(smem + L::kA);
-    uint64_t *bar_tma = reinterpret_cast<uint64_t *>(smem + L::kBar);
-    uint64_t *bar_mma = bar_tma + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_tma + 2);
-    int *s_abort = reinterpret_cast<int *>(bar_tma + 3);
+    float *sG = reinterpret_cast<float *>(smem + L::kG);
+    ItemInfo *sItem = reinterpret_cast<ItemInfo *>(smem + L::kItem);
+    ChunkReq *sReq = reinterpret_cast<ChunkReq *>(smem + L::kReq);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBar);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
 
     const int tid = threadIdx.x;
-    const int warp = tid >> 5;
+    const int warp = tid >> 5, lane = tid & 31;
     const int dv_tile = blockIdx.x;
-    const int h = blockIdx.y, b = blockIdx.z;
-    const int bh = b * H + h;
+    const int h = blockIdx.y;
+    const int nseg_launch = p.mode == kModeFull ? p.n_seg : p.n_seg - 1;
+    const int b = blockIdx.z / nseg_launch;
+    const int seg = blockIdx.z % nseg_launch + (p.mode == kModeFull ? 0 : 1);
+    const int bh = b * p.H + h;
     const int dv0 = dv_tile * DVT;
+    const int T = p.T;
+    const int n_chunks = (T + kChunk - 1) / kChunk;
+    const int c_begin = seg * p.seg_chunks;
+    const int c_end = min(n_chunks, c_begin + p.seg_chunks);
+    const size_t BHn = static_cast<size_t>(gridDim.z / nseg_launch) * p.H;  // B * H
 
     if (tid == 0) {
-        mbar_init(bar_tma, 1);
-        mbar_init(bar_mma, 1);
+        for (int i = 0; i < kNumBars; ++i) mbar_init(&bars[i], kBarCounts[i]);
         fence_mbar_init();
-        *s_abort = 0;
-        prefetch_tensormap(&tm_q);
-        prefetch_tensormap(&tm_k);
-        prefetch_tensormap(&tm_v);
-        prefetch_tensormap(&tm_a);
     }
-    if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
+    if (warp == kTmaWarp && lane == 0) {
+        prefetch_tensormap(&p.tm_q);
+        prefetch_tensormap(&p.tm_k);
+        prefetch_tensormap(&p.tm_a);
+        prefetch_tensormap(&p.tm_v);
+    }
+    if (warp == kMmaWarp) tmem_alloc(tmem_slot, TM::kCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;  // this warp's TMEM lanes
-    const uint32_t t_P = tmem + lane_base + kTmemP;
-    const uint32_t t_O = tmem + lane_base + kTmemO;
-    const uint32_t t_S = tmem + lane_base + kTmemS;
-    const bool owns_state_row = (warp * 32) < DK;  // warp-uniform: lanes < DK are S rows
-    const int d = tid;                             // key channel of this thread (if < DK)
 
-    // ---- initial state: TMEM S (fp32) and its bf16 operand copy.
-    if (owns_state_row) {
-        const float *src = h0 ? h0 + (static_cast<size_t>(bh) * DK + d) * dv + dv0 : nullptr;
-#pragma unroll
-        for (int c0 = 0; c0 < DVT; c0 += 32) {
-            uint32_t r[32];
-#pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-                float4 x = src ? *reinterpret_cast<const float4 *>(src + c0 + j)
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
-                r[j] = __float_as_uint(x.x);
-                r[j + 1] = __float_as_uint(x.y);
-                r[j + 2] = __float_as_uint(x.z);
-                r[j + 3] = __float_as_uint(x.w);
+    if (warp < 4) {
+        // =========================================================== prep warps
+        constexpr int NP = DK / 2;          // channel pairs
+        constexpr int NQ = kChunk / NP;     // token parts
+        constexpr int TP = kChunk / NQ;     // tokens per part
+        const int pt = tid;
+        const int pr = pt % NP, part = pt / NP;
+        const int ch = 2 * pr;
+        const bool last_part = part == NQ - 1;
+        const size_t row0 = static_cast<size_t>(bh) * T;
+        const uint32_t *qb = p.q + (row0 * DK + ch) / 2;   // global rows, sub-chunk path only
+        const uint32_t *kb = p.k + (row0 * DK + ch) / 2;
+        constexpr int kStride = DK / 2;     // row stride in bf16 pairs
+        const float *sAc = sA + ch;         // this thread's channel pair in the A tile
+        float gseg0 = 0.f, gseg1 = 0.f;     // decay since the segment start (last part only)
+        bool closed = (p.mode == kModeFull && seg == 0);  // no correction window
+        int n = 0;
+        bool ok = true;
+        for (int c = c_begin, lc = 0;; ++c, ++lc) {
+            // ---- decide this chunk: past the segment end, or (correction pass)
+            // past the point where the segment's start state has decayed away.
+            // The reduction doubles as the barrier after which the previous
+            // chunk's A tile is free.
+            const bool win = !closed && last_part && (gseg0 > -kWindowCut || gseg1 > -kWindowCut);
+            const bool any_win = bar_or(1, 128, win);
+            if (!closed && !any_win) closed = true;
+            const bool end = c >= c_end || !ok || (p.mode == kModeCorrect && closed);
+            if (pt == 0) {
+                sReq[0] = ChunkReq{end ? -1 : c * kChunk, n, end ? 1 : 0, 0};
+                mbar_arrive(&bars[kBarReq]);
             }
-            tmem_st32(t_S + c0, r);
-#pragma unroll
-            for (int j = 0; j < 32; j += 8) {
-                uint4 pk;
-                pk.x = pack_bf16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
-                pk.y = pack_bf16x2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
-                pk.z = pack_bf16x2(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5]));
-                pk.w = pack_bf16x2(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7]));
-                *reinterpret_cast<uint4 *>(sS + sw128_offset(d, c0 + j, L::kSBlk)) = pk;
+            if (end) break;
+            const int t0 = c * kChunk;
+            const bool store = p.mode == kModeCorrect || closed;
+            bool okw = mbar_wait_bounded(&bars[kBarAFull], lc & 1, p.status);
+            okw = okw && mbar_wait_bounded(&bars[kBarQkRaw], lc & 1, p.status);
+            ok = !bar_or(4, 128, !okw);   // one verdict for all prep threads
+            if (!ok) break;
+            // ---- prefix over the earlier parts of this chunk
+            float g0 = 0.f, g1 = 0.f;
+#pragma unroll 8
+            for (int i = 0; i < part * TP; ++i) {
+                const float2 a = *reinterpret_cast<const float2 *>(sAc + i * DK);
+                g0 += a.x;
+                g1 += a.y;
+            }
+            // ---- fast attempt: one block, reference = chunk start, in place
+            float mn = 0.f, mx = 0.f;
+#pragma unroll 8
+            for (int ii = 0; ii < TP; ++ii) {
+                const int i = part * TP + ii;
+                const float2 a = *reinterpret_cast<const float2 *>(sAc + i * DK);
+                const uint32_t off = sw128_offset(i, ch, kBlk);
+                const uint32_t qw = *reinterpret_cast<const uint32_t *>(sQ + off);
+                const uint32_t kw = *reinterpret_cast<const uint32_t *>(sK + off);
+                g0 += a.x;
+                g1 += a.y;
+                mn = fminf(mn, fminf(g0, g1));
+                mx = fmaxf(mx, fmaxf(g0, g1));
+                const float2 qf = unpack_bf16x2(qw), kf = unpack_bf16x2(kw);
+                *reinterpret_cast<uint32_t *>(sQ + off) =
+                    bf16x2_bits(qf.x * __expf(g0), qf.y * __expf(g1));
+                uint32_t hi, lo;
+                split_pair(kf.x * __expf(-g0), kf.y * __expf(-g1), hi, lo);
+                *reinterpret_cast<uint32_t *>(sK + off) = hi;
+                *reinterpret_cast<uint32_t *>(sKlo + off) = lo;
+            }
+            const bool bad = bar_or(2, 128, fmaxf(-mn, mx) > kExpBound || p.force_sub != 0);
+            if (!bad) {
+                if (last_part) {
+                    sG[(n & 1) * DK + ch] = __expf(g0);
+                    sG[(n & 1) * DK + ch + 1] = __expf(g1);
+                    gseg0 += g0;
+                    gseg1 += g1;
+                }
+                if (pt == 0) {
+                    sItem[n & 1] = ItemInfo{t0, 0, kChunk, kItemLast | (store ? kItemStore : 0), lc,
+                                            {0, 0, 0}};
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[kBarQkFull]);
+                ++n;
+                continue;
+            }
+            // ---- sub-chunk rescaling: the largest power-of-two block length cs
+            // whose every block keeps |Gamma - r_block| <= kExpBound (clamped
+            // gates).  Q and K are re-read from global memory: the tiles hold
+            // the fast attempt.
+            float bnd0[NQ], bnd1[NQ];  // clamped Gamma just before each part start
+            {
+                float c0 = 0.f, c1 = 0.f;
+                bnd0[0] = 0.f;
+                bnd1[0] = 0.f;
+                for (int qq = 1; qq < NQ; ++qq) {
+                    for (int i = (qq - 1) * TP; i < qq * TP; ++i) {
+                        const float2 a = *reinterpret_cast<const float2 *>(sAc + i * DK);
+                        c0 += clamp_gate(a.x);
+                        c1 += clamp_gate(a.y);
+                    }
+                    bnd0[qq] = c0;
+                    bnd1[qq] = c1;
+                }
+            }
+            int cs = 64;
+            for (; cs > 1; cs >>= 1) {
+                float c0 = bnd0[part], c1 = bnd1[part];
+                const int s_first = (part * TP) / cs * cs;
+                float r0 = (s_first >= part * TP) ? c0 : bnd0[s_first / TP];
+                float r1 = (s_first >= part * TP) ? c1 : bnd1[s_first / TP];
+                bool viol = false;
+                for (int ii = 0; ii < TP; ++ii) {
+                    const int i = part * TP + ii;
+                    if (i % cs == 0) {
+                        r0 = c0;
+                        r1 = c1;
+                    }
+                    const float2 a = *reinterpret_cast<const float2 *>(sAc + i * DK);
+                    c0 += clamp_gate(a.x);
+                    c1 += clamp_gate(a.y);
+                    viol |= fabsf(c0 - r0) > kExpBound || fabsf(c1 - r1) > kExpBound;
+                }
+                if (!bar_or(3, 128, viol)) break;
+            }
+            // cs == 1 always satisfies the bound: a single clamped gate is within it.
+            const int n_sub = kChunk / cs;
+            float gtot0 = 0.f, gtot1 = 0.f;
+            for (int sidx = 0; sidx < n_sub; ++sidx) {
+                const int sa = sidx * cs, sb = sa + cs;
+                okw = true;
+                if (sidx > 0) okw = mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status);
+                ok = !bar_or(4, 128, !okw);
+                if (!ok) break;
+                // reference for block sidx: clamped Gamma just before token sa
+                float c0 = bnd0[part], c1 = bnd1[part];
+                float r0 = 0.f, r1 = 0.f;
+                if (sa <= part * TP) {
+                    r0 = bnd0[sa / TP];
+                    r1 = bnd1[sa / TP];
+                }
+                for (int ii = 0; ii < TP; ++ii) {
+                    const int i = part * TP + ii;
+                    if (i == sa) {
+                        r0 = c0;
+                        r1 = c1;
+                    }
+                    const int t = t0 + i;
+                    const float2 a = *reinterpret_cast<const float2 *>(sAc + i * DK);
+                    c0 += clamp_gate(a.x);
+                    c1 += clamp_gate(a.y);
+                    const uint32_t off = sw128_offset(i, ch, kBlk);
+                    uint32_t hi = 0u, lo = 0u, qv = 0u;
+                    if (i >= sa && i < sb && t < T) {
+                        const float2 qf = unpack_bf16x2(qb[static_cast<size_t>(t) * kStride]);
+                        const float2 kf = unpack_bf16x2(kb[static_cast<size_t>(t) * kStride]);
+                        qv = bf16x2_bits(qf.x * __expf(c0 - r0), qf.y * __expf(c1 - r1));
+                        split_pair(kf.x * __expf(r0 - c0), kf.y * __expf(r1 - c1), hi, lo);
+                    }
+                    *reinterpret_cast<uint32_t *>(sQ + off) = qv;
+                    *reinterpret_cast<uint32_t *>(sK + off) = hi;
+                    *reinterpret_cast<uint32_t *>(sKlo + off) = lo;
+                    if (i == sb - 1) {
+                        sG[(n & 1) * DK + ch] = __expf(c0 - r0);
+                        sG[(n & 1) * DK + ch + 1] = __expf(c1 - r1);
+                    }
+                }
+                if (last_part) {
+                    gtot0 = c0;
+                    gtot1 = c1;
+                }
+                if (pt == 0) {
+                    sItem[n & 1] = ItemInfo{
+                        t0, sa, sb, (sidx == n_sub - 1 ? kItemLast : 0) | (store ? kItemStore : 0),
+                        lc, {0, 0, 0}};
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[kBarQkFull]);
+                ++n;
+            }
+            if (last_part) {
+                gseg0 += gtot0;
+                gseg1 += gtot1;
             }
         }
-        tmem_wait_st();
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-
-    const uint32_t load_bytes = 2u * L::kQBytes + L::kVBytes + L::kABytes;
-    const uint32_t qk_bytes = 2u * L::kQBytes;
-    constexpr uint32_t id_qk = idesc_bf16(128, 128, false, false);   // P = Qh Kh^T
-    constexpr uint32_t id_qs = idesc_bf16(128, DVT, false, true);    // O = Qh S
-    constexpr uint32_t id_pv = idesc_bf16(128, DVT, false, true);    // O += P V
-    constexpr uint32_t id_kv = idesc_bf16(128, DVT, true, true);     // S += Kh^T V
-    const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aKlo = smem_u32(sKlo);
-    const uint32_t aV = smem_u32(sV), aS = smem_u32(sS);
-
-    uint32_t ph_tma = 0, ph_mma = 0;
-    const int n_chunks = (T + kChunk - 1) / kChunk;
-    bool ok = true;
-
-    for (int u = 0; u < n_chunks && ok; ++u) {
-        const int t0 = u * kChunk;
-        // ---------------- A1: TMA loads of the chunk
-        if (tid == 0) {
-            fence_proxy_async_smem();
-            mbar_arrive_expect_tx(bar_tma, load_bytes);
-#pragma unroll
-            for (int kb = 0; kb < DK / 64; ++kb) {
-                tma_load_3d(sQ + kb * kBlk, &tm_q, bar_tma, kb * 64, t0, bh);
-                tma_load_3d(sK + kb * kBlk, &tm_k, bar_tma, kb * 64, t0, bh);
-            }
-#pragma unroll
-            for (int nb = 0; nb < DVT / 64; ++nb)
-                tma_load_3d(sV + nb * kBlk, &tm_v, bar_tma, dv0 + nb * 64, t0, bh);
-            tma_load_3d(sA, &tm_a, bar_tma, 0, t0, bh);
+        // ---- end of the item stream
+        if (n > 0 && !mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status)) ok = false;
+        if (pt == 0) sItem[n & 1] = ItemInfo{0, 0, 0, kItemEnd, 0, {0, 0, 0}};
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kBarQkFull]);
+        // segment summary: total decay of this segment (FULL mode, several segments)
+        if (p.mode == kModeFull && p.n_seg > 1 && dv_tile == 0 && last_part) {
+            float *dst = p.ws_decay + (static_cast<size_t>(seg) * BHn + bh) * DK;
+            dst[ch] = gseg0;
+            dst[ch + 1] = gseg1;
         }
-        if (!mbar_wait_bounded(bar_tma, ph_tma, status)) *s_abort = 1;
-        ph_tma ^= 1;
-
-        // ---------------- A2: in-chunk fp32 prefix sum of the log gates and the
-        // bounded rescaling of Q and K (fast path, in place; Kh split hi + lo).
-        float gC = 0.f;     // Gamma at the chunk end, channel d
-        bool big = false;
-        if (d < DK) {
-            float g = 0.f, gmin = 0.f, gmax = 0.f;
-            for (int i = 0; i < kChunk; ++i) {
-                g += sA[i * DK + d];
-                gmin = fminf(gmin, g);
-                gmax = fmaxf(gmax, g);
-                const float eq = __expf(g), ek = __expf(-g);
-                const uint32_t off = sw128_offset(i, d, kBlk);
-                bf16_put(sQ, off, bf16_at(sQ, off) * eq);
-                bf16_split_put(sK, sKlo, off, bf16_at(sK, off) * ek);
+    } else if (warp == kTmaWarp) {
+        // =========================================================== TMA producer
+        if (lane == 0) {
+            for (int lc = 0;; ++lc) {
+                if (!mbar_wait_bounded(&bars[kBarReq], lc & 1, p.status)) break;
+                const ChunkReq rq = sReq[0];
+                if (rq.end) break;
+                const int t0 = rq.t0;
+                // A: the prep has released the previous chunk's A tile (request barrier)
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(&bars[kBarAFull], L::kABytes);
+                tma_load_3d(sA, &p.tm_a, &bars[kBarAFull], 0, t0, bh);
+                // Q, K: after the last item of the previous chunk has been consumed
+                if (rq.first_item > 0 &&
+                    !mbar_wait_bounded(&bars[kBarQkEmpty], (rq.first_item - 1) & 1, p.status))
+                    break;
+                mbar_arrive_expect_tx(&bars[kBarQkRaw], 2u * L::kQBytes);
+#pragma unroll
+                for (int kb = 0; kb < DK / 64; ++kb) {
+                    tma_load_3d(sQ + kb * kBlk, &p.tm_q, &bars[kBarQkRaw], kb * 64, t0, bh);
+                    tma_load_3d(sK + kb * kBlk, &p.tm_k, &bars[kBarQkRaw], kb * 64, t0, bh);
+                }
+                // V: after the previous chunk's P V and state products
+                if (lc > 0 && !mbar_wait_bounded(&bars[kBarVEmpty], (lc - 1) & 1, p.status)) break;
+                mbar_arrive_expect_tx(&bars[kBarVFull], L::kVBytes);
+#pragma unroll
+                for (int nb = 0; nb < DVT / 64; ++nb)
+                    tma_load_3d(sV + nb * kBlk, &p.tm_v, &bars[kBarVFull], dv0 + nb * 64, t0, bh);
             }
-            gC = g;
-            big = fmaxf(-gmin, gmax) > kExpBound;
         }
-        fence_proxy_async_smem();
-        const bool exact = __syncthreads_or((big || force_exact) ? 1 : 0) != 0;
-        if (*s_abort) { ok = false; break; }
-
-        if (!exact) {
-            // ---------------- A3/A5: P = Qh Kh^T, O = Qh S_prev, S += Kh^T V
-            if (tid == 0) {
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        // =========================================================== MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t id_qk = idesc_bf16(128, 128, false, false);   // P = Qh Kh^T
+            constexpr uint32_t id_ov = idesc_bf16(128, DVT, false, true);    // O = Qh S, O += P V
+            constexpr uint32_t id_kv = idesc_bf16(128, DVT, true, true);     // S += Kh^T V
+            const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aKlo = smem_u32(sKlo);
+            const uint32_t aV0 = smem_u32(sV), aS = smem_u32(sS);
+            for (int n = 0;; ++n) {
+                if (!mbar_wait_bounded(&bars[kBarQkFull], n & 1, p.status)) break;
+                const ItemInfo it = sItem[n & 1];
+                mbar_arrive(&bars[kBarItem]);
+                if (it.flags & kItemEnd) break;
+                const int ob = n & 1;
+                const uint32_t tO = tmem + (ob ? TM::kO1 : TM::kO0);
+                const uint32_t aV = aV0;
+                bool okw = true;
+                if (n >= 2) okw &= mbar_wait_bounded(&bars[kBarOFree0 + ob], ((n >> 1) + 1) & 1, p.status);
+                okw &= mbar_wait_bounded(&bars[kBarVFull], it.lc & 1, p.status);
+                if (!okw) break;
                 tc_fence_after();
+                // P = Qh (Kh_hi + Kh_lo)^T
 #pragma unroll
                 for (int ks = 0; ks < DK / 16; ++ks) {
                     const uint32_t koff = (ks >> 2) * kBlk + (ks & 3) * 32;
-                    mma_bf16_ss(tmem + kTmemP, sw128_desc(aQ + koff, 16, 1024),
+                    mma_bf16_ss(tmem + TM::kP, sw128_desc(aQ + koff, 16, 1024),
                                 sw128_desc(aK + koff, 16, 1024), id_qk, ks > 0);
                 }
 #pragma unroll
                 for (int ks = 0; ks < DK / 16; ++ks) {
                     const uint32_t koff = (ks >> 2) * kBlk + (ks & 3) * 32;
-                    mma_bf16_ss(tmem + kTmemP, sw128_desc(aQ + koff, 16, 1024),
+                    mma_bf16_ss(tmem + TM::kP, sw128_desc(aQ + koff, 16, 1024),
                                 sw128_desc(aKlo + koff, 16, 1024), id_qk, 1);
                 }
-#pragma unroll
-                for (int ks = 0; ks < DK / 16; ++ks) {
-                    const uint32_t koff = (ks >> 2) * kBlk + (ks & 3) * 32;
-                    mma_bf16_ss(tmem + kTmemO, sw128_desc(aQ + koff, 16, 1024),
-                                sw128_desc(aS + ks * 2048, L::kSBlk, 1024), id_qs, ks > 0);
-                }
-#pragma unroll
-                for (int ks = 0; ks < kChunk / 16; ++ks) {
-                    mma_bf16_ss(tmem + kTmemS, sw128_desc(aK + ks * 2048, kBlk, 1024),
-                                sw128_desc(aV + ks * 2048, kBlk, 1024), id_kv, 1);
-                    mma_bf16_ss(tmem + kTmemS, sw128_desc(aKlo + ks * 2048, kBlk, 1024),
-                                sw128_desc(aV + ks * 2048, kBlk, 1024), id_kv, 1);
-                }
-                mma_commit(bar_mma);
-            }
-            if (!mbar_wait_bounded(bar_mma, ph_mma, status)) *s_abort = 1;
-            ph_mma ^= 1;
-            tc_fence_after();
-
-            // ---------------- causal mask of P (row i = tid), split into the TMEM A operand
-            {
-                const int i = tid;
-#pragma unroll
-                for (int q = 0; q < kChunk / 32; ++q) {
-                    uint32_t r[32];
-                    tmem_ld32(t_P + 32 * q, r);
-                    tmem_wait_ld();
-                    float x[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) x[e] = (32 * q + e <= i) ? __uint_as_float(r[e]) : 0.f;
-                    store_p_split(t_P, q, x);
-                }
-                tmem_wait_st();
-            }
-            tc_fence_before();
-            __syncthreads();
-            if (*s_abort) { ok = false; break; }
-        } else {
-            // ---------------- exact path: reload raw Q, K; Gamma in place of A.
-            __syncthreads();
-            if (tid == 0) {
-                fence_proxy_async_smem();
-                mbar_arrive_expect_tx(bar_tma, qk_bytes);
-#pragma unroll
-                for (int kb = 0; kb < DK / 64; ++kb) {
-                    tma_load_3d(sQ + kb * kBlk, &tm_q, bar_tma, kb * 64, t0, bh);
-                    tma_load_3d(sK + kb * kBlk, &tm_k, bar_tma, kb * 64, t0, bh);
-                }
-            }
-            if (d < DK) {
-                float g = 0.f;
-                for (int i = 0; i < kChunk; ++i) {
-                    g += sA[i * DK + d];
-                    sA[i * DK + d] = g;
-                }
-            }
-            if (!mbar_wait_bounded(bar_tma, ph_tma, status)) *s_abort = 1;
-            ph_tma ^= 1;
-            __syncthreads();
-            if (*s_abort) { ok = false; break; }
-            // Score row i, elementwise: P_ij = sum_d Q_id K_jd e^(Gamma_id - Gamma_jd), j <= i.
-            {
-                const int i = tid;
-#pragma unroll 1
-                for (int q = 0; q < kChunk / 32; ++q) {
-                    float x[32];
-#pragma unroll 1
-                    for (int e = 0; e < 32; ++e) {
-                        const int j = 32 * q + e;
-                        float acc = 0.f;
-                        if (j <= i) {
-                            for (int dd = 0; dd < DK; ++dd) {
-                                acc += bf16_at(sQ, sw128_offset(i, dd, kBlk)) *
-                                       bf16_at(sK, sw128_offset(j, dd, kBlk)) *
-                                       __expf(sA[i * DK + dd] - sA[j * DK + dd]);
-                            }
-                        }
-                        x[e] = acc;
-                    }
-                    store_p_split(t_P, q, x);
-                }
-                tmem_wait_st();
-            }
-            __syncthreads();
-            if (d < DK) {
-                for (int i = 0; i < kChunk; ++i) {
-                    const float g = sA[i * DK + d];
-                    const uint32_t off = sw128_offset(i, d, kBlk);
-                    bf16_put(sQ, off, bf16_at(sQ, off) * __expf(g));
-                    bf16_split_put(sK, sKlo, off, bf16_at(sK, off) * __expf(gC - g));
-                }
-            }
-            // S_prev <- diag(e^Gamma_C) S_prev before the K^T V accumulation.
-            if (owns_state_row) {
-                const float f = __expf(gC);
-#pragma unroll
-                for (int c0 = 0; c0 < DVT; c0 += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(t_S + c0, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * f);
-                    tmem_st32(t_S + c0, r);
-                }
-                tmem_wait_st();
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncthreads();
-            if (tid == 0) {
+                mma_commit(&bars[kBarPFull]);
+                // O = Qh S_prev (needs the previous state scaled and copied)
+                if (!mbar_wait_bounded(&bars[kBarSReady], n & 1, p.status)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < DK / 16; ++ks) {
                     const uint32_t koff = (ks >> 2) * kBlk + (ks & 3) * 32;
-                    mma_bf16_ss(tmem + kTmemO, sw128_desc(aQ + koff, 16, 1024),
-                                sw128_desc(aS + ks * 2048, L::kSBlk, 1024), id_qs, ks > 0);
+                    mma_bf16_ss(tO, sw128_desc(aQ + koff, 16, 1024),
+                                sw128_desc(aS + ks * 2048, L::kSBlk, 1024), id_ov, ks > 0);
                 }
+                // S += (Kh_hi + Kh_lo)^T V
 #pragma unroll
                 for (int ks = 0; ks < kChunk / 16; ++ks) {
-                    mma_bf16_ss(tmem + kTmemS, sw128_desc(aK + ks * 2048, kBlk, 1024),
+                    mma_bf16_ss(tmem + TM::kS, sw128_desc(aK + ks * 2048, kBlk, 1024),
                                 sw128_desc(aV + ks * 2048, kBlk, 1024), id_kv, 1);
-                    mma_bf16_ss(tmem + kTmemS, sw128_desc(aKlo + ks * 2048, kBlk, 1024),
+                    mma_bf16_ss(tmem + TM::kS, sw128_desc(aKlo + ks * 2048, kBlk, 1024),
                                 sw128_desc(aV + ks * 2048, kBlk, 1024), id_kv, 1);
                 }
-                // (O += P V is issued below, shared with the fast path.)
-            }
-        }
-
-        // ---------------- A4: O += P V with P = hi + lo from TMEM
-        if (tid == 0) {
-            tc_fence_after();
+                mma_commit(&bars[kBarSDone]);
+                mma_commit(&bars[kBarQkEmpty]);
+                // O += (P_hi + P_lo) V, P from TMEM
+                if (!mbar_wait_bounded(&bars[kBarPSplit], n & 1, p.status)) break;
+                tc_fence_after();
 #pragma unroll
-            for (int ks = 0; ks < kChunk / 16; ++ks) {
-                const uint32_t pcol = kTmemP + 32 * (ks >> 1) + 8 * (ks & 1);
-                mma_bf16_ts(tmem + kTmemO, tmem + pcol, sw128_desc(aV + ks * 2048, kBlk, 1024),
-                            id_pv, 1);
-                mma_bf16_ts(tmem + kTmemO, tmem + pcol + 16, sw128_desc(aV + ks * 2048, kBlk, 1024),
-                            id_pv, 1);
+                for (int ks = 0; ks < kChunk / 16; ++ks) {
+                    const uint32_t pcol = TM::kP + 32 * (ks >> 1) + 8 * (ks & 1);
+                    mma_bf16_ts(tO, tmem + pcol, sw128_desc(aV + ks * 2048, kBlk, 1024), id_ov, 1);
+                    mma_bf16_ts(tO, tmem + pcol + 16, sw128_desc(aV + ks * 2048, kBlk, 1024), id_ov,
+                                1);
+                }
+                mma_commit(&bars[kBarOFull0 + ob]);
+                if (it.flags & kItemLast) mma_commit(&bars[kBarVEmpty]);
             }
-            mma_commit(bar_mma);
         }
-        if (!mbar_wait_bounded(bar_mma, ph_mma, status)) *s_abort = 1;
-        ph_mma ^= 1;
-        tc_fence_after();
+        __syncwarp();
+    } else {
+        // =========================================================== TMEM warps
+        const int i = tid - 128;                  // TMEM lane = row = key channel
+        const uint32_t lane_base = static_cast<uint32_t>((warp - 4) * 32) << 16;
+        const bool has_state_row = ((warp - 4) * 32) < DK;  // warp-uniform
+        const uint32_t tP = tmem + lane_base + TM::kP;
+        const uint32_t tS = tmem + lane_base + TM::kS;
 
-        // ---------------- epilogue: O rows out; state scale and bf16 copy.
-        {
-            const int i = tid;
-            const bool row_valid = (t0 + i) < T;
-            __nv_bfloat16 *orow = o + (static_cast<size_t>(bh) * T + (t0 + i)) * dv + dv0;
+        // ---- initial state
+        if (has_state_row) {
+            float *hT_dst = nullptr;
+            float eG = 0.f;
+            const float *sstar = nullptr;
+            if (p.mode == kModeCorrect && seg == p.n_seg - 1 && p.hT) {
+                hT_dst = p.hT + (static_cast<size_t>(bh) * DK + i) * p.dv + dv0;
+                eG = __expf(p.ws_decay[(static_cast<size_t>(seg) * BHn + bh) * DK + i]);
+                sstar = p.ws_state + ((static_cast<size_t>(seg) * BHn + bh) * DK + i) * p.dv + dv0;
+            }
 #pragma unroll
             for (int c0 = 0; c0 < DVT; c0 += 32) {
-                uint32_t r[32];
-                tmem_ld32(t_O + c0, r);
-                tmem_wait_ld();
-                if (row_valid) {
+                float x[32];
 #pragma unroll
-                    for (int j = 0; j < 32; j += 8) {
-                        uint4 pk;
-                        pk.x = pack_bf16x2(scale * __uint_as_float(r[j]), scale * __uint_as_float(r[j + 1]));
-                        pk.y = pack_bf16x2(scale * __uint_as_float(r[j + 2]), scale * __uint_as_float(r[j + 3]));
-                        pk.z = pack_bf16x2(scale * __uint_as_float(r[j + 4]), scale * __uint_as_float(r[j + 5]));
-                        pk.w = pack_bf16x2(scale * __uint_as_float(r[j + 6]), scale * __uint_as_float(r[j + 7]));
-                        *reinterpret_cast<uint4 *>(orow + c0 + j) = pk;
+                for (int j = 0; j < 32; ++j) x[j] = 0.f;
+                if (p.mode == kModeFull) {
+                    if (seg == 0 && p.h0) {
+                        const float *src = p.h0 + (static_cast<size_t>(bh) * DK + i) * p.dv + dv0 + c0;
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4) {
+                            const float4 v4 = *reinterpret_cast<const float4 *>(src + j);
+                            x[j] = v4.x;
+                            x[j + 1] = v4.y;
+                            x[j + 2] = v4.z;
+                            x[j + 3] = v4.w;
+                        }
+                    }
+                } else {
+                    // S_start(seg) by the scan of the segment summaries before it
+                    for (int s2 = 0; s2 < seg; ++s2) {
+                        const float e = __expf(p.ws_decay[(static_cast<size_t>(s2) * BHn + bh) * DK + i]);
+                        const float *src = p.ws_state +
+                                           ((static_cast<size_t>(s2) * BHn + bh) * DK + i) * p.dv + dv0 + c0;
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4) {
+                            const float4 v4 = *reinterpret_cast<const float4 *>(src + j);
+                            x[j] = fmaf(e, x[j], v4.x);
+                            x[j + 1] = fmaf(e, x[j + 1], v4.y);
+                            x[j + 2] = fmaf(e, x[j + 2], v4.z);
+                            x[j + 3] = fmaf(e, x[j + 3], v4.w);
+                        }
+                    }
+                    if (hT_dst) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4) {
+                            const float4 v4 = *reinterpret_cast<const float4 *>(sstar + c0 + j);
+                            *reinterpret_cast<float4 *>(hT_dst + c0 + j) =
+                                make_float4(fmaf(eG, x[j], v4.x), fmaf(eG, x[j + 1], v4.y),
+                                            fmaf(eG, x[j + 2], v4.z), fmaf(eG, x[j + 3], v4.w));
+                        }
                     }
                 }
-            }
-        }
-        if (owns_state_row) {
-            const float f = exact ? 1.f : __expf(gC);
-#pragma unroll
-            for (int c0 = 0; c0 < DVT; c0 += 32) {
                 uint32_t r[32];
-                tmem_ld32(t_S + c0, r);
-                tmem_wait_ld();
-                if (!exact) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * f);
-                    tmem_st32(t_S + c0, r);
-                }
+                for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(x[j]);
+                tmem_st32(tS + c0, r);
 #pragma unroll
                 for (int j = 0; j < 32; j += 8) {
                     uint4 pk;
-                    pk.x = pack_bf16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
-                    pk.y = pack_bf16x2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
-                    pk.z = pack_bf16x2(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5]));
-                    pk.w = pack_bf16x2(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7]));
-                    *reinterpret_cast<uint4 *>(sS + sw128_offset(d, c0 + j, L::kSBlk)) = pk;
+                    pk.x = pack_bf16x2(x[j], x[j + 1]);
+                    pk.y = pack_bf16x2(x[j + 2], x[j + 3]);
+                    pk.z = pack_bf16x2(x[j + 4], x[j + 5]);
+                    pk.w = pack_bf16x2(x[j + 6], x[j + 7]);
+                    *reinterpret_cast<uint4 *>(sS + sw128_offset(i, c0 + j, L::kSBlk)) = pk;
                 }
             }
             tmem_wait_st();
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        __syncthreads();
-        if (*s_abort) ok = false;
-    }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kBarSReady]);   // phase 0: initial state ready
 
-    // ---- final state out.
-    if (ok && hT && owns_state_row) {
-        tc_fence_after();
-        float *dst = hT + (static_cast<size_t>(bh) * DK + d) * dv + dv0;
+        for (int n = 0;; ++n) {
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarItem], n & 1, p.status))) break;
+            const ItemInfo it = sItem[n & 1];
+            if (it.flags & kItemEnd) break;
+            const int ob = n & 1;
+            // ---- causal mask of P (row i), split into the TMEM A operand of P V
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarPFull], n & 1, p.status))) break;
+            tc_fence_after();
 #pragma unroll
-        for (int c0 = 0; c0 < DVT; c0 += 32) {
-            uint32_t r[32];
-            tmem_ld32(t_S + c0, r);
-            tmem_wait_ld();
+            for (int qd = 0; qd < kChunk / 32; ++qd) {
+                uint32_t r[32];
+                tmem_ld32(tP + 32 * qd, r);
+                tmem_wait_ld();
+                uint32_t hi[16], lo[16];
 #pragma unroll
-            for (int j = 0; j < 32; j += 4)
-                *reinterpret_cast<float4 *>(dst + c0 + j) =
-                    make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                                __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+                for (int w = 0; w < 16; ++w) {
+                    const int j = 32 * qd + 2 * w;
+                    const float x0 = (j <= i) ? __uint_as_float(r[2 * w]) : 0.f;
+                    const float x1 = (j + 1 <= i) ? __uint_as_float(r[2 * w + 1]) : 0.f;
+                    split_pair(x0, x1, hi[w], lo[w]);
+                }
+                tmem_st16(tP + 32 * qd, hi);
+                tmem_st16(tP + 32 * qd + 16, lo);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kBarPSplit]);
+            // ---- state: S <- diag(e^decay) S, and its bf16 copy for the next item
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarSDone], n & 1, p.status))) break;
+            tc_fence_after();
+            if (has_state_row) {
+                const float f = sG[(n & 1) * DK + i];
+#pragma unroll
+                for (int c0 = 0; c0 < DVT; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tS + c0, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * f);
+                    tmem_st32(tS + c0, r);
+#pragma unroll
+                    for (int j = 0; j < 32; j += 8) {
+                        uint4 pk;
+                        pk.x = pack_bf16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+                        pk.y = pack_bf16x2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+                        pk.z = pack_bf16x2(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5]));
+                        pk.w = pack_bf16x2(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7]));
+                        *reinterpret_cast<uint4 *>(sS + sw128_offset(i, c0 + j, L::kSBlk)) = pk;
+                    }
+                }
+                tmem_wait_st();
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kBarSReady]);
+            // ---- output rows
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarOFull0 + ob], (n >> 1) & 1, p.status)))
+                break;
+            tc_fence_after();
+            {
+                const uint32_t tO = tmem + lane_base + (ob ? TM::kO1 : TM::kO0);
+                const int t = it.t0 + i;
+                const bool st = (it.flags & kItemStore) && i >= it.r0 && i < it.r1 && t < T;
+                __nv_bfloat16 *orow = p.o + (static_cast<size_t>(bh) * T + t) * p.dv + dv0;
+#pragma unroll
+                for (int c0 = 0; c0 < DVT; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tO + c0, r);
+                    tmem_wait_ld();
+                    if (st) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 8) {
+                            uint4 pk;
+                            pk.x = pack_bf16x2(p.scale * __uint_as_float(r[j]), p.scale * __uint_as_float(r[j + 1]));
+                            pk.y = pack_bf16x2(p.scale * __uint_as_float(r[j + 2]), p.scale * __uint_as_float(r[j + 3]));
+                            pk.z = pack_bf16x2(p.scale * __uint_as_float(r[j + 4]), p.scale * __uint_as_float(r[j + 5]));
+                            pk.w = pack_bf16x2(p.scale * __uint_as_float(r[j + 6]), p.scale * __uint_as_float(r[j + 7]));
+                            *reinterpret_cast<uint4 *>(orow + c0 + j) = pk;
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kBarOFree0 + ob]);
+        }
+        // ---- final state of a FULL pass
+        if (p.mode == kModeFull && has_state_row) {
+            float *dst = nullptr;
+            if (p.n_seg == 1) {
+                if (p.hT) dst = p.hT + (static_cast<size_t>(bh) * DK + i) * p.dv + dv0;
+            } else {
+                dst = p.ws_state + ((static_cast<size_t>(seg) * BHn + bh) * DK + i) * p.dv + dv0;
+            }
+            if (dst) {
+                tc_fence_after();
+#pragma unroll
+                for (int c0 = 0; c0 < DVT; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tS + c0, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4 *>(dst + c0 + j) =
+                            make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                                        __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+                }
+            }
         }
     }
+
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(tmem, TM::kCols);
     }
 }
 
 template <int DK, int DVT>
-int launch_tiles(const ChunkLaunch &p, cudaStream_t stream) {
+int launch_tiles(const ChunkLaunch &c, cudaStream_t stream) {
     using L = Smem<DK, DVT>;
     auto kern = chunk_fwd_kernel<DK, DVT>;
     static bool attr_set = false;  // per instantiation, per process
@@ -492,10 +734,34 @@ int launch_tiles(const ChunkLaunch &p, cudaStream_t stream) {
         if (e != cudaSuccess) return static_cast<int>(e);
         attr_set = true;
     }
-    dim3 grid(p.dv / DVT, p.H, p.B);
-    kern<<<grid, kThreads, L::kAlloc, stream>>>(p.tm_q, p.tm_k, p.tm_v, p.tm_a, p.h0, p.hT,
-                                                static_cast<__nv_bfloat16 *>(p.o), p.scale, p.H,
-                                                p.T, p.dv, p.force_exact, p.status);
+    KParams p;
+    p.tm_q = c.tm_q;
+    p.tm_k = c.tm_k;
+    p.tm_a = c.tm_a;
+    p.tm_v = c.tm_v;
+    p.q = static_cast<const uint32_t *>(c.q);
+    p.k = static_cast<const uint32_t *>(c.k);
+    p.a = reinterpret_cast<const float2 *>(c.log_alpha);
+    p.h0 = c.h0;
+    p.hT = c.hT;
+    p.o = static_cast<__nv_bfloat16 *>(c.o);
+    p.ws_state = c.ws_state;
+    p.ws_decay = c.ws_decay;
+    p.scale = c.scale;
+    p.H = c.H;
+    p.T = c.T;
+    p.dv = c.dv;
+    p.n_seg = c.n_seg;
+    p.seg_chunks = c.seg_chunks;
+    p.force_sub = c.force_exact;
+    p.status = c.status;
+    const int n_dvt = c.dv / DVT;
+    p.mode = kModeFull;
+    kern<<<dim3(n_dvt, c.H, c.B * c.n_seg), kThreads, L::kAlloc, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || c.n_seg == 1) return static_cast<int>(e);
+    p.mode = kModeCorrect;
+    kern<<<dim3(n_dvt, c.H, c.B * (c.n_seg - 1)), kThreads, L::kAlloc, stream>>>(p);
     return static_cast<int>(cudaGetLastError());
 }
 

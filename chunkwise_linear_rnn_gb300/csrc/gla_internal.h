@@ -8,15 +8,20 @@
 namespace gla {
 
 struct ChunkLaunch {
-    // Tensor maps (3-D: channel, token, batch*head) for q, k, v, log_alpha.
-    CUtensorMap tm_q, tm_k, tm_v, tm_a;
+    // 3-D tensor maps (channel, token, batch*head): q, k, log_alpha, v
+    CUtensorMap tm_q, tm_k, tm_a, tm_v;
+    const void *q, *k;        // bf16 [BH, T, dk]
+    const float *log_alpha;   // fp32 [BH, T, dk]
     const float *h0;          // [BH, dk, dv] or null (zero state)
     float *hT;                // [BH, dk, dv] or null
     void *o;                  // bf16 [BH, T, dv]
+    float *ws_state;          // segment summaries [n_seg, BH, dk, dv] (n_seg > 1)
+    float *ws_decay;          // segment total decays [n_seg, BH, dk]   (n_seg > 1)
     float scale;
     int B, H, T, dk, dv;
     int dv_tile;              // 64 or 128
-    int force_exact;
+    int n_seg, seg_chunks;    // sequence segments and chunks per segment
+    int force_exact;          // process every chunk in rescaled sub-chunks
     unsigned int *status;     // device status word
 };
 

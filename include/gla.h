@@ -84,7 +84,7 @@ int gla_chunk_fwd(const void *q, const void *k, const void *v, const float *log_
 typedef struct gla_chunk_options {
     int segments;      /* sequence segments per (batch, head); 0 = automatic, 1 = no split */
     int dv_tile;       /* value columns per CTA: 0 = automatic, else 64 or 128             */
-    int force_exact;   /* 1 = take the exact (elementwise-decay) path for every chunk       */
+    int force_exact;   /* 1 = process every chunk as rescaled sub-chunks (test knob)          */
     int reserved[5];
 } gla_chunk_options;
 

@@ -117,9 +117,48 @@ def test_gate_of_one_is_linear_attention():
     _run_and_check(q, k, v, a, h0, "alpha = 1")
 
 
-def test_forced_exact_path_matches_oracle():
+def test_forced_sub_chunk_rescaling_matches_oracle():
     q, k, v, a, h0 = _inputs(1, 2, 300, 128, 128, h0=True, seed=8, sigma_z=2.0)
     _run_and_check(q, k, v, a, h0, "force_exact", force_exact=True)
+
+
+def test_gates_beyond_the_exponent_bound_are_exact():
+    # single tokens with log alpha far below -30: sub-chunks of one token, clamped gate
+    q, k, v, a, h0 = _inputs(1, 2, 260, 64, 128, h0=True, seed=12)
+    a[..., 5, :] = -200.0
+    a[..., 130:140, 3] = -45.0
+    _run_and_check(q, k, v, a, h0, "log alpha = -200 / -45 spikes")
+
+
+@pytest.mark.parametrize("segments", [2, 3, 5])
+def test_sequence_segments_match_oracle(segments):
+    q, k, v, a, h0 = _inputs(1, 2, 2600, 128, 128, h0=True, seed=20 + segments)
+    _run_and_check(q, k, v, a, h0, f"segments={segments}", segments=segments)
+
+
+def test_segments_with_slow_decay_recompute_whole_segments():
+    # alpha = 1: the start state never fades, every segment is recomputed from the scan
+    q, k, v, a, h0 = _inputs(1, 2, 1100, 64, 64, h0=True, seed=31)
+    a = torch.zeros_like(a)
+    _run_and_check(q, k, v, a, h0, "alpha=1 segments=4", segments=4)
+
+
+def test_segments_with_aliased_state():
+    q, k, v, a, h0 = _inputs(2, 1, 1500, 128, 256, h0=True, seed=32)
+    h = h0.clone()
+    o_ref, h_ref = _oracle(q, k, v, a, 128 ** -0.5, h0)
+    o, hT = gla.gla_chunk_fwd(q, k, v, a, None, h, final_state=h, segments=3)
+    assert_close(o.float().cpu().numpy(), o_ref, "segments aliased o", bf16_output=True)
+    assert_close(h.cpu().numpy(), h_ref, "segments aliased hT")
+
+
+def test_segment_count_does_not_change_results_beyond_tolerance():
+    q, k, v, a, h0 = _inputs(1, 1, 2048, 128, 128, h0=True, seed=33)
+    outs = [gla.gla_chunk_fwd(q, k, v, a, None, h0, segments=s) for s in (1, 2, 4)]
+    o_ref, h_ref = _oracle(q, k, v, a, 128 ** -0.5, h0)
+    for o, hT in outs:
+        assert_close(o.float().cpu().numpy(), o_ref, "segment sweep o", bf16_output=True)
+        assert_close(hT.cpu().numpy(), h_ref, "segment sweep hT")
 
 
 def test_mixed_fast_and_exact_chunks():
