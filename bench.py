@@ -162,7 +162,7 @@ def run_ours(args, rank, world, local_rank):
     def step():
         gla.gla_chunk_fwd(q, k, v, a, cfg.scale, h0, out=o, final_state=hT)
 
-    launches_per_step = 1
+    launches_per_step = gla.gla_chunk_fwd_plan(cfg.B, cfg.H, cfg.T, cfg.dk, cfg.dv)["launches"]
     for _ in range(args.warmup):
         step()
     barrier()

@@ -23,7 +23,7 @@ import torch
 from . import _lib
 from ._lib import GlaChunkOptions, GlaError, status_string  # noqa: F401
 
-__all__ = ["gla_chunk_fwd", "gla_recurrent_step", "gla_last_device_status", "GlaError",
+__all__ = ["gla_chunk_fwd", "gla_chunk_fwd_plan", "gla_recurrent_step", "gla_last_device_status", "GlaError",
            "status_string", "library_path"]
 
 library_path = _lib.LIB_PATH
@@ -89,6 +89,21 @@ def gla_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: 
             _stream(dev))
     _lib.check(st, "gla_chunk_fwd")
     return out, hT
+
+
+def gla_chunk_fwd_plan(B: int, H: int, T: int, dk: int, dv: int, *, segments: int = 0,
+                       dv_tile: int = 0, force_exact: bool = False) -> dict:
+    """The launch plan gla_chunk_fwd would use on the current device (no GPU work)."""
+    opts = GlaChunkOptions(segments=int(segments), dv_tile=int(dv_tile),
+                           force_exact=1 if force_exact else 0)
+    nseg, tile, launches = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    scratch = ctypes.c_ulong()
+    st = _lib.lib().gla_chunk_fwd_plan(B, H, T, dk, dv, ctypes.byref(opts), ctypes.byref(nseg),
+                                       ctypes.byref(tile), ctypes.byref(launches),
+                                       ctypes.byref(scratch))
+    _lib.check(st, "gla_chunk_fwd_plan")
+    return {"segments": nseg.value, "dv_tile": tile.value, "launches": launches.value,
+            "scratch_bytes": scratch.value}
 
 
 def gla_recurrent_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: torch.Tensor,

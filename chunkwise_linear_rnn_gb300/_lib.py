@@ -22,8 +22,8 @@ GLA_ERR_LAUNCH = 4
 GLA_ERR_TIMEOUT = 5
 GLA_ERR_ALLOC = 6
 
-EXPORTED = ("gla_chunk_fwd", "gla_chunk_fwd_ex", "gla_recurrent_step", "gla_status_string",
-            "gla_last_device_status", "gla_version")
+EXPORTED = ("gla_chunk_fwd", "gla_chunk_fwd_ex", "gla_chunk_fwd_plan", "gla_recurrent_step",
+            "gla_status_string", "gla_last_device_status", "gla_version")
 
 
 class GlaChunkOptions(ctypes.Structure):
@@ -48,6 +48,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.gla_chunk_fwd_ex.argtypes = [vp, vp, vp, fp, f, fp, vp, fp, i, i, i, i, i,
                                      ctypes.POINTER(GlaChunkOptions), vp]
     lib.gla_chunk_fwd_ex.restype = i
+    ip = ctypes.POINTER(ctypes.c_int)
+    lib.gla_chunk_fwd_plan.argtypes = [i, i, i, i, i, ctypes.POINTER(GlaChunkOptions), ip, ip, ip,
+                                       ctypes.POINTER(ctypes.c_ulong)]
+    lib.gla_chunk_fwd_plan.restype = i
     lib.gla_recurrent_step.argtypes = [vp, vp, vp, fp, f, fp, vp, i, i, i, i, vp]
     lib.gla_recurrent_step.restype = i
     lib.gla_status_string.argtypes = [i]

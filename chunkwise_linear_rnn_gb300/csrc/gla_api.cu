@@ -104,6 +104,30 @@ bool make_map(EncodeTiledFn enc, CUtensorMap *m, const void *ptr, CUtensorMapDat
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+struct Plan {
+    int dv_tile, n_seg, seg_chunks;
+};
+
+// Launch plan of gla_chunk_fwd: value-column tile, sequence segments.
+// Segments: enough (batch, head, tile, segment) units to fill the SMs once,
+// each segment at least 8 chunks long to amortise its correction window.
+Plan make_plan(int B, int H, int T, int dv, const gla_chunk_options &op, int sm_count) {
+    Plan pl;
+    pl.dv_tile = op.dv_tile ? op.dv_tile : (dv >= 128 ? 128 : 64);
+    const int n_chunks = (T + 127) / 128;
+    int n_seg = op.segments;
+    if (n_seg == 0) {
+        const long long units = static_cast<long long>(B) * H * (dv / pl.dv_tile);
+        n_seg = units > 0 ? static_cast<int>(sm_count / units) : 1;
+        n_seg = n_seg < n_chunks / 8 ? n_seg : n_chunks / 8;
+        if (n_seg < 1) n_seg = 1;
+    }
+    if (n_seg > n_chunks) n_seg = n_chunks;
+    pl.seg_chunks = (n_chunks + n_seg - 1) / n_seg;
+    pl.n_seg = (n_chunks + pl.seg_chunks - 1) / pl.seg_chunks;
+    return pl;
+}
+
 bool dk_ok(int dk) { return dk == 64 || dk == 128; }
 bool dv_ok(int dv) { return dv == 64 || dv == 128 || dv == 256; }
 
@@ -152,21 +176,8 @@ int gla_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *l
     if (st != GLA_OK) return st;
 
     const int BH = B * H;
-    const int dvt = op.dv_tile ? op.dv_tile : (dv >= 128 ? 128 : 64);
-    const int n_chunks = (T + 127) / 128;
-    // Sequence segments: enough (batch, head, tile, segment) units to fill the
-    // SMs once, each segment long enough (>= 8 chunks) to amortise its
-    // correction window.
-    int n_seg = op.segments;
-    if (n_seg == 0) {
-        const int units = BH * (dv / dvt);
-        n_seg = units > 0 ? dev->sm_count / units : 1;
-        n_seg = n_seg < n_chunks / 8 ? n_seg : n_chunks / 8;
-        if (n_seg < 1) n_seg = 1;
-    }
-    if (n_seg > n_chunks) n_seg = n_chunks;
-    const int seg_chunks = (n_chunks + n_seg - 1) / n_seg;
-    n_seg = (n_chunks + seg_chunks - 1) / seg_chunks;
+    const Plan pl = make_plan(B, H, T, dv, op, dev->sm_count);
+    const int dvt = pl.dv_tile, n_seg = pl.n_seg, seg_chunks = pl.seg_chunks;
 
     ChunkLaunch p;
     if (!make_map(enc, &p.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dk, T, BH, 64, 128,
@@ -211,6 +222,31 @@ int gla_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *l
     const int err = launch_chunk_fwd(p, stream);
     if (ws) cudaFreeAsync(ws, stream);
     return err == 0 ? GLA_OK : GLA_ERR_LAUNCH;
+}
+
+int gla_chunk_fwd_plan(int B, int H, int T, int dk, int dv, const gla_chunk_options *opts,
+                       int *n_segments, int *dv_tile, int *launches, unsigned long *scratch_bytes) {
+    using namespace gla;
+    if (B <= 0 || H <= 0 || T <= 0) return GLA_ERR_ARG;
+    if (static_cast<long long>(B) * H > 0x7fffffffLL) return GLA_ERR_ARG;
+    if (!dk_ok(dk) || !dv_ok(dv)) return GLA_ERR_SHAPE;
+    gla_chunk_options o_def = {};
+    const gla_chunk_options &op = opts ? *opts : o_def;
+    if ((op.dv_tile != 0 && op.dv_tile != 64 && op.dv_tile != 128) || op.dv_tile > dv ||
+        op.segments < 0)
+        return GLA_ERR_ARG;
+    DeviceInfo *dev = nullptr;
+    const int st = current_device(&dev);
+    if (st != GLA_OK) return st;
+    const Plan pl = make_plan(B, H, T, dv, op, dev->sm_count);
+    if (n_segments) *n_segments = pl.n_seg;
+    if (dv_tile) *dv_tile = pl.dv_tile;
+    if (launches) *launches = pl.n_seg > 1 ? 2 : 1;
+    if (scratch_bytes)
+        *scratch_bytes = pl.n_seg > 1 ? static_cast<size_t>(pl.n_seg) * B * H * dk * (dv + 1) *
+                                            sizeof(float)
+                                      : 0;
+    return GLA_OK;
 }
 
 int gla_chunk_fwd(const void *q, const void *k, const void *v, const float *log_alpha,

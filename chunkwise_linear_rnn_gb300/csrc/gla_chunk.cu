@@ -29,16 +29,16 @@
 // score block P (the A operand of P V, kept in TMEM).
 //
 // CTA organisation (one CTA per (batch, head, value-column tile, sequence
-// segment); 320 threads):
-//   warp 9 "tma": streams each chunk's A (fp32), Q, K (bf16, 128-byte swizzle,
+// segment); 448 threads):
+//   warp 13 "tma": streams each chunk's A (fp32), Q, K (bf16, 128-byte swizzle,
 //     already in the K-major operand layout) and V (MN-major) tiles with TMA,
 //     each as soon as the tile it replaces has been consumed.
-//   warps 0-3 "prep": run the fp32 prefix sum of A (two channels x 64 tokens
-//     per thread, 8-byte shared-memory vectors), rescale Q and K in place to Qh
+//   warps 0-7 "prep": run the fp32 prefix sum of A (two channels x 32 tokens
+//     per thread for dk = 128, 8-byte shared-memory vectors), rescale Q and K in place to Qh
 //     and Kh_hi, write Kh_lo, and decide the item sequence (one block, or
 //     rescaled sub-chunks) and the correction window of each chunk.
-//   warp 8 "mma": one thread issues every tcgen05.mma and commit.
-//   warps 4-7 "tmem": thread i owns TMEM lane i — causal mask and hi/lo split
+//   warp 12 "mma": one thread issues every tcgen05.mma and commit.
+//   warps 8-11 "tmem": thread i owns TMEM lane i — causal mask and hi/lo split
 //     of P, the per-row state scale and its bf16 copy for the next chunk's
 //     Qh S product, and the output epilogue.
 // The O accumulator is double-buffered so the next chunk's products overlap
@@ -67,9 +67,12 @@ namespace gla {
 namespace {
 
 constexpr int kChunk = 128;
-constexpr int kThreads = 320;           // 10 warps
-constexpr int kMmaWarp = 8;
-constexpr int kTmaWarp = 9;
+constexpr int kPrepWarps = 8;           // warps 0-7
+constexpr int kPrepThreads = 32 * kPrepWarps;
+constexpr int kTmemWarp0 = 8;           // warps 8-11
+constexpr int kMmaWarp = 12;
+constexpr int kTmaWarp = 13;
+constexpr int kThreads = 448;           // 14 warps
 constexpr float kExpBound = 30.f;
 constexpr float kWindowCut = 41.58883083f;  // 60 ln 2
 constexpr uint32_t kBlk = kChunk * 128;     // one 64-column block of a 128-row tile
@@ -94,7 +97,7 @@ enum Bar {
     kBarQkRaw, kBarReq, kNumBars
 };
 // arrival counts, in enum order
-__device__ constexpr uint32_t kBarCounts[kNumBars] = {4, 1, 1, 1, 4, 1, 4, 1, 1, 4, 4, 1, 1, 1, 1, 1};
+__device__ constexpr uint32_t kBarCounts[kNumBars] = {kPrepWarps, 1, 1, 1, 4, 1, 4, 1, 1, 4, 4, 1, 1, 1, 1, 1};
 
 template <int DK, int DVT>
 struct Smem {
@@ -163,12 +166,13 @@ __device__ __forceinline__ float2 unpack_bf16x2(uint32_t w) {
     return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
-// Split (x, y) into bf16 hi pair and bf16 lo pair.
+// Split (x, y) into a bf16 hi pair and a bf16 lo pair, x = hi + lo to 16
+// significant bits.  Two packed conversions; the hi halves are widened back
+// to fp32 by bit shifts.
 __device__ __forceinline__ void split_pair(float x, float y, uint32_t &hi, uint32_t &lo) {
-    const __nv_bfloat16 hx = __float2bfloat16_rn(x), hy = __float2bfloat16_rn(y);
-    hi = static_cast<uint32_t>(__bfloat16_as_ushort(hx)) |
-         (static_cast<uint32_t>(__bfloat16_as_ushort(hy)) << 16);
-    lo = pack_bf16x2(x - __bfloat162float(hx), y - __bfloat162float(hy));
+    hi = pack_bf16x2(x, y);
+    const float2 h = unpack_bf16x2(hi);
+    lo = pack_bf16x2(x - h.x, y - h.y);
 }
 
 __device__ __forceinline__ float clamp_gate(float a) {
@@ -225,11 +229,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp < 4) {
+    if (warp < kPrepWarps) {
         // =========================================================== prep warps
-        constexpr int NP = DK / 2;          // channel pairs
-        constexpr int NQ = kChunk / NP;     // token parts
-        constexpr int TP = kChunk / NQ;     // tokens per part
+        constexpr int NP = DK / 2;              // channel pairs
+        constexpr int NQ = kPrepThreads / NP;   // token parts
+        constexpr int TP = kChunk / NQ;         // tokens per part
+        static_assert(TP % 8 == 0, "token parts must hold whole batches");
         const int pt = tid;
         const int pr = pt % NP, part = pt / NP;
         const int ch = 2 * pr;
@@ -249,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             // The reduction doubles as the barrier after which the previous
             // chunk's A tile is free.
             const bool win = !closed && last_part && (gseg0 > -kWindowCut || gseg1 > -kWindowCut);
-            const bool any_win = bar_or(1, 128, win);
+            const bool any_win = bar_or(1, kPrepThreads, win);
             if (!closed && !any_win) closed = true;
             const bool end = c >= c_end || !ok || (p.mode == kModeCorrect && closed);
             if (pt == 0) {
@@ -261,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             const bool store = p.mode == kModeCorrect || closed;
             bool okw = mbar_wait_bounded(&bars[kBarAFull], lc & 1, p.status);
             okw = okw && mbar_wait_bounded(&bars[kBarQkRaw], lc & 1, p.status);
-            ok = !bar_or(4, 128, !okw);   // one verdict for all prep threads
+            ok = !bar_or(4, kPrepThreads, !okw);   // one verdict for all prep threads
             if (!ok) break;
             // ---- prefix over the earlier parts of this chunk
             float g0 = 0.f, g1 = 0.f;
@@ -271,28 +276,58 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                 g0 += a.x;
                 g1 += a.y;
             }
-            // ---- fast attempt: one block, reference = chunk start, in place
+            // ---- fast attempt: one block, reference = chunk start, in place.
+            // Batches of kB tokens; the next batch's shared-memory loads are
+            // issued before this batch's in-place stores.
+            constexpr int kB = 8;
             float mn = 0.f, mx = 0.f;
-#pragma unroll 8
-            for (int ii = 0; ii < TP; ++ii) {
-                const int i = part * TP + ii;
-                const float2 a = *reinterpret_cast<const float2 *>(sAc + i * DK);
+            float2 ab8[kB];
+            uint32_t qw8[kB], kw8[kB];
+#pragma unroll
+            for (int e = 0; e < kB; ++e) {
+                const int i = part * TP + e;
                 const uint32_t off = sw128_offset(i, ch, kBlk);
-                const uint32_t qw = *reinterpret_cast<const uint32_t *>(sQ + off);
-                const uint32_t kw = *reinterpret_cast<const uint32_t *>(sK + off);
-                g0 += a.x;
-                g1 += a.y;
-                mn = fminf(mn, fminf(g0, g1));
-                mx = fmaxf(mx, fmaxf(g0, g1));
-                const float2 qf = unpack_bf16x2(qw), kf = unpack_bf16x2(kw);
-                *reinterpret_cast<uint32_t *>(sQ + off) =
-                    bf16x2_bits(qf.x * __expf(g0), qf.y * __expf(g1));
-                uint32_t hi, lo;
-                split_pair(kf.x * __expf(-g0), kf.y * __expf(-g1), hi, lo);
-                *reinterpret_cast<uint32_t *>(sK + off) = hi;
-                *reinterpret_cast<uint32_t *>(sKlo + off) = lo;
+                ab8[e] = *reinterpret_cast<const float2 *>(sAc + i * DK);
+                qw8[e] = *reinterpret_cast<const uint32_t *>(sQ + off);
+                kw8[e] = *reinterpret_cast<const uint32_t *>(sK + off);
             }
-            const bool bad = bar_or(2, 128, fmaxf(-mn, mx) > kExpBound || p.force_sub != 0);
+            for (int i0 = part * TP; i0 < (part + 1) * TP; i0 += kB) {
+                float2 ca[kB];
+                uint32_t cq[kB], ck[kB];
+#pragma unroll
+                for (int e = 0; e < kB; ++e) {
+                    ca[e] = ab8[e];
+                    cq[e] = qw8[e];
+                    ck[e] = kw8[e];
+                }
+                if (i0 + kB < (part + 1) * TP) {
+#pragma unroll
+                    for (int e = 0; e < kB; ++e) {
+                        const int i = i0 + kB + e;
+                        const uint32_t off = sw128_offset(i, ch, kBlk);
+                        ab8[e] = *reinterpret_cast<const float2 *>(sAc + i * DK);
+                        qw8[e] = *reinterpret_cast<const uint32_t *>(sQ + off);
+                        kw8[e] = *reinterpret_cast<const uint32_t *>(sK + off);
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < kB; ++e) {
+                    const int i = i0 + e;
+                    g0 += ca[e].x;
+                    g1 += ca[e].y;
+                    mn = fminf(mn, fminf(g0, g1));
+                    mx = fmaxf(mx, fmaxf(g0, g1));
+                    const float2 qf = unpack_bf16x2(cq[e]), kf = unpack_bf16x2(ck[e]);
+                    const uint32_t off = sw128_offset(i, ch, kBlk);
+                    *reinterpret_cast<uint32_t *>(sQ + off) =
+                        bf16x2_bits(qf.x * __expf(g0), qf.y * __expf(g1));
+                    uint32_t hi, lo;
+                    split_pair(kf.x * __expf(-g0), kf.y * __expf(-g1), hi, lo);
+                    *reinterpret_cast<uint32_t *>(sK + off) = hi;
+                    *reinterpret_cast<uint32_t *>(sKlo + off) = lo;
+                }
+            }
+            const bool bad = bar_or(2, kPrepThreads, fmaxf(-mn, mx) > kExpBound || p.force_sub != 0);
             if (!bad) {
                 if (last_part) {
                     sG[(n & 1) * DK + ch] = __expf(g0);
@@ -347,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                     c1 += clamp_gate(a.y);
                     viol |= fabsf(c0 - r0) > kExpBound || fabsf(c1 - r1) > kExpBound;
                 }
-                if (!bar_or(3, 128, viol)) break;
+                if (!bar_or(3, kPrepThreads, viol)) break;
             }
             // cs == 1 always satisfies the bound: a single clamped gate is within it.
             const int n_sub = kChunk / cs;
@@ -356,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                 const int sa = sidx * cs, sb = sa + cs;
                 okw = true;
                 if (sidx > 0) okw = mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status);
-                ok = !bar_or(4, 128, !okw);
+                ok = !bar_or(4, kPrepThreads, !okw);
                 if (!ok) break;
                 // reference for block sidx: clamped Gamma just before token sa
                 float c0 = bnd0[part], c1 = bnd1[part];
@@ -523,9 +558,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
         __syncwarp();
     } else {
         // =========================================================== TMEM warps
-        const int i = tid - 128;                  // TMEM lane = row = key channel
-        const uint32_t lane_base = static_cast<uint32_t>((warp - 4) * 32) << 16;
-        const bool has_state_row = ((warp - 4) * 32) < DK;  // warp-uniform
+        const int i = tid - 32 * kTmemWarp0;      // TMEM lane = row = key channel
+        const uint32_t lane_base = static_cast<uint32_t>((warp - kTmemWarp0) * 32) << 16;
+        const bool has_state_row = ((warp - kTmemWarp0) * 32) < DK;  // warp-uniform
         const uint32_t tP = tmem + lane_base + TM::kP;
         const uint32_t tS = tmem + lane_base + TM::kS;
 
@@ -611,20 +646,26 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarPFull], n & 1, p.status))) break;
             tc_fence_after();
 #pragma unroll
-            for (int qd = 0; qd < kChunk / 32; ++qd) {
-                uint32_t r[32];
-                tmem_ld32(tP + 32 * qd, r);
+            for (int qd = 0; qd < kChunk / 32; qd += 2) {
+                uint32_t r0[32], r1[32];
+                tmem_ld32(tP + 32 * qd, r0);
+                tmem_ld32(tP + 32 * (qd + 1), r1);
                 tmem_wait_ld();
-                uint32_t hi[16], lo[16];
 #pragma unroll
-                for (int w = 0; w < 16; ++w) {
-                    const int j = 32 * qd + 2 * w;
-                    const float x0 = (j <= i) ? __uint_as_float(r[2 * w]) : 0.f;
-                    const float x1 = (j + 1 <= i) ? __uint_as_float(r[2 * w + 1]) : 0.f;
-                    split_pair(x0, x1, hi[w], lo[w]);
+                for (int half = 0; half < 2; ++half) {
+                    const uint32_t(&r)[32] = half ? r1 : r0;
+                    const int qq = qd + half;
+                    uint32_t hi[16], lo[16];
+#pragma unroll
+                    for (int w = 0; w < 16; ++w) {
+                        const int j = 32 * qq + 2 * w;
+                        const float x0 = (j <= i) ? __uint_as_float(r[2 * w]) : 0.f;
+                        const float x1 = (j + 1 <= i) ? __uint_as_float(r[2 * w + 1]) : 0.f;
+                        split_pair(x0, x1, hi[w], lo[w]);
+                    }
+                    tmem_st16(tP + 32 * qq, hi);
+                    tmem_st16(tP + 32 * qq + 16, lo);
                 }
-                tmem_st16(tP + 32 * qd, hi);
-                tmem_st16(tP + 32 * qd + 16, lo);
             }
             tmem_wait_st();
             tc_fence_before();

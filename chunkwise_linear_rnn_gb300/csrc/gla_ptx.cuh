@@ -56,15 +56,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return done != 0;
 }
 
+// try_wait that lets the hardware suspend the thread for up to `hint_ns`
+// nanoseconds (or until the phase completes) instead of returning at once.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return done != 0;
+}
+
 // Wait for the phase with the given parity to complete.  Returns false (and
 // raises the timeout bit in *status) if it did not within kWaitLimitNs.
+// Waiting threads sleep in the barrier unit rather than spin, leaving issue
+// slots to the warps that share their scheduler.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
                                                   unsigned int *status) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_timer_ns();
     while (true) {
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
         if (global_timer_ns() - t0 > kWaitLimitNs) {
             atomicOr(status, kStatusTimeout);
             return false;

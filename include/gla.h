@@ -94,6 +94,16 @@ int gla_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *l
                      int dk, int dv, const gla_chunk_options *opts, cudaStream_t stream);
 
 /*
+ * gla_chunk_fwd_plan — the launch plan gla_chunk_fwd_ex would use on the
+ * current device for these sizes and options (no GPU work is enqueued):
+ * the number of sequence segments, the value-column tile, the number of
+ * kernel launches (1, or 2 when segments > 1) and the bytes of stream-ordered
+ * scratch it allocates.  Any output pointer may be NULL.
+ */
+int gla_chunk_fwd_plan(int B, int H, int T, int dk, int dv, const gla_chunk_options *opts,
+                       int *n_segments, int *dv_tile, int *launches, unsigned long *scratch_bytes);
+
+/*
  * gla_recurrent_step — one decode token for B * H independent heads.
  *
  * h (fp32 [B, H, dk, dv]) is read and overwritten in place with
