@@ -187,6 +187,8 @@ int gla_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *l
         !make_map(enc, &p.tm_a, log_alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dk, T, BH, dk, 128,
                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_map(enc, &p.tm_v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dv, T, BH, 64, 128,
+                  CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(enc, &p.tm_o, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dv, T, BH, 64, 128,
                   CU_TENSOR_MAP_SWIZZLE_128B))
         return GLA_ERR_LAUNCH;
     p.q = q;

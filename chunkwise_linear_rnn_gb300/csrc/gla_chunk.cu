@@ -94,10 +94,11 @@ struct ChunkReq {
 enum Bar {
     kBarQkFull = 0, kBarQkEmpty, kBarItem, kBarPFull, kBarPSplit, kBarSDone, kBarSReady,
     kBarOFull0, kBarOFull1, kBarOFree0, kBarOFree1, kBarVFull, kBarVEmpty, kBarAFull,
-    kBarQkRaw, kBarReq, kNumBars
+    kBarQkRaw, kBarReq, kBarStage, kNumBars
 };
 // arrival counts, in enum order
-__device__ constexpr uint32_t kBarCounts[kNumBars] = {kPrepWarps, 1, 1, 1, 4, 1, 4, 1, 1, 4, 4, 1, 1, 1, 1, 1};
+__device__ constexpr uint32_t kBarCounts[kNumBars] = {kPrepWarps, 1, 1, 1, 4, 1, 4, 1, 1, 4, 4,
+                                                      1, 1, 1, 1, 1, 4};
 
 template <int DK, int DVT>
 struct Smem {
@@ -133,7 +134,7 @@ struct Tmem {
 };
 
 struct KParams {
-    CUtensorMap tm_q, tm_k, tm_a, tm_v;
+    CUtensorMap tm_q, tm_k, tm_a, tm_v, tm_o;
     const uint32_t *q;  // bf16 pairs
     const uint32_t *k;
     const float2 *a;
@@ -222,6 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
         prefetch_tensormap(&p.tm_k);
         prefetch_tensormap(&p.tm_a);
         prefetch_tensormap(&p.tm_v);
+        prefetch_tensormap(&p.tm_o);
     }
     if (warp == kMmaWarp) tmem_alloc(tmem_slot, TM::kCols);
     tc_fence_before();
@@ -552,7 +554,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                                 1);
                 }
                 mma_commit(&bars[kBarOFull0 + ob]);
-                if (it.flags & kItemLast) mma_commit(&bars[kBarVEmpty]);
             }
         }
         __syncwarp();
@@ -637,6 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kBarSReady]);   // phase 0: initial state ready
 
+        int n_staged = 0;   // chunks written through the staging tile
         for (int n = 0;; ++n) {
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarItem], n & 1, p.status))) break;
             const ItemInfo it = sItem[n & 1];
@@ -705,16 +707,25 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                 break;
             tc_fence_after();
             {
+                // A whole stored chunk leaves through the V tile (free once its
+                // P V product is done) and one TMA tensor store; rows of
+                // sub-chunk items are stored directly.
                 const uint32_t tO = tmem + lane_base + (ob ? TM::kO1 : TM::kO0);
+                const bool store_item = (it.flags & kItemStore) != 0;
+                const bool staged = store_item && it.r0 == 0 && it.r1 == kChunk;
                 const int t = it.t0 + i;
-                const bool st = (it.flags & kItemStore) && i >= it.r0 && i < it.r1 && t < T;
+                const bool st = store_item && !staged && i >= it.r0 && i < it.r1 && t < T;
                 __nv_bfloat16 *orow = p.o + (static_cast<size_t>(bh) * T + t) * p.dv + dv0;
 #pragma unroll
-                for (int c0 = 0; c0 < DVT; c0 += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(tO + c0, r);
+                for (int c0 = 0; c0 < DVT; c0 += 64) {
+                    uint32_t ra[32], rb[32];
+                    tmem_ld32(tO + c0, ra);
+                    tmem_ld32(tO + c0 + 32, rb);
                     tmem_wait_ld();
-                    if (st) {
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        const uint32_t(&r)[32] = half ? rb : ra;
+                        const int cc = c0 + 32 * half;
 #pragma unroll
                         for (int j = 0; j < 32; j += 8) {
                             uint4 pk;
@@ -722,15 +733,36 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                             pk.y = pack_bf16x2(p.scale * __uint_as_float(r[j + 2]), p.scale * __uint_as_float(r[j + 3]));
                             pk.z = pack_bf16x2(p.scale * __uint_as_float(r[j + 4]), p.scale * __uint_as_float(r[j + 5]));
                             pk.w = pack_bf16x2(p.scale * __uint_as_float(r[j + 6]), p.scale * __uint_as_float(r[j + 7]));
-                            *reinterpret_cast<uint4 *>(orow + c0 + j) = pk;
+                            if (staged)
+                                *reinterpret_cast<uint4 *>(sV + sw128_offset(i, cc + j, kBlk)) = pk;
+                            else if (st)
+                                *reinterpret_cast<uint4 *>(orow + cc + j) = pk;
                         }
                     }
+                }
+                if (staged) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars[kBarStage]);
+                    if (tid == 32 * kTmemWarp0) {
+                        if (mbar_wait_bounded(&bars[kBarStage], n_staged & 1, p.status)) {
+#pragma unroll
+                            for (int nb = 0; nb < DVT / 64; ++nb)
+                                tma_store_3d(&p.tm_o, sV + nb * kBlk, dv0 + nb * 64, it.t0, bh);
+                            tma_store_commit();
+                            tma_store_wait_read_all();
+                        }
+                    }
+                    ++n_staged;
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[kBarOFree0 + ob]);
+            // the chunk's V tile may be refilled once its last item is done
+            if ((it.flags & kItemLast) && tid == 32 * kTmemWarp0) mbar_arrive(&bars[kBarVEmpty]);
         }
+        if (tid == 32 * kTmemWarp0) tma_store_wait_all();
         // ---- final state of a FULL pass
         if (p.mode == kModeFull && has_state_row) {
             float *dst = nullptr;
@@ -780,6 +812,7 @@ int launch_tiles(const ChunkLaunch &c, cudaStream_t stream) {
     p.tm_k = c.tm_k;
     p.tm_a = c.tm_a;
     p.tm_v = c.tm_v;
+    p.tm_o = c.tm_o;
     p.q = static_cast<const uint32_t *>(c.q);
     p.k = static_cast<const uint32_t *>(c.k);
     p.a = reinterpret_cast<const float2 *>(c.log_alpha);

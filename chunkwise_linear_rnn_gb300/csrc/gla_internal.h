@@ -8,8 +8,8 @@
 namespace gla {
 
 struct ChunkLaunch {
-    // 3-D tensor maps (channel, token, batch*head): q, k, log_alpha, v
-    CUtensorMap tm_q, tm_k, tm_a, tm_v;
+    // 3-D tensor maps (channel, token, batch*head): q, k, log_alpha, v, o
+    CUtensorMap tm_q, tm_k, tm_a, tm_v, tm_o;
     const void *q, *k;        // bf16 [BH, T, dk]
     const float *log_alpha;   // fp32 [BH, T, dk]
     const float *h0;          // [BH, dk, dv] or null (zero state)
