@@ -33,10 +33,12 @@
 //   warp 13 "tma": streams each chunk's A (fp32), Q, K (bf16, 128-byte swizzle,
 //     already in the K-major operand layout) and V (MN-major) tiles with TMA,
 //     each as soon as the tile it replaces has been consumed.
-//   warps 0-7 "prep": run the fp32 prefix sum of A (two channels x 32 tokens
-//     per thread for dk = 128, 8-byte shared-memory vectors), rescale Q and K in place to Qh
-//     and Kh_hi, write Kh_lo, and decide the item sequence (one block, or
-//     rescaled sub-chunks) and the correction window of each chunk.
+//   warps 0-7 "prep": two channels x 32 tokens per thread (dk = 128).  As
+//     soon as the A tile lands (before Q and K): the fp32 prefix sum per token
+//     part, written in place of A, the exponent-bound check that picks one
+//     block or rescaled sub-chunks, and the state factor and correction-window
+//     bookkeeping.  When Q and K land: Gamma = part offset + local sum, and the
+//     elementwise in-place rescale to Qh and Kh_hi plus Kh_lo.
 //   warp 12 "mma": one thread issues every tcgen05.mma and commit.
 //   warps 8-11 "tmem": thread i owns TMEM lane i — causal mask and hi/lo split
 //     of P, the per-row state scale and its bf16 copy for the next chunk's
@@ -266,76 +268,107 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             if (end) break;
             const int t0 = c * kChunk;
             const bool store = p.mode == kModeCorrect || closed;
+            // ---- phase A (needs only the A tile, which arrives early): the
+            // local prefix sum of this thread's part, written in place of A.
+            constexpr int kB = 8;
             bool okw = mbar_wait_bounded(&bars[kBarAFull], lc & 1, p.status);
-            okw = okw && mbar_wait_bounded(&bars[kBarQkRaw], lc & 1, p.status);
             ok = !bar_or(4, kPrepThreads, !okw);   // one verdict for all prep threads
             if (!ok) break;
-            // ---- prefix over the earlier parts of this chunk
-            float g0 = 0.f, g1 = 0.f;
-#pragma unroll 8
-            for (int i = 0; i < part * TP; ++i) {
-                const float2 a = *reinterpret_cast<const float2 *>(sAc + i * DK);
-                g0 += a.x;
-                g1 += a.y;
-            }
-            // ---- fast attempt: one block, reference = chunk start, in place.
-            // Batches of kB tokens; the next batch's shared-memory loads are
-            // issued before this batch's in-place stores.
-            constexpr int kB = 8;
-            float mn = 0.f, mx = 0.f;
-            float2 ab8[kB];
-            uint32_t qw8[kB], kw8[kB];
+            float c0 = 0.f, c1 = 0.f;
+            float lmn = 3.0e38f, lmx = -3.0e38f;
+            {
+                float2 nx[kB];
 #pragma unroll
-            for (int e = 0; e < kB; ++e) {
-                const int i = part * TP + e;
-                const uint32_t off = sw128_offset(i, ch, kBlk);
-                ab8[e] = *reinterpret_cast<const float2 *>(sAc + i * DK);
-                qw8[e] = *reinterpret_cast<const uint32_t *>(sQ + off);
-                kw8[e] = *reinterpret_cast<const uint32_t *>(sK + off);
-            }
-            for (int i0 = part * TP; i0 < (part + 1) * TP; i0 += kB) {
-                float2 ca[kB];
-                uint32_t cq[kB], ck[kB];
+                for (int e = 0; e < kB; ++e)
+                    nx[e] = *reinterpret_cast<const float2 *>(sAc + (part * TP + e) * DK);
+                for (int i0 = part * TP; i0 < (part + 1) * TP; i0 += kB) {
+                    float2 cur[kB];
 #pragma unroll
-                for (int e = 0; e < kB; ++e) {
-                    ca[e] = ab8[e];
-                    cq[e] = qw8[e];
-                    ck[e] = kw8[e];
-                }
-                if (i0 + kB < (part + 1) * TP) {
+                    for (int e = 0; e < kB; ++e) cur[e] = nx[e];
+                    if (i0 + kB < (part + 1) * TP) {
+#pragma unroll
+                        for (int e = 0; e < kB; ++e)
+                            nx[e] = *reinterpret_cast<const float2 *>(sAc + (i0 + kB + e) * DK);
+                    }
 #pragma unroll
                     for (int e = 0; e < kB; ++e) {
-                        const int i = i0 + kB + e;
-                        const uint32_t off = sw128_offset(i, ch, kBlk);
-                        ab8[e] = *reinterpret_cast<const float2 *>(sAc + i * DK);
-                        qw8[e] = *reinterpret_cast<const uint32_t *>(sQ + off);
-                        kw8[e] = *reinterpret_cast<const uint32_t *>(sK + off);
+                        c0 += cur[e].x;
+                        c1 += cur[e].y;
+                        lmn = fminf(lmn, fminf(c0, c1));
+                        lmx = fmaxf(lmx, fmaxf(c0, c1));
+                        *reinterpret_cast<float2 *>(const_cast<float *>(sAc) + (i0 + e) * DK) =
+                            make_float2(c0, c1);
                     }
                 }
+            }
+            named_barrier(5, kPrepThreads);
+            // offset of this part: the totals of the parts before it
+            float o0 = 0.f, o1 = 0.f;
+            for (int qq = 0; qq < part; ++qq) {
+                const float2 tt = *reinterpret_cast<const float2 *>(sAc + (qq * TP + TP - 1) * DK);
+                o0 += tt.x;
+                o1 += tt.y;
+            }
+            // Gamma_i = o + local_i; the fast path needs every |Gamma_i| <= kExpBound
+            const float gmin = fminf(o0, o1) + lmn, gmax = fmaxf(o0, o1) + lmx;
+            const bool bad = bar_or(2, kPrepThreads,
+                                    fmaxf(-fminf(gmin, 0.f), fmaxf(gmax, 0.f)) > kExpBound ||
+                                        p.force_sub != 0);
+            okw = mbar_wait_bounded(&bars[kBarQkRaw], lc & 1, p.status);
+            ok = !bar_or(4, kPrepThreads, !okw);
+            if (!ok) break;
+            if (!bad) {
+                // ---- phase B (needs Q, K): Qh, Kh_hi in place, Kh_lo.  Purely
+                // elementwise; the next batch's loads precede this batch's stores.
+                if (last_part) {
+                    const float gc0 = o0 + c0, gc1 = o1 + c1;   // Gamma at the chunk end
+                    sG[(n & 1) * DK + ch] = __expf(gc0);
+                    sG[(n & 1) * DK + ch + 1] = __expf(gc1);
+                    gseg0 += gc0;
+                    gseg1 += gc1;
+                }
+                float2 ab8[kB];
+                uint32_t qw8[kB], kw8[kB];
 #pragma unroll
                 for (int e = 0; e < kB; ++e) {
-                    const int i = i0 + e;
-                    g0 += ca[e].x;
-                    g1 += ca[e].y;
-                    mn = fminf(mn, fminf(g0, g1));
-                    mx = fmaxf(mx, fmaxf(g0, g1));
-                    const float2 qf = unpack_bf16x2(cq[e]), kf = unpack_bf16x2(ck[e]);
+                    const int i = part * TP + e;
                     const uint32_t off = sw128_offset(i, ch, kBlk);
-                    *reinterpret_cast<uint32_t *>(sQ + off) =
-                        bf16x2_bits(qf.x * __expf(g0), qf.y * __expf(g1));
-                    uint32_t hi, lo;
-                    split_pair(kf.x * __expf(-g0), kf.y * __expf(-g1), hi, lo);
-                    *reinterpret_cast<uint32_t *>(sK + off) = hi;
-                    *reinterpret_cast<uint32_t *>(sKlo + off) = lo;
+                    ab8[e] = *reinterpret_cast<const float2 *>(sAc + i * DK);
+                    qw8[e] = *reinterpret_cast<const uint32_t *>(sQ + off);
+                    kw8[e] = *reinterpret_cast<const uint32_t *>(sK + off);
                 }
-            }
-            const bool bad = bar_or(2, kPrepThreads, fmaxf(-mn, mx) > kExpBound || p.force_sub != 0);
-            if (!bad) {
-                if (last_part) {
-                    sG[(n & 1) * DK + ch] = __expf(g0);
-                    sG[(n & 1) * DK + ch + 1] = __expf(g1);
-                    gseg0 += g0;
-                    gseg1 += g1;
+                for (int i0 = part * TP; i0 < (part + 1) * TP; i0 += kB) {
+                    float2 ca[kB];
+                    uint32_t cq[kB], ck[kB];
+#pragma unroll
+                    for (int e = 0; e < kB; ++e) {
+                        ca[e] = ab8[e];
+                        cq[e] = qw8[e];
+                        ck[e] = kw8[e];
+                    }
+                    if (i0 + kB < (part + 1) * TP) {
+#pragma unroll
+                        for (int e = 0; e < kB; ++e) {
+                            const int i = i0 + kB + e;
+                            const uint32_t off = sw128_offset(i, ch, kBlk);
+                            ab8[e] = *reinterpret_cast<const float2 *>(sAc + i * DK);
+                            qw8[e] = *reinterpret_cast<const uint32_t *>(sQ + off);
+                            kw8[e] = *reinterpret_cast<const uint32_t *>(sK + off);
+                        }
+                    }
+#pragma unroll
+                    for (int e = 0; e < kB; ++e) {
+                        const int i = i0 + e;
+                        const float g0 = o0 + ca[e].x, g1 = o1 + ca[e].y;
+                        const float2 qf = unpack_bf16x2(cq[e]), kf = unpack_bf16x2(ck[e]);
+                        const uint32_t off = sw128_offset(i, ch, kBlk);
+                        *reinterpret_cast<uint32_t *>(sQ + off) =
+                            bf16x2_bits(qf.x * __expf(g0), qf.y * __expf(g1));
+                        uint32_t hi, lo;
+                        split_pair(kf.x * __expf(-g0), kf.y * __expf(-g1), hi, lo);
+                        *reinterpret_cast<uint32_t *>(sK + off) = hi;
+                        *reinterpret_cast<uint32_t *>(sKlo + off) = lo;
+                    }
                 }
                 if (pt == 0) {
                     sItem[n & 1] = ItemInfo{t0, 0, kChunk, kItemLast | (store ? kItemStore : 0), lc,
@@ -349,8 +382,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             }
             // ---- sub-chunk rescaling: the largest power-of-two block length cs
             // whose every block keeps |Gamma - r_block| <= kExpBound (clamped
-            // gates).  Q and K are re-read from global memory: the tiles hold
-            // the fast attempt.
+            // gates).  Gates, Q and K are re-read from global memory: the tiles
+            // hold prefix sums and the raw inputs.
+            const float2 *ab = p.a + (row0 * DK + ch) / 2;
+            auto raw_gate = [&](int i) {
+                const int t = t0 + i;
+                return t < T ? ab[static_cast<size_t>(t) * kStride] : make_float2(0.f, 0.f);
+            };
             float bnd0[NQ], bnd1[NQ];  // clamped Gamma just before each part start
             {
                 float c0 = 0.f, c1 = 0.f;
@@ -358,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                 bnd1[0] = 0.f;
                 for (int qq = 1; qq < NQ; ++qq) {
                     for (int i = (qq - 1) * TP; i < qq * TP; ++i) {
-                        const float2 a = *reinterpret_cast<const float2 *>(sAc + i * DK);
+                        const float2 a = raw_gate(i);
                         c0 += clamp_gate(a.x);
                         c1 += clamp_gate(a.y);
                     }
@@ -379,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                         r0 = c0;
                         r1 = c1;
                     }
-                    const float2 a = *reinterpret_cast<const float2 *>(sAc + i * DK);
+                    const float2 a = raw_gate(i);
                     c0 += clamp_gate(a.x);
                     c1 += clamp_gate(a.y);
                     viol |= fabsf(c0 - r0) > kExpBound || fabsf(c1 - r1) > kExpBound;
@@ -409,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                         r1 = c1;
                     }
                     const int t = t0 + i;
-                    const float2 a = *reinterpret_cast<const float2 *>(sAc + i * DK);
+                    const float2 a = raw_gate(i);
                     c0 += clamp_gate(a.x);
                     c1 += clamp_gate(a.y);
                     const uint32_t off = sw128_offset(i, ch, kBlk);
