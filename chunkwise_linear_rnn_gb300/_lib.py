@@ -21,9 +21,10 @@ GLA_ERR_DEVICE = 3
 GLA_ERR_LAUNCH = 4
 GLA_ERR_TIMEOUT = 5
 GLA_ERR_ALLOC = 6
+GLA_ERR_SCRATCH = 7
 
-EXPORTED = ("gla_chunk_fwd", "gla_chunk_fwd_ex", "gla_chunk_fwd_plan", "gla_recurrent_step",
-            "gla_status_string", "gla_last_device_status", "gla_version")
+EXPORTED = ("gla_chunk_fwd", "gla_chunk_fwd_ex", "gla_chunk_fwd_plan", "gla_chunk_fwd_noalloc",
+            "gla_recurrent_step", "gla_status_string", "gla_last_device_status", "gla_version")
 
 
 class GlaChunkOptions(ctypes.Structure):
@@ -48,6 +49,9 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.gla_chunk_fwd_ex.argtypes = [vp, vp, vp, fp, f, fp, vp, fp, i, i, i, i, i,
                                      ctypes.POINTER(GlaChunkOptions), vp]
     lib.gla_chunk_fwd_ex.restype = i
+    lib.gla_chunk_fwd_noalloc.argtypes = [vp, vp, vp, fp, f, fp, vp, fp, i, i, i, i, i,
+                                          ctypes.POINTER(GlaChunkOptions), vp]
+    lib.gla_chunk_fwd_noalloc.restype = i
     ip = ctypes.POINTER(ctypes.c_int)
     lib.gla_chunk_fwd_plan.argtypes = [i, i, i, i, i, ctypes.POINTER(GlaChunkOptions), ip, ip, ip,
                                        ctypes.POINTER(ctypes.c_ulong)]

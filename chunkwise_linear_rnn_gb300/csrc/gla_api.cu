@@ -132,6 +132,78 @@ bool dk_ok(int dk) { return dk == 64 || dk == 128; }
 bool dv_ok(int dv) { return dv == 64 || dv == 128 || dv == 256; }
 
 }  // namespace
+
+int chunk_fwd_with_scratch(const void *q, const void *k, const void *v, const float *log_alpha,
+                           float scale, const float *h0, void *o, float *hT, int B, int H, int T,
+                           int dk, int dv, const gla_chunk_options *opts, cudaStream_t stream,
+                           void *scratch, size_t scratch_bytes) {
+    if (!q || !k || !v || !log_alpha || !o) return GLA_ERR_ARG;
+    if (B <= 0 || H <= 0 || T <= 0) return GLA_ERR_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_alpha) ||
+        !aligned16(o) || (h0 && !aligned16(h0)) || (hT && !aligned16(hT)))
+        return GLA_ERR_ARG;
+    if (!dk_ok(dk) || !dv_ok(dv)) return GLA_ERR_SHAPE;
+    gla_chunk_options o_def = {};
+    const gla_chunk_options &op = opts ? *opts : o_def;
+    if ((op.dv_tile != 0 && op.dv_tile != 64 && op.dv_tile != 128) || op.dv_tile > dv ||
+        op.segments < 0)
+        return GLA_ERR_ARG;
+    if (static_cast<long long>(B) * H > 0x7fffffffLL) return GLA_ERR_ARG;
+    if (scratch && !aligned16(scratch)) return GLA_ERR_ARG;
+
+    DeviceInfo *dev = nullptr;
+    int st = current_device(&dev);
+    if (st != GLA_OK) return st;
+    EncodeTiledFn enc = nullptr;
+    st = encode_fn(&enc);
+    if (st != GLA_OK) return st;
+
+    const int BH = B * H;
+    const Plan pl = make_plan(B, H, T, dv, op, dev->sm_count);
+    const size_t state_bytes =
+        pl.n_seg > 1 ? static_cast<size_t>(pl.n_seg) * BH * dk * dv * sizeof(float) : 0;
+    const size_t decay_bytes =
+        pl.n_seg > 1 ? static_cast<size_t>(pl.n_seg) * BH * dk * sizeof(float) : 0;
+    if (state_bytes + decay_bytes > (scratch ? scratch_bytes : 0)) return GLA_ERR_SCRATCH;
+
+    ChunkLaunch p;
+    if (!make_map(enc, &p.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dk, T, BH, 64, 128,
+                  CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(enc, &p.tm_k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dk, T, BH, 64, 128,
+                  CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(enc, &p.tm_a, log_alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dk, T, BH, dk, 128,
+                  CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(enc, &p.tm_v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dv, T, BH, 64, 128,
+                  CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(enc, &p.tm_o, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dv, T, BH, 64, 128,
+                  CU_TENSOR_MAP_SWIZZLE_128B))
+        return GLA_ERR_LAUNCH;
+    p.q = q;
+    p.k = k;
+    p.log_alpha = log_alpha;
+    p.h0 = h0;
+    p.hT = hT;
+    p.o = o;
+    // Every scratch entry a launch reads is written earlier in the same call,
+    // so nothing in it needs to start at zero.
+    p.ws_state = pl.n_seg > 1 ? static_cast<float *>(scratch) : nullptr;
+    p.ws_decay = pl.n_seg > 1
+                     ? reinterpret_cast<float *>(static_cast<char *>(scratch) + state_bytes)
+                     : nullptr;
+    p.scale = scale;
+    p.B = B;
+    p.H = H;
+    p.T = T;
+    p.dk = dk;
+    p.dv = dv;
+    p.dv_tile = pl.dv_tile;
+    p.n_seg = pl.n_seg;
+    p.seg_chunks = pl.seg_chunks;
+    p.force_exact = op.force_exact ? 1 : 0;
+    p.status = dev->status;
+    return launch_chunk_fwd(p, stream) == 0 ? GLA_OK : GLA_ERR_LAUNCH;
+}
+
 }  // namespace gla
 
 extern "C" {
@@ -147,6 +219,7 @@ const char *gla_status_string(int status) {
         case GLA_ERR_LAUNCH: return "a CUDA call failed while enqueuing work";
         case GLA_ERR_TIMEOUT: return "a bounded device-side wait expired";
         case GLA_ERR_ALLOC: return "stream-ordered scratch allocation failed";
+        case GLA_ERR_SCRATCH: return "the launch plan needs more scratch than the fixed no-allocation scratch holds";
         default: return "unknown status";
     }
 }

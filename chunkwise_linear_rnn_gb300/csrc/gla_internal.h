@@ -5,6 +5,10 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cstddef>
+
+#include "gla.h"
+
 namespace gla {
 
 struct ChunkLaunch {
@@ -27,6 +31,15 @@ struct ChunkLaunch {
 
 // Returns a cudaError_t value (0 on success).
 int launch_chunk_fwd(const ChunkLaunch &p, cudaStream_t stream);
+
+// gla_chunk_fwd_ex with the segment scratch supplied by the caller instead of
+// allocated (`scratch_bytes` bytes of device memory, 16-byte aligned; may be
+// null when the plan needs none).  Returns a GLA status; GLA_ERR_SCRATCH when
+// the launch plan needs more scratch than given.
+int chunk_fwd_with_scratch(const void *q, const void *k, const void *v, const float *log_alpha,
+                           float scale, const float *h0, void *o, float *hT, int B, int H, int T,
+                           int dk, int dv, const gla_chunk_options *opts, cudaStream_t stream,
+                           void *scratch, size_t scratch_bytes);
 
 struct DecodeLaunch {
     const void *q, *k, *v;

@@ -57,7 +57,8 @@ enum gla_status {
     GLA_ERR_DEVICE = 3,      /* no CUDA device, or the device is not sm_103            */
     GLA_ERR_LAUNCH = 4,      /* a CUDA call failed while enqueuing the work            */
     GLA_ERR_TIMEOUT = 5,     /* a bounded device-side wait expired (from the status word) */
-    GLA_ERR_ALLOC = 6        /* stream-ordered scratch allocation failed               */
+    GLA_ERR_ALLOC = 6,       /* stream-ordered scratch allocation failed               */
+    GLA_ERR_SCRATCH = 7      /* plan needs more than gla_chunk_fwd_noalloc's fixed scratch */
 };
 
 /*
@@ -102,6 +103,39 @@ int gla_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *l
  */
 int gla_chunk_fwd_plan(int B, int H, int T, int dk, int dv, const gla_chunk_options *opts,
                        int *n_segments, int *dv_tile, int *launches, unsigned long *scratch_bytes);
+
+/*
+ * gla_chunk_fwd_noalloc — gla_chunk_fwd_ex that allocates no device memory.
+ *
+ * The pages describe no counterpart: this is a service to callers that cannot
+ * let a library allocate, such as serving runtimes that reserve all of HBM up
+ * front and account for every byte themselves, or that run with the
+ * stream-ordered memory pool disabled.  For them the cudaMallocAsync that
+ * gla_chunk_fwd_ex makes when it splits sequences into segments is not an
+ * option.  This entry point computes exactly what gla_chunk_fwd_ex computes,
+ * with the segment scratch taken from one fixed array of
+ * GLA_NOALLOC_SCRATCH_BYTES (16 MiB) that lives in the library and is held
+ * on every GPU that loads it, until the process exits.  The caller still
+ * passes every input and output buffer.
+ *
+ * Limit: when the launch plan (see gla_chunk_fwd_plan) needs more scratch
+ * than the array holds, the call returns GLA_ERR_SCRATCH and enqueues nothing.
+ * Automatic plans on a GB300 need at most about 10 MB; larger needs come
+ * only from an explicit opts->segments.
+ *
+ * Set-up: the first call on each device looks up the array's device address
+ * (with that device current) and caches it; make that first call before any
+ * stream capture begins.
+ *
+ * Sharing: every call uses the same array and leaves the last call's contents
+ * in it.  Calls whose GPU work overlaps (different streams, or several host
+ * threads without ordering between their streams) race on the array; order
+ * such calls on one stream.  Nothing in the array needs to start at zero.
+ */
+#define GLA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+int gla_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const float *log_alpha,
+                          float scale, const float *h0, void *o, float *hT, int B, int H, int T,
+                          int dk, int dv, const gla_chunk_options *opts, cudaStream_t stream);
 
 /*
  * gla_recurrent_step — one decode token for B * H independent heads.

@@ -48,7 +48,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for code in range(0, 7):
+    for code in range(0, 8):
         s = _lib.status_string(code)
         assert s and s != "unknown status"
     assert _lib.status_string(99) == "unknown status"
@@ -80,6 +80,14 @@ def test_chunk_rejects_shapes(lib, dk, dv):
     assert _chunk(lib, dk=dk, dv=dv) == _lib.GLA_ERR_SHAPE
 
 
+def test_noalloc_validates_on_the_host(lib):
+    f = lib.gla_chunk_fwd_noalloc
+    assert f(None, P, P, P, 0.1, None, P, None, 1, 1, 16, 64, 64, None, None) == _lib.GLA_ERR_ARG
+    assert f(P, P, P, P, 0.1, None, P, None, 1, 1, 0, 64, 64, None, None) == _lib.GLA_ERR_ARG
+    assert f(P + 8, P, P, P, 0.1, None, P, None, 1, 1, 16, 64, 64, None, None) == _lib.GLA_ERR_ARG
+    assert f(P, P, P, P, 0.1, None, P, None, 1, 1, 16, 96, 64, None, None) == _lib.GLA_ERR_SHAPE
+
+
 def test_chunk_rejects_misaligned(lib):
     assert _chunk(lib, q=P + 8) == _lib.GLA_ERR_ARG
     assert _chunk(lib, hT=P + 4) == _lib.GLA_ERR_ARG
@@ -107,6 +115,8 @@ def test_valid_arguments_without_gpu_report_device_error(lib):
     assert _chunk(lib) == _lib.GLA_ERR_DEVICE
     assert lib.gla_recurrent_step(P, P, P, P, 1.0, P, P, 1, 1, 64, 64, None) == _lib.GLA_ERR_DEVICE
     assert lib.gla_last_device_status(None) == _lib.GLA_ERR_DEVICE
+    assert lib.gla_chunk_fwd_noalloc(P, P, P, P, 0.125, None, P, None, 1, 1, 16, 64, 64, None,
+                                     None) == _lib.GLA_ERR_DEVICE
 
 
 def test_python_binding_rejects_cpu_tensors():
