@@ -85,11 +85,30 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}",
                                           f"--query-gpu={self.QUERY}", "--format=csv,noheader",
-                                          "-lms", "100"], stdout=self.f,
+                                          "-lms", "20"], stdout=self.f,
                                          stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return self
+        # nvidia-smi takes a moment to start: wait (bounded) for its first line so that
+        # the samples cover the timed region rather than only what follows it.
+        deadline = time.time() + 5.0
+        while time.time() < deadline and self.proc.poll() is None:
+            try:
+                if os.path.getsize(self.path) > 0:
+                    break
+            except OSError:
+                pass
+            time.sleep(0.01)
+        self.first_line = self._count()
         return self
+
+    def _count(self) -> int:
+        try:
+            with open(self.path) as f:
+                return sum(1 for _ in f)
+        except OSError:
+            return 0
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -106,7 +125,11 @@ class ClockSampler:
         sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         try:
-            for line in open(self.path):
+            lines = open(self.path).read().splitlines()
+            # drop the sample(s) written before the timed region started
+            inside = lines[getattr(self, "first_line", 0):]
+            # a region shorter than the sampling period keeps the sample nearest to it
+            for line in (inside or lines[-1:]):
                 parts = [x.strip() for x in line.split(",")]
                 if len(parts) < 9:
                     continue
@@ -131,7 +154,6 @@ def run_ours(args, rank, world, local_rank):
     import __graft_entry__ as ge
     ge.build()
     import chunkwise_linear_rnn_gb300 as gla
-    from synth import CHUNK_CONFIGS, DECODE_CONFIG, make_config_inputs, make_decode_inputs
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -153,7 +175,33 @@ def run_ours(args, rank, world, local_rank):
         return float(t.item())
 
     pk, pk_kind = peaks()
+    cfg = chunk_config(args)
+    line = None
+    if args.only != "decode":
+        line = chunk_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_kind)
+    else:
+        line = {"metric": METRIC, "value": None, "unit": "tokens/s", "n_gpus": world,
+                "steps": 0, "warmup": args.warmup, "note": "chunked forward skipped (--only decode)"}
+    if args.only != "chunk":
+        line["decode"] = decode_leg(args, world, rank, dev, gla, barrier, max_over_ranks, pk)
+    return line
+
+
+def chunk_config(args):
+    """The workload's ChunkConfig, with --batch / --heads overrides (used for small profiles)."""
+    import dataclasses
+    from synth import CHUNK_CONFIGS
     cfg = CHUNK_CONFIGS[args.workload]
+    if args.batch or args.heads:
+        B = args.batch or cfg.B
+        H = args.heads or cfg.H
+        cfg = dataclasses.replace(cfg, B=B, H=H, name=f"B{B}-H{H}-T{cfg.T}-dk{cfg.dk}-dv{cfg.dv}")
+    return cfg
+
+
+def chunk_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_kind):
+    import torch
+    from synth import make_config_inputs
     q, k, v, a, h0 = make_config_inputs(cfg, seed=rank, device=dev)
     o = torch.empty(cfg.B, cfg.H, cfg.T, cfg.dv, dtype=torch.bfloat16, device=dev)
     hT = torch.empty(cfg.B, cfg.H, cfg.dk, cfg.dv, dtype=torch.float32, device=dev)
@@ -234,36 +282,6 @@ def run_ours(args, rank, world, local_rank):
     del q, k, v, a, h0, o, hT
     torch.cuda.empty_cache()
 
-    # ---- decode step (secondary numbers on the same line)
-    decode = None
-    if not args.no_decode:
-        dc = DECODE_CONFIG
-        nsteps = args.decode_steps
-        dh0, dqs, dks, dvs, das = make_decode_inputs(dc.B, dc.H, dc.dk, dc.dv, nsteps,
-                                                     sigma_z=dc.sigma_z, tau=dc.tau,
-                                                     sigma_h0=dc.sigma_h0, seed=rank, device=dev)
-        h = dh0.clone()
-        do = torch.empty(dc.B, dc.H, dc.dv, dtype=torch.bfloat16, device=dev)
-        for s in range(min(3, nsteps)):
-            gla.gla_recurrent_step(dqs[s], dks[s], dvs[s], das[s], h, dc.scale, out=do)
-        barrier()
-        d0 = torch.cuda.Event(enable_timing=True)
-        d1 = torch.cuda.Event(enable_timing=True)
-        d0.record(stream)
-        for s in range(nsteps):
-            gla.gla_recurrent_step(dqs[s], dks[s], dvs[s], das[s], h, dc.scale, out=do)
-        d1.record(stream)
-        barrier()
-        dms = max_over_ranks(d0.elapsed_time(d1)) / nsteps
-        dbytes = decode_bytes(dc)
-        dgbs = dbytes / (dms / 1e3) / 1e9
-        decode = {"workload": dc.name, "steps_per_s": 1e3 / dms, "replicas": world,
-                  "ms_per_step": dms, "hbm_gbs": dgbs, "bytes_per_step": dbytes,
-                  "frac_of_hbm_peak": dgbs / pk["hbm_gbs"], "timed_steps": nsteps,
-                  "gpu_launches": nsteps}
-        del dh0, dqs, dks, dvs, das, h, do
-        torch.cuda.empty_cache()
-
     line = {
         "metric": METRIC,
         "value": value,
@@ -292,40 +310,99 @@ def run_ours(args, rank, world, local_rank):
     }
     if e2e is not None:
         line["e2e"] = e2e
-    if decode is not None:
-        line["decode"] = decode
     return line
+
+
+def decode_leg(args, world, rank, dev, gla, barrier, max_over_ranks, pk):
+    """Decode steps at B=256, H=32, dk=dv=128 (secondary numbers on the same JSON line)."""
+    import torch
+    from synth import DECODE_CONFIG, make_decode_inputs
+    stream = torch.cuda.current_stream(dev)
+    dc = DECODE_CONFIG
+    nsteps = args.decode_steps
+    dh0, dqs, dks, dvs, das = make_decode_inputs(dc.B, dc.H, dc.dk, dc.dv, nsteps,
+                                                 sigma_z=dc.sigma_z, tau=dc.tau,
+                                                 sigma_h0=dc.sigma_h0, seed=rank, device=dev)
+    h = dh0.clone()
+    do = torch.empty(dc.B, dc.H, dc.dv, dtype=torch.bfloat16, device=dev)
+    for s in range(min(3, nsteps)):
+        gla.gla_recurrent_step(dqs[s], dks[s], dvs[s], das[s], h, dc.scale, out=do)
+    barrier()
+    d0 = torch.cuda.Event(enable_timing=True)
+    d1 = torch.cuda.Event(enable_timing=True)
+    d0.record(stream)
+    for s in range(nsteps):
+        gla.gla_recurrent_step(dqs[s], dks[s], dvs[s], das[s], h, dc.scale, out=do)
+    d1.record(stream)
+    barrier()
+    dms = max_over_ranks(d0.elapsed_time(d1)) / nsteps
+    dbytes = decode_bytes(dc)
+    dgbs = dbytes / (dms / 1e3) / 1e9
+    decode = {"workload": dc.name, "steps_per_s": 1e3 / dms, "replicas": world,
+              "ms_per_step": dms, "hbm_gbs": dgbs, "bytes_per_step": dbytes,
+              "frac_of_hbm_peak": dgbs / pk["hbm_gbs"], "timed_steps": nsteps,
+              "gpu_launches": nsteps}
+    del dh0, dqs, dks, dvs, das, h, do
+    torch.cuda.empty_cache()
+    return decode
 
 
 # --------------------------------------------------------------------------- CPU baseline
 
-def oracle_sample(cfg, target_s: float, threads: int):
+class OracleSample:
+    """A bounded sample of the workload for timing the fp64 CPU oracle.
+
+    The sample takes whole heads of the workload (up to all B*H of them) and a
+    prefix of T tokens, sized from a short probe so that one pass costs about
+    target_s seconds of host time; a workload smaller than that is run whole,
+    repeated to fill the time.
+    """
+
+    def __init__(self, cfg, target_s: float, threads: int):
+        from oracle import gla_oracle
+        gla_oracle.build()
+        self.oracle, self.cfg, self.threads = gla_oracle, cfg, threads
+        heads = max(1, min(cfg.B * cfg.H, threads))
+        t_probe = min(cfg.T, 2048)
+        probe = self._inputs(heads, t_probe)
+        self._pass(heads, t_probe, probe)          # first call pays for thread start-up
+        dt = self._pass(heads, t_probe, probe)
+        per_token = dt / (heads * t_probe) * min(heads, threads)   # host-seconds per token
+        budget = target_s * threads / per_token                     # tokens that fill target_s
+        T = int(min(cfg.T, max(t_probe, budget / heads)))
+        if T == cfg.T:
+            heads = int(min(cfg.B * cfg.H, max(heads, budget / T)))
+        self.heads, self.T = heads, T
+        self.repeat = max(1, int(budget / (heads * T))) if (heads == cfg.B * cfg.H and T == cfg.T) else 1
+        self.inputs = self._inputs(heads, T)
+
+    def _inputs(self, heads, T):
+        from synth import make_chunk_inputs
+        c = self.cfg
+        q, k, v, a, h0 = make_chunk_inputs(1, heads, T, c.dk, c.dv, sigma_z=c.sigma_z, tau=c.tau,
+                                           sigma_h0=c.sigma_h0, seed=0)
+        f = lambda t: t.float().numpy()  # noqa: E731
+        return f(q), f(k), f(v), a.numpy(), None if h0 is None else h0.double().numpy()
+
+    def _pass(self, heads, T, inputs=None):
+        q, k, v, a, h0 = inputs if inputs is not None else self._inputs(heads, T)
+        t0 = time.perf_counter()
+        self.oracle.forward(q, k, v, a, self.cfg.scale, h0, nthreads=self.threads)
+        return time.perf_counter() - t0
+
+    def run(self) -> dict:
+        dt = sum(self._pass(self.heads, self.T, self.inputs) for _ in range(self.repeat))
+        tokens = self.repeat * self.heads * self.T
+        c = self.cfg
+        return {"value": tokens / dt, "unit": "tokens/s", "cores": min(self.threads, self.heads),
+                "kind": "oracle",
+                "sample": f"{self.repeat} x {self.heads} heads x {self.T} tokens of {c.name} "
+                          f"(dk={c.dk}, dv={c.dv}), fp64 recurrence, {dt:.1f} s"}
+
+
+def oracle_sample(cfg, target_s: float, threads: int) -> dict:
     """Time the fp64 oracle on a bounded sample of the workload; returns a cpu_baseline dict."""
-    import torch
-    from oracle import gla_oracle
-    from synth import make_chunk_inputs
-    gla_oracle.build()
-    heads = max(1, min(cfg.B * cfg.H, threads))
-    # estimate the per-token rate on a short probe, then size the sample to ~target_s
-    t_probe = 256
-    q, k, v, a, h0 = make_chunk_inputs(1, heads, t_probe, cfg.dk, cfg.dv, sigma_z=cfg.sigma_z,
-                                       tau=cfg.tau, sigma_h0=cfg.sigma_h0, seed=0)
-    c = lambda t: t.float().numpy()  # noqa: E731
-    t0 = time.perf_counter()
-    gla_oracle.forward(c(q), c(k), c(v), a.numpy(), cfg.scale,
-                       None if h0 is None else h0.double().numpy(), nthreads=threads)
-    dt = max(time.perf_counter() - t0, 1e-4)
-    T = int(min(cfg.T, max(t_probe, t_probe * target_s / dt)))
-    q, k, v, a, h0 = make_chunk_inputs(1, heads, T, cfg.dk, cfg.dv, sigma_z=cfg.sigma_z,
-                                       tau=cfg.tau, sigma_h0=cfg.sigma_h0, seed=0)
-    t0 = time.perf_counter()
-    gla_oracle.forward(c(q), c(k), c(v), a.numpy(), cfg.scale,
-                       None if h0 is None else h0.double().numpy(), nthreads=threads)
-    dt = time.perf_counter() - t0
-    used = min(threads, heads)
-    return {"value": heads * T / dt, "unit": "tokens/s", "cores": used, "kind": "oracle",
-            "sample": f"{heads} heads x {T} tokens of {cfg.name} (dk={cfg.dk}, dv={cfg.dv}), "
-                      f"fp64 recurrence, {dt:.1f} s"}
+    return OracleSample(cfg, target_s, threads).run()
 
 
 def host_threads() -> int:
@@ -336,21 +413,21 @@ def host_threads() -> int:
 
 
 def run_reference(args):
-    from synth import CHUNK_CONFIGS
-    cfg = CHUNK_CONFIGS[args.workload]
+    """The reference arm: the fp64 CPU oracle on the host cores, one bounded sample per step."""
+    cfg = chunk_config(args)
     threads = host_threads()
-    per = []
-    base = None
-    for _ in range(max(1, args.warmup)):
-        oracle_sample(cfg, 0.5, threads)
-    for _ in range(args.steps):
-        base = oracle_sample(cfg, args.ref_seconds, threads)
-        per.append(base["value"])
-    value = statistics.median(per)
+    per_step_s = max(0.5, min(args.ref_seconds, 150.0 / max(1, args.steps + args.warmup)))
+    sample = OracleSample(cfg, per_step_s, threads)
+    for _ in range(args.warmup):
+        sample.run()
+    per = [sample.run() for _ in range(args.steps)]
+    base = dict(per[-1])
+    value = statistics.median(p["value"] for p in per)
     base["value"] = value
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 0,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": None,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * sample.repeat * sample.heads * sample.T / value,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": cfg.name, "B": cfg.B, "H": cfg.H, "T": cfg.T,
                                         "dk": cfg.dk, "dv": cfg.dv},
@@ -364,17 +441,23 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="long", choices=["small", "medium", "long", "very_long"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--decode-steps", type=int, default=256)
-    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--only", default="both", choices=["both", "chunk", "decode"],
+                    help="run only the chunked forward or only the decode step")
+    ap.add_argument("--no-decode", action="store_true", help="same as --only chunk")
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's B")
+    ap.add_argument("--heads", type=int, default=0, help="override the workload's H")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ref-seconds", type=float, default=10.0,
+    ap.add_argument("--ref-seconds", type=float, default=15.0,
                     help="CPU seconds per oracle sample")
     args = ap.parse_args()
+    if args.no_decode:
+        args.only = "chunk"
     if args.warmup < 3 and args.impl == "ours":
         log("warning: fewer than 3 warm-up steps")
 
@@ -390,8 +473,7 @@ def main():
     line = run_ours(args, rank, world, local_rank)
     if rank == 0:
         if not args.no_cpu_baseline:
-            from synth import CHUNK_CONFIGS
-            line["cpu_baseline"] = oracle_sample(CHUNK_CONFIGS[args.workload], args.ref_seconds,
+            line["cpu_baseline"] = oracle_sample(chunk_config(args), args.ref_seconds,
                                                  host_threads())
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -50,13 +50,14 @@ def gla_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: 
                   scale: float | None = None, h0: torch.Tensor | None = None,
                   output_final_state: bool = True, *, out: torch.Tensor | None = None,
                   final_state: torch.Tensor | None = None, segments: int = 0, dv_tile: int = 0,
-                  force_exact: bool = False):
+                  force_exact: bool = False, cta_pair: int = 0):
     """Chunkwise-parallel GLA forward over whole sequences.
 
     Returns ``(o, hT)``; ``hT`` is None when ``output_final_state`` is False.
     ``final_state`` may be ``h0`` itself (in-place state update).
-    ``segments``, ``dv_tile`` and ``force_exact`` are the C ABI's options
-    (0 / False = automatic).
+    ``segments``, ``dv_tile``, ``force_exact`` and ``cta_pair`` are the C ABI's
+    options (0 / False = automatic; ``cta_pair=-1`` keeps the value tiles of a
+    head in independent CTAs).
     """
     if q.dim() != 4:
         raise ValueError("q must be [B, H, T, dk]")
@@ -80,7 +81,7 @@ def gla_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: 
     if scale is None:
         scale = dk ** -0.5
     opts = GlaChunkOptions(segments=int(segments), dv_tile=int(dv_tile),
-                           force_exact=1 if force_exact else 0)
+                           force_exact=1 if force_exact else 0, cta_pair=int(cta_pair))
     with torch.cuda.device(dev):
         st = _lib.lib().gla_chunk_fwd_ex(
             q.data_ptr(), k.data_ptr(), v.data_ptr(), log_alpha.data_ptr(), float(scale),
@@ -92,10 +93,10 @@ def gla_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: 
 
 
 def gla_chunk_fwd_plan(B: int, H: int, T: int, dk: int, dv: int, *, segments: int = 0,
-                       dv_tile: int = 0, force_exact: bool = False) -> dict:
+                       dv_tile: int = 0, force_exact: bool = False, cta_pair: int = 0) -> dict:
     """The launch plan gla_chunk_fwd would use on the current device (no GPU work)."""
     opts = GlaChunkOptions(segments=int(segments), dv_tile=int(dv_tile),
-                           force_exact=1 if force_exact else 0)
+                           force_exact=1 if force_exact else 0, cta_pair=int(cta_pair))
     nseg, tile, launches = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     scratch = ctypes.c_ulong()
     st = _lib.lib().gla_chunk_fwd_plan(B, H, T, dk, dv, ctypes.byref(opts), ctypes.byref(nseg),

@@ -29,7 +29,8 @@ EXPORTED = ("gla_chunk_fwd", "gla_chunk_fwd_ex", "gla_chunk_fwd_plan", "gla_chun
 
 class GlaChunkOptions(ctypes.Structure):
     _fields_ = [("segments", ctypes.c_int), ("dv_tile", ctypes.c_int),
-                ("force_exact", ctypes.c_int), ("reserved", ctypes.c_int * 5)]
+                ("force_exact", ctypes.c_int), ("cta_pair", ctypes.c_int),
+                ("reserved", ctypes.c_int * 4)]
 
 
 class GlaError(RuntimeError):

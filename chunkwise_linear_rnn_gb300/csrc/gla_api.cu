@@ -106,14 +106,18 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 struct Plan {
     int dv_tile, n_seg, seg_chunks;
+    bool pair;   // the two value-column tiles of a head run as a 2-CTA cluster
 };
 
-// Launch plan of gla_chunk_fwd: value-column tile, sequence segments.
+// Launch plan of gla_chunk_fwd: value-column tile, CTA pairs, sequence segments.
+// Pairs: with dk = 128 and exactly two value-column tiles, the tiles of a head
+// share the key-side preparation (each CTA prepares one half of the channels).
 // Segments: enough (batch, head, tile, segment) units to fill the SMs once,
 // each segment at least 8 chunks long to amortise its correction window.
-Plan make_plan(int B, int H, int T, int dv, const gla_chunk_options &op, int sm_count) {
+Plan make_plan(int B, int H, int T, int dk, int dv, const gla_chunk_options &op, int sm_count) {
     Plan pl;
     pl.dv_tile = op.dv_tile ? op.dv_tile : (dv >= 128 ? 128 : 64);
+    pl.pair = dk == 128 && dv == 2 * pl.dv_tile && op.cta_pair >= 0;
     const int n_chunks = (T + 127) / 128;
     int n_seg = op.segments;
     if (n_seg == 0) {
@@ -126,6 +130,17 @@ Plan make_plan(int B, int H, int T, int dv, const gla_chunk_options &op, int sm_
     pl.seg_chunks = (n_chunks + n_seg - 1) / n_seg;
     pl.n_seg = (n_chunks + pl.seg_chunks - 1) / pl.seg_chunks;
     return pl;
+}
+
+bool options_ok(int dv, const gla_chunk_options &op) {
+    if (op.dv_tile != 0 && op.dv_tile != 64 && op.dv_tile != 128) return false;
+    if (op.dv_tile > dv || op.segments < 0) return false;
+    return op.cta_pair >= -1 && op.cta_pair <= 1;
+}
+
+size_t scratch_needed(const Plan &pl, int B, int H, int dk, int dv) {
+    return pl.n_seg > 1 ? static_cast<size_t>(pl.n_seg) * B * H * dk * (dv + 1) * sizeof(float)
+                        : 0;
 }
 
 bool dk_ok(int dk) { return dk == 64 || dk == 128; }
@@ -145,9 +160,7 @@ int chunk_fwd_with_scratch(const void *q, const void *k, const void *v, const fl
     if (!dk_ok(dk) || !dv_ok(dv)) return GLA_ERR_SHAPE;
     gla_chunk_options o_def = {};
     const gla_chunk_options &op = opts ? *opts : o_def;
-    if ((op.dv_tile != 0 && op.dv_tile != 64 && op.dv_tile != 128) || op.dv_tile > dv ||
-        op.segments < 0)
-        return GLA_ERR_ARG;
+    if (!options_ok(dv, op)) return GLA_ERR_ARG;
     if (static_cast<long long>(B) * H > 0x7fffffffLL) return GLA_ERR_ARG;
     if (scratch && !aligned16(scratch)) return GLA_ERR_ARG;
 
@@ -159,7 +172,7 @@ int chunk_fwd_with_scratch(const void *q, const void *k, const void *v, const fl
     if (st != GLA_OK) return st;
 
     const int BH = B * H;
-    const Plan pl = make_plan(B, H, T, dv, op, dev->sm_count);
+    const Plan pl = make_plan(B, H, T, dk, dv, op, dev->sm_count);
     const size_t state_bytes =
         pl.n_seg > 1 ? static_cast<size_t>(pl.n_seg) * BH * dk * dv * sizeof(float) : 0;
     const size_t decay_bytes =
@@ -171,8 +184,8 @@ int chunk_fwd_with_scratch(const void *q, const void *k, const void *v, const fl
                   CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(enc, &p.tm_k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dk, T, BH, 64, 128,
                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(enc, &p.tm_a, log_alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dk, T, BH, dk, 128,
-                  CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(enc, &p.tm_a, log_alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dk, T, BH,
+                  pl.pair ? dk / 2 : dk, 128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_map(enc, &p.tm_v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dv, T, BH, 64, 128,
                   CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(enc, &p.tm_o, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dv, T, BH, 64, 128,
@@ -197,6 +210,7 @@ int chunk_fwd_with_scratch(const void *q, const void *k, const void *v, const fl
     p.dk = dk;
     p.dv = dv;
     p.dv_tile = pl.dv_tile;
+    p.pair = pl.pair ? 1 : 0;
     p.n_seg = pl.n_seg;
     p.seg_chunks = pl.seg_chunks;
     p.force_exact = op.force_exact ? 1 : 0;
@@ -236,67 +250,26 @@ int gla_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *l
     if (!dk_ok(dk) || !dv_ok(dv)) return GLA_ERR_SHAPE;
     gla_chunk_options o_def = {};
     const gla_chunk_options &op = opts ? *opts : o_def;
-    if (op.dv_tile != 0 && op.dv_tile != 64 && op.dv_tile != 128) return GLA_ERR_ARG;
-    if (op.dv_tile > dv) return GLA_ERR_ARG;
-    if (op.segments < 0) return GLA_ERR_ARG;
+    if (!options_ok(dv, op)) return GLA_ERR_ARG;
     if (static_cast<long long>(B) * H > 0x7fffffffLL) return GLA_ERR_ARG;
 
     DeviceInfo *dev = nullptr;
-    int st = current_device(&dev);
+    const int st = current_device(&dev);
     if (st != GLA_OK) return st;
-    EncodeTiledFn enc = nullptr;
-    st = encode_fn(&enc);
-    if (st != GLA_OK) return st;
-
-    const int BH = B * H;
-    const Plan pl = make_plan(B, H, T, dv, op, dev->sm_count);
-    const int dvt = pl.dv_tile, n_seg = pl.n_seg, seg_chunks = pl.seg_chunks;
-
-    ChunkLaunch p;
-    if (!make_map(enc, &p.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dk, T, BH, 64, 128,
-                  CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(enc, &p.tm_k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dk, T, BH, 64, 128,
-                  CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(enc, &p.tm_a, log_alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dk, T, BH, dk, 128,
-                  CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map(enc, &p.tm_v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dv, T, BH, 64, 128,
-                  CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(enc, &p.tm_o, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dv, T, BH, 64, 128,
-                  CU_TENSOR_MAP_SWIZZLE_128B))
-        return GLA_ERR_LAUNCH;
-    p.q = q;
-    p.k = k;
-    p.log_alpha = log_alpha;
-    p.h0 = h0;
-    p.hT = hT;
-    p.o = o;
-    p.ws_state = nullptr;
-    p.ws_decay = nullptr;
-    p.scale = scale;
-    p.B = B;
-    p.H = H;
-    p.T = T;
-    p.dk = dk;
-    p.dv = dv;
-    p.dv_tile = dvt;
-    p.n_seg = n_seg;
-    p.seg_chunks = seg_chunks;
-    p.force_exact = op.force_exact ? 1 : 0;
-    p.status = dev->status;
+    // the segment workspace (summaries S*, total decays) is stream-ordered
+    const size_t ws_bytes = scratch_needed(make_plan(B, H, T, dk, dv, op, dev->sm_count), B, H,
+                                           dk, dv);
     void *ws = nullptr;
-    if (n_seg > 1) {
-        const size_t state_bytes = static_cast<size_t>(n_seg) * BH * dk * dv * sizeof(float);
-        const size_t decay_bytes = static_cast<size_t>(n_seg) * BH * dk * sizeof(float);
-        if (cudaMallocAsync(&ws, state_bytes + decay_bytes, stream) != cudaSuccess) {
+    if (ws_bytes) {
+        if (cudaMallocAsync(&ws, ws_bytes, stream) != cudaSuccess) {
             cudaGetLastError();
             return GLA_ERR_ALLOC;
         }
-        p.ws_state = static_cast<float *>(ws);
-        p.ws_decay = reinterpret_cast<float *>(static_cast<char *>(ws) + state_bytes);
     }
-    const int err = launch_chunk_fwd(p, stream);
+    const int r = chunk_fwd_with_scratch(q, k, v, log_alpha, scale, h0, o, hT, B, H, T, dk, dv,
+                                         &op, stream, ws, ws_bytes);
     if (ws) cudaFreeAsync(ws, stream);
-    return err == 0 ? GLA_OK : GLA_ERR_LAUNCH;
+    return r;
 }
 
 int gla_chunk_fwd_plan(int B, int H, int T, int dk, int dv, const gla_chunk_options *opts,
@@ -307,20 +280,15 @@ int gla_chunk_fwd_plan(int B, int H, int T, int dk, int dv, const gla_chunk_opti
     if (!dk_ok(dk) || !dv_ok(dv)) return GLA_ERR_SHAPE;
     gla_chunk_options o_def = {};
     const gla_chunk_options &op = opts ? *opts : o_def;
-    if ((op.dv_tile != 0 && op.dv_tile != 64 && op.dv_tile != 128) || op.dv_tile > dv ||
-        op.segments < 0)
-        return GLA_ERR_ARG;
+    if (!options_ok(dv, op)) return GLA_ERR_ARG;
     DeviceInfo *dev = nullptr;
     const int st = current_device(&dev);
     if (st != GLA_OK) return st;
-    const Plan pl = make_plan(B, H, T, dv, op, dev->sm_count);
+    const Plan pl = make_plan(B, H, T, dk, dv, op, dev->sm_count);
     if (n_segments) *n_segments = pl.n_seg;
     if (dv_tile) *dv_tile = pl.dv_tile;
     if (launches) *launches = pl.n_seg > 1 ? 2 : 1;
-    if (scratch_bytes)
-        *scratch_bytes = pl.n_seg > 1 ? static_cast<size_t>(pl.n_seg) * B * H * dk * (dv + 1) *
-                                            sizeof(float)
-                                      : 0;
+    if (scratch_bytes) *scratch_bytes = scratch_needed(pl, B, H, dk, dv);
     return GLA_OK;
 }
 

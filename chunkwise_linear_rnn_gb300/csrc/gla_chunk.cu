@@ -93,38 +93,59 @@ struct ChunkReq {
     int t0, first_item, end, pad;
 };
 
+// An output tile staged in shared memory for the TMA store; after the last
+// one, `count` holds the number of tiles staged (kBarStageEnd).
+struct StoreRec {
+    int t0, count;
+};
+
 enum Bar {
     kBarQkFull = 0, kBarQkEmpty, kBarItem, kBarPFull, kBarPSplit, kBarSDone, kBarSReady,
     kBarOFull0, kBarOFull1, kBarOFree0, kBarOFree1, kBarVFull, kBarVEmpty, kBarAFull,
-    kBarQkRaw, kBarReq, kBarStage, kNumBars
+    kBarQkRaw, kBarReq, kBarStage, kBarXchg, kBarStageEnd, kNumBars
 };
-// arrival counts, in enum order
+// arrival counts, in enum order (a CTA pair doubles kBarQkEmpty: both MMAs commit to it)
 __device__ constexpr uint32_t kBarCounts[kNumBars] = {kPrepWarps, 1, 1, 1, 4, 1, 4, 1, 1, 4, 4,
-                                                      1, 1, 1, 1, 1, 4};
+                                                      1, 1, 1, 1, 1, 4, 1, 4};
 
-template <int DK, int DVT>
+// What one CTA of a pair sends its peer each chunk besides its three operand
+// blocks: the chunk-end Gamma of its key channels and its exponent-bound verdict.
+struct PairMeta {
+    float gam[64];
+    int bad, pad[3];
+};
+
+template <int DK, int DVT, bool PAIR>
 struct Smem {
+    static constexpr int kDKA = PAIR ? DK / 2 : DK;       // key channels prepared here
     static constexpr uint32_t kQBytes = kChunk * DK * 2;
-    static constexpr uint32_t kQ = 0;                     // Q, rescaled in place to Qh
-    static constexpr uint32_t kK = kQ + kQBytes;          // K, rescaled in place to Kh_hi
+    static constexpr uint32_t kQ = 0;                     // Qh (rescaled in place when single)
+    static constexpr uint32_t kK = kQ + kQBytes;          // Kh_hi
     static constexpr uint32_t kKlo = kK + kQBytes;        // Kh_lo
-    static constexpr uint32_t kA = kKlo + kQBytes;        // fp32 log gates [128][DK]
-    static constexpr uint32_t kABytes = kChunk * DK * 4;
+    static constexpr uint32_t kA = kKlo + kQBytes;        // fp32 log gates [128][kDKA]
+    static constexpr uint32_t kABytes = kChunk * kDKA * 4;
+    static constexpr uint32_t kRaw = kA + kABytes;        // pair: raw Q, K of this CTA's channels
+    static constexpr uint32_t kRawBytes = PAIR ? 2 * kBlk : 0;
     static constexpr uint32_t kVBytes = kChunk * DVT * 2;
-    static constexpr uint32_t kV = kA + kABytes;
+    static constexpr uint32_t kV = kRaw + kRawBytes;
     static constexpr uint32_t kSBlk = DK * 128;
     static constexpr uint32_t kSBytes = DK * DVT * 2;
     static constexpr uint32_t kS = kV + kVBytes;
     static constexpr uint32_t kG = kS + kSBytes;          // float [2][DK]: state scale per item
     static constexpr uint32_t kItem = kG + 2 * DK * 4;    // ItemInfo[2]
     static constexpr uint32_t kReq = kItem + 64;          // ChunkReq
-    static constexpr uint32_t kBar = kReq + 16;           // mbarriers
+    static constexpr uint32_t kStore = kReq + 16;         // StoreRec[2]: staged output tiles
+    static constexpr uint32_t kMeta = kStore + 16;        // pair: PairMeta[2], by CTA rank
+    static constexpr uint32_t kMetaBytes = PAIR ? 2 * sizeof(PairMeta) : 0;
+    static constexpr uint32_t kBar = kMeta + kMetaBytes;  // mbarriers
     static constexpr uint32_t kMisc = kBar + 8 * kNumBars;  // tmem slot
     static constexpr uint32_t kTotal = kMisc + 16;
     // At least 120 KB so that only one CTA fits on an SM: each CTA allocates
     // all 512 TMEM columns.
     static constexpr uint32_t kAlloc = (kTotal + 1024) > 122880u ? (kTotal + 1024) : 122880u;
     static_assert(kAlloc <= 232448, "shared memory budget exceeded");
+    static_assert(!PAIR || DK == 128, "CTA pairs split 128 key channels into two 64-channel blocks");
+    static_assert(kMeta % 16 == 0 && sizeof(PairMeta) % 16 == 0, "bulk copies move 16-byte units");
 };
 
 // TMEM columns: P [0,128) (fp32 scores, then the bf16 hi/lo pair in place),
@@ -182,9 +203,347 @@ __device__ __forceinline__ float clamp_gate(float a) {
     return fminf(fmaxf(a, -kExpBound), kExpBound);
 }
 
+// Sub-chunk rescaling of one chunk (prep threads): the largest power-of-two
+// block length cs whose every block keeps |Gamma - r_block| <= kExpBound
+// (clamped gates); each block becomes one item, written to the operand tiles
+// with its own reference.  Gates, Q and K are read from global memory.
+// Thread pt owns the channel pair 2*(pt % (DK/2)) of token part pt / (DK/2).
+// `n` counts items; gtot0/gtot1 return the chunk's clamped Gamma at its end
+// for the thread's channels (valid in the last token part).  Returns false if
+// a bounded wait expired.
+template <int DK>
+__device__ __forceinline__ bool sub_chunk_items(const KParams &p, int bh, int t0, int lc,
+                                                bool store, int pt, uint8_t *sQ, uint8_t *sK,
+                                                uint8_t *sKlo, float *sG, ItemInfo *sItem,
+                                                uint64_t *bars, int &n, float &gtot0,
+                                                float &gtot1) {
+    constexpr int NP = DK / 2;
+    constexpr int NQ = kPrepThreads / NP;
+    constexpr int TP = kChunk / NQ;
+    constexpr int kStride = DK / 2;     // row stride in bf16 pairs
+    const int pr = pt % NP, part = pt / NP;
+    const int ch = 2 * pr;
+    const bool last_part = part == NQ - 1;
+    const int lane = pt & 31;
+    const int T = p.T;
+    const size_t row0 = static_cast<size_t>(bh) * T;
+    const uint32_t *qb = p.q + (row0 * DK + ch) / 2;
+    const uint32_t *kb = p.k + (row0 * DK + ch) / 2;
+    const float2 *ab = p.a + (row0 * DK + ch) / 2;
+    auto raw_gate = [&](int i) {
+        const int t = t0 + i;
+        return t < T ? ab[static_cast<size_t>(t) * kStride] : make_float2(0.f, 0.f);
+    };
+    float bnd0[NQ], bnd1[NQ];  // clamped Gamma just before each part start
+    {
+        float c0 = 0.f, c1 = 0.f;
+        bnd0[0] = 0.f;
+        bnd1[0] = 0.f;
+        for (int qq = 1; qq < NQ; ++qq) {
+            for (int i = (qq - 1) * TP; i < qq * TP; ++i) {
+                const float2 a = raw_gate(i);
+                c0 += clamp_gate(a.x);
+                c1 += clamp_gate(a.y);
+            }
+            bnd0[qq] = c0;
+            bnd1[qq] = c1;
+        }
+    }
+    int cs = 64;
+    for (; cs > 1; cs >>= 1) {
+        float c0 = bnd0[part], c1 = bnd1[part];
+        const int s_first = (part * TP) / cs * cs;
+        float r0 = (s_first >= part * TP) ? c0 : bnd0[s_first / TP];
+        float r1 = (s_first >= part * TP) ? c1 : bnd1[s_first / TP];
+        bool viol = false;
+        for (int ii = 0; ii < TP; ++ii) {
+            const int i = part * TP + ii;
+            if (i % cs == 0) {
+                r0 = c0;
+                r1 = c1;
+            }
+            const float2 a = raw_gate(i);
+            c0 += clamp_gate(a.x);
+            c1 += clamp_gate(a.y);
+            viol |= fabsf(c0 - r0) > kExpBound || fabsf(c1 - r1) > kExpBound;
+        }
+        if (!bar_or(3, kPrepThreads, viol)) break;
+    }
+    // cs == 1 always satisfies the bound: a single clamped gate is within it.
+    const int n_sub = kChunk / cs;
+    bool ok = true;
+    for (int sidx = 0; sidx < n_sub; ++sidx) {
+        const int sa = sidx * cs, sb = sa + cs;
+        bool okw = true;
+        if (sidx > 0) okw = mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status);
+        ok = !bar_or(4, kPrepThreads, !okw);
+        if (!ok) break;
+        // reference for block sidx: clamped Gamma just before token sa
+        float c0 = bnd0[part], c1 = bnd1[part];
+        float r0 = 0.f, r1 = 0.f;
+        if (sa <= part * TP) {
+            r0 = bnd0[sa / TP];
+            r1 = bnd1[sa / TP];
+        }
+        for (int ii = 0; ii < TP; ++ii) {
+            const int i = part * TP + ii;
+            if (i == sa) {
+                r0 = c0;
+                r1 = c1;
+            }
+            const int t = t0 + i;
+            const float2 a = raw_gate(i);
+            c0 += clamp_gate(a.x);
+            c1 += clamp_gate(a.y);
+            const uint32_t off = sw128_offset(i, ch, kBlk);
+            uint32_t hi = 0u, lo = 0u, qv = 0u;
+            if (i >= sa && i < sb && t < T) {
+                const float2 qf = unpack_bf16x2(qb[static_cast<size_t>(t) * kStride]);
+                const float2 kf = unpack_bf16x2(kb[static_cast<size_t>(t) * kStride]);
+                qv = bf16x2_bits(qf.x * __expf(c0 - r0), qf.y * __expf(c1 - r1));
+                split_pair(kf.x * __expf(r0 - c0), kf.y * __expf(r1 - c1), hi, lo);
+            }
+            *reinterpret_cast<uint32_t *>(sQ + off) = qv;
+            *reinterpret_cast<uint32_t *>(sK + off) = hi;
+            *reinterpret_cast<uint32_t *>(sKlo + off) = lo;
+            if (i == sb - 1) {
+                sG[(n & 1) * DK + ch] = __expf(c0 - r0);
+                sG[(n & 1) * DK + ch + 1] = __expf(c1 - r1);
+            }
+        }
+        if (last_part) {
+            gtot0 = c0;
+            gtot1 = c1;
+        }
+        if (pt == 0) {
+            sItem[n & 1] = ItemInfo{
+                t0, sa, sb, (sidx == n_sub - 1 ? kItemLast : 0) | (store ? kItemStore : 0), lc,
+                {0, 0, 0}};
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kBarQkFull]);
+        ++n;
+    }
+    return ok;
+}
+
+// Prep warps of one CTA of a pair.  The CTA owns key channels
+// [64 rank, 64 rank + 64): 32 channel pairs x 8 token parts of 16 tokens.
+// Per chunk:
+//   1. phase A on the A half tile: in-chunk prefix sums in place, part
+//      offsets, the exponent-bound verdict for these channels;
+//   2. phase B into registers from the raw Q and K staging tiles (Qh, Kh_hi,
+//      Kh_lo for 16 tokens x 2 channels); after it the A and staging tiles are
+//      free and the next chunk is requested, so its loads overlap this
+//      chunk's products;
+//   3. once both CTAs' MMAs have released the previous item's operand tiles,
+//      the registers go to this CTA's 64-channel block of the Qh, Kh_hi and
+//      Kh_lo tiles, and the three blocks plus a PairMeta record are copied
+//      into the peer's shared memory at the same offsets;
+//   4. after the peer's copy has landed here: if neither CTA's channels broke
+//      the exponent bound, the chunk is one item; otherwise both CTAs run the
+//      sub-chunk path over all channels on their own (same inputs, same items).
+// Threads pt < DK keep the decay since the segment start of channel pt; both
+// CTAs compute it identically (from the exchanged chunk-end Gammas, or from
+// the raw gates), so their window decisions agree.
 template <int DK, int DVT>
+__device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint32_t rank, int bh,
+                                          int seg, int c_begin, int c_end, size_t BHn,
+                                          int dv_tile) {
+    using L = Smem<DK, DVT, true>;
+    constexpr int DKH = DK / 2;                 // channels prepared by this CTA
+    constexpr int NP = DKH / 2;                 // channel pairs
+    constexpr int NQ = kPrepThreads / NP;       // token parts
+    constexpr int TP = kChunk / NQ;             // tokens per part
+    constexpr uint32_t kXchgBytes = 3u * kBlk + static_cast<uint32_t>(sizeof(PairMeta));
+    uint8_t *sQ = smem + L::kQ;
+    uint8_t *sK = smem + L::kK;
+    uint8_t *sKlo = smem + L::kKlo;
+    const uint8_t *sRawQ = smem + L::kRaw;
+    const uint8_t *sRawK = sRawQ + kBlk;
+    float *sA = reinterpret_cast<float *>(smem + L::kA);
+    float *sG = reinterpret_cast<float *>(smem + L::kG);
+    ItemInfo *sItem = reinterpret_cast<ItemInfo *>(smem + L::kItem);
+    ChunkReq *sReq = reinterpret_cast<ChunkReq *>(smem + L::kReq);
+    PairMeta *meta = reinterpret_cast<PairMeta *>(smem + L::kMeta);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBar);
+
+    const int pt = threadIdx.x;
+    const int lane = pt & 31;
+    const int pr = pt % NP, part = pt / NP;
+    const int chl = 2 * pr;                      // channel within this CTA's half
+    const int ch = static_cast<int>(rank) * DKH + chl;
+    const bool last_part = part == NQ - 1;
+    const float *sAc = sA + chl;
+    const uint32_t peer = rank ^ 1u;
+    const int T = p.T;
+
+    float gseg = 0.f;                            // threads pt < DK: channel pt
+    bool closed = (p.mode == kModeFull && seg == 0);
+    int n = 0;
+    bool ok = true;
+    bool requested = false, end_posted = false;
+    auto post = [&](int c) {                     // request the loads of chunk c (or the end)
+        const bool e = c >= c_end;
+        if (pt == 0) {
+            sReq[0] = ChunkReq{e ? -1 : c * kChunk, 0, e ? 1 : 0, 0};
+            mbar_arrive(&bars[kBarReq]);
+        }
+        requested = !e;
+        end_posted = e;
+    };
+    post(c_begin);
+    // A wait that expires clears `ok` in its thread only: every thread still
+    // runs the same sequence of barriers (each wait is bounded), and the loop
+    // ends at the next chunk boundary, where the threads' verdicts are combined.
+    for (int c = c_begin, lc = 0;; ++c, ++lc) {
+        // ---- end of the segment, or (correction pass) of the decay window
+        const bool win = !closed && pt < DK && gseg > -kWindowCut;
+        const bool any_win = bar_or(1, kPrepThreads, win);
+        if (!closed && !any_win) closed = true;
+        ok = !bar_or(4, kPrepThreads, !ok);
+        const bool end = c >= c_end || !ok || (p.mode == kModeCorrect && closed);
+        if (end) {
+            if (requested && ok) {
+                // a speculative request for this chunk is in flight: let it land
+                bool okw = mbar_wait_bounded(&bars[kBarAFull], lc & 1, p.status);
+                okw &= mbar_wait_bounded(&bars[kBarQkRaw], lc & 1, p.status);
+                okw &= mbar_wait_bounded(&bars[kBarVFull], lc & 1, p.status);
+                ok = !bar_or(4, kPrepThreads, !okw);
+            }
+            break;
+        }
+        const int t0 = c * kChunk;
+        const bool store = p.mode == kModeCorrect || closed;
+        // ---- phase A: prefix sums of this thread's part, in place
+        ok &= mbar_wait_bounded(&bars[kBarAFull], lc & 1, p.status);
+        float c0 = 0.f, c1 = 0.f;
+        float lmn = 3.0e38f, lmx = -3.0e38f;
+        {
+            float2 av[TP];
+#pragma unroll
+            for (int e = 0; e < TP; ++e)
+                av[e] = *reinterpret_cast<const float2 *>(sAc + (part * TP + e) * DKH);
+#pragma unroll
+            for (int e = 0; e < TP; ++e) {
+                c0 += av[e].x;
+                c1 += av[e].y;
+                lmn = fminf(lmn, fminf(c0, c1));
+                lmx = fmaxf(lmx, fmaxf(c0, c1));
+                *reinterpret_cast<float2 *>(sA + chl + (part * TP + e) * DKH) = make_float2(c0, c1);
+            }
+        }
+        named_barrier(5, kPrepThreads);
+        float o0 = 0.f, o1 = 0.f;
+#pragma unroll
+        for (int qq = 0; qq < NQ - 1; ++qq) {
+            if (qq < part) {
+                const float2 tt = *reinterpret_cast<const float2 *>(sAc + (qq * TP + TP - 1) * DKH);
+                o0 += tt.x;
+                o1 += tt.y;
+            }
+        }
+        const float gmin = fminf(o0, o1) + lmn, gmax = fmaxf(o0, o1) + lmx;
+        const bool bad_mine =
+            fmaxf(-fminf(gmin, 0.f), fmaxf(gmax, 0.f)) > kExpBound || p.force_sub != 0;
+        // ---- phase B into registers (values of a chunk that broke the bound
+        // are computed but never used)
+        ok &= mbar_wait_bounded(&bars[kBarQkRaw], lc & 1, p.status);
+        uint32_t rq[TP], rh[TP], rl[TP];
+#pragma unroll
+        for (int e = 0; e < TP; ++e) {
+            const int i = part * TP + e;
+            const uint32_t off = sw128_offset(i, chl, kBlk);
+            const float2 a = *reinterpret_cast<const float2 *>(sAc + i * DKH);
+            const float2 qf = unpack_bf16x2(*reinterpret_cast<const uint32_t *>(sRawQ + off));
+            const float2 kf = unpack_bf16x2(*reinterpret_cast<const uint32_t *>(sRawK + off));
+            const float g0 = o0 + a.x, g1 = o1 + a.y;
+            rq[e] = bf16x2_bits(qf.x * __expf(g0), qf.y * __expf(g1));
+            split_pair(kf.x * __expf(-g0), kf.y * __expf(-g1), rh[e], rl[e]);
+        }
+        const float gc0 = o0 + c0, gc1 = o1 + c1;   // Gamma at the chunk end (last part)
+        // the A and staging tiles are consumed: start the next chunk's loads
+        named_barrier(5, kPrepThreads);
+        post(c + 1);
+        // ---- both CTAs' MMAs are done with the previous item's tiles
+        if (n > 0) ok &= mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status);
+#pragma unroll
+        for (int e = 0; e < TP; ++e) {
+            const uint32_t off = sw128_offset(part * TP + e, ch, kBlk);
+            *reinterpret_cast<uint32_t *>(sQ + off) = rq[e];
+            *reinterpret_cast<uint32_t *>(sK + off) = rh[e];
+            *reinterpret_cast<uint32_t *>(sKlo + off) = rl[e];
+        }
+        if (last_part) {
+            meta[rank].gam[chl] = gc0;
+            meta[rank].gam[chl + 1] = gc1;
+        }
+        fence_proxy_async_smem();
+        // all blocks written; one exponent-bound verdict for this CTA's channels
+        const bool bad_here = bar_or(2, kPrepThreads, bad_mine);
+        if (pt == 0) {
+            meta[rank].bad = bad_here ? 1 : 0;
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&bars[kBarXchg], kXchgBytes);
+            const uint32_t pbar = mapa_shared(smem_u32(&bars[kBarXchg]), peer);
+            const uint32_t blk = rank * kBlk;
+            bulk_copy_to_peer(mapa_shared(smem_u32(sQ + blk), peer), sQ + blk, kBlk, pbar);
+            bulk_copy_to_peer(mapa_shared(smem_u32(sK + blk), peer), sK + blk, kBlk, pbar);
+            bulk_copy_to_peer(mapa_shared(smem_u32(sKlo + blk), peer), sKlo + blk, kBlk, pbar);
+            bulk_copy_to_peer(mapa_shared(smem_u32(&meta[rank]), peer), &meta[rank],
+                              static_cast<uint32_t>(sizeof(PairMeta)), pbar);
+        }
+        // ---- the peer's blocks and record have landed here
+        ok &= mbar_wait_bounded(&bars[kBarXchg], lc & 1, p.status);
+        // one branch for all threads, even for one whose wait expired
+        const bool bad = bar_or(2, kPrepThreads, (meta[0].bad | meta[1].bad) != 0);
+        if (!bad) {
+            if (pt < DK) {
+                const float g = meta[pt / DKH].gam[pt % DKH];
+                gseg += g;
+                sG[(n & 1) * DK + pt] = __expf(g);
+            }
+            if (pt == 0) {
+                sItem[n & 1] = ItemInfo{t0, 0, kChunk, kItemLast | (store ? kItemStore : 0), lc,
+                                        {0, 0, 0}};
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kBarQkFull]);
+            ++n;
+            continue;
+        }
+        // ---- a chunk whose decay breaks the bound: sub-chunk items over all
+        // channels, computed by each CTA of the pair on its own
+        float gt0 = 0.f, gt1 = 0.f;
+        ok &= sub_chunk_items<DK>(p, bh, t0, lc, store, pt, sQ, sK, sKlo, sG, sItem, bars, n, gt0,
+                                  gt1);
+        if (pt < DK) {
+            // the chunk's clamped decay of channel pt, summed in token order
+            const float *ab = reinterpret_cast<const float *>(p.a) + static_cast<size_t>(bh) * T * DK + pt;
+            float gsum = 0.f;
+            for (int i = 0; i < kChunk && t0 + i < T; ++i)
+                gsum += clamp_gate(ab[static_cast<size_t>(t0 + i) * DK]);
+            gseg += gsum;
+        }
+    }
+    // ---- end of the item stream (and of the load requests)
+    if (!end_posted && pt == 0) {
+        sReq[0] = ChunkReq{-1, 0, 1, 0};
+        mbar_arrive(&bars[kBarReq]);
+    }
+    if (n > 0 && !mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status)) ok = false;
+    if (pt == 0) sItem[n & 1] = ItemInfo{0, 0, 0, kItemEnd, 0, {0, 0, 0}};
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars[kBarQkFull]);
+    // segment summary: total decay of this segment (FULL mode, several segments)
+    if (p.mode == kModeFull && p.n_seg > 1 && dv_tile == 0 && pt < DK)
+        p.ws_decay[(static_cast<size_t>(seg) * BHn + bh) * DK + pt] = gseg;
+}
+
+template <int DK, int DVT, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_constant__ KParams p) {
-    using L = Smem<DK, DVT>;
+    using L = Smem<DK, DVT, PAIR>;
     using TM = Tmem<DVT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -198,6 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
     float *sG = reinterpret_cast<float *>(smem + L::kG);
     ItemInfo *sItem = reinterpret_cast<ItemInfo *>(smem + L::kItem);
     ChunkReq *sReq = reinterpret_cast<ChunkReq *>(smem + L::kReq);
+    StoreRec *sStore = reinterpret_cast<StoreRec *>(smem + L::kStore);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBar);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
 
@@ -216,8 +576,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
     const int c_end = min(n_chunks, c_begin + p.seg_chunks);
     const size_t BHn = static_cast<size_t>(gridDim.z / nseg_launch) * p.H;  // B * H
 
+    // CTA pair: the two value-column tiles of one head, cluster ranks 0 and 1
+    // (rank == dv_tile); each prepares the operands of one half of the key
+    // channels and sends them to the other.
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
     if (tid == 0) {
-        for (int i = 0; i < kNumBars; ++i) mbar_init(&bars[i], kBarCounts[i]);
+        for (int i = 0; i < kNumBars; ++i)
+            mbar_init(&bars[i], (PAIR && i == kBarQkEmpty) ? 2u : kBarCounts[i]);
         fence_mbar_init();
     }
     if (warp == kTmaWarp && lane == 0) {
@@ -230,10 +595,15 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
     if (warp == kMmaWarp) tmem_alloc(tmem_slot, TM::kCols);
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync_all();   // the peer's barriers exist before any remote use
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp < kPrepWarps) {
+    if (warp < kPrepWarps && PAIR) {
+        if constexpr (PAIR) {
+            prep_pair<DK, DVT>(p, smem, rank, bh, seg, c_begin, c_end, BHn, dv_tile);
+        }
+    } else if (warp < kPrepWarps) {
         // =========================================================== prep warps
         constexpr int NP = DK / 2;              // channel pairs
         constexpr int NQ = kPrepThreads / NP;   // token parts
@@ -243,10 +613,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
         const int pr = pt % NP, part = pt / NP;
         const int ch = 2 * pr;
         const bool last_part = part == NQ - 1;
-        const size_t row0 = static_cast<size_t>(bh) * T;
-        const uint32_t *qb = p.q + (row0 * DK + ch) / 2;   // global rows, sub-chunk path only
-        const uint32_t *kb = p.k + (row0 * DK + ch) / 2;
-        constexpr int kStride = DK / 2;     // row stride in bf16 pairs
         const float *sAc = sA + ch;         // this thread's channel pair in the A tile
         float gseg0 = 0.f, gseg1 = 0.f;     // decay since the segment start (last part only)
         bool closed = (p.mode == kModeFull && seg == 0);  // no correction window
@@ -380,110 +746,15 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                 ++n;
                 continue;
             }
-            // ---- sub-chunk rescaling: the largest power-of-two block length cs
-            // whose every block keeps |Gamma - r_block| <= kExpBound (clamped
-            // gates).  Gates, Q and K are re-read from global memory: the tiles
-            // hold prefix sums and the raw inputs.
-            const float2 *ab = p.a + (row0 * DK + ch) / 2;
-            auto raw_gate = [&](int i) {
-                const int t = t0 + i;
-                return t < T ? ab[static_cast<size_t>(t) * kStride] : make_float2(0.f, 0.f);
-            };
-            float bnd0[NQ], bnd1[NQ];  // clamped Gamma just before each part start
-            {
-                float c0 = 0.f, c1 = 0.f;
-                bnd0[0] = 0.f;
-                bnd1[0] = 0.f;
-                for (int qq = 1; qq < NQ; ++qq) {
-                    for (int i = (qq - 1) * TP; i < qq * TP; ++i) {
-                        const float2 a = raw_gate(i);
-                        c0 += clamp_gate(a.x);
-                        c1 += clamp_gate(a.y);
-                    }
-                    bnd0[qq] = c0;
-                    bnd1[qq] = c1;
-                }
-            }
-            int cs = 64;
-            for (; cs > 1; cs >>= 1) {
-                float c0 = bnd0[part], c1 = bnd1[part];
-                const int s_first = (part * TP) / cs * cs;
-                float r0 = (s_first >= part * TP) ? c0 : bnd0[s_first / TP];
-                float r1 = (s_first >= part * TP) ? c1 : bnd1[s_first / TP];
-                bool viol = false;
-                for (int ii = 0; ii < TP; ++ii) {
-                    const int i = part * TP + ii;
-                    if (i % cs == 0) {
-                        r0 = c0;
-                        r1 = c1;
-                    }
-                    const float2 a = raw_gate(i);
-                    c0 += clamp_gate(a.x);
-                    c1 += clamp_gate(a.y);
-                    viol |= fabsf(c0 - r0) > kExpBound || fabsf(c1 - r1) > kExpBound;
-                }
-                if (!bar_or(3, kPrepThreads, viol)) break;
-            }
-            // cs == 1 always satisfies the bound: a single clamped gate is within it.
-            const int n_sub = kChunk / cs;
+            // ---- sub-chunk rescaling (chunks whose decay exceeds the bound)
             float gtot0 = 0.f, gtot1 = 0.f;
-            for (int sidx = 0; sidx < n_sub; ++sidx) {
-                const int sa = sidx * cs, sb = sa + cs;
-                okw = true;
-                if (sidx > 0) okw = mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status);
-                ok = !bar_or(4, kPrepThreads, !okw);
-                if (!ok) break;
-                // reference for block sidx: clamped Gamma just before token sa
-                float c0 = bnd0[part], c1 = bnd1[part];
-                float r0 = 0.f, r1 = 0.f;
-                if (sa <= part * TP) {
-                    r0 = bnd0[sa / TP];
-                    r1 = bnd1[sa / TP];
-                }
-                for (int ii = 0; ii < TP; ++ii) {
-                    const int i = part * TP + ii;
-                    if (i == sa) {
-                        r0 = c0;
-                        r1 = c1;
-                    }
-                    const int t = t0 + i;
-                    const float2 a = raw_gate(i);
-                    c0 += clamp_gate(a.x);
-                    c1 += clamp_gate(a.y);
-                    const uint32_t off = sw128_offset(i, ch, kBlk);
-                    uint32_t hi = 0u, lo = 0u, qv = 0u;
-                    if (i >= sa && i < sb && t < T) {
-                        const float2 qf = unpack_bf16x2(qb[static_cast<size_t>(t) * kStride]);
-                        const float2 kf = unpack_bf16x2(kb[static_cast<size_t>(t) * kStride]);
-                        qv = bf16x2_bits(qf.x * __expf(c0 - r0), qf.y * __expf(c1 - r1));
-                        split_pair(kf.x * __expf(r0 - c0), kf.y * __expf(r1 - c1), hi, lo);
-                    }
-                    *reinterpret_cast<uint32_t *>(sQ + off) = qv;
-                    *reinterpret_cast<uint32_t *>(sK + off) = hi;
-                    *reinterpret_cast<uint32_t *>(sKlo + off) = lo;
-                    if (i == sb - 1) {
-                        sG[(n & 1) * DK + ch] = __expf(c0 - r0);
-                        sG[(n & 1) * DK + ch + 1] = __expf(c1 - r1);
-                    }
-                }
-                if (last_part) {
-                    gtot0 = c0;
-                    gtot1 = c1;
-                }
-                if (pt == 0) {
-                    sItem[n & 1] = ItemInfo{
-                        t0, sa, sb, (sidx == n_sub - 1 ? kItemLast : 0) | (store ? kItemStore : 0),
-                        lc, {0, 0, 0}};
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[kBarQkFull]);
-                ++n;
-            }
+            ok = sub_chunk_items<DK>(p, bh, t0, lc, store, pt, sQ, sK, sKlo, sG, sItem, bars, n,
+                                     gtot0, gtot1);
             if (last_part) {
                 gseg0 += gtot0;
                 gseg1 += gtot1;
             }
+            // an expired wait (!ok) ends the stream at the top of the loop
         }
         // ---- end of the item stream
         if (n > 0 && !mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status)) ok = false;
@@ -498,33 +769,104 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
         }
     } else if (warp == kTmaWarp) {
         // =========================================================== TMA producer
+        // Three load streams and the output store stream, each served as soon
+        // as its own condition holds, so that none waits behind another: per
+        // requested chunk, A (and, in a CTA pair, the raw Q/K staging tiles) at
+        // once; single-CTA Q and K once the previous chunk's items have released
+        // the operand tiles; V once the previous chunk's V tile (also the output
+        // staging tile) is free; a staged output tile as soon as it is complete.
         if (lane == 0) {
-            for (int lc = 0;; ++lc) {
-                if (!mbar_wait_bounded(&bars[kBarReq], lc & 1, p.status)) break;
-                const ChunkReq rq = sReq[0];
-                if (rq.end) break;
-                const int t0 = rq.t0;
-                // A: the prep has released the previous chunk's A tile (request barrier)
-                fence_proxy_async_smem();
-                mbar_arrive_expect_tx(&bars[kBarAFull], L::kABytes);
-                tma_load_3d(sA, &p.tm_a, &bars[kBarAFull], 0, t0, bh);
-                // Q, K: after the last item of the previous chunk has been consumed
-                if (rq.first_item > 0 &&
-                    !mbar_wait_bounded(&bars[kBarQkEmpty], (rq.first_item - 1) & 1, p.status))
-                    break;
-                mbar_arrive_expect_tx(&bars[kBarQkRaw], 2u * L::kQBytes);
-#pragma unroll
-                for (int kb = 0; kb < DK / 64; ++kb) {
-                    tma_load_3d(sQ + kb * kBlk, &p.tm_q, &bars[kBarQkRaw], kb * 64, t0, bh);
-                    tma_load_3d(sK + kb * kBlk, &p.tm_k, &bars[kBarQkRaw], kb * 64, t0, bh);
+            int n_req = 0, n_qk = 0, n_v = 0;   // chunks requested / Q,K issued / V issued
+            int n_st = 0, st_total = -1;        // staged output tiles taken / in all
+            bool req_end = false;
+            int t0s[4], firsts[4];              // at most 3 chunks are ever outstanding
+            unsigned long long idle_since = 0;
+            while (true) {
+                bool progress = false;
+                if (!req_end && mbar_test_wait(&bars[kBarReq], n_req & 1)) {
+                    const ChunkReq rq = sReq[0];
+                    progress = true;
+                    if (rq.end) {
+                        req_end = true;
+                    } else {
+                        const int t0 = rq.t0;
+                        t0s[n_req & 3] = t0;
+                        firsts[n_req & 3] = rq.first_item;
+                        // A (and staging): the prep released them with the request
+                        fence_proxy_async_smem();
+                        mbar_arrive_expect_tx(&bars[kBarAFull], L::kABytes);
+                        tma_load_3d(sA, &p.tm_a, &bars[kBarAFull], static_cast<int>(rank) * L::kDKA,
+                                    t0, bh);
+                        if constexpr (PAIR) {
+                            uint8_t *sRaw = smem + L::kRaw;
+                            mbar_arrive_expect_tx(&bars[kBarQkRaw], 2u * kBlk);
+                            tma_load_3d(sRaw, &p.tm_q, &bars[kBarQkRaw], static_cast<int>(rank) * 64,
+                                        t0, bh);
+                            tma_load_3d(sRaw + kBlk, &p.tm_k, &bars[kBarQkRaw],
+                                        static_cast<int>(rank) * 64, t0, bh);
+                        }
+                        ++n_req;
+                    }
                 }
-                // V: after the previous chunk's P V and state products
-                if (lc > 0 && !mbar_wait_bounded(&bars[kBarVEmpty], (lc - 1) & 1, p.status)) break;
-                mbar_arrive_expect_tx(&bars[kBarVFull], L::kVBytes);
+                if constexpr (!PAIR) {
+                    // Q, K in place: after the last item of the previous chunk
+                    if (n_qk < n_req) {
+                        const int first = firsts[n_qk & 3];
+                        if (first == 0 || mbar_test_wait(&bars[kBarQkEmpty], (first - 1) & 1)) {
+                            const int t0 = t0s[n_qk & 3];
+                            mbar_arrive_expect_tx(&bars[kBarQkRaw], 2u * L::kQBytes);
 #pragma unroll
-                for (int nb = 0; nb < DVT / 64; ++nb)
-                    tma_load_3d(sV + nb * kBlk, &p.tm_v, &bars[kBarVFull], dv0 + nb * 64, t0, bh);
+                            for (int kb = 0; kb < DK / 64; ++kb) {
+                                tma_load_3d(sQ + kb * kBlk, &p.tm_q, &bars[kBarQkRaw], kb * 64, t0, bh);
+                                tma_load_3d(sK + kb * kBlk, &p.tm_k, &bars[kBarQkRaw], kb * 64, t0, bh);
+                            }
+                            ++n_qk;
+                            progress = true;
+                        }
+                    }
+                }
+                // V: after the previous chunk's products and output store
+                if (n_v < n_req && (n_v == 0 || mbar_test_wait(&bars[kBarVEmpty], (n_v - 1) & 1))) {
+                    const int t0 = t0s[n_v & 3];
+                    mbar_arrive_expect_tx(&bars[kBarVFull], L::kVBytes);
+#pragma unroll
+                    for (int nb = 0; nb < DVT / 64; ++nb)
+                        tma_load_3d(sV + nb * kBlk, &p.tm_v, &bars[kBarVFull], dv0 + nb * 64, t0, bh);
+                    ++n_v;
+                    progress = true;
+                }
+                // staged output tiles: store, and free the V tile once the store
+                // has read it
+                if (mbar_test_wait(&bars[kBarStage], n_st & 1)) {
+                    const int t0 = sStore[n_st & 1].t0;
+#pragma unroll
+                    for (int nb = 0; nb < DVT / 64; ++nb)
+                        tma_store_3d(&p.tm_o, sV + nb * kBlk, dv0 + nb * 64, t0, bh);
+                    tma_store_commit();
+                    tma_store_wait_read_all();
+                    mbar_arrive(&bars[kBarVEmpty]);
+                    ++n_st;
+                    progress = true;
+                }
+                if (st_total < 0 && mbar_test_wait(&bars[kBarStageEnd], 0)) {
+                    st_total = sStore[0].count;
+                    progress = true;
+                }
+                if (req_end && n_st == st_total && n_v == n_req && (PAIR || n_qk == n_req)) break;
+                if (progress) {
+                    idle_since = 0;
+                } else {
+                    const unsigned long long now = global_timer_ns();
+                    if (idle_since == 0) {
+                        idle_since = now;
+                    } else if (now - idle_since > kWaitLimitNs) {
+                        atomicOr(p.status, kStatusTimeout);
+                        break;
+                    }
+                    __nanosleep(64);
+                }
             }
+            tma_store_wait_all();
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
@@ -543,10 +885,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                 const int ob = n & 1;
                 const uint32_t tO = tmem + (ob ? TM::kO1 : TM::kO0);
                 const uint32_t aV = aV0;
-                bool okw = true;
-                if (n >= 2) okw &= mbar_wait_bounded(&bars[kBarOFree0 + ob], ((n >> 1) + 1) & 1, p.status);
-                okw &= mbar_wait_bounded(&bars[kBarVFull], it.lc & 1, p.status);
-                if (!okw) break;
                 tc_fence_after();
                 // P = Qh (Kh_hi + Kh_lo)^T
 #pragma unroll
@@ -562,8 +900,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                                 sw128_desc(aKlo + koff, 16, 1024), id_qk, 1);
                 }
                 mma_commit(&bars[kBarPFull]);
-                // O = Qh S_prev (needs the previous state scaled and copied)
-                if (!mbar_wait_bounded(&bars[kBarSReady], n & 1, p.status)) break;
+                // O = Qh S_prev: needs this O buffer drained and the previous
+                // state scaled and copied
+                bool okw = true;
+                if (n >= 2) okw &= mbar_wait_bounded(&bars[kBarOFree0 + ob], ((n >> 1) + 1) & 1, p.status);
+                okw &= mbar_wait_bounded(&bars[kBarSReady], n & 1, p.status);
+                if (!okw) break;
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < DK / 16; ++ks) {
@@ -572,6 +914,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                                 sw128_desc(aS + ks * 2048, L::kSBlk, 1024), id_ov, ks > 0);
                 }
                 // S += (Kh_hi + Kh_lo)^T V
+                if (!mbar_wait_bounded(&bars[kBarVFull], it.lc & 1, p.status)) break;
+                tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < kChunk / 16; ++ks) {
                     mma_bf16_ss(tmem + TM::kS, sw128_desc(aK + ks * 2048, kBlk, 1024),
@@ -580,7 +924,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                                 sw128_desc(aV + ks * 2048, kBlk, 1024), id_kv, 1);
                 }
                 mma_commit(&bars[kBarSDone]);
-                mma_commit(&bars[kBarQkEmpty]);
+                if constexpr (PAIR)
+                    mma_commit_multicast(&bars[kBarQkEmpty], 0x3);   // both CTAs' tiles
+                else
+                    mma_commit(&bars[kBarQkEmpty]);
                 // O += (P_hi + P_lo) V, P from TMEM
                 if (!mbar_wait_bounded(&bars[kBarPSplit], n & 1, p.status)) break;
                 tc_fence_after();
@@ -685,16 +1032,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             // ---- causal mask of P (row i), split into the TMEM A operand of P V
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarPFull], n & 1, p.status))) break;
             tc_fence_after();
-#pragma unroll
-            for (int qd = 0; qd < kChunk / 32; qd += 2) {
-                uint32_t r0[32], r1[32];
-                tmem_ld32(tP + 32 * qd, r0);
-                tmem_ld32(tP + 32 * (qd + 1), r1);
-                tmem_wait_ld();
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const uint32_t(&r)[32] = half ? r1 : r0;
-                    const int qq = qd + half;
+            {
+                // This warp's rows are 32 wq .. 32 wq + 31: column blocks past
+                // block wq are masked whole (zeros, nothing to read), block wq
+                // is the diagonal, the blocks before it are unmasked.
+                const int wq = warp - kTmemWarp0;
+                auto split_block = [&](const uint32_t(&r)[32], int qq) {
                     uint32_t hi[16], lo[16];
 #pragma unroll
                     for (int w = 0; w < 16; ++w) {
@@ -705,6 +1048,33 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                     }
                     tmem_st16(tP + 32 * qq, hi);
                     tmem_st16(tP + 32 * qq + 16, lo);
+                };
+                auto zero_block = [&](int qq) {
+                    uint32_t z[16];
+#pragma unroll
+                    for (int w = 0; w < 16; ++w) z[w] = 0u;
+                    tmem_st16(tP + 32 * qq, z);
+                    tmem_st16(tP + 32 * qq + 16, z);
+                };
+#pragma unroll
+                for (int qd = 0; qd < kChunk / 32; qd += 2) {
+                    if (qd > wq) {
+                        zero_block(qd);
+                        zero_block(qd + 1);
+                    } else if (qd + 1 > wq) {
+                        uint32_t r0[32];
+                        tmem_ld32(tP + 32 * qd, r0);
+                        tmem_wait_ld();
+                        split_block(r0, qd);
+                        zero_block(qd + 1);
+                    } else {
+                        uint32_t r0[32], r1[32];
+                        tmem_ld32(tP + 32 * qd, r0);
+                        tmem_ld32(tP + 32 * (qd + 1), r1);
+                        tmem_wait_ld();
+                        split_block(r0, qd);
+                        split_block(r1, qd + 1);
+                    }
                 }
             }
             tmem_wait_st();
@@ -744,13 +1114,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarOFull0 + ob], (n >> 1) & 1, p.status)))
                 break;
             tc_fence_after();
+            // A whole stored chunk leaves through the V tile (free once its P V
+            // product is done) and one TMA tensor store; rows of sub-chunk items
+            // are stored directly.
+            const bool store_item = (it.flags & kItemStore) != 0;
+            const bool staged = store_item && it.r0 == 0 && it.r1 == kChunk;
             {
-                // A whole stored chunk leaves through the V tile (free once its
-                // P V product is done) and one TMA tensor store; rows of
-                // sub-chunk items are stored directly.
                 const uint32_t tO = tmem + lane_base + (ob ? TM::kO1 : TM::kO0);
-                const bool store_item = (it.flags & kItemStore) != 0;
-                const bool staged = store_item && it.r0 == 0 && it.r1 == kChunk;
                 const int t = it.t0 + i;
                 const bool st = store_item && !staged && i >= it.r0 && i < it.r1 && t < T;
                 __nv_bfloat16 *orow = p.o + (static_cast<size_t>(bh) * T + t) * p.dv + dv0;
@@ -779,18 +1149,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                     }
                 }
                 if (staged) {
+                    // the TMA thread stores the tile and then frees the V tile
                     fence_proxy_async_smem();
+                    if (tid == 32 * kTmemWarp0) sStore[n_staged & 1].t0 = it.t0;
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bars[kBarStage]);
-                    if (tid == 32 * kTmemWarp0) {
-                        if (mbar_wait_bounded(&bars[kBarStage], n_staged & 1, p.status)) {
-#pragma unroll
-                            for (int nb = 0; nb < DVT / 64; ++nb)
-                                tma_store_3d(&p.tm_o, sV + nb * kBlk, dv0 + nb * 64, it.t0, bh);
-                            tma_store_commit();
-                            tma_store_wait_read_all();
-                        }
-                    }
                     ++n_staged;
                 }
             }
@@ -798,9 +1161,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[kBarOFree0 + ob]);
             // the chunk's V tile may be refilled once its last item is done
-            if ((it.flags & kItemLast) && tid == 32 * kTmemWarp0) mbar_arrive(&bars[kBarVEmpty]);
+            if ((it.flags & kItemLast) && !staged && tid == 32 * kTmemWarp0)
+                mbar_arrive(&bars[kBarVEmpty]);
         }
-        if (tid == 32 * kTmemWarp0) tma_store_wait_all();
+        // end of the staged-store stream: its own barrier, since a phase of
+        // kBarStage completing right after the last stage could go unseen
+        if (tid == 32 * kTmemWarp0) sStore[0].count = n_staged;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kBarStageEnd]);
         // ---- final state of a FULL pass
         if (p.mode == kModeFull && has_state_row) {
             float *dst = nullptr;
@@ -832,12 +1200,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
         tc_fence_after();
         tmem_dealloc(tmem, TM::kCols);
     }
+    // the peer may still copy into, or arrive on, this CTA's shared memory
+    if constexpr (PAIR) cluster_sync_all();
 }
 
-template <int DK, int DVT>
+template <int DK, int DVT, bool PAIR>
 int launch_tiles(const ChunkLaunch &c, cudaStream_t stream) {
-    using L = Smem<DK, DVT>;
-    auto kern = chunk_fwd_kernel<DK, DVT>;
+    using L = Smem<DK, DVT, PAIR>;
+    auto kern = chunk_fwd_kernel<DK, DVT, PAIR>;
     static bool attr_set = false;  // per instantiation, per process
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -868,24 +1238,42 @@ int launch_tiles(const ChunkLaunch &c, cudaStream_t stream) {
     p.force_sub = c.force_exact;
     p.status = c.status;
     const int n_dvt = c.dv / DVT;
-    p.mode = kModeFull;
-    kern<<<dim3(n_dvt, c.H, c.B * c.n_seg), kThreads, L::kAlloc, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
+    auto launch = [&](int mode, int z) -> cudaError_t {
+        p.mode = mode;
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        cfg.gridDim = dim3(n_dvt, c.H, z);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = L::kAlloc;
+        cfg.stream = stream;
+        if (PAIR) {
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;   // the two value-column tiles of one head
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+        }
+        return cudaLaunchKernelEx(&cfg, kern, p);
+    };
+    cudaError_t e = launch(kModeFull, c.B * c.n_seg);
     if (e != cudaSuccess || c.n_seg == 1) return static_cast<int>(e);
-    p.mode = kModeCorrect;
-    kern<<<dim3(n_dvt, c.H, c.B * (c.n_seg - 1)), kThreads, L::kAlloc, stream>>>(p);
-    return static_cast<int>(cudaGetLastError());
+    return static_cast<int>(launch(kModeCorrect, c.B * (c.n_seg - 1)));
 }
 
 }  // namespace
 
 int launch_chunk_fwd(const ChunkLaunch &p, cudaStream_t stream) {
     if (p.dk == 64) {
-        if (p.dv_tile == 64) return launch_tiles<64, 64>(p, stream);
-        if (p.dv_tile == 128) return launch_tiles<64, 128>(p, stream);
+        if (p.dv_tile == 64) return launch_tiles<64, 64, false>(p, stream);
+        if (p.dv_tile == 128) return launch_tiles<64, 128, false>(p, stream);
+    } else if (p.dk == 128 && p.pair) {
+        if (p.dv != 2 * p.dv_tile) return static_cast<int>(cudaErrorInvalidValue);
+        if (p.dv_tile == 64) return launch_tiles<128, 64, true>(p, stream);
+        if (p.dv_tile == 128) return launch_tiles<128, 128, true>(p, stream);
     } else if (p.dk == 128) {
-        if (p.dv_tile == 64) return launch_tiles<128, 64>(p, stream);
-        if (p.dv_tile == 128) return launch_tiles<128, 128>(p, stream);
+        if (p.dv_tile == 64) return launch_tiles<128, 64, false>(p, stream);
+        if (p.dv_tile == 128) return launch_tiles<128, 128, false>(p, stream);
     }
     return static_cast<int>(cudaErrorInvalidValue);
 }

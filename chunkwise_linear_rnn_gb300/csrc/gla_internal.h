@@ -24,6 +24,7 @@ struct ChunkLaunch {
     float scale;
     int B, H, T, dk, dv;
     int dv_tile;              // 64 or 128
+    int pair;                 // 1: the two value tiles of a head run as a 2-CTA cluster
     int n_seg, seg_chunks;    // sequence segments and chunks per segment
     int force_exact;          // process every chunk in rescaled sub-chunks
     unsigned int *status;     // device status word

@@ -56,6 +56,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return done != 0;
 }
 
+// Non-blocking test of a phase (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
 // try_wait that lets the hardware suspend the thread for up to `hint_ns`
 // nanoseconds (or until the phase completes) instead of returning at once.
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity,
@@ -137,6 +150,41 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ----------------------------------------------------------------- clusters
+
+// This CTA's rank inside its thread-block cluster.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// The shared::cluster address of the same shared-memory offset in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+// Copy `bytes` (multiple of 16, both addresses 16-byte aligned) from this
+// CTA's shared memory into another CTA's (dst and bar are shared::cluster
+// addresses from mapa_shared); completes as transaction bytes on that CTA's
+// mbarrier.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, const void *src,
+                                                  uint32_t bytes, uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst_cluster),
+        "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
+        : "memory");
+}
+
+// Every thread of every CTA of the cluster (aligned: whole warps).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+
 // ----------------------------------------------------------------- tcgen05
 
 // Allocate `ncols` TMEM columns (power of two >= 32); one full warp executes.
@@ -212,6 +260,16 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_u32(bar))
+        : "memory");
+}
+
+// As mma_commit, but arrives on the mbarrier at the same shared-memory offset
+// in every CTA of the cluster whose rank bit is set in `cta_mask`.
+__device__ __forceinline__ void mma_commit_multicast(uint64_t *bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)),
+        "h"(cta_mask)
         : "memory");
 }
 

@@ -86,7 +86,10 @@ typedef struct gla_chunk_options {
     int segments;      /* sequence segments per (batch, head); 0 = automatic, 1 = no split */
     int dv_tile;       /* value columns per CTA: 0 = automatic, else 64 or 128             */
     int force_exact;   /* 1 = process every chunk as rescaled sub-chunks (test knob)          */
-    int reserved[5];
+    int cta_pair;      /* dk = 128 with two value-column tiles: 0 = run the tiles of a head as
+                          a 2-CTA cluster sharing the key-side preparation (default),
+                          -1 = independent CTAs; other values are GLA_ERR_ARG              */
+    int reserved[4];
 } gla_chunk_options;
 
 /* gla_chunk_fwd with explicit options (opts may be NULL = all automatic). */

@@ -182,6 +182,65 @@ def test_split_sequence_equals_one_call():
     assert_close(o.float().cpu().numpy(), ref_o, "whole o", bf16_output=True)
 
 
+# ---- CTA pairs: dk = 128 with two value-column tiles (dv = 256, or dv = 128 at
+# tile 64) runs each head's tiles as a 2-CTA cluster that splits the key-side
+# preparation between them.  Each case is checked against the oracle, with and
+# without pairs.
+
+@pytest.mark.parametrize("cta_pair", [0, -1])
+@pytest.mark.parametrize("dv,dv_tile,T", [(256, 0, 300), (256, 128, 129), (128, 64, 513),
+                                          (256, 0, 1)])
+def test_cta_pair_matches_oracle(dv, dv_tile, T, cta_pair):
+    q, k, v, a, h0 = _inputs(2, 2, T, 128, dv, h0=True, seed=40 + T + dv)
+    _run_and_check(q, k, v, a, h0, f"pair={cta_pair} dv={dv} tile={dv_tile} T={T}",
+                   dv_tile=dv_tile, cta_pair=cta_pair)
+
+
+def test_cta_pair_one_half_breaks_the_bound():
+    # gate spikes only in key channels 0-63 (the first CTA's half) and only in
+    # channels 64-127 in a later chunk: both CTAs must take the sub-chunk path
+    q, k, v, a, h0 = _inputs(1, 2, 520, 128, 256, h0=True, seed=41)
+    a[..., 10, 0:64] = -80.0
+    a[..., 300:310, 100] = -40.0
+    _run_and_check(q, k, v, a, h0, "pair spikes")
+
+
+def test_cta_pair_forced_sub_chunks():
+    q, k, v, a, h0 = _inputs(1, 2, 300, 128, 256, h0=True, seed=42, sigma_z=2.0)
+    _run_and_check(q, k, v, a, h0, "pair force_exact", force_exact=True)
+
+
+@pytest.mark.parametrize("segments", [2, 4])
+def test_cta_pair_segments(segments):
+    q, k, v, a, h0 = _inputs(1, 2, 2300, 128, 256, h0=True, seed=43 + segments)
+    _run_and_check(q, k, v, a, h0, f"pair segments={segments}", segments=segments)
+
+
+def test_cta_pair_segments_without_decay():
+    # alpha = 1 in every channel: the correction window spans whole segments
+    q, k, v, a, h0 = _inputs(1, 1, 1100, 128, 256, h0=True, seed=45)
+    a = torch.zeros_like(a)
+    _run_and_check(q, k, v, a, h0, "pair alpha=1 segments=3", segments=3)
+
+
+def test_cta_pair_window_closes_in_one_half_first():
+    # channels 64-127 decay fast, channels 0-63 slowly: the window stays open
+    # until the slow half has decayed too, a decision both CTAs must share
+    q, k, v, a, h0 = _inputs(1, 1, 2600, 128, 256, h0=True, seed=46)
+    a[..., 0:64] = -0.002
+    a[..., 64:128] = -0.5
+    _run_and_check(q, k, v, a, h0, "pair split window", segments=3)
+
+
+def test_cta_pair_aliased_state():
+    q, k, v, a, h0 = _inputs(2, 1, 700, 128, 256, h0=True, seed=47)
+    h = h0.clone()
+    o_ref, h_ref = _oracle(q, k, v, a, 128 ** -0.5, h0)
+    o, hT = gla.gla_chunk_fwd(q, k, v, a, None, h, final_state=h, segments=2)
+    assert_close(o.float().cpu().numpy(), o_ref, "pair aliased o", bf16_output=True)
+    assert_close(h.cpu().numpy(), h_ref, "pair aliased hT")
+
+
 def test_medium_config_all_heads():
     cfg = CHUNK_CONFIGS["medium"]
     q, k, v, a, h0 = make_config_inputs(cfg, device=DEV)

@@ -97,6 +97,18 @@ def test_chunk_rejects_bad_options(lib):
     assert _chunk(lib, opts=ctypes.byref(_lib.GlaChunkOptions(dv_tile=96))) == _lib.GLA_ERR_ARG
     assert _chunk(lib, opts=ctypes.byref(_lib.GlaChunkOptions(dv_tile=128)), dv=64) == _lib.GLA_ERR_ARG
     assert _chunk(lib, opts=ctypes.byref(_lib.GlaChunkOptions(segments=-1))) == _lib.GLA_ERR_ARG
+    assert _chunk(lib, opts=ctypes.byref(_lib.GlaChunkOptions(cta_pair=2))) == _lib.GLA_ERR_ARG
+    assert _chunk(lib, opts=ctypes.byref(_lib.GlaChunkOptions(cta_pair=-2))) == _lib.GLA_ERR_ARG
+
+
+def test_options_struct_matches_the_header(lib):
+    text = open(HEADER).read()
+    body = text[text.index("typedef struct gla_chunk_options"):text.index("} gla_chunk_options;")]
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = re.findall(r"int\s+(\w+)(?:\[(\d+)\])?;", body)
+    ours = [(n, str(t._length_) if hasattr(t, "_length_") else "")
+            for n, t in _lib.GlaChunkOptions._fields_]
+    assert fields == ours
 
 
 def test_step_validation(lib):
