@@ -85,8 +85,10 @@ constexpr int kItemEnd = 4;    // end of the item stream
 
 constexpr int kModeFull = 0, kModeCorrect = 1;
 
+// One MMA work item: chunk start t0, token rows [r0, r1), flags, chunk
+// counter lc, and (CTA pair) the index of the operand exchange it needs, or -1.
 struct ItemInfo {
-    int t0, r0, r1, flags, lc, pad[3];
+    int t0, r0, r1, flags, lc, xi, pad[2];
 };
 
 struct ChunkReq {
@@ -102,18 +104,12 @@ struct StoreRec {
 enum Bar {
     kBarQkFull = 0, kBarQkEmpty, kBarItem, kBarPFull, kBarPSplit, kBarSDone, kBarSReady,
     kBarOFull0, kBarOFull1, kBarOFree0, kBarOFree1, kBarVFull, kBarVEmpty, kBarAFull,
-    kBarQkRaw, kBarReq, kBarStage, kBarXchg, kBarStageEnd, kNumBars
+    kBarQkRaw, kBarReq, kBarStage, kBarStageEnd, kBarXchg0, kBarXchg1, kBarVerd0, kBarVerd1,
+    kNumBars
 };
 // arrival counts, in enum order (a CTA pair doubles kBarQkEmpty: both MMAs commit to it)
 __device__ constexpr uint32_t kBarCounts[kNumBars] = {kPrepWarps, 1, 1, 1, 4, 1, 4, 1, 1, 4, 4,
-                                                      1, 1, 1, 1, 1, 4, 1, 4};
-
-// What one CTA of a pair sends its peer each chunk besides its three operand
-// blocks: the chunk-end Gamma of its key channels and its exponent-bound verdict.
-struct PairMeta {
-    float gam[64];
-    int bad, pad[3];
-};
+                                                      1, 1, 1, 1, 1, 4, 4, 1, 1, 1, 1};
 
 template <int DK, int DVT, bool PAIR>
 struct Smem {
@@ -135,9 +131,8 @@ struct Smem {
     static constexpr uint32_t kItem = kG + 2 * DK * 4;    // ItemInfo[2]
     static constexpr uint32_t kReq = kItem + 64;          // ChunkReq
     static constexpr uint32_t kStore = kReq + 16;         // StoreRec[2]: staged output tiles
-    static constexpr uint32_t kMeta = kStore + 16;        // pair: PairMeta[2], by CTA rank
-    static constexpr uint32_t kMetaBytes = PAIR ? 2 * sizeof(PairMeta) : 0;
-    static constexpr uint32_t kBar = kMeta + kMetaBytes;  // mbarriers
+    static constexpr uint32_t kVerd = kStore + 16;        // pair: the peer's verdicts [2]
+    static constexpr uint32_t kBar = kVerd + (PAIR ? 16 : 0);  // mbarriers
     static constexpr uint32_t kMisc = kBar + 8 * kNumBars;  // tmem slot
     static constexpr uint32_t kTotal = kMisc + 16;
     // At least 120 KB so that only one CTA fits on an SM: each CTA allocates
@@ -145,7 +140,7 @@ struct Smem {
     static constexpr uint32_t kAlloc = (kTotal + 1024) > 122880u ? (kTotal + 1024) : 122880u;
     static_assert(kAlloc <= 232448, "shared memory budget exceeded");
     static_assert(!PAIR || DK == 128, "CTA pairs split 128 key channels into two 64-channel blocks");
-    static_assert(kMeta % 16 == 0 && sizeof(PairMeta) % 16 == 0, "bulk copies move 16-byte units");
+    static_assert(kG % 16 == 0, "bulk copies move 16-byte units");
 };
 
 // TMEM columns: P [0,128) (fp32 scores, then the bf16 hi/lo pair in place),
@@ -318,7 +313,7 @@ __device__ __forceinline__ bool sub_chunk_items(const KParams &p, int bh, int t0
         if (pt == 0) {
             sItem[n & 1] = ItemInfo{
                 t0, sa, sb, (sidx == n_sub - 1 ? kItemLast : 0) | (store ? kItemStore : 0), lc,
-                {0, 0, 0}};
+                -1, {0, 0}};
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -330,23 +325,27 @@ __device__ __forceinline__ bool sub_chunk_items(const KParams &p, int bh, int t0
 
 // Prep warps of one CTA of a pair.  The CTA owns key channels
 // [64 rank, 64 rank + 64): 32 channel pairs x 8 token parts of 16 tokens.
-// Per chunk:
+// Per chunk c:
 //   1. phase A on the A half tile: in-chunk prefix sums in place, part
-//      offsets, the exponent-bound verdict for these channels;
+//      offsets, and the exponent-bound verdict for these channels, which is
+//      sent to the peer at once (one remote word);
 //   2. phase B into registers from the raw Q and K staging tiles (Qh, Kh_hi,
-//      Kh_lo for 16 tokens x 2 channels); after it the A and staging tiles are
-//      free and the next chunk is requested, so its loads overlap this
-//      chunk's products;
-//   3. once both CTAs' MMAs have released the previous item's operand tiles,
-//      the registers go to this CTA's 64-channel block of the Qh, Kh_hi and
-//      Kh_lo tiles, and the three blocks plus a PairMeta record are copied
-//      into the peer's shared memory at the same offsets;
-//   4. after the peer's copy has landed here: if neither CTA's channels broke
-//      the exponent bound, the chunk is one item; otherwise both CTAs run the
-//      sub-chunk path over all channels on their own (same inputs, same items).
+//      Kh_lo for 16 tokens x 2 channels); the A and staging tiles are then
+//      free and chunk c+1 is requested, so its loads overlap this chunk;
+//   3. the segment decay of every channel through chunk c-1, from the state
+//      factors of the previous exchange, and the window decision for chunk c;
+//   4. if neither CTA's channels broke the bound: once both CTAs' MMAs have
+//      released the operand tiles, the registers go to this CTA's 64-channel
+//      block of the Qh, Kh_hi and Kh_lo tiles, its half of the state factors
+//      e^Gamma_C to the factor table, and all four are copied into the
+//      peer's shared memory at the same offsets.  The item is published at
+//      once; the MMA issuer (and the TMEM warps, for the factors) wait for the
+//      peer's copy themselves, so the prep warps go on to chunk c+1.
+//      Otherwise both CTAs run the sub-chunk path over all channels on their
+//      own (same inputs, same items).
 // Threads pt < DK keep the decay since the segment start of channel pt; both
-// CTAs compute it identically (from the exchanged chunk-end Gammas, or from
-// the raw gates), so their window decisions agree.
+// CTAs compute it from identical bits (the exchanged factor table, or the raw
+// gates), so their window decisions agree.
 template <int DK, int DVT>
 __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint32_t rank, int bh,
                                           int seg, int c_begin, int c_end, size_t BHn,
@@ -356,7 +355,7 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
     constexpr int NP = DKH / 2;                 // channel pairs
     constexpr int NQ = kPrepThreads / NP;       // token parts
     constexpr int TP = kChunk / NQ;             // tokens per part
-    constexpr uint32_t kXchgBytes = 3u * kBlk + static_cast<uint32_t>(sizeof(PairMeta));
+    constexpr uint32_t kXchgBytes = 3u * kBlk + DKH * 4u;
     uint8_t *sQ = smem + L::kQ;
     uint8_t *sK = smem + L::kK;
     uint8_t *sKlo = smem + L::kKlo;
@@ -366,7 +365,7 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
     float *sG = reinterpret_cast<float *>(smem + L::kG);
     ItemInfo *sItem = reinterpret_cast<ItemInfo *>(smem + L::kItem);
     ChunkReq *sReq = reinterpret_cast<ChunkReq *>(smem + L::kReq);
-    PairMeta *meta = reinterpret_cast<PairMeta *>(smem + L::kMeta);
+    uint32_t *sVerd = reinterpret_cast<uint32_t *>(smem + L::kVerd);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBar);
 
     const int pt = threadIdx.x;
@@ -381,159 +380,190 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
 
     float gseg = 0.f;                            // threads pt < DK: channel pt
     bool closed = (p.mode == kModeFull && seg == 0);
-    int n = 0;
+    int n = 0;                                   // items published
+    int nx = 0;                                  // operand exchanges made
+    int used = 0;                                // chunks published
     bool ok = true;
-    bool requested = false, end_posted = false;
-    auto post = [&](int c) {                     // request the loads of chunk c (or the end)
-        const bool e = c >= c_end;
-        if (pt == 0) {
-            sReq[0] = ChunkReq{e ? -1 : c * kChunk, 0, e ? 1 : 0, 0};
-            mbar_arrive(&bars[kBarReq]);
-        }
-        requested = !e;
-        end_posted = e;
-    };
-    post(c_begin);
+    bool pend = false;                           // last exchange's factors not yet read
+    bool prepped_last = false;                   // the last chunk prepared was not used
+    bool spec = false;                           // chunk lc_last + 1 requested, A not yet landed
+    int lc_last = 0;
+    if (pt == 0) {
+        const bool e = c_begin >= c_end;
+        sReq[0] = ChunkReq{e ? 0 : c_begin * kChunk, 0, e ? 1 : 0, 0};
+        mbar_arrive(&bars[kBarReq]);
+    }
+    bool end_posted = c_begin >= c_end;
     // A wait that expires clears `ok` in its thread only: every thread still
     // runs the same sequence of barriers (each wait is bounded), and the loop
     // ends at the next chunk boundary, where the threads' verdicts are combined.
     for (int c = c_begin, lc = 0;; ++c, ++lc) {
+        ok = !bar_or(4, kPrepThreads, !ok);
+        const bool have = c < c_end && ok;
+        const int t0 = c * kChunk;
+        uint32_t rq[TP], rh[TP], rl[TP];
+        float gc0 = 0.f, gc1 = 0.f;
+        bool bad_here = false;
+        if (have) {
+            // ---- phase A: prefix sums of this thread's part, in place
+            if (pt == 0) mbar_arrive_expect_tx(&bars[kBarVerd0 + (lc & 1)], 4u);
+            ok &= mbar_wait_bounded(&bars[kBarAFull], lc & 1, p.status);
+            spec = false;
+            float c0 = 0.f, c1 = 0.f;
+            float lmn = 3.0e38f, lmx = -3.0e38f;
+            {
+                float2 av[TP];
+#pragma unroll
+                for (int e = 0; e < TP; ++e)
+                    av[e] = *reinterpret_cast<const float2 *>(sAc + (part * TP + e) * DKH);
+#pragma unroll
+                for (int e = 0; e < TP; ++e) {
+                    c0 += av[e].x;
+                    c1 += av[e].y;
+                    lmn = fminf(lmn, fminf(c0, c1));
+                    lmx = fmaxf(lmx, fmaxf(c0, c1));
+                    *reinterpret_cast<float2 *>(sA + chl + (part * TP + e) * DKH) =
+                        make_float2(c0, c1);
+                }
+            }
+            named_barrier(5, kPrepThreads);
+            float o0 = 0.f, o1 = 0.f;
+#pragma unroll
+            for (int qq = 0; qq < NQ - 1; ++qq) {
+                if (qq < part) {
+                    const float2 tt =
+                        *reinterpret_cast<const float2 *>(sAc + (qq * TP + TP - 1) * DKH);
+                    o0 += tt.x;
+                    o1 += tt.y;
+                }
+            }
+            const float gmin = fminf(o0, o1) + lmn, gmax = fmaxf(o0, o1) + lmx;
+            bad_here = bar_or(2, kPrepThreads,
+                              fmaxf(-fminf(gmin, 0.f), fmaxf(gmax, 0.f)) > kExpBound ||
+                                  p.force_sub != 0);
+            if (pt == 0) {
+                const uint32_t dst = mapa_shared(smem_u32(&sVerd[lc & 1]), peer);
+                const uint32_t pbar = mapa_shared(smem_u32(&bars[kBarVerd0 + (lc & 1)]), peer);
+                st_async_to_peer(dst, bad_here ? 1u : 0u, pbar);
+            }
+            // ---- phase B into registers (values of a chunk that broke the
+            // bound are computed but never used)
+            ok &= mbar_wait_bounded(&bars[kBarQkRaw], lc & 1, p.status);
+#pragma unroll
+            for (int e = 0; e < TP; ++e) {
+                const int i = part * TP + e;
+                const uint32_t off = sw128_offset(i, chl, kBlk);
+                const float2 a = *reinterpret_cast<const float2 *>(sAc + i * DKH);
+                const float2 qf = unpack_bf16x2(*reinterpret_cast<const uint32_t *>(sRawQ + off));
+                const float2 kf = unpack_bf16x2(*reinterpret_cast<const uint32_t *>(sRawK + off));
+                const float g0 = o0 + a.x, g1 = o1 + a.y;
+                rq[e] = bf16x2_bits(qf.x * __expf(g0), qf.y * __expf(g1));
+                split_pair(kf.x * __expf(-g0), kf.y * __expf(-g1), rh[e], rl[e]);
+            }
+            gc0 = o0 + c0;                       // Gamma at the chunk end (last part)
+            gc1 = o1 + c1;
+            // the A and staging tiles are consumed: start the next chunk's loads
+            named_barrier(5, kPrepThreads);
+            if (c + 1 < c_end) {
+                if (pt == 0) {
+                    sReq[0] = ChunkReq{(c + 1) * kChunk, 0, 0, 0};
+                    mbar_arrive(&bars[kBarReq]);
+                }
+                spec = true;   // taken by the TMA thread once A(c+1) has landed
+            }
+            prepped_last = true;
+            lc_last = lc;
+        }
+        // ---- segment decay through chunk c-1 (the previous exchange's factors)
+        if (pend) {
+            const int x = nx - 1;
+            ok &= mbar_wait_bounded(&bars[kBarXchg0 + (x & 1)], (x >> 1) & 1, p.status);
+            if (pt < DK) gseg += __logf(sG[((n - 1) & 1) * DK + pt]);
+            pend = false;
+        }
         // ---- end of the segment, or (correction pass) of the decay window
         const bool win = !closed && pt < DK && gseg > -kWindowCut;
         const bool any_win = bar_or(1, kPrepThreads, win);
         if (!closed && !any_win) closed = true;
-        ok = !bar_or(4, kPrepThreads, !ok);
-        const bool end = c >= c_end || !ok || (p.mode == kModeCorrect && closed);
-        if (end) {
-            if (requested && ok) {
-                // a speculative request for this chunk is in flight: let it land
-                bool okw = mbar_wait_bounded(&bars[kBarAFull], lc & 1, p.status);
-                okw &= mbar_wait_bounded(&bars[kBarQkRaw], lc & 1, p.status);
-                okw &= mbar_wait_bounded(&bars[kBarVFull], lc & 1, p.status);
-                ok = !bar_or(4, kPrepThreads, !okw);
-            }
-            break;
-        }
-        const int t0 = c * kChunk;
+        if (!have || (p.mode == kModeCorrect && closed)) break;
         const bool store = p.mode == kModeCorrect || closed;
-        // ---- phase A: prefix sums of this thread's part, in place
-        ok &= mbar_wait_bounded(&bars[kBarAFull], lc & 1, p.status);
-        float c0 = 0.f, c1 = 0.f;
-        float lmn = 3.0e38f, lmx = -3.0e38f;
-        {
-            float2 av[TP];
-#pragma unroll
-            for (int e = 0; e < TP; ++e)
-                av[e] = *reinterpret_cast<const float2 *>(sAc + (part * TP + e) * DKH);
+        // ---- both CTAs' verdicts: one branch for all threads, even for one
+        // whose wait expired
+        ok &= mbar_wait_bounded(&bars[kBarVerd0 + (lc & 1)], (lc >> 1) & 1, p.status);
+        const bool bad = bar_or(2, kPrepThreads, bad_here || sVerd[lc & 1] != 0u);
+        prepped_last = false;
+        ++used;
+        if (!bad) {
+            // ---- both CTAs' MMAs are done with the previous item's tiles
+            if (n > 0) ok &= mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status);
 #pragma unroll
             for (int e = 0; e < TP; ++e) {
-                c0 += av[e].x;
-                c1 += av[e].y;
-                lmn = fminf(lmn, fminf(c0, c1));
-                lmx = fmaxf(lmx, fmaxf(c0, c1));
-                *reinterpret_cast<float2 *>(sA + chl + (part * TP + e) * DKH) = make_float2(c0, c1);
+                const uint32_t off = sw128_offset(part * TP + e, ch, kBlk);
+                *reinterpret_cast<uint32_t *>(sQ + off) = rq[e];
+                *reinterpret_cast<uint32_t *>(sK + off) = rh[e];
+                *reinterpret_cast<uint32_t *>(sKlo + off) = rl[e];
             }
-        }
-        named_barrier(5, kPrepThreads);
-        float o0 = 0.f, o1 = 0.f;
-#pragma unroll
-        for (int qq = 0; qq < NQ - 1; ++qq) {
-            if (qq < part) {
-                const float2 tt = *reinterpret_cast<const float2 *>(sAc + (qq * TP + TP - 1) * DKH);
-                o0 += tt.x;
-                o1 += tt.y;
+            if (last_part) {
+                sG[(n & 1) * DK + ch] = __expf(gc0);
+                sG[(n & 1) * DK + ch + 1] = __expf(gc1);
             }
-        }
-        const float gmin = fminf(o0, o1) + lmn, gmax = fmaxf(o0, o1) + lmx;
-        const bool bad_mine =
-            fmaxf(-fminf(gmin, 0.f), fmaxf(gmax, 0.f)) > kExpBound || p.force_sub != 0;
-        // ---- phase B into registers (values of a chunk that broke the bound
-        // are computed but never used)
-        ok &= mbar_wait_bounded(&bars[kBarQkRaw], lc & 1, p.status);
-        uint32_t rq[TP], rh[TP], rl[TP];
-#pragma unroll
-        for (int e = 0; e < TP; ++e) {
-            const int i = part * TP + e;
-            const uint32_t off = sw128_offset(i, chl, kBlk);
-            const float2 a = *reinterpret_cast<const float2 *>(sAc + i * DKH);
-            const float2 qf = unpack_bf16x2(*reinterpret_cast<const uint32_t *>(sRawQ + off));
-            const float2 kf = unpack_bf16x2(*reinterpret_cast<const uint32_t *>(sRawK + off));
-            const float g0 = o0 + a.x, g1 = o1 + a.y;
-            rq[e] = bf16x2_bits(qf.x * __expf(g0), qf.y * __expf(g1));
-            split_pair(kf.x * __expf(-g0), kf.y * __expf(-g1), rh[e], rl[e]);
-        }
-        const float gc0 = o0 + c0, gc1 = o1 + c1;   // Gamma at the chunk end (last part)
-        // the A and staging tiles are consumed: start the next chunk's loads
-        named_barrier(5, kPrepThreads);
-        post(c + 1);
-        // ---- both CTAs' MMAs are done with the previous item's tiles
-        if (n > 0) ok &= mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status);
-#pragma unroll
-        for (int e = 0; e < TP; ++e) {
-            const uint32_t off = sw128_offset(part * TP + e, ch, kBlk);
-            *reinterpret_cast<uint32_t *>(sQ + off) = rq[e];
-            *reinterpret_cast<uint32_t *>(sK + off) = rh[e];
-            *reinterpret_cast<uint32_t *>(sKlo + off) = rl[e];
-        }
-        if (last_part) {
-            meta[rank].gam[chl] = gc0;
-            meta[rank].gam[chl + 1] = gc1;
-        }
-        fence_proxy_async_smem();
-        // all blocks written; one exponent-bound verdict for this CTA's channels
-        const bool bad_here = bar_or(2, kPrepThreads, bad_mine);
-        if (pt == 0) {
-            meta[rank].bad = bad_here ? 1 : 0;
             fence_proxy_async_smem();
-            mbar_arrive_expect_tx(&bars[kBarXchg], kXchgBytes);
-            const uint32_t pbar = mapa_shared(smem_u32(&bars[kBarXchg]), peer);
-            const uint32_t blk = rank * kBlk;
-            bulk_copy_to_peer(mapa_shared(smem_u32(sQ + blk), peer), sQ + blk, kBlk, pbar);
-            bulk_copy_to_peer(mapa_shared(smem_u32(sK + blk), peer), sK + blk, kBlk, pbar);
-            bulk_copy_to_peer(mapa_shared(smem_u32(sKlo + blk), peer), sKlo + blk, kBlk, pbar);
-            bulk_copy_to_peer(mapa_shared(smem_u32(&meta[rank]), peer), &meta[rank],
-                              static_cast<uint32_t>(sizeof(PairMeta)), pbar);
-        }
-        // ---- the peer's blocks and record have landed here
-        ok &= mbar_wait_bounded(&bars[kBarXchg], lc & 1, p.status);
-        // one branch for all threads, even for one whose wait expired
-        const bool bad = bar_or(2, kPrepThreads, (meta[0].bad | meta[1].bad) != 0);
-        if (!bad) {
-            if (pt < DK) {
-                const float g = meta[pt / DKH].gam[pt % DKH];
-                gseg += g;
-                sG[(n & 1) * DK + pt] = __expf(g);
-            }
+            named_barrier(5, kPrepThreads);
             if (pt == 0) {
-                sItem[n & 1] = ItemInfo{t0, 0, kChunk, kItemLast | (store ? kItemStore : 0), lc,
-                                        {0, 0, 0}};
+                sItem[n & 1] = ItemInfo{t0, 0, kChunk, kItemLast | (store ? kItemStore : 0), lc, nx,
+                                        {0, 0}};
+                mbar_arrive_expect_tx(&bars[kBarXchg0 + (nx & 1)], kXchgBytes);
+                const uint32_t pbar = mapa_shared(smem_u32(&bars[kBarXchg0 + (nx & 1)]), peer);
+                const uint32_t blk = rank * kBlk;
+                float *g_own = sG + (n & 1) * DK + rank * DKH;
+                bulk_copy_to_peer(mapa_shared(smem_u32(sQ + blk), peer), sQ + blk, kBlk, pbar);
+                bulk_copy_to_peer(mapa_shared(smem_u32(sK + blk), peer), sK + blk, kBlk, pbar);
+                bulk_copy_to_peer(mapa_shared(smem_u32(sKlo + blk), peer), sKlo + blk, kBlk, pbar);
+                bulk_copy_to_peer(mapa_shared(smem_u32(g_own), peer), g_own, DKH * 4u, pbar);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[kBarQkFull]);
             ++n;
+            ++nx;
+            pend = true;
             continue;
         }
         // ---- a chunk whose decay breaks the bound: sub-chunk items over all
         // channels, computed by each CTA of the pair on its own
+        if (n > 0) ok &= mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status);
         float gt0 = 0.f, gt1 = 0.f;
         ok &= sub_chunk_items<DK>(p, bh, t0, lc, store, pt, sQ, sK, sKlo, sG, sItem, bars, n, gt0,
                                   gt1);
         if (pt < DK) {
             // the chunk's clamped decay of channel pt, summed in token order
-            const float *ab = reinterpret_cast<const float *>(p.a) + static_cast<size_t>(bh) * T * DK + pt;
+            const float *ab =
+                reinterpret_cast<const float *>(p.a) + static_cast<size_t>(bh) * T * DK + pt;
             float gsum = 0.f;
             for (int i = 0; i < kChunk && t0 + i < T; ++i)
                 gsum += clamp_gate(ab[static_cast<size_t>(t0 + i) * DK]);
             gseg += gsum;
         }
     }
-    // ---- end of the item stream (and of the load requests)
+    // ---- end of the item stream and of the load requests
+    if (pend) {
+        const int x = nx - 1;
+        ok &= mbar_wait_bounded(&bars[kBarXchg0 + (x & 1)], (x >> 1) & 1, p.status);
+        if (pt < DK) gseg += __logf(sG[((n - 1) & 1) * DK + pt]);
+    }
+    // the peer's verdict for a chunk prepared here but not used has to land
+    // before this CTA may exit
+    if (prepped_last) ok &= mbar_wait_bounded(&bars[kBarVerd0 + (lc_last & 1)], (lc_last >> 1) & 1, p.status);
+    // the request mailbox holds one request: the end may be posted only once
+    // the TMA thread has taken the last one (its A tile has landed)
+    if (spec) ok &= mbar_wait_bounded(&bars[kBarAFull], (lc_last + 1) & 1, p.status);
+    named_barrier(5, kPrepThreads);
     if (!end_posted && pt == 0) {
-        sReq[0] = ChunkReq{-1, 0, 1, 0};
+        // the count of chunks used, so that no V load waits for a tile never freed
+        sReq[0] = ChunkReq{used, 0, 1, 0};
         mbar_arrive(&bars[kBarReq]);
     }
     if (n > 0 && !mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status)) ok = false;
-    if (pt == 0) sItem[n & 1] = ItemInfo{0, 0, 0, kItemEnd, 0, {0, 0, 0}};
+    if (pt == 0) sItem[n & 1] = ItemInfo{0, 0, 0, kItemEnd, 0, -1, {0, 0}};
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars[kBarQkFull]);
     // segment summary: total decay of this segment (FULL mode, several segments)
@@ -738,7 +768,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                 }
                 if (pt == 0) {
                     sItem[n & 1] = ItemInfo{t0, 0, kChunk, kItemLast | (store ? kItemStore : 0), lc,
-                                            {0, 0, 0}};
+                                            -1, {0, 0}};
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -758,7 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
         }
         // ---- end of the item stream
         if (n > 0 && !mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status)) ok = false;
-        if (pt == 0) sItem[n & 1] = ItemInfo{0, 0, 0, kItemEnd, 0, {0, 0, 0}};
+        if (pt == 0) sItem[n & 1] = ItemInfo{0, 0, 0, kItemEnd, 0, -1, {0, 0}};
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kBarQkFull]);
         // segment summary: total decay of this segment (FULL mode, several segments)
@@ -778,6 +808,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
         if (lane == 0) {
             int n_req = 0, n_qk = 0, n_v = 0;   // chunks requested / Q,K issued / V issued
             int n_st = 0, st_total = -1;        // staged output tiles taken / in all
+            int n_use = 0;                      // chunks used (known at the end request)
             bool req_end = false;
             int t0s[4], firsts[4];              // at most 3 chunks are ever outstanding
             unsigned long long idle_since = 0;
@@ -787,7 +818,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                     const ChunkReq rq = sReq[0];
                     progress = true;
                     if (rq.end) {
+                        // a CTA pair requests one chunk ahead and says at the end
+                        // how many chunks were used: no V load for the others
                         req_end = true;
+                        n_use = PAIR ? rq.t0 : n_req;
                     } else {
                         const int t0 = rq.t0;
                         t0s[n_req & 3] = t0;
@@ -826,7 +860,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                     }
                 }
                 // V: after the previous chunk's products and output store
-                if (n_v < n_req && (n_v == 0 || mbar_test_wait(&bars[kBarVEmpty], (n_v - 1) & 1))) {
+                if (n_v < (req_end ? n_use : n_req) &&
+                    (n_v == 0 || mbar_test_wait(&bars[kBarVEmpty], (n_v - 1) & 1))) {
                     const int t0 = t0s[n_v & 3];
                     mbar_arrive_expect_tx(&bars[kBarVFull], L::kVBytes);
 #pragma unroll
@@ -852,7 +887,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                     st_total = sStore[0].count;
                     progress = true;
                 }
-                if (req_end && n_st == st_total && n_v == n_req && (PAIR || n_qk == n_req)) break;
+                if (req_end && n_st == st_total && n_v >= n_use && (PAIR || n_qk == n_req)) break;
                 if (progress) {
                     idle_since = 0;
                 } else {
@@ -866,6 +901,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                     __nanosleep(64);
                 }
             }
+            // loads issued for chunks that were never used must land before exit
+            // (the last phase of each barrier; no later phase follows)
+            if (n_req > 0) {
+                mbar_wait_bounded(&bars[kBarAFull], (n_req - 1) & 1, p.status);
+                if (PAIR) mbar_wait_bounded(&bars[kBarQkRaw], (n_req - 1) & 1, p.status);
+            }
+            if (n_v > 0) mbar_wait_bounded(&bars[kBarVFull], (n_v - 1) & 1, p.status);
             tma_store_wait_all();
         }
         __syncwarp();
@@ -885,6 +927,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                 const int ob = n & 1;
                 const uint32_t tO = tmem + (ob ? TM::kO1 : TM::kO0);
                 const uint32_t aV = aV0;
+                // a CTA pair's item: the peer's half of the operand tiles
+                if (it.xi >= 0 &&
+                    !mbar_wait_bounded(&bars[kBarXchg0 + (it.xi & 1)], (it.xi >> 1) & 1, p.status))
+                    break;
                 tc_fence_after();
                 // P = Qh (Kh_hi + Kh_lo)^T
 #pragma unroll
@@ -1083,6 +1129,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             if (lane == 0) mbar_arrive(&bars[kBarPSplit]);
             // ---- state: S <- diag(e^decay) S, and its bf16 copy for the next item
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarSDone], n & 1, p.status))) break;
+            // a CTA pair's item: the peer's half of the state factors
+            if (it.xi >= 0 &&
+                !__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarXchg0 + (it.xi & 1)],
+                                                           (it.xi >> 1) & 1, p.status)))
+                break;
             tc_fence_after();
             if (has_state_row) {
                 const float f = sG[(n & 1) * DK + i];

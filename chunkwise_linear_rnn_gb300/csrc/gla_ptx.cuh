@@ -179,6 +179,17 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, const vo
         : "memory");
 }
 
+// Store one 32-bit word into another CTA's shared memory (dst and bar are
+// shared::cluster addresses); completes as 4 transaction bytes on its mbarrier.
+__device__ __forceinline__ void st_async_to_peer(uint32_t dst_cluster, uint32_t value,
+                                                 uint32_t bar_cluster) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.u32 [%0], %1, [%2];" ::"r"(
+            dst_cluster),
+        "r"(value), "r"(bar_cluster)
+        : "memory");
+}
+
 // Every thread of every CTA of the cluster (aligned: whole warps).
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
