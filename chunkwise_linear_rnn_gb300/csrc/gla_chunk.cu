@@ -77,6 +77,11 @@ constexpr int kTmaWarp = 13;
 constexpr int kThreads = 448;           // 14 warps
 constexpr float kExpBound = 30.f;
 constexpr float kWindowCut = 41.58883083f;  // 60 ln 2
+// The fast path keeps in-chunk prefix sums in log2 units (Gamma log2 e), so
+// that every exponential is one ex2.
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kExpBound2 = kExpBound * kLog2e;
 constexpr uint32_t kBlk = kChunk * 128;     // one 64-column block of a 128-row tile
 
 constexpr int kItemLast = 1;   // last item of its chunk: releases the chunk's V stage
@@ -405,27 +410,26 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
         float gc0 = 0.f, gc1 = 0.f;
         bool bad_here = false;
         if (have) {
-            // ---- phase A: prefix sums of this thread's part, in place
+            // ---- phase A: prefix sums of this thread's part (log2 units) in
+            // registers; the part total goes to the A tile's last row of the part
             if (pt == 0) mbar_arrive_expect_tx(&bars[kBarVerd0 + (lc & 1)], 4u);
             ok &= mbar_wait_bounded(&bars[kBarAFull], lc & 1, p.status);
             spec = false;
             float c0 = 0.f, c1 = 0.f;
             float lmn = 3.0e38f, lmx = -3.0e38f;
-            {
-                float2 av[TP];
+            float2 av[TP];
 #pragma unroll
-                for (int e = 0; e < TP; ++e)
-                    av[e] = *reinterpret_cast<const float2 *>(sAc + (part * TP + e) * DKH);
+            for (int e = 0; e < TP; ++e)
+                av[e] = *reinterpret_cast<const float2 *>(sAc + (part * TP + e) * DKH);
 #pragma unroll
-                for (int e = 0; e < TP; ++e) {
-                    c0 += av[e].x;
-                    c1 += av[e].y;
-                    lmn = fminf(lmn, fminf(c0, c1));
-                    lmx = fmaxf(lmx, fmaxf(c0, c1));
-                    *reinterpret_cast<float2 *>(sA + chl + (part * TP + e) * DKH) =
-                        make_float2(c0, c1);
-                }
+            for (int e = 0; e < TP; ++e) {
+                c0 = fmaf(av[e].x, kLog2e, c0);
+                c1 = fmaf(av[e].y, kLog2e, c1);
+                av[e] = make_float2(c0, c1);
+                lmn = fminf(lmn, fminf(c0, c1));
+                lmx = fmaxf(lmx, fmaxf(c0, c1));
             }
+            *reinterpret_cast<float2 *>(sA + chl + (part * TP + TP - 1) * DKH) = make_float2(c0, c1);
             named_barrier(5, kPrepThreads);
             float o0 = 0.f, o1 = 0.f;
 #pragma unroll
@@ -439,7 +443,7 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
             }
             const float gmin = fminf(o0, o1) + lmn, gmax = fmaxf(o0, o1) + lmx;
             bad_here = bar_or(2, kPrepThreads,
-                              fmaxf(-fminf(gmin, 0.f), fmaxf(gmax, 0.f)) > kExpBound ||
+                              fmaxf(-fminf(gmin, 0.f), fmaxf(gmax, 0.f)) > kExpBound2 ||
                                   p.force_sub != 0);
             if (pt == 0) {
                 const uint32_t dst = mapa_shared(smem_u32(&sVerd[lc & 1]), peer);
@@ -453,14 +457,13 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
             for (int e = 0; e < TP; ++e) {
                 const int i = part * TP + e;
                 const uint32_t off = sw128_offset(i, chl, kBlk);
-                const float2 a = *reinterpret_cast<const float2 *>(sAc + i * DKH);
                 const float2 qf = unpack_bf16x2(*reinterpret_cast<const uint32_t *>(sRawQ + off));
                 const float2 kf = unpack_bf16x2(*reinterpret_cast<const uint32_t *>(sRawK + off));
-                const float g0 = o0 + a.x, g1 = o1 + a.y;
-                rq[e] = bf16x2_bits(qf.x * __expf(g0), qf.y * __expf(g1));
-                split_pair(kf.x * __expf(-g0), kf.y * __expf(-g1), rh[e], rl[e]);
+                const float g0 = o0 + av[e].x, g1 = o1 + av[e].y;
+                rq[e] = bf16x2_bits(qf.x * ex2f(g0), qf.y * ex2f(g1));
+                split_pair(kf.x * ex2f(-g0), kf.y * ex2f(-g1), rh[e], rl[e]);
             }
-            gc0 = o0 + c0;                       // Gamma at the chunk end (last part)
+            gc0 = o0 + c0;                       // Gamma log2 e at the chunk end (last part)
             gc1 = o1 + c1;
             // the A and staging tiles are consumed: start the next chunk's loads
             named_barrier(5, kPrepThreads);
@@ -504,8 +507,8 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
                 *reinterpret_cast<uint32_t *>(sKlo + off) = rl[e];
             }
             if (last_part) {
-                sG[(n & 1) * DK + ch] = __expf(gc0);
-                sG[(n & 1) * DK + ch + 1] = __expf(gc1);
+                sG[(n & 1) * DK + ch] = ex2f(gc0);
+                sG[(n & 1) * DK + ch + 1] = ex2f(gc1);
             }
             fence_proxy_async_smem();
             named_barrier(5, kPrepThreads);
@@ -688,8 +691,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                     }
 #pragma unroll
                     for (int e = 0; e < kB; ++e) {
-                        c0 += cur[e].x;
-                        c1 += cur[e].y;
+                        c0 = fmaf(cur[e].x, kLog2e, c0);   // log2 units
+                        c1 = fmaf(cur[e].y, kLog2e, c1);
                         lmn = fminf(lmn, fminf(c0, c1));
                         lmx = fmaxf(lmx, fmaxf(c0, c1));
                         *reinterpret_cast<float2 *>(const_cast<float *>(sAc) + (i0 + e) * DK) =
@@ -708,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             // Gamma_i = o + local_i; the fast path needs every |Gamma_i| <= kExpBound
             const float gmin = fminf(o0, o1) + lmn, gmax = fmaxf(o0, o1) + lmx;
             const bool bad = bar_or(2, kPrepThreads,
-                                    fmaxf(-fminf(gmin, 0.f), fmaxf(gmax, 0.f)) > kExpBound ||
+                                    fmaxf(-fminf(gmin, 0.f), fmaxf(gmax, 0.f)) > kExpBound2 ||
                                         p.force_sub != 0);
             okw = mbar_wait_bounded(&bars[kBarQkRaw], lc & 1, p.status);
             ok = !bar_or(4, kPrepThreads, !okw);
@@ -717,11 +720,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                 // ---- phase B (needs Q, K): Qh, Kh_hi in place, Kh_lo.  Purely
                 // elementwise; the next batch's loads precede this batch's stores.
                 if (last_part) {
-                    const float gc0 = o0 + c0, gc1 = o1 + c1;   // Gamma at the chunk end
-                    sG[(n & 1) * DK + ch] = __expf(gc0);
-                    sG[(n & 1) * DK + ch + 1] = __expf(gc1);
-                    gseg0 += gc0;
-                    gseg1 += gc1;
+                    const float gc0 = o0 + c0, gc1 = o1 + c1;   // Gamma log2 e at the chunk end
+                    sG[(n & 1) * DK + ch] = ex2f(gc0);
+                    sG[(n & 1) * DK + ch + 1] = ex2f(gc1);
+                    gseg0 += gc0 * kLn2;
+                    gseg1 += gc1 * kLn2;
                 }
                 float2 ab8[kB];
                 uint32_t qw8[kB], kw8[kB];
@@ -759,9 +762,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                         const float2 qf = unpack_bf16x2(cq[e]), kf = unpack_bf16x2(ck[e]);
                         const uint32_t off = sw128_offset(i, ch, kBlk);
                         *reinterpret_cast<uint32_t *>(sQ + off) =
-                            bf16x2_bits(qf.x * __expf(g0), qf.y * __expf(g1));
+                            bf16x2_bits(qf.x * ex2f(g0), qf.y * ex2f(g1));
                         uint32_t hi, lo;
-                        split_pair(kf.x * __expf(-g0), kf.y * __expf(-g1), hi, lo);
+                        split_pair(kf.x * ex2f(-g0), kf.y * ex2f(-g1), hi, lo);
                         *reinterpret_cast<uint32_t *>(sK + off) = hi;
                         *reinterpret_cast<uint32_t *>(sKlo + off) = lo;
                     }

@@ -343,6 +343,14 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int k, uint32_t block_
            ((chunk ^ (static_cast<uint32_t>(row) & 7u)) << 4) + ((static_cast<uint32_t>(k) & 7u) << 1);
 }
 
+// 2^x by the hardware's approximate base-2 exponential (flushes subnormal
+// results to zero); callers keep their exponents in log2 units.
+__device__ __forceinline__ float ex2f(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&p);
