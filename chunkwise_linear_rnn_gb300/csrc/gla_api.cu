@@ -188,7 +188,7 @@ int chunk_fwd_with_scratch(const void *q, const void *k, const void *v, const fl
                   pl.pair ? dk / 2 : dk, 128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_map(enc, &p.tm_v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dv, T, BH, 64, 128,
                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(enc, &p.tm_o, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dv, T, BH, 64, 128,
+        !make_map(enc, &p.tm_o32, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dv, T, BH, 64, 32,
                   CU_TENSOR_MAP_SWIZZLE_128B))
         return GLA_ERR_LAUNCH;
     p.q = q;

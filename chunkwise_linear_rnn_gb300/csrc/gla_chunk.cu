@@ -100,21 +100,15 @@ struct ChunkReq {
     int t0, first_item, end, pad;
 };
 
-// An output tile staged in shared memory for the TMA store; after the last
-// one, `count` holds the number of tiles staged (kBarStageEnd).
-struct StoreRec {
-    int t0, count;
-};
 
 enum Bar {
     kBarQkFull = 0, kBarQkEmpty, kBarItem, kBarPFull, kBarPSplit, kBarSDone, kBarSReady,
     kBarOFull0, kBarOFull1, kBarOFree0, kBarOFree1, kBarVFull, kBarVEmpty, kBarAFull,
-    kBarQkRaw, kBarReq, kBarStage, kBarStageEnd, kBarXchg0, kBarXchg1, kBarVerd0, kBarVerd1,
-    kNumBars
+    kBarQkRaw, kBarReq, kBarXchg0, kBarXchg1, kBarVerd0, kBarVerd1, kNumBars
 };
 // arrival counts, in enum order (a CTA pair doubles kBarQkEmpty: both MMAs commit to it)
 __device__ constexpr uint32_t kBarCounts[kNumBars] = {kPrepWarps, 1, 1, 1, 4, 1, 4, 1, 1, 4, 4,
-                                                      1, 1, 1, 1, 1, 4, 4, 1, 1, 1, 1};
+                                                      1, 4, 1, 1, 1, 1, 1, 1, 1};
 
 template <int DK, int DVT, bool PAIR>
 struct Smem {
@@ -135,8 +129,7 @@ struct Smem {
     static constexpr uint32_t kG = kS + kSBytes;          // float [2][DK]: state scale per item
     static constexpr uint32_t kItem = kG + 2 * DK * 4;    // ItemInfo[2]
     static constexpr uint32_t kReq = kItem + 64;          // ChunkReq
-    static constexpr uint32_t kStore = kReq + 16;         // StoreRec[2]: staged output tiles
-    static constexpr uint32_t kVerd = kStore + 16;        // pair: the peer's verdicts [2]
+    static constexpr uint32_t kVerd = kReq + 16;          // pair: the peer's verdicts [2]
     static constexpr uint32_t kBar = kVerd + (PAIR ? 16 : 0);  // mbarriers
     static constexpr uint32_t kMisc = kBar + 8 * kNumBars;  // tmem slot
     static constexpr uint32_t kTotal = kMisc + 16;
@@ -157,7 +150,7 @@ struct Tmem {
 };
 
 struct KParams {
-    CUtensorMap tm_q, tm_k, tm_a, tm_v, tm_o;
+    CUtensorMap tm_q, tm_k, tm_a, tm_v, tm_o32;
     const uint32_t *q;  // bf16 pairs
     const uint32_t *k;
     const float2 *a;
@@ -590,7 +583,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
     float *sG = reinterpret_cast<float *>(smem + L::kG);
     ItemInfo *sItem = reinterpret_cast<ItemInfo *>(smem + L::kItem);
     ChunkReq *sReq = reinterpret_cast<ChunkReq *>(smem + L::kReq);
-    StoreRec *sStore = reinterpret_cast<StoreRec *>(smem + L::kStore);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBar);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
 
@@ -623,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
         prefetch_tensormap(&p.tm_k);
         prefetch_tensormap(&p.tm_a);
         prefetch_tensormap(&p.tm_v);
-        prefetch_tensormap(&p.tm_o);
+        prefetch_tensormap(&p.tm_o32);
     }
     if (warp == kMmaWarp) tmem_alloc(tmem_slot, TM::kCols);
     tc_fence_before();
@@ -802,15 +794,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
         }
     } else if (warp == kTmaWarp) {
         // =========================================================== TMA producer
-        // Three load streams and the output store stream, each served as soon
-        // as its own condition holds, so that none waits behind another: per
-        // requested chunk, A (and, in a CTA pair, the raw Q/K staging tiles) at
-        // once; single-CTA Q and K once the previous chunk's items have released
-        // the operand tiles; V once the previous chunk's V tile (also the output
-        // staging tile) is free; a staged output tile as soon as it is complete.
+        // Three load streams, each served as soon as its own condition holds,
+        // so that none waits behind another: per requested chunk, A (and, in a
+        // CTA pair, the raw Q/K staging tiles) at once; single-CTA Q and K once
+        // the previous chunk's items have released the operand tiles; V once the
+        // previous chunk's V tile (also the output staging tile) is free.
         if (lane == 0) {
             int n_req = 0, n_qk = 0, n_v = 0;   // chunks requested / Q,K issued / V issued
-            int n_st = 0, st_total = -1;        // staged output tiles taken / in all
             int n_use = 0;                      // chunks used (known at the end request)
             bool req_end = false;
             int t0s[4], firsts[4];              // at most 3 chunks are ever outstanding
@@ -873,24 +863,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                     ++n_v;
                     progress = true;
                 }
-                // staged output tiles: store, and free the V tile once the store
-                // has read it
-                if (mbar_test_wait(&bars[kBarStage], n_st & 1)) {
-                    const int t0 = sStore[n_st & 1].t0;
-#pragma unroll
-                    for (int nb = 0; nb < DVT / 64; ++nb)
-                        tma_store_3d(&p.tm_o, sV + nb * kBlk, dv0 + nb * 64, t0, bh);
-                    tma_store_commit();
-                    tma_store_wait_read_all();
-                    mbar_arrive(&bars[kBarVEmpty]);
-                    ++n_st;
-                    progress = true;
-                }
-                if (st_total < 0 && mbar_test_wait(&bars[kBarStageEnd], 0)) {
-                    st_total = sStore[0].count;
-                    progress = true;
-                }
-                if (req_end && n_st == st_total && n_v >= n_use && (PAIR || n_qk == n_req)) break;
+                if (req_end && n_v >= n_use && (PAIR || n_qk == n_req)) break;
                 if (progress) {
                     idle_since = 0;
                 } else {
@@ -911,7 +884,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                 if (PAIR) mbar_wait_bounded(&bars[kBarQkRaw], (n_req - 1) & 1, p.status);
             }
             if (n_v > 0) mbar_wait_bounded(&bars[kBarVFull], (n_v - 1) & 1, p.status);
-            tma_store_wait_all();
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
@@ -1072,7 +1044,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kBarSReady]);   // phase 0: initial state ready
 
-        int n_staged = 0;   // chunks written through the staging tile
         for (int n = 0;; ++n) {
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarItem], n & 1, p.status))) break;
             const ItemInfo it = sItem[n & 1];
@@ -1202,27 +1173,28 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                         }
                     }
                 }
-                if (staged) {
-                    // the TMA thread stores the tile and then frees the V tile
-                    fence_proxy_async_smem();
-                    if (tid == 32 * kTmemWarp0) sStore[n_staged & 1].t0 = it.t0;
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars[kBarStage]);
-                    ++n_staged;
-                }
             }
             tc_fence_before();
+            fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[kBarOFree0 + ob]);
-            // the chunk's V tile may be refilled once its last item is done
-            if ((it.flags & kItemLast) && !staged && tid == 32 * kTmemWarp0)
-                mbar_arrive(&bars[kBarVEmpty]);
+            if (lane == 0) {
+                mbar_arrive(&bars[kBarOFree0 + ob]);
+                // This warp's 32 rows of a staged tile leave with one TMA store
+                // per 64-column block; once the store has read them, this warp's
+                // share of the V tile is free (four arrivals free it).
+                const int r0w = it.t0 + 32 * (warp - kTmemWarp0);
+                if (staged && r0w < T) {
+#pragma unroll
+                    for (int nb = 0; nb < DVT / 64; ++nb)
+                        tma_store_3d(&p.tm_o32, sV + nb * kBlk + (warp - kTmemWarp0) * 32 * 128,
+                                     dv0 + nb * 64, r0w, bh);
+                    tma_store_commit();
+                    tma_store_wait_read_all();
+                }
+                if (it.flags & kItemLast) mbar_arrive(&bars[kBarVEmpty]);
+            }
         }
-        // end of the staged-store stream: its own barrier, since a phase of
-        // kBarStage completing right after the last stage could go unseen
-        if (tid == 32 * kTmemWarp0) sStore[0].count = n_staged;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kBarStageEnd]);
+        if (lane == 0) tma_store_wait_all();
         // ---- final state of a FULL pass
         if (p.mode == kModeFull && has_state_row) {
             float *dst = nullptr;
@@ -1274,7 +1246,7 @@ int launch_tiles(const ChunkLaunch &c, cudaStream_t stream) {
     p.tm_k = c.tm_k;
     p.tm_a = c.tm_a;
     p.tm_v = c.tm_v;
-    p.tm_o = c.tm_o;
+    p.tm_o32 = c.tm_o32;
     p.q = static_cast<const uint32_t *>(c.q);
     p.k = static_cast<const uint32_t *>(c.k);
     p.a = reinterpret_cast<const float2 *>(c.log_alpha);

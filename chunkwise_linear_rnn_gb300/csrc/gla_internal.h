@@ -12,8 +12,9 @@
 namespace gla {
 
 struct ChunkLaunch {
-    // 3-D tensor maps (channel, token, batch*head): q, k, log_alpha, v, o
-    CUtensorMap tm_q, tm_k, tm_a, tm_v, tm_o;
+    // 3-D tensor maps (channel, token, batch*head): q, k, log_alpha, v, and o
+    // (32-token boxes: each TMEM warp stores its own rows)
+    CUtensorMap tm_q, tm_k, tm_a, tm_v, tm_o32;
     const void *q, *k;        // bf16 [BH, T, dk]
     const float *log_alpha;   // fp32 [BH, T, dk]
     const float *h0;          // [BH, dk, dv] or null (zero state)
