@@ -1101,97 +1101,118 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[kBarPSplit]);
-            // ---- state: S <- diag(e^decay) S, and its bf16 copy for the next item
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarSDone], n & 1, p.status))) break;
-            // a CTA pair's item: the peer's half of the state factors
-            if (it.xi >= 0 &&
-                !__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarXchg0 + (it.xi & 1)],
-                                                           (it.xi >> 1) & 1, p.status)))
-                break;
-            tc_fence_after();
-            if (has_state_row) {
-                const float f = sG[(n & 1) * DK + i];
-#pragma unroll
-                for (int c0 = 0; c0 < DVT; c0 += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(tS + c0, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * f);
-                    tmem_st32(tS + c0, r);
-#pragma unroll
-                    for (int j = 0; j < 32; j += 8) {
-                        uint4 pk;
-                        pk.x = pack_bf16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
-                        pk.y = pack_bf16x2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
-                        pk.z = pack_bf16x2(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5]));
-                        pk.w = pack_bf16x2(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7]));
-                        *reinterpret_cast<uint4 *>(sS + sw128_offset(i, c0 + j, L::kSBlk)) = pk;
-                    }
-                }
-                tmem_wait_st();
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[kBarSReady]);
-            // ---- output rows
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarOFull0 + ob], (n >> 1) & 1, p.status)))
-                break;
-            tc_fence_after();
-            // A whole stored chunk leaves through the V tile (free once its P V
-            // product is done) and one TMA tensor store; rows of sub-chunk items
-            // are stored directly.
+            // The state step (S <- diag(e^decay) S and its bf16 copy for the next
+            // item's Qh S) and the output step (this item's rows).  With dk = 128
+            // the bf16 state copy and an output tile have the same size and
+            // layout, so a whole stored chunk is staged in the copy, which this
+            // item's Qh S product has finished reading once its output is ready:
+            // the output step runs first, and V is free as soon as P V is done.
+            // With dk = 64 the output is staged in the V tile after the state step.
+            constexpr bool kStageInS = DK == 128;
+            uint8_t *sStage = kStageInS ? sS : sV;
             const bool store_item = (it.flags & kItemStore) != 0;
             const bool staged = store_item && it.r0 == 0 && it.r1 == kChunk;
-            {
-                const uint32_t tO = tmem + lane_base + (ob ? TM::kO1 : TM::kO0);
-                const int t = it.t0 + i;
-                const bool st = store_item && !staged && i >= it.r0 && i < it.r1 && t < T;
-                __nv_bfloat16 *orow = p.o + (static_cast<size_t>(bh) * T + t) * p.dv + dv0;
+            auto state_step = [&]() -> bool {
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarSDone], n & 1, p.status)))
+                    return false;
+                // a CTA pair's item: the peer's half of the state factors
+                if (it.xi >= 0 &&
+                    !__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarXchg0 + (it.xi & 1)],
+                                                               (it.xi >> 1) & 1, p.status)))
+                    return false;
+                tc_fence_after();
+                if (has_state_row) {
+                    const float f = sG[(n & 1) * DK + i];
 #pragma unroll
-                for (int c0 = 0; c0 < DVT; c0 += 64) {
-                    uint32_t ra[32], rb[32];
-                    tmem_ld32(tO + c0, ra);
-                    tmem_ld32(tO + c0 + 32, rb);
-                    tmem_wait_ld();
+                    for (int c0 = 0; c0 < DVT; c0 += 32) {
+                        uint32_t r[32];
+                        tmem_ld32(tS + c0, r);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        const uint32_t(&r)[32] = half ? rb : ra;
-                        const int cc = c0 + 32 * half;
+                        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * f);
+                        tmem_st32(tS + c0, r);
 #pragma unroll
                         for (int j = 0; j < 32; j += 8) {
                             uint4 pk;
-                            pk.x = pack_bf16x2(p.scale * __uint_as_float(r[j]), p.scale * __uint_as_float(r[j + 1]));
-                            pk.y = pack_bf16x2(p.scale * __uint_as_float(r[j + 2]), p.scale * __uint_as_float(r[j + 3]));
-                            pk.z = pack_bf16x2(p.scale * __uint_as_float(r[j + 4]), p.scale * __uint_as_float(r[j + 5]));
-                            pk.w = pack_bf16x2(p.scale * __uint_as_float(r[j + 6]), p.scale * __uint_as_float(r[j + 7]));
-                            if (staged)
-                                *reinterpret_cast<uint4 *>(sV + sw128_offset(i, cc + j, kBlk)) = pk;
-                            else if (st)
-                                *reinterpret_cast<uint4 *>(orow + cc + j) = pk;
+                            pk.x = pack_bf16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+                            pk.y = pack_bf16x2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+                            pk.z = pack_bf16x2(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5]));
+                            pk.w = pack_bf16x2(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7]));
+                            *reinterpret_cast<uint4 *>(sS + sw128_offset(i, c0 + j, L::kSBlk)) = pk;
+                        }
+                    }
+                    tmem_wait_st();
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[kBarSReady]);
+                return true;
+            };
+            auto output_step = [&]() -> bool {
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait_bounded(&bars[kBarOFull0 + ob], (n >> 1) & 1, p.status)))
+                    return false;
+                tc_fence_after();
+                // staged in the state copy: the V tile is free now
+                if (kStageInS && (it.flags & kItemLast) && lane == 0) mbar_arrive(&bars[kBarVEmpty]);
+                {
+                    const uint32_t tO = tmem + lane_base + (ob ? TM::kO1 : TM::kO0);
+                    const int t = it.t0 + i;
+                    const bool st = store_item && !staged && i >= it.r0 && i < it.r1 && t < T;
+                    __nv_bfloat16 *orow = p.o + (static_cast<size_t>(bh) * T + t) * p.dv + dv0;
+#pragma unroll
+                    for (int c0 = 0; c0 < DVT; c0 += 64) {
+                        uint32_t ra[32], rb[32];
+                        tmem_ld32(tO + c0, ra);
+                        tmem_ld32(tO + c0 + 32, rb);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            const uint32_t(&r)[32] = half ? rb : ra;
+                            const int cc = c0 + 32 * half;
+#pragma unroll
+                            for (int j = 0; j < 32; j += 8) {
+                                uint4 pk;
+                                pk.x = pack_bf16x2(p.scale * __uint_as_float(r[j]), p.scale * __uint_as_float(r[j + 1]));
+                                pk.y = pack_bf16x2(p.scale * __uint_as_float(r[j + 2]), p.scale * __uint_as_float(r[j + 3]));
+                                pk.z = pack_bf16x2(p.scale * __uint_as_float(r[j + 4]), p.scale * __uint_as_float(r[j + 5]));
+                                pk.w = pack_bf16x2(p.scale * __uint_as_float(r[j + 6]), p.scale * __uint_as_float(r[j + 7]));
+                                if (staged)
+                                    *reinterpret_cast<uint4 *>(sStage + sw128_offset(i, cc + j, kBlk)) = pk;
+                                else if (st)
+                                    *reinterpret_cast<uint4 *>(orow + cc + j) = pk;
+                            }
                         }
                     }
                 }
-            }
-            tc_fence_before();
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&bars[kBarOFree0 + ob]);
-                // This warp's 32 rows of a staged tile leave with one TMA store
-                // per 64-column block; once the store has read them, this warp's
-                // share of the V tile is free (four arrivals free it).
-                const int r0w = it.t0 + 32 * (warp - kTmemWarp0);
-                if (staged && r0w < T) {
+                tc_fence_before();
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&bars[kBarOFree0 + ob]);
+                    // This warp's 32 rows of a staged tile leave with one TMA store
+                    // per 64-column block, and the staging rows are reused only
+                    // once the store has read them.
+                    const int r0w = it.t0 + 32 * (warp - kTmemWarp0);
+                    if (staged && r0w < T) {
 #pragma unroll
-                    for (int nb = 0; nb < DVT / 64; ++nb)
-                        tma_store_3d(&p.tm_o32, sV + nb * kBlk + (warp - kTmemWarp0) * 32 * 128,
-                                     dv0 + nb * 64, r0w, bh);
-                    tma_store_commit();
-                    tma_store_wait_read_all();
+                        for (int nb = 0; nb < DVT / 64; ++nb)
+                            tma_store_3d(&p.tm_o32, sStage + nb * kBlk + (warp - kTmemWarp0) * 32 * 128,
+                                         dv0 + nb * 64, r0w, bh);
+                        tma_store_commit();
+                        tma_store_wait_read_all();
+                    }
+                    // staged in the V tile: four arrivals free it after the stores
+                    if (!kStageInS && (it.flags & kItemLast)) mbar_arrive(&bars[kBarVEmpty]);
                 }
-                if (it.flags & kItemLast) mbar_arrive(&bars[kBarVEmpty]);
+                __syncwarp();
+                return true;
+            };
+            if constexpr (kStageInS) {
+                if (!output_step() || !state_step()) break;
+            } else {
+                if (!state_step() || !output_step()) break;
             }
         }
         if (lane == 0) tma_store_wait_all();
