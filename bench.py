@@ -51,6 +51,35 @@ def peaks():
 
 # --------------------------------------------------------------------------- workloads
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum, both launches of
+# one call) measured with ncu on the long workload at full size, with the
+# sources whose hash is given (profiles/chunk_fwd_B2-H16-T32768-dk128-dv256.md).
+# Any change to those sources makes the figure stale: it is then reported as null.
+MEASURED_TRAFFIC = {"workload": "B2-H16-T32768-dk128-dv256", "sources": "a2f88e9b7a28e269",
+                    "bytes_per_call": 1.61e9 + 499.63e6 + 54.69e6 + 278.78e3}
+TRAFFIC_SOURCES = ["gla_api.cu", "gla_chunk.cu", "gla_internal.h", "gla_ptx.cuh"]
+
+
+def kernel_sources_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, "chunkwise_linear_rnn_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(cfg):
+    if cfg.name != MEASURED_TRAFFIC["workload"]:
+        return None
+    try:
+        if kernel_sources_hash() != MEASURED_TRAFFIC["sources"]:
+            return None
+    except OSError:
+        return None
+    return MEASURED_TRAFFIC["bytes_per_call"]
+
+
 def chunk_bytes(cfg) -> int:
     """Algorithmic bytes of one chunked forward: each input read once, each output written once."""
     per_token = 2 * cfg.dk + 2 * cfg.dk + 2 * cfg.dv + 4 * cfg.dk + 2 * cfg.dv
@@ -299,7 +328,8 @@ def chunk_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_
                    "dv": cfg.dv, "chunk": 128, "replicas": world,
                    "l2": "inputs (%.2f GB) larger than L2; no flush" % (byts / 1e9)},
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": pk["hbm_gbs"],
-                     "unit": "GB/s", "frac": achieved_gbs / pk["hbm_gbs"], "traffic": None,
+                     "unit": "GB/s", "frac": achieved_gbs / pk["hbm_gbs"],
+                     "traffic": measured_traffic(cfg), "traffic_unit": "bytes per call",
                      "peak_kind": pk_kind, "kernel": "chunk_fwd_kernel",
                      "algorithmic_bytes_per_launch": byts,
                      "flops_per_launch": chunk_flops(cfg),
