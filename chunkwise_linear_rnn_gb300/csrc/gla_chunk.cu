@@ -76,7 +76,7 @@ constexpr int kMmaWarp = 12;
 constexpr int kTmaWarp = 13;
 constexpr int kThreads = 448;           // 14 warps
 constexpr float kExpBound = 30.f;
-constexpr float kWindowCut = 41.58883083f;  // 60 ln 2
+constexpr float kWindowCut = 20.79441542f;  // 30 ln 2
 // The fast path keeps in-chunk prefix sums in log2 units (Gamma log2 e), so
 // that every exponential is one ex2.
 constexpr float kLog2e = 1.4426950408889634f;
@@ -902,24 +902,28 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                 const int ob = n & 1;
                 const uint32_t tO = tmem + (ob ? TM::kO1 : TM::kO0);
                 const uint32_t aV = aV0;
-                // a CTA pair's item: the peer's half of the operand tiles
-                if (it.xi >= 0 &&
-                    !mbar_wait_bounded(&bars[kBarXchg0 + (it.xi & 1)], (it.xi >> 1) & 1, p.status))
-                    break;
                 tc_fence_after();
-                // P = Qh (Kh_hi + Kh_lo)^T
+                // P = Qh (Kh_hi + Kh_lo)^T, k-steps of 16 key channels.  In a CTA
+                // pair the steps over this CTA's own 64-channel block go first,
+                // while the peer's block may still be arriving.
+                auto p_steps = [&](int kb, bool first) {
 #pragma unroll
-                for (int ks = 0; ks < DK / 16; ++ks) {
-                    const uint32_t koff = (ks >> 2) * kBlk + (ks & 3) * 32;
-                    mma_bf16_ss(tmem + TM::kP, sw128_desc(aQ + koff, 16, 1024),
-                                sw128_desc(aK + koff, 16, 1024), id_qk, ks > 0);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t koff = kb * kBlk + kk * 32;
+                        mma_bf16_ss(tmem + TM::kP, sw128_desc(aQ + koff, 16, 1024),
+                                    sw128_desc(aK + koff, 16, 1024), id_qk, (first && kk == 0) ? 0 : 1);
+                        mma_bf16_ss(tmem + TM::kP, sw128_desc(aQ + koff, 16, 1024),
+                                    sw128_desc(aKlo + koff, 16, 1024), id_qk, 1);
+                    }
+                };
+                // a CTA pair's item: the peer's half of the operand tiles first
+                if (PAIR && it.xi >= 0) {
+                    if (!mbar_wait_bounded(&bars[kBarXchg0 + (it.xi & 1)], (it.xi >> 1) & 1, p.status))
+                        break;
+                    tc_fence_after();
                 }
 #pragma unroll
-                for (int ks = 0; ks < DK / 16; ++ks) {
-                    const uint32_t koff = (ks >> 2) * kBlk + (ks & 3) * 32;
-                    mma_bf16_ss(tmem + TM::kP, sw128_desc(aQ + koff, 16, 1024),
-                                sw128_desc(aKlo + koff, 16, 1024), id_qk, 1);
-                }
+                for (int kb = 0; kb < DK / 64; ++kb) p_steps(kb, kb == 0);
                 mma_commit(&bars[kBarPFull]);
                 // O = Qh S_prev: needs this O buffer drained and the previous
                 // state scaled and copied
