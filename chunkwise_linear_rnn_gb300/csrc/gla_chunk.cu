@@ -51,8 +51,9 @@
 // s > 0 first runs from a zero state (FULL mode), storing its end state and
 // total decay.  Its outputs depend on the true start state only through
 // (Q * e^Gamma_seg) S_start, where Gamma_seg is the decay since the segment
-// start; once every channel has decayed past e^-41.6 = 2^-60 that term is
-// below 2^-60 of the read-out and the FULL outputs are stored as they are.
+// start; once every channel has decayed past e^-20.8 = 2^-30 that term is
+// below 2^-30 of the start state's read-out, far below the bf16 resolution of
+// the output, and the FULL outputs are stored as they are.
 // The chunks before that point are recomputed by a second launch (CORRECT
 // mode) from the exact start state, obtained by scanning the segment summaries
 // S_start(s+1) = diag(e^G_s) S_start(s) + S*_s.
