@@ -34,9 +34,13 @@ def _stream(device: torch.device) -> ctypes.c_void_p:
 
 
 def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape: tuple, device) -> None:
+    """Checks a tensor argument; `device` is a CUDA device, or the CPU for host entry points."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if t.device.type != "cuda" or (device is not None and t.device != device):
+    if device is not None and device.type == "cpu":
+        if t.device.type != "cpu":
+            raise ValueError(f"{name} must be a CPU tensor")
+    elif t.device.type != "cuda" or (device is not None and t.device != device):
         raise ValueError(f"{name} must be on the CUDA device {device}")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
@@ -64,6 +68,8 @@ def gla_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: 
     B, H, T, dk = q.shape
     dv = v.shape[-1]
     dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("q must be on a CUDA device (gla_chunk_fwd_host takes CPU tensors)")
     _need(q, "q", torch.bfloat16, (B, H, T, dk), dev)
     _need(k, "k", torch.bfloat16, (B, H, T, dk), dev)
     _need(v, "v", torch.bfloat16, (B, H, T, dv), dev)
@@ -89,6 +95,51 @@ def gla_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: 
             None if hT is None else hT.data_ptr(), B, H, T, dk, dv, ctypes.byref(opts),
             _stream(dev))
     _lib.check(st, "gla_chunk_fwd")
+    return out, hT
+
+
+def gla_chunk_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: torch.Tensor,
+                       scale: float | None = None, h0: torch.Tensor | None = None,
+                       output_final_state: bool = True, *, out: torch.Tensor | None = None,
+                       final_state: torch.Tensor | None = None, device: int | None = None):
+    """gla_chunk_fwd on CPU tensors, end to end (copies in, forward, copies out).
+
+    The inputs are CPU tensors; pin them (``tensor.pin_memory()``) for the
+    copies to overlap the computation.  The outputs are CPU tensors too;
+    when not given, they are allocated pinned.  The work is enqueued on the
+    current stream of ``device`` (default: the current CUDA device).  The
+    results are valid once that stream has completed; call
+    ``torch.cuda.synchronize`` or wait on an event before reading them.
+    Returns ``(o, hT)``.
+    """
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, T, dk]")
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    cpu = torch.device("cpu")
+    _need(q, "q", torch.bfloat16, (B, H, T, dk), cpu)
+    _need(k, "k", torch.bfloat16, (B, H, T, dk), cpu)
+    _need(v, "v", torch.bfloat16, (B, H, T, dv), cpu)
+    _need(log_alpha, "log_alpha", torch.float32, (B, H, T, dk), cpu)
+    if h0 is not None:
+        _need(h0, "h0", torch.float32, (B, H, dk, dv), cpu)
+    if out is None:
+        out = torch.empty(B, H, T, dv, dtype=torch.bfloat16, pin_memory=True)
+    _need(out, "out", torch.bfloat16, (B, H, T, dv), cpu)
+    hT = None
+    if output_final_state:
+        hT = final_state if final_state is not None else torch.empty(
+            B, H, dk, dv, dtype=torch.float32, pin_memory=True)
+        _need(hT, "final_state", torch.float32, (B, H, dk, dv), cpu)
+    if scale is None:
+        scale = dk ** -0.5
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+    with torch.cuda.device(dev):
+        st = _lib.lib().gla_chunk_fwd_host(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), log_alpha.data_ptr(), float(scale),
+            None if h0 is None else h0.data_ptr(), out.data_ptr(),
+            None if hT is None else hT.data_ptr(), B, H, T, dk, dv, _stream(dev))
+    _lib.check(st, "gla_chunk_fwd_host")
     return out, hT
 
 
@@ -118,6 +169,8 @@ def gla_recurrent_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_al
         raise ValueError("h must be [B, H, dk, dv]")
     B, H, dk, dv = h.shape
     dev = h.device
+    if dev.type != "cuda":
+        raise ValueError("h must be on a CUDA device")
     _need(h, "h", torch.float32, (B, H, dk, dv), dev)
     _need(q, "q", torch.bfloat16, (B, H, dk), dev)
     _need(k, "k", torch.bfloat16, (B, H, dk), dev)

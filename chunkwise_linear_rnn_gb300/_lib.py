@@ -24,7 +24,8 @@ GLA_ERR_ALLOC = 6
 GLA_ERR_SCRATCH = 7
 
 EXPORTED = ("gla_chunk_fwd", "gla_chunk_fwd_ex", "gla_chunk_fwd_plan", "gla_chunk_fwd_noalloc",
-            "gla_recurrent_step", "gla_status_string", "gla_last_device_status", "gla_version")
+            "gla_chunk_fwd_host", "gla_recurrent_step", "gla_status_string",
+            "gla_last_device_status", "gla_version")
 
 
 class GlaChunkOptions(ctypes.Structure):
@@ -53,6 +54,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.gla_chunk_fwd_noalloc.argtypes = [vp, vp, vp, fp, f, fp, vp, fp, i, i, i, i, i,
                                           ctypes.POINTER(GlaChunkOptions), vp]
     lib.gla_chunk_fwd_noalloc.restype = i
+    lib.gla_chunk_fwd_host.argtypes = [vp, vp, vp, fp, f, fp, vp, fp, i, i, i, i, i, vp]
+    lib.gla_chunk_fwd_host.restype = i
     ip = ctypes.POINTER(ctypes.c_int)
     lib.gla_chunk_fwd_plan.argtypes = [i, i, i, i, i, ctypes.POINTER(GlaChunkOptions), ip, ip, ip,
                                        ctypes.POINTER(ctypes.c_ulong)]

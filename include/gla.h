@@ -141,6 +141,40 @@ int gla_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const flo
                           int dk, int dv, const gla_chunk_options *opts, cudaStream_t stream);
 
 /*
+ * gla_chunk_fwd_host — gla_chunk_fwd on buffers in host memory, end to end.
+ *
+ * Computes what gla_chunk_fwd computes (the same page and sections), for
+ * q, k, v, log_alpha, h0 (nullable), o and hT (nullable) that live in host
+ * memory, with gla_chunk_fwd's layouts.  The inputs are copied to the device,
+ * the chunked forward runs, and the outputs are copied back.  The work is
+ * pipelined over up to 8 groups of consecutive (batch, head) rows: while one
+ * group computes, the next group's inputs travel host->device and the
+ * previous group's outputs travel device->host on two internal streams.
+ *
+ * Ordering: the call is asynchronous and ordered on `stream`.  Once `stream`
+ * has completed the work enqueued here, o and hT hold the results.
+ * Copies overlap only when the host buffers are page-locked (cudaHostAlloc
+ * or cudaHostRegister); pageable buffers give the same results, more slowly.
+ * hT may alias h0.
+ *
+ * Device memory: two input slots and two output slots of one group each
+ * (about 2/8 of the whole problem's device footprint, plus segment scratch).
+ * They are allocated with cudaMallocAsync on `stream` and freed with
+ * cudaFreeAsync once the call's work is done.  The internal streams and
+ * events are created and destroyed inside each call, so the call cannot be
+ * captured into a CUDA graph.
+ *
+ * Errors are those of gla_chunk_fwd: GLA_ERR_ARG / GLA_ERR_SHAPE before any
+ * CUDA call; GLA_ERR_ALLOC when the slots cannot be allocated; GLA_ERR_LAUNCH
+ * when a copy, event or kernel launch fails.  After an error, no further work
+ * is enqueued.  Work already enqueued completes before the slots are freed;
+ * outputs are then incomplete.
+ */
+int gla_chunk_fwd_host(const void *q, const void *k, const void *v, const float *log_alpha,
+                       float scale, const float *h0, void *o, float *hT, int B, int H, int T,
+                       int dk, int dv, cudaStream_t stream);
+
+/*
  * gla_recurrent_step — one decode token for B * H independent heads.
  *
  * h (fp32 [B, H, dk, dv]) is read and overwritten in place with

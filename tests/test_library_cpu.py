@@ -88,6 +88,22 @@ def test_noalloc_validates_on_the_host(lib):
     assert f(P, P, P, P, 0.1, None, P, None, 1, 1, 16, 96, 64, None, None) == _lib.GLA_ERR_SHAPE
 
 
+def test_host_entry_validates_before_any_cuda_call(lib):
+    f = lib.gla_chunk_fwd_host
+    assert f(None, P, P, P, 0.1, None, P, None, 1, 1, 16, 64, 64, None) == _lib.GLA_ERR_ARG
+    assert f(P, P, P, P, 0.1, None, None, None, 1, 1, 16, 64, 64, None) == _lib.GLA_ERR_ARG
+    assert f(P, P, P, P, 0.1, None, P, None, 1, 0, 16, 64, 64, None) == _lib.GLA_ERR_ARG
+    assert f(P, P, P, P, 0.1, None, P, None, 1, 1, 16, 64, 48, None) == _lib.GLA_ERR_SHAPE
+
+
+def test_python_host_binding_checks_dtypes():
+    import torch
+    import chunkwise_linear_rnn_gb300 as gla
+    q = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        gla.gla_chunk_fwd_host(q, q, q, torch.zeros(1, 1, 4, 64, dtype=torch.float64))
+
+
 def test_chunk_rejects_misaligned(lib):
     assert _chunk(lib, q=P + 8) == _lib.GLA_ERR_ARG
     assert _chunk(lib, hT=P + 4) == _lib.GLA_ERR_ARG
@@ -129,6 +145,8 @@ def test_valid_arguments_without_gpu_report_device_error(lib):
     assert lib.gla_last_device_status(None) == _lib.GLA_ERR_DEVICE
     assert lib.gla_chunk_fwd_noalloc(P, P, P, P, 0.125, None, P, None, 1, 1, 16, 64, 64, None,
                                      None) == _lib.GLA_ERR_DEVICE
+    assert lib.gla_chunk_fwd_host(P, P, P, P, 0.125, None, P, None, 1, 1, 16, 64, 64,
+                                  None) == _lib.GLA_ERR_DEVICE
 
 
 def test_python_binding_rejects_cpu_tensors():
