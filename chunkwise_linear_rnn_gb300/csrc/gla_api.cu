@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <algorithm>
 #include <mutex>
 
 #include "gla.h"
@@ -105,30 +106,68 @@ bool make_map(EncodeTiledFn enc, CUtensorMap *m, const void *ptr, CUtensorMapDat
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct Plan {
-    int dv_tile, n_seg, seg_chunks;
-    bool pair;   // the two value-column tiles of a head run as a 2-CTA cluster
+    int dv_tile;
+    bool pair;      // the two value-column tiles of a head run as a 2-CTA cluster
+    int NC;         // chunks (of 128 tokens) per sequence
+    int L;          // chunks per range of the work split
+    int W;          // ranges: CTAs (clusters, for pairs) of the FULL pass per tile column
+    int seg_max;    // most segments a sequence is cut into
 };
 
-// Launch plan of gla_chunk_fwd: value-column tile, CTA pairs, sequence segments.
+constexpr int kMinRange = 16;   // shortest automatic range, in chunks
+
+// Segments of sequence u when ranges of L chunks tile all sequences' chunks
+// (the same arithmetic as the kernel's).
+int nseg_host(long long u, int NC, int L) {
+    const long long a = u * NC;
+    return 1 + static_cast<int>((a + NC - 1) / L - a / L);
+}
+
+// Launch plan of gla_chunk_fwd: value-column tile, CTA pairs, work split.
 // Pairs: with dk = 128 and exactly two value-column tiles, the tiles of a head
 // share the key-side preparation (each CTA prepares one half of the channels).
-// Segments: enough (batch, head, tile, segment) units to fill the SMs once,
-// each segment at least 8 chunks long to amortise its correction window.
+// Work split: when there are fewer sequences than CTAs that can run at once,
+// the chunks of all sequences, one after another, are cut into equal ranges,
+// one per resident CTA (or cluster), so that every SM has the same work; a
+// cut inside a sequence makes a new segment of it, joined by the state
+// correction.  Ranges stay at least kMinRange chunks long, so that the
+// correction windows stay a small part of the work.
 Plan make_plan(int B, int H, int T, int dk, int dv, const gla_chunk_options &op, int sm_count) {
     Plan pl;
     pl.dv_tile = op.dv_tile ? op.dv_tile : (dv >= 128 ? 128 : 64);
     pl.pair = dk == 128 && dv == 2 * pl.dv_tile && op.cta_pair >= 0;
-    const int n_chunks = (T + 127) / 128;
-    int n_seg = op.segments;
-    if (n_seg == 0) {
-        const long long units = static_cast<long long>(B) * H * (dv / pl.dv_tile);
-        n_seg = units > 0 ? static_cast<int>(sm_count / units) : 1;
-        n_seg = n_seg < n_chunks / 8 ? n_seg : n_chunks / 8;
-        if (n_seg < 1) n_seg = 1;
+    const long long BH = static_cast<long long>(B) * H;
+    pl.NC = (T + 127) / 128;
+    const long long total = BH * pl.NC;
+    long long L;
+    if (op.segments > 0) {
+        L = (pl.NC + op.segments - 1) / op.segments;
+    } else {
+        const int n_dvt = dv / pl.dv_tile;
+        int resident = gla::chunk_fwd_max_resident(dk, pl.dv_tile, pl.pair ? 1 : 0);
+        if (resident <= 0) resident = pl.pair ? sm_count / 2 : sm_count;
+        const long long ranges = pl.pair ? resident : resident / n_dvt;
+        if (ranges <= BH) {
+            L = pl.NC;   // enough sequences: one per CTA, none cut
+        } else if (pl.pair) {
+            // CTA pairs: whole-number segments per sequence.  Measured on the
+            // GB300, a pair kernel's chunk rate does not grow with more
+            // clusters than that (the extra clusters only add correction work).
+            const long long per = ranges / BH;
+            L = (pl.NC + per - 1) / per;
+            if (L < kMinRange) L = std::min<long long>(kMinRange, pl.NC);
+        } else {
+            L = (total + ranges - 1) / ranges;
+            if (L < kMinRange) L = kMinRange;
+            if (L > pl.NC) L = pl.NC;
+        }
     }
-    if (n_seg > n_chunks) n_seg = n_chunks;
-    pl.seg_chunks = (n_chunks + n_seg - 1) / n_seg;
-    pl.n_seg = (n_chunks + pl.seg_chunks - 1) / pl.seg_chunks;
+    if (L < 1) L = 1;
+    pl.L = static_cast<int>(L);
+    pl.W = static_cast<int>((total + L - 1) / L);
+    pl.seg_max = 1;
+    if (pl.L < pl.NC)
+        for (long long u = 0; u < BH; ++u) pl.seg_max = std::max(pl.seg_max, nseg_host(u, pl.NC, pl.L));
     return pl;
 }
 
@@ -139,8 +178,9 @@ bool options_ok(int dv, const gla_chunk_options &op) {
 }
 
 size_t scratch_needed(const Plan &pl, int B, int H, int dk, int dv) {
-    return pl.n_seg > 1 ? static_cast<size_t>(pl.n_seg) * B * H * dk * (dv + 1) * sizeof(float)
-                        : 0;
+    return pl.seg_max > 1
+               ? static_cast<size_t>(pl.seg_max) * B * H * dk * (dv + 1) * sizeof(float)
+               : 0;
 }
 
 bool dk_ok(int dk) { return dk == 64 || dk == 128; }
@@ -174,9 +214,9 @@ int chunk_fwd_with_scratch(const void *q, const void *k, const void *v, const fl
     const int BH = B * H;
     const Plan pl = make_plan(B, H, T, dk, dv, op, dev->sm_count);
     const size_t state_bytes =
-        pl.n_seg > 1 ? static_cast<size_t>(pl.n_seg) * BH * dk * dv * sizeof(float) : 0;
+        pl.seg_max > 1 ? static_cast<size_t>(pl.seg_max) * BH * dk * dv * sizeof(float) : 0;
     const size_t decay_bytes =
-        pl.n_seg > 1 ? static_cast<size_t>(pl.n_seg) * BH * dk * sizeof(float) : 0;
+        pl.seg_max > 1 ? static_cast<size_t>(pl.seg_max) * BH * dk * sizeof(float) : 0;
     if (state_bytes + decay_bytes > (scratch ? scratch_bytes : 0)) return GLA_ERR_SCRATCH;
 
     ChunkLaunch p;
@@ -199,8 +239,8 @@ int chunk_fwd_with_scratch(const void *q, const void *k, const void *v, const fl
     p.o = o;
     // Every scratch entry a launch reads is written earlier in the same call,
     // so nothing in it needs to start at zero.
-    p.ws_state = pl.n_seg > 1 ? static_cast<float *>(scratch) : nullptr;
-    p.ws_decay = pl.n_seg > 1
+    p.ws_state = pl.seg_max > 1 ? static_cast<float *>(scratch) : nullptr;
+    p.ws_decay = pl.seg_max > 1
                      ? reinterpret_cast<float *>(static_cast<char *>(scratch) + state_bytes)
                      : nullptr;
     p.scale = scale;
@@ -211,8 +251,10 @@ int chunk_fwd_with_scratch(const void *q, const void *k, const void *v, const fl
     p.dv = dv;
     p.dv_tile = pl.dv_tile;
     p.pair = pl.pair ? 1 : 0;
-    p.n_seg = pl.n_seg;
-    p.seg_chunks = pl.seg_chunks;
+    p.NC = pl.NC;
+    p.L = pl.L;
+    p.W = pl.W;
+    p.seg_max = pl.seg_max;
     p.force_exact = op.force_exact ? 1 : 0;
     p.status = dev->status;
     return launch_chunk_fwd(p, stream) == 0 ? GLA_OK : GLA_ERR_LAUNCH;
@@ -285,9 +327,9 @@ int gla_chunk_fwd_plan(int B, int H, int T, int dk, int dv, const gla_chunk_opti
     const int st = current_device(&dev);
     if (st != GLA_OK) return st;
     const Plan pl = make_plan(B, H, T, dk, dv, op, dev->sm_count);
-    if (n_segments) *n_segments = pl.n_seg;
+    if (n_segments) *n_segments = pl.seg_max;
     if (dv_tile) *dv_tile = pl.dv_tile;
-    if (launches) *launches = pl.n_seg > 1 ? 2 : 1;
+    if (launches) *launches = pl.seg_max > 1 ? 2 : 1;
     if (scratch_bytes) *scratch_bytes = scratch_needed(pl, B, H, dk, dv);
     return GLA_OK;
 }

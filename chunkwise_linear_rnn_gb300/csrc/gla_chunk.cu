@@ -62,6 +62,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "gla_internal.h"
 #include "gla_ptx.cuh"
@@ -85,31 +86,35 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kExpBound2 = kExpBound * kLog2e;
 constexpr uint32_t kBlk = kChunk * 128;     // one 64-column block of a 128-row tile
 
-constexpr int kItemLast = 1;   // last item of its chunk: releases the chunk's V stage
-constexpr int kItemStore = 2;  // store this item's output rows
-constexpr int kItemEnd = 4;    // end of the item stream
+constexpr int kItemLast = 1;      // last item of its chunk: releases the chunk's V stage
+constexpr int kItemStore = 2;     // store this item's output rows
+constexpr int kItemEnd = 4;       // end of the item stream
+constexpr int kItemPieceEnd = 8;  // last item of a piece (FULL pass): its end state is stored
 
 constexpr int kModeFull = 0, kModeCorrect = 1;
 
-// One MMA work item: chunk start t0, token rows [r0, r1), flags, chunk
-// counter lc, and (CTA pair) the index of the operand exchange it needs, or -1.
+// One MMA work item: sequence bh, chunk start t0, token rows [r0, r1), flags,
+// chunk counter lc, and (CTA pair) the index of the operand exchange it
+// needs, or -1.
 struct ItemInfo {
-    int t0, r0, r1, flags, lc, xi, pad[2];
+    int t0, r0, r1, flags, lc, xi, bh, pad;
 };
 
+// A chunk load request (t0 of sequence bh), or the end of the requests.
 struct ChunkReq {
-    int t0, first_item, end, pad;
+    int t0, first_item, end, bh;
 };
 
 
 enum Bar {
-    kBarQkFull = 0, kBarQkEmpty, kBarItem, kBarPFull, kBarPSplit, kBarSDone, kBarSReady,
-    kBarOFull0, kBarOFull1, kBarOFree0, kBarOFree1, kBarVFull, kBarVEmpty, kBarAFull,
-    kBarQkRaw, kBarReq, kBarXchg0, kBarXchg1, kBarVerd0, kBarVerd1, kNumBars
+    kBarQkFull = 0, kBarQkEmpty, kBarItem0, kBarItem1, kBarPFull, kBarPSplit, kBarSDone, kBarSReady,
+    kBarOFull0, kBarOFull1, kBarOFree0, kBarOFree1, kBarVFull0, kBarVFull1, kBarVEmpty0,
+    kBarVEmpty1, kBarAFull, kBarQkRaw, kBarReq, kBarXchg0, kBarXchg1, kBarVerd0, kBarVerd1,
+    kNumBars
 };
 // arrival counts, in enum order (a CTA pair doubles kBarQkEmpty: both MMAs commit to it)
-__device__ constexpr uint32_t kBarCounts[kNumBars] = {kPrepWarps, 1, 1, 1, 4, 1, 4, 1, 1, 4, 4,
-                                                      1, 4, 1, 1, 1, 1, 1, 1, 1};
+__device__ constexpr uint32_t kBarCounts[kNumBars] = {kPrepWarps, 1, 1, 1, 1, 4, 1, 4, 1, 1, 4, 4,
+                                                      1, 1, 4, 4, 1, 1, 1, 1, 1, 1, 1};
 
 template <int DK, int DVT, bool PAIR>
 struct Smem {
@@ -123,10 +128,15 @@ struct Smem {
     static constexpr uint32_t kRaw = kA + kABytes;        // pair: raw Q, K of this CTA's channels
     static constexpr uint32_t kRawBytes = PAIR ? 2 * kBlk : 0;
     static constexpr uint32_t kVBytes = kChunk * DVT * 2;
-    static constexpr uint32_t kV = kRaw + kRawBytes;
     static constexpr uint32_t kSBlk = DK * 128;
     static constexpr uint32_t kSBytes = DK * DVT * 2;
-    static constexpr uint32_t kS = kV + kVBytes;
+    // V tiles: two slots where they fit (the next chunk's V loads while this
+    // chunk's products read the other slot), else one
+    static constexpr uint32_t kRest = 2 * DK * 4 + 64 + 16 + 16 + 8 * kNumBars + 16 + 1024;
+    static constexpr int kVSlots =
+        (kRaw + kRawBytes + 2 * kVBytes + kSBytes + kRest) <= 232448u ? 2 : 1;
+    static constexpr uint32_t kV = kRaw + kRawBytes;      // V slots
+    static constexpr uint32_t kS = kV + kVSlots * kVBytes;
     static constexpr uint32_t kG = kS + kSBytes;          // float [2][DK]: state scale per item
     static constexpr uint32_t kItem = kG + 2 * DK * 4;    // ItemInfo[2]
     static constexpr uint32_t kReq = kItem + 64;          // ChunkReq
@@ -142,8 +152,10 @@ struct Smem {
     static_assert(kG % 16 == 0, "bulk copies move 16-byte units");
 };
 
-// TMEM columns: P [0,128) (fp32 scores, then the bf16 hi/lo pair in place),
-// O0 [128,128+DVT), O1, S after them.
+// TMEM columns: P [0,128), O0 [128,128+DVT), O1, S after them.  P holds the
+// fp32 scores of key tokens j = column; each 16-column piece (tokens 16 p ..
+// 16 p + 15) is then replaced in place by its bf16 hi pairs (first 8 columns)
+// and lo pairs (last 8), the A operand of the P V products.
 template <int DVT>
 struct Tmem {
     static constexpr uint32_t kP = 0, kO0 = 128, kO1 = 128 + DVT, kS = 128 + 2 * DVT;
@@ -158,12 +170,54 @@ struct KParams {
     const float *h0;
     float *hT;
     __nv_bfloat16 *o;
-    float *ws_state;    // [n_seg][BH][DK][dv]
-    float *ws_decay;    // [n_seg][BH][DK]
+    float *ws_state;    // [seg_max][BH][DK][dv]: segment end states S*
+    float *ws_decay;    // [seg_max][BH][DK]: segment total log-decays G
     float scale;
-    int H, T, dv, n_seg, seg_chunks, mode, force_sub;
+    int BH, T, dv;
+    // Work split: the chunks of all BH sequences, one after another, cut into
+    // ranges of L chunks, one range per CTA (per cluster for a CTA pair) of
+    // the FULL pass.  A cut inside a sequence starts a new segment of it.
+    int NC;        // chunks per sequence
+    int L;         // chunks per range
+    int seg_max;   // most segments any sequence has
+    int mode, force_sub;
+    long long n_units;   // CTAs (clusters) per tile column in this launch
     unsigned int *status;
 };
+
+// Segment geometry of the work split (identical on the host).  Sequence u
+// occupies global chunks [u NC, (u+1) NC); cuts fall at multiples of L.
+__device__ __forceinline__ int nseg_of(const KParams &p, int u) {
+    const long long a = static_cast<long long>(u) * p.NC;
+    return 1 + static_cast<int>((a + p.NC - 1) / p.L - a / p.L);
+}
+__device__ __forceinline__ int seg_start(const KParams &p, int u, int s) {
+    if (s == 0) return 0;
+    const long long a = static_cast<long long>(u) * p.NC;
+    return static_cast<int>((a / p.L + s) * p.L - a);
+}
+
+// End (global chunk) of this CTA's FULL-pass range, recomputed from the block
+// index where needed instead of being held in registers.
+__device__ __forceinline__ long long full_range_end(const KParams &p) {
+    const long long unit = blockIdx.y + static_cast<long long>(blockIdx.z) * gridDim.y;
+    return min((unit + 1) * p.L, static_cast<long long>(p.BH) * p.NC);
+}
+
+// One piece of a CTA's range: chunks [c0, c1) of sequence u, its segment seg.
+struct Piece {
+    int u, c0, c1, seg;
+};
+
+// The piece that starts at global chunk g of a range ending at g_end.
+__device__ __forceinline__ Piece piece_at(const KParams &p, long long g, long long g_end) {
+    Piece pc;
+    pc.u = static_cast<int>(g / p.NC);
+    pc.c0 = static_cast<int>(g - static_cast<long long>(pc.u) * p.NC);
+    pc.c1 = static_cast<int>(min(static_cast<long long>(p.NC), pc.c0 + (g_end - g)));
+    pc.seg = static_cast<int>(g / p.L - (static_cast<long long>(pc.u) * p.NC) / p.L);
+    return pc;
+}
 
 __device__ __forceinline__ bool bar_or(int id, int n, bool pred) {
     uint32_t r;
@@ -197,20 +251,55 @@ __device__ __forceinline__ float clamp_gate(float a) {
     return fminf(fmaxf(a, -kExpBound), kExpBound);
 }
 
+// Causal split of one 32-column block of P (key tokens j0 .. j0 + 31) for
+// row i, from its fp32 scores r: both 16-column pieces are stored back in
+// place as 8 columns of bf16 hi pairs followed by 8 of lo pairs, with the
+// entries j > i zeroed where the block holds the diagonal (`diag`, uniform
+// over the warp).  One piece is stored before the next is split.
+__device__ __forceinline__ void split_p_block(uint32_t taddr, const uint32_t (&r)[32], int j0, int i,
+                                              bool diag) {
+#pragma unroll
+    for (int pc = 0; pc < 2; ++pc) {
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            float x0 = __uint_as_float(r[16 * pc + 2 * e]);
+            float x1 = __uint_as_float(r[16 * pc + 2 * e + 1]);
+            if (diag) {
+                const int j = j0 + 16 * pc + 2 * e;
+                x0 = j <= i ? x0 : 0.f;
+                x1 = j + 1 <= i ? x1 : 0.f;
+            }
+            split_pair(x0, x1, w[e], w[8 + e]);
+        }
+        tmem_st16(taddr + 16 * pc, w);
+    }
+}
+
+// A 32-column block of P past the diagonal for every row of the warp: zeros.
+__device__ __forceinline__ void zero_p_block(uint32_t taddr) {
+    uint32_t z[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) z[e] = 0u;
+    tmem_st16(taddr, z);
+    tmem_st16(taddr + 16, z);
+}
+
 // Sub-chunk rescaling of one chunk (prep threads): the largest power-of-two
 // block length cs whose every block keeps |Gamma - r_block| <= kExpBound
 // (clamped gates); each block becomes one item, written to the operand tiles
 // with its own reference.  Gates, Q and K are read from global memory.
 // Thread pt owns the channel pair 2*(pt % (DK/2)) of token part pt / (DK/2).
-// `n` counts items; gtot0/gtot1 return the chunk's clamped Gamma at its end
-// for the thread's channels (valid in the last token part).  Returns false if
-// a bounded wait expired.
-template <int DK>
+// `n` counts items; `last_flags` go to the chunk's last item; gtot0/gtot1
+// return the chunk's clamped Gamma at its end for the thread's channels (valid
+// in the last token part).  Returns false if a bounded wait expired.
+template <int DK, typename BeforeEmptyWait>
 __device__ __forceinline__ bool sub_chunk_items(const KParams &p, int bh, int t0, int lc,
-                                                bool store, int pt, uint8_t *sQ, uint8_t *sK,
+                                                bool store, int last_flags, int pt, uint8_t *sQ,
+                                                uint8_t *sK,
                                                 uint8_t *sKlo, float *sG, ItemInfo *sItem,
                                                 uint64_t *bars, int &n, float &gtot0,
-                                                float &gtot1) {
+                                                float &gtot1, BeforeEmptyWait &&before_empty_wait) {
     constexpr int NP = DK / 2;
     constexpr int NQ = kPrepThreads / NP;
     constexpr int TP = kChunk / NQ;
@@ -269,7 +358,10 @@ __device__ __forceinline__ bool sub_chunk_items(const KParams &p, int bh, int t0
     for (int sidx = 0; sidx < n_sub; ++sidx) {
         const int sa = sidx * cs, sb = sa + cs;
         bool okw = true;
-        if (sidx > 0) okw = mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status);
+        if (sidx > 0) {
+            before_empty_wait();
+            okw = mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status);
+        }
         ok = !bar_or(4, kPrepThreads, !okw);
         if (!ok) break;
         // reference for block sidx: clamped Gamma just before token sa
@@ -311,8 +403,9 @@ __device__ __forceinline__ bool sub_chunk_items(const KParams &p, int bh, int t0
         }
         if (pt == 0) {
             sItem[n & 1] = ItemInfo{
-                t0, sa, sb, (sidx == n_sub - 1 ? kItemLast : 0) | (store ? kItemStore : 0), lc,
-                -1, {0, 0}};
+                t0, sa, sb,
+                (sidx == n_sub - 1 ? (kItemLast | last_flags) : 0) | (store ? kItemStore : 0), lc,
+                -1, bh, 0};
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -346,8 +439,8 @@ __device__ __forceinline__ bool sub_chunk_items(const KParams &p, int bh, int t0
 // CTAs compute it from identical bits (the exchanged factor table, or the raw
 // gates), so their window decisions agree.
 template <int DK, int DVT>
-__device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint32_t rank, int bh,
-                                          int seg, int c_begin, int c_end, size_t BHn,
+__device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint32_t rank,
+                                          long long g_begin, long long g_end, size_t BHn,
                                           int dv_tile) {
     using L = Smem<DK, DVT, true>;
     constexpr int DKH = DK / 2;                 // channels prepared by this CTA
@@ -377,8 +470,18 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
     const uint32_t peer = rank ^ 1u;
     const int T = p.T;
 
+    // the pieces of this CTA's range, one after another: the current piece is
+    // chunks [c, c_end) of sequence bh (the rest is recomputed at piece ends)
+    int bh, c, c_end;
+    bool closed;
+    {
+        const Piece pc = piece_at(p, g_begin, g_end);
+        bh = pc.u;
+        c = pc.c0;
+        c_end = pc.c1;
+        closed = p.mode == kModeFull && pc.seg == 0;
+    }
     float gseg = 0.f;                            // threads pt < DK: channel pt
-    bool closed = (p.mode == kModeFull && seg == 0);
     int n = 0;                                   // items published
     int nx = 0;                                  // operand exchanges made
     int used = 0;                                // chunks published
@@ -388,15 +491,13 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
     bool spec = false;                           // chunk lc_last + 1 requested, A not yet landed
     int lc_last = 0;
     if (pt == 0) {
-        const bool e = c_begin >= c_end;
-        sReq[0] = ChunkReq{e ? 0 : c_begin * kChunk, 0, e ? 1 : 0, 0};
+        sReq[0] = ChunkReq{c * kChunk, 0, 0, bh};
         mbar_arrive(&bars[kBarReq]);
     }
-    bool end_posted = c_begin >= c_end;
     // A wait that expires clears `ok` in its thread only: every thread still
     // runs the same sequence of barriers (each wait is bounded), and the loop
     // ends at the next chunk boundary, where the threads' verdicts are combined.
-    for (int c = c_begin, lc = 0;; ++c, ++lc) {
+    for (int lc = 0;; ++lc) {
         ok = !bar_or(4, kPrepThreads, !ok);
         const bool have = c < c_end && ok;
         const int t0 = c * kChunk;
@@ -461,12 +562,24 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
             gc1 = o1 + c1;
             // the A and staging tiles are consumed: start the next chunk's loads
             named_barrier(5, kPrepThreads);
+            // the next chunk of the stream: in this piece, or the next piece's first
+            int nc = -1, nbh = bh;
             if (c + 1 < c_end) {
+                nc = c + 1;
+            } else if (p.mode == kModeFull) {
+                const long long gn = static_cast<long long>(bh) * p.NC + c_end, ge = full_range_end(p);
+                if (gn < ge) {
+                    const Piece next = piece_at(p, gn, ge);
+                    nc = next.c0;
+                    nbh = next.u;
+                }
+            }
+            if (nc >= 0) {
                 if (pt == 0) {
-                    sReq[0] = ChunkReq{(c + 1) * kChunk, 0, 0, 0};
+                    sReq[0] = ChunkReq{nc * kChunk, 0, 0, nbh};
                     mbar_arrive(&bars[kBarReq]);
                 }
-                spec = true;   // taken by the TMA thread once A(c+1) has landed
+                spec = true;   // taken by the TMA thread once A(next) has landed
             }
             prepped_last = true;
             lc_last = lc;
@@ -484,6 +597,8 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
         if (!closed && !any_win) closed = true;
         if (!have || (p.mode == kModeCorrect && closed)) break;
         const bool store = p.mode == kModeCorrect || closed;
+        // the FULL pass stores the state at the end of every piece
+        const int piece_end = (p.mode == kModeFull && c + 1 == c_end) ? kItemPieceEnd : 0;
         // ---- both CTAs' verdicts: one branch for all threads, even for one
         // whose wait expired
         ok &= mbar_wait_bounded(&bars[kBarVerd0 + (lc & 1)], (lc >> 1) & 1, p.status);
@@ -507,8 +622,9 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
             fence_proxy_async_smem();
             named_barrier(5, kPrepThreads);
             if (pt == 0) {
-                sItem[n & 1] = ItemInfo{t0, 0, kChunk, kItemLast | (store ? kItemStore : 0), lc, nx,
-                                        {0, 0}};
+                sItem[n & 1] = ItemInfo{t0, 0, kChunk,
+                                        kItemLast | (store ? kItemStore : 0) | piece_end, lc, nx,
+                                        bh, 0};
                 mbar_arrive_expect_tx(&bars[kBarXchg0 + (nx & 1)], kXchgBytes);
                 const uint32_t pbar = mapa_shared(smem_u32(&bars[kBarXchg0 + (nx & 1)]), peer);
                 const uint32_t blk = rank * kBlk;
@@ -523,22 +639,45 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
             ++n;
             ++nx;
             pend = true;
-            continue;
+        } else {
+            // ---- a chunk whose decay breaks the bound: sub-chunk items over all
+            // channels, computed by each CTA of the pair on its own
+            if (n > 0) ok &= mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status);
+            float gt0 = 0.f, gt1 = 0.f;
+            ok &= sub_chunk_items<DK>(p, bh, t0, lc, store, piece_end, pt, sQ, sK, sKlo, sG, sItem,
+                                      bars, n, gt0, gt1, [] {});
+            if (pt < DK) {
+                // the chunk's clamped decay of channel pt, summed in token order
+                const float *ab =
+                    reinterpret_cast<const float *>(p.a) + static_cast<size_t>(bh) * T * DK + pt;
+                float gsum = 0.f;
+                for (int i = 0; i < kChunk && t0 + i < T; ++i)
+                    gsum += clamp_gate(ab[static_cast<size_t>(t0 + i) * DK]);
+                gseg += gsum;
+            }
         }
-        // ---- a chunk whose decay breaks the bound: sub-chunk items over all
-        // channels, computed by each CTA of the pair on its own
-        if (n > 0) ok &= mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status);
-        float gt0 = 0.f, gt1 = 0.f;
-        ok &= sub_chunk_items<DK>(p, bh, t0, lc, store, pt, sQ, sK, sKlo, sG, sItem, bars, n, gt0,
-                                  gt1);
-        if (pt < DK) {
-            // the chunk's clamped decay of channel pt, summed in token order
-            const float *ab =
-                reinterpret_cast<const float *>(p.a) + static_cast<size_t>(bh) * T * DK + pt;
-            float gsum = 0.f;
-            for (int i = 0; i < kChunk && t0 + i < T; ++i)
-                gsum += clamp_gate(ab[static_cast<size_t>(t0 + i) * DK]);
-            gseg += gsum;
+        ++c;
+        if (piece_end) {
+            // ---- end of a FULL-pass piece: its decay, then the next piece
+            if (pend) {
+                const int x = nx - 1;
+                ok &= mbar_wait_bounded(&bars[kBarXchg0 + (x & 1)], (x >> 1) & 1, p.status);
+                if (pt < DK) gseg += __logf(sG[((n - 1) & 1) * DK + pt]);
+                pend = false;
+            }
+            const long long a = static_cast<long long>(bh) * p.NC;
+            if (nseg_of(p, bh) > 1 && dv_tile == 0 && pt < DK) {
+                const int seg = static_cast<int>((a + c_end - 1) / p.L - a / p.L);
+                p.ws_decay[(static_cast<size_t>(seg) * BHn + bh) * DK + pt] = gseg;
+            }
+            const long long gn = a + c_end, ge = full_range_end(p);
+            if (gn >= ge) break;
+            const Piece next = piece_at(p, gn, ge);
+            bh = next.u;
+            c = next.c0;
+            c_end = next.c1;
+            gseg = 0.f;
+            closed = next.seg == 0;
         }
     }
     // ---- end of the item stream and of the load requests
@@ -554,24 +693,22 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
     // the TMA thread has taken the last one (its A tile has landed)
     if (spec) ok &= mbar_wait_bounded(&bars[kBarAFull], (lc_last + 1) & 1, p.status);
     named_barrier(5, kPrepThreads);
-    if (!end_posted && pt == 0) {
+    if (pt == 0) {
         // the count of chunks used, so that no V load waits for a tile never freed
         sReq[0] = ChunkReq{used, 0, 1, 0};
         mbar_arrive(&bars[kBarReq]);
     }
     if (n > 0 && !mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status)) ok = false;
-    if (pt == 0) sItem[n & 1] = ItemInfo{0, 0, 0, kItemEnd, 0, -1, {0, 0}};
+    if (pt == 0) sItem[n & 1] = ItemInfo{0, 0, 0, kItemEnd, 0, -1, 0, 0};
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars[kBarQkFull]);
-    // segment summary: total decay of this segment (FULL mode, several segments)
-    if (p.mode == kModeFull && p.n_seg > 1 && dv_tile == 0 && pt < DK)
-        p.ws_decay[(static_cast<size_t>(seg) * BHn + bh) * DK + pt] = gseg;
 }
 
 template <int DK, int DVT, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_constant__ KParams p) {
     using L = Smem<DK, DVT, PAIR>;
     using TM = Tmem<DVT>;
+    constexpr int VS = L::kVSlots;   // V tile slots: chunk j uses slot j % VS
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -590,17 +727,30 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int dv_tile = blockIdx.x;
-    const int h = blockIdx.y;
-    const int nseg_launch = p.mode == kModeFull ? p.n_seg : p.n_seg - 1;
-    const int b = blockIdx.z / nseg_launch;
-    const int seg = blockIdx.z % nseg_launch + (p.mode == kModeFull ? 0 : 1);
-    const int bh = b * p.H + h;
     const int dv0 = dv_tile * DVT;
     const int T = p.T;
-    const int n_chunks = (T + kChunk - 1) / kChunk;
-    const int c_begin = seg * p.seg_chunks;
-    const int c_end = min(n_chunks, c_begin + p.seg_chunks);
-    const size_t BHn = static_cast<size_t>(gridDim.z / nseg_launch) * p.H;  // B * H
+    const size_t BHn = static_cast<size_t>(p.BH);
+    // This CTA's chunks: FULL pass, range `unit` of the work split (one or
+    // more pieces); CORRECT pass, segment 1 + unit % (seg_max - 1) of
+    // sequence unit / (seg_max - 1), if that sequence has it (a CTA pair's two
+    // CTAs decide alike and leave together, before any cluster barrier or TMEM
+    // allocation).
+    const long long unit = blockIdx.y + static_cast<long long>(blockIdx.z) * gridDim.y;
+    if (unit >= p.n_units) return;
+    long long g_begin, g_end;
+    if (p.mode == kModeFull) {
+        g_begin = unit * p.L;
+        g_end = min(g_begin + p.L, static_cast<long long>(p.BH) * p.NC);
+    } else {
+        const int u = static_cast<int>(unit / (p.seg_max - 1));
+        const int sg = 1 + static_cast<int>(unit % (p.seg_max - 1));
+        const int ns = nseg_of(p, u);
+        if (sg >= ns) return;
+        const long long a = static_cast<long long>(u) * p.NC;
+        g_begin = a + seg_start(p, u, sg);
+        g_end = a + (sg + 1 < ns ? seg_start(p, u, sg + 1) : p.NC);
+    }
+    if (g_begin >= g_end) return;
 
     // CTA pair: the two value-column tiles of one head, cluster ranks 0 and 1
     // (rank == dv_tile); each prepares the operands of one half of the key
@@ -627,7 +777,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
 
     if (warp < kPrepWarps && PAIR) {
         if constexpr (PAIR) {
-            prep_pair<DK, DVT>(p, smem, rank, bh, seg, c_begin, c_end, BHn, dv_tile);
+            prep_pair<DK, DVT>(p, smem, rank, g_begin, g_end, BHn, dv_tile);
         }
     } else if (warp < kPrepWarps) {
         // =========================================================== prep warps
@@ -640,26 +790,33 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
         const int ch = 2 * pr;
         const bool last_part = part == NQ - 1;
         const float *sAc = sA + ch;         // this thread's channel pair in the A tile
-        float gseg0 = 0.f, gseg1 = 0.f;     // decay since the segment start (last part only)
-        bool closed = (p.mode == kModeFull && seg == 0);  // no correction window
-        int n = 0;
+        int n = 0, lc = 0;
         bool ok = true;
-        for (int c = c_begin, lc = 0;; ++c, ++lc) {
-            // ---- decide this chunk: past the segment end, or (correction pass)
+        for (long long g = g_begin; g < g_end && ok;) {
+          // ---- one piece: chunks [pc.c0, pc.c1) of sequence pc.u
+          const Piece pc = piece_at(p, g, g_end);
+          g += pc.c1 - pc.c0;
+          const int bh = pc.u;
+          float gseg0 = 0.f, gseg1 = 0.f;     // decay since the segment start (last part only)
+          bool closed = (p.mode == kModeFull && pc.seg == 0);  // no correction window
+          for (int c = pc.c0;; ++c, ++lc) {
+            // ---- decide this chunk: past the piece end, or (correction pass)
             // past the point where the segment's start state has decayed away.
             // The reduction doubles as the barrier after which the previous
             // chunk's A tile is free.
             const bool win = !closed && last_part && (gseg0 > -kWindowCut || gseg1 > -kWindowCut);
             const bool any_win = bar_or(1, kPrepThreads, win);
             if (!closed && !any_win) closed = true;
-            const bool end = c >= c_end || !ok || (p.mode == kModeCorrect && closed);
+            const bool end = c >= pc.c1 || !ok || (p.mode == kModeCorrect && closed);
+            if (end) break;
             if (pt == 0) {
-                sReq[0] = ChunkReq{end ? -1 : c * kChunk, n, end ? 1 : 0, 0};
+                sReq[0] = ChunkReq{c * kChunk, n, 0, bh};
                 mbar_arrive(&bars[kBarReq]);
             }
-            if (end) break;
             const int t0 = c * kChunk;
             const bool store = p.mode == kModeCorrect || closed;
+            // the FULL pass stores the state at the end of every piece
+            const int piece_end = (p.mode == kModeFull && c + 1 == pc.c1) ? kItemPieceEnd : 0;
             // ---- phase A (needs only the A tile, which arrives early): the
             // local prefix sum of this thread's part, written in place of A.
             constexpr int kB = 8;
@@ -763,8 +920,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                     }
                 }
                 if (pt == 0) {
-                    sItem[n & 1] = ItemInfo{t0, 0, kChunk, kItemLast | (store ? kItemStore : 0), lc,
-                                            -1, {0, 0}};
+                    sItem[n & 1] = ItemInfo{t0, 0, kChunk,
+                                            kItemLast | (store ? kItemStore : 0) | piece_end, lc,
+                                            -1, bh, 0};
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -774,37 +932,42 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             }
             // ---- sub-chunk rescaling (chunks whose decay exceeds the bound)
             float gtot0 = 0.f, gtot1 = 0.f;
-            ok = sub_chunk_items<DK>(p, bh, t0, lc, store, pt, sQ, sK, sKlo, sG, sItem, bars, n,
-                                     gtot0, gtot1);
+            ok = sub_chunk_items<DK>(p, bh, t0, lc, store, piece_end, pt, sQ, sK, sKlo, sG, sItem,
+                                     bars, n, gtot0, gtot1, [] {});
             if (last_part) {
                 gseg0 += gtot0;
                 gseg1 += gtot1;
             }
             // an expired wait (!ok) ends the stream at the top of the loop
+          }
+          // segment summary: total decay of this segment (FULL pass, split sequence)
+          if (p.mode == kModeFull && nseg_of(p, bh) > 1 && dv_tile == 0 && last_part) {
+              float *dst = p.ws_decay + (static_cast<size_t>(pc.seg) * BHn + bh) * DK;
+              dst[ch] = gseg0;
+              dst[ch + 1] = gseg1;
+          }
         }
-        // ---- end of the item stream
+        // ---- end of the requests and of the item stream
+        if (pt == 0) {
+            sReq[0] = ChunkReq{0, n, 1, 0};
+            mbar_arrive(&bars[kBarReq]);
+        }
         if (n > 0 && !mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status)) ok = false;
-        if (pt == 0) sItem[n & 1] = ItemInfo{0, 0, 0, kItemEnd, 0, -1, {0, 0}};
+        if (pt == 0) sItem[n & 1] = ItemInfo{0, 0, 0, kItemEnd, 0, -1, 0, 0};
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kBarQkFull]);
-        // segment summary: total decay of this segment (FULL mode, several segments)
-        if (p.mode == kModeFull && p.n_seg > 1 && dv_tile == 0 && last_part) {
-            float *dst = p.ws_decay + (static_cast<size_t>(seg) * BHn + bh) * DK;
-            dst[ch] = gseg0;
-            dst[ch + 1] = gseg1;
-        }
     } else if (warp == kTmaWarp) {
         // =========================================================== TMA producer
         // Three load streams, each served as soon as its own condition holds,
         // so that none waits behind another: per requested chunk, A (and, in a
         // CTA pair, the raw Q/K staging tiles) at once; single-CTA Q and K once
-        // the previous chunk's items have released the operand tiles; V once the
-        // previous chunk's V tile (also the output staging tile) is free.
+        // the previous chunk's items have released the operand tiles; V once
+        // its slot (also the output staging tile with two slots) is free.
         if (lane == 0) {
             int n_req = 0, n_qk = 0, n_v = 0;   // chunks requested / Q,K issued / V issued
             int n_use = 0;                      // chunks used (known at the end request)
             bool req_end = false;
-            int t0s[4], firsts[4];              // at most 3 chunks are ever outstanding
+            int t0s[4], firsts[4], bhs[4];      // at most 3 chunks are ever outstanding
             unsigned long long idle_since = 0;
             while (true) {
                 bool progress = false;
@@ -817,9 +980,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                         req_end = true;
                         n_use = PAIR ? rq.t0 : n_req;
                     } else {
-                        const int t0 = rq.t0;
+                        const int t0 = rq.t0, bh = rq.bh;
                         t0s[n_req & 3] = t0;
                         firsts[n_req & 3] = rq.first_item;
+                        bhs[n_req & 3] = bh;
                         // A (and staging): the prep released them with the request
                         fence_proxy_async_smem();
                         mbar_arrive_expect_tx(&bars[kBarAFull], L::kABytes);
@@ -841,7 +1005,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                     if (n_qk < n_req) {
                         const int first = firsts[n_qk & 3];
                         if (first == 0 || mbar_test_wait(&bars[kBarQkEmpty], (first - 1) & 1)) {
-                            const int t0 = t0s[n_qk & 3];
+                            const int t0 = t0s[n_qk & 3], bh = bhs[n_qk & 3];
                             mbar_arrive_expect_tx(&bars[kBarQkRaw], 2u * L::kQBytes);
 #pragma unroll
                             for (int kb = 0; kb < DK / 64; ++kb) {
@@ -853,14 +1017,19 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                         }
                     }
                 }
-                // V: after the previous chunk's products and output store
+                // V of chunk n_v into slot n_v % VS: once the chunk that last
+                // used the slot is done with it (products and output store)
                 if (n_v < (req_end ? n_use : n_req) &&
-                    (n_v == 0 || mbar_test_wait(&bars[kBarVEmpty], (n_v - 1) & 1))) {
-                    const int t0 = t0s[n_v & 3];
-                    mbar_arrive_expect_tx(&bars[kBarVFull], L::kVBytes);
+                    (n_v < VS ||
+                     mbar_test_wait(&bars[kBarVEmpty0 + n_v % VS], (n_v / VS - 1) & 1))) {
+                    const int t0 = t0s[n_v & 3], bh = bhs[n_v & 3];
+                    const int slot = n_v % VS;
+                    uint8_t *dst = sV + slot * L::kVBytes;
+                    mbar_arrive_expect_tx(&bars[kBarVFull0 + slot], L::kVBytes);
 #pragma unroll
                     for (int nb = 0; nb < DVT / 64; ++nb)
-                        tma_load_3d(sV + nb * kBlk, &p.tm_v, &bars[kBarVFull], dv0 + nb * 64, t0, bh);
+                        tma_load_3d(dst + nb * kBlk, &p.tm_v, &bars[kBarVFull0 + slot], dv0 + nb * 64,
+                                    t0, bh);
                     ++n_v;
                     progress = true;
                 }
@@ -884,7 +1053,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                 mbar_wait_bounded(&bars[kBarAFull], (n_req - 1) & 1, p.status);
                 if (PAIR) mbar_wait_bounded(&bars[kBarQkRaw], (n_req - 1) & 1, p.status);
             }
-            if (n_v > 0) mbar_wait_bounded(&bars[kBarVFull], (n_v - 1) & 1, p.status);
+            for (int j = n_v - VS < 0 ? 0 : n_v - VS; j < n_v; ++j)
+                mbar_wait_bounded(&bars[kBarVFull0 + j % VS], (j / VS) & 1, p.status);
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
@@ -898,11 +1068,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             for (int n = 0;; ++n) {
                 if (!mbar_wait_bounded(&bars[kBarQkFull], n & 1, p.status)) break;
                 const ItemInfo it = sItem[n & 1];
-                mbar_arrive(&bars[kBarItem]);
+                mbar_arrive(&bars[kBarItem0 + (n & 1)]);
                 if (it.flags & kItemEnd) break;
                 const int ob = n & 1;
                 const uint32_t tO = tmem + (ob ? TM::kO1 : TM::kO0);
-                const uint32_t aV = aV0;
+                const uint32_t aV = aV0 + (it.lc % VS) * L::kVBytes;   // this chunk's V slot
                 tc_fence_after();
                 // P = Qh (Kh_hi + Kh_lo)^T, k-steps of 16 key channels.  In a CTA
                 // pair the steps over this CTA's own 64-channel block go first,
@@ -940,7 +1110,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                                 sw128_desc(aS + ks * 2048, L::kSBlk, 1024), id_ov, ks > 0);
                 }
                 // S += (Kh_hi + Kh_lo)^T V
-                if (!mbar_wait_bounded(&bars[kBarVFull], it.lc & 1, p.status)) break;
+                if (!mbar_wait_bounded(&bars[kBarVFull0 + it.lc % VS], (it.lc / VS) & 1, p.status))
+                    break;
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < kChunk / 16; ++ks) {
@@ -959,9 +1130,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < kChunk / 16; ++ks) {
-                    const uint32_t pcol = TM::kP + 32 * (ks >> 1) + 8 * (ks & 1);
+                    const uint32_t pcol = TM::kP + 16 * ks;   // hi pairs, then lo pairs
                     mma_bf16_ts(tO, tmem + pcol, sw128_desc(aV + ks * 2048, kBlk, 1024), id_ov, 1);
-                    mma_bf16_ts(tO, tmem + pcol + 16, sw128_desc(aV + ks * 2048, kBlk, 1024), id_ov,
+                    mma_bf16_ts(tO, tmem + pcol + 8, sw128_desc(aV + ks * 2048, kBlk, 1024), id_ov,
                                 1);
                 }
                 mma_commit(&bars[kBarOFull0 + ob]);
@@ -976,147 +1147,171 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
         const uint32_t tP = tmem + lane_base + TM::kP;
         const uint32_t tS = tmem + lane_base + TM::kS;
 
-        // ---- initial state
-        if (has_state_row) {
-            float *hT_dst = nullptr;
-            float eG = 0.f;
-            const float *sstar = nullptr;
-            if (p.mode == kModeCorrect && seg == p.n_seg - 1 && p.hT) {
-                hT_dst = p.hT + (static_cast<size_t>(bh) * DK + i) * p.dv + dv0;
-                eG = __expf(p.ws_decay[(static_cast<size_t>(seg) * BHn + bh) * DK + i]);
-                sstar = p.ws_state + ((static_cast<size_t>(seg) * BHn + bh) * DK + i) * p.dv + dv0;
+        // ---- start state of a piece into TMEM (fp32) and its bf16 copy, then
+        // "state ready" for the piece's first item.  FULL pass: h0 for a
+        // sequence's first segment, zero for later ones.  CORRECT pass: the
+        // exact start state by the scan of the segment summaries before it; the
+        // last segment's CTA also writes hT = diag(e^G) S_start + S*.
+        auto load_state = [&](const Piece &pc) {
+            const int bh = pc.u, seg = pc.seg;
+            if (has_state_row) {
+                float *hT_dst = nullptr;
+                float eG = 0.f;
+                const float *sstar = nullptr;
+                if (p.mode == kModeCorrect && seg == nseg_of(p, bh) - 1 && p.hT) {
+                    hT_dst = p.hT + (static_cast<size_t>(bh) * DK + i) * p.dv + dv0;
+                    eG = __expf(p.ws_decay[(static_cast<size_t>(seg) * BHn + bh) * DK + i]);
+                    sstar = p.ws_state + ((static_cast<size_t>(seg) * BHn + bh) * DK + i) * p.dv + dv0;
+                }
+#pragma unroll
+                for (int c0 = 0; c0 < DVT; c0 += 32) {
+                    float x[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) x[j] = 0.f;
+                    if (p.mode == kModeFull) {
+                        if (seg == 0 && p.h0) {
+                            const float *src =
+                                p.h0 + (static_cast<size_t>(bh) * DK + i) * p.dv + dv0 + c0;
+#pragma unroll
+                            for (int j = 0; j < 32; j += 4) {
+                                const float4 v4 = *reinterpret_cast<const float4 *>(src + j);
+                                x[j] = v4.x;
+                                x[j + 1] = v4.y;
+                                x[j + 2] = v4.z;
+                                x[j + 3] = v4.w;
+                            }
+                        }
+                    } else {
+                        for (int s2 = 0; s2 < seg; ++s2) {
+                            const float e =
+                                __expf(p.ws_decay[(static_cast<size_t>(s2) * BHn + bh) * DK + i]);
+                            const float *src = p.ws_state +
+                                               ((static_cast<size_t>(s2) * BHn + bh) * DK + i) * p.dv +
+                                               dv0 + c0;
+#pragma unroll
+                            for (int j = 0; j < 32; j += 4) {
+                                const float4 v4 = *reinterpret_cast<const float4 *>(src + j);
+                                x[j] = fmaf(e, x[j], v4.x);
+                                x[j + 1] = fmaf(e, x[j + 1], v4.y);
+                                x[j + 2] = fmaf(e, x[j + 2], v4.z);
+                                x[j + 3] = fmaf(e, x[j + 3], v4.w);
+                            }
+                        }
+                        if (hT_dst) {
+#pragma unroll
+                            for (int j = 0; j < 32; j += 4) {
+                                const float4 v4 = *reinterpret_cast<const float4 *>(sstar + c0 + j);
+                                *reinterpret_cast<float4 *>(hT_dst + c0 + j) =
+                                    make_float4(fmaf(eG, x[j], v4.x), fmaf(eG, x[j + 1], v4.y),
+                                                fmaf(eG, x[j + 2], v4.z), fmaf(eG, x[j + 3], v4.w));
+                            }
+                        }
+                    }
+                    uint32_t r[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(x[j]);
+                    tmem_st32(tS + c0, r);
+#pragma unroll
+                    for (int j = 0; j < 32; j += 8) {
+                        uint4 pk;
+                        pk.x = pack_bf16x2(x[j], x[j + 1]);
+                        pk.y = pack_bf16x2(x[j + 2], x[j + 3]);
+                        pk.z = pack_bf16x2(x[j + 4], x[j + 5]);
+                        pk.w = pack_bf16x2(x[j + 6], x[j + 7]);
+                        *reinterpret_cast<uint4 *>(sS + sw128_offset(i, c0 + j, L::kSBlk)) = pk;
+                    }
+                }
+                tmem_wait_st();
             }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kBarSReady]);
+        };
+        // ---- end state of a FULL-pass piece: hT for an unsplit sequence,
+        // else the segment summary S* of the workspace
+        auto store_state = [&](const Piece &pc) {
+            if (!has_state_row) return;
+            float *dst = nullptr;
+            if (nseg_of(p, pc.u) == 1) {
+                if (p.hT) dst = p.hT + (static_cast<size_t>(pc.u) * DK + i) * p.dv + dv0;
+            } else {
+                dst = p.ws_state + ((static_cast<size_t>(pc.seg) * BHn + pc.u) * DK + i) * p.dv + dv0;
+            }
+            if (!dst) return;
+            tc_fence_after();
 #pragma unroll
             for (int c0 = 0; c0 < DVT; c0 += 32) {
-                float x[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) x[j] = 0.f;
-                if (p.mode == kModeFull) {
-                    if (seg == 0 && p.h0) {
-                        const float *src = p.h0 + (static_cast<size_t>(bh) * DK + i) * p.dv + dv0 + c0;
-#pragma unroll
-                        for (int j = 0; j < 32; j += 4) {
-                            const float4 v4 = *reinterpret_cast<const float4 *>(src + j);
-                            x[j] = v4.x;
-                            x[j + 1] = v4.y;
-                            x[j + 2] = v4.z;
-                            x[j + 3] = v4.w;
-                        }
-                    }
-                } else {
-                    // S_start(seg) by the scan of the segment summaries before it
-                    for (int s2 = 0; s2 < seg; ++s2) {
-                        const float e = __expf(p.ws_decay[(static_cast<size_t>(s2) * BHn + bh) * DK + i]);
-                        const float *src = p.ws_state +
-                                           ((static_cast<size_t>(s2) * BHn + bh) * DK + i) * p.dv + dv0 + c0;
-#pragma unroll
-                        for (int j = 0; j < 32; j += 4) {
-                            const float4 v4 = *reinterpret_cast<const float4 *>(src + j);
-                            x[j] = fmaf(e, x[j], v4.x);
-                            x[j + 1] = fmaf(e, x[j + 1], v4.y);
-                            x[j + 2] = fmaf(e, x[j + 2], v4.z);
-                            x[j + 3] = fmaf(e, x[j + 3], v4.w);
-                        }
-                    }
-                    if (hT_dst) {
-#pragma unroll
-                        for (int j = 0; j < 32; j += 4) {
-                            const float4 v4 = *reinterpret_cast<const float4 *>(sstar + c0 + j);
-                            *reinterpret_cast<float4 *>(hT_dst + c0 + j) =
-                                make_float4(fmaf(eG, x[j], v4.x), fmaf(eG, x[j + 1], v4.y),
-                                            fmaf(eG, x[j + 2], v4.z), fmaf(eG, x[j + 3], v4.w));
-                        }
-                    }
-                }
                 uint32_t r[32];
+                tmem_ld32(tS + c0, r);
+                tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(x[j]);
-                tmem_st32(tS + c0, r);
-#pragma unroll
-                for (int j = 0; j < 32; j += 8) {
-                    uint4 pk;
-                    pk.x = pack_bf16x2(x[j], x[j + 1]);
-                    pk.y = pack_bf16x2(x[j + 2], x[j + 3]);
-                    pk.z = pack_bf16x2(x[j + 4], x[j + 5]);
-                    pk.w = pack_bf16x2(x[j + 6], x[j + 7]);
-                    *reinterpret_cast<uint4 *>(sS + sw128_offset(i, c0 + j, L::kSBlk)) = pk;
-                }
+                for (int j = 0; j < 32; j += 4)
+                    *reinterpret_cast<float4 *>(dst + c0 + j) =
+                        make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                                    __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
             }
-            tmem_wait_st();
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kBarSReady]);   // phase 0: initial state ready
+        };
+        load_state(piece_at(p, g_begin, g_end));   // phase 0 of "state ready"
 
         for (int n = 0;; ++n) {
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarItem], n & 1, p.status))) break;
+            // (one barrier per item parity, so that the MMA issuer may run up
+            // to two items ahead of these warps)
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait_bounded(&bars[kBarItem0 + (n & 1)], (n >> 1) & 1, p.status)))
+                break;
             const ItemInfo it = sItem[n & 1];
             if (it.flags & kItemEnd) break;
             const int ob = n & 1;
             // ---- causal mask of P (row i), split into the TMEM A operand of P V
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarPFull], n & 1, p.status))) break;
-            tc_fence_after();
             {
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarPFull], n & 1, p.status)))
+                    break;
+                tc_fence_after();
                 // This warp's rows are 32 wq .. 32 wq + 31: column blocks past
-                // block wq are masked whole (zeros, nothing to read), block wq
-                // is the diagonal, the blocks before it are unmasked.
+                // block wq are zero (nothing to read), block wq is the diagonal,
+                // the blocks before it are unmasked.
                 const int wq = warp - kTmemWarp0;
-                auto split_block = [&](const uint32_t(&r)[32], int qq) {
-                    uint32_t hi[16], lo[16];
-#pragma unroll
-                    for (int w = 0; w < 16; ++w) {
-                        const int j = 32 * qq + 2 * w;
-                        const float x0 = (j <= i) ? __uint_as_float(r[2 * w]) : 0.f;
-                        const float x1 = (j + 1 <= i) ? __uint_as_float(r[2 * w + 1]) : 0.f;
-                        split_pair(x0, x1, hi[w], lo[w]);
-                    }
-                    tmem_st16(tP + 32 * qq, hi);
-                    tmem_st16(tP + 32 * qq + 16, lo);
-                };
-                auto zero_block = [&](int qq) {
-                    uint32_t z[16];
-#pragma unroll
-                    for (int w = 0; w < 16; ++w) z[w] = 0u;
-                    tmem_st16(tP + 32 * qq, z);
-                    tmem_st16(tP + 32 * qq + 16, z);
-                };
 #pragma unroll
                 for (int qd = 0; qd < kChunk / 32; qd += 2) {
                     if (qd > wq) {
-                        zero_block(qd);
-                        zero_block(qd + 1);
+                        zero_p_block(tP + 32 * qd);
+                        zero_p_block(tP + 32 * (qd + 1));
                     } else if (qd + 1 > wq) {
                         uint32_t r0[32];
                         tmem_ld32(tP + 32 * qd, r0);
                         tmem_wait_ld();
-                        split_block(r0, qd);
-                        zero_block(qd + 1);
+                        split_p_block(tP + 32 * qd, r0, 32 * qd, i, true);
+                        zero_p_block(tP + 32 * (qd + 1));
                     } else {
                         uint32_t r0[32], r1[32];
                         tmem_ld32(tP + 32 * qd, r0);
                         tmem_ld32(tP + 32 * (qd + 1), r1);
                         tmem_wait_ld();
-                        split_block(r0, qd);
-                        split_block(r1, qd + 1);
+                        split_p_block(tP + 32 * qd, r0, 32 * qd, i, false);
+                        split_p_block(tP + 32 * (qd + 1), r1, 32 * (qd + 1), i, qd + 1 == wq);
                     }
                 }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[kBarPSplit]);
             }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[kBarPSplit]);
             // The state step (S <- diag(e^decay) S and its bf16 copy for the next
-            // item's Qh S) and the output step (this item's rows).  With dk = 128
-            // the bf16 state copy and an output tile have the same size and
-            // layout, so a whole stored chunk is staged in the copy, which this
-            // item's Qh S product has finished reading once its output is ready:
-            // the output step runs first, and V is free as soon as P V is done.
-            // With dk = 64 the output is staged in the V tile after the state step.
-            constexpr bool kStageInS = DK == 128;
-            uint8_t *sStage = kStageInS ? sS : sV;
+            // item's Qh S) and the output step (this item's rows).  With two V
+            // slots the output is staged in the chunk's V slot once P V is done,
+            // after the state step, which therefore waits for nothing but the
+            // chunk's S products.  With one slot (dk = 128 only) the bf16 state
+            // copy, which has the output tile's size and layout, is the staging
+            // tile: this item's Qh S product has finished reading it once the
+            // output is ready, so the output step runs first, V is free as soon
+            // as P V is done, and the state step follows the staging store.
+            static_assert(VS == 2 || DK == 128, "one V slot only where the state copy can stage");
+            constexpr bool kStageInS = VS == 1;
+            uint8_t *sStage = kStageInS ? sS : sV + (it.lc % VS) * L::kVBytes;
             const bool store_item = (it.flags & kItemStore) != 0;
             const bool staged = store_item && it.r0 == 0 && it.r1 == kChunk;
+            const bool piece_end = (it.flags & kItemPieceEnd) != 0;
             auto state_step = [&]() -> bool {
                 if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarSDone], n & 1, p.status)))
                     return false;
@@ -1136,6 +1331,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
 #pragma unroll
                         for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * f);
                         tmem_st32(tS + c0, r);
+                        if (piece_end) continue;   // the next piece starts afresh
 #pragma unroll
                         for (int j = 0; j < 32; j += 8) {
                             uint4 pk;
@@ -1147,6 +1343,19 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                         }
                     }
                     tmem_wait_st();
+                }
+                if (piece_end) {
+                    // this piece's end state, then the next piece's start state
+                    // (both found from the item: the piece ends with its chunk)
+                    const long long a = static_cast<long long>(it.bh) * p.NC;
+                    const int cl = it.t0 / kChunk;
+                    Piece done;
+                    done.u = it.bh;
+                    done.seg = static_cast<int>((a + cl) / p.L - a / p.L);
+                    store_state(done);
+                    const long long gn = a + cl + 1, ge = full_range_end(p);
+                    if (gn < ge) load_state(piece_at(p, gn, ge));
+                    return true;
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -1160,12 +1369,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                     return false;
                 tc_fence_after();
                 // staged in the state copy: the V tile is free now
-                if (kStageInS && (it.flags & kItemLast) && lane == 0) mbar_arrive(&bars[kBarVEmpty]);
+                if (kStageInS && (it.flags & kItemLast) && lane == 0)
+                    mbar_arrive(&bars[kBarVEmpty0 + it.lc % VS]);
                 {
                     const uint32_t tO = tmem + lane_base + (ob ? TM::kO1 : TM::kO0);
                     const int t = it.t0 + i;
                     const bool st = store_item && !staged && i >= it.r0 && i < it.r1 && t < T;
-                    __nv_bfloat16 *orow = p.o + (static_cast<size_t>(bh) * T + t) * p.dv + dv0;
+                    __nv_bfloat16 *orow = p.o + (static_cast<size_t>(it.bh) * T + t) * p.dv + dv0;
 #pragma unroll
                     for (int c0 = 0; c0 < DVT; c0 += 64) {
                         uint32_t ra[32], rb[32];
@@ -1204,12 +1414,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
 #pragma unroll
                         for (int nb = 0; nb < DVT / 64; ++nb)
                             tma_store_3d(&p.tm_o32, sStage + nb * kBlk + (warp - kTmemWarp0) * 32 * 128,
-                                         dv0 + nb * 64, r0w, bh);
+                                         dv0 + nb * 64, r0w, it.bh);
                         tma_store_commit();
                         tma_store_wait_read_all();
                     }
                     // staged in the V tile: four arrivals free it after the stores
-                    if (!kStageInS && (it.flags & kItemLast)) mbar_arrive(&bars[kBarVEmpty]);
+                    if (!kStageInS && (it.flags & kItemLast))
+                        mbar_arrive(&bars[kBarVEmpty0 + it.lc % VS]);
                 }
                 __syncwarp();
                 return true;
@@ -1221,29 +1432,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             }
         }
         if (lane == 0) tma_store_wait_all();
-        // ---- final state of a FULL pass
-        if (p.mode == kModeFull && has_state_row) {
-            float *dst = nullptr;
-            if (p.n_seg == 1) {
-                if (p.hT) dst = p.hT + (static_cast<size_t>(bh) * DK + i) * p.dv + dv0;
-            } else {
-                dst = p.ws_state + ((static_cast<size_t>(seg) * BHn + bh) * DK + i) * p.dv + dv0;
-            }
-            if (dst) {
-                tc_fence_after();
-#pragma unroll
-                for (int c0 = 0; c0 < DVT; c0 += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(tS + c0, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 32; j += 4)
-                        *reinterpret_cast<float4 *>(dst + c0 + j) =
-                            make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                                        __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
-                }
-            }
-        }
     }
 
     tc_fence_before();
@@ -1282,19 +1470,25 @@ int launch_tiles(const ChunkLaunch &c, cudaStream_t stream) {
     p.ws_state = c.ws_state;
     p.ws_decay = c.ws_decay;
     p.scale = c.scale;
-    p.H = c.H;
+    p.BH = c.B * c.H;
     p.T = c.T;
     p.dv = c.dv;
-    p.n_seg = c.n_seg;
-    p.seg_chunks = c.seg_chunks;
+    p.NC = c.NC;
+    p.L = c.L;
+    p.seg_max = c.seg_max;
     p.force_sub = c.force_exact;
     p.status = c.status;
     const int n_dvt = c.dv / DVT;
-    auto launch = [&](int mode, int z) -> cudaError_t {
+    // `count` CTAs (clusters) per tile column; the index is blockIdx.y +
+    // blockIdx.z * gridDim.y, so that any count fits the grid's limits
+    auto launch = [&](int mode, long long count) -> cudaError_t {
         p.mode = mode;
+        p.n_units = count;
+        const unsigned gy = static_cast<unsigned>(count < 32768 ? count : 32768);
+        const unsigned gz = static_cast<unsigned>((count + gy - 1) / gy);
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
-        cfg.gridDim = dim3(n_dvt, c.H, z);
+        cfg.gridDim = dim3(n_dvt, gy, gz);
         cfg.blockDim = dim3(kThreads, 1, 1);
         cfg.dynamicSmemBytes = L::kAlloc;
         cfg.stream = stream;
@@ -1308,12 +1502,80 @@ int launch_tiles(const ChunkLaunch &c, cudaStream_t stream) {
         }
         return cudaLaunchKernelEx(&cfg, kern, p);
     };
-    cudaError_t e = launch(kModeFull, c.B * c.n_seg);
-    if (e != cudaSuccess || c.n_seg == 1) return static_cast<int>(e);
-    return static_cast<int>(launch(kModeCorrect, c.B * (c.n_seg - 1)));
+    // FULL pass: one CTA (cluster) per range; CORRECT pass: one per (sequence,
+    // segment >= 1), those past a sequence's segment count leave at once
+    cudaError_t e = launch(kModeFull, c.W);
+    if (e != cudaSuccess || c.seg_max == 1) return static_cast<int>(e);
+    return static_cast<int>(
+        launch(kModeCorrect, static_cast<long long>(c.B) * c.H * (c.seg_max - 1)));
+}
+
+template <int DK, int DVT, bool PAIR>
+int max_resident() {
+    using L = Smem<DK, DVT, PAIR>;
+    auto kern = chunk_fwd_kernel<DK, DVT, PAIR>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(L::kAlloc)) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (!PAIR) return sms;   // one CTA per SM (the CTA takes all of TMEM)
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = L::kAlloc;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return clusters;
 }
 
 }  // namespace
+
+int chunk_fwd_max_resident(int dk, int dv_tile, int pair) {
+    // cached per device and kernel variant (the query is a driver round trip)
+    constexpr int kDevs = 64;
+    static std::mutex mu;
+    static int cache[kDevs][6];
+    static bool init = false;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) {
+        cudaGetLastError();
+        return 0;
+    }
+    const int variant = (dk == 128 ? 2 : 0) + (dv_tile == 64 ? 0 : 1) + (dk == 128 && pair ? 2 : 0);
+    std::lock_guard<std::mutex> lock(mu);
+    if (!init) {
+        for (auto &row : cache)
+            for (int &x : row) x = -1;
+        init = true;
+    }
+    int &slot = cache[dev][variant];
+    if (slot < 0) {
+        if (dk == 128 && pair)
+            slot = dv_tile == 64 ? max_resident<128, 64, true>() : max_resident<128, 128, true>();
+        else if (dk == 128)
+            slot = dv_tile == 64 ? max_resident<128, 64, false>() : max_resident<128, 128, false>();
+        else
+            slot = dv_tile == 64 ? max_resident<64, 64, false>() : max_resident<64, 128, false>();
+    }
+    return slot;
+}
 
 int launch_chunk_fwd(const ChunkLaunch &p, cudaStream_t stream) {
     if (p.dk == 64) {

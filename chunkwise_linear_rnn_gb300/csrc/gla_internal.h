@@ -20,19 +20,26 @@ struct ChunkLaunch {
     const float *h0;          // [BH, dk, dv] or null (zero state)
     float *hT;                // [BH, dk, dv] or null
     void *o;                  // bf16 [BH, T, dv]
-    float *ws_state;          // segment summaries [n_seg, BH, dk, dv] (n_seg > 1)
-    float *ws_decay;          // segment total decays [n_seg, BH, dk]   (n_seg > 1)
+    float *ws_state;          // segment summaries [seg_max, BH, dk, dv] (seg_max > 1)
+    float *ws_decay;          // segment total decays [seg_max, BH, dk]   (seg_max > 1)
     float scale;
     int B, H, T, dk, dv;
     int dv_tile;              // 64 or 128
     int pair;                 // 1: the two value tiles of a head run as a 2-CTA cluster
-    int n_seg, seg_chunks;    // sequence segments and chunks per segment
+    // Work split: the chunks of all sequences, one after another, cut into W
+    // ranges of L chunks (the last may be short); NC chunks per sequence;
+    // seg_max = most segments any sequence is cut into (1: no sequence is cut).
+    int NC, L, W, seg_max;
     int force_exact;          // process every chunk in rescaled sub-chunks
     unsigned int *status;     // device status word
 };
 
 // Returns a cudaError_t value (0 on success).
 int launch_chunk_fwd(const ChunkLaunch &p, cudaStream_t stream);
+
+// How many CTAs (clusters, for a CTA pair) of the chunked forward for these
+// head dimensions can run at once on the current device; 0 if unknown.
+int chunk_fwd_max_resident(int dk, int dv_tile, int pair);
 
 // gla_chunk_fwd_ex with the segment scratch supplied by the caller instead of
 // allocated (`scratch_bytes` bytes of device memory, 16-byte aligned; may be
