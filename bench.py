@@ -57,7 +57,7 @@ def peaks():
 # Any change to those sources makes the figure stale: it is then reported as null.
 MEASURED_TRAFFIC = {"workload": "B2-H16-T32768-dk128-dv256", "sources": "2ccab0ebfa65b295",
                     "bytes_per_call": 1615141888 + 507587840 + 35878400 + 512}
-TRAFFIC_SOURCES = ["gla_api.cu", "gla_chunk.cu", "gla_internal.h", "gla_ptx.cuh"]
+TRAFFIC_SOURCES = ["gla_api.cu", "gla_chunk.cu", "gla_chunk_kernel.cuh", "gla_internal.h", "gla_ptx.cuh"]
 
 
 def kernel_sources_hash() -> str:
@@ -80,11 +80,25 @@ def measured_traffic(cfg):
     return MEASURED_TRAFFIC["bytes_per_call"]
 
 
-def chunk_bytes(cfg) -> int:
-    """Algorithmic bytes of one chunked forward: each input read once, each output written once."""
+def chunk_bytes(cfg, n_states: int | None = None) -> int:
+    """Algorithmic bytes of one chunked forward: each input read once, each output written once.
+
+    n_states: the (sequence, head) states read and written (default B * H).
+    """
     per_token = 2 * cfg.dk + 2 * cfg.dk + 2 * cfg.dv + 4 * cfg.dk + 2 * cfg.dv
-    state = cfg.B * cfg.H * cfg.dk * cfg.dv * 4 * (2 if cfg.sigma_h0 is not None else 1)
+    if n_states is None:
+        n_states = cfg.B * cfg.H
+    state = n_states * cfg.dk * cfg.dv * 4 * (2 if cfg.sigma_h0 is not None else 1)
     return cfg.tokens * per_token + state
+
+
+def packed_lengths(total: int, n: int, seed: int) -> list:
+    """A seeded mix of n sequence lengths (log-normal weights, sigma 1) summing to total."""
+    import numpy as np
+    w = np.random.default_rng(seed).lognormal(0.0, 1.0, size=n)
+    lens = np.maximum(1, np.floor(w / w.sum() * total)).astype(np.int64)
+    lens[int(np.argmax(lens))] += total - int(lens.sum())
+    return [int(x) for x in lens]
 
 
 def chunk_flops(cfg, C: int = 64) -> int:
@@ -230,16 +244,47 @@ def chunk_config(args):
 
 def chunk_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_kind):
     import torch
-    from synth import make_config_inputs
-    q, k, v, a, h0 = make_config_inputs(cfg, seed=rank, device=dev)
-    o = torch.empty(cfg.B, cfg.H, cfg.T, cfg.dv, dtype=torch.bfloat16, device=dev)
-    hT = torch.empty(cfg.B, cfg.H, cfg.dk, cfg.dv, dtype=torch.float32, device=dev)
+    from synth import make_chunk_inputs, make_config_inputs
     stream = torch.cuda.current_stream(dev)
+    n_states = None
+    packed = None
+    if args.varlen:
+        # the same tokens per head, packed: --varlen sequences of mixed lengths
+        # through gla_chunk_fwd_varlen (q, k, v, gates drawn as for the workload)
+        per_head = cfg.B * cfg.T
+        lens = packed_lengths(per_head, args.varlen, seed=1234 + rank)
+        cu = [0]
+        for n in lens:
+            cu.append(cu[-1] + n)
+        q, k, v, a, _ = make_chunk_inputs(1, cfg.H, per_head, cfg.dk, cfg.dv, sigma_z=cfg.sigma_z,
+                                          tau=cfg.tau, seed=rank, device=dev)
+        q, k, v, a = (t[0] for t in (q, k, v, a))
+        h0 = None
+        if cfg.sigma_h0 is not None:
+            g = torch.Generator(device=dev)
+            g.manual_seed(5678 + rank)
+            h0 = torch.randn(len(lens), cfg.H, cfg.dk, cfg.dv, generator=g, device=dev,
+                             dtype=torch.float32).mul_(cfg.sigma_h0)
+        o = torch.empty(cfg.H, per_head, cfg.dv, dtype=torch.bfloat16, device=dev)
+        hT = torch.empty(len(lens), cfg.H, cfg.dk, cfg.dv, dtype=torch.float32, device=dev)
+        n_states = len(lens) * cfg.H
+        srt = sorted(lens)
+        packed = {"sequences": len(lens), "min_len": srt[0], "median_len": srt[len(srt) // 2],
+                  "max_len": srt[-1], "lengths": "log-normal weights (sigma 1), seed 1234"}
 
-    def step():
-        gla.gla_chunk_fwd(q, k, v, a, cfg.scale, h0, out=o, final_state=hT)
+        def step():
+            gla.gla_chunk_fwd_varlen(q, k, v, a, cu, cfg.scale, h0, out=o, final_state=hT)
 
-    launches_per_step = gla.gla_chunk_fwd_plan(cfg.B, cfg.H, cfg.T, cfg.dk, cfg.dv)["launches"]
+        launches_per_step = gla.gla_chunk_fwd_varlen_plan(cu, cfg.H, cfg.dk, cfg.dv)["launches"]
+    else:
+        q, k, v, a, h0 = make_config_inputs(cfg, seed=rank, device=dev)
+        o = torch.empty(cfg.B, cfg.H, cfg.T, cfg.dv, dtype=torch.bfloat16, device=dev)
+        hT = torch.empty(cfg.B, cfg.H, cfg.dk, cfg.dv, dtype=torch.float32, device=dev)
+
+        def step():
+            gla.gla_chunk_fwd(q, k, v, a, cfg.scale, h0, out=o, final_state=hT)
+
+        launches_per_step = gla.gla_chunk_fwd_plan(cfg.B, cfg.H, cfg.T, cfg.dk, cfg.dv)["launches"]
     for _ in range(args.warmup):
         step()
     barrier()
@@ -263,7 +308,7 @@ def chunk_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_
     ms_per_step = total_ms / args.steps
     tokens_all = cfg.tokens * world
     value = tokens_all / (ms_per_step / 1e3)
-    byts = chunk_bytes(cfg)
+    byts = chunk_bytes(cfg, n_states)
     achieved_gbs = byts / (per_launch_ms / 1e3) / 1e9
     clocks = clk.summary()
 
@@ -271,7 +316,7 @@ def chunk_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_
     # buffers; every call copies its inputs in and its outputs out (pipelined
     # over groups of heads), all inside the timed region
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.varlen:
         hq, hk, hv, ha = (t.cpu().pin_memory() for t in (q, k, v, a))
         hh0 = None if h0 is None else h0.cpu().pin_memory()
         ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
@@ -317,12 +362,14 @@ def chunk_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": cfg.name, "B": cfg.B, "H": cfg.H, "T": cfg.T, "dk": cfg.dk,
+        "config": {"workload": cfg.name + (f"-packed{args.varlen}" if args.varlen else ""),
+                   "B": cfg.B, "H": cfg.H, "T": cfg.T, "dk": cfg.dk,
                    "dv": cfg.dv, "chunk": 128, "replicas": world,
                    "l2": "inputs (%.2f GB) larger than L2; no flush" % (byts / 1e9)},
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": pk["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved_gbs / pk["hbm_gbs"],
-                     "traffic": measured_traffic(cfg), "traffic_unit": "bytes per call",
+                     "traffic": None if args.varlen else measured_traffic(cfg),
+                     "traffic_unit": "bytes per call",
                      "peak_kind": pk_kind, "kernel": "chunk_fwd_kernel",
                      "algorithmic_bytes_per_launch": byts,
                      "flops_per_launch": chunk_flops(cfg),
@@ -333,6 +380,8 @@ def chunk_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if packed is not None:
+        line["config"]["packed"] = packed
     return line
 
 
@@ -475,6 +524,9 @@ def main():
     ap.add_argument("--batch", type=int, default=0, help="override the workload's B")
     ap.add_argument("--heads", type=int, default=0, help="override the workload's H")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--varlen", type=int, default=0,
+                    help="pack each head's tokens into this many sequences of mixed lengths "
+                         "(gla_chunk_fwd_varlen; no e2e leg)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-seconds", type=float, default=15.0,
                     help="CPU seconds per oracle sample")

@@ -23,7 +23,7 @@ import torch
 from . import _lib
 from ._lib import GlaChunkOptions, GlaError, status_string  # noqa: F401
 
-__all__ = ["gla_chunk_fwd", "gla_chunk_fwd_plan", "gla_recurrent_step", "gla_last_device_status", "GlaError",
+__all__ = ["gla_chunk_fwd", "gla_chunk_fwd_varlen", "gla_chunk_fwd_varlen_plan", "gla_chunk_fwd_plan", "gla_recurrent_step", "gla_last_device_status", "GlaError",
            "status_string", "library_path"]
 
 library_path = _lib.LIB_PATH
@@ -96,6 +96,86 @@ def gla_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: 
             _stream(dev))
     _lib.check(st, "gla_chunk_fwd")
     return out, hT
+
+
+def gla_chunk_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                         log_alpha: torch.Tensor, cu_seqlens, scale: float | None = None,
+                         h0: torch.Tensor | None = None, output_final_state: bool = True, *,
+                         out: torch.Tensor | None = None, final_state: torch.Tensor | None = None,
+                         segments: int = 0, dv_tile: int = 0, force_exact: bool = False,
+                         cta_pair: int = 0):
+    """Chunkwise-parallel GLA forward over a packed batch of variable-length sequences.
+
+    ``q``, ``k``, ``log_alpha`` are ``[H, T_total, dk]`` and ``v`` is
+    ``[H, T_total, dv]`` (a leading batch dimension of 1 is accepted too);
+    sequence ``n`` holds rows ``cu_seqlens[n] : cu_seqlens[n+1]`` of every head.
+    ``cu_seqlens`` is a host sequence of ``N + 1`` ints (list, tuple or CPU
+    tensor).  ``h0`` and the returned ``hT`` are ``[N, H, dk, dv]``.
+    Returns ``(o, hT)`` with ``o`` shaped like ``v``.
+    """
+    squeeze = q.dim() == 4
+    if squeeze:
+        if q.shape[0] != 1:
+            raise ValueError("a packed batch has a leading dimension of 1")
+        q, k, v, log_alpha = q[0], k[0], v[0], log_alpha[0]
+        if out is not None:
+            out = out[0]
+    if q.dim() != 3:
+        raise ValueError("q must be [H, T_total, dk]")
+    H, T_total, dk = q.shape
+    dv = v.shape[-1]
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("q must be on a CUDA device")
+    cu = [int(x) for x in (cu_seqlens.tolist() if torch.is_tensor(cu_seqlens) else cu_seqlens)]
+    N = len(cu) - 1
+    if N < 1:
+        raise ValueError("cu_seqlens needs at least two entries")
+    _need(q, "q", torch.bfloat16, (H, T_total, dk), dev)
+    _need(k, "k", torch.bfloat16, (H, T_total, dk), dev)
+    _need(v, "v", torch.bfloat16, (H, T_total, dv), dev)
+    _need(log_alpha, "log_alpha", torch.float32, (H, T_total, dk), dev)
+    if h0 is not None:
+        _need(h0, "h0", torch.float32, (N, H, dk, dv), dev)
+    if out is None:
+        out = torch.empty(H, T_total, dv, dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, (H, T_total, dv), dev)
+    hT = None
+    if output_final_state:
+        hT = final_state if final_state is not None else torch.empty(
+            N, H, dk, dv, dtype=torch.float32, device=dev)
+        _need(hT, "final_state", torch.float32, (N, H, dk, dv), dev)
+    if scale is None:
+        scale = dk ** -0.5
+    opts = GlaChunkOptions(segments=int(segments), dv_tile=int(dv_tile),
+                           force_exact=1 if force_exact else 0, cta_pair=int(cta_pair))
+    cu_arr = (ctypes.c_int * len(cu))(*cu)
+    with torch.cuda.device(dev):
+        st = _lib.lib().gla_chunk_fwd_varlen_ex(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), log_alpha.data_ptr(), float(scale),
+            None if h0 is None else h0.data_ptr(), out.data_ptr(),
+            None if hT is None else hT.data_ptr(), cu_arr, N, H, T_total, dk, dv,
+            ctypes.byref(opts), _stream(dev))
+    _lib.check(st, "gla_chunk_fwd_varlen")
+    return (out.unsqueeze(0) if squeeze else out), hT
+
+
+def gla_chunk_fwd_varlen_plan(cu_seqlens, H: int, dk: int, dv: int, *, segments: int = 0,
+                              dv_tile: int = 0, force_exact: bool = False,
+                              cta_pair: int = 0) -> dict:
+    """The launch plan gla_chunk_fwd_varlen would use for this packed batch (no GPU work)."""
+    cu = [int(x) for x in (cu_seqlens.tolist() if torch.is_tensor(cu_seqlens) else cu_seqlens)]
+    opts = GlaChunkOptions(segments=int(segments), dv_tile=int(dv_tile),
+                           force_exact=1 if force_exact else 0, cta_pair=int(cta_pair))
+    nseg, tile, launches = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    sb = ctypes.c_ulong()
+    st = _lib.lib().gla_chunk_fwd_varlen_plan((ctypes.c_int * len(cu))(*cu), len(cu) - 1, H,
+                                               cu[-1], dk, dv, ctypes.byref(opts),
+                                               ctypes.byref(nseg), ctypes.byref(tile),
+                                               ctypes.byref(launches), ctypes.byref(sb))
+    _lib.check(st, "gla_chunk_fwd_varlen_plan")
+    return {"segments": nseg.value, "dv_tile": tile.value, "launches": launches.value,
+            "scratch_bytes": sb.value}
 
 
 def gla_chunk_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: torch.Tensor,

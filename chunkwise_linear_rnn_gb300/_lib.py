@@ -57,6 +57,14 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.gla_chunk_fwd_host.argtypes = [vp, vp, vp, fp, f, fp, vp, fp, i, i, i, i, i, vp]
     lib.gla_chunk_fwd_host.restype = i
     ip = ctypes.POINTER(ctypes.c_int)
+    lib.gla_chunk_fwd_varlen_plan.argtypes = [ip, i, i, i, i, i, ctypes.POINTER(GlaChunkOptions),
+                                              ip, ip, ip, ctypes.POINTER(ctypes.c_ulong)]
+    lib.gla_chunk_fwd_varlen_plan.restype = i
+    lib.gla_chunk_fwd_varlen.argtypes = [vp, vp, vp, fp, f, fp, vp, fp, ip, i, i, i, i, i, vp]
+    lib.gla_chunk_fwd_varlen.restype = i
+    lib.gla_chunk_fwd_varlen_ex.argtypes = [vp, vp, vp, fp, f, fp, vp, fp, ip, i, i, i, i, i,
+                                            ctypes.POINTER(GlaChunkOptions), vp]
+    lib.gla_chunk_fwd_varlen_ex.restype = i
     lib.gla_chunk_fwd_plan.argtypes = [i, i, i, i, i, ctypes.POINTER(GlaChunkOptions), ip, ip, ip,
                                        ctypes.POINTER(ctypes.c_ulong)]
     lib.gla_chunk_fwd_plan.restype = i

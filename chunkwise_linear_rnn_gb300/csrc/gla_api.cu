@@ -9,6 +9,7 @@
 #include <cstdint>
 #include <algorithm>
 #include <mutex>
+#include <vector>
 
 #include "gla.h"
 #include "gla_internal.h"
@@ -255,9 +256,194 @@ int chunk_fwd_with_scratch(const void *q, const void *k, const void *v, const fl
     p.L = pl.L;
     p.W = pl.W;
     p.seg_max = pl.seg_max;
+    p.total = static_cast<long long>(BH) * pl.NC;
+    p.seqs = nullptr;
+    p.NS = 0;
     p.force_exact = op.force_exact ? 1 : 0;
     p.status = dev->status;
     return launch_chunk_fwd(p, stream) == 0 ? GLA_OK : GLA_ERR_LAUNCH;
+}
+
+// ---------------------------------------------------------------- packed batches
+
+namespace {
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Packed variable-length batch: per sequence n, {first row, length, chunks,
+// chunk offset}, and the chunks of one head in all.
+struct Packed {
+    std::vector<int4> seqs;
+    long long chunks = 0;
+    int max_chunks = 0;
+};
+
+// Checks cu_seqlens (N + 1 offsets, from 0 to T_total, nondecreasing) and
+// builds the sequence table.  Returns a GLA status.
+int packed_layout(const int *cu_seqlens, int N, int T_total, Packed *pk) {
+    if (!cu_seqlens || N <= 0 || T_total < 0) return GLA_ERR_ARG;
+    if (cu_seqlens[0] != 0 || cu_seqlens[N] != T_total) return GLA_ERR_ARG;
+    pk->seqs.resize(N);
+    long long off = 0;
+    for (int n = 0; n < N; ++n) {
+        const int len = cu_seqlens[n + 1] - cu_seqlens[n];
+        if (len < 0) return GLA_ERR_ARG;
+        const int nch = (len + 127) / 128;
+        if (off > 0x7fffffffLL) return GLA_ERR_ARG;
+        pk->seqs[n] = make_int4(cu_seqlens[n], len, nch, static_cast<int>(off));
+        off += nch;
+        pk->max_chunks = std::max(pk->max_chunks, nch);
+    }
+    pk->chunks = off;
+    return GLA_OK;
+}
+
+// Launch plan for a packed batch: ranges of equal chunk counts over all
+// sequences' chunks (the sequences differ in length, so cuts follow the
+// chunk count, not the sequences), at least kMinRange chunks long.
+Plan make_plan_packed(const Packed &pk, int H, int dk, int dv, const gla_chunk_options &op,
+                      int sm_count) {
+    Plan pl;
+    pl.dv_tile = op.dv_tile ? op.dv_tile : (dv >= 128 ? 128 : 64);
+    pl.pair = dk == 128 && dv == 2 * pl.dv_tile && op.cta_pair >= 0;
+    pl.NC = pk.max_chunks;
+    const long long total = static_cast<long long>(H) * pk.chunks;
+    long long L;
+    if (op.segments > 0) {
+        L = (pk.max_chunks + op.segments - 1) / op.segments;
+    } else {
+        const int n_dvt = dv / pl.dv_tile;
+        int resident = gla::chunk_fwd_max_resident(dk, pl.dv_tile, pl.pair ? 1 : 0);
+        if (resident <= 0) resident = pl.pair ? sm_count / 2 : sm_count;
+        const long long ranges = std::max<long long>(1, pl.pair ? resident : resident / n_dvt);
+        L = (total + ranges - 1) / ranges;
+        if (L < kMinRange) L = kMinRange;
+        if (L > pk.max_chunks) L = pk.max_chunks;
+    }
+    if (L < 1) L = 1;
+    pl.L = static_cast<int>(L);
+    pl.W = static_cast<int>((total + L - 1) / L);
+    pl.seg_max = 1;
+    for (size_t n = 0; n < pk.seqs.size(); ++n) {
+        const int4 e = pk.seqs[n];
+        if (e.z == 0) continue;
+        for (int h = 0; h < H; ++h) {
+            const long long a = static_cast<long long>(H) * e.w + static_cast<long long>(h) * e.z;
+            pl.seg_max = std::max(pl.seg_max, 1 + static_cast<int>((a + e.z - 1) / L - a / L));
+        }
+    }
+    return pl;
+}
+
+}  // namespace
+
+int chunk_fwd_packed(const void *q, const void *k, const void *v, const float *log_alpha,
+                     float scale, const float *h0, void *o, float *hT, const int *cu_seqlens,
+                     int N, int H, int T_total, int dk, int dv, const gla_chunk_options *opts,
+                     cudaStream_t stream) {
+    if (!q || !k || !v || !log_alpha || !o) return GLA_ERR_ARG;
+    if (N <= 0 || H <= 0 || T_total < 0) return GLA_ERR_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_alpha) ||
+        !aligned16(o) || (h0 && !aligned16(h0)) || (hT && !aligned16(hT)))
+        return GLA_ERR_ARG;
+    if (!dk_ok(dk) || !dv_ok(dv)) return GLA_ERR_SHAPE;
+    gla_chunk_options o_def = {};
+    const gla_chunk_options &op = opts ? *opts : o_def;
+    if (!options_ok(dv, op)) return GLA_ERR_ARG;
+    if (static_cast<long long>(N) * H > 0x7fffffffLL) return GLA_ERR_ARG;
+    Packed pk;
+    int st = packed_layout(cu_seqlens, N, T_total, &pk);
+    if (st != GLA_OK) return st;
+
+    DeviceInfo *dev = nullptr;
+    st = current_device(&dev);
+    if (st != GLA_OK) return st;
+    EncodeTiledFn enc = nullptr;
+    st = encode_fn(&enc);
+    if (st != GLA_OK) return st;
+
+    // empty sequences: hT = h0 (zero without h0); nothing else to do for them
+    const size_t state_elems = static_cast<size_t>(H) * dk * dv;
+    if (hT && hT != h0) {
+        for (int n = 0; n < N; ++n) {
+            if (pk.seqs[n].y != 0) continue;
+            float *dst = hT + n * state_elems;
+            const cudaError_t e =
+                h0 ? cudaMemcpyAsync(dst, h0 + n * state_elems, state_elems * sizeof(float),
+                                     cudaMemcpyDeviceToDevice, stream)
+                   : cudaMemsetAsync(dst, 0, state_elems * sizeof(float), stream);
+            if (e != cudaSuccess) {
+                cudaGetLastError();
+                return GLA_ERR_LAUNCH;
+            }
+        }
+    }
+    if (pk.chunks == 0) return GLA_OK;
+
+    const long long NH = static_cast<long long>(N) * H;
+    const Plan pl = make_plan_packed(pk, H, dk, dv, op, dev->sm_count);
+    const size_t table_bytes = align256(pk.seqs.size() * sizeof(int4));
+    const size_t state_bytes =
+        pl.seg_max > 1 ? static_cast<size_t>(pl.seg_max) * NH * dk * dv * sizeof(float) : 0;
+    const size_t decay_bytes =
+        pl.seg_max > 1 ? static_cast<size_t>(pl.seg_max) * NH * dk * sizeof(float) : 0;
+    void *scratch = nullptr;
+    if (cudaMallocAsync(&scratch, table_bytes + state_bytes + decay_bytes, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return GLA_ERR_ALLOC;
+    }
+    int result = GLA_OK;
+    // the table goes up with the launch; a copy from pageable memory has
+    // taken the host data by the time the call returns
+    if (cudaMemcpyAsync(scratch, pk.seqs.data(), pk.seqs.size() * sizeof(int4),
+                        cudaMemcpyHostToDevice, stream) != cudaSuccess) {
+        cudaGetLastError();
+        result = GLA_ERR_LAUNCH;
+    }
+    ChunkLaunch p;
+    if (result == GLA_OK &&
+        (!make_map(enc, &p.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dk, T_total, H, 64, 128,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+         !make_map(enc, &p.tm_k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dk, T_total, H, 64, 128,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+         !make_map(enc, &p.tm_a, log_alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dk, T_total, H,
+                   pl.pair ? dk / 2 : dk, 128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+         !make_map(enc, &p.tm_v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dv, T_total, H, 64, 128,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+         !make_map(enc, &p.tm_o32, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dv, T_total, H, 64, 32,
+                   CU_TENSOR_MAP_SWIZZLE_128B)))
+        result = GLA_ERR_LAUNCH;
+    if (result == GLA_OK) {
+        char *ws = static_cast<char *>(scratch) + table_bytes;
+        p.q = q;
+        p.k = k;
+        p.log_alpha = log_alpha;
+        p.h0 = h0;
+        p.hT = hT;
+        p.o = o;
+        p.ws_state = pl.seg_max > 1 ? reinterpret_cast<float *>(ws) : nullptr;
+        p.ws_decay = pl.seg_max > 1 ? reinterpret_cast<float *>(ws + state_bytes) : nullptr;
+        p.scale = scale;
+        p.B = N;
+        p.H = H;
+        p.T = T_total;
+        p.dk = dk;
+        p.dv = dv;
+        p.dv_tile = pl.dv_tile;
+        p.pair = pl.pair ? 1 : 0;
+        p.NC = pl.NC;
+        p.L = pl.L;
+        p.W = pl.W;
+        p.seg_max = pl.seg_max;
+        p.total = static_cast<long long>(H) * pk.chunks;
+        p.seqs = static_cast<const int4 *>(scratch);
+        p.NS = N;
+        p.force_exact = op.force_exact ? 1 : 0;
+        p.status = dev->status;
+        if (launch_chunk_fwd(p, stream) != 0) result = GLA_ERR_LAUNCH;
+    }
+    cudaFreeAsync(scratch, stream);
+    return result;
 }
 
 }  // namespace gla
@@ -332,6 +518,57 @@ int gla_chunk_fwd_plan(int B, int H, int T, int dk, int dv, const gla_chunk_opti
     if (launches) *launches = pl.seg_max > 1 ? 2 : 1;
     if (scratch_bytes) *scratch_bytes = scratch_needed(pl, B, H, dk, dv);
     return GLA_OK;
+}
+
+int gla_chunk_fwd_varlen_ex(const void *q, const void *k, const void *v, const float *log_alpha,
+                            float scale, const float *h0, void *o, float *hT,
+                            const int *cu_seqlens, int N, int H, int T_total, int dk, int dv,
+                            const gla_chunk_options *opts, cudaStream_t stream) {
+    return gla::chunk_fwd_packed(q, k, v, log_alpha, scale, h0, o, hT, cu_seqlens, N, H, T_total,
+                                 dk, dv, opts, stream);
+}
+
+int gla_chunk_fwd_varlen_plan(const int *cu_seqlens, int N, int H, int T_total, int dk, int dv,
+                              const gla_chunk_options *opts, int *n_segments, int *dv_tile,
+                              int *launches, unsigned long *scratch_bytes) {
+    using namespace gla;
+    if (N <= 0 || H <= 0 || T_total < 0) return GLA_ERR_ARG;
+    if (static_cast<long long>(N) * H > 0x7fffffffLL) return GLA_ERR_ARG;
+    if (!dk_ok(dk) || !dv_ok(dv)) return GLA_ERR_SHAPE;
+    gla_chunk_options o_def = {};
+    const gla_chunk_options &op = opts ? *opts : o_def;
+    if (!options_ok(dv, op)) return GLA_ERR_ARG;
+    Packed pk;
+    int st = packed_layout(cu_seqlens, N, T_total, &pk);
+    if (st != GLA_OK) return st;
+    DeviceInfo *dev = nullptr;
+    st = current_device(&dev);
+    if (st != GLA_OK) return st;
+    if (pk.chunks == 0) {
+        if (n_segments) *n_segments = 0;
+        if (dv_tile) *dv_tile = 0;
+        if (launches) *launches = 0;
+        if (scratch_bytes) *scratch_bytes = 0;
+        return GLA_OK;
+    }
+    const Plan pl = make_plan_packed(pk, H, dk, dv, op, dev->sm_count);
+    const size_t NH = static_cast<size_t>(N) * H;
+    if (n_segments) *n_segments = pl.seg_max;
+    if (dv_tile) *dv_tile = pl.dv_tile;
+    if (launches) *launches = pl.seg_max > 1 ? 2 : 1;
+    if (scratch_bytes)
+        *scratch_bytes = align256(pk.seqs.size() * sizeof(int4)) +
+                         (pl.seg_max > 1 ? static_cast<size_t>(pl.seg_max) * NH * dk * (dv + 1) *
+                                               sizeof(float)
+                                         : 0);
+    return GLA_OK;
+}
+
+int gla_chunk_fwd_varlen(const void *q, const void *k, const void *v, const float *log_alpha,
+                         float scale, const float *h0, void *o, float *hT, const int *cu_seqlens,
+                         int N, int H, int T_total, int dk, int dv, cudaStream_t stream) {
+    return gla::chunk_fwd_packed(q, k, v, log_alpha, scale, h0, o, hT, cu_seqlens, N, H, T_total,
+                                 dk, dv, nullptr, stream);
 }
 
 int gla_chunk_fwd(const void *q, const void *k, const void *v, const float *log_alpha,

@@ -1,1551 +1,12 @@
-// gla_chunk.cu — chunkwise-parallel GLA forward on sm_103a tensor cores.
-//
-// Method ("Gated Linear Attention (GLA): Mathematical Foundations, ..."
-// (llms.blog), sections "Sequence Partitioning and State Factorization",
-// "Cumulative Decay Representation", "Intra-Chunk Matrix Multiplications",
-// "Inter-Chunk Recurrence and Output Projection", "I/O-Aware Kernel Design"):
-// per chunk of C tokens with A = log alpha and Gamma = in-chunk inclusive
-// prefix sum of A (per key channel),
-//     O     = scale * ( M V + (Q * e^Gamma) S_prev ),
-//             M_ij = sum_d Q_id K_jd e^(Gamma_id - Gamma_jd)  for j <= i, else 0
-//     S_new = diag(e^Gamma_C) S_prev + (K * e^(Gamma_C - Gamma))^T V,
-// with the state S held on chip (TMEM, fp32) across the whole chunk loop.
-//
-// Rescaling (bounded exponents).  With a reference r (the Gamma value just
-// before the first token of a block of tokens), Qh = Q e^(Gamma - r) <= |Q| and
-// Kh = K e^(r - Gamma): the decayed score block factorises as P = Qh Kh^T and
-// the state update as S_new = diag(e^(Gamma_end - r)) (S_prev + Kh^T V).  Both
-// are plain tensor-core products.  A chunk is processed as one block when
-// every |Gamma - r| <= kExpBound over it (the common case); otherwise it is
-// cut into equal power-of-two sub-chunks, each with its own reference, small
-// enough that the bound holds in each (sub-chunk rescaling).  A single token
-// whose own |log alpha| exceeds the bound is clamped to it: the state term
-// that changes is below e^-30 ~ 9e-14 of the state, under fp32 resolution.
-// Masked score entries are selected away, never multiplied by zero.
-//
-// Precision.  bf16 operands carry 8 significant bits; the two roundings that
-// dominate the output error are removed by splitting the operand into a bf16
-// pair x = hi + lo: the rescaled keys Kh (score and state products) and the
-// score block P (the A operand of P V, kept in TMEM).
-//
-// CTA organisation (one CTA per (batch, head, value-column tile, sequence
-// segment); 448 threads):
-//   warp 13 "tma": streams each chunk's A (fp32), Q, K (bf16, 128-byte swizzle,
-//     already in the K-major operand layout) and V (MN-major) tiles with TMA,
-//     each as soon as the tile it replaces has been consumed.
-//   warps 0-7 "prep": two channels x 32 tokens per thread (dk = 128).  As
-//     soon as the A tile lands (before Q and K): the fp32 prefix sum per token
-//     part, written in place of A, the exponent-bound check that picks one
-//     block or rescaled sub-chunks, and the state factor and correction-window
-//     bookkeeping.  When Q and K land: Gamma = part offset + local sum, and the
-//     elementwise in-place rescale to Qh and Kh_hi plus Kh_lo.
-//   warp 12 "mma": one thread issues every tcgen05.mma and commit.
-//   warps 8-11 "tmem": thread i owns TMEM lane i — causal mask and hi/lo split
-//     of P, the per-row state scale and its bf16 copy for the next chunk's
-//     Qh S product, and the output epilogue.
-// The O accumulator is double-buffered so the next chunk's products overlap
-// the current chunk's epilogue; the next chunk's Q/K/A loads overlap the
-// current chunk's P V product and epilogue.
-//
-// Sequence segments (when B*H*tiles is too small to fill the GPU): segment
-// s > 0 first runs from a zero state (FULL mode), storing its end state and
-// total decay.  Its outputs depend on the true start state only through
-// (Q * e^Gamma_seg) S_start, where Gamma_seg is the decay since the segment
-// start; once every channel has decayed past e^-20.8 = 2^-30 that term is
-// below 2^-30 of the start state's read-out, far below the bf16 resolution of
-// the output, and the FULL outputs are stored as they are.
-// The chunks before that point are recomputed by a second launch (CORRECT
-// mode) from the exact start state, obtained by scanning the segment summaries
-// S_start(s+1) = diag(e^G_s) S_start(s) + S*_s.
-#include <cuda.h>
-#include <cuda_bf16.h>
-#include <cuda_runtime.h>
-
-#include <cstdint>
+// gla_chunk.cu — the chunked forward's fixed-length instantiations, its
+// dispatch, and the occupancy query the launch plans use.  The kernel itself
+// is in gla_chunk_kernel.cuh.
 #include <mutex>
 
-#include "gla_internal.h"
-#include "gla_ptx.cuh"
+#include "gla_chunk_kernel.cuh"
 
 namespace gla {
-namespace {
 
-constexpr int kChunk = 128;
-constexpr int kPrepWarps = 8;           // warps 0-7
-constexpr int kPrepThreads = 32 * kPrepWarps;
-constexpr int kTmemWarp0 = 8;           // warps 8-11
-constexpr int kMmaWarp = 12;
-constexpr int kTmaWarp = 13;
-constexpr int kThreads = 448;           // 14 warps
-constexpr float kExpBound = 30.f;
-constexpr float kWindowCut = 20.79441542f;  // 30 ln 2
-// The fast path keeps in-chunk prefix sums in log2 units (Gamma log2 e), so
-// that every exponential is one ex2.
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kExpBound2 = kExpBound * kLog2e;
-constexpr uint32_t kBlk = kChunk * 128;     // one 64-column block of a 128-row tile
-
-constexpr int kItemLast = 1;      // last item of its chunk: releases the chunk's V stage
-constexpr int kItemStore = 2;     // store this item's output rows
-constexpr int kItemEnd = 4;       // end of the item stream
-constexpr int kItemPieceEnd = 8;  // last item of a piece (FULL pass): its end state is stored
-
-constexpr int kModeFull = 0, kModeCorrect = 1;
-
-// One MMA work item: sequence bh, chunk start t0, token rows [r0, r1), flags,
-// chunk counter lc, and (CTA pair) the index of the operand exchange it
-// needs, or -1.
-struct ItemInfo {
-    int t0, r0, r1, flags, lc, xi, bh, pad;
-};
-
-// A chunk load request (t0 of sequence bh), or the end of the requests.
-struct ChunkReq {
-    int t0, first_item, end, bh;
-};
-
-
-enum Bar {
-    kBarQkFull = 0, kBarQkEmpty, kBarItem0, kBarItem1, kBarPFull, kBarPSplit, kBarSDone, kBarSReady,
-    kBarOFull0, kBarOFull1, kBarOFree0, kBarOFree1, kBarVFull0, kBarVFull1, kBarVEmpty0,
-    kBarVEmpty1, kBarAFull, kBarQkRaw, kBarReq, kBarXchg0, kBarXchg1, kBarVerd0, kBarVerd1,
-    kNumBars
-};
-// arrival counts, in enum order (a CTA pair doubles kBarQkEmpty: both MMAs commit to it)
-__device__ constexpr uint32_t kBarCounts[kNumBars] = {kPrepWarps, 1, 1, 1, 1, 4, 1, 4, 1, 1, 4, 4,
-                                                      1, 1, 4, 4, 1, 1, 1, 1, 1, 1, 1};
-
-template <int DK, int DVT, bool PAIR>
-struct Smem {
-    static constexpr int kDKA = PAIR ? DK / 2 : DK;       // key channels prepared here
-    static constexpr uint32_t kQBytes = kChunk * DK * 2;
-    static constexpr uint32_t kQ = 0;                     // Qh (rescaled in place when single)
-    static constexpr uint32_t kK = kQ + kQBytes;          // Kh_hi
-    static constexpr uint32_t kKlo = kK + kQBytes;        // Kh_lo
-    static constexpr uint32_t kA = kKlo + kQBytes;        // fp32 log gates [128][kDKA]
-    static constexpr uint32_t kABytes = kChunk * kDKA * 4;
-    static constexpr uint32_t kRaw = kA + kABytes;        // pair: raw Q, K of this CTA's channels
-    static constexpr uint32_t kRawBytes = PAIR ? 2 * kBlk : 0;
-    static constexpr uint32_t kVBytes = kChunk * DVT * 2;
-    static constexpr uint32_t kSBlk = DK * 128;
-    static constexpr uint32_t kSBytes = DK * DVT * 2;
-    // V tiles: two slots where they fit (the next chunk's V loads while this
-    // chunk's products read the other slot), else one
-    static constexpr uint32_t kRest = 2 * DK * 4 + 64 + 16 + 16 + 8 * kNumBars + 16 + 1024;
-    static constexpr int kVSlots =
-        (kRaw + kRawBytes + 2 * kVBytes + kSBytes + kRest) <= 232448u ? 2 : 1;
-    static constexpr uint32_t kV = kRaw + kRawBytes;      // V slots
-    static constexpr uint32_t kS = kV + kVSlots * kVBytes;
-    static constexpr uint32_t kG = kS + kSBytes;          // float [2][DK]: state scale per item
-    static constexpr uint32_t kItem = kG + 2 * DK * 4;    // ItemInfo[2]
-    static constexpr uint32_t kReq = kItem + 64;          // ChunkReq
-    static constexpr uint32_t kVerd = kReq + 16;          // pair: the peer's verdicts [2]
-    static constexpr uint32_t kBar = kVerd + (PAIR ? 16 : 0);  // mbarriers
-    static constexpr uint32_t kMisc = kBar + 8 * kNumBars;  // tmem slot
-    static constexpr uint32_t kTotal = kMisc + 16;
-    // At least 120 KB so that only one CTA fits on an SM: each CTA allocates
-    // all 512 TMEM columns.
-    static constexpr uint32_t kAlloc = (kTotal + 1024) > 122880u ? (kTotal + 1024) : 122880u;
-    static_assert(kAlloc <= 232448, "shared memory budget exceeded");
-    static_assert(!PAIR || DK == 128, "CTA pairs split 128 key channels into two 64-channel blocks");
-    static_assert(kG % 16 == 0, "bulk copies move 16-byte units");
-};
-
-// TMEM columns: P [0,128), O0 [128,128+DVT), O1, S after them.  P holds the
-// fp32 scores of key tokens j = column; each 16-column piece (tokens 16 p ..
-// 16 p + 15) is then replaced in place by its bf16 hi pairs (first 8 columns)
-// and lo pairs (last 8), the A operand of the P V products.
-template <int DVT>
-struct Tmem {
-    static constexpr uint32_t kP = 0, kO0 = 128, kO1 = 128 + DVT, kS = 128 + 2 * DVT;
-    static constexpr uint32_t kCols = 512;
-};
-
-struct KParams {
-    CUtensorMap tm_q, tm_k, tm_a, tm_v, tm_o32;
-    const uint32_t *q;  // bf16 pairs
-    const uint32_t *k;
-    const float2 *a;
-    const float *h0;
-    float *hT;
-    __nv_bfloat16 *o;
-    float *ws_state;    // [seg_max][BH][DK][dv]: segment end states S*
-    float *ws_decay;    // [seg_max][BH][DK]: segment total log-decays G
-    float scale;
-    int BH, T, dv;
-    // Work split: the chunks of all BH sequences, one after another, cut into
-    // ranges of L chunks, one range per CTA (per cluster for a CTA pair) of
-    // the FULL pass.  A cut inside a sequence starts a new segment of it.
-    int NC;        // chunks per sequence
-    int L;         // chunks per range
-    int seg_max;   // most segments any sequence has
-    int mode, force_sub;
-    long long n_units;   // CTAs (clusters) per tile column in this launch
-    unsigned int *status;
-};
-
-// Segment geometry of the work split (identical on the host).  Sequence u
-// occupies global chunks [u NC, (u+1) NC); cuts fall at multiples of L.
-__device__ __forceinline__ int nseg_of(const KParams &p, int u) {
-    const long long a = static_cast<long long>(u) * p.NC;
-    return 1 + static_cast<int>((a + p.NC - 1) / p.L - a / p.L);
-}
-__device__ __forceinline__ int seg_start(const KParams &p, int u, int s) {
-    if (s == 0) return 0;
-    const long long a = static_cast<long long>(u) * p.NC;
-    return static_cast<int>((a / p.L + s) * p.L - a);
-}
-
-// End (global chunk) of this CTA's FULL-pass range, recomputed from the block
-// index where needed instead of being held in registers.
-__device__ __forceinline__ long long full_range_end(const KParams &p) {
-    const long long unit = blockIdx.y + static_cast<long long>(blockIdx.z) * gridDim.y;
-    return min((unit + 1) * p.L, static_cast<long long>(p.BH) * p.NC);
-}
-
-// One piece of a CTA's range: chunks [c0, c1) of sequence u, its segment seg.
-struct Piece {
-    int u, c0, c1, seg;
-};
-
-// The piece that starts at global chunk g of a range ending at g_end.
-__device__ __forceinline__ Piece piece_at(const KParams &p, long long g, long long g_end) {
-    Piece pc;
-    pc.u = static_cast<int>(g / p.NC);
-    pc.c0 = static_cast<int>(g - static_cast<long long>(pc.u) * p.NC);
-    pc.c1 = static_cast<int>(min(static_cast<long long>(p.NC), pc.c0 + (g_end - g)));
-    pc.seg = static_cast<int>(g / p.L - (static_cast<long long>(pc.u) * p.NC) / p.L);
-    return pc;
-}
-
-__device__ __forceinline__ bool bar_or(int id, int n, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 q, %1, 0;\n\t"
-        "bar.red.or.pred p, %2, %3, q;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(r)
-        : "r"(pred ? 1u : 0u), "r"(id), "r"(n)
-        : "memory");
-    return r != 0;
-}
-
-__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) { return pack_bf16x2(lo, hi); }
-
-__device__ __forceinline__ float2 unpack_bf16x2(uint32_t w) {
-    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-}
-
-// Split (x, y) into a bf16 hi pair and a bf16 lo pair, x = hi + lo to 16
-// significant bits.  Two packed conversions; the hi halves are widened back
-// to fp32 by bit shifts.
-__device__ __forceinline__ void split_pair(float x, float y, uint32_t &hi, uint32_t &lo) {
-    hi = pack_bf16x2(x, y);
-    const float2 h = unpack_bf16x2(hi);
-    lo = pack_bf16x2(x - h.x, y - h.y);
-}
-
-__device__ __forceinline__ float clamp_gate(float a) {
-    return fminf(fmaxf(a, -kExpBound), kExpBound);
-}
-
-// Causal split of one 32-column block of P (key tokens j0 .. j0 + 31) for
-// row i, from its fp32 scores r: both 16-column pieces are stored back in
-// place as 8 columns of bf16 hi pairs followed by 8 of lo pairs, with the
-// entries j > i zeroed where the block holds the diagonal (`diag`, uniform
-// over the warp).  One piece is stored before the next is split.
-__device__ __forceinline__ void split_p_block(uint32_t taddr, const uint32_t (&r)[32], int j0, int i,
-                                              bool diag) {
-#pragma unroll
-    for (int pc = 0; pc < 2; ++pc) {
-        uint32_t w[16];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            float x0 = __uint_as_float(r[16 * pc + 2 * e]);
-            float x1 = __uint_as_float(r[16 * pc + 2 * e + 1]);
-            if (diag) {
-                const int j = j0 + 16 * pc + 2 * e;
-                x0 = j <= i ? x0 : 0.f;
-                x1 = j + 1 <= i ? x1 : 0.f;
-            }
-            split_pair(x0, x1, w[e], w[8 + e]);
-        }
-        tmem_st16(taddr + 16 * pc, w);
-    }
-}
-
-// A 32-column block of P past the diagonal for every row of the warp: zeros.
-__device__ __forceinline__ void zero_p_block(uint32_t taddr) {
-    uint32_t z[16];
-#pragma unroll
-    for (int e = 0; e < 16; ++e) z[e] = 0u;
-    tmem_st16(taddr, z);
-    tmem_st16(taddr + 16, z);
-}
-
-// Sub-chunk rescaling of one chunk (prep threads): the largest power-of-two
-// block length cs whose every block keeps |Gamma - r_block| <= kExpBound
-// (clamped gates); each block becomes one item, written to the operand tiles
-// with its own reference.  Gates, Q and K are read from global memory.
-// Thread pt owns the channel pair 2*(pt % (DK/2)) of token part pt / (DK/2).
-// `n` counts items; `last_flags` go to the chunk's last item; gtot0/gtot1
-// return the chunk's clamped Gamma at its end for the thread's channels (valid
-// in the last token part).  Returns false if a bounded wait expired.
-template <int DK, typename BeforeEmptyWait>
-__device__ __forceinline__ bool sub_chunk_items(const KParams &p, int bh, int t0, int lc,
-                                                bool store, int last_flags, int pt, uint8_t *sQ,
-                                                uint8_t *sK,
-                                                uint8_t *sKlo, float *sG, ItemInfo *sItem,
-                                                uint64_t *bars, int &n, float &gtot0,
-                                                float &gtot1, BeforeEmptyWait &&before_empty_wait) {
-    constexpr int NP = DK / 2;
-    constexpr int NQ = kPrepThreads / NP;
-    constexpr int TP = kChunk / NQ;
-    constexpr int kStride = DK / 2;     // row stride in bf16 pairs
-    const int pr = pt % NP, part = pt / NP;
-    const int ch = 2 * pr;
-    const bool last_part = part == NQ - 1;
-    const int lane = pt & 31;
-    const int T = p.T;
-    const size_t row0 = static_cast<size_t>(bh) * T;
-    const uint32_t *qb = p.q + (row0 * DK + ch) / 2;
-    const uint32_t *kb = p.k + (row0 * DK + ch) / 2;
-    const float2 *ab = p.a + (row0 * DK + ch) / 2;
-    auto raw_gate = [&](int i) {
-        const int t = t0 + i;
-        return t < T ? ab[static_cast<size_t>(t) * kStride] : make_float2(0.f, 0.f);
-    };
-    float bnd0[NQ], bnd1[NQ];  // clamped Gamma just before each part start
-    {
-        float c0 = 0.f, c1 = 0.f;
-        bnd0[0] = 0.f;
-        bnd1[0] = 0.f;
-        for (int qq = 1; qq < NQ; ++qq) {
-            for (int i = (qq - 1) * TP; i < qq * TP; ++i) {
-                const float2 a = raw_gate(i);
-                c0 += clamp_gate(a.x);
-                c1 += clamp_gate(a.y);
-            }
-            bnd0[qq] = c0;
-            bnd1[qq] = c1;
-        }
-    }
-    int cs = 64;
-    for (; cs > 1; cs >>= 1) {
-        float c0 = bnd0[part], c1 = bnd1[part];
-        const int s_first = (part * TP) / cs * cs;
-        float r0 = (s_first >= part * TP) ? c0 : bnd0[s_first / TP];
-        float r1 = (s_first >= part * TP) ? c1 : bnd1[s_first / TP];
-        bool viol = false;
-        for (int ii = 0; ii < TP; ++ii) {
-            const int i = part * TP + ii;
-            if (i % cs == 0) {
-                r0 = c0;
-                r1 = c1;
-            }
-            const float2 a = raw_gate(i);
-            c0 += clamp_gate(a.x);
-            c1 += clamp_gate(a.y);
-            viol |= fabsf(c0 - r0) > kExpBound || fabsf(c1 - r1) > kExpBound;
-        }
-        if (!bar_or(3, kPrepThreads, viol)) break;
-    }
-    // cs == 1 always satisfies the bound: a single clamped gate is within it.
-    const int n_sub = kChunk / cs;
-    bool ok = true;
-    for (int sidx = 0; sidx < n_sub; ++sidx) {
-        const int sa = sidx * cs, sb = sa + cs;
-        bool okw = true;
-        if (sidx > 0) {
-            before_empty_wait();
-            okw = mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status);
-        }
-        ok = !bar_or(4, kPrepThreads, !okw);
-        if (!ok) break;
-        // reference for block sidx: clamped Gamma just before token sa
-        float c0 = bnd0[part], c1 = bnd1[part];
-        float r0 = 0.f, r1 = 0.f;
-        if (sa <= part * TP) {
-            r0 = bnd0[sa / TP];
-            r1 = bnd1[sa / TP];
-        }
-        for (int ii = 0; ii < TP; ++ii) {
-            const int i = part * TP + ii;
-            if (i == sa) {
-                r0 = c0;
-                r1 = c1;
-            }
-            const int t = t0 + i;
-            const float2 a = raw_gate(i);
-            c0 += clamp_gate(a.x);
-            c1 += clamp_gate(a.y);
-            const uint32_t off = sw128_offset(i, ch, kBlk);
-            uint32_t hi = 0u, lo = 0u, qv = 0u;
-            if (i >= sa && i < sb && t < T) {
-                const float2 qf = unpack_bf16x2(qb[static_cast<size_t>(t) * kStride]);
-                const float2 kf = unpack_bf16x2(kb[static_cast<size_t>(t) * kStride]);
-                qv = bf16x2_bits(qf.x * __expf(c0 - r0), qf.y * __expf(c1 - r1));
-                split_pair(kf.x * __expf(r0 - c0), kf.y * __expf(r1 - c1), hi, lo);
-            }
-            *reinterpret_cast<uint32_t *>(sQ + off) = qv;
-            *reinterpret_cast<uint32_t *>(sK + off) = hi;
-            *reinterpret_cast<uint32_t *>(sKlo + off) = lo;
-            if (i == sb - 1) {
-                sG[(n & 1) * DK + ch] = __expf(c0 - r0);
-                sG[(n & 1) * DK + ch + 1] = __expf(c1 - r1);
-            }
-        }
-        if (last_part) {
-            gtot0 = c0;
-            gtot1 = c1;
-        }
-        if (pt == 0) {
-            sItem[n & 1] = ItemInfo{
-                t0, sa, sb,
-                (sidx == n_sub - 1 ? (kItemLast | last_flags) : 0) | (store ? kItemStore : 0), lc,
-                -1, bh, 0};
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kBarQkFull]);
-        ++n;
-    }
-    return ok;
-}
-
-// Prep warps of one CTA of a pair.  The CTA owns key channels
-// [64 rank, 64 rank + 64): 32 channel pairs x 8 token parts of 16 tokens.
-// Per chunk c:
-//   1. phase A on the A half tile: in-chunk prefix sums in place, part
-//      offsets, and the exponent-bound verdict for these channels, which is
-//      sent to the peer at once (one remote word);
-//   2. phase B into registers from the raw Q and K staging tiles (Qh, Kh_hi,
-//      Kh_lo for 16 tokens x 2 channels); the A and staging tiles are then
-//      free and chunk c+1 is requested, so its loads overlap this chunk;
-//   3. the segment decay of every channel through chunk c-1, from the state
-//      factors of the previous exchange, and the window decision for chunk c;
-//   4. if neither CTA's channels broke the bound: once both CTAs' MMAs have
-//      released the operand tiles, the registers go to this CTA's 64-channel
-//      block of the Qh, Kh_hi and Kh_lo tiles, its half of the state factors
-//      e^Gamma_C to the factor table, and all four are copied into the
-//      peer's shared memory at the same offsets.  The item is published at
-//      once; the MMA issuer (and the TMEM warps, for the factors) wait for the
-//      peer's copy themselves, so the prep warps go on to chunk c+1.
-//      Otherwise both CTAs run the sub-chunk path over all channels on their
-//      own (same inputs, same items).
-// Threads pt < DK keep the decay since the segment start of channel pt; both
-// CTAs compute it from identical bits (the exchanged factor table, or the raw
-// gates), so their window decisions agree.
-template <int DK, int DVT>
-__device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint32_t rank,
-                                          long long g_begin, long long g_end, size_t BHn,
-                                          int dv_tile) {
-    using L = Smem<DK, DVT, true>;
-    constexpr int DKH = DK / 2;                 // channels prepared by this CTA
-    constexpr int NP = DKH / 2;                 // channel pairs
-    constexpr int NQ = kPrepThreads / NP;       // token parts
-    constexpr int TP = kChunk / NQ;             // tokens per part
-    constexpr uint32_t kXchgBytes = 3u * kBlk + DKH * 4u;
-    uint8_t *sQ = smem + L::kQ;
-    uint8_t *sK = smem + L::kK;
-    uint8_t *sKlo = smem + L::kKlo;
-    const uint8_t *sRawQ = smem + L::kRaw;
-    const uint8_t *sRawK = sRawQ + kBlk;
-    float *sA = reinterpret_cast<float *>(smem + L::kA);
-    float *sG = reinterpret_cast<float *>(smem + L::kG);
-    ItemInfo *sItem = reinterpret_cast<ItemInfo *>(smem + L::kItem);
-    ChunkReq *sReq = reinterpret_cast<ChunkReq *>(smem + L::kReq);
-    uint32_t *sVerd = reinterpret_cast<uint32_t *>(smem + L::kVerd);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBar);
-
-    const int pt = threadIdx.x;
-    const int lane = pt & 31;
-    const int pr = pt % NP, part = pt / NP;
-    const int chl = 2 * pr;                      // channel within this CTA's half
-    const int ch = static_cast<int>(rank) * DKH + chl;
-    const bool last_part = part == NQ - 1;
-    const float *sAc = sA + chl;
-    const uint32_t peer = rank ^ 1u;
-    const int T = p.T;
-
-    // the pieces of this CTA's range, one after another: the current piece is
-    // chunks [c, c_end) of sequence bh (the rest is recomputed at piece ends)
-    int bh, c, c_end;
-    bool closed;
-    {
-        const Piece pc = piece_at(p, g_begin, g_end);
-        bh = pc.u;
-        c = pc.c0;
-        c_end = pc.c1;
-        closed = p.mode == kModeFull && pc.seg == 0;
-    }
-    float gseg = 0.f;                            // threads pt < DK: channel pt
-    int n = 0;                                   // items published
-    int nx = 0;                                  // operand exchanges made
-    int used = 0;                                // chunks published
-    bool ok = true;
-    bool pend = false;                           // last exchange's factors not yet read
-    bool prepped_last = false;                   // the last chunk prepared was not used
-    bool spec = false;                           // chunk lc_last + 1 requested, A not yet landed
-    int lc_last = 0;
-    if (pt == 0) {
-        sReq[0] = ChunkReq{c * kChunk, 0, 0, bh};
-        mbar_arrive(&bars[kBarReq]);
-    }
-    // A wait that expires clears `ok` in its thread only: every thread still
-    // runs the same sequence of barriers (each wait is bounded), and the loop
-    // ends at the next chunk boundary, where the threads' verdicts are combined.
-    for (int lc = 0;; ++lc) {
-        ok = !bar_or(4, kPrepThreads, !ok);
-        const bool have = c < c_end && ok;
-        const int t0 = c * kChunk;
-        uint32_t rq[TP], rh[TP], rl[TP];
-        float gc0 = 0.f, gc1 = 0.f;
-        bool bad_here = false;
-        if (have) {
-            // ---- phase A: prefix sums of this thread's part (log2 units) in
-            // registers; the part total goes to the A tile's last row of the part
-            if (pt == 0) mbar_arrive_expect_tx(&bars[kBarVerd0 + (lc & 1)], 4u);
-            ok &= mbar_wait_bounded(&bars[kBarAFull], lc & 1, p.status);
-            spec = false;
-            float c0 = 0.f, c1 = 0.f;
-            float lmn = 3.0e38f, lmx = -3.0e38f;
-            float2 av[TP];
-#pragma unroll
-            for (int e = 0; e < TP; ++e)
-                av[e] = *reinterpret_cast<const float2 *>(sAc + (part * TP + e) * DKH);
-#pragma unroll
-            for (int e = 0; e < TP; ++e) {
-                c0 = fmaf(av[e].x, kLog2e, c0);
-                c1 = fmaf(av[e].y, kLog2e, c1);
-                av[e] = make_float2(c0, c1);
-                lmn = fminf(lmn, fminf(c0, c1));
-                lmx = fmaxf(lmx, fmaxf(c0, c1));
-            }
-            *reinterpret_cast<float2 *>(sA + chl + (part * TP + TP - 1) * DKH) = make_float2(c0, c1);
-            named_barrier(5, kPrepThreads);
-            float o0 = 0.f, o1 = 0.f;
-#pragma unroll
-            for (int qq = 0; qq < NQ - 1; ++qq) {
-                if (qq < part) {
-                    const float2 tt =
-                        *reinterpret_cast<const float2 *>(sAc + (qq * TP + TP - 1) * DKH);
-                    o0 += tt.x;
-                    o1 += tt.y;
-                }
-            }
-            const float gmin = fminf(o0, o1) + lmn, gmax = fmaxf(o0, o1) + lmx;
-            bad_here = bar_or(2, kPrepThreads,
-                              fmaxf(-fminf(gmin, 0.f), fmaxf(gmax, 0.f)) > kExpBound2 ||
-                                  p.force_sub != 0);
-            if (pt == 0) {
-                const uint32_t dst = mapa_shared(smem_u32(&sVerd[lc & 1]), peer);
-                const uint32_t pbar = mapa_shared(smem_u32(&bars[kBarVerd0 + (lc & 1)]), peer);
-                st_async_to_peer(dst, bad_here ? 1u : 0u, pbar);
-            }
-            // ---- phase B into registers (values of a chunk that broke the
-            // bound are computed but never used)
-            ok &= mbar_wait_bounded(&bars[kBarQkRaw], lc & 1, p.status);
-#pragma unroll
-            for (int e = 0; e < TP; ++e) {
-                const int i = part * TP + e;
-                const uint32_t off = sw128_offset(i, chl, kBlk);
-                const float2 qf = unpack_bf16x2(*reinterpret_cast<const uint32_t *>(sRawQ + off));
-                const float2 kf = unpack_bf16x2(*reinterpret_cast<const uint32_t *>(sRawK + off));
-                const float g0 = o0 + av[e].x, g1 = o1 + av[e].y;
-                rq[e] = bf16x2_bits(qf.x * ex2f(g0), qf.y * ex2f(g1));
-                split_pair(kf.x * ex2f(-g0), kf.y * ex2f(-g1), rh[e], rl[e]);
-            }
-            gc0 = o0 + c0;                       // Gamma log2 e at the chunk end (last part)
-            gc1 = o1 + c1;
-            // the A and staging tiles are consumed: start the next chunk's loads
-            named_barrier(5, kPrepThreads);
-            // the next chunk of the stream: in this piece, or the next piece's first
-            int nc = -1, nbh = bh;
-            if (c + 1 < c_end) {
-                nc = c + 1;
-            } else if (p.mode == kModeFull) {
-                const long long gn = static_cast<long long>(bh) * p.NC + c_end, ge = full_range_end(p);
-                if (gn < ge) {
-                    const Piece next = piece_at(p, gn, ge);
-                    nc = next.c0;
-                    nbh = next.u;
-                }
-            }
-            if (nc >= 0) {
-                if (pt == 0) {
-                    sReq[0] = ChunkReq{nc * kChunk, 0, 0, nbh};
-                    mbar_arrive(&bars[kBarReq]);
-                }
-                spec = true;   // taken by the TMA thread once A(next) has landed
-            }
-            prepped_last = true;
-            lc_last = lc;
-        }
-        // ---- segment decay through chunk c-1 (the previous exchange's factors)
-        if (pend) {
-            const int x = nx - 1;
-            ok &= mbar_wait_bounded(&bars[kBarXchg0 + (x & 1)], (x >> 1) & 1, p.status);
-            if (pt < DK) gseg += __logf(sG[((n - 1) & 1) * DK + pt]);
-            pend = false;
-        }
-        // ---- end of the segment, or (correction pass) of the decay window
-        const bool win = !closed && pt < DK && gseg > -kWindowCut;
-        const bool any_win = bar_or(1, kPrepThreads, win);
-        if (!closed && !any_win) closed = true;
-        if (!have || (p.mode == kModeCorrect && closed)) break;
-        const bool store = p.mode == kModeCorrect || closed;
-        // the FULL pass stores the state at the end of every piece
-        const int piece_end = (p.mode == kModeFull && c + 1 == c_end) ? kItemPieceEnd : 0;
-        // ---- both CTAs' verdicts: one branch for all threads, even for one
-        // whose wait expired
-        ok &= mbar_wait_bounded(&bars[kBarVerd0 + (lc & 1)], (lc >> 1) & 1, p.status);
-        const bool bad = bar_or(2, kPrepThreads, bad_here || sVerd[lc & 1] != 0u);
-        prepped_last = false;
-        ++used;
-        if (!bad) {
-            // ---- both CTAs' MMAs are done with the previous item's tiles
-            if (n > 0) ok &= mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status);
-#pragma unroll
-            for (int e = 0; e < TP; ++e) {
-                const uint32_t off = sw128_offset(part * TP + e, ch, kBlk);
-                *reinterpret_cast<uint32_t *>(sQ + off) = rq[e];
-                *reinterpret_cast<uint32_t *>(sK + off) = rh[e];
-                *reinterpret_cast<uint32_t *>(sKlo + off) = rl[e];
-            }
-            if (last_part) {
-                sG[(n & 1) * DK + ch] = ex2f(gc0);
-                sG[(n & 1) * DK + ch + 1] = ex2f(gc1);
-            }
-            fence_proxy_async_smem();
-            named_barrier(5, kPrepThreads);
-            if (pt == 0) {
-                sItem[n & 1] = ItemInfo{t0, 0, kChunk,
-                                        kItemLast | (store ? kItemStore : 0) | piece_end, lc, nx,
-                                        bh, 0};
-                mbar_arrive_expect_tx(&bars[kBarXchg0 + (nx & 1)], kXchgBytes);
-                const uint32_t pbar = mapa_shared(smem_u32(&bars[kBarXchg0 + (nx & 1)]), peer);
-                const uint32_t blk = rank * kBlk;
-                float *g_own = sG + (n & 1) * DK + rank * DKH;
-                bulk_copy_to_peer(mapa_shared(smem_u32(sQ + blk), peer), sQ + blk, kBlk, pbar);
-                bulk_copy_to_peer(mapa_shared(smem_u32(sK + blk), peer), sK + blk, kBlk, pbar);
-                bulk_copy_to_peer(mapa_shared(smem_u32(sKlo + blk), peer), sKlo + blk, kBlk, pbar);
-                bulk_copy_to_peer(mapa_shared(smem_u32(g_own), peer), g_own, DKH * 4u, pbar);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[kBarQkFull]);
-            ++n;
-            ++nx;
-            pend = true;
-        } else {
-            // ---- a chunk whose decay breaks the bound: sub-chunk items over all
-            // channels, computed by each CTA of the pair on its own
-            if (n > 0) ok &= mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status);
-            float gt0 = 0.f, gt1 = 0.f;
-            ok &= sub_chunk_items<DK>(p, bh, t0, lc, store, piece_end, pt, sQ, sK, sKlo, sG, sItem,
-                                      bars, n, gt0, gt1, [] {});
-            if (pt < DK) {
-                // the chunk's clamped decay of channel pt, summed in token order
-                const float *ab =
-                    reinterpret_cast<const float *>(p.a) + static_cast<size_t>(bh) * T * DK + pt;
-                float gsum = 0.f;
-                for (int i = 0; i < kChunk && t0 + i < T; ++i)
-                    gsum += clamp_gate(ab[static_cast<size_t>(t0 + i) * DK]);
-                gseg += gsum;
-            }
-        }
-        ++c;
-        if (piece_end) {
-            // ---- end of a FULL-pass piece: its decay, then the next piece
-            if (pend) {
-                const int x = nx - 1;
-                ok &= mbar_wait_bounded(&bars[kBarXchg0 + (x & 1)], (x >> 1) & 1, p.status);
-                if (pt < DK) gseg += __logf(sG[((n - 1) & 1) * DK + pt]);
-                pend = false;
-            }
-            const long long a = static_cast<long long>(bh) * p.NC;
-            if (nseg_of(p, bh) > 1 && dv_tile == 0 && pt < DK) {
-                const int seg = static_cast<int>((a + c_end - 1) / p.L - a / p.L);
-                p.ws_decay[(static_cast<size_t>(seg) * BHn + bh) * DK + pt] = gseg;
-            }
-            const long long gn = a + c_end, ge = full_range_end(p);
-            if (gn >= ge) break;
-            const Piece next = piece_at(p, gn, ge);
-            bh = next.u;
-            c = next.c0;
-            c_end = next.c1;
-            gseg = 0.f;
-            closed = next.seg == 0;
-        }
-    }
-    // ---- end of the item stream and of the load requests
-    if (pend) {
-        const int x = nx - 1;
-        ok &= mbar_wait_bounded(&bars[kBarXchg0 + (x & 1)], (x >> 1) & 1, p.status);
-        if (pt < DK) gseg += __logf(sG[((n - 1) & 1) * DK + pt]);
-    }
-    // the peer's verdict for a chunk prepared here but not used has to land
-    // before this CTA may exit
-    if (prepped_last) ok &= mbar_wait_bounded(&bars[kBarVerd0 + (lc_last & 1)], (lc_last >> 1) & 1, p.status);
-    // the request mailbox holds one request: the end may be posted only once
-    // the TMA thread has taken the last one (its A tile has landed)
-    if (spec) ok &= mbar_wait_bounded(&bars[kBarAFull], (lc_last + 1) & 1, p.status);
-    named_barrier(5, kPrepThreads);
-    if (pt == 0) {
-        // the count of chunks used, so that no V load waits for a tile never freed
-        sReq[0] = ChunkReq{used, 0, 1, 0};
-        mbar_arrive(&bars[kBarReq]);
-    }
-    if (n > 0 && !mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status)) ok = false;
-    if (pt == 0) sItem[n & 1] = ItemInfo{0, 0, 0, kItemEnd, 0, -1, 0, 0};
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&bars[kBarQkFull]);
-}
-
-template <int DK, int DVT, bool PAIR>
-__global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_constant__ KParams p) {
-    using L = Smem<DK, DVT, PAIR>;
-    using TM = Tmem<DVT>;
-    constexpr int VS = L::kVSlots;   // V tile slots: chunk j uses slot j % VS
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t *sQ = smem + L::kQ;
-    uint8_t *sK = smem + L::kK;
-    uint8_t *sKlo = smem + L::kKlo;
-    uint8_t *sV = smem + L::kV;
-    uint8_t *sS = smem + L::kS;
-    float *sA = reinterpret_cast<float *>(smem + L::kA);
-    float *sG = reinterpret_cast<float *>(smem + L::kG);
-    ItemInfo *sItem = reinterpret_cast<ItemInfo *>(smem + L::kItem);
-    ChunkReq *sReq = reinterpret_cast<ChunkReq *>(smem + L::kReq);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBar);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
-
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5, lane = tid & 31;
-    const int dv_tile = blockIdx.x;
-    const int dv0 = dv_tile * DVT;
-    const int T = p.T;
-    const size_t BHn = static_cast<size_t>(p.BH);
-    // This CTA's chunks: FULL pass, range `unit` of the work split (one or
-    // more pieces); CORRECT pass, segment 1 + unit % (seg_max - 1) of
-    // sequence unit / (seg_max - 1), if that sequence has it (a CTA pair's two
-    // CTAs decide alike and leave together, before any cluster barrier or TMEM
-    // allocation).
-    const long long unit = blockIdx.y + static_cast<long long>(blockIdx.z) * gridDim.y;
-    if (unit >= p.n_units) return;
-    long long g_begin, g_end;
-    if (p.mode == kModeFull) {
-        g_begin = unit * p.L;
-        g_end = min(g_begin + p.L, static_cast<long long>(p.BH) * p.NC);
-    } else {
-        const int u = static_cast<int>(unit / (p.seg_max - 1));
-        const int sg = 1 + static_cast<int>(unit % (p.seg_max - 1));
-        const int ns = nseg_of(p, u);
-        if (sg >= ns) return;
-        const long long a = static_cast<long long>(u) * p.NC;
-        g_begin = a + seg_start(p, u, sg);
-        g_end = a + (sg + 1 < ns ? seg_start(p, u, sg + 1) : p.NC);
-    }
-    if (g_begin >= g_end) return;
-
-    // CTA pair: the two value-column tiles of one head, cluster ranks 0 and 1
-    // (rank == dv_tile); each prepares the operands of one half of the key
-    // channels and sends them to the other.
-    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
-    if (tid == 0) {
-        for (int i = 0; i < kNumBars; ++i)
-            mbar_init(&bars[i], (PAIR && i == kBarQkEmpty) ? 2u : kBarCounts[i]);
-        fence_mbar_init();
-    }
-    if (warp == kTmaWarp && lane == 0) {
-        prefetch_tensormap(&p.tm_q);
-        prefetch_tensormap(&p.tm_k);
-        prefetch_tensormap(&p.tm_a);
-        prefetch_tensormap(&p.tm_v);
-        prefetch_tensormap(&p.tm_o32);
-    }
-    if (warp == kMmaWarp) tmem_alloc(tmem_slot, TM::kCols);
-    tc_fence_before();
-    __syncthreads();
-    if constexpr (PAIR) cluster_sync_all();   // the peer's barriers exist before any remote use
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-
-    if (warp < kPrepWarps && PAIR) {
-        if constexpr (PAIR) {
-            prep_pair<DK, DVT>(p, smem, rank, g_begin, g_end, BHn, dv_tile);
-        }
-    } else if (warp < kPrepWarps) {
-        // =========================================================== prep warps
-        constexpr int NP = DK / 2;              // channel pairs
-        constexpr int NQ = kPrepThreads / NP;   // token parts
-        constexpr int TP = kChunk / NQ;         // tokens per part
-        static_assert(TP % 8 == 0, "token parts must hold whole batches");
-        const int pt = tid;
-        const int pr = pt % NP, part = pt / NP;
-        const int ch = 2 * pr;
-        const bool last_part = part == NQ - 1;
-        const float *sAc = sA + ch;         // this thread's channel pair in the A tile
-        int n = 0, lc = 0;
-        bool ok = true;
-        for (long long g = g_begin; g < g_end && ok;) {
-          // ---- one piece: chunks [pc.c0, pc.c1) of sequence pc.u
-          const Piece pc = piece_at(p, g, g_end);
-          g += pc.c1 - pc.c0;
-          const int bh = pc.u;
-          float gseg0 = 0.f, gseg1 = 0.f;     // decay since the segment start (last part only)
-          bool closed = (p.mode == kModeFull && pc.seg == 0);  // no correction window
-          for (int c = pc.c0;; ++c, ++lc) {
-            // ---- decide this chunk: past the piece end, or (correction pass)
-            // past the point where the segment's start state has decayed away.
-            // The reduction doubles as the barrier after which the previous
-            // chunk's A tile is free.
-            const bool win = !closed && last_part && (gseg0 > -kWindowCut || gseg1 > -kWindowCut);
-            const bool any_win = bar_or(1, kPrepThreads, win);
-            if (!closed && !any_win) closed = true;
-            const bool end = c >= pc.c1 || !ok || (p.mode == kModeCorrect && closed);
-            if (end) break;
-            if (pt == 0) {
-                sReq[0] = ChunkReq{c * kChunk, n, 0, bh};
-                mbar_arrive(&bars[kBarReq]);
-            }
-            const int t0 = c * kChunk;
-            const bool store = p.mode == kModeCorrect || closed;
-            // the FULL pass stores the state at the end of every piece
-            const int piece_end = (p.mode == kModeFull && c + 1 == pc.c1) ? kItemPieceEnd : 0;
-            // ---- phase A (needs only the A tile, which arrives early): the
-            // local prefix sum of this thread's part, written in place of A.
-            constexpr int kB = 8;
-            bool okw = mbar_wait_bounded(&bars[kBarAFull], lc & 1, p.status);
-            ok = !bar_or(4, kPrepThreads, !okw);   // one verdict for all prep threads
-            if (!ok) break;
-            float c0 = 0.f, c1 = 0.f;
-            float lmn = 3.0e38f, lmx = -3.0e38f;
-            {
-                float2 nx[kB];
-#pragma unroll
-                for (int e = 0; e < kB; ++e)
-                    nx[e] = *reinterpret_cast<const float2 *>(sAc + (part * TP + e) * DK);
-                for (int i0 = part * TP; i0 < (part + 1) * TP; i0 += kB) {
-                    float2 cur[kB];
-#pragma unroll
-                    for (int e = 0; e < kB; ++e) cur[e] = nx[e];
-                    if (i0 + kB < (part + 1) * TP) {
-#pragma unroll
-                        for (int e = 0; e < kB; ++e)
-                            nx[e] = *reinterpret_cast<const float2 *>(sAc + (i0 + kB + e) * DK);
-                    }
-#pragma unroll
-                    for (int e = 0; e < kB; ++e) {
-                        c0 = fmaf(cur[e].x, kLog2e, c0);   // log2 units
-                        c1 = fmaf(cur[e].y, kLog2e, c1);
-                        lmn = fminf(lmn, fminf(c0, c1));
-                        lmx = fmaxf(lmx, fmaxf(c0, c1));
-                        *reinterpret_cast<float2 *>(const_cast<float *>(sAc) + (i0 + e) * DK) =
-                            make_float2(c0, c1);
-                    }
-                }
-            }
-            named_barrier(5, kPrepThreads);
-            // offset of this part: the totals of the parts before it
-            float o0 = 0.f, o1 = 0.f;
-            for (int qq = 0; qq < part; ++qq) {
-                const float2 tt = *reinterpret_cast<const float2 *>(sAc + (qq * TP + TP - 1) * DK);
-                o0 += tt.x;
-                o1 += tt.y;
-            }
-            // Gamma_i = o + local_i; the fast path needs every |Gamma_i| <= kExpBound
-            const float gmin = fminf(o0, o1) + lmn, gmax = fmaxf(o0, o1) + lmx;
-            const bool bad = bar_or(2, kPrepThreads,
-                                    fmaxf(-fminf(gmin, 0.f), fmaxf(gmax, 0.f)) > kExpBound2 ||
-                                        p.force_sub != 0);
-            okw = mbar_wait_bounded(&bars[kBarQkRaw], lc & 1, p.status);
-            ok = !bar_or(4, kPrepThreads, !okw);
-            if (!ok) break;
-            if (!bad) {
-                // ---- phase B (needs Q, K): Qh, Kh_hi in place, Kh_lo.  Purely
-                // elementwise; the next batch's loads precede this batch's stores.
-                if (last_part) {
-                    const float gc0 = o0 + c0, gc1 = o1 + c1;   // Gamma log2 e at the chunk end
-                    sG[(n & 1) * DK + ch] = ex2f(gc0);
-                    sG[(n & 1) * DK + ch + 1] = ex2f(gc1);
-                    gseg0 += gc0 * kLn2;
-                    gseg1 += gc1 * kLn2;
-                }
-                float2 ab8[kB];
-                uint32_t qw8[kB], kw8[kB];
-#pragma unroll
-                for (int e = 0; e < kB; ++e) {
-                    const int i = part * TP + e;
-                    const uint32_t off = sw128_offset(i, ch, kBlk);
-                    ab8[e] = *reinterpret_cast<const float2 *>(sAc + i * DK);
-                    qw8[e] = *reinterpret_cast<const uint32_t *>(sQ + off);
-                    kw8[e] = *reinterpret_cast<const uint32_t *>(sK + off);
-                }
-                for (int i0 = part * TP; i0 < (part + 1) * TP; i0 += kB) {
-                    float2 ca[kB];
-                    uint32_t cq[kB], ck[kB];
-#pragma unroll
-                    for (int e = 0; e < kB; ++e) {
-                        ca[e] = ab8[e];
-                        cq[e] = qw8[e];
-                        ck[e] = kw8[e];
-                    }
-                    if (i0 + kB < (part + 1) * TP) {
-#pragma unroll
-                        for (int e = 0; e < kB; ++e) {
-                            const int i = i0 + kB + e;
-                            const uint32_t off = sw128_offset(i, ch, kBlk);
-                            ab8[e] = *reinterpret_cast<const float2 *>(sAc + i * DK);
-                            qw8[e] = *reinterpret_cast<const uint32_t *>(sQ + off);
-                            kw8[e] = *reinterpret_cast<const uint32_t *>(sK + off);
-                        }
-                    }
-#pragma unroll
-                    for (int e = 0; e < kB; ++e) {
-                        const int i = i0 + e;
-                        const float g0 = o0 + ca[e].x, g1 = o1 + ca[e].y;
-                        const float2 qf = unpack_bf16x2(cq[e]), kf = unpack_bf16x2(ck[e]);
-                        const uint32_t off = sw128_offset(i, ch, kBlk);
-                        *reinterpret_cast<uint32_t *>(sQ + off) =
-                            bf16x2_bits(qf.x * ex2f(g0), qf.y * ex2f(g1));
-                        uint32_t hi, lo;
-                        split_pair(kf.x * ex2f(-g0), kf.y * ex2f(-g1), hi, lo);
-                        *reinterpret_cast<uint32_t *>(sK + off) = hi;
-                        *reinterpret_cast<uint32_t *>(sKlo + off) = lo;
-                    }
-                }
-                if (pt == 0) {
-                    sItem[n & 1] = ItemInfo{t0, 0, kChunk,
-                                            kItemLast | (store ? kItemStore : 0) | piece_end, lc,
-                                            -1, bh, 0};
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[kBarQkFull]);
-                ++n;
-                continue;
-            }
-            // ---- sub-chunk rescaling (chunks whose decay exceeds the bound)
-            float gtot0 = 0.f, gtot1 = 0.f;
-            ok = sub_chunk_items<DK>(p, bh, t0, lc, store, piece_end, pt, sQ, sK, sKlo, sG, sItem,
-                                     bars, n, gtot0, gtot1, [] {});
-            if (last_part) {
-                gseg0 += gtot0;
-                gseg1 += gtot1;
-            }
-            // an expired wait (!ok) ends the stream at the top of the loop
-          }
-          // segment summary: total decay of this segment (FULL pass, split sequence)
-          if (p.mode == kModeFull && nseg_of(p, bh) > 1 && dv_tile == 0 && last_part) {
-              float *dst = p.ws_decay + (static_cast<size_t>(pc.seg) * BHn + bh) * DK;
-              dst[ch] = gseg0;
-              dst[ch + 1] = gseg1;
-          }
-        }
-        // ---- end of the requests and of the item stream
-        if (pt == 0) {
-            sReq[0] = ChunkReq{0, n, 1, 0};
-            mbar_arrive(&bars[kBarReq]);
-        }
-        if (n > 0 && !mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status)) ok = false;
-        if (pt == 0) sItem[n & 1] = ItemInfo{0, 0, 0, kItemEnd, 0, -1, 0, 0};
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kBarQkFull]);
-    } else if (warp == kTmaWarp) {
-        // =========================================================== TMA producer
-        // Three load streams, each served as soon as its own condition holds,
-        // so that none waits behind another: per requested chunk, A (and, in a
-        // CTA pair, the raw Q/K staging tiles) at once; single-CTA Q and K once
-        // the previous chunk's items have released the operand tiles; V once
-        // its slot (also the output staging tile with two slots) is free.
-        if (lane == 0) {
-            int n_req = 0, n_qk = 0, n_v = 0;   // chunks requested / Q,K issued / V issued
-            int n_use = 0;                      // chunks used (known at the end request)
-            bool req_end = false;
-            int t0s[4], firsts[4], bhs[4];      // at most 3 chunks are ever outstanding
-            unsigned long long idle_since = 0;
-            while (true) {
-                bool progress = false;
-                if (!req_end && mbar_test_wait(&bars[kBarReq], n_req & 1)) {
-                    const ChunkReq rq = sReq[0];
-                    progress = true;
-                    if (rq.end) {
-                        // a CTA pair requests one chunk ahead and says at the end
-                        // how many chunks were used: no V load for the others
-                        req_end = true;
-                        n_use = PAIR ? rq.t0 : n_req;
-                    } else {
-                        const int t0 = rq.t0, bh = rq.bh;
-                        t0s[n_req & 3] = t0;
-                        firsts[n_req & 3] = rq.first_item;
-                        bhs[n_req & 3] = bh;
-                        // A (and staging): the prep released them with the request
-                        fence_proxy_async_smem();
-                        mbar_arrive_expect_tx(&bars[kBarAFull], L::kABytes);
-                        tma_load_3d(sA, &p.tm_a, &bars[kBarAFull], static_cast<int>(rank) * L::kDKA,
-                                    t0, bh);
-                        if constexpr (PAIR) {
-                            uint8_t *sRaw = smem + L::kRaw;
-                            mbar_arrive_expect_tx(&bars[kBarQkRaw], 2u * kBlk);
-                            tma_load_3d(sRaw, &p.tm_q, &bars[kBarQkRaw], static_cast<int>(rank) * 64,
-                                        t0, bh);
-                            tma_load_3d(sRaw + kBlk, &p.tm_k, &bars[kBarQkRaw],
-                                        static_cast<int>(rank) * 64, t0, bh);
-                        }
-                        ++n_req;
-                    }
-                }
-                if constexpr (!PAIR) {
-                    // Q, K in place: after the last item of the previous chunk
-                    if (n_qk < n_req) {
-                        const int first = firsts[n_qk & 3];
-                        if (first == 0 || mbar_test_wait(&bars[kBarQkEmpty], (first - 1) & 1)) {
-                            const int t0 = t0s[n_qk & 3], bh = bhs[n_qk & 3];
-                            mbar_arrive_expect_tx(&bars[kBarQkRaw], 2u * L::kQBytes);
-#pragma unroll
-                            for (int kb = 0; kb < DK / 64; ++kb) {
-                                tma_load_3d(sQ + kb * kBlk, &p.tm_q, &bars[kBarQkRaw], kb * 64, t0, bh);
-                                tma_load_3d(sK + kb * kBlk, &p.tm_k, &bars[kBarQkRaw], kb * 64, t0, bh);
-                            }
-                            ++n_qk;
-                            progress = true;
-                        }
-                    }
-                }
-                // V of chunk n_v into slot n_v % VS: once the chunk that last
-                // used the slot is done with it (products and output store)
-                if (n_v < (req_end ? n_use : n_req) &&
-                    (n_v < VS ||
-                     mbar_test_wait(&bars[kBarVEmpty0 + n_v % VS], (n_v / VS - 1) & 1))) {
-                    const int t0 = t0s[n_v & 3], bh = bhs[n_v & 3];
-                    const int slot = n_v % VS;
-                    uint8_t *dst = sV + slot * L::kVBytes;
-                    mbar_arrive_expect_tx(&bars[kBarVFull0 + slot], L::kVBytes);
-#pragma unroll
-                    for (int nb = 0; nb < DVT / 64; ++nb)
-                        tma_load_3d(dst + nb * kBlk, &p.tm_v, &bars[kBarVFull0 + slot], dv0 + nb * 64,
-                                    t0, bh);
-                    ++n_v;
-                    progress = true;
-                }
-                if (req_end && n_v >= n_use && (PAIR || n_qk == n_req)) break;
-                if (progress) {
-                    idle_since = 0;
-                } else {
-                    const unsigned long long now = global_timer_ns();
-                    if (idle_since == 0) {
-                        idle_since = now;
-                    } else if (now - idle_since > kWaitLimitNs) {
-                        atomicOr(p.status, kStatusTimeout);
-                        break;
-                    }
-                    __nanosleep(64);
-                }
-            }
-            // loads issued for chunks that were never used must land before exit
-            // (the last phase of each barrier; no later phase follows)
-            if (n_req > 0) {
-                mbar_wait_bounded(&bars[kBarAFull], (n_req - 1) & 1, p.status);
-                if (PAIR) mbar_wait_bounded(&bars[kBarQkRaw], (n_req - 1) & 1, p.status);
-            }
-            for (int j = n_v - VS < 0 ? 0 : n_v - VS; j < n_v; ++j)
-                mbar_wait_bounded(&bars[kBarVFull0 + j % VS], (j / VS) & 1, p.status);
-        }
-        __syncwarp();
-    } else if (warp == kMmaWarp) {
-        // =========================================================== MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t id_qk = idesc_bf16(128, 128, false, false);   // P = Qh Kh^T
-            constexpr uint32_t id_ov = idesc_bf16(128, DVT, false, true);    // O = Qh S, O += P V
-            constexpr uint32_t id_kv = idesc_bf16(128, DVT, true, true);     // S += Kh^T V
-            const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aKlo = smem_u32(sKlo);
-            const uint32_t aV0 = smem_u32(sV), aS = smem_u32(sS);
-            for (int n = 0;; ++n) {
-                if (!mbar_wait_bounded(&bars[kBarQkFull], n & 1, p.status)) break;
-                const ItemInfo it = sItem[n & 1];
-                mbar_arrive(&bars[kBarItem0 + (n & 1)]);
-                if (it.flags & kItemEnd) break;
-                const int ob = n & 1;
-                const uint32_t tO = tmem + (ob ? TM::kO1 : TM::kO0);
-                const uint32_t aV = aV0 + (it.lc % VS) * L::kVBytes;   // this chunk's V slot
-                tc_fence_after();
-                // P = Qh (Kh_hi + Kh_lo)^T, k-steps of 16 key channels.  In a CTA
-                // pair the steps over this CTA's own 64-channel block go first,
-                // while the peer's block may still be arriving.
-                auto p_steps = [&](int kb, bool first) {
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint32_t koff = kb * kBlk + kk * 32;
-                        mma_bf16_ss(tmem + TM::kP, sw128_desc(aQ + koff, 16, 1024),
-                                    sw128_desc(aK + koff, 16, 1024), id_qk, (first && kk == 0) ? 0 : 1);
-                        mma_bf16_ss(tmem + TM::kP, sw128_desc(aQ + koff, 16, 1024),
-                                    sw128_desc(aKlo + koff, 16, 1024), id_qk, 1);
-                    }
-                };
-                // a CTA pair's item: the peer's half of the operand tiles first
-                if (PAIR && it.xi >= 0) {
-                    if (!mbar_wait_bounded(&bars[kBarXchg0 + (it.xi & 1)], (it.xi >> 1) & 1, p.status))
-                        break;
-                    tc_fence_after();
-                }
-#pragma unroll
-                for (int kb = 0; kb < DK / 64; ++kb) p_steps(kb, kb == 0);
-                mma_commit(&bars[kBarPFull]);
-                // O = Qh S_prev: needs this O buffer drained and the previous
-                // state scaled and copied
-                bool okw = true;
-                if (n >= 2) okw &= mbar_wait_bounded(&bars[kBarOFree0 + ob], ((n >> 1) + 1) & 1, p.status);
-                okw &= mbar_wait_bounded(&bars[kBarSReady], n & 1, p.status);
-                if (!okw) break;
-                tc_fence_after();
-#pragma unroll
-                for (int ks = 0; ks < DK / 16; ++ks) {
-                    const uint32_t koff = (ks >> 2) * kBlk + (ks & 3) * 32;
-                    mma_bf16_ss(tO, sw128_desc(aQ + koff, 16, 1024),
-                                sw128_desc(aS + ks * 2048, L::kSBlk, 1024), id_ov, ks > 0);
-                }
-                // S += (Kh_hi + Kh_lo)^T V
-                if (!mbar_wait_bounded(&bars[kBarVFull0 + it.lc % VS], (it.lc / VS) & 1, p.status))
-                    break;
-                tc_fence_after();
-#pragma unroll
-                for (int ks = 0; ks < kChunk / 16; ++ks) {
-                    mma_bf16_ss(tmem + TM::kS, sw128_desc(aK + ks * 2048, kBlk, 1024),
-                                sw128_desc(aV + ks * 2048, kBlk, 1024), id_kv, 1);
-                    mma_bf16_ss(tmem + TM::kS, sw128_desc(aKlo + ks * 2048, kBlk, 1024),
-                                sw128_desc(aV + ks * 2048, kBlk, 1024), id_kv, 1);
-                }
-                mma_commit(&bars[kBarSDone]);
-                if constexpr (PAIR)
-                    mma_commit_multicast(&bars[kBarQkEmpty], 0x3);   // both CTAs' tiles
-                else
-                    mma_commit(&bars[kBarQkEmpty]);
-                // O += (P_hi + P_lo) V, P from TMEM
-                if (!mbar_wait_bounded(&bars[kBarPSplit], n & 1, p.status)) break;
-                tc_fence_after();
-#pragma unroll
-                for (int ks = 0; ks < kChunk / 16; ++ks) {
-                    const uint32_t pcol = TM::kP + 16 * ks;   // hi pairs, then lo pairs
-                    mma_bf16_ts(tO, tmem + pcol, sw128_desc(aV + ks * 2048, kBlk, 1024), id_ov, 1);
-                    mma_bf16_ts(tO, tmem + pcol + 8, sw128_desc(aV + ks * 2048, kBlk, 1024), id_ov,
-                                1);
-                }
-                mma_commit(&bars[kBarOFull0 + ob]);
-            }
-        }
-        __syncwarp();
-    } else {
-        // =========================================================== TMEM warps
-        const int i = tid - 32 * kTmemWarp0;      // TMEM lane = row = key channel
-        const uint32_t lane_base = static_cast<uint32_t>((warp - kTmemWarp0) * 32) << 16;
-        const bool has_state_row = ((warp - kTmemWarp0) * 32) < DK;  // warp-uniform
-        const uint32_t tP = tmem + lane_base + TM::kP;
-        const uint32_t tS = tmem + lane_base + TM::kS;
-
-        // ---- start state of a piece into TMEM (fp32) and its bf16 copy, then
-        // "state ready" for the piece's first item.  FULL pass: h0 for a
-        // sequence's first segment, zero for later ones.  CORRECT pass: the
-        // exact start state by the scan of the segment summaries before it; the
-        // last segment's CTA also writes hT = diag(e^G) S_start + S*.
-        auto load_state = [&](const Piece &pc) {
-            const int bh = pc.u, seg = pc.seg;
-            if (has_state_row) {
-                float *hT_dst = nullptr;
-                float eG = 0.f;
-                const float *sstar = nullptr;
-                if (p.mode == kModeCorrect && seg == nseg_of(p, bh) - 1 && p.hT) {
-                    hT_dst = p.hT + (static_cast<size_t>(bh) * DK + i) * p.dv + dv0;
-                    eG = __expf(p.ws_decay[(static_cast<size_t>(seg) * BHn + bh) * DK + i]);
-                    sstar = p.ws_state + ((static_cast<size_t>(seg) * BHn + bh) * DK + i) * p.dv + dv0;
-                }
-#pragma unroll
-                for (int c0 = 0; c0 < DVT; c0 += 32) {
-                    float x[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) x[j] = 0.f;
-                    if (p.mode == kModeFull) {
-                        if (seg == 0 && p.h0) {
-                            const float *src =
-                                p.h0 + (static_cast<size_t>(bh) * DK + i) * p.dv + dv0 + c0;
-#pragma unroll
-                            for (int j = 0; j < 32; j += 4) {
-                                const float4 v4 = *reinterpret_cast<const float4 *>(src + j);
-                                x[j] = v4.x;
-                                x[j + 1] = v4.y;
-                                x[j + 2] = v4.z;
-                                x[j + 3] = v4.w;
-                            }
-                        }
-                    } else {
-                        for (int s2 = 0; s2 < seg; ++s2) {
-                            const float e =
-                                __expf(p.ws_decay[(static_cast<size_t>(s2) * BHn + bh) * DK + i]);
-                            const float *src = p.ws_state +
-                                               ((static_cast<size_t>(s2) * BHn + bh) * DK + i) * p.dv +
-                                               dv0 + c0;
-#pragma unroll
-                            for (int j = 0; j < 32; j += 4) {
-                                const float4 v4 = *reinterpret_cast<const float4 *>(src + j);
-                                x[j] = fmaf(e, x[j], v4.x);
-                                x[j + 1] = fmaf(e, x[j + 1], v4.y);
-                                x[j + 2] = fmaf(e, x[j + 2], v4.z);
-                                x[j + 3] = fmaf(e, x[j + 3], v4.w);
-                            }
-                        }
-                        if (hT_dst) {
-#pragma unroll
-                            for (int j = 0; j < 32; j += 4) {
-                                const float4 v4 = *reinterpret_cast<const float4 *>(sstar + c0 + j);
-                                *reinterpret_cast<float4 *>(hT_dst + c0 + j) =
-                                    make_float4(fmaf(eG, x[j], v4.x), fmaf(eG, x[j + 1], v4.y),
-                                                fmaf(eG, x[j + 2], v4.z), fmaf(eG, x[j + 3], v4.w));
-                            }
-                        }
-                    }
-                    uint32_t r[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(x[j]);
-                    tmem_st32(tS + c0, r);
-#pragma unroll
-                    for (int j = 0; j < 32; j += 8) {
-                        uint4 pk;
-                        pk.x = pack_bf16x2(x[j], x[j + 1]);
-                        pk.y = pack_bf16x2(x[j + 2], x[j + 3]);
-                        pk.z = pack_bf16x2(x[j + 4], x[j + 5]);
-                        pk.w = pack_bf16x2(x[j + 6], x[j + 7]);
-                        *reinterpret_cast<uint4 *>(sS + sw128_offset(i, c0 + j, L::kSBlk)) = pk;
-                    }
-                }
-                tmem_wait_st();
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[kBarSReady]);
-        };
-        // ---- end state of a FULL-pass piece: hT for an unsplit sequence,
-        // else the segment summary S* of the workspace
-        auto store_state = [&](const Piece &pc) {
-            if (!has_state_row) return;
-            float *dst = nullptr;
-            if (nseg_of(p, pc.u) == 1) {
-                if (p.hT) dst = p.hT + (static_cast<size_t>(pc.u) * DK + i) * p.dv + dv0;
-            } else {
-                dst = p.ws_state + ((static_cast<size_t>(pc.seg) * BHn + pc.u) * DK + i) * p.dv + dv0;
-            }
-            if (!dst) return;
-            tc_fence_after();
-#pragma unroll
-            for (int c0 = 0; c0 < DVT; c0 += 32) {
-                uint32_t r[32];
-                tmem_ld32(tS + c0, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 32; j += 4)
-                    *reinterpret_cast<float4 *>(dst + c0 + j) =
-                        make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                                    __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
-            }
-        };
-        load_state(piece_at(p, g_begin, g_end));   // phase 0 of "state ready"
-
-        for (int n = 0;; ++n) {
-            // (one barrier per item parity, so that the MMA issuer may run up
-            // to two items ahead of these warps)
-            if (!__all_sync(0xffffffffu,
-                            mbar_wait_bounded(&bars[kBarItem0 + (n & 1)], (n >> 1) & 1, p.status)))
-                break;
-            const ItemInfo it = sItem[n & 1];
-            if (it.flags & kItemEnd) break;
-            const int ob = n & 1;
-            // ---- causal mask of P (row i), split into the TMEM A operand of P V
-            {
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarPFull], n & 1, p.status)))
-                    break;
-                tc_fence_after();
-                // This warp's rows are 32 wq .. 32 wq + 31: column blocks past
-                // block wq are zero (nothing to read), block wq is the diagonal,
-                // the blocks before it are unmasked.
-                const int wq = warp - kTmemWarp0;
-#pragma unroll
-                for (int qd = 0; qd < kChunk / 32; qd += 2) {
-                    if (qd > wq) {
-                        zero_p_block(tP + 32 * qd);
-                        zero_p_block(tP + 32 * (qd + 1));
-                    } else if (qd + 1 > wq) {
-                        uint32_t r0[32];
-                        tmem_ld32(tP + 32 * qd, r0);
-                        tmem_wait_ld();
-                        split_p_block(tP + 32 * qd, r0, 32 * qd, i, true);
-                        zero_p_block(tP + 32 * (qd + 1));
-                    } else {
-                        uint32_t r0[32], r1[32];
-                        tmem_ld32(tP + 32 * qd, r0);
-                        tmem_ld32(tP + 32 * (qd + 1), r1);
-                        tmem_wait_ld();
-                        split_p_block(tP + 32 * qd, r0, 32 * qd, i, false);
-                        split_p_block(tP + 32 * (qd + 1), r1, 32 * (qd + 1), i, qd + 1 == wq);
-                    }
-                }
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[kBarPSplit]);
-            }
-            // The state step (S <- diag(e^decay) S and its bf16 copy for the next
-            // item's Qh S) and the output step (this item's rows).  With two V
-            // slots the output is staged in the chunk's V slot once P V is done,
-            // after the state step, which therefore waits for nothing but the
-            // chunk's S products.  With one slot (dk = 128 only) the bf16 state
-            // copy, which has the output tile's size and layout, is the staging
-            // tile: this item's Qh S product has finished reading it once the
-            // output is ready, so the output step runs first, V is free as soon
-            // as P V is done, and the state step follows the staging store.
-            static_assert(VS == 2 || DK == 128, "one V slot only where the state copy can stage");
-            constexpr bool kStageInS = VS == 1;
-            uint8_t *sStage = kStageInS ? sS : sV + (it.lc % VS) * L::kVBytes;
-            const bool store_item = (it.flags & kItemStore) != 0;
-            const bool staged = store_item && it.r0 == 0 && it.r1 == kChunk;
-            const bool piece_end = (it.flags & kItemPieceEnd) != 0;
-            auto state_step = [&]() -> bool {
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarSDone], n & 1, p.status)))
-                    return false;
-                // a CTA pair's item: the peer's half of the state factors
-                if (it.xi >= 0 &&
-                    !__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarXchg0 + (it.xi & 1)],
-                                                               (it.xi >> 1) & 1, p.status)))
-                    return false;
-                tc_fence_after();
-                if (has_state_row) {
-                    const float f = sG[(n & 1) * DK + i];
-#pragma unroll
-                    for (int c0 = 0; c0 < DVT; c0 += 32) {
-                        uint32_t r[32];
-                        tmem_ld32(tS + c0, r);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * f);
-                        tmem_st32(tS + c0, r);
-                        if (piece_end) continue;   // the next piece starts afresh
-#pragma unroll
-                        for (int j = 0; j < 32; j += 8) {
-                            uint4 pk;
-                            pk.x = pack_bf16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
-                            pk.y = pack_bf16x2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
-                            pk.z = pack_bf16x2(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5]));
-                            pk.w = pack_bf16x2(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7]));
-                            *reinterpret_cast<uint4 *>(sS + sw128_offset(i, c0 + j, L::kSBlk)) = pk;
-                        }
-                    }
-                    tmem_wait_st();
-                }
-                if (piece_end) {
-                    // this piece's end state, then the next piece's start state
-                    // (both found from the item: the piece ends with its chunk)
-                    const long long a = static_cast<long long>(it.bh) * p.NC;
-                    const int cl = it.t0 / kChunk;
-                    Piece done;
-                    done.u = it.bh;
-                    done.seg = static_cast<int>((a + cl) / p.L - a / p.L);
-                    store_state(done);
-                    const long long gn = a + cl + 1, ge = full_range_end(p);
-                    if (gn < ge) load_state(piece_at(p, gn, ge));
-                    return true;
-                }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[kBarSReady]);
-                return true;
-            };
-            auto output_step = [&]() -> bool {
-                if (!__all_sync(0xffffffffu,
-                                mbar_wait_bounded(&bars[kBarOFull0 + ob], (n >> 1) & 1, p.status)))
-                    return false;
-                tc_fence_after();
-                // staged in the state copy: the V tile is free now
-                if (kStageInS && (it.flags & kItemLast) && lane == 0)
-                    mbar_arrive(&bars[kBarVEmpty0 + it.lc % VS]);
-                {
-                    const uint32_t tO = tmem + lane_base + (ob ? TM::kO1 : TM::kO0);
-                    const int t = it.t0 + i;
-                    const bool st = store_item && !staged && i >= it.r0 && i < it.r1 && t < T;
-                    __nv_bfloat16 *orow = p.o + (static_cast<size_t>(it.bh) * T + t) * p.dv + dv0;
-#pragma unroll
-                    for (int c0 = 0; c0 < DVT; c0 += 64) {
-                        uint32_t ra[32], rb[32];
-                        tmem_ld32(tO + c0, ra);
-                        tmem_ld32(tO + c0 + 32, rb);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int half = 0; half < 2; ++half) {
-                            const uint32_t(&r)[32] = half ? rb : ra;
-                            const int cc = c0 + 32 * half;
-#pragma unroll
-                            for (int j = 0; j < 32; j += 8) {
-                                uint4 pk;
-                                pk.x = pack_bf16x2(p.scale * __uint_as_float(r[j]), p.scale * __uint_as_float(r[j + 1]));
-                                pk.y = pack_bf16x2(p.scale * __uint_as_float(r[j + 2]), p.scale * __uint_as_float(r[j + 3]));
-                                pk.z = pack_bf16x2(p.scale * __uint_as_float(r[j + 4]), p.scale * __uint_as_float(r[j + 5]));
-                                pk.w = pack_bf16x2(p.scale * __uint_as_float(r[j + 6]), p.scale * __uint_as_float(r[j + 7]));
-                                if (staged)
-                                    *reinterpret_cast<uint4 *>(sStage + sw128_offset(i, cc + j, kBlk)) = pk;
-                                else if (st)
-                                    *reinterpret_cast<uint4 *>(orow + cc + j) = pk;
-                            }
-                        }
-                    }
-                }
-                tc_fence_before();
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&bars[kBarOFree0 + ob]);
-                    // This warp's 32 rows of a staged tile leave with one TMA store
-                    // per 64-column block, and the staging rows are reused only
-                    // once the store has read them.
-                    const int r0w = it.t0 + 32 * (warp - kTmemWarp0);
-                    if (staged && r0w < T) {
-#pragma unroll
-                        for (int nb = 0; nb < DVT / 64; ++nb)
-                            tma_store_3d(&p.tm_o32, sStage + nb * kBlk + (warp - kTmemWarp0) * 32 * 128,
-                                         dv0 + nb * 64, r0w, it.bh);
-                        tma_store_commit();
-                        tma_store_wait_read_all();
-                    }
-                    // staged in the V tile: four arrivals free it after the stores
-                    if (!kStageInS && (it.flags & kItemLast))
-                        mbar_arrive(&bars[kBarVEmpty0 + it.lc % VS]);
-                }
-                __syncwarp();
-                return true;
-            };
-            if constexpr (kStageInS) {
-                if (!output_step() || !state_step()) break;
-            } else {
-                if (!state_step() || !output_step()) break;
-            }
-        }
-        if (lane == 0) tma_store_wait_all();
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    if (warp == kMmaWarp) {
-        tc_fence_after();
-        tmem_dealloc(tmem, TM::kCols);
-    }
-    // the peer may still copy into, or arrive on, this CTA's shared memory
-    if constexpr (PAIR) cluster_sync_all();
-}
-
-template <int DK, int DVT, bool PAIR>
-int launch_tiles(const ChunkLaunch &c, cudaStream_t stream) {
-    using L = Smem<DK, DVT, PAIR>;
-    auto kern = chunk_fwd_kernel<DK, DVT, PAIR>;
-    static bool attr_set = false;  // per instantiation, per process
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(L::kAlloc));
-        if (e != cudaSuccess) return static_cast<int>(e);
-        attr_set = true;
-    }
-    KParams p;
-    p.tm_q = c.tm_q;
-    p.tm_k = c.tm_k;
-    p.tm_a = c.tm_a;
-    p.tm_v = c.tm_v;
-    p.tm_o32 = c.tm_o32;
-    p.q = static_cast<const uint32_t *>(c.q);
-    p.k = static_cast<const uint32_t *>(c.k);
-    p.a = reinterpret_cast<const float2 *>(c.log_alpha);
-    p.h0 = c.h0;
-    p.hT = c.hT;
-    p.o = static_cast<__nv_bfloat16 *>(c.o);
-    p.ws_state = c.ws_state;
-    p.ws_decay = c.ws_decay;
-    p.scale = c.scale;
-    p.BH = c.B * c.H;
-    p.T = c.T;
-    p.dv = c.dv;
-    p.NC = c.NC;
-    p.L = c.L;
-    p.seg_max = c.seg_max;
-    p.force_sub = c.force_exact;
-    p.status = c.status;
-    const int n_dvt = c.dv / DVT;
-    // `count` CTAs (clusters) per tile column; the index is blockIdx.y +
-    // blockIdx.z * gridDim.y, so that any count fits the grid's limits
-    auto launch = [&](int mode, long long count) -> cudaError_t {
-        p.mode = mode;
-        p.n_units = count;
-        const unsigned gy = static_cast<unsigned>(count < 32768 ? count : 32768);
-        const unsigned gz = static_cast<unsigned>((count + gy - 1) / gy);
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        cfg.gridDim = dim3(n_dvt, gy, gz);
-        cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = L::kAlloc;
-        cfg.stream = stream;
-        if (PAIR) {
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = 2;   // the two value-column tiles of one head
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-        }
-        return cudaLaunchKernelEx(&cfg, kern, p);
-    };
-    // FULL pass: one CTA (cluster) per range; CORRECT pass: one per (sequence,
-    // segment >= 1), those past a sequence's segment count leave at once
-    cudaError_t e = launch(kModeFull, c.W);
-    if (e != cudaSuccess || c.seg_max == 1) return static_cast<int>(e);
-    return static_cast<int>(
-        launch(kModeCorrect, static_cast<long long>(c.B) * c.H * (c.seg_max - 1)));
-}
-
-template <int DK, int DVT, bool PAIR>
-int max_resident() {
-    using L = Smem<DK, DVT, PAIR>;
-    auto kern = chunk_fwd_kernel<DK, DVT, PAIR>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(L::kAlloc)) != cudaSuccess) {
-        cudaGetLastError();
-        return 0;
-    }
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-        cudaGetLastError();
-        return 0;
-    }
-    if (!PAIR) return sms;   // one CTA per SM (the CTA takes all of TMEM)
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = L::kAlloc;
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess) {
-        cudaGetLastError();
-        return 0;
-    }
-    return clusters;
-}
-
-}  // namespace
 
 int chunk_fwd_max_resident(int dk, int dv_tile, int pair) {
     // cached per device and kernel variant (the query is a driver round trip)
@@ -1578,16 +39,17 @@ int chunk_fwd_max_resident(int dk, int dv_tile, int pair) {
 }
 
 int launch_chunk_fwd(const ChunkLaunch &p, cudaStream_t stream) {
+    if (p.seqs) return launch_chunk_fwd_packed(p, stream);
     if (p.dk == 64) {
-        if (p.dv_tile == 64) return launch_tiles<64, 64, false>(p, stream);
-        if (p.dv_tile == 128) return launch_tiles<64, 128, false>(p, stream);
+        if (p.dv_tile == 64) return launch_tiles<64, 64, false, false>(p, stream);
+        if (p.dv_tile == 128) return launch_tiles<64, 128, false, false>(p, stream);
     } else if (p.dk == 128 && p.pair) {
         if (p.dv != 2 * p.dv_tile) return static_cast<int>(cudaErrorInvalidValue);
-        if (p.dv_tile == 64) return launch_tiles<128, 64, true>(p, stream);
-        if (p.dv_tile == 128) return launch_tiles<128, 128, true>(p, stream);
+        if (p.dv_tile == 64) return launch_tiles<128, 64, true, false>(p, stream);
+        if (p.dv_tile == 128) return launch_tiles<128, 128, true, false>(p, stream);
     } else if (p.dk == 128) {
-        if (p.dv_tile == 64) return launch_tiles<128, 64, false>(p, stream);
-        if (p.dv_tile == 128) return launch_tiles<128, 128, false>(p, stream);
+        if (p.dv_tile == 64) return launch_tiles<128, 64, false, false>(p, stream);
+        if (p.dv_tile == 128) return launch_tiles<128, 128, false, false>(p, stream);
     }
     return static_cast<int>(cudaErrorInvalidValue);
 }

@@ -15,7 +15,7 @@ struct ChunkLaunch {
     // 3-D tensor maps (channel, token, batch*head): q, k, log_alpha, v, and o
     // (32-token boxes: each TMEM warp stores its own rows)
     CUtensorMap tm_q, tm_k, tm_a, tm_v, tm_o32;
-    const void *q, *k;        // bf16 [BH, T, dk]
+    const void *q, *k;        // bf16 [BH, T, dk] (packed: [H, T, dk])
     const float *log_alpha;   // fp32 [BH, T, dk]
     const float *h0;          // [BH, dk, dv] or null (zero state)
     float *hT;                // [BH, dk, dv] or null
@@ -30,12 +30,21 @@ struct ChunkLaunch {
     // ranges of L chunks (the last may be short); NC chunks per sequence;
     // seg_max = most segments any sequence is cut into (1: no sequence is cut).
     int NC, L, W, seg_max;
+    long long total;          // chunks of all sequences
+    // Packed variable-length batches (B = NS sequences per head, T = the
+    // packed rows): device table of NS entries {first row, length, chunks,
+    // chunk offset}, sequence u = n H + h.  Null for fixed-length batches.
+    const int4 *seqs;
+    int NS;
     int force_exact;          // process every chunk in rescaled sub-chunks
     unsigned int *status;     // device status word
 };
 
 // Returns a cudaError_t value (0 on success).
 int launch_chunk_fwd(const ChunkLaunch &p, cudaStream_t stream);
+
+// launch_chunk_fwd for a packed batch (p.seqs set); gla_chunk_packed.cu.
+int launch_chunk_fwd_packed(const ChunkLaunch &p, cudaStream_t stream);
 
 // How many CTAs (clusters, for a CTA pair) of the chunked forward for these
 // head dimensions can run at once on the current device; 0 if unknown.
@@ -49,6 +58,13 @@ int chunk_fwd_with_scratch(const void *q, const void *k, const void *v, const fl
                            float scale, const float *h0, void *o, float *hT, int B, int H, int T,
                            int dk, int dv, const gla_chunk_options *opts, cudaStream_t stream,
                            void *scratch, size_t scratch_bytes);
+
+// The chunked forward over a packed variable-length batch (see
+// gla_chunk_fwd_varlen_ex).  Returns a GLA status.
+int chunk_fwd_packed(const void *q, const void *k, const void *v, const float *log_alpha,
+                     float scale, const float *h0, void *o, float *hT, const int *cu_seqlens,
+                     int N, int H, int T_total, int dk, int dv, const gla_chunk_options *opts,
+                     cudaStream_t stream);
 
 struct DecodeLaunch {
     const void *q, *k, *v;

@@ -98,6 +98,59 @@ int gla_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *l
                      int dk, int dv, const gla_chunk_options *opts, cudaStream_t stream);
 
 /*
+ * gla_chunk_fwd_varlen — the chunked forward over a packed batch of N
+ * sequences of different lengths: the chunkwise form above (the GLA page's
+ * sections "Cumulative Decay Representation" to "Inter-Chunk Recurrence and
+ * Output Projection") applied to each sequence on its own.  The FlashQLA
+ * page, section "Application Scenarios and Outlook", lists variable-length
+ * sequences among the cases such a kernel serves.
+ *
+ * Sequence n holds the token rows [cu_seqlens[n], cu_seqlens[n+1]) of every
+ * head; its recurrence starts from its own initial state and ends in its own
+ * final state, exactly as gla_chunk_fwd with B = 1 on that slice.
+ *
+ *   q, k       : [H, T_total, dk] bf16, device (head-first, sequences packed
+ *                along the token axis)
+ *   v          : [H, T_total, dv] bf16, device
+ *   log_alpha  : [H, T_total, dk] fp32, device
+ *   h0         : [N, H, dk, dv] fp32, device, or NULL (zero initial states)
+ *   o          : [H, T_total, dv] bf16, device, written
+ *   hT         : [N, H, dk, dv] fp32, device, or NULL; may alias h0
+ *   cu_seqlens : HOST array of N + 1 ints: 0 = cu_seqlens[0] <= ... <=
+ *                cu_seqlens[N] = T_total.  Read during the call only; the
+ *                library keeps no pointer to it.  Empty sequences are
+ *                allowed: their hT is their h0 (zero without h0).
+ *
+ * Device pointers must be 16-byte aligned.  Stream-ordered like
+ * gla_chunk_fwd: the call allocates a small per-sequence table (plus the
+ * segment scratch when sequences are split) with cudaMallocAsync on `stream`
+ * and frees it on the same stream.  Returns GLA_ERR_ARG for null required
+ * pointers, N or H <= 0, T_total < 0, cu_seqlens that do not run from 0 to
+ * T_total without decreasing, or misaligned pointers; GLA_ERR_SHAPE for
+ * unsupported dk/dv; GLA_ERR_ALLOC if the scratch cannot be allocated.
+ */
+int gla_chunk_fwd_varlen(const void *q, const void *k, const void *v, const float *log_alpha,
+                         float scale, const float *h0, void *o, float *hT, const int *cu_seqlens,
+                         int N, int H, int T_total, int dk, int dv, cudaStream_t stream);
+
+/* gla_chunk_fwd_varlen with explicit options (opts may be NULL).  With a packed
+ * batch, opts->segments caps the chunks of one range at ceil(longest
+ * sequence's chunks / segments). */
+int gla_chunk_fwd_varlen_ex(const void *q, const void *k, const void *v, const float *log_alpha,
+                            float scale, const float *h0, void *o, float *hT,
+                            const int *cu_seqlens, int N, int H, int T_total, int dk, int dv,
+                            const gla_chunk_options *opts, cudaStream_t stream);
+
+/* The launch plan gla_chunk_fwd_varlen_ex would use for this packed batch
+ * (no GPU work): most segments of any sequence, value-column tile, kernel
+ * launches (0 when every sequence is empty) and stream-ordered scratch bytes
+ * (sequence table included).  Output pointers may be NULL; cu_seqlens is a
+ * host array as for gla_chunk_fwd_varlen. */
+int gla_chunk_fwd_varlen_plan(const int *cu_seqlens, int N, int H, int T_total, int dk, int dv,
+                              const gla_chunk_options *opts, int *n_segments, int *dv_tile,
+                              int *launches, unsigned long *scratch_bytes);
+
+/*
  * gla_chunk_fwd_plan — the launch plan gla_chunk_fwd_ex would use on the
  * current device for these sizes and options (no GPU work is enqueued):
  * the number of sequence segments, the value-column tile, the number of

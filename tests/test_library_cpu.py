@@ -96,6 +96,31 @@ def test_host_entry_validates_before_any_cuda_call(lib):
     assert f(P, P, P, P, 0.1, None, P, None, 1, 1, 16, 64, 48, None) == _lib.GLA_ERR_SHAPE
 
 
+def _cu(*xs):
+    return (ctypes.c_int * len(xs))(*xs)
+
+
+def test_packed_entry_validates_cu_seqlens_on_the_host(lib):
+    f = lib.gla_chunk_fwd_varlen
+    ok = _cu(0, 5, 5, 16)
+    # well-formed offsets reach the device check (no GPU here)
+    assert f(P, P, P, P, 0.1, None, P, None, ok, 3, 2, 16, 64, 64, None) == _lib.GLA_ERR_DEVICE
+    # offsets must start at 0, end at T_total and never decrease
+    assert f(P, P, P, P, 0.1, None, P, None, _cu(1, 5, 16), 2, 2, 16, 64, 64, None) == _lib.GLA_ERR_ARG
+    assert f(P, P, P, P, 0.1, None, P, None, _cu(0, 5, 15), 2, 2, 16, 64, 64, None) == _lib.GLA_ERR_ARG
+    assert f(P, P, P, P, 0.1, None, P, None, _cu(0, 9, 5, 16), 3, 2, 16, 64, 64, None) == _lib.GLA_ERR_ARG
+    assert f(P, P, P, P, 0.1, None, P, None, None, 3, 2, 16, 64, 64, None) == _lib.GLA_ERR_ARG
+    # sizes, pointers, alignment and head dimensions as for gla_chunk_fwd
+    assert f(P, P, P, P, 0.1, None, P, None, ok, 0, 2, 16, 64, 64, None) == _lib.GLA_ERR_ARG
+    assert f(P, P, P, P, 0.1, None, P, None, ok, 3, 0, 16, 64, 64, None) == _lib.GLA_ERR_ARG
+    assert f(None, P, P, P, 0.1, None, P, None, ok, 3, 2, 16, 64, 64, None) == _lib.GLA_ERR_ARG
+    assert f(P + 8, P, P, P, 0.1, None, P, None, ok, 3, 2, 16, 64, 64, None) == _lib.GLA_ERR_ARG
+    assert f(P, P, P, P, 0.1, None, P, None, ok, 3, 2, 16, 96, 64, None) == _lib.GLA_ERR_SHAPE
+    ex = lib.gla_chunk_fwd_varlen_ex
+    bad = ctypes.byref(_lib.GlaChunkOptions(cta_pair=3))
+    assert ex(P, P, P, P, 0.1, None, P, None, ok, 3, 2, 16, 64, 64, bad, None) == _lib.GLA_ERR_ARG
+
+
 def test_python_host_binding_checks_dtypes():
     import torch
     import chunkwise_linear_rnn_gb300 as gla
