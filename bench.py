@@ -80,12 +80,14 @@ def measured_traffic(cfg):
     return MEASURED_TRAFFIC["bytes_per_call"]
 
 
-def chunk_bytes(cfg, n_states: int | None = None) -> int:
+def chunk_bytes(cfg, n_states: int | None = None, gate_per_head: bool = False) -> int:
     """Algorithmic bytes of one chunked forward: each input read once, each output written once.
 
-    n_states: the (sequence, head) states read and written (default B * H).
+    n_states: the (sequence, head) states read and written (default B * H);
+    gate_per_head: one fp32 gate per token instead of one per key channel.
     """
-    per_token = 2 * cfg.dk + 2 * cfg.dk + 2 * cfg.dv + 4 * cfg.dk + 2 * cfg.dv
+    gate = 4 if gate_per_head else 4 * cfg.dk
+    per_token = 2 * cfg.dk + 2 * cfg.dk + 2 * cfg.dv + gate + 2 * cfg.dv
     if n_states is None:
         n_states = cfg.B * cfg.H
     state = n_states * cfg.dk * cfg.dv * 4 * (2 if cfg.sigma_h0 is not None else 1)
@@ -248,6 +250,8 @@ def chunk_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_
     stream = torch.cuda.current_stream(dev)
     n_states = None
     packed = None
+    if args.varlen and args.gate == "head":
+        raise SystemExit("--gate head takes fixed-length batches only")
     if args.varlen:
         # the same tokens per head, packed: --varlen sequences of mixed lengths
         # through gla_chunk_fwd_varlen (q, k, v, gates drawn as for the workload)
@@ -278,6 +282,8 @@ def chunk_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_
         launches_per_step = gla.gla_chunk_fwd_varlen_plan(cu, cfg.H, cfg.dk, cfg.dv)["launches"]
     else:
         q, k, v, a, h0 = make_config_inputs(cfg, seed=rank, device=dev)
+        if args.gate == "head":
+            a = a[..., 0].contiguous()   # one gate per token and head (its first channel's draw)
         o = torch.empty(cfg.B, cfg.H, cfg.T, cfg.dv, dtype=torch.bfloat16, device=dev)
         hT = torch.empty(cfg.B, cfg.H, cfg.dk, cfg.dv, dtype=torch.float32, device=dev)
 
@@ -308,7 +314,7 @@ def chunk_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_
     ms_per_step = total_ms / args.steps
     tokens_all = cfg.tokens * world
     value = tokens_all / (ms_per_step / 1e3)
-    byts = chunk_bytes(cfg, n_states)
+    byts = chunk_bytes(cfg, n_states, gate_per_head=args.gate == "head")
     achieved_gbs = byts / (per_launch_ms / 1e3) / 1e9
     clocks = clk.summary()
 
@@ -316,7 +322,7 @@ def chunk_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_
     # buffers; every call copies its inputs in and its outputs out (pipelined
     # over groups of heads), all inside the timed region
     e2e = None
-    if not args.no_e2e and not args.varlen:
+    if not args.no_e2e and not args.varlen and args.gate == "channel":
         hq, hk, hv, ha = (t.cpu().pin_memory() for t in (q, k, v, a))
         hh0 = None if h0 is None else h0.cpu().pin_memory()
         ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
@@ -362,13 +368,14 @@ def chunk_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": cfg.name + (f"-packed{args.varlen}" if args.varlen else ""),
+        "config": {"workload": cfg.name + (f"-packed{args.varlen}" if args.varlen else "") +
+                   ("-gate-per-head" if args.gate == "head" else ""),
                    "B": cfg.B, "H": cfg.H, "T": cfg.T, "dk": cfg.dk,
                    "dv": cfg.dv, "chunk": 128, "replicas": world,
                    "l2": "inputs (%.2f GB) larger than L2; no flush" % (byts / 1e9)},
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": pk["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved_gbs / pk["hbm_gbs"],
-                     "traffic": None if args.varlen else measured_traffic(cfg),
+                     "traffic": None if (args.varlen or args.gate == "head") else measured_traffic(cfg),
                      "traffic_unit": "bytes per call",
                      "peak_kind": pk_kind, "kernel": "chunk_fwd_kernel",
                      "algorithmic_bytes_per_launch": byts,
@@ -524,6 +531,9 @@ def main():
     ap.add_argument("--batch", type=int, default=0, help="override the workload's B")
     ap.add_argument("--heads", type=int, default=0, help="override the workload's H")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--gate", default="channel", choices=["channel", "head"],
+                    help="log_alpha per key channel [B,H,T,dk] (the workloads') or per head "
+                         "[B,H,T] (no e2e leg)")
     ap.add_argument("--varlen", type=int, default=0,
                     help="pack each head's tokens into this many sequences of mixed lengths "
                          "(gla_chunk_fwd_varlen; no e2e leg)")

@@ -57,6 +57,8 @@ def gla_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: 
                   force_exact: bool = False, cta_pair: int = 0):
     """Chunkwise-parallel GLA forward over whole sequences.
 
+    ``log_alpha`` is ``[B, H, T, dk]`` (one gate per key channel) or
+    ``[B, H, T]`` (one gate per token and head, used for every channel).
     Returns ``(o, hT)``; ``hT`` is None when ``output_final_state`` is False.
     ``final_state`` may be ``h0`` itself (in-place state update).
     ``segments``, ``dv_tile``, ``force_exact`` and ``cta_pair`` are the C ABI's
@@ -73,7 +75,9 @@ def gla_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: 
     _need(q, "q", torch.bfloat16, (B, H, T, dk), dev)
     _need(k, "k", torch.bfloat16, (B, H, T, dk), dev)
     _need(v, "v", torch.bfloat16, (B, H, T, dv), dev)
-    _need(log_alpha, "log_alpha", torch.float32, (B, H, T, dk), dev)
+    # a [B, H, T] gate is one decay per token and head, the same for every channel
+    per_head = log_alpha.dim() == 3
+    _need(log_alpha, "log_alpha", torch.float32, (B, H, T) if per_head else (B, H, T, dk), dev)
     if h0 is not None:
         _need(h0, "h0", torch.float32, (B, H, dk, dv), dev)
     if out is None:
@@ -87,7 +91,8 @@ def gla_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: 
     if scale is None:
         scale = dk ** -0.5
     opts = GlaChunkOptions(segments=int(segments), dv_tile=int(dv_tile),
-                           force_exact=1 if force_exact else 0, cta_pair=int(cta_pair))
+                           force_exact=1 if force_exact else 0, cta_pair=int(cta_pair),
+                           gate_per_head=1 if per_head else 0)
     with torch.cuda.device(dev):
         st = _lib.lib().gla_chunk_fwd_ex(
             q.data_ptr(), k.data_ptr(), v.data_ptr(), log_alpha.data_ptr(), float(scale),

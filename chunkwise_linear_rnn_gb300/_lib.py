@@ -31,7 +31,7 @@ EXPORTED = ("gla_chunk_fwd", "gla_chunk_fwd_ex", "gla_chunk_fwd_plan", "gla_chun
 class GlaChunkOptions(ctypes.Structure):
     _fields_ = [("segments", ctypes.c_int), ("dv_tile", ctypes.c_int),
                 ("force_exact", ctypes.c_int), ("cta_pair", ctypes.c_int),
-                ("reserved", ctypes.c_int * 4)]
+                ("gate_per_head", ctypes.c_int), ("reserved", ctypes.c_int * 3)]
 
 
 class GlaError(RuntimeError):

@@ -175,6 +175,7 @@ Plan make_plan(int B, int H, int T, int dk, int dv, const gla_chunk_options &op,
 bool options_ok(int dv, const gla_chunk_options &op) {
     if (op.dv_tile != 0 && op.dv_tile != 64 && op.dv_tile != 128) return false;
     if (op.dv_tile > dv || op.segments < 0) return false;
+    if (op.gate_per_head != 0 && op.gate_per_head != 1) return false;
     return op.cta_pair >= -1 && op.cta_pair <= 1;
 }
 
@@ -220,13 +221,15 @@ int chunk_fwd_with_scratch(const void *q, const void *k, const void *v, const fl
         pl.seg_max > 1 ? static_cast<size_t>(pl.seg_max) * BH * dk * sizeof(float) : 0;
     if (state_bytes + decay_bytes > (scratch ? scratch_bytes : 0)) return GLA_ERR_SCRATCH;
 
-    ChunkLaunch p;
+    ChunkLaunch p = {};
+    // with one gate per token the kernel reads the gates itself (no A map)
     if (!make_map(enc, &p.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dk, T, BH, 64, 128,
                   CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(enc, &p.tm_k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dk, T, BH, 64, 128,
                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(enc, &p.tm_a, log_alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dk, T, BH,
-                  pl.pair ? dk / 2 : dk, 128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        (!op.gate_per_head &&
+         !make_map(enc, &p.tm_a, log_alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dk, T, BH,
+                   pl.pair ? dk / 2 : dk, 128, CU_TENSOR_MAP_SWIZZLE_NONE)) ||
         !make_map(enc, &p.tm_v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dv, T, BH, 64, 128,
                   CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(enc, &p.tm_o32, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dv, T, BH, 64, 32,
@@ -259,6 +262,7 @@ int chunk_fwd_with_scratch(const void *q, const void *k, const void *v, const fl
     p.total = static_cast<long long>(BH) * pl.NC;
     p.seqs = nullptr;
     p.NS = 0;
+    p.gate_per_head = op.gate_per_head;
     p.force_exact = op.force_exact ? 1 : 0;
     p.status = dev->status;
     return launch_chunk_fwd(p, stream) == 0 ? GLA_OK : GLA_ERR_LAUNCH;
@@ -349,7 +353,7 @@ int chunk_fwd_packed(const void *q, const void *k, const void *v, const float *l
     if (!dk_ok(dk) || !dv_ok(dv)) return GLA_ERR_SHAPE;
     gla_chunk_options o_def = {};
     const gla_chunk_options &op = opts ? *opts : o_def;
-    if (!options_ok(dv, op)) return GLA_ERR_ARG;
+    if (!options_ok(dv, op) || op.gate_per_head) return GLA_ERR_ARG;
     if (static_cast<long long>(N) * H > 0x7fffffffLL) return GLA_ERR_ARG;
     Packed pk;
     int st = packed_layout(cu_seqlens, N, T_total, &pk);
@@ -400,7 +404,7 @@ int chunk_fwd_packed(const void *q, const void *k, const void *v, const float *l
         cudaGetLastError();
         result = GLA_ERR_LAUNCH;
     }
-    ChunkLaunch p;
+    ChunkLaunch p = {};
     if (result == GLA_OK &&
         (!make_map(enc, &p.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dk, T_total, H, 64, 128,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||

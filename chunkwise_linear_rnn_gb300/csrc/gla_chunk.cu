@@ -40,16 +40,17 @@ int chunk_fwd_max_resident(int dk, int dv_tile, int pair) {
 
 int launch_chunk_fwd(const ChunkLaunch &p, cudaStream_t stream) {
     if (p.seqs) return launch_chunk_fwd_packed(p, stream);
+    if (p.gate_per_head) return launch_chunk_fwd_scalar(p, stream);
     if (p.dk == 64) {
-        if (p.dv_tile == 64) return launch_tiles<64, 64, false, false>(p, stream);
-        if (p.dv_tile == 128) return launch_tiles<64, 128, false, false>(p, stream);
+        if (p.dv_tile == 64) return launch_tiles<64, 64, false, false, false>(p, stream);
+        if (p.dv_tile == 128) return launch_tiles<64, 128, false, false, false>(p, stream);
     } else if (p.dk == 128 && p.pair) {
         if (p.dv != 2 * p.dv_tile) return static_cast<int>(cudaErrorInvalidValue);
-        if (p.dv_tile == 64) return launch_tiles<128, 64, true, false>(p, stream);
-        if (p.dv_tile == 128) return launch_tiles<128, 128, true, false>(p, stream);
+        if (p.dv_tile == 64) return launch_tiles<128, 64, true, false, false>(p, stream);
+        if (p.dv_tile == 128) return launch_tiles<128, 128, true, false, false>(p, stream);
     } else if (p.dk == 128) {
-        if (p.dv_tile == 64) return launch_tiles<128, 64, false, false>(p, stream);
-        if (p.dv_tile == 128) return launch_tiles<128, 128, false, false>(p, stream);
+        if (p.dv_tile == 64) return launch_tiles<128, 64, false, false, false>(p, stream);
+        if (p.dv_tile == 128) return launch_tiles<128, 128, false, false, false>(p, stream);
     }
     return static_cast<int>(cudaErrorInvalidValue);
 }

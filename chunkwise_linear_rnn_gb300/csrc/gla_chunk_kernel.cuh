@@ -171,6 +171,7 @@ struct KParams {
     const uint32_t *q;  // bf16 pairs
     const uint32_t *k;
     const float2 *a;
+    const float *g;     // one gate per (sequence, token), [BH][T] (SCALAR kernels), else null
     const float *h0;
     float *hT;
     __nv_bfloat16 *o;
@@ -360,7 +361,7 @@ __device__ __forceinline__ void zero_p_block(uint32_t taddr) {
 // `n` counts items; `last_flags` go to the chunk's last item; gtot0/gtot1
 // return the chunk's clamped Gamma at its end for the thread's channels (valid
 // in the last token part).  Returns false if a bounded wait expired.
-template <int DK, bool PACKED, typename BeforeEmptyWait>
+template <int DK, bool PACKED, bool SCALAR, typename BeforeEmptyWait>
 __device__ __forceinline__ bool sub_chunk_items(const KParams &p, int bh, int t0, int lc,
                                                 bool store, int last_flags, int pt, uint8_t *sQ,
                                                 uint8_t *sK,
@@ -380,10 +381,15 @@ __device__ __forceinline__ bool sub_chunk_items(const KParams &p, int bh, int t0
     const size_t row0 = static_cast<size_t>(sq.z) * p.T + sq.y0;
     const uint32_t *qb = p.q + (row0 * DK + ch) / 2;
     const uint32_t *kb = p.k + (row0 * DK + ch) / 2;
-    const float2 *ab = p.a + (row0 * DK + ch) / 2;
     auto raw_gate = [&](int i) {
         const int t = t0 + i;
-        return t < T ? ab[static_cast<size_t>(t) * kStride] : make_float2(0.f, 0.f);
+        if constexpr (SCALAR) {
+            const float g = t < T ? p.g[row0 + t] : 0.f;
+            return make_float2(g, g);
+        } else {
+            const float2 *ab = p.a + (row0 * DK + ch) / 2;
+            return t < T ? ab[static_cast<size_t>(t) * kStride] : make_float2(0.f, 0.f);
+        }
     };
     float bnd0[NQ], bnd1[NQ];  // clamped Gamma just before each part start
     {
@@ -506,7 +512,7 @@ __device__ __forceinline__ bool sub_chunk_items(const KParams &p, int bh, int t0
 // Threads pt < DK keep the decay since the segment start of channel pt; both
 // CTAs compute it from identical bits (the exchanged factor table, or the raw
 // gates), so their window decisions agree.
-template <int DK, int DVT, bool PACKED>
+template <int DK, int DVT, bool PACKED, bool SCALAR>
 __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint32_t rank,
                                           long long g_begin, long long g_end, size_t BHn,
                                           int dv_tile) {
@@ -583,9 +589,21 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
             float c0 = 0.f, c1 = 0.f;
             float lmn = 3.0e38f, lmx = -3.0e38f;
             float2 av[TP];
+            if constexpr (SCALAR) {
+                // one gate per token, the same for every channel
+                const Seq sq = seq_of<PACKED>(p, bh);
+                const float *gr = p.g + static_cast<size_t>(sq.z) * p.T + sq.y0 + t0 + part * TP;
+                const int left = sq.len - t0 - part * TP;
 #pragma unroll
-            for (int e = 0; e < TP; ++e)
-                av[e] = *reinterpret_cast<const float2 *>(sAc + (part * TP + e) * DKH);
+                for (int e = 0; e < TP; ++e) {
+                    const float g = e < left ? __ldg(gr + e) : 0.f;
+                    av[e] = make_float2(g, g);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < TP; ++e)
+                    av[e] = *reinterpret_cast<const float2 *>(sAc + (part * TP + e) * DKH);
+            }
             if (PACKED && valid < kChunk) {
 #pragma unroll
                 for (int e = 0; e < TP; ++e)
@@ -722,16 +740,17 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
             // channels, computed by each CTA of the pair on its own
             if (n > 0) ok &= mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status);
             float gt0 = 0.f, gt1 = 0.f;
-            ok &= sub_chunk_items<DK, PACKED>(p, bh, t0, lc, store, piece_end, pt, sQ, sK, sKlo, sG, sItem,
+            ok &= sub_chunk_items<DK, PACKED, SCALAR>(p, bh, t0, lc, store, piece_end, pt, sQ, sK, sKlo, sG, sItem,
                                       bars, n, gt0, gt1, [] {});
             if (pt < DK) {
                 // the chunk's clamped decay of channel pt, summed in token order
                 const Seq sq = seq_of<PACKED>(p, bh);
-                const float *ab = reinterpret_cast<const float *>(p.a) +
-                                  (static_cast<size_t>(sq.z) * p.T + sq.y0) * DK + pt;
+                const size_t row0 = static_cast<size_t>(sq.z) * p.T + sq.y0;
                 float gsum = 0.f;
                 for (int i = 0; i < kChunk && t0 + i < sq.len; ++i)
-                    gsum += clamp_gate(ab[static_cast<size_t>(t0 + i) * DK]);
+                    gsum += clamp_gate(SCALAR ? p.g[row0 + t0 + i]
+                                              : reinterpret_cast<const float *>(
+                                                    p.a)[(row0 + t0 + i) * DK + pt]);
                 gseg += gsum;
             }
         }
@@ -783,7 +802,7 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
     if (lane == 0) mbar_arrive(&bars[kBarQkFull]);
 }
 
-template <int DK, int DVT, bool PAIR, bool PACKED>
+template <int DK, int DVT, bool PAIR, bool PACKED, bool SCALAR>
 __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_constant__ KParams p) {
     using L = Smem<DK, DVT, PAIR>;
     using TM = Tmem<DVT>;
@@ -843,7 +862,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
     if (warp == kTmaWarp && lane == 0) {
         prefetch_tensormap(&p.tm_q);
         prefetch_tensormap(&p.tm_k);
-        prefetch_tensormap(&p.tm_a);
+        if (!SCALAR) prefetch_tensormap(&p.tm_a);
         prefetch_tensormap(&p.tm_v);
         prefetch_tensormap(&p.tm_o32);
     }
@@ -856,7 +875,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
 
     if (warp < kPrepWarps && PAIR) {
         if constexpr (PAIR) {
-            prep_pair<DK, DVT, PACKED>(p, smem, rank, g_begin, g_end, BHn, dv_tile);
+            prep_pair<DK, DVT, PACKED, SCALAR>(p, smem, rank, g_begin, g_end, BHn, dv_tile);
         }
     } else if (warp < kPrepWarps) {
         // =========================================================== prep warps
@@ -908,10 +927,26 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             float c0 = 0.f, c1 = 0.f;
             float lmn = 3.0e38f, lmx = -3.0e38f;
             {
+                // the gates of token i: this thread's channel pair of the A
+                // tile, or the token's one gate for every channel
+                const float *gr = nullptr;
+                int left = kChunk;
+                if constexpr (SCALAR) {
+                    const Seq sq = seq_of<PACKED>(p, bh);
+                    gr = p.g + static_cast<size_t>(sq.z) * p.T + sq.y0 + t0;
+                    left = sq.len - t0;
+                }
+                auto gate = [&](int i) -> float2 {
+                    if constexpr (SCALAR) {
+                        const float g = i < left ? __ldg(gr + i) : 0.f;
+                        return make_float2(g, g);
+                    } else {
+                        return *reinterpret_cast<const float2 *>(sAc + i * DK);
+                    }
+                };
                 float2 nx[kB];
 #pragma unroll
-                for (int e = 0; e < kB; ++e)
-                    nx[e] = *reinterpret_cast<const float2 *>(sAc + (part * TP + e) * DK);
+                for (int e = 0; e < kB; ++e) nx[e] = gate(part * TP + e);
                 for (int i0 = part * TP; i0 < (part + 1) * TP; i0 += kB) {
                     float2 cur[kB];
 #pragma unroll
@@ -919,8 +954,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                         cur[e] = (PACKED && i0 + e >= valid) ? make_float2(0.f, 0.f) : nx[e];
                     if (i0 + kB < (part + 1) * TP) {
 #pragma unroll
-                        for (int e = 0; e < kB; ++e)
-                            nx[e] = *reinterpret_cast<const float2 *>(sAc + (i0 + kB + e) * DK);
+                        for (int e = 0; e < kB; ++e) nx[e] = gate(i0 + kB + e);
                     }
 #pragma unroll
                     for (int e = 0; e < kB; ++e) {
@@ -1016,7 +1050,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             }
             // ---- sub-chunk rescaling (chunks whose decay exceeds the bound)
             float gtot0 = 0.f, gtot1 = 0.f;
-            ok = sub_chunk_items<DK, PACKED>(p, bh, t0, lc, store, piece_end, pt, sQ, sK, sKlo, sG, sItem,
+            ok = sub_chunk_items<DK, PACKED, SCALAR>(p, bh, t0, lc, store, piece_end, pt, sQ, sK, sKlo, sG, sItem,
                                      bars, n, gtot0, gtot1, [] {});
             if (last_part) {
                 gseg0 += gtot0;
@@ -1072,9 +1106,25 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                         bhs[n_req & 3] = bh;
                         // A (and staging): the prep released them with the request
                         fence_proxy_async_smem();
-                        mbar_arrive_expect_tx(&bars[kBarAFull], L::kABytes);
-                        tma_load_3d(sA, &p.tm_a, &bars[kBarAFull], static_cast<int>(rank) * L::kDKA,
-                                    t0, bh);
+                        if constexpr (SCALAR) {
+                            // one gate per token: the prep threads read the
+                            // chunk's 512 bytes themselves; pull them into L2
+                            // (16-byte blocks inside the gate array only)
+                            const uintptr_t a0 = reinterpret_cast<uintptr_t>(
+                                p.g + static_cast<size_t>(bh) * p.T + t0);
+                            const uintptr_t end = reinterpret_cast<uintptr_t>(
+                                p.g + static_cast<size_t>(p.BH) * p.T);
+                            const uintptr_t lo = (a0 + 15) & ~static_cast<uintptr_t>(15);
+                            const uintptr_t hi = min(a0 + kChunk * 4, end) & ~static_cast<uintptr_t>(15);
+                            if (hi > lo)
+                                prefetch_l2_bulk(reinterpret_cast<const void *>(lo),
+                                                 static_cast<uint32_t>(hi - lo));
+                            mbar_arrive(&bars[kBarAFull]);
+                        } else {
+                            mbar_arrive_expect_tx(&bars[kBarAFull], L::kABytes);
+                            tma_load_3d(sA, &p.tm_a, &bars[kBarAFull],
+                                        static_cast<int>(rank) * L::kDKA, t0, bh);
+                        }
                         if constexpr (PAIR) {
                             uint8_t *sRaw = smem + L::kRaw;
                             mbar_arrive_expect_tx(&bars[kBarQkRaw], 2u * kBlk);
@@ -1536,10 +1586,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
     if constexpr (PAIR) cluster_sync_all();
 }
 
-template <int DK, int DVT, bool PAIR, bool PACKED>
+template <int DK, int DVT, bool PAIR, bool PACKED, bool SCALAR>
 int launch_tiles(const ChunkLaunch &c, cudaStream_t stream) {
     using L = Smem<DK, DVT, PAIR>;
-    auto kern = chunk_fwd_kernel<DK, DVT, PAIR, PACKED>;
+    auto kern = chunk_fwd_kernel<DK, DVT, PAIR, PACKED, SCALAR>;
     static bool attr_set = false;  // per instantiation, per process
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1555,7 +1605,8 @@ int launch_tiles(const ChunkLaunch &c, cudaStream_t stream) {
     p.tm_o32 = c.tm_o32;
     p.q = static_cast<const uint32_t *>(c.q);
     p.k = static_cast<const uint32_t *>(c.k);
-    p.a = reinterpret_cast<const float2 *>(c.log_alpha);
+    p.a = SCALAR ? nullptr : reinterpret_cast<const float2 *>(c.log_alpha);
+    p.g = SCALAR ? c.log_alpha : nullptr;
     p.h0 = c.h0;
     p.hT = c.hT;
     p.o = static_cast<__nv_bfloat16 *>(c.o);
@@ -1609,7 +1660,7 @@ int launch_tiles(const ChunkLaunch &c, cudaStream_t stream) {
 template <int DK, int DVT, bool PAIR>
 int max_resident() {
     using L = Smem<DK, DVT, PAIR>;
-    auto kern = chunk_fwd_kernel<DK, DVT, PAIR, false>;
+    auto kern = chunk_fwd_kernel<DK, DVT, PAIR, false, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(L::kAlloc)) != cudaSuccess) {
         cudaGetLastError();

@@ -36,6 +36,7 @@ struct ChunkLaunch {
     // chunk offset}, sequence u = n H + h.  Null for fixed-length batches.
     const int4 *seqs;
     int NS;
+    int gate_per_head;        // 1: log_alpha is [BH, T], one gate per token (fixed length only)
     int force_exact;          // process every chunk in rescaled sub-chunks
     unsigned int *status;     // device status word
 };
@@ -45,6 +46,10 @@ int launch_chunk_fwd(const ChunkLaunch &p, cudaStream_t stream);
 
 // launch_chunk_fwd for a packed batch (p.seqs set); gla_chunk_packed.cu.
 int launch_chunk_fwd_packed(const ChunkLaunch &p, cudaStream_t stream);
+
+// launch_chunk_fwd with one gate per token and head (p.gate_per_head);
+// gla_chunk_scalar.cu.
+int launch_chunk_fwd_scalar(const ChunkLaunch &p, cudaStream_t stream);
 
 // How many CTAs (clusters, for a CTA pair) of the chunked forward for these
 // head dimensions can run at once on the current device; 0 if unknown.

@@ -125,6 +125,14 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+// Pull `bytes` (a multiple of 16) of global memory from a 16-byte aligned
+// address into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src, int x, int y,
                                              int z) {
     asm volatile(

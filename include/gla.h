@@ -89,7 +89,14 @@ typedef struct gla_chunk_options {
     int cta_pair;      /* dk = 128 with two value-column tiles: 0 = run the tiles of a head as
                           a 2-CTA cluster sharing the key-side preparation (default),
                           -1 = independent CTAs; other values are GLA_ERR_ARG              */
-    int reserved[4];
+    int gate_per_head; /* 1 = log_alpha is [B, H, T] fp32: one gate per token and head, the
+                          same for every key channel (RetNet's fixed decay, the GLA page's
+                          "The Retention and Recall Degradation Problem"; Mamba-2's scalar
+                          gate, its "Structural Comparison Across Sub-Quadratic
+                          Architectures"); the result is that of the [B, H, T, dk] gate
+                          with every channel equal.  Fixed-length calls only
+                          (gla_chunk_fwd_varlen_ex returns GLA_ERR_ARG); 0 = per channel */
+    int reserved[3];
 } gla_chunk_options;
 
 /* gla_chunk_fwd with explicit options (opts may be NULL = all automatic). */

@@ -119,6 +119,16 @@ def test_packed_entry_validates_cu_seqlens_on_the_host(lib):
     ex = lib.gla_chunk_fwd_varlen_ex
     bad = ctypes.byref(_lib.GlaChunkOptions(cta_pair=3))
     assert ex(P, P, P, P, 0.1, None, P, None, ok, 3, 2, 16, 64, 64, bad, None) == _lib.GLA_ERR_ARG
+    # one gate per head is for fixed-length calls only
+    per_head = ctypes.byref(_lib.GlaChunkOptions(gate_per_head=1))
+    assert ex(P, P, P, P, 0.1, None, P, None, ok, 3, 2, 16, 64, 64, per_head, None) == _lib.GLA_ERR_ARG
+
+
+def test_gate_per_head_option_is_validated(lib):
+    assert _chunk(lib, opts=ctypes.byref(_lib.GlaChunkOptions(gate_per_head=2))) == _lib.GLA_ERR_ARG
+    import torch
+    if not torch.cuda.is_available():
+        assert _chunk(lib, opts=ctypes.byref(_lib.GlaChunkOptions(gate_per_head=1))) == _lib.GLA_ERR_DEVICE
 
 
 def test_python_host_binding_checks_dtypes():
