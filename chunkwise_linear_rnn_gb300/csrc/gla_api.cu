@@ -133,7 +133,13 @@ int nseg_host(long long u, int NC, int L) {
 // cut inside a sequence makes a new segment of it, joined by the state
 // correction.  Ranges stay at least kMinRange chunks long, so that the
 // correction windows stay a small part of the work.
-Plan make_plan(int B, int H, int T, int dk, int dv, const gla_chunk_options &op, int sm_count) {
+size_t scratch_needed(const Plan &pl, int B, int H, int dk, int dv);
+
+// scratch_cap: bytes of segment scratch available (SIZE_MAX: allocated to
+// fit).  An automatic plan whose segments would need more takes longer
+// ranges, down to one range per sequence (no scratch).
+Plan make_plan(int B, int H, int T, int dk, int dv, const gla_chunk_options &op, int sm_count,
+               size_t scratch_cap = SIZE_MAX) {
     Plan pl;
     pl.dv_tile = op.dv_tile ? op.dv_tile : (dv >= 128 ? 128 : 64);
     pl.pair = dk == 128 && dv == 2 * pl.dv_tile && op.cta_pair >= 0;
@@ -164,12 +170,17 @@ Plan make_plan(int B, int H, int T, int dk, int dv, const gla_chunk_options &op,
         }
     }
     if (L < 1) L = 1;
-    pl.L = static_cast<int>(L);
-    pl.W = static_cast<int>((total + L - 1) / L);
-    pl.seg_max = 1;
-    if (pl.L < pl.NC)
-        for (long long u = 0; u < BH; ++u) pl.seg_max = std::max(pl.seg_max, nseg_host(u, pl.NC, pl.L));
-    return pl;
+    while (true) {
+        pl.L = static_cast<int>(L);
+        pl.W = static_cast<int>((total + L - 1) / L);
+        pl.seg_max = 1;
+        if (pl.L < pl.NC)
+            for (long long u = 0; u < BH; ++u)
+                pl.seg_max = std::max(pl.seg_max, nseg_host(u, pl.NC, pl.L));
+        if (op.segments > 0 || pl.seg_max == 1 || scratch_needed(pl, B, H, dk, dv) <= scratch_cap)
+            return pl;
+        L = std::min<long long>(2 * L, pl.NC);
+    }
 }
 
 bool options_ok(int dv, const gla_chunk_options &op) {
@@ -214,7 +225,8 @@ int chunk_fwd_with_scratch(const void *q, const void *k, const void *v, const fl
     if (st != GLA_OK) return st;
 
     const int BH = B * H;
-    const Plan pl = make_plan(B, H, T, dk, dv, op, dev->sm_count);
+    const Plan pl =
+        make_plan(B, H, T, dk, dv, op, dev->sm_count, scratch ? scratch_bytes : SIZE_MAX);
     const size_t state_bytes =
         pl.seg_max > 1 ? static_cast<size_t>(pl.seg_max) * BH * dk * dv * sizeof(float) : 0;
     const size_t decay_bytes =

@@ -181,10 +181,12 @@ int gla_chunk_fwd_plan(int B, int H, int T, int dk, int dv, const gla_chunk_opti
  * on every GPU that loads it, until the process exits.  The caller still
  * passes every input and output buffer.
  *
- * Limit: when the launch plan (see gla_chunk_fwd_plan) needs more scratch
- * than the array holds, the call returns GLA_ERR_SCRATCH and enqueues nothing.
- * Automatic plans on a GB300 need at most about 10 MB; larger needs come
- * only from an explicit opts->segments.
+ * Limit: an automatic plan (opts->segments == 0) whose segments would need
+ * more scratch than the array holds cuts the sequences into fewer, longer
+ * segments (down to none), so it always fits; the results stay within the
+ * accuracy bar either way.  An explicit opts->segments that needs more
+ * returns GLA_ERR_SCRATCH and enqueues nothing.  gla_chunk_fwd_plan reports
+ * the allocating entry point's plan.
  *
  * Set-up: the first call on each device looks up the array's device address
  * (with that device current) and caches it; make that first call before any

@@ -78,3 +78,25 @@ def test_noalloc_rejects_plans_beyond_its_scratch(lib):
     assert _abi_call(lib.gla_chunk_fwd_noalloc, q, k, v, a, None, o, h, opts) == _lib.GLA_ERR_SCRATCH
     torch.cuda.synchronize()
     assert torch.count_nonzero(o).item() == 0 and torch.count_nonzero(h).item() == 0
+
+
+def test_automatic_plans_beyond_the_scratch_take_longer_segments(lib):
+    # many sequences of a few dozen chunks: the allocating plan cuts them into
+    # segments whose scratch exceeds the fixed array; the no-allocation call
+    # takes longer segments instead of failing
+    B, H, T, dk, dv = 50, 2, 4096, 128, 128
+    plan = gla.gla_chunk_fwd_plan(B, H, T, dk, dv)
+    if plan["scratch_bytes"] <= _lib_scratch_limit():
+        pytest.skip(f"the allocating plan fits the fixed scratch on this device ({plan})")
+    q, k, v, a, h0 = make_chunk_inputs(B, H, T, dk, dv, sigma_h0=0.1, seed=3, device=DEV)
+    o_ref = torch.empty(B, H, T, dv, dtype=torch.bfloat16, device=DEV)
+    h_ref = torch.empty(B, H, dk, dv, dtype=torch.float32, device=DEV)
+    o = torch.full_like(o_ref, float("nan"))
+    h = torch.full_like(h_ref, float("nan"))
+    assert _abi_call(lib.gla_chunk_fwd_ex, q, k, v, a, h0, o_ref, h_ref) == _lib.GLA_OK
+    assert _abi_call(lib.gla_chunk_fwd_noalloc, q, k, v, a, h0, o, h) == _lib.GLA_OK
+    torch.cuda.synchronize()
+    assert lib.gla_last_device_status(None) == _lib.GLA_OK
+    assert_close(o.float().cpu().numpy(), o_ref.double().cpu().numpy(), "longer segments o",
+                 bf16_output=True)
+    assert_close(h.cpu().numpy(), h_ref.double().cpu().numpy(), "longer segments hT")
