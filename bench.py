@@ -194,6 +194,35 @@ class ClockSampler:
 
 # --------------------------------------------------------------------------- our arm
 
+class Ranks:
+    """The replicas' rank helpers: a barrier and the maximum over ranks.
+
+    With a process group (any backend; NCCL on the GPU machine, gloo in the CPU
+    tests) they go through it; alone they are a device synchronisation and
+    the identity.  `device` is where the reduction tensor lives.
+    """
+
+    def __init__(self, dist=None, device=None):
+        import torch
+        self.dist = dist
+        self.device = device if device is not None else torch.device("cpu")
+
+    def barrier(self):
+        import torch
+        if self.dist is not None:
+            self.dist.barrier()
+        if self.device.type == "cuda":
+            torch.cuda.synchronize(self.device)
+
+    def max_over_ranks(self, x: float) -> float:
+        import torch
+        if self.dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=self.device)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import __graft_entry__ as ge
@@ -206,18 +235,8 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-
-    def barrier():
-        if dist is not None:
-            dist.barrier()
-        torch.cuda.synchronize(dev)
-
-    def max_over_ranks(x: float) -> float:
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    ranks = Ranks(dist, dev)
+    barrier, max_over_ranks = ranks.barrier, ranks.max_over_ranks
 
     pk, pk_kind = peaks()
     cfg = chunk_config(args)

@@ -1,0 +1,71 @@
+"""The replica path of bench.py (one process per GPU, no data exchange) on the CPU.
+
+Two gloo ranks exercise the rank helpers the GPU run uses over NCCL: the
+barrier, and the maximum over ranks that turns per-rank times into the job's
+time.  The reference arm's ranks other than 0 exit at once, without output.
+"""
+
+from __future__ import annotations
+
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank: int, world: int, port: int, out):
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
+                            world_size=world)
+    try:
+        r = bench.Ranks(dist)
+        r.barrier()
+        t = r.max_over_ranks(10.0 + 5.0 * rank)   # per-rank "ms"; the slowest rank wins
+        r.barrier()
+        out.put((rank, t))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_agree_on_the_slowest_time():
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = dict(q.get(timeout=10) for _ in range(world))
+    assert got == {0: 15.0, 1: 15.0}
+
+
+def test_single_process_helpers_are_the_identity():
+    sys.path.insert(0, ROOT)
+    import bench
+    r = bench.Ranks()
+    r.barrier()
+    assert r.max_over_ranks(3.25) == 3.25
+
+
+def test_reference_arm_other_ranks_exit_without_output():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference"],
+                         env=env, capture_output=True, text=True, timeout=300)
+    assert res.returncode == 0, res.stderr[-2000:]
+    assert res.stdout.strip() == ""
