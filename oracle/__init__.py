@@ -9,17 +9,23 @@ Foundations, ..." (llms.blog), section "The Gated Recurrent Update"):
 
     S_t = diag(alpha_t) S_{t-1} + k_t^T v_t,   o_t = scale * q_t S_t,
 
-token by token, in double precision, from S_0 = h0 (zero when absent).
+token by token, in double precision, from S_0 = h0 (zero when absent), and
+``backward``: the gradients of sum_t <do_t, o_t> + <dhT, hT> with respect to
+q, k, v, log alpha and h0, by reverse-mode differentiation of the same loop.
 
 Pins (checked by ``tests/test_oracle_pins.py``): the unrolled dual attention
 form by brute force, vanilla causal linear attention at alpha = 1, RetNet's
 fixed decay at alpha = gamma, the chunkwise equations at every chunk size,
 state passing across a split, the T = 1 closed form, the alpha -> 0 limit,
 linearity in (v, h0), the contraction bound, a hand-worked example, and
-mutants of this file that each of those pins must reject.
+mutants of this file that each of those pins must reject.  The backward is
+pinned by ``tests/test_oracle_bwd_pins.py``: central differences of the
+forward, autograd through the dual attention form, the log-gate identity and
+mutants of the backward.
 """
 
 from .gla_oracle import (  # noqa: F401
+    backward,
     build,
     forward,
     forward_torch,

@@ -114,3 +114,142 @@ void gla_oracle_step(const float *q, const float *k, const float *v, const float
                          log_alpha + bh * dk, scale, o + bh * dv, dk, dv);
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/*
+ * Backward pass — gradients of a scalar loss through the same recurrence.
+ *
+ * Source: the recurrence of "The Gated Recurrent Update" above; the pages
+ * state that training differentiates it and that the chunkwise method keeps
+ * its states for the backward pass ("Gated Linear Attention (GLA) ...",
+ * section "Chunkwise Parallel Form", closing remark on hardware efficiency).
+ * They print no backward equations, so this is reverse-mode differentiation
+ * of the token loop, written out.  With the loss
+ *
+ *     L = sum_t <do_t, o_t> + <dhT, hT>,
+ *
+ * the adjoint G_t = dL/dS_t obeys G_T = dhT + scale q_T^T do_T and
+ * G_{t-1} = diag(alpha_t) G_t + scale q_{t-1}^T do_{t-1}; per token t:
+ *
+ *     dq_t = scale * S_t do_t                   (S_t after token t)
+ *     dk_t = G_t v_t^T,  dv_t = k_t G_t
+ *     dlog_alpha_t = alpha_t (.) rowsum(G_t (.) S_{t-1})
+ *     dh0 = diag(alpha_1) G_1
+ *
+ * (the last because S_{t-1} -> S_t multiplies row d by alpha_t[d], and
+ * d alpha / d log alpha = alpha).
+ *
+ * Memory schedule: the loop needs S_{t-1} and S_t going backward in t.  States
+ * are kept at checkpoints every `ck` tokens and each block of tokens is
+ * replayed from its checkpoint with the same update as the forward pass, so
+ * every state is bit-identical to the one the forward loop computes.  `ck` is
+ * a memory setting only (0 = about sqrt(T)); results do not depend on it.
+ */
+
+/* S <- diag(exp(a)) S + k^T v, the state half of gla_oracle_token. */
+static void gla_oracle_update(double *S, const float *k, const float *v, const float *a, int dk,
+                              int dv) {
+    for (int d = 0; d < dk; ++d) {
+        const double alpha = exp((double)a[d]);
+        const double kd = (double)k[d];
+        double *row = S + (int64_t)d * dv;
+        for (int c = 0; c < dv; ++c) row[c] = alpha * row[c] + kd * (double)v[c];
+    }
+}
+
+/*
+ * q, k, log_alpha [BH][T][dk]; v, d_o [BH][T][dv]; h0, dhT [BH][dk][dv]
+ * (either may be NULL = zero).  Writes grad_q, grad_k, grad_log_alpha
+ * [BH][T][dk], grad_v [BH][T][dv] and, when grad_h0 != NULL, [BH][dk][dv].
+ * Returns 0, or -1 when a work buffer cannot be allocated.
+ */
+int gla_oracle_backward(const float *q, const float *k, const float *v, const float *log_alpha,
+                        double scale, const double *h0, const float *d_o, const double *dhT,
+                        double *grad_q, double *grad_k, double *grad_v, double *grad_log_alpha,
+                        double *grad_h0, int64_t BH, int64_t T, int dk, int dv, int64_t ck,
+                        int nthreads) {
+    set_threads(nthreads);
+    if (ck <= 0) {
+        ck = 1;
+        while (ck * ck < T) ++ck;
+    }
+    const int64_t nck = T > 0 ? (T + ck - 1) / ck : 0;  /* checkpoints at t = 0, ck, 2ck, ... */
+    const size_t ssz = (size_t)dk * (size_t)dv;
+    int failed = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
+    for (int64_t bh = 0; bh < BH; ++bh) {
+        double *cp = (double *)malloc(sizeof(double) * ssz * (size_t)(nck > 0 ? nck : 1));
+        double *blk = (double *)malloc(sizeof(double) * ssz * (size_t)(ck + 1));
+        double *G = (double *)malloc(sizeof(double) * ssz);
+        if (!cp || !blk || !G) {
+            free(cp); free(blk); free(G);
+            failed |= 1;
+            continue;
+        }
+        const float *qh = q + bh * T * dk, *kh = k + bh * T * dk, *ah = log_alpha + bh * T * dk;
+        const float *vh = v + bh * T * dv, *doh = d_o + bh * T * dv;
+        /* forward sweep: keep S_t at t = 0, ck, 2ck, ... (S_0 = h0) */
+        double *S = blk;
+        if (h0) memcpy(S, h0 + bh * (int64_t)ssz, sizeof(double) * ssz);
+        else memset(S, 0, sizeof(double) * ssz);
+        for (int64_t t = 0; t < T; ++t) {
+            if (t % ck == 0) memcpy(cp + (t / ck) * (int64_t)ssz, S, sizeof(double) * ssz);
+            gla_oracle_update(S, kh + t * dk, vh + t * dv, ah + t * dk, dk, dv);
+        }
+        /* adjoint of the final state */
+        if (dhT) memcpy(G, dhT + bh * (int64_t)ssz, sizeof(double) * ssz);
+        else memset(G, 0, sizeof(double) * ssz);
+        for (int64_t b = nck - 1; b >= 0; --b) {
+            const int64_t t0 = b * ck, t1 = (t0 + ck < T) ? t0 + ck : T;
+            /* replay: blk[j] = S_{t0 + j} for j = 0 .. t1 - t0 */
+            memcpy(blk, cp + b * (int64_t)ssz, sizeof(double) * ssz);
+            for (int64_t t = t0; t < t1; ++t) {
+                double *nxt = blk + (t - t0 + 1) * (int64_t)ssz;
+                memcpy(nxt, blk + (t - t0) * (int64_t)ssz, sizeof(double) * ssz);
+                gla_oracle_update(nxt, kh + t * dk, vh + t * dv, ah + t * dk, dk, dv);
+            }
+            /* token t (0-based) maps S_t -> S_{t+1}; o_t reads S_{t+1} */
+            for (int64_t t = t1 - 1; t >= t0; --t) {
+                const double *Sprev = blk + (t - t0) * (int64_t)ssz;
+                const double *Scur = blk + (t - t0 + 1) * (int64_t)ssz;
+                const float *qt = qh + t * dk, *kt = kh + t * dk, *at = ah + t * dk;
+                const float *vt = vh + t * dv, *dot = doh + t * dv;
+                double *gq = grad_q + (bh * T + t) * dk, *gk = grad_k + (bh * T + t) * dk;
+                double *ga = grad_log_alpha + (bh * T + t) * dk, *gv = grad_v + (bh * T + t) * dv;
+                /* o_t = scale q_t S_{t+1}: add its share to the adjoint of S_{t+1} */
+                for (int d = 0; d < dk; ++d) {
+                    const double sq = scale * (double)qt[d];
+                    double *row = G + (int64_t)d * dv;
+                    for (int c = 0; c < dv; ++c) row[c] += sq * (double)dot[c];
+                }
+                for (int d = 0; d < dk; ++d) {
+                    const double *srow = Scur + (int64_t)d * dv, *grow = G + (int64_t)d * dv;
+                    const double *prow = Sprev + (int64_t)d * dv;
+                    double aq = 0.0, ak = 0.0, aa = 0.0;
+                    for (int c = 0; c < dv; ++c) {
+                        aq += srow[c] * (double)dot[c];
+                        ak += grow[c] * (double)vt[c];
+                        aa += grow[c] * prow[c];
+                    }
+                    gq[d] = scale * aq;
+                    gk[d] = ak;
+                    ga[d] = exp((double)at[d]) * aa;
+                }
+                for (int c = 0; c < dv; ++c) {
+                    double acc = 0.0;
+                    for (int d = 0; d < dk; ++d) acc += (double)kt[d] * G[(int64_t)d * dv + c];
+                    gv[c] = acc;
+                }
+                /* S_{t+1} = diag(alpha_t) S_t + ...: pass the adjoint back to S_t */
+                for (int d = 0; d < dk; ++d) {
+                    const double alpha = exp((double)at[d]);
+                    double *row = G + (int64_t)d * dv;
+                    for (int c = 0; c < dv; ++c) row[c] *= alpha;
+                }
+            }
+        }
+        if (grad_h0) memcpy(grad_h0 + bh * (int64_t)ssz, G, sizeof(double) * ssz);
+        free(cp); free(blk); free(G);
+    }
+    return failed ? -1 : 0;
+}

@@ -50,6 +50,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.gla_oracle_step.argtypes = [f, f, f, f, ctypes.c_double, d, d, ctypes.c_int64,
                                     ctypes.c_int, ctypes.c_int, ctypes.c_int]
     lib.gla_oracle_step.restype = None
+    i64 = ctypes.c_int64
+    lib.gla_oracle_backward.argtypes = [f, f, f, f, ctypes.c_double, d, f, d, d, d, d, d, d, i64,
+                                        i64, ctypes.c_int, ctypes.c_int, i64, ctypes.c_int]
+    lib.gla_oracle_backward.restype = ctypes.c_int
     lib.gla_oracle_max_threads.argtypes = []
     lib.gla_oracle_max_threads.restype = ctypes.c_int
     return lib
@@ -122,6 +126,48 @@ def step(q, k, v, log_alpha, scale: float, h: np.ndarray, *, nthreads: int = 0, 
                         _ptr(a, ctypes.c_float), float(scale), _ptr(h, ctypes.c_double),
                         _ptr(o, ctypes.c_double), BH, dk, dv, int(nthreads))
     return o
+
+
+def backward(q, k, v, log_alpha, scale: float, d_o, h0=None, dhT=None, *, ck: int = 0,
+             nthreads: int = 0, lib=None):
+    """Gradients of L = sum_t <d_o_t, o_t> + <dhT, hT> through the recurrence.
+
+    Shapes as in ``forward``; d_o: [..., T, dv]; h0, dhT: [..., dk, dv] or None
+    (zero).  ``ck`` is the checkpoint spacing of the state replay (0 = about
+    sqrt(T)); it changes memory use only.  Returns float64
+    (dq, dk, dv, dlog_alpha, dh0), each shaped like its input.
+    """
+    lib = lib or load()
+    q, k, v, a, g = _f32(q), _f32(k), _f32(v), _f32(log_alpha), _f32(d_o)
+    lead = q.shape[:-2]
+    T, dk = q.shape[-2], q.shape[-1]
+    dv = v.shape[-1]
+    assert k.shape == q.shape and a.shape == q.shape and v.shape == lead + (T, dv)
+    assert g.shape == v.shape
+    BH = int(np.prod(lead, dtype=np.int64)) if lead else 1
+
+    def state(x):
+        if x is None:
+            return None, None
+        xa = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+        assert xa.shape == lead + (dk, dv)
+        return xa, _ptr(xa, ctypes.c_double)
+
+    h0a, h0p = state(h0)
+    dhTa, dhTp = state(dhT)
+    dq = np.empty(q.shape, dtype=np.float64)
+    dkk = np.empty(q.shape, dtype=np.float64)
+    dvv = np.empty(v.shape, dtype=np.float64)
+    da = np.empty(q.shape, dtype=np.float64)
+    dh0 = np.empty(lead + (dk, dv), dtype=np.float64)
+    dp = lambda x: _ptr(x, ctypes.c_double)  # noqa: E731
+    rc = lib.gla_oracle_backward(_ptr(q, ctypes.c_float), _ptr(k, ctypes.c_float),
+                                 _ptr(v, ctypes.c_float), _ptr(a, ctypes.c_float), float(scale),
+                                 h0p, _ptr(g, ctypes.c_float), dhTp, dp(dq), dp(dkk), dp(dvv),
+                                 dp(da), dp(dh0), BH, T, dk, dv, int(ck), int(nthreads))
+    if rc != 0:
+        raise MemoryError("oracle could not allocate its state buffers")
+    return dq, dkk, dvv, da, dh0
 
 
 def forward_torch(q, k, v, log_alpha, scale: float, h0=None, *, nthreads: int = 0):
