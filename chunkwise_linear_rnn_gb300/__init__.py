@@ -23,8 +23,10 @@ import torch
 from . import _lib
 from ._lib import GlaChunkOptions, GlaError, status_string  # noqa: F401
 
-__all__ = ["gla_chunk_fwd", "gla_chunk_fwd_varlen", "gla_chunk_fwd_varlen_plan", "gla_chunk_fwd_plan", "gla_recurrent_step", "gla_last_device_status", "GlaError",
-           "status_string", "library_path"]
+__all__ = ["gla_chunk_fwd", "gla_chunk_fwd_varlen", "gla_chunk_fwd_varlen_plan",
+           "gla_chunk_fwd_plan", "gla_chunk_bwd", "gla_chunk_bwd_plan", "gla_chunk",
+           "gla_recurrent_step", "gla_last_device_status", "GlaError", "status_string",
+           "library_path"]
 
 library_path = _lib.LIB_PATH
 
@@ -241,6 +243,92 @@ def gla_chunk_fwd_plan(B: int, H: int, T: int, dk: int, dv: int, *, segments: in
     _lib.check(st, "gla_chunk_fwd_plan")
     return {"segments": nseg.value, "dv_tile": tile.value, "launches": launches.value,
             "scratch_bytes": scratch.value}
+
+
+def gla_chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: torch.Tensor,
+                  d_o: torch.Tensor, scale: float | None = None, h0: torch.Tensor | None = None,
+                  dhT: torch.Tensor | None = None, *, need_dh0: bool = True,
+                  force_exact: bool = False):
+    """Gradients of L = sum <d_o, o> + <dhT, hT> through the chunked forward.
+
+    Inputs as for ``gla_chunk_fwd`` (per-channel gates ``[B,H,T,dk]``), with
+    ``d_o`` ``[B,H,T,dv]`` bf16 and ``dhT`` ``[B,H,dk,dv]`` fp32 or None (zero).
+    Returns ``(dq, dk, dv, dlog_alpha, dh0)``: bf16, bf16, bf16, fp32, and fp32
+    or None when ``need_dh0`` is False.  The states are recomputed on the GPU.
+    """
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, T, dk]")
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("q must be on a CUDA device")
+    _need(q, "q", torch.bfloat16, (B, H, T, dk), dev)
+    _need(k, "k", torch.bfloat16, (B, H, T, dk), dev)
+    _need(v, "v", torch.bfloat16, (B, H, T, dv), dev)
+    _need(log_alpha, "log_alpha", torch.float32, (B, H, T, dk), dev)
+    _need(d_o, "d_o", torch.bfloat16, (B, H, T, dv), dev)
+    if h0 is not None:
+        _need(h0, "h0", torch.float32, (B, H, dk, dv), dev)
+    if dhT is not None:
+        _need(dhT, "dhT", torch.float32, (B, H, dk, dv), dev)
+    if scale is None:
+        scale = dk ** -0.5
+    dq = torch.empty_like(q)
+    dkk = torch.empty_like(k)
+    dvv = torch.empty_like(v)
+    da = torch.empty_like(log_alpha)
+    dh0 = torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev) if need_dh0 else None
+    opts = GlaChunkOptions(force_exact=1 if force_exact else 0)
+    ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+    with torch.cuda.device(dev):
+        st = _lib.lib().gla_chunk_bwd_ex(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), log_alpha.data_ptr(), float(scale),
+            ptr(h0), d_o.data_ptr(), ptr(dhT), dq.data_ptr(), dkk.data_ptr(), dvv.data_ptr(),
+            da.data_ptr(), ptr(dh0), B, H, T, dk, dv, ctypes.byref(opts), _stream(dev))
+    _lib.check(st, "gla_chunk_bwd")
+    return dq, dkk, dvv, da, dh0
+
+
+def gla_chunk_bwd_plan(B: int, H: int, T: int, dk: int, dv: int) -> dict:
+    """Chunk length, launches and scratch bytes of gla_chunk_bwd for a shape (no GPU work)."""
+    chunk, launches, scratch = ctypes.c_int(), ctypes.c_int(), ctypes.c_ulong()
+    st = _lib.lib().gla_chunk_bwd_plan(B, H, T, dk, dv, ctypes.byref(chunk),
+                                       ctypes.byref(launches), ctypes.byref(scratch))
+    _lib.check(st, "gla_chunk_bwd_plan")
+    return {"chunk": chunk.value, "launches": launches.value, "scratch_bytes": scratch.value}
+
+
+class _GlaChunk(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, log_alpha, h0, scale):
+        o, hT = gla_chunk_fwd(q, k, v, log_alpha, scale, h0)
+        ctx.save_for_backward(q, k, v, log_alpha, h0)
+        ctx.scale = scale
+        return o, hT
+
+    @staticmethod
+    def backward(ctx, d_o, dhT):
+        q, k, v, log_alpha, h0 = ctx.saved_tensors
+        if d_o is None:
+            d_o = torch.zeros(*q.shape[:-1], v.shape[-1], dtype=torch.bfloat16, device=q.device)
+        d_o = d_o.to(torch.bfloat16).contiguous()
+        dhT = None if dhT is None else dhT.float().contiguous()
+        dq, dk, dv, da, dh0 = gla_chunk_bwd(q, k, v, log_alpha, d_o, ctx.scale, h0, dhT,
+                                            need_dh0=h0 is not None and ctx.needs_input_grad[4])
+        return dq, dk, dv, da, dh0, None
+
+
+def gla_chunk(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: torch.Tensor,
+              scale: float | None = None, h0: torch.Tensor | None = None):
+    """Differentiable chunked GLA: ``(o, hT)`` with gradients through ``gla_chunk_bwd``.
+
+    Per-channel gates ``[B,H,T,dk]`` only.  The backward recomputes the states
+    from the saved inputs; ``d_o`` is taken in bf16, ``dhT`` in fp32.
+    """
+    if scale is None:
+        scale = q.shape[-1] ** -0.5
+    return _GlaChunk.apply(q, k, v, log_alpha, h0, float(scale))
 
 
 def gla_recurrent_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: torch.Tensor,

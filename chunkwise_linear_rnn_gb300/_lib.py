@@ -68,6 +68,13 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.gla_chunk_fwd_plan.argtypes = [i, i, i, i, i, ctypes.POINTER(GlaChunkOptions), ip, ip, ip,
                                        ctypes.POINTER(ctypes.c_ulong)]
     lib.gla_chunk_fwd_plan.restype = i
+    bwd = [vp, vp, vp, fp, f, fp, vp, fp, vp, vp, vp, fp, fp, i, i, i, i, i]
+    lib.gla_chunk_bwd.argtypes = bwd + [vp]
+    lib.gla_chunk_bwd.restype = i
+    lib.gla_chunk_bwd_ex.argtypes = bwd + [ctypes.POINTER(GlaChunkOptions), vp]
+    lib.gla_chunk_bwd_ex.restype = i
+    lib.gla_chunk_bwd_plan.argtypes = [i, i, i, i, i, ip, ip, ctypes.POINTER(ctypes.c_ulong)]
+    lib.gla_chunk_bwd_plan.restype = i
     lib.gla_recurrent_step.argtypes = [vp, vp, vp, fp, f, fp, vp, i, i, i, i, vp]
     lib.gla_recurrent_step.restype = i
     lib.gla_status_string.argtypes = [i]

@@ -613,6 +613,115 @@ int gla_recurrent_step(const void *q, const void *k, const void *v, const float 
     return launch_recurrent_step(p, stream) == 0 ? GLA_OK : GLA_ERR_LAUNCH;
 }
 
+namespace {
+
+// Scratch of the chunkwise backward, in bytes: chunk-start states, state
+// gradients and per-tile log-gate carries, each 256-byte aligned.
+bool bwd_layout(int B, int H, int T, int dk, int dv, size_t *states, size_t *adjoints,
+                size_t *carry) {
+    const long long BH = static_cast<long long>(B) * H;
+    const long long NC = (static_cast<long long>(T) + gla::bwd_chunk_tokens() - 1) /
+                         gla::bwd_chunk_tokens();
+    const auto al = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    *states = al(sizeof(float) * static_cast<size_t>(BH) * (NC + 1) * dk * dv);
+    *adjoints = al(sizeof(float) * static_cast<size_t>(BH) * NC * dk * dv);
+    *carry = al(sizeof(float) * static_cast<size_t>(BH) * NC * gla::bwd_value_tiles(dv) * dk);
+    return NC <= 0x7fffffffLL;
+}
+
+int bwd_shape_ok(int B, int H, int T, int dk, int dv) {
+    if (B <= 0 || H <= 0 || T <= 0) return GLA_ERR_ARG;
+    if (static_cast<long long>(B) * H > 65535) return GLA_ERR_ARG;
+    if (!gla::dk_ok(dk) || !gla::dv_ok(dv)) return GLA_ERR_SHAPE;
+    return GLA_OK;
+}
+
+bool misaligned(const void *p, uintptr_t bytes) {
+    return (reinterpret_cast<uintptr_t>(p) & (bytes - 1)) != 0;
+}
+
+}  // namespace
+
+int gla_chunk_bwd_plan(int B, int H, int T, int dk, int dv, int *chunk, int *launches,
+                       unsigned long *scratch_bytes) {
+    const int st = bwd_shape_ok(B, H, T, dk, dv);
+    if (st != GLA_OK) return st;
+    size_t a = 0, b = 0, c = 0;
+    if (!bwd_layout(B, H, T, dk, dv, &a, &b, &c)) return GLA_ERR_ARG;
+    if (chunk) *chunk = gla::bwd_chunk_tokens();
+    if (launches) *launches = 3;
+    if (scratch_bytes) *scratch_bytes = static_cast<unsigned long>(a + b + c);
+    return GLA_OK;
+}
+
+int gla_chunk_bwd_ex(const void *q, const void *k, const void *v, const float *log_alpha,
+                     float scale, const float *h0, const void *d_o, const float *dhT,
+                     void *grad_q, void *grad_k, void *grad_v, float *grad_log_alpha,
+                     float *grad_h0, int B, int H, int T, int dk, int dv,
+                     const gla_chunk_options *opts, cudaStream_t stream) {
+    using namespace gla;
+    if (!q || !k || !v || !log_alpha || !d_o || !grad_q || !grad_k || !grad_v ||
+        !grad_log_alpha)
+        return GLA_ERR_ARG;
+    const int shape = bwd_shape_ok(B, H, T, dk, dv);
+    if (shape != GLA_OK) return shape;
+    if (misaligned(q, 2) || misaligned(k, 2) || misaligned(v, 2) || misaligned(d_o, 2) ||
+        misaligned(grad_q, 2) || misaligned(grad_k, 2) || misaligned(grad_v, 2) ||
+        misaligned(log_alpha, 4) || misaligned(grad_log_alpha, 4) ||
+        (h0 && misaligned(h0, 4)) || (dhT && misaligned(dhT, 4)) ||
+        (grad_h0 && misaligned(grad_h0, 4)))
+        return GLA_ERR_ARG;
+    gla_chunk_options o_def = {};
+    const gla_chunk_options &op = opts ? *opts : o_def;
+    if (op.gate_per_head != 0 || (op.force_exact != 0 && op.force_exact != 1)) return GLA_ERR_ARG;
+    size_t st_b = 0, adj_b = 0, car_b = 0;
+    if (!bwd_layout(B, H, T, dk, dv, &st_b, &adj_b, &car_b)) return GLA_ERR_ARG;
+
+    DeviceInfo *dev = nullptr;
+    const int st = current_device(&dev);
+    if (st != GLA_OK) return st;
+    char *ws = nullptr;
+    if (cudaMallocAsync(reinterpret_cast<void **>(&ws), st_b + adj_b + car_b, stream) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return GLA_ERR_ALLOC;
+    }
+    BwdLaunch p = {};
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.k = static_cast<const __nv_bfloat16 *>(k);
+    p.v = static_cast<const __nv_bfloat16 *>(v);
+    p.d_o = static_cast<const __nv_bfloat16 *>(d_o);
+    p.log_alpha = log_alpha;
+    p.h0 = h0;
+    p.dhT = dhT;
+    p.gq = static_cast<__nv_bfloat16 *>(grad_q);
+    p.gk = static_cast<__nv_bfloat16 *>(grad_k);
+    p.gv = static_cast<__nv_bfloat16 *>(grad_v);
+    p.ga = grad_log_alpha;
+    p.gh0 = grad_h0;
+    p.states = reinterpret_cast<float *>(ws);
+    p.adjoints = reinterpret_cast<float *>(ws + st_b);
+    p.carry = reinterpret_cast<float *>(ws + st_b + adj_b);
+    p.scale = scale;
+    p.BH = B * H;
+    p.T = T;
+    p.NC = (T + bwd_chunk_tokens() - 1) / bwd_chunk_tokens();
+    p.dk = dk;
+    p.dv = dv;
+    p.force_exact = op.force_exact;
+    const int r = launch_chunk_bwd(p, stream) == 0 ? GLA_OK : GLA_ERR_LAUNCH;
+    cudaFreeAsync(ws, stream);
+    return r;
+}
+
+int gla_chunk_bwd(const void *q, const void *k, const void *v, const float *log_alpha,
+                  float scale, const float *h0, const void *d_o, const float *dhT,
+                  void *grad_q, void *grad_k, void *grad_v, float *grad_log_alpha,
+                  float *grad_h0, int B, int H, int T, int dk, int dv, cudaStream_t stream) {
+    return gla_chunk_bwd_ex(q, k, v, log_alpha, scale, h0, d_o, dhT, grad_q, grad_k, grad_v,
+                            grad_log_alpha, grad_h0, B, H, T, dk, dv, nullptr, stream);
+}
+
 int gla_last_device_status(cudaStream_t stream) {
     using namespace gla;
     DeviceInfo *dev = nullptr;

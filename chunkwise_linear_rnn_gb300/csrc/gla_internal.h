@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -81,5 +82,28 @@ struct DecodeLaunch {
 };
 
 int launch_recurrent_step(const DecodeLaunch &p, cudaStream_t stream);
+
+// The chunkwise backward (gla_backward.cu).
+struct BwdLaunch {
+    const __nv_bfloat16 *q, *k, *v, *d_o;   // [BH, T, dk] / [BH, T, dv]
+    const float *log_alpha;                  // [BH, T, dk]
+    const float *h0, *dhT;                   // [BH, dk, dv] or null (zero)
+    __nv_bfloat16 *gq, *gk, *gv;             // gradients of q, k, v
+    float *ga;                               // gradient of log_alpha [BH, T, dk]
+    float *gh0;                              // gradient of h0 [BH, dk, dv] or null
+    float *states;                           // scratch [BH, NC + 1, dk, dv]
+    float *adjoints;                         // scratch [BH, NC, dk, dv]
+    float *carry;                            // scratch [BH, NC, dv / 32, dk]
+    float scale;
+    int BH, T, NC, dk, dv;
+    int force_exact;
+};
+
+// Tokens per backward chunk, and value-column tiles of the state passes.
+int bwd_chunk_tokens();
+int bwd_value_tiles(int dv);
+
+// Enqueues the three backward kernels; returns a cudaError_t value.
+int launch_chunk_bwd(const BwdLaunch &p, cudaStream_t stream);
 
 }  // namespace gla

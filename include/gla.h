@@ -250,6 +250,62 @@ int gla_recurrent_step(const void *q, const void *k, const void *v, const float 
                        float scale, float *h, void *o, int B, int H, int dk, int dv,
                        cudaStream_t stream);
 
+/*
+ * gla_chunk_bwd — gradients of the chunked forward, for training.
+ *
+ * With the forward above (same q, k, v, log_alpha, scale, h0) and the loss
+ * L = sum_t <d_o_t, o_t> + <dhT, hT>, writes
+ *     grad_q, grad_k    bf16 [B, H, T, dk]    dL/dq, dL/dk
+ *     grad_v            bf16 [B, H, T, dv]    dL/dv
+ *     grad_log_alpha    fp32 [B, H, T, dk]    dL/dlog_alpha
+ *     grad_h0           fp32 [B, H, dk, dv]   dL/dh0 (nullable: not written)
+ * from d_o (bf16 [B, H, T, dv], the gradient of o) and dhT (fp32
+ * [B, H, dk, dv], the gradient of hT; NULL = zero).  h0 NULL = zero state.
+ * No output may alias an input.
+ *
+ * The states are recomputed from the inputs (no forward activations are
+ * needed): one pass over the chunks forward for the chunk-start states, one
+ * backward for the state gradients, then every chunk's gradients
+ * independently.  Source: the recurrence and chunk equations of the page
+ * named above (sections "The Gated Recurrent Update", "Cumulative Decay
+ * Representation", "Intra-Chunk Matrix Multiplications", "Inter-Chunk
+ * Recurrence and Output Projection"), differentiated; the page notes that
+ * the chunkwise form keeps its states for the backward pass.
+ *
+ * Scratch: (2 NC + 1) * B * H * dk * dv fp32 plus the log-gate carries, NC =
+ * ceil(T / 64), taken stream-ordered (cudaMallocAsync) and released on
+ * `stream` (GLA_ERR_ALLOC when the pool cannot supply it).
+ *
+ * Shapes as for gla_chunk_fwd, with B * H <= 65535.  Pointers need only their
+ * element alignment.  Accuracy: each gradient matches the fp64 reverse-mode
+ * differentiation of the recurrence to relative L2 error <= 1e-2 and max-abs
+ * error <= 2e-2 * RMS(reference).
+ */
+int gla_chunk_bwd(const void *q, const void *k, const void *v, const float *log_alpha,
+                  float scale, const float *h0, const void *d_o, const float *dhT,
+                  void *grad_q, void *grad_k, void *grad_v, float *grad_log_alpha,
+                  float *grad_h0, int B, int H, int T, int dk, int dv, cudaStream_t stream);
+
+/*
+ * gla_chunk_bwd with options: only `force_exact` applies (every chunk takes
+ * each in-chunk decay factor as its own exponential, the path chunks whose
+ * decay spans more than 2^120 always take); `gate_per_head` must be 0; the
+ * other fields are ignored.  opts NULL = defaults.
+ */
+int gla_chunk_bwd_ex(const void *q, const void *k, const void *v, const float *log_alpha,
+                     float scale, const float *h0, const void *d_o, const float *dhT,
+                     void *grad_q, void *grad_k, void *grad_v, float *grad_log_alpha,
+                     float *grad_h0, int B, int H, int T, int dk, int dv,
+                     const gla_chunk_options *opts, cudaStream_t stream);
+
+/*
+ * The launch plan gla_chunk_bwd uses for a shape (host only, no GPU work):
+ * tokens per chunk, kernel launches per call and scratch bytes.  Any output
+ * pointer may be NULL.  Returns GLA_OK, GLA_ERR_ARG or GLA_ERR_SHAPE.
+ */
+int gla_chunk_bwd_plan(int B, int H, int T, int dk, int dv, int *chunk, int *launches,
+                       unsigned long *scratch_bytes);
+
 /* Static text for a status code (never NULL). */
 const char *gla_status_string(int status);
 

@@ -2,8 +2,8 @@
 
 This package holds only the random-number recipes that both the fp64 CPU
 oracle (``oracle/``) and the CUDA path are fed with.  It contains none of the
-method's arithmetic: it draws q, k, v, the log forget gates and the initial
-state, nothing else.
+method's arithmetic: it draws q, k, v, the log forget gates, the initial
+state and the upstream gradients of a backward call, nothing else.
 """
 
 from .gla_inputs import (  # noqa: F401
@@ -11,6 +11,7 @@ from .gla_inputs import (  # noqa: F401
     DECODE_CONFIG,
     ChunkConfig,
     DecodeConfig,
+    make_backward_grads,
     make_chunk_inputs,
     make_config_inputs,
     make_decode_inputs,

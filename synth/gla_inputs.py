@@ -13,6 +13,11 @@ Recipe (the same for every workload, only sizes and spreads differ):
 Layouts are head-first and contiguous: q, k, log_alpha ``[B, H, T, dk]``,
 v ``[B, H, T, dv]``, h0 ``[B, H, dk, dv]`` (row index = key channel).
 
+The backward of a chunked workload also draws the upstream gradients, from a
+second generator seeded with ``seed + 1``: d_o ~ N(0, 1) in bf16
+``[B, H, T, dv]``, then dhT ~ N(0, sigma_dhT^2) in fp32 ``[B, H, dk, dv]``
+when the final state has a gradient.
+
 For the decode workload the per-step tensors carry a leading step axis:
 ``[steps, B, H, dk]`` etc., and h0 is drawn before them.
 """
@@ -108,6 +113,17 @@ def make_chunk_inputs(B: int, H: int, T: int, dk: int, dv: int, *, sigma_z: floa
 def make_config_inputs(cfg: ChunkConfig, seed: int = 0, device="cpu"):
     return make_chunk_inputs(cfg.B, cfg.H, cfg.T, cfg.dk, cfg.dv, sigma_z=cfg.sigma_z,
                              tau=cfg.tau, sigma_h0=cfg.sigma_h0, seed=seed, device=device)
+
+
+def make_backward_grads(B: int, H: int, T: int, dk: int, dv: int, *,
+                        sigma_dhT: float | None = None, seed: int = 0, device="cpu"):
+    """Draw the upstream gradients (d_o bf16, dhT fp32 or None) of one backward call."""
+    g = _gen(seed + 1, device)
+    d_o = torch.randn(B, H, T, dv, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+    dhT = None
+    if sigma_dhT is not None:
+        dhT = torch.randn(B, H, dk, dv, generator=g, device=device, dtype=torch.float32).mul_(sigma_dhT)
+    return d_o, dhT
 
 
 def make_decode_inputs(B: int, H: int, dk: int, dv: int, steps: int, *, sigma_z: float = 1.0,
