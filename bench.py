@@ -32,6 +32,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "GLA chunk-fwd tokens/s (B·H·T) and % roofline; decode steps/s and HBM GB/s"
+BWD_METRIC = "GLA chunk-bwd tokens/s (B·H·T): gradients of q, k, v, log_alpha and h0"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -92,6 +93,15 @@ def chunk_bytes(cfg, n_states: int | None = None, gate_per_head: bool = False) -
         n_states = cfg.B * cfg.H
     state = n_states * cfg.dk * cfg.dv * 4 * (2 if cfg.sigma_h0 is not None else 1)
     return cfg.tokens * per_token + state
+
+
+def bwd_bytes(cfg) -> int:
+    """Algorithmic bytes of one backward call: q, k, v, log alpha, d_o, h0 and dhT read
+    once; dq, dk, dv, dlog alpha and dh0 written once."""
+    per_token = 2 * cfg.dk * 2 + cfg.dv * 2 + cfg.dk * 4 + cfg.dv * 2 \
+        + 2 * cfg.dk * 2 + cfg.dv * 2 + cfg.dk * 4
+    states = 3 * cfg.B * cfg.H * cfg.dk * cfg.dv * 4
+    return cfg.tokens * per_token + states
 
 
 def packed_lengths(total: int, n: int, seed: int) -> list:
@@ -241,6 +251,8 @@ def run_ours(args, rank, world, local_rank):
     pk, pk_kind = peaks()
     cfg = chunk_config(args)
     line = None
+    if args.only == "bwd":
+        return bwd_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_kind)
     if args.only != "decode":
         line = chunk_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_kind)
     else:
@@ -411,6 +423,102 @@ def chunk_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_
     return line
 
 
+def bwd_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_kind):
+    """The chunkwise backward (gla_chunk_bwd) on the workload, its own JSON line."""
+    import torch
+    from synth import make_backward_grads, make_config_inputs
+    stream = torch.cuda.current_stream(dev)
+    q, k, v, a, h0 = make_config_inputs(cfg, seed=rank, device=dev)
+    d_o, dhT = make_backward_grads(cfg.B, cfg.H, cfg.T, cfg.dk, cfg.dv,
+                                   sigma_dhT=0.1 if h0 is not None else None, seed=rank,
+                                   device=dev)
+    plan = gla.gla_chunk_bwd_plan(cfg.B, cfg.H, cfg.T, cfg.dk, cfg.dv)
+
+    def step():
+        return gla.gla_chunk_bwd(q, k, v, a, d_o, cfg.scale, h0, dhT)
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    with ClockSampler(dev.index) as clk:
+        barrier()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for s0, e0 in ev:
+            s0.record(stream)
+            step()
+            e0.record(stream)
+        t_end.record(stream)
+        barrier()
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end))
+    per_call_ms = statistics.mean(s0.elapsed_time(e0) for s0, e0 in ev)
+    ms_per_step = total_ms / args.steps
+    tokens_all = cfg.tokens * world
+    byts = bwd_bytes(cfg)
+    achieved = byts / (per_call_ms / 1e3) / 1e9
+
+    # end to end: pinned host inputs copied in and gradients copied out every call
+    e2e = None
+    if not args.no_e2e:
+        host_in = [t.cpu().pin_memory() for t in (q, k, v, a, d_o, h0, dhT) if t is not None]
+        dev_in = [torch.empty_like(t, device=dev) for t in host_in]
+        outs = step()
+        host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
+        st = 3 if h0 is not None else None
+
+        def e2e_step():
+            for hsrc, dst in zip(host_in, dev_in):
+                dst.copy_(hsrc, non_blocking=True)
+            di = dev_in
+            res = gla.gla_chunk_bwd(di[0], di[1], di[2], di[3], di[4], cfg.scale,
+                                    di[5] if st else None, di[6] if st else None)
+            for src, hdst in zip(res, host_out):
+                hdst.copy_(src, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        x0 = torch.cuda.Event(enable_timing=True)
+        x1 = torch.cuda.Event(enable_timing=True)
+        n_e2e = max(2, min(args.steps, 5))
+        x0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        x1.record(stream)
+        barrier()
+        e2e_ms = max_over_ranks(x0.elapsed_time(x1)) / n_e2e
+        e2e = {"value": tokens_all / (e2e_ms / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in host_in)),
+               "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in host_out)),
+               "ms_per_step": e2e_ms, "api": "gla_chunk_bwd with pinned-host copies"}
+        del host_in, dev_in, host_out, outs
+    del q, k, v, a, h0, d_o, dhT
+    torch.cuda.empty_cache()
+    line = {
+        "metric": BWD_METRIC,
+        "value": tokens_all / (ms_per_step / 1e3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": cfg.name + "-backward", "B": cfg.B, "H": cfg.H, "T": cfg.T,
+                   "dk": cfg.dk, "dv": cfg.dv, "chunk": plan["chunk"], "replicas": world,
+                   "l2": "inputs (%.2f GB) larger than L2; no flush" % (byts / 1e9)},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / pk["hbm_gbs"], "traffic": None,
+                     "peak_kind": pk_kind, "kernel": "gla_chunk_bwd (whole call, %d launches)"
+                     % plan["launches"], "algorithmic_bytes_per_launch": byts,
+                     "scratch_bytes": plan["scratch_bytes"]},
+        "gpu_launches": plan["launches"] * args.steps,
+        "clocks": clk.summary(),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    return line
+
+
 def decode_leg(args, world, rank, dev, gla, barrier, max_over_ranks, pk):
     """Decode steps at B=256, H=32, dk=dv=128 (secondary numbers on the same JSON line)."""
     import torch
@@ -456,10 +564,11 @@ class OracleSample:
     repeated to fill the time.
     """
 
-    def __init__(self, cfg, target_s: float, threads: int):
+    def __init__(self, cfg, target_s: float, threads: int, backward: bool = False):
         from oracle import gla_oracle
         gla_oracle.build()
         self.oracle, self.cfg, self.threads = gla_oracle, cfg, threads
+        self.backward = backward
         heads = max(1, min(cfg.B * cfg.H, threads))
         t_probe = min(cfg.T, 2048)
         probe = self._inputs(heads, t_probe)
@@ -480,12 +589,23 @@ class OracleSample:
         q, k, v, a, h0 = make_chunk_inputs(1, heads, T, c.dk, c.dv, sigma_z=c.sigma_z, tau=c.tau,
                                            sigma_h0=c.sigma_h0, seed=0)
         f = lambda t: t.float().numpy()  # noqa: E731
-        return f(q), f(k), f(v), a.numpy(), None if h0 is None else h0.double().numpy()
+        ins = [f(q), f(k), f(v), a.numpy(), None if h0 is None else h0.double().numpy()]
+        if self.backward:
+            from synth import make_backward_grads
+            d_o, dhT = make_backward_grads(1, heads, T, c.dk, c.dv,
+                                           sigma_dhT=0.1 if h0 is not None else None, seed=0)
+            ins += [f(d_o), None if dhT is None else dhT.double().numpy()]
+        return ins
 
     def _pass(self, heads, T, inputs=None):
-        q, k, v, a, h0 = inputs if inputs is not None else self._inputs(heads, T)
+        ins = inputs if inputs is not None else self._inputs(heads, T)
+        q, k, v, a, h0 = ins[:5]
         t0 = time.perf_counter()
-        self.oracle.forward(q, k, v, a, self.cfg.scale, h0, nthreads=self.threads)
+        if self.backward:
+            self.oracle.backward(q, k, v, a, self.cfg.scale, ins[5], h0, ins[6],
+                                 nthreads=self.threads)
+        else:
+            self.oracle.forward(q, k, v, a, self.cfg.scale, h0, nthreads=self.threads)
         return time.perf_counter() - t0
 
     def run(self) -> dict:
@@ -495,12 +615,13 @@ class OracleSample:
         return {"value": tokens / dt, "unit": "tokens/s", "cores": min(self.threads, self.heads),
                 "kind": "oracle",
                 "sample": f"{self.repeat} x {self.heads} heads x {self.T} tokens of {c.name} "
-                          f"(dk={c.dk}, dv={c.dv}), fp64 recurrence, {dt:.1f} s"}
+                          f"(dk={c.dk}, dv={c.dv}), fp64 recurrence"
+                          f"{' and its reverse-mode backward' if self.backward else ''}, {dt:.1f} s"}
 
 
-def oracle_sample(cfg, target_s: float, threads: int) -> dict:
+def oracle_sample(cfg, target_s: float, threads: int, backward: bool = False) -> dict:
     """Time the fp64 oracle on a bounded sample of the workload; returns a cpu_baseline dict."""
-    return OracleSample(cfg, target_s, threads).run()
+    return OracleSample(cfg, target_s, threads, backward).run()
 
 
 def host_threads() -> int:
@@ -515,7 +636,7 @@ def run_reference(args):
     cfg = chunk_config(args)
     threads = host_threads()
     per_step_s = max(0.5, min(args.ref_seconds, 150.0 / max(1, args.steps + args.warmup)))
-    sample = OracleSample(cfg, per_step_s, threads)
+    sample = OracleSample(cfg, per_step_s, threads, backward=args.only == "bwd")
     for _ in range(args.warmup):
         sample.run()
     per = [sample.run() for _ in range(args.steps)]
@@ -523,11 +644,13 @@ def run_reference(args):
     value = statistics.median(p["value"] for p in per)
     base["value"] = value
     return {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 0,
+        "impl": "reference", "metric": BWD_METRIC if args.only == "bwd" else METRIC,
+        "value": value, "unit": "tokens/s", "n_gpus": 0,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * sample.repeat * sample.heads * sample.T / value,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": cfg.name, "B": cfg.B, "H": cfg.H, "T": cfg.T,
+        "data": "synthetic", "config": {"workload": cfg.name + ("-backward" if args.only == "bwd"
+                                                                else ""), "B": cfg.B, "H": cfg.H, "T": cfg.T,
                                         "dk": cfg.dk, "dv": cfg.dv},
         "cpu_baseline": base,
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -544,8 +667,9 @@ def main():
     ap.add_argument("--workload", default="long", choices=["small", "medium", "long", "very_long"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--decode-steps", type=int, default=256)
-    ap.add_argument("--only", default="both", choices=["both", "chunk", "decode"],
-                    help="run only the chunked forward or only the decode step")
+    ap.add_argument("--only", default="both", choices=["both", "chunk", "decode", "bwd"],
+                    help="run only the chunked forward, only the decode step, or only the "
+                         "chunkwise backward (its own JSON line)")
     ap.add_argument("--no-decode", action="store_true", help="same as --only chunk")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's B")
     ap.add_argument("--heads", type=int, default=0, help="override the workload's H")
@@ -578,7 +702,7 @@ def main():
     if rank == 0:
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = oracle_sample(chunk_config(args), args.ref_seconds,
-                                                 host_threads())
+                                                 host_threads(), backward=args.only == "bwd")
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
