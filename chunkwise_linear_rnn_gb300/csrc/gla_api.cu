@@ -618,7 +618,7 @@ namespace {
 // Scratch of the chunkwise backward, in bytes: chunk-start states, state
 // gradients and per-tile log-gate carries, each 256-byte aligned.
 bool bwd_layout(int B, int H, int T, int dk, int dv, size_t *states, size_t *adjoints,
-                size_t *carry) {
+                size_t *carry, size_t *decay, size_t *partials = nullptr) {
     const long long BH = static_cast<long long>(B) * H;
     const long long NC = (static_cast<long long>(T) + gla::bwd_chunk_tokens() - 1) /
                          gla::bwd_chunk_tokens();
@@ -626,6 +626,8 @@ bool bwd_layout(int B, int H, int T, int dk, int dv, size_t *states, size_t *adj
     *states = al(sizeof(float) * static_cast<size_t>(BH) * (NC + 1) * dk * dv);
     *adjoints = al(sizeof(float) * static_cast<size_t>(BH) * NC * dk * dv);
     *carry = al(sizeof(float) * static_cast<size_t>(BH) * NC * gla::bwd_value_tiles(dv) * dk);
+    *decay = al(sizeof(float) * static_cast<size_t>(BH) * NC * dk);
+    if (partials) *partials = al(sizeof(float) * static_cast<size_t>(BH) * T * (2 * dk + dv));
     return NC <= 0x7fffffffLL;
 }
 
@@ -636,21 +638,17 @@ int bwd_shape_ok(int B, int H, int T, int dk, int dv) {
     return GLA_OK;
 }
 
-bool misaligned(const void *p, uintptr_t bytes) {
-    return (reinterpret_cast<uintptr_t>(p) & (bytes - 1)) != 0;
-}
-
 }  // namespace
 
 int gla_chunk_bwd_plan(int B, int H, int T, int dk, int dv, int *chunk, int *launches,
                        unsigned long *scratch_bytes) {
     const int st = bwd_shape_ok(B, H, T, dk, dv);
     if (st != GLA_OK) return st;
-    size_t a = 0, b = 0, c = 0;
-    if (!bwd_layout(B, H, T, dk, dv, &a, &b, &c)) return GLA_ERR_ARG;
+    size_t a = 0, b = 0, c = 0, d = 0, e = 0;
+    if (!bwd_layout(B, H, T, dk, dv, &a, &b, &c, &d, &e)) return GLA_ERR_ARG;
     if (chunk) *chunk = gla::bwd_chunk_tokens();
-    if (launches) *launches = 3;
-    if (scratch_bytes) *scratch_bytes = static_cast<unsigned long>(a + b + c);
+    if (launches) *launches = 5;
+    if (scratch_bytes) *scratch_bytes = static_cast<unsigned long>(a + b + c + d + e);
     return GLA_OK;
 }
 
@@ -665,23 +663,23 @@ int gla_chunk_bwd_ex(const void *q, const void *k, const void *v, const float *l
         return GLA_ERR_ARG;
     const int shape = bwd_shape_ok(B, H, T, dk, dv);
     if (shape != GLA_OK) return shape;
-    if (misaligned(q, 2) || misaligned(k, 2) || misaligned(v, 2) || misaligned(d_o, 2) ||
-        misaligned(grad_q, 2) || misaligned(grad_k, 2) || misaligned(grad_v, 2) ||
-        misaligned(log_alpha, 4) || misaligned(grad_log_alpha, 4) ||
-        (h0 && misaligned(h0, 4)) || (dhT && misaligned(dhT, 4)) ||
-        (grad_h0 && misaligned(grad_h0, 4)))
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(d_o) ||
+        !aligned16(grad_q) || !aligned16(grad_k) || !aligned16(grad_v) ||
+        !aligned16(log_alpha) || !aligned16(grad_log_alpha) || (h0 && !aligned16(h0)) ||
+        (dhT && !aligned16(dhT)) || (grad_h0 && !aligned16(grad_h0)))
         return GLA_ERR_ARG;
     gla_chunk_options o_def = {};
     const gla_chunk_options &op = opts ? *opts : o_def;
     if (op.gate_per_head != 0 || (op.force_exact != 0 && op.force_exact != 1)) return GLA_ERR_ARG;
-    size_t st_b = 0, adj_b = 0, car_b = 0;
-    if (!bwd_layout(B, H, T, dk, dv, &st_b, &adj_b, &car_b)) return GLA_ERR_ARG;
+    size_t st_b = 0, adj_b = 0, car_b = 0, dec_b = 0, par_b = 0;
+    if (!bwd_layout(B, H, T, dk, dv, &st_b, &adj_b, &car_b, &dec_b, &par_b)) return GLA_ERR_ARG;
 
     DeviceInfo *dev = nullptr;
     const int st = current_device(&dev);
     if (st != GLA_OK) return st;
     char *ws = nullptr;
-    if (cudaMallocAsync(reinterpret_cast<void **>(&ws), st_b + adj_b + car_b, stream) !=
+    if (cudaMallocAsync(reinterpret_cast<void **>(&ws), st_b + adj_b + car_b + dec_b + par_b,
+                        stream) !=
         cudaSuccess) {
         cudaGetLastError();
         return GLA_ERR_ALLOC;
@@ -702,6 +700,11 @@ int gla_chunk_bwd_ex(const void *q, const void *k, const void *v, const float *l
     p.states = reinterpret_cast<float *>(ws);
     p.adjoints = reinterpret_cast<float *>(ws + st_b);
     p.carry = reinterpret_cast<float *>(ws + st_b + adj_b);
+    p.decay = reinterpret_cast<float *>(ws + st_b + adj_b + car_b);
+    p.pq = reinterpret_cast<float *>(ws + st_b + adj_b + car_b + dec_b);
+    p.pk = p.pq + static_cast<size_t>(B) * H * T * dk;
+    p.pv = p.pk + static_cast<size_t>(B) * H * T * dk;
+    p.status = dev->status;
     p.scale = scale;
     p.BH = B * H;
     p.T = T;

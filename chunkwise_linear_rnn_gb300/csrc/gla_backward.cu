@@ -24,13 +24,16 @@
 // The log-gate carry is the gradient of the first token of the next chunk:
 // shifting log alpha there scales the state leaving chunk u row by row.
 //
-// Three kernels, all on CUDA cores in fp32:
-//   1. bwd_states:  one CTA per (32-column tile, head) walks the chunks
-//      forward and writes S_u for u = 0 .. NC (S_0 = h0) to scratch;
-//   2. bwd_adjoint: the same tiling walks the chunks backward, writes R_u,
-//      the per-tile row sums of R_u * S_(u+1) (the log-gate carry), and dh0;
-//   3. bwd_grads:   one CTA per (chunk, head), independent of every other
-//      chunk, computes dq, dk, dv and dlog_alpha.
+// Five launches:
+//   1. bwd_sums:  every chunk independently, on the tensor cores (tcgen05,
+//      TMEM accumulators): the state it adds from a zero start and the state
+//      gradient its outputs add, plus its total decay;
+//   2. bwd_state_scan:   S_u for u = 0 .. NC from those sums (elementwise);
+//   3. bwd_adjoint_scan: R_u, the log-gate carries rowsum(R_u * S_(u+1)), dh0;
+//   4. bwd_inter: every chunk's state terms of dq, dk, dv on the tensor cores;
+//   5. bwd_grads: one CTA per (chunk, head) adds the in-chunk terms (64 x 64
+//      score-sized products on CUDA cores in fp32) and writes dq, dk, dv and
+//      dlog_alpha.
 // Inside a chunk the decay factor e^(Gamma_t - Gamma_j) (t >= j) is split
 // around a per-channel reference r = (Gamma_0 + Gamma_(C-1)) / 2, so both
 // halves stay within 2^+-60 when the chunk's decay spans at most 2^120; a
@@ -42,6 +45,7 @@
 #include <cstdint>
 
 #include "gla_internal.h"
+#include "gla_ptx.cuh"
 
 namespace gla {
 namespace {
@@ -56,14 +60,42 @@ __device__ __forceinline__ float bf(const __nv_bfloat16 *p, size_t i) {
     return __bfloat162float(p[i]);
 }
 
+// (x, y) as a bf16 pair hi plus a bf16 pair lo, x = hi + lo to 16 significant bits.
+__device__ __forceinline__ void split_pair(float x, float y, uint32_t &hi, uint32_t &lo) {
+    hi = pack_bf16x2(x, y);
+    const float hx = __uint_as_float(hi << 16), hy = __uint_as_float(hi & 0xffff0000u);
+    lo = pack_bf16x2(x - hx, y - hy);
+}
+
+// Per-chunk states and state gradients live in scratch as [BH][dk][dv/32]
+// [slots][32]: the 32-column groups of one row, chunk after chunk, so that a
+// scan over the chunks reads and writes whole consecutive lines.
+template <int DK, int DV>
+__device__ __forceinline__ size_t slot_index(int bh, int i, int c, int u, int slots) {
+    return ((static_cast<size_t>(bh) * DK + i) * (DV / 32) + (c >> 5)) * slots * 32 +
+           static_cast<size_t>(u) * 32 + (c & 31);
+}
+
 // Load one chunk of log-gates (log2 units, rows past the sequence end zero,
 // so the prefix sum stays flat there) and take the inclusive prefix sum per
-// channel.  sG is [BC][LD].
-template <int DK, int LD>
+// channel.  sG is [BC][LD].  All loads are issued before the first use.
+template <int DK, int LD, int NTH = NT>
 __device__ __forceinline__ void load_prefix(float *sG, const float *__restrict__ la, int n) {
-    for (int e = threadIdx.x; e < BC * DK; e += NT) {
-        const int t = e / DK, i = e % DK;
-        sG[t * LD + i] = t < n ? la[static_cast<size_t>(t) * DK + i] * kLog2e : 0.f;
+    constexpr int PER = BC * DK / 4 / NTH;
+    float4 r[PER];
+#pragma unroll
+    for (int m = 0; m < PER; ++m) {
+        const int e = (threadIdx.x + m * NTH) * 4, t = e / DK;
+        r[m] = t < n ? *reinterpret_cast<const float4 *>(la + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int m = 0; m < PER; ++m) {
+        const int e = (threadIdx.x + m * NTH) * 4, t = e / DK, i = e % DK;
+        float *d = sG + t * LD + i;
+        d[0] = r[m].x * kLog2e;
+        d[1] = r[m].y * kLog2e;
+        d[2] = r[m].z * kLog2e;
+        d[3] = r[m].w * kLog2e;
     }
     __syncthreads();
     if (threadIdx.x < DK) {
@@ -77,119 +109,411 @@ __device__ __forceinline__ void load_prefix(float *sG, const float *__restrict__
 }
 
 // ---------------------------------------------------------------------------
-// 1. chunk-start states.  Thread (warp w, lane c) owns column c of the tile and
-//    rows w, w + 8, w + 16, ...
+// 1. chunk sums on the tensor cores.  CTA (u, bh, which): which = 0 gives the
+//    state a chunk adds from a zero start, dS_u = (K e^(Gamma_C - Gamma))^T V;
+//    which = 1 the state gradient its outputs add, dR_u = scale (Q e^Gamma)^T dO.
+//    M = 128 key channels (zero rows past dk), N = dv, K = the chunk's tokens.
+//    The key-side operand is split into a bf16 pair (hi + lo, 16 significant
+//    bits) because these sums accumulate over the whole sequence; V and dO
+//    are bf16 inputs, exact.  Operand tiles are 128-byte swizzled, 64
+//    channels (or value columns) per block, read MN-major.
 template <int DK, int DV>
-__global__ void __launch_bounds__(NT) bwd_states_kernel(BwdLaunch p) {
-    constexpr int RPT = DK / 8;
-    extern __shared__ float smem[];
-    float *sG = smem;                  // [BC][DK]
-    float *sK = sG + BC * DK;          // [BC][DK]: k e^(Gamma_C - Gamma)
-    float *sV = sK + BC * DK;          // [BC][TW]
-    const int tile = blockIdx.x, bh = blockIdx.y;
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int c0 = tile * TW;
-    const size_t base_k = static_cast<size_t>(bh) * p.T * DK;
-    const size_t base_v = static_cast<size_t>(bh) * p.T * DV;
-    float *Sout = p.states + static_cast<size_t>(bh) * (p.NC + 1) * DK * DV;
+struct SumSmem {
+    static constexpr uint32_t kBlk = BC * 128;              // one 64-column block of a tile
+    static constexpr uint32_t kA = 0;                       // A hi: two blocks (128 channels)
+    static constexpr uint32_t kAlo = kA + 2 * kBlk;
+    static constexpr uint32_t kB = kAlo + 2 * kBlk;         // B: DV / 64 blocks
+    static constexpr uint32_t kG = kB + (DV / 64) * kBlk;   // fp32 prefix sums [BC][DK]
+    static constexpr uint32_t kBar = kG + BC * DK * 4;
+    static constexpr uint32_t kSlot = kBar + 8;
+    static constexpr uint32_t kBytes = kSlot + 8 + 1024;    // + alignment slack
+};
 
-    float S[RPT];
-#pragma unroll
-    for (int m = 0; m < RPT; ++m)
-        S[m] = p.h0 ? p.h0[(static_cast<size_t>(bh) * DK + w + 8 * m) * DV + c0 + lane] : 0.f;
+template <int DK, int DV>
+__global__ void __launch_bounds__(128, 1) bwd_sums_kernel(BwdLaunch p) {
+    using L = SumSmem<DK, DV>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *sA = sm + L::kA, *sAlo = sm + L::kAlo, *sB = sm + L::kB;
+    float *sG = reinterpret_cast<float *>(sm + L::kG);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::kBar);
+    uint32_t *slot = reinterpret_cast<uint32_t *>(sm + L::kSlot);
+    const int u = blockIdx.x, bh = blockIdx.y, which = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int t0 = u * BC, n = min(BC, p.T - t0);
+    const size_t rk = (static_cast<size_t>(bh) * p.T + t0) * DK;
+    const size_t rv = (static_cast<size_t>(bh) * p.T + t0) * DV;
 
-    for (int u = 0; u < p.NC; ++u) {
-        const int t0 = u * BC, n = min(BC, p.T - t0);
-        load_prefix<DK, DK>(sG, p.log_alpha + base_k + static_cast<size_t>(t0) * DK, n);
-        for (int e = threadIdx.x; e < BC * DK; e += NT) {
-            const int t = e / DK, i = e % DK;
-            const float kk = t < n ? bf(p.k, base_k + static_cast<size_t>(t0 + t) * DK + i) : 0.f;
-            sK[e] = kk * exp2f(sG[(BC - 1) * DK + i] - sG[e]);
-        }
-        for (int e = threadIdx.x; e < BC * TW; e += NT) {
-            const int t = e / TW, c = e % TW;
-            sV[e] = t < n ? bf(p.v, base_v + static_cast<size_t>(t0 + t) * DV + c0 + c) : 0.f;
-        }
-        __syncthreads();
-        float *dst = Sout + static_cast<size_t>(u) * DK * DV;
-#pragma unroll
-        for (int m = 0; m < RPT; ++m) {
-            const int i = w + 8 * m;
-            dst[static_cast<size_t>(i) * DV + c0 + lane] = S[m];
-            float acc = exp2f(sG[(BC - 1) * DK + i]) * S[m];
-            for (int j = 0; j < BC; ++j) acc = fmaf(sK[j * DK + i], sV[j * TW + lane], acc);
-            S[m] = acc;
-        }
-        __syncthreads();
+    if (warp == 0) tmem_alloc(slot, DV);
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
     }
-    float *dst = Sout + static_cast<size_t>(p.NC) * DK * DV;
+    // issue the key-side and value-side loads first; they land during the prefix sums
+    const __nv_bfloat16 *asrc = which ? p.q : p.k;
+    const __nv_bfloat16 *bsrc = which ? p.d_o : p.v;
+    constexpr int APER = BC * 64 / 128;           // channel pairs per thread
+    constexpr int BPER = BC * DV / 8 / 128;       // 16-byte value groups per thread
+    uint32_t araw[APER];
+    uint4 braw[BPER];
 #pragma unroll
-    for (int m = 0; m < RPT; ++m) dst[static_cast<size_t>(w + 8 * m) * DV + c0 + lane] = S[m];
+    for (int m = 0; m < APER; ++m) {
+        const int e = tid + m * 128, t = e >> 6, i = (e & 63) * 2;
+        araw[m] = (t < n && i < DK)
+                      ? *reinterpret_cast<const uint32_t *>(asrc + rk + static_cast<size_t>(t) * DK + i)
+                      : 0u;
+    }
+#pragma unroll
+    for (int m = 0; m < BPER; ++m) {
+        const int e = tid + m * 128, t = e / (DV / 8), c = (e % (DV / 8)) * 8;
+        braw[m] = t < n ? *reinterpret_cast<const uint4 *>(bsrc + rv + static_cast<size_t>(t) * DV + c)
+                        : make_uint4(0u, 0u, 0u, 0u);
+    }
+    load_prefix<DK, DK, 128>(sG, p.log_alpha + rk, n);
+
+    // A: rows = tokens, columns = key channels, scaled and split
+#pragma unroll
+    for (int m = 0; m < APER; ++m) {
+        const int e = tid + m * 128, t = e >> 6, i = (e & 63) * 2;
+        uint32_t hi = 0u, lo = 0u;
+        if (t < n && i < DK) {
+            const float f0 = __uint_as_float(araw[m] << 16), f1 = __uint_as_float(araw[m] & 0xffff0000u);
+            const float g0 = sG[t * DK + i], g1 = sG[t * DK + i + 1];
+            const float e0 = which ? exp2f(g0) : exp2f(sG[(BC - 1) * DK + i] - g0);
+            const float e1 = which ? exp2f(g1) : exp2f(sG[(BC - 1) * DK + i + 1] - g1);
+            split_pair(f0 * e0, f1 * e1, hi, lo);
+        }
+        const uint32_t off = sw128_offset(t, i, L::kBlk);
+        *reinterpret_cast<uint32_t *>(sA + off) = hi;
+        *reinterpret_cast<uint32_t *>(sAlo + off) = lo;
+    }
+    // B: rows = tokens, columns = value columns (bf16 copied as is)
+#pragma unroll
+    for (int m = 0; m < BPER; ++m) {
+        const int e = tid + m * 128, t = e / (DV / 8), c = (e % (DV / 8)) * 8;
+        *reinterpret_cast<uint4 *>(sB + sw128_offset(t, c, L::kBlk)) = braw[m];
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *slot;
+    if (tid == 0) {
+        constexpr uint32_t id = idesc_bf16(128, DV, true, true);
+        const uint32_t aA = smem_u32(sA), aAlo = smem_u32(sAlo), aB = smem_u32(sB);
+#pragma unroll
+        for (int ks = 0; ks < BC / 16; ++ks) {
+            const uint64_t db = sw128_desc(aB + ks * 2048, L::kBlk, 1024);
+            mma_bf16_ss(tmem, sw128_desc(aA + ks * 2048, L::kBlk, 1024), db, id, ks > 0);
+            mma_bf16_ss(tmem, sw128_desc(aAlo + ks * 2048, L::kBlk, 1024), db, id, 1);
+        }
+        mma_commit(bar);
+    }
+    const bool ok = mbar_wait_bounded(bar, 0, p.status);
+    tc_fence_after();
+
+    // epilogue: thread = key channel = TMEM lane
+    const int i = tid;
+    const float mult = which ? p.scale : 1.f;
+    const int slots = which ? p.NC : p.NC + 1;
+    float *dst = (which ? p.adjoints : p.states) + slot_index<DK, DV>(bh, i < DK ? i : 0, 0, u, slots);
+    const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+#pragma unroll 1
+    for (int c0 = 0; c0 < DV; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(taddr + c0, r);
+        tmem_wait_ld();
+        if (ok && i < DK) {
+            float *row = dst + static_cast<size_t>(c0 >> 5) * slots * 32;
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4 *>(row + j) =
+                    make_float4(__uint_as_float(r[j]) * mult, __uint_as_float(r[j + 1]) * mult,
+                                __uint_as_float(r[j + 2]) * mult, __uint_as_float(r[j + 3]) * mult);
+        }
+    }
+    if (which == 0 && i < DK)
+        p.decay[(static_cast<size_t>(bh) * p.NC + u) * DK + i] = exp2f(sG[(BC - 1) * DK + i]);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, DV);
 }
 
 // ---------------------------------------------------------------------------
-// 2. adjoint states, walking the chunks backward.  Same thread layout.
+// 2. scans over the chunks, one thread per state element (bh, i, c), value
+//    columns fastest so that a warp covers 32 columns of one row.
+//    States:    slot u holds dS_u on entry and S_u on exit, slot NC gets hT:
+//               S_(u+1) = e^Gamma_C(u) S_u + dS_u, S_0 = h0.
+//    Gradients: slot u holds dR_u on entry and R_u on exit, dh0 = R_(-1):
+//               R_(u-1) = e^Gamma_C(u) R_u + dR_u, R_(NC-1) = dhT;
+//               plus the log-gate carry rowsum(R_u * S_(u+1)) per 32 columns.
+constexpr int kScanUnroll = 16;
+
 template <int DK, int DV>
-__global__ void __launch_bounds__(NT) bwd_adjoint_kernel(BwdLaunch p) {
-    constexpr int RPT = DK / 8;
+__global__ void __launch_bounds__(256) bwd_state_scan_kernel(BwdLaunch p) {
+    const size_t e = static_cast<size_t>(blockIdx.x) * 256 + threadIdx.x;
+    const int bh = static_cast<int>(e / (DK * DV));
+    const int rem = static_cast<int>(e % (DK * DV)), i = rem / DV;
+    constexpr size_t kM = 32;   // one slot step
+    float *buf = p.states + slot_index<DK, DV>(bh, i, rem % DV, 0, p.NC + 1);
+    const float *dec = p.decay + static_cast<size_t>(bh) * p.NC * DK + i;
+    float S = p.h0 ? p.h0[e] : 0.f;
+    for (int u0 = 0; u0 < p.NC; u0 += kScanUnroll) {
+        float d[kScanUnroll], a[kScanUnroll];
+#pragma unroll
+        for (int j = 0; j < kScanUnroll; ++j) {
+            if (u0 + j < p.NC) {
+                d[j] = buf[(u0 + j) * kM];
+                a[j] = dec[static_cast<size_t>(u0 + j) * DK];
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kScanUnroll; ++j) {
+            if (u0 + j < p.NC) {
+                buf[(u0 + j) * kM] = S;
+                S = fmaf(a[j], S, d[j]);
+            }
+        }
+    }
+    buf[static_cast<size_t>(p.NC) * kM] = S;
+}
+
+template <int DK, int DV>
+__global__ void __launch_bounds__(256) bwd_adjoint_scan_kernel(BwdLaunch p) {
     constexpr int NTILE = DV / TW;
-    extern __shared__ float smem[];
-    float *sG = smem;                  // [BC][DK]
-    float *sQ = sG + BC * DK;          // [BC][DK]: q e^Gamma
-    float *sD = sQ + BC * DK;          // [BC][TW]: do
-    const int tile = blockIdx.x, bh = blockIdx.y;
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int c0 = tile * TW;
-    const size_t base_k = static_cast<size_t>(bh) * p.T * DK;
-    const size_t base_v = static_cast<size_t>(bh) * p.T * DV;
-    const float *Sin = p.states + static_cast<size_t>(bh) * (p.NC + 1) * DK * DV;
-    float *Rout = p.adjoints + static_cast<size_t>(bh) * p.NC * DK * DV;
-    float *carry = p.carry + static_cast<size_t>(bh) * p.NC * NTILE * DK;
-
-    float R[RPT];
+    const size_t e = static_cast<size_t>(blockIdx.x) * 256 + threadIdx.x;
+    const int bh = static_cast<int>(e / (DK * DV));
+    const int rem = static_cast<int>(e % (DK * DV)), i = rem / DV, c = rem % DV;
+    const int lane = threadIdx.x & 31;
+    constexpr size_t kM = 32;   // one slot step
+    float *buf = p.adjoints + slot_index<DK, DV>(bh, i, c, 0, p.NC);
+    const float *st = p.states + slot_index<DK, DV>(bh, i, c, 0, p.NC + 1);
+    const float *dec = p.decay + static_cast<size_t>(bh) * p.NC * DK + i;
+    float *carry = p.carry + static_cast<size_t>(bh) * p.NC * NTILE * DK + (c / TW) * DK + i;
+    float R = p.dhT ? p.dhT[e] : 0.f;
+    for (int u0 = p.NC - 1; u0 >= 0; u0 -= kScanUnroll) {
+        float d[kScanUnroll], a[kScanUnroll], sn[kScanUnroll];
 #pragma unroll
-    for (int m = 0; m < RPT; ++m)
-        R[m] = p.dhT ? p.dhT[(static_cast<size_t>(bh) * DK + w + 8 * m) * DV + c0 + lane] : 0.f;
-
-    for (int u = p.NC - 1; u >= 0; --u) {
-        const int t0 = u * BC, n = min(BC, p.T - t0);
-        load_prefix<DK, DK>(sG, p.log_alpha + base_k + static_cast<size_t>(t0) * DK, n);
-        for (int e = threadIdx.x; e < BC * DK; e += NT) {
-            const int t = e / DK, i = e % DK;
-            const float qq = t < n ? bf(p.q, base_k + static_cast<size_t>(t0 + t) * DK + i) : 0.f;
-            sQ[e] = qq * exp2f(sG[e]);
+        for (int j = 0; j < kScanUnroll; ++j) {
+            if (u0 - j >= 0) {
+                d[j] = buf[(u0 - j) * kM];
+                a[j] = dec[static_cast<size_t>(u0 - j) * DK];
+                sn[j] = st[(u0 - j + 1) * kM];
+            }
         }
-        for (int e = threadIdx.x; e < BC * TW; e += NT) {
-            const int t = e / TW, c = e % TW;
-            sD[e] = t < n ? bf(p.d_o, base_v + static_cast<size_t>(t0 + t) * DV + c0 + c) : 0.f;
-        }
-        __syncthreads();
-        float *dst = Rout + static_cast<size_t>(u) * DK * DV;
-        const float *snext = Sin + static_cast<size_t>(u + 1) * DK * DV;
 #pragma unroll
-        for (int m = 0; m < RPT; ++m) {
-            const int i = w + 8 * m;
-            const size_t off = static_cast<size_t>(i) * DV + c0 + lane;
-            dst[off] = R[m];
-            float part = R[m] * snext[off];
+        for (int j = 0; j < kScanUnroll; ++j) {
+            const int u = u0 - j;
+            if (u >= 0) {
+                buf[u * kM] = R;
+                float part = R * sn[j];
 #pragma unroll
-            for (int s = 16; s > 0; s >>= 1) part += __shfl_xor_sync(0xffffffffu, part, s);
-            if (lane == 0) carry[(static_cast<size_t>(u) * NTILE + tile) * DK + i] = part;
-            float acc = 0.f;
-            for (int t = 0; t < BC; ++t) acc = fmaf(sQ[t * DK + i], sD[t * TW + lane], acc);
-            R[m] = fmaf(exp2f(sG[(BC - 1) * DK + i]), R[m], p.scale * acc);
+                for (int m = 16; m > 0; m >>= 1) part += __shfl_xor_sync(0xffffffffu, part, m);
+                if (lane == 0) carry[static_cast<size_t>(u) * NTILE * DK] = part;
+                R = fmaf(a[j], R, d[j]);
+            }
         }
-        __syncthreads();
     }
-    if (p.gh0) {
-#pragma unroll
-        for (int m = 0; m < RPT; ++m)
-            p.gh0[(static_cast<size_t>(bh) * DK + w + 8 * m) * DV + c0 + lane] = R[m];
-    }
+    if (p.gh0) p.gh0[e] = R;
 }
 
 // ---------------------------------------------------------------------------
-// 3. per-chunk gradients.  Thread (ty, tx) = (tid / 16, tid % 16) owns rows
+// 3. the state terms of the gradients on the tensor cores, one CTA per
+//    (chunk, head), written as fp32 partial gradients:
+//       pq = scale e^Gamma (dO S_u^T),  pk = e^(Gamma_C - Gamma) (V R_u^T),
+//       pv = (K e^(Gamma_C - Gamma)) R_u.
+//    Transposed so that every product has M = 128 (key channels or value
+//    columns on the TMEM lanes) and N = the chunk's 64 tokens:
+//       D1 = S_u dO^T, D2 = R_u V^T (K = value columns), D3 = R_u^T K'^T
+//       (K = key channels).  The value columns go through in slabs of 128
+//    (zero-padded when dv = 64).  S_u and R_u are split into bf16 pairs (hi +
+//    lo): dlog_alpha takes the difference q dq - k dk, which cancels, so dq
+//    and dk need more than one bf16 rounding of the states.
+template <int DK, int DV>
+struct InterSmem {
+    static constexpr int kSlab = 128;
+    static constexpr int kSlabs = DV > kSlab ? DV / kSlab : 1;
+    static constexpr uint32_t kBlkI = 128 * 128;   // 64-column block of a 128-row tile
+    static constexpr uint32_t kBlkT = BC * 128;    // 64-column block of a 64-row tile
+    static constexpr uint32_t kS = 0;
+    static constexpr uint32_t kSlo = kS + 2 * kBlkI;
+    static constexpr uint32_t kR = kSlo + 2 * kBlkI;
+    static constexpr uint32_t kRlo = kR + 2 * kBlkI;
+    static constexpr uint32_t kDo = kRlo + 2 * kBlkI;
+    static constexpr uint32_t kV = kDo + 2 * kBlkT;
+    static constexpr uint32_t kKp = kV + 2 * kBlkT;
+    static constexpr uint32_t kG = kKp + 2 * kBlkT;
+    static constexpr uint32_t kBar = kG + BC * DK * 4;
+    static constexpr uint32_t kSlot = kBar + 8;
+    static constexpr uint32_t kBytes = kSlot + 8 + 1024;
+    static constexpr uint32_t kCols = 256;         // D1 | D2 | D3 slab 0 | D3 slab 1
+};
+
+template <int DK, int DV>
+__global__ void __launch_bounds__(128, 1) bwd_inter_kernel(BwdLaunch p) {
+    using L = InterSmem<DK, DV>;
+    constexpr int SLAB = L::kSlab;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *sS = sm + L::kS, *sR = sm + L::kR, *sDo = sm + L::kDo, *sV = sm + L::kV;
+    uint8_t *sSlo = sm + L::kSlo, *sRlo = sm + L::kRlo;
+    uint8_t *sKp = sm + L::kKp;
+    float *sG = reinterpret_cast<float *>(sm + L::kG);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::kBar);
+    uint32_t *slot = reinterpret_cast<uint32_t *>(sm + L::kSlot);
+    const int u = blockIdx.x, bh = blockIdx.y;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int t0 = u * BC, n = min(BC, p.T - t0);
+    const size_t rk = (static_cast<size_t>(bh) * p.T + t0) * DK;
+    const size_t rv = (static_cast<size_t>(bh) * p.T + t0) * DV;
+
+    if (warp == 0) tmem_alloc(slot, L::kCols);
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    // keys, loaded before the prefix sums; K' = k e^(Gamma_C - Gamma), one bf16
+    constexpr int KPER = BC * DK / 2 / 128;
+    uint32_t kraw[KPER];
+#pragma unroll
+    for (int m = 0; m < KPER; ++m) {
+        const int e = (tid + m * 128) * 2, t = e / DK;
+        kraw[m] = t < n ? *reinterpret_cast<const uint32_t *>(p.k + rk + e) : 0u;
+    }
+    load_prefix<DK, DK, 128>(sG, p.log_alpha + rk, n);
+#pragma unroll
+    for (int m = 0; m < KPER; ++m) {
+        const int e = (tid + m * 128) * 2, t = e / DK, i = e % DK;
+        const float k0 = __uint_as_float(kraw[m] << 16), k1 = __uint_as_float(kraw[m] & 0xffff0000u);
+        const float f0 = exp2f(sG[(BC - 1) * DK + i] - sG[t * DK + i]);
+        const float f1 = exp2f(sG[(BC - 1) * DK + i + 1] - sG[t * DK + i + 1]);
+        *reinterpret_cast<uint32_t *>(sKp + sw128_offset(t, i, L::kBlkT)) = pack_bf16x2(k0 * f0, k1 * f1);
+    }
+
+    bool ok = true;
+    for (int h = 0; h < L::kSlabs; ++h) {
+        if (h > 0) {   // the previous slab's products must be done reading smem
+            ok = ok && mbar_wait_bounded(bar, (h - 1) & 1, p.status);
+            tc_fence_after();
+        }
+        const int cb = h * SLAB;
+        // S_u and R_u rows (128, zero past dk) x 128 value columns -> bf16
+#pragma unroll 4
+        for (int m = 0; m < 128 * SLAB / 4 / 128; ++m) {
+            const int e = tid + m * 128, i = e / (SLAB / 4), cl = (e % (SLAB / 4)) * 4;
+            float4 sv = make_float4(0.f, 0.f, 0.f, 0.f), rr = sv;
+            if (i < DK && cb + cl < DV) {
+                sv = *reinterpret_cast<const float4 *>(
+                    p.states + slot_index<DK, DV>(bh, i, cb + cl, u, p.NC + 1));
+                rr = *reinterpret_cast<const float4 *>(
+                    p.adjoints + slot_index<DK, DV>(bh, i, cb + cl, u, p.NC));
+            }
+            const uint32_t off = sw128_offset(i, cl, L::kBlkI);
+            uint32_t h0, l0, h1, l1;
+            split_pair(sv.x, sv.y, h0, l0);
+            split_pair(sv.z, sv.w, h1, l1);
+            *reinterpret_cast<uint2 *>(sS + off) = make_uint2(h0, h1);
+            *reinterpret_cast<uint2 *>(sSlo + off) = make_uint2(l0, l1);
+            split_pair(rr.x, rr.y, h0, l0);
+            split_pair(rr.z, rr.w, h1, l1);
+            *reinterpret_cast<uint2 *>(sR + off) = make_uint2(h0, h1);
+            *reinterpret_cast<uint2 *>(sRlo + off) = make_uint2(l0, l1);
+        }
+        // dO and V rows (64 tokens) x 128 value columns
+#pragma unroll
+        for (int m = 0; m < BC * SLAB / 8 / 128; ++m) {
+            const int e = tid + m * 128, t = e / (SLAB / 8), cl = (e % (SLAB / 8)) * 8;
+            uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
+            if (t < n && cb + cl < DV) {
+                const size_t off = rv + static_cast<size_t>(t) * DV + cb + cl;
+                a = *reinterpret_cast<const uint4 *>(p.d_o + off);
+                b = *reinterpret_cast<const uint4 *>(p.v + off);
+            }
+            const uint32_t off = sw128_offset(t, cl, L::kBlkT);
+            *reinterpret_cast<uint4 *>(sDo + off) = a;
+            *reinterpret_cast<uint4 *>(sV + off) = b;
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0) {
+            const uint32_t tmem = *slot;
+            constexpr uint32_t id_kk = idesc_bf16(128, BC, false, false);
+            constexpr uint32_t id_mk = idesc_bf16(128, BC, true, false);
+            const uint32_t aS = smem_u32(sS), aR = smem_u32(sR), aDo = smem_u32(sDo);
+            const uint32_t aSlo = smem_u32(sSlo), aRlo = smem_u32(sRlo);
+            const uint32_t aV = smem_u32(sV), aKp = smem_u32(sKp);
+#pragma unroll
+            for (int kk = 0; kk < SLAB / 16; ++kk) {
+                const uint32_t oi = (kk >> 2) * L::kBlkI + (kk & 3) * 32;
+                const uint32_t ot = (kk >> 2) * L::kBlkT + (kk & 3) * 32;
+                const uint32_t acc = (h > 0 || kk > 0) ? 1u : 0u;
+                const uint64_t bdo = sw128_desc(aDo + ot, 16, 1024), bv = sw128_desc(aV + ot, 16, 1024);
+                mma_bf16_ss(tmem, sw128_desc(aS + oi, 16, 1024), bdo, id_kk, acc);
+                mma_bf16_ss(tmem, sw128_desc(aSlo + oi, 16, 1024), bdo, id_kk, 1u);
+                mma_bf16_ss(tmem + BC, sw128_desc(aR + oi, 16, 1024), bv, id_kk, acc);
+                mma_bf16_ss(tmem + BC, sw128_desc(aRlo + oi, 16, 1024), bv, id_kk, 1u);
+            }
+#pragma unroll
+            for (int kk = 0; kk < DK / 16; ++kk) {
+                const uint32_t ot = (kk >> 2) * L::kBlkT + (kk & 3) * 32;
+                const uint64_t bk = sw128_desc(aKp + ot, 16, 1024);
+                mma_bf16_ss(tmem + 2 * BC + h * BC, sw128_desc(aR + kk * 2048, L::kBlkI, 1024), bk,
+                            id_mk, kk > 0 ? 1u : 0u);
+                mma_bf16_ss(tmem + 2 * BC + h * BC, sw128_desc(aRlo + kk * 2048, L::kBlkI, 1024), bk,
+                            id_mk, 1u);
+            }
+            mma_commit(bar);
+        }
+    }
+    ok = mbar_wait_bounded(bar, (L::kSlabs - 1) & 1, p.status) && ok;
+    tc_fence_after();
+
+    // epilogue: TMEM lane r = 32 warp + lane
+    const uint32_t tmem = *slot;
+    const int r = tid;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const float gc = r < DK ? sG[(BC - 1) * DK + r] : 0.f;
+#pragma unroll 1
+    for (int part = 0; part < 2 + L::kSlabs; ++part) {
+#pragma unroll 1
+        for (int tb = 0; tb < BC; tb += 32) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_off + part * BC + tb, v);
+            tmem_wait_ld();
+            if (!ok) continue;
+            if (part < 2) {
+                if (r >= DK) continue;
+                float *dst = (part == 0 ? p.pq : p.pk) + rk + r;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int t = tb + j;
+                    if (t < n) {
+                        const float g = sG[t * DK + r];
+                        const float f = part == 0 ? p.scale * exp2f(g) : exp2f(gc - g);
+                        dst[static_cast<size_t>(t) * DK] = f * __uint_as_float(v[j]);
+                    }
+                }
+            } else {
+                const int c = (part - 2) * SLAB + r;
+                if (c >= DV) continue;
+                float *dst = p.pv + rv + c;
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (tb + j < n) dst[static_cast<size_t>(tb + j) * DV] = __uint_as_float(v[j]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, L::kCols);
+}
+
+// ---------------------------------------------------------------------------
+// 4. per-chunk gradients.  Thread (ty, tx) = (tid / 16, tid % 16) owns rows
 //    4 ty .. 4 ty + 3 and columns tx, tx + 16, ... of every C x C, C x dk and
 //    C x 32 block it computes.
 template <int DK>
@@ -200,8 +524,7 @@ struct GradSmem {
     static constexpr int kG = 0, kQ = kG + BC * LD, kK = kQ + BC * LD, kP = kK + BC * LD;
     static constexpr int kAM = kP + BC * LD;
     static constexpr int kDo = kAM + BC * LA, kV = kDo + BC * LS;
-    static constexpr int kS = kV + BC * LS, kR = kS + DK * LS;
-    static constexpr int kRef = kR + DK * LS, kGC = kRef + DK, kCarry = kGC + DK;
+    static constexpr int kRef = kV + BC * LS, kGC = kRef + DK, kCarry = kGC + DK;
     static constexpr int kFloats = kCarry + DK;
     static constexpr size_t kBytes = sizeof(float) * kFloats;
 };
@@ -215,7 +538,6 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdLaunch p) {
     extern __shared__ float smem[];
     float *sG = smem + L::kG, *sQ = smem + L::kQ, *sK = smem + L::kK, *sP = smem + L::kP;
     float *sAM = smem + L::kAM, *sDo = smem + L::kDo, *sV = smem + L::kV;
-    float *sS = smem + L::kS, *sR = smem + L::kR;
     float *sRef = smem + L::kRef, *sGC = smem + L::kGC, *sCarry = smem + L::kCarry;
 
     const int u = blockIdx.x, bh = blockIdx.y;
@@ -223,9 +545,19 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdLaunch p) {
     const int t0 = u * BC, n = min(BC, p.T - t0);
     const size_t rk = (static_cast<size_t>(bh) * p.T + t0) * DK;   // first row, key tensors
     const size_t rv = (static_cast<size_t>(bh) * p.T + t0) * DV;   // first row, value tensors
-    const float *Su = p.states + (static_cast<size_t>(bh) * (p.NC + 1) + u) * DK * DV;
-    const float *Ru = p.adjoints + (static_cast<size_t>(bh) * p.NC + u) * DK * DV;
     const float s = p.scale;
+
+    // the state terms of dq and dk (bwd_inter), fetched early for phase 2
+    float pq[4][NB], pk[4][NB];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            const int t = 4 * ty + a;
+            const size_t off = rk + static_cast<size_t>(t) * DK + tx + 16 * b;
+            pq[a][b] = t < n ? p.pq[off] : 0.f;
+            pk[a][b] = t < n ? p.pk[off] : 0.f;
+        }
 
     // prefix sums, the reference and the path choice
     load_prefix<DK, LD>(sG, p.log_alpha + rk, n);
@@ -243,55 +575,64 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdLaunch p) {
     const bool exact = __syncthreads_or(wide) || p.force_exact;
 
     // q and k: rescaled around the reference (fast path) or raw (exact path)
-    for (int e = tid; e < BC * DK; e += NT) {
-        const int t = e / DK, i = e % DK;
-        const float qq = t < n ? bf(p.q, rk + static_cast<size_t>(t) * DK + i) : 0.f;
-        const float kk = t < n ? bf(p.k, rk + static_cast<size_t>(t) * DK + i) : 0.f;
-        const float d = exact ? 0.f : sG[t * LD + i] - sRef[i];
-        sQ[t * LD + i] = qq * exp2f(d);
-        sK[t * LD + i] = kk * exp2f(-d);
+    {
+        constexpr int PER = BC * DK / 2 / NT;
+        uint32_t qr[PER], kr[PER];
+#pragma unroll
+        for (int m = 0; m < PER; ++m) {
+            const int e = (tid + m * NT) * 2, t = e / DK;
+            const size_t off = rk + static_cast<size_t>(e);
+            qr[m] = t < n ? *reinterpret_cast<const uint32_t *>(p.q + off) : 0u;
+            kr[m] = t < n ? *reinterpret_cast<const uint32_t *>(p.k + off) : 0u;
+        }
+#pragma unroll
+        for (int m = 0; m < PER; ++m) {
+            const int e = (tid + m * NT) * 2, t = e / DK, i = e % DK;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float qq = __uint_as_float(h ? (qr[m] & 0xffff0000u) : (qr[m] << 16));
+                const float kk = __uint_as_float(h ? (kr[m] & 0xffff0000u) : (kr[m] << 16));
+                const float d = exact ? 0.f : sG[t * LD + i + h] - sRef[i + h];
+                sQ[t * LD + i + h] = qq * exp2f(d);
+                sK[t * LD + i + h] = kk * exp2f(-d);
+            }
+        }
     }
 
-    // phase 1: stream the value columns: A = dO V^T, dO S_u^T, V R_u^T
-    float accA[4][4] = {}, accQ[4][NB] = {}, accK[4][NB] = {};
+    // phase 1: A = dO V^T, streaming the value columns
+    float accA[4][4] = {};
     for (int c0 = 0; c0 < DV; c0 += TW) {
         __syncthreads();
-        for (int e = tid; e < BC * TW; e += NT) {
-            const int t = e / TW, c = e % TW;
-            const bool in = t < n;
-            sDo[t * LS + c] = in ? bf(p.d_o, rv + static_cast<size_t>(t) * DV + c0 + c) : 0.f;
-            sV[t * LS + c] = in ? bf(p.v, rv + static_cast<size_t>(t) * DV + c0 + c) : 0.f;
-        }
-        for (int e = tid; e < DK * TW; e += NT) {
-            const int i = e / TW, c = e % TW;
-            sS[i * LS + c] = Su[static_cast<size_t>(i) * DV + c0 + c];
-            sR[i * LS + c] = Ru[static_cast<size_t>(i) * DV + c0 + c];
+        {
+            constexpr int PV = BC * TW / NT;
+            float dov[PV], vv[PV];
+#pragma unroll
+            for (int m = 0; m < PV; ++m) {
+                const int e = tid + m * NT, t = e / TW, c = e % TW;
+                const size_t off = rv + static_cast<size_t>(t) * DV + c0 + c;
+                dov[m] = t < n ? bf(p.d_o, off) : 0.f;
+                vv[m] = t < n ? bf(p.v, off) : 0.f;
+            }
+#pragma unroll
+            for (int m = 0; m < PV; ++m) {
+                const int e = tid + m * NT, t = e / TW, c = e % TW;
+                sDo[t * LS + c] = dov[m];
+                sV[t * LS + c] = vv[m];
+            }
         }
         __syncthreads();
 #pragma unroll 4
         for (int c = 0; c < TW; ++c) {
-            float dr[4], vr[4], vj[4], sc[NB], rc[NB];
+            float dr[4], vj[4];
 #pragma unroll
             for (int a = 0; a < 4; ++a) {
                 dr[a] = sDo[(4 * ty + a) * LS + c];
-                vr[a] = sV[(4 * ty + a) * LS + c];
                 vj[a] = sV[(tx + 16 * a) * LS + c];
             }
 #pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                sc[b] = sS[(tx + 16 * b) * LS + c];
-                rc[b] = sR[(tx + 16 * b) * LS + c];
-            }
-#pragma unroll
-            for (int a = 0; a < 4; ++a) {
+            for (int a = 0; a < 4; ++a)
 #pragma unroll
                 for (int b = 0; b < 4; ++b) accA[a][b] = fmaf(dr[a], vj[b], accA[a][b]);
-#pragma unroll
-                for (int b = 0; b < NB; ++b) {
-                    accQ[a][b] = fmaf(dr[a], sc[b], accQ[a][b]);
-                    accK[a][b] = fmaf(vr[a], rc[b], accK[a][b]);
-                }
-            }
         }
     }
 #pragma unroll
@@ -342,8 +683,8 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdLaunch p) {
             const int i = tx + 16 * b;
             const float g = sG[t * LD + i];
             const float d = exact ? 0.f : g - sRef[i];
-            const float dq = s * (exp2f(d) * iq[b] + exp2f(g) * accQ[a][b]);
-            const float dk = s * exp2f(-d) * ik[b] + exp2f(sGC[i] - g) * accK[a][b];
+            const float dq = s * exp2f(d) * iq[b] + pq[a][b];
+            const float dk = s * exp2f(-d) * ik[b] + pk[a][b];
             float pr = 0.f;
             if (t < n) {
                 const size_t off = rk + static_cast<size_t>(t) * DK + i;
@@ -381,38 +722,40 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdLaunch p) {
     for (int a = 0; a < 4; ++a)
 #pragma unroll
         for (int b = 0; b < 4; ++b) sAM[(4 * ty + a) * LA + tx + 16 * b] = accA[a][b];
-    // keys for the state term of dV: k e^(Gamma_C - Gamma)
-    for (int e = tid; e < BC * DK; e += NT) {
-        const int t = e / DK, i = e % DK;
-        const float f = exact ? exp2f(sGC[i] - sG[t * LD + i]) : exp2f(sGC[i] - sRef[i]);
-        sK[t * LD + i] *= f;
-    }
-
-    // phase 4: dV = M^T dO + K' R_u, one slice of value columns at a time
+    // phase 4: dV = M^T dO + the state term (bwd_inter), a slice of value columns at a time
     for (int c0 = 0; c0 < DV; c0 += TW) {
         __syncthreads();
-        for (int e = tid; e < BC * TW; e += NT) {
-            const int t = e / TW, c = e % TW;
-            sDo[t * LS + c] = t < n ? bf(p.d_o, rv + static_cast<size_t>(t) * DV + c0 + c) : 0.f;
-        }
-        for (int e = tid; e < DK * TW; e += NT) {
-            const int i = e / TW, c = e % TW;
-            sR[i * LS + c] = Ru[static_cast<size_t>(i) * DV + c0 + c];
+        float pvv[4][2];
+        {
+            constexpr int PV = BC * TW / NT;
+            float dov[PV];
+#pragma unroll
+            for (int m = 0; m < PV; ++m) {
+                const int e = tid + m * NT, t = e / TW, c = e % TW;
+                dov[m] = t < n ? bf(p.d_o, rv + static_cast<size_t>(t) * DV + c0 + c) : 0.f;
+            }
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const int j = 4 * ty + a;
+                const size_t off = rv + static_cast<size_t>(j) * DV + c0 + tx;
+                pvv[a][0] = j < n ? p.pv[off] : 0.f;
+                pvv[a][1] = j < n ? p.pv[off + 16] : 0.f;
+            }
+#pragma unroll
+            for (int m = 0; m < PV; ++m) {
+                const int e = tid + m * NT;
+                sDo[(e / TW) * LS + e % TW] = dov[m];
+            }
         }
         __syncthreads();
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
             const int j = 4 * ty + a;
-            float acc0 = 0.f, acc1 = 0.f;
+            float acc0 = pvv[a][0], acc1 = pvv[a][1];
             for (int x = j; x < BC; ++x) {
                 const float mxj = sAM[x * LA + j];
                 acc0 = fmaf(mxj, sDo[x * LS + tx], acc0);
                 acc1 = fmaf(mxj, sDo[x * LS + tx + 16], acc1);
-            }
-            for (int i = 0; i < DK; ++i) {
-                const float kji = sK[j * LD + i];
-                acc0 = fmaf(kji, sR[i * LS + tx], acc0);
-                acc1 = fmaf(kji, sR[i * LS + tx + 16], acc1);
             }
             if (j < n) {
                 const size_t off = rv + static_cast<size_t>(j) * DV + c0;
@@ -434,24 +777,27 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdLaunch p) {
 
 template <int DK, int DV>
 int launch_bwd_dims(const BwdLaunch &p, cudaStream_t stream) {
-    const size_t seq_bytes = sizeof(float) * (2 * BC * DK + BC * TW);
+    const size_t sum_bytes = SumSmem<DK, DV>::kBytes;
     const size_t grad_bytes = GradSmem<DK>::kBytes;
-    cudaError_t e = cudaFuncSetAttribute(bwd_states_kernel<DK, DV>,
+    const size_t inter_bytes = InterSmem<DK, DV>::kBytes;
+    cudaError_t e = cudaFuncSetAttribute(bwd_sums_kernel<DK, DV>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(seq_bytes));
+                                         static_cast<int>(sum_bytes));
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(bwd_adjoint_kernel<DK, DV>,
+        e = cudaFuncSetAttribute(bwd_inter_kernel<DK, DV>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(seq_bytes));
+                                 static_cast<int>(inter_bytes));
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(bwd_grads_kernel<DK, DV>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(grad_bytes));
     if (e != cudaSuccess) return static_cast<int>(e);
-    const dim3 tiles(DV / TW, p.BH), chunks(p.NC, p.BH);
-    bwd_states_kernel<DK, DV><<<tiles, NT, seq_bytes, stream>>>(p);
-    bwd_adjoint_kernel<DK, DV><<<tiles, NT, seq_bytes, stream>>>(p);
-    bwd_grads_kernel<DK, DV><<<chunks, NT, grad_bytes, stream>>>(p);
+    const unsigned scan_blocks = static_cast<unsigned>(static_cast<size_t>(p.BH) * DK * DV / 256);
+    bwd_sums_kernel<DK, DV><<<dim3(p.NC, p.BH, 2), 128, sum_bytes, stream>>>(p);
+    bwd_state_scan_kernel<DK, DV><<<scan_blocks, 256, 0, stream>>>(p);
+    bwd_adjoint_scan_kernel<DK, DV><<<scan_blocks, 256, 0, stream>>>(p);
+    bwd_inter_kernel<DK, DV><<<dim3(p.NC, p.BH), 128, inter_bytes, stream>>>(p);
+    bwd_grads_kernel<DK, DV><<<dim3(p.NC, p.BH), NT, grad_bytes, stream>>>(p);
     return static_cast<int>(cudaGetLastError());
 }
 

@@ -94,6 +94,10 @@ struct BwdLaunch {
     float *states;                           // scratch [BH, NC + 1, dk, dv]
     float *adjoints;                         // scratch [BH, NC, dk, dv]
     float *carry;                            // scratch [BH, NC, dv / 32, dk]
+    float *decay;                            // scratch [BH, NC, dk]: e^Gamma_C per chunk
+    float *pq, *pk;                          // scratch [BH, T, dk]: state terms of dq, dk
+    float *pv;                               // scratch [BH, T, dv]: state term of dv
+    unsigned int *status;                    // device status word (bounded waits)
     float scale;
     int BH, T, NC, dk, dv;
     int force_exact;
@@ -103,7 +107,7 @@ struct BwdLaunch {
 int bwd_chunk_tokens();
 int bwd_value_tiles(int dv);
 
-// Enqueues the three backward kernels; returns a cudaError_t value.
+// Enqueues the five backward kernels; returns a cudaError_t value.
 int launch_chunk_bwd(const BwdLaunch &p, cudaStream_t stream);
 
 }  // namespace gla

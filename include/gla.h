@@ -264,20 +264,22 @@ int gla_recurrent_step(const void *q, const void *k, const void *v, const float 
  * No output may alias an input.
  *
  * The states are recomputed from the inputs (no forward activations are
- * needed): one pass over the chunks forward for the chunk-start states, one
- * backward for the state gradients, then every chunk's gradients
+ * needed): every chunk's own state and state-gradient sums in parallel, two
+ * scans over the chunks for the chunk-start states and the state gradients,
+ * then every chunk's gradients
  * independently.  Source: the recurrence and chunk equations of the page
  * named above (sections "The Gated Recurrent Update", "Cumulative Decay
  * Representation", "Intra-Chunk Matrix Multiplications", "Inter-Chunk
  * Recurrence and Output Projection"), differentiated; the page notes that
  * the chunkwise form keeps its states for the backward pass.
  *
- * Scratch: (2 NC + 1) * B * H * dk * dv fp32 plus the log-gate carries, NC =
- * ceil(T / 64), taken stream-ordered (cudaMallocAsync) and released on
+ * Scratch: (2 NC + 1) * B * H * dk * dv fp32 plus per-chunk decays and
+ * log-gate carries, NC = ceil(T / 64), taken stream-ordered (cudaMallocAsync) and released on
  * `stream` (GLA_ERR_ALLOC when the pool cannot supply it).
  *
- * Shapes as for gla_chunk_fwd, with B * H <= 65535.  Pointers need only their
- * element alignment.  Accuracy: each gradient matches the fp64 reverse-mode
+ * Shapes as for gla_chunk_fwd, with B * H <= 65535; pointers 16-byte aligned.
+ * A bounded device wait that expires leaves the gradients unspecified and is
+ * reported by gla_last_device_status (GLA_ERR_TIMEOUT).  Accuracy: each gradient matches the fp64 reverse-mode
  * differentiation of the recurrence to relative L2 error <= 1e-2 and max-abs
  * error <= 2e-2 * RMS(reference).
  */
