@@ -350,8 +350,11 @@ struct InterSmem {
     static constexpr uint32_t kCols = 256;         // D1 | D2 | D3 slab 0 | D3 slab 1
 };
 
+constexpr int kInterThreads = 256;
+
 template <int DK, int DV>
-__global__ void __launch_bounds__(128, 1) bwd_inter_kernel(BwdLaunch p) {
+__global__ void __launch_bounds__(kInterThreads, 1) bwd_inter_kernel(BwdLaunch p) {
+    constexpr int NTI = kInterThreads;
     using L = InterSmem<DK, DV>;
     constexpr int SLAB = L::kSlab;
     extern __shared__ uint8_t smem_raw[];
@@ -375,17 +378,17 @@ __global__ void __launch_bounds__(128, 1) bwd_inter_kernel(BwdLaunch p) {
         fence_mbar_init();
     }
     // keys, loaded before the prefix sums; K' = k e^(Gamma_C - Gamma), one bf16
-    constexpr int KPER = BC * DK / 2 / 128;
+    constexpr int KPER = BC * DK / 2 / NTI;
     uint32_t kraw[KPER];
 #pragma unroll
     for (int m = 0; m < KPER; ++m) {
-        const int e = (tid + m * 128) * 2, t = e / DK;
+        const int e = (tid + m * NTI) * 2, t = e / DK;
         kraw[m] = t < n ? *reinterpret_cast<const uint32_t *>(p.k + rk + e) : 0u;
     }
-    load_prefix<DK, DK, 128>(sG, p.log_alpha + rk, n);
+    load_prefix<DK, DK, NTI>(sG, p.log_alpha + rk, n);
 #pragma unroll
     for (int m = 0; m < KPER; ++m) {
-        const int e = (tid + m * 128) * 2, t = e / DK, i = e % DK;
+        const int e = (tid + m * NTI) * 2, t = e / DK, i = e % DK;
         const float k0 = __uint_as_float(kraw[m] << 16), k1 = __uint_as_float(kraw[m] & 0xffff0000u);
         const float f0 = exp2f(sG[(BC - 1) * DK + i] - sG[t * DK + i]);
         const float f1 = exp2f(sG[(BC - 1) * DK + i + 1] - sG[t * DK + i + 1]);
@@ -399,32 +402,43 @@ __global__ void __launch_bounds__(128, 1) bwd_inter_kernel(BwdLaunch p) {
             tc_fence_after();
         }
         const int cb = h * SLAB;
-        // S_u and R_u rows (128, zero past dk) x 128 value columns -> bf16
-#pragma unroll 4
-        for (int m = 0; m < 128 * SLAB / 4 / 128; ++m) {
-            const int e = tid + m * 128, i = e / (SLAB / 4), cl = (e % (SLAB / 4)) * 4;
-            float4 sv = make_float4(0.f, 0.f, 0.f, 0.f), rr = sv;
-            if (i < DK && cb + cl < DV) {
-                sv = *reinterpret_cast<const float4 *>(
-                    p.states + slot_index<DK, DV>(bh, i, cb + cl, u, p.NC + 1));
-                rr = *reinterpret_cast<const float4 *>(
-                    p.adjoints + slot_index<DK, DV>(bh, i, cb + cl, u, p.NC));
+        // S_u and R_u rows (128, zero past dk) x 128 value columns -> bf16 pairs;
+        // batches of 8 float4 per matrix in flight per thread
+        constexpr int SPER = 128 * SLAB / 4 / NTI, SB = 8;
+#pragma unroll 1
+        for (int mb = 0; mb < SPER; mb += SB) {
+            float4 sv[SB], rr[SB];
+#pragma unroll
+            for (int m = 0; m < SB; ++m) {
+                const int e = tid + (mb + m) * NTI, i = e / (SLAB / 4), cl = (e % (SLAB / 4)) * 4;
+                sv[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+                rr[m] = sv[m];
+                if (i < DK && cb + cl < DV) {
+                    sv[m] = *reinterpret_cast<const float4 *>(
+                        p.states + slot_index<DK, DV>(bh, i, cb + cl, u, p.NC + 1));
+                    rr[m] = *reinterpret_cast<const float4 *>(
+                        p.adjoints + slot_index<DK, DV>(bh, i, cb + cl, u, p.NC));
+                }
             }
-            const uint32_t off = sw128_offset(i, cl, L::kBlkI);
-            uint32_t h0, l0, h1, l1;
-            split_pair(sv.x, sv.y, h0, l0);
-            split_pair(sv.z, sv.w, h1, l1);
-            *reinterpret_cast<uint2 *>(sS + off) = make_uint2(h0, h1);
-            *reinterpret_cast<uint2 *>(sSlo + off) = make_uint2(l0, l1);
-            split_pair(rr.x, rr.y, h0, l0);
-            split_pair(rr.z, rr.w, h1, l1);
-            *reinterpret_cast<uint2 *>(sR + off) = make_uint2(h0, h1);
-            *reinterpret_cast<uint2 *>(sRlo + off) = make_uint2(l0, l1);
+#pragma unroll
+            for (int m = 0; m < SB; ++m) {
+                const int e = tid + (mb + m) * NTI, i = e / (SLAB / 4), cl = (e % (SLAB / 4)) * 4;
+                const uint32_t off = sw128_offset(i, cl, L::kBlkI);
+                uint32_t h0, l0, h1, l1;
+                split_pair(sv[m].x, sv[m].y, h0, l0);
+                split_pair(sv[m].z, sv[m].w, h1, l1);
+                *reinterpret_cast<uint2 *>(sS + off) = make_uint2(h0, h1);
+                *reinterpret_cast<uint2 *>(sSlo + off) = make_uint2(l0, l1);
+                split_pair(rr[m].x, rr[m].y, h0, l0);
+                split_pair(rr[m].z, rr[m].w, h1, l1);
+                *reinterpret_cast<uint2 *>(sR + off) = make_uint2(h0, h1);
+                *reinterpret_cast<uint2 *>(sRlo + off) = make_uint2(l0, l1);
+            }
         }
         // dO and V rows (64 tokens) x 128 value columns
 #pragma unroll
-        for (int m = 0; m < BC * SLAB / 8 / 128; ++m) {
-            const int e = tid + m * 128, t = e / (SLAB / 8), cl = (e % (SLAB / 8)) * 8;
+        for (int m = 0; m < BC * SLAB / 8 / NTI; ++m) {
+            const int e = tid + m * NTI, t = e / (SLAB / 8), cl = (e % (SLAB / 8)) * 8;
             uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
             if (t < n && cb + cl < DV) {
                 const size_t off = rv + static_cast<size_t>(t) * DV + cb + cl;
@@ -472,13 +486,15 @@ __global__ void __launch_bounds__(128, 1) bwd_inter_kernel(BwdLaunch p) {
     ok = mbar_wait_bounded(bar, (L::kSlabs - 1) & 1, p.status) && ok;
     tc_fence_after();
 
-    // epilogue: TMEM lane r = 32 warp + lane
+    // epilogue: TMEM lane r = 32 (warp % 4) + lane; warps 0-3 take D1 and D2,
+    // warps 4-7 the D3 slabs
     const uint32_t tmem = *slot;
-    const int r = tid;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int r = 32 * (warp & 3) + (tid & 31);
+    const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const float gc = r < DK ? sG[(BC - 1) * DK + r] : 0.f;
+    const int part0 = warp < 4 ? 0 : 2, part1 = warp < 4 ? 2 : 2 + L::kSlabs;
 #pragma unroll 1
-    for (int part = 0; part < 2 + L::kSlabs; ++part) {
+    for (int part = part0; part < part1; ++part) {
 #pragma unroll 1
         for (int tb = 0; tb < BC; tb += 32) {
             uint32_t v[32];
@@ -796,7 +812,7 @@ int launch_bwd_dims(const BwdLaunch &p, cudaStream_t stream) {
     bwd_sums_kernel<DK, DV><<<dim3(p.NC, p.BH, 2), 128, sum_bytes, stream>>>(p);
     bwd_state_scan_kernel<DK, DV><<<scan_blocks, 256, 0, stream>>>(p);
     bwd_adjoint_scan_kernel<DK, DV><<<scan_blocks, 256, 0, stream>>>(p);
-    bwd_inter_kernel<DK, DV><<<dim3(p.NC, p.BH), 128, inter_bytes, stream>>>(p);
+    bwd_inter_kernel<DK, DV><<<dim3(p.NC, p.BH), kInterThreads, inter_bytes, stream>>>(p);
     bwd_grads_kernel<DK, DV><<<dim3(p.NC, p.BH), NT, grad_bytes, stream>>>(p);
     return static_cast<int>(cudaGetLastError());
 }
