@@ -270,8 +270,9 @@ int gla_recurrent_step(const void *q, const void *k, const void *v, const float 
  * independently.  Source: the recurrence and chunk equations of the page
  * named above (sections "The Gated Recurrent Update", "Cumulative Decay
  * Representation", "Intra-Chunk Matrix Multiplications", "Inter-Chunk
- * Recurrence and Output Projection"), differentiated; the page notes that
- * the chunkwise form keeps its states for the backward pass.
+ * Recurrence and Output Projection"), differentiated; its section "I/O-Aware
+ * Kernel Design in FlashLinearAttention" has the backward recompute the chunk
+ * states rather than cache them, as this call does.
  *
  * Scratch: (2 NC + 1) * B * H * dk * dv fp32 plus per-chunk decays and
  * log-gate carries, NC = ceil(T / 64), taken stream-ordered (cudaMallocAsync) and released on

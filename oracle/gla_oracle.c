@@ -119,12 +119,11 @@ void gla_oracle_step(const float *q, const float *k, const float *v, const float
 /*
  * Backward pass — gradients of a scalar loss through the same recurrence.
  *
- * Source: the recurrence of "The Gated Recurrent Update" above; the pages
- * state that training differentiates it and that the chunkwise method keeps
- * its states for the backward pass ("Gated Linear Attention (GLA) ...",
- * section "Chunkwise Parallel Form", closing remark on hardware efficiency).
- * They print no backward equations, so this is reverse-mode differentiation
- * of the token loop, written out.  With the loss
+ * Source: the recurrence of "The Gated Recurrent Update" above; the same
+ * page's section "I/O-Aware Kernel Design in FlashLinearAttention" names a
+ * backward pass that recomputes the chunk states instead of caching them.
+ * The pages print no backward equations, so this is reverse-mode
+ * differentiation of the token loop, written out.  With the loss
  *
  *     L = sum_t <do_t, o_t> + <dhT, hT>,
  *
