@@ -213,7 +213,8 @@ __global__ void __launch_bounds__(128, 1) bwd_sums_kernel(BwdLaunch p) {
     const bool ok = mbar_wait_bounded(bar, 0, p.status);
     tc_fence_after();
 
-    // epilogue: thread = key channel = TMEM lane
+    // epilogue: thread = key channel = TMEM lane; each 32-column group of a
+    // row is one 128-byte line of the scratch
     const int i = tid;
     const float mult = which ? p.scale : 1.f;
     const int slots = which ? p.NC : p.NC + 1;
@@ -251,7 +252,7 @@ __global__ void __launch_bounds__(128, 1) bwd_sums_kernel(BwdLaunch p) {
 constexpr int kScanUnroll = 16;
 
 template <int DK, int DV>
-__global__ void __launch_bounds__(256) bwd_state_scan_kernel(BwdLaunch p) {
+__global__ void __launch_bounds__(256, 3) bwd_state_scan_kernel(BwdLaunch p) {
     const size_t e = static_cast<size_t>(blockIdx.x) * 256 + threadIdx.x;
     const int bh = static_cast<int>(e / (DK * DV));
     const int rem = static_cast<int>(e % (DK * DV)), i = rem / DV;
@@ -259,8 +260,8 @@ __global__ void __launch_bounds__(256) bwd_state_scan_kernel(BwdLaunch p) {
     float *buf = p.states + slot_index<DK, DV>(bh, i, rem % DV, 0, p.NC + 1);
     const float *dec = p.decay + static_cast<size_t>(bh) * p.NC * DK + i;
     float S = p.h0 ? p.h0[e] : 0.f;
-    for (int u0 = 0; u0 < p.NC; u0 += kScanUnroll) {
-        float d[kScanUnroll], a[kScanUnroll];
+    float d[kScanUnroll], a[kScanUnroll];
+    auto fetch = [&](int u0) {
 #pragma unroll
         for (int j = 0; j < kScanUnroll; ++j) {
             if (u0 + j < p.NC) {
@@ -268,11 +269,21 @@ __global__ void __launch_bounds__(256) bwd_state_scan_kernel(BwdLaunch p) {
                 a[j] = dec[static_cast<size_t>(u0 + j) * DK];
             }
         }
+    };
+    fetch(0);
+    for (int u0 = 0; u0 < p.NC; u0 += kScanUnroll) {
+        float dn[kScanUnroll], an[kScanUnroll];
+#pragma unroll
+        for (int j = 0; j < kScanUnroll; ++j) {
+            dn[j] = d[j];
+            an[j] = a[j];
+        }
+        if (u0 + kScanUnroll < p.NC) fetch(u0 + kScanUnroll);   // next group in flight
 #pragma unroll
         for (int j = 0; j < kScanUnroll; ++j) {
             if (u0 + j < p.NC) {
                 buf[(u0 + j) * kM] = S;
-                S = fmaf(a[j], S, d[j]);
+                S = fmaf(an[j], S, dn[j]);
             }
         }
     }
@@ -280,7 +291,7 @@ __global__ void __launch_bounds__(256) bwd_state_scan_kernel(BwdLaunch p) {
 }
 
 template <int DK, int DV>
-__global__ void __launch_bounds__(256) bwd_adjoint_scan_kernel(BwdLaunch p) {
+__global__ void __launch_bounds__(256, 2) bwd_adjoint_scan_kernel(BwdLaunch p) {
     constexpr int NTILE = DV / TW;
     const size_t e = static_cast<size_t>(blockIdx.x) * 256 + threadIdx.x;
     const int bh = static_cast<int>(e / (DK * DV));
@@ -292,8 +303,8 @@ __global__ void __launch_bounds__(256) bwd_adjoint_scan_kernel(BwdLaunch p) {
     const float *dec = p.decay + static_cast<size_t>(bh) * p.NC * DK + i;
     float *carry = p.carry + static_cast<size_t>(bh) * p.NC * NTILE * DK + (c / TW) * DK + i;
     float R = p.dhT ? p.dhT[e] : 0.f;
-    for (int u0 = p.NC - 1; u0 >= 0; u0 -= kScanUnroll) {
-        float d[kScanUnroll], a[kScanUnroll], sn[kScanUnroll];
+    float d[kScanUnroll], a[kScanUnroll], sn[kScanUnroll];
+    auto fetch = [&](int u0) {
 #pragma unroll
         for (int j = 0; j < kScanUnroll; ++j) {
             if (u0 - j >= 0) {
@@ -302,16 +313,27 @@ __global__ void __launch_bounds__(256) bwd_adjoint_scan_kernel(BwdLaunch p) {
                 sn[j] = st[(u0 - j + 1) * kM];
             }
         }
+    };
+    fetch(p.NC - 1);
+    for (int u0 = p.NC - 1; u0 >= 0; u0 -= kScanUnroll) {
+        float dc[kScanUnroll], ac[kScanUnroll], sc[kScanUnroll];
+#pragma unroll
+        for (int j = 0; j < kScanUnroll; ++j) {
+            dc[j] = d[j];
+            ac[j] = a[j];
+            sc[j] = sn[j];
+        }
+        if (u0 - kScanUnroll >= 0) fetch(u0 - kScanUnroll);   // next group in flight
 #pragma unroll
         for (int j = 0; j < kScanUnroll; ++j) {
             const int u = u0 - j;
             if (u >= 0) {
                 buf[u * kM] = R;
-                float part = R * sn[j];
+                float part = R * sc[j];
 #pragma unroll
                 for (int m = 16; m > 0; m >>= 1) part += __shfl_xor_sync(0xffffffffu, part, m);
                 if (lane == 0) carry[static_cast<size_t>(u) * NTILE * DK] = part;
-                R = fmaf(a[j], R, d[j]);
+                R = fmaf(ac[j], R, dc[j]);
             }
         }
     }
@@ -615,13 +637,13 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdLaunch p) {
         }
     }
 
-    // phase 1: A = dO V^T, streaming the value columns
+    // phase 1: A = dO V^T, streaming the value columns; the next slice's loads
+    // are in flight while the current slice is multiplied
     float accA[4][4] = {};
-    for (int c0 = 0; c0 < DV; c0 += TW) {
-        __syncthreads();
-        {
-            constexpr int PV = BC * TW / NT;
-            float dov[PV], vv[PV];
+    {
+        constexpr int PV = BC * TW / NT;
+        float dov[PV], vv[PV];
+        auto fetch = [&](int c0) {
 #pragma unroll
             for (int m = 0; m < PV; ++m) {
                 const int e = tid + m * NT, t = e / TW, c = e % TW;
@@ -629,26 +651,31 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdLaunch p) {
                 dov[m] = t < n ? bf(p.d_o, off) : 0.f;
                 vv[m] = t < n ? bf(p.v, off) : 0.f;
             }
+        };
+        fetch(0);
+        for (int c0 = 0; c0 < DV; c0 += TW) {
+            __syncthreads();
 #pragma unroll
             for (int m = 0; m < PV; ++m) {
                 const int e = tid + m * NT, t = e / TW, c = e % TW;
                 sDo[t * LS + c] = dov[m];
                 sV[t * LS + c] = vv[m];
             }
-        }
-        __syncthreads();
+            __syncthreads();
+            if (c0 + TW < DV) fetch(c0 + TW);
 #pragma unroll 4
-        for (int c = 0; c < TW; ++c) {
-            float dr[4], vj[4];
+            for (int c = 0; c < TW; ++c) {
+                float dr[4], vj[4];
 #pragma unroll
-            for (int a = 0; a < 4; ++a) {
-                dr[a] = sDo[(4 * ty + a) * LS + c];
-                vj[a] = sV[(tx + 16 * a) * LS + c];
+                for (int a = 0; a < 4; ++a) {
+                    dr[a] = sDo[(4 * ty + a) * LS + c];
+                    vj[a] = sV[(tx + 16 * a) * LS + c];
+                }
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) accA[a][b] = fmaf(dr[a], vj[b], accA[a][b]);
             }
-#pragma unroll
-            for (int a = 0; a < 4; ++a)
-#pragma unroll
-                for (int b = 0; b < 4; ++b) accA[a][b] = fmaf(dr[a], vj[b], accA[a][b]);
         }
     }
 #pragma unroll
@@ -738,13 +765,12 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdLaunch p) {
     for (int a = 0; a < 4; ++a)
 #pragma unroll
         for (int b = 0; b < 4; ++b) sAM[(4 * ty + a) * LA + tx + 16 * b] = accA[a][b];
-    // phase 4: dV = M^T dO + the state term (bwd_inter), a slice of value columns at a time
-    for (int c0 = 0; c0 < DV; c0 += TW) {
-        __syncthreads();
-        float pvv[4][2];
-        {
-            constexpr int PV = BC * TW / NT;
-            float dov[PV];
+    // phase 4: dV = M^T dO + the state term (bwd_inter), a slice of value
+    // columns at a time, the next slice's loads in flight
+    {
+        constexpr int PV = BC * TW / NT;
+        float dov[PV], pvv[4][2];
+        auto fetch = [&](int c0) {
 #pragma unroll
             for (int m = 0; m < PV; ++m) {
                 const int e = tid + m * NT, t = e / TW, c = e % TW;
@@ -757,26 +783,36 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdLaunch p) {
                 pvv[a][0] = j < n ? p.pv[off] : 0.f;
                 pvv[a][1] = j < n ? p.pv[off + 16] : 0.f;
             }
+        };
+        fetch(0);
+        for (int c0 = 0; c0 < DV; c0 += TW) {
+            __syncthreads();
 #pragma unroll
             for (int m = 0; m < PV; ++m) {
                 const int e = tid + m * NT;
                 sDo[(e / TW) * LS + e % TW] = dov[m];
             }
-        }
-        __syncthreads();
+            float acc[4][2];
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
-            const int j = 4 * ty + a;
-            float acc0 = pvv[a][0], acc1 = pvv[a][1];
-            for (int x = j; x < BC; ++x) {
-                const float mxj = sAM[x * LA + j];
-                acc0 = fmaf(mxj, sDo[x * LS + tx], acc0);
-                acc1 = fmaf(mxj, sDo[x * LS + tx + 16], acc1);
+            for (int a = 0; a < 4; ++a) {
+                acc[a][0] = pvv[a][0];
+                acc[a][1] = pvv[a][1];
             }
-            if (j < n) {
-                const size_t off = rv + static_cast<size_t>(j) * DV + c0;
-                p.gv[off + tx] = __float2bfloat16_rn(acc0);
-                p.gv[off + tx + 16] = __float2bfloat16_rn(acc1);
+            __syncthreads();
+            if (c0 + TW < DV) fetch(c0 + TW);
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const int j = 4 * ty + a;
+                for (int x = j; x < BC; ++x) {
+                    const float mxj = sAM[x * LA + j];
+                    acc[a][0] = fmaf(mxj, sDo[x * LS + tx], acc[a][0]);
+                    acc[a][1] = fmaf(mxj, sDo[x * LS + tx + 16], acc[a][1]);
+                }
+                if (j < n) {
+                    const size_t off = rv + static_cast<size_t>(j) * DV + c0;
+                    p.gv[off + tx] = __float2bfloat16_rn(acc[a][0]);
+                    p.gv[off + tx + 16] = __float2bfloat16_rn(acc[a][1]);
+                }
             }
         }
     }
