@@ -117,6 +117,8 @@ __device__ __forceinline__ void load_prefix(float *sG, const float *__restrict__
 //    bits) because these sums accumulate over the whole sequence; V and dO
 //    are bf16 inputs, exact.  Operand tiles are 128-byte swizzled, 64
 //    channels (or value columns) per block, read MN-major.
+constexpr int kSumThreads = 256;
+
 template <int DK, int DV>
 struct SumSmem {
     static constexpr uint32_t kBlk = BC * 128;              // one 64-column block of a tile
@@ -130,7 +132,8 @@ struct SumSmem {
 };
 
 template <int DK, int DV>
-__global__ void __launch_bounds__(128, 1) bwd_sums_kernel(BwdLaunch p) {
+__global__ void __launch_bounds__(kSumThreads, 2) bwd_sums_kernel(BwdLaunch p) {
+    constexpr int NTS = kSumThreads;
     using L = SumSmem<DK, DV>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(
@@ -153,29 +156,29 @@ __global__ void __launch_bounds__(128, 1) bwd_sums_kernel(BwdLaunch p) {
     // issue the key-side and value-side loads first; they land during the prefix sums
     const __nv_bfloat16 *asrc = which ? p.q : p.k;
     const __nv_bfloat16 *bsrc = which ? p.d_o : p.v;
-    constexpr int APER = BC * 64 / 128;           // channel pairs per thread
-    constexpr int BPER = BC * DV / 8 / 128;       // 16-byte value groups per thread
+    constexpr int APER = BC * 64 / NTS;           // channel pairs per thread
+    constexpr int BPER = BC * DV / 8 / NTS;       // 16-byte value groups per thread
     uint32_t araw[APER];
     uint4 braw[BPER];
 #pragma unroll
     for (int m = 0; m < APER; ++m) {
-        const int e = tid + m * 128, t = e >> 6, i = (e & 63) * 2;
+        const int e = tid + m * NTS, t = e >> 6, i = (e & 63) * 2;
         araw[m] = (t < n && i < DK)
                       ? *reinterpret_cast<const uint32_t *>(asrc + rk + static_cast<size_t>(t) * DK + i)
                       : 0u;
     }
 #pragma unroll
     for (int m = 0; m < BPER; ++m) {
-        const int e = tid + m * 128, t = e / (DV / 8), c = (e % (DV / 8)) * 8;
+        const int e = tid + m * NTS, t = e / (DV / 8), c = (e % (DV / 8)) * 8;
         braw[m] = t < n ? *reinterpret_cast<const uint4 *>(bsrc + rv + static_cast<size_t>(t) * DV + c)
                         : make_uint4(0u, 0u, 0u, 0u);
     }
-    load_prefix<DK, DK, 128>(sG, p.log_alpha + rk, n);
+    load_prefix<DK, DK, NTS>(sG, p.log_alpha + rk, n);
 
     // A: rows = tokens, columns = key channels, scaled and split
 #pragma unroll
     for (int m = 0; m < APER; ++m) {
-        const int e = tid + m * 128, t = e >> 6, i = (e & 63) * 2;
+        const int e = tid + m * NTS, t = e >> 6, i = (e & 63) * 2;
         uint32_t hi = 0u, lo = 0u;
         if (t < n && i < DK) {
             const float f0 = __uint_as_float(araw[m] << 16), f1 = __uint_as_float(araw[m] & 0xffff0000u);
@@ -191,7 +194,7 @@ __global__ void __launch_bounds__(128, 1) bwd_sums_kernel(BwdLaunch p) {
     // B: rows = tokens, columns = value columns (bf16 copied as is)
 #pragma unroll
     for (int m = 0; m < BPER; ++m) {
-        const int e = tid + m * 128, t = e / (DV / 8), c = (e % (DV / 8)) * 8;
+        const int e = tid + m * NTS, t = e / (DV / 8), c = (e % (DV / 8)) * 8;
         *reinterpret_cast<uint4 *>(sB + sw128_offset(t, c, L::kBlk)) = braw[m];
     }
     fence_proxy_async_smem();
@@ -213,15 +216,17 @@ __global__ void __launch_bounds__(128, 1) bwd_sums_kernel(BwdLaunch p) {
     const bool ok = mbar_wait_bounded(bar, 0, p.status);
     tc_fence_after();
 
-    // epilogue: thread = key channel = TMEM lane; each 32-column group of a
-    // row is one 128-byte line of the scratch
-    const int i = tid;
+    // epilogue: thread = key channel = TMEM lane (32 (warp % 4) + lane); warps
+    // 0-3 store the first half of the value columns, warps 4-7 the second.
+    // Each 32-column group of a row is one 128-byte line of the scratch.
+    const int i = 32 * (warp & 3) + (tid & 31);
     const float mult = which ? p.scale : 1.f;
     const int slots = which ? p.NC : p.NC + 1;
     float *dst = (which ? p.adjoints : p.states) + slot_index<DK, DV>(bh, i < DK ? i : 0, 0, u, slots);
-    const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    const int cbeg = warp < 4 ? 0 : DV / 2, cend = warp < 4 ? DV / 2 : DV;
 #pragma unroll 1
-    for (int c0 = 0; c0 < DV; c0 += 32) {
+    for (int c0 = cbeg; c0 < cend; c0 += 32) {
         uint32_t r[32];
         tmem_ld32(taddr + c0, r);
         tmem_wait_ld();
@@ -234,7 +239,7 @@ __global__ void __launch_bounds__(128, 1) bwd_sums_kernel(BwdLaunch p) {
                                 __uint_as_float(r[j + 2]) * mult, __uint_as_float(r[j + 3]) * mult);
         }
     }
-    if (which == 0 && i < DK)
+    if (which == 0 && warp < 4 && i < DK)
         p.decay[(static_cast<size_t>(bh) * p.NC + u) * DK + i] = exp2f(sG[(BC - 1) * DK + i]);
     tc_fence_before();
     __syncthreads();
@@ -426,7 +431,7 @@ __global__ void __launch_bounds__(kInterThreads, 1) bwd_inter_kernel(BwdLaunch p
         const int cb = h * SLAB;
         // S_u and R_u rows (128, zero past dk) x 128 value columns -> bf16 pairs;
         // batches of 8 float4 per matrix in flight per thread
-        constexpr int SPER = 128 * SLAB / 4 / NTI, SB = 8;
+        constexpr int SPER = 128 * SLAB / 4 / NTI, SB = SPER;
 #pragma unroll 1
         for (int mb = 0; mb < SPER; mb += SB) {
             float4 sv[SB], rr[SB];
@@ -845,7 +850,7 @@ int launch_bwd_dims(const BwdLaunch &p, cudaStream_t stream) {
                                  static_cast<int>(grad_bytes));
     if (e != cudaSuccess) return static_cast<int>(e);
     const unsigned scan_blocks = static_cast<unsigned>(static_cast<size_t>(p.BH) * DK * DV / 256);
-    bwd_sums_kernel<DK, DV><<<dim3(p.NC, p.BH, 2), 128, sum_bytes, stream>>>(p);
+    bwd_sums_kernel<DK, DV><<<dim3(p.NC, p.BH, 2), kSumThreads, sum_bytes, stream>>>(p);
     bwd_state_scan_kernel<DK, DV><<<scan_blocks, 256, 0, stream>>>(p);
     bwd_adjoint_scan_kernel<DK, DV><<<scan_blocks, 256, 0, stream>>>(p);
     bwd_inter_kernel<DK, DV><<<dim3(p.NC, p.BH), kInterThreads, inter_bytes, stream>>>(p);
