@@ -627,7 +627,9 @@ bool bwd_layout(int B, int H, int T, int dk, int dv, size_t *states, size_t *adj
     *adjoints = al(sizeof(float) * static_cast<size_t>(BH) * NC * dk * dv);
     *carry = al(sizeof(float) * static_cast<size_t>(BH) * NC * gla::bwd_value_tiles(dv) * dk);
     *decay = al(sizeof(float) * static_cast<size_t>(BH) * NC * dk);
-    if (partials) *partials = al(sizeof(float) * static_cast<size_t>(BH) * T * (2 * dk + dv));
+    if (partials)
+        *partials = al(sizeof(float) * static_cast<size_t>(BH) * T * (2 * dk + dv)) +
+                    al(static_cast<size_t>(BH) * NC);   // + per-chunk path flags
     return NC <= 0x7fffffffLL;
 }
 
@@ -647,7 +649,7 @@ int gla_chunk_bwd_plan(int B, int H, int T, int dk, int dv, int *chunk, int *lau
     size_t a = 0, b = 0, c = 0, d = 0, e = 0;
     if (!bwd_layout(B, H, T, dk, dv, &a, &b, &c, &d, &e)) return GLA_ERR_ARG;
     if (chunk) *chunk = gla::bwd_chunk_tokens();
-    if (launches) *launches = 5;
+    if (launches) *launches = 6;
     if (scratch_bytes) *scratch_bytes = static_cast<unsigned long>(a + b + c + d + e);
     return GLA_OK;
 }
@@ -704,6 +706,9 @@ int gla_chunk_bwd_ex(const void *q, const void *k, const void *v, const float *l
     p.pq = reinterpret_cast<float *>(ws + st_b + adj_b + car_b + dec_b);
     p.pk = p.pq + static_cast<size_t>(B) * H * T * dk;
     p.pv = p.pk + static_cast<size_t>(B) * H * T * dk;
+    p.wide = reinterpret_cast<unsigned char *>(
+        ws + st_b + adj_b + car_b + dec_b +
+        ((sizeof(float) * static_cast<size_t>(B) * H * T * (2 * dk + dv) + 255) & ~static_cast<size_t>(255)));
     p.status = dev->status;
     p.scale = scale;
     p.BH = B * H;

@@ -556,7 +556,311 @@ __global__ void __launch_bounds__(kInterThreads, 1) bwd_inter_kernel(BwdLaunch p
 }
 
 // ---------------------------------------------------------------------------
-// 4. per-chunk gradients.  Thread (ty, tx) = (tid / 16, tid % 16) owns rows
+// 4. the in-chunk terms on the tensor cores, one CTA per (chunk, head), for
+//    every chunk whose decay span allows the reference split (the others are
+//    flagged for the CUDA-core kernel below).  With M = 64 rows per product
+//    (row m of an M = 64 accumulator sits in TMEM lane 32 (m / 16) + m % 16):
+//       A  = dO V^T                 (K = dv)      masked to j <= t
+//       M  = scale Qh Kh^T          (K = dk)      masked to j <= t
+//       dQ = A Kh,  dK = A^T Qh     (K = 64)      Qh = Q e^(Gamma - r), Kh = K e^(r - Gamma)
+//       dV = M^T dO                 (K = 64)
+//    Every fp32-valued operand (Qh, Kh, A, M) is a bf16 hi/lo pair; products
+//    of two pairs take the hi.hi, hi.lo and lo.hi terms.  The epilogue adds
+//    the state terms (bwd_inter), writes dq, dk, dv and takes dlog_alpha.
+constexpr int kIntraThreads = 256;
+
+template <int DK, int DV>
+struct IntraSmem {
+    static constexpr uint32_t kBlk = BC * 128;              // one 64-column block of a 64-row tile
+    static constexpr uint32_t kQh = 0, kQl = kQh + (DK / 64) * kBlk;
+    static constexpr uint32_t kKh = kQl + (DK / 64) * kBlk, kKl = kKh + (DK / 64) * kBlk;
+    static constexpr uint32_t kDo = kKl + (DK / 64) * kBlk, kV = kDo + (DV / 64) * kBlk;
+    static constexpr uint32_t kAh = kV + (DV / 64) * kBlk, kAl = kAh + kBlk;
+    static constexpr uint32_t kMh = kAl + kBlk, kMl = kMh + kBlk;
+    static constexpr int LG = DK + 4;                       // fp32 prefix sums [BC][LG]
+    static constexpr uint32_t kG = kMl + kBlk;
+    static constexpr uint32_t kRef = kG + BC * LG * 4;      // reference, Gamma_C, carry: 3 x DK
+    static constexpr uint32_t kBar = kRef + 3 * DK * 4;
+    static constexpr uint32_t kSlot = kBar + 16;
+    static constexpr uint32_t kBytes = kSlot + 16 + 1024;
+    static constexpr int LP = DK + 1;                       // q dq - k dk, fp32 [BC][LP], over Qh..Kl
+    // TMEM columns used: A, M / dV first half [0, 128), dQ, dK, then dV's second half
+    static constexpr uint32_t kUsed = 128 + 2 * DK + (DV > 128 ? 128 : 0);
+    static constexpr uint32_t kCols = kUsed <= 256 ? 256 : 512;
+    static_assert(BC * LP * 4 <= 4 * (DK / 64) * kBlk, "P fits over the q/k tiles");
+};
+
+// Columns: A [0, 64), M [64, 128) first; then dV over [0, 128) (+ [2 dk + 128, ...) for
+// its second half), dQ [128, 128 + dk), dK [128 + dk, 128 + 2 dk).
+template <int DK, int DV>
+__global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p) {
+    using L = IntraSmem<DK, DV>;
+    constexpr int NTI = kIntraThreads, LG = L::LG, LP = L::LP;
+    constexpr int NTILE = DV / TW;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    float *sG = reinterpret_cast<float *>(sm + L::kG);
+    float *sRef = reinterpret_cast<float *>(sm + L::kRef), *sGC = sRef + DK, *sCarry = sGC + DK;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::kBar);
+    uint32_t *slot = reinterpret_cast<uint32_t *>(sm + L::kSlot);
+    const int u = blockIdx.x, bh = blockIdx.y;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int t0 = u * BC, n = min(BC, p.T - t0);
+    const size_t rk = (static_cast<size_t>(bh) * p.T + t0) * DK;
+    const size_t rv = (static_cast<size_t>(bh) * p.T + t0) * DV;
+    const float s = p.scale;
+
+    // loads first: q, k pairs and dO, V 16-byte groups; then the prefix sums
+    constexpr int QPER = BC * DK / 2 / NTI, VPER = BC * DV / 8 / NTI;
+    uint32_t qr[QPER], kr[QPER];
+    uint4 dor[VPER], vr[VPER];
+#pragma unroll
+    for (int m = 0; m < QPER; ++m) {
+        const int e = (tid + m * NTI) * 2, t = e / DK;
+        qr[m] = t < n ? *reinterpret_cast<const uint32_t *>(p.q + rk + e) : 0u;
+        kr[m] = t < n ? *reinterpret_cast<const uint32_t *>(p.k + rk + e) : 0u;
+    }
+#pragma unroll
+    for (int m = 0; m < VPER; ++m) {
+        const int e = tid + m * NTI, t = e / (DV / 8), c = (e % (DV / 8)) * 8;
+        const size_t off = rv + static_cast<size_t>(t) * DV + c;
+        dor[m] = t < n ? *reinterpret_cast<const uint4 *>(p.d_o + off) : make_uint4(0u, 0u, 0u, 0u);
+        vr[m] = t < n ? *reinterpret_cast<const uint4 *>(p.v + off) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    load_prefix<DK, LG, NTI>(sG, p.log_alpha + rk, n);
+    int wide = 0;
+    if (tid < DK) {
+        const float g0 = sG[tid], gl = sG[(BC - 1) * LG + tid];
+        sRef[tid] = 0.5f * (g0 + gl);
+        sGC[tid] = gl;
+        wide = (g0 - gl) > kMaxSpan;
+        float c = 0.f;
+        for (int x = 0; x < NTILE; ++x)
+            c += p.carry[((static_cast<size_t>(bh) * p.NC + u) * NTILE + x) * DK + tid];
+        sCarry[tid] = c;
+    }
+    const bool exact = __syncthreads_or(wide) || p.force_exact;
+    if (tid == 0) p.wide[static_cast<size_t>(bh) * p.NC + u] = exact ? 1 : 0;
+    if (exact) return;   // the CUDA-core kernel takes this chunk
+
+    if (warp == 0) tmem_alloc(slot, L::kCols);
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    // Qh, Kh (hi/lo) as [t][i] tiles; dO, V as [t][c] tiles
+#pragma unroll
+    for (int m = 0; m < QPER; ++m) {
+        const int e = (tid + m * NTI) * 2, t = e / DK, i = e % DK;
+        const float d0 = sG[t * LG + i] - sRef[i], d1 = sG[t * LG + i + 1] - sRef[i + 1];
+        const float q0 = __uint_as_float(qr[m] << 16), q1 = __uint_as_float(qr[m] & 0xffff0000u);
+        const float k0 = __uint_as_float(kr[m] << 16), k1 = __uint_as_float(kr[m] & 0xffff0000u);
+        uint32_t hi, lo;
+        const uint32_t off = sw128_offset(t, i, L::kBlk);
+        split_pair(q0 * exp2f(d0), q1 * exp2f(d1), hi, lo);
+        *reinterpret_cast<uint32_t *>(sm + L::kQh + off) = hi;
+        *reinterpret_cast<uint32_t *>(sm + L::kQl + off) = lo;
+        split_pair(k0 * exp2f(-d0), k1 * exp2f(-d1), hi, lo);
+        *reinterpret_cast<uint32_t *>(sm + L::kKh + off) = hi;
+        *reinterpret_cast<uint32_t *>(sm + L::kKl + off) = lo;
+    }
+#pragma unroll
+    for (int m = 0; m < VPER; ++m) {
+        const int e = tid + m * NTI, t = e / (DV / 8), c = (e % (DV / 8)) * 8;
+        const uint32_t off = sw128_offset(t, c, L::kBlk);
+        *reinterpret_cast<uint4 *>(sm + L::kDo + off) = dor[m];
+        *reinterpret_cast<uint4 *>(sm + L::kV + off) = vr[m];
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *slot;
+    const uint32_t a0 = smem_u32(sm);
+    // group 1: A and M
+    if (tid == 0) {
+        constexpr uint32_t id_a = idesc_bf16(64, BC, false, false);
+#pragma unroll
+        for (int kk = 0; kk < DV / 16; ++kk) {
+            const uint32_t o = (kk >> 2) * L::kBlk + (kk & 3) * 32;
+            mma_bf16_ss(tmem, sw128_desc(a0 + L::kDo + o, 16, 1024), sw128_desc(a0 + L::kV + o, 16, 1024),
+                        id_a, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < DK / 16; ++kk) {
+            const uint32_t o = (kk >> 2) * L::kBlk + (kk & 3) * 32;
+            const uint64_t qh = sw128_desc(a0 + L::kQh + o, 16, 1024), ql = sw128_desc(a0 + L::kQl + o, 16, 1024);
+            const uint64_t kh = sw128_desc(a0 + L::kKh + o, 16, 1024), kl = sw128_desc(a0 + L::kKl + o, 16, 1024);
+            mma_bf16_ss(tmem + 64, qh, kh, id_a, kk > 0 ? 1u : 0u);
+            mma_bf16_ss(tmem + 64, qh, kl, id_a, 1u);
+            mma_bf16_ss(tmem + 64, ql, kh, id_a, 1u);
+        }
+        mma_commit(bar);
+    }
+    bool ok = mbar_wait_bounded(bar, 0, p.status);
+    tc_fence_after();
+
+    // epilogue 1: mask A and scale * M to j <= t, split into bf16 pairs, [t][j] tiles.
+    // Warp q (= warp % 4) holds rows 16 q .. 16 q + 15 in lanes 0-15; warps 0-3 take
+    // A, warps 4-7 take M.
+    {
+        const int q4 = warp & 3, t = 16 * q4 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
+        const int col = warp < 4 ? 0 : 64;
+        const float mult = warp < 4 ? 1.f : s;
+        uint8_t *th = sm + (warp < 4 ? L::kAh : L::kMh), *tl = sm + (warp < 4 ? L::kAl : L::kMl);
+#pragma unroll 1
+        for (int jb = 0; jb < BC; jb += 32) {
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_off + col + jb, r);
+            tmem_wait_ld();
+            if (lane < 16) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) {
+                    const int jj = jb + j;
+                    const float x0 = (jj <= t) ? __uint_as_float(r[j]) * mult : 0.f;
+                    const float x1 = (jj + 1 <= t) ? __uint_as_float(r[j + 1]) * mult : 0.f;
+                    uint32_t hi, lo;
+                    split_pair(x0, x1, hi, lo);
+                    const uint32_t off = sw128_offset(t, jj, L::kBlk);
+                    *reinterpret_cast<uint32_t *>(th + off) = hi;
+                    *reinterpret_cast<uint32_t *>(tl + off) = lo;
+                }
+            }
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // group 2: dQ, dK, dV
+    if (tid == 0) {
+        constexpr uint32_t id_q = idesc_bf16(64, DK, false, true);   // A [t][j] K-major, Kh [j][i] MN-major
+        constexpr uint32_t id_k = idesc_bf16(64, DK, true, true);    // A^T (MN-major), Qh [t][i] MN-major
+        constexpr int NV = DV > 128 ? 128 : DV;
+        constexpr uint32_t id_v = idesc_bf16(64, NV, true, true);    // M^T (MN-major), dO [t][c] MN-major
+#pragma unroll
+        for (int kk = 0; kk < BC / 16; ++kk) {
+            const uint32_t ok_ = (kk & 3) * 32;          // K-major step inside the 64-column block
+            const uint32_t om = kk * 2048;               // MN-major step: 16 rows
+            const uint64_t ah = sw128_desc(a0 + L::kAh + ok_, 16, 1024), al = sw128_desc(a0 + L::kAl + ok_, 16, 1024);
+            const uint64_t kh = sw128_desc(a0 + L::kKh + om, L::kBlk, 1024), kl = sw128_desc(a0 + L::kKl + om, L::kBlk, 1024);
+            mma_bf16_ss(tmem + 128, ah, kh, id_q, kk > 0 ? 1u : 0u);
+            mma_bf16_ss(tmem + 128, al, kh, id_q, 1u);
+            mma_bf16_ss(tmem + 128, ah, kl, id_q, 1u);
+            const uint64_t ath = sw128_desc(a0 + L::kAh + om, L::kBlk, 1024), atl = sw128_desc(a0 + L::kAl + om, L::kBlk, 1024);
+            const uint64_t qh = sw128_desc(a0 + L::kQh + om, L::kBlk, 1024), ql = sw128_desc(a0 + L::kQl + om, L::kBlk, 1024);
+            mma_bf16_ss(tmem + 128 + DK, ath, qh, id_k, kk > 0 ? 1u : 0u);
+            mma_bf16_ss(tmem + 128 + DK, atl, qh, id_k, 1u);
+            mma_bf16_ss(tmem + 128 + DK, ath, ql, id_k, 1u);
+            const uint64_t mth = sw128_desc(a0 + L::kMh + om, L::kBlk, 1024), mtl = sw128_desc(a0 + L::kMl + om, L::kBlk, 1024);
+#pragma unroll
+            for (int hv = 0; hv < DV / NV; ++hv) {
+                const uint32_t dcol = hv == 0 ? 0u : 128u + 2u * DK;
+                const uint64_t db = sw128_desc(a0 + L::kDo + om + hv * 2 * L::kBlk, L::kBlk, 1024);
+                mma_bf16_ss(tmem + dcol, mth, db, id_v, kk > 0 ? 1u : 0u);
+                mma_bf16_ss(tmem + dcol, mtl, db, id_v, 1u);
+            }
+        }
+        mma_commit(bar);
+    }
+    ok = mbar_wait_bounded(bar, 1, p.status) && ok;
+    tc_fence_after();
+    __syncthreads();   // every thread is past the tile reads; P may overwrite the q/k tiles
+
+    // epilogue 2.  Warps 0-3: row t of dQ and dK (lanes 0-15), q dq - k dk into P.
+    // Warps 4-7: row j of dV.
+    float *sP = reinterpret_cast<float *>(sm + L::kQh);
+    {
+        const int q4 = warp & 3, t = 16 * q4 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
+        const bool row_ok = ok && lane < 16 && t < n;
+        if (warp < 4) {
+            const float *gr = sG + t * LG;
+#pragma unroll 1
+            for (int ib = 0; ib < DK; ib += 32) {
+                uint32_t rq[32], rkk[32];
+                tmem_ld32(tmem + lane_off + 128 + ib, rq);
+                tmem_ld32(tmem + lane_off + 128 + DK + ib, rkk);
+                tmem_wait_ld();
+                if (lane < 16) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        const int i = ib + j;
+                        float pr[4] = {0.f, 0.f, 0.f, 0.f};
+                        if (row_ok) {
+                            const size_t off = rk + static_cast<size_t>(t) * DK + i;
+                            const float4 pq4 = *reinterpret_cast<const float4 *>(p.pq + off);
+                            const float4 pk4 = *reinterpret_cast<const float4 *>(p.pk + off);
+                            const uint2 qv = *reinterpret_cast<const uint2 *>(p.q + off);
+                            const uint2 kv = *reinterpret_cast<const uint2 *>(p.k + off);
+                            const float pqa[4] = {pq4.x, pq4.y, pq4.z, pq4.w};
+                            const float pka[4] = {pk4.x, pk4.y, pk4.z, pk4.w};
+                            const float qa[4] = {__uint_as_float(qv.x << 16), __uint_as_float(qv.x & 0xffff0000u),
+                                                 __uint_as_float(qv.y << 16), __uint_as_float(qv.y & 0xffff0000u)};
+                            const float ka[4] = {__uint_as_float(kv.x << 16), __uint_as_float(kv.x & 0xffff0000u),
+                                                 __uint_as_float(kv.y << 16), __uint_as_float(kv.y & 0xffff0000u)};
+                            uint32_t dqw[2], dkw[2];
+#pragma unroll
+                            for (int h = 0; h < 4; h += 2) {
+                                float dqv[2], dkv[2];
+#pragma unroll
+                                for (int x = 0; x < 2; ++x) {
+                                    const float d = gr[i + h + x] - sRef[i + h + x];
+                                    dqv[x] = s * exp2f(d) * __uint_as_float(rq[j + h + x]) + pqa[h + x];
+                                    dkv[x] = s * exp2f(-d) * __uint_as_float(rkk[j + h + x]) + pka[h + x];
+                                    pr[h + x] = qa[h + x] * dqv[x] - ka[h + x] * dkv[x];
+                                }
+                                dqw[h / 2] = pack_bf16x2(dqv[0], dqv[1]);
+                                dkw[h / 2] = pack_bf16x2(dkv[0], dkv[1]);
+                            }
+                            *reinterpret_cast<uint2 *>(p.gq + off) = make_uint2(dqw[0], dqw[1]);
+                            *reinterpret_cast<uint2 *>(p.gk + off) = make_uint2(dkw[0], dkw[1]);
+                        }
+#pragma unroll
+                        for (int x = 0; x < 4; ++x) sP[t * LP + i + x] = pr[x];
+                    }
+                }
+            }
+        } else {
+#pragma unroll 1
+            for (int cb = 0; cb < DV; cb += 32) {
+                const uint32_t dcol = cb < 128 ? static_cast<uint32_t>(cb) : 128u + 2u * DK + (cb - 128);
+                uint32_t rv_[32];
+                tmem_ld32(tmem + lane_off + dcol, rv_);
+                tmem_wait_ld();
+                if (row_ok) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        const size_t off = rv + static_cast<size_t>(t) * DV + cb + j;
+                        const float4 pv4 = *reinterpret_cast<const float4 *>(p.pv + off);
+                        const uint32_t w0 = pack_bf16x2(__uint_as_float(rv_[j]) + pv4.x,
+                                                        __uint_as_float(rv_[j + 1]) + pv4.y);
+                        const uint32_t w1 = pack_bf16x2(__uint_as_float(rv_[j + 2]) + pv4.z,
+                                                        __uint_as_float(rv_[j + 3]) + pv4.w);
+                        *reinterpret_cast<uint2 *>(p.gv + off) = make_uint2(w0, w1);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, L::kCols);
+    // dlog_alpha = carry + reverse in-chunk sum of q dq - k dk
+    if (tid < DK) {
+        float acc = sCarry[tid];
+        for (int t = n - 1; t >= 0; --t) {
+            acc += sP[t * LP + tid];
+            p.ga[rk + static_cast<size_t>(t) * DK + tid] = acc;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// 5. per-chunk gradients on CUDA cores, for the chunks the tensor-core kernel
+//    leaves (decay span beyond the reference split, or force_exact).  Thread (ty, tx) = (tid / 16, tid % 16) owns rows
 //    4 ty .. 4 ty + 3 and columns tx, tx + 16, ... of every C x C, C x dk and
 //    C x 32 block it computes.
 template <int DK>
@@ -584,6 +888,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdLaunch p) {
     float *sRef = smem + L::kRef, *sGC = smem + L::kGC, *sCarry = smem + L::kCarry;
 
     const int u = blockIdx.x, bh = blockIdx.y;
+    if (!p.wide[static_cast<size_t>(bh) * p.NC + u]) return;   // done by the tensor-core kernel
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
     const int t0 = u * BC, n = min(BC, p.T - t0);
     const size_t rk = (static_cast<size_t>(bh) * p.T + t0) * DK;   // first row, key tensors
@@ -616,6 +921,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdLaunch p) {
         sCarry[tid] = c;
     }
     const bool exact = __syncthreads_or(wide) || p.force_exact;
+    if (!exact) return;   // done by the tensor-core kernel
 
     // q and k: rescaled around the reference (fast path) or raw (exact path)
     {
@@ -837,9 +1143,14 @@ int launch_bwd_dims(const BwdLaunch &p, cudaStream_t stream) {
     const size_t sum_bytes = SumSmem<DK, DV>::kBytes;
     const size_t grad_bytes = GradSmem<DK>::kBytes;
     const size_t inter_bytes = InterSmem<DK, DV>::kBytes;
+    const size_t intra_bytes = IntraSmem<DK, DV>::kBytes;
     cudaError_t e = cudaFuncSetAttribute(bwd_sums_kernel<DK, DV>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(sum_bytes));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(bwd_intra_kernel<DK, DV>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(intra_bytes));
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(bwd_inter_kernel<DK, DV>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -854,6 +1165,7 @@ int launch_bwd_dims(const BwdLaunch &p, cudaStream_t stream) {
     bwd_state_scan_kernel<DK, DV><<<scan_blocks, 256, 0, stream>>>(p);
     bwd_adjoint_scan_kernel<DK, DV><<<scan_blocks, 256, 0, stream>>>(p);
     bwd_inter_kernel<DK, DV><<<dim3(p.NC, p.BH), kInterThreads, inter_bytes, stream>>>(p);
+    bwd_intra_kernel<DK, DV><<<dim3(p.NC, p.BH), kIntraThreads, intra_bytes, stream>>>(p);
     bwd_grads_kernel<DK, DV><<<dim3(p.NC, p.BH), NT, grad_bytes, stream>>>(p);
     return static_cast<int>(cudaGetLastError());
 }

@@ -97,6 +97,7 @@ struct BwdLaunch {
     float *decay;                            // scratch [BH, NC, dk]: e^Gamma_C per chunk
     float *pq, *pk;                          // scratch [BH, T, dk]: state terms of dq, dk
     float *pv;                               // scratch [BH, T, dv]: state term of dv
+    unsigned char *wide;                     // scratch [BH, NC]: 1 = chunk left to the CUDA-core kernel
     unsigned int *status;                    // device status word (bounded waits)
     float scale;
     int BH, T, NC, dk, dv;
@@ -107,7 +108,7 @@ struct BwdLaunch {
 int bwd_chunk_tokens();
 int bwd_value_tiles(int dv);
 
-// Enqueues the five backward kernels; returns a cudaError_t value.
+// Enqueues the six backward kernels; returns a cudaError_t value.
 int launch_chunk_bwd(const BwdLaunch &p, cudaStream_t stream);
 
 }  // namespace gla
