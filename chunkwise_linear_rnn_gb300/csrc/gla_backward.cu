@@ -24,16 +24,17 @@
 // The log-gate carry is the gradient of the first token of the next chunk:
 // shifting log alpha there scales the state leaving chunk u row by row.
 //
-// Five launches:
+// Six launches:
 //   1. bwd_sums:  every chunk independently, on the tensor cores (tcgen05,
 //      TMEM accumulators): the state it adds from a zero start and the state
 //      gradient its outputs add, plus its total decay;
 //   2. bwd_state_scan:   S_u for u = 0 .. NC from those sums (elementwise);
 //   3. bwd_adjoint_scan: R_u, the log-gate carries rowsum(R_u * S_(u+1)), dh0;
 //   4. bwd_inter: every chunk's state terms of dq, dk, dv on the tensor cores;
-//   5. bwd_grads: one CTA per (chunk, head) adds the in-chunk terms (64 x 64
-//      score-sized products on CUDA cores in fp32) and writes dq, dk, dv and
-//      dlog_alpha.
+//   5. bwd_intra: every chunk's in-chunk terms on the tensor cores, plus the
+//      state terms, written as dq, dk, dv and dlog_alpha;
+//   6. bwd_grads: the same on CUDA cores in fp32, for the chunks that need
+//      exact decay factors (flagged by bwd_intra; the rest exit at once).
 // Inside a chunk the decay factor e^(Gamma_t - Gamma_j) (t >= j) is split
 // around a per-channel reference r = (Gamma_0 + Gamma_(C-1)) / 2, so both
 // halves stay within 2^+-60 when the chunk's decay spans at most 2^120; a
