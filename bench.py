@@ -260,6 +260,16 @@ def run_ours(args, rank, world, local_rank):
                 "steps": 0, "warmup": args.warmup, "note": "chunked forward skipped (--only decode)"}
     if args.only != "chunk":
         line["decode"] = decode_leg(args, world, rank, dev, gla, barrier, max_over_ranks, pk)
+    if args.only == "both" and not args.varlen and args.gate == "channel":
+        # the backward on the same workload, a secondary number on the same line
+        import argparse as _ap
+        bargs = _ap.Namespace(**vars(args))
+        bargs.steps, bargs.warmup, bargs.no_e2e = min(args.steps, 20), max(args.warmup, 3), True
+        b = bwd_leg(bargs, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_kind)
+        line["backward"] = {"metric": b["metric"], "value": b["value"], "unit": b["unit"],
+                            "ms_per_step": b["ms_per_step"], "steps": b["steps"],
+                            "workload": b["config"]["workload"], "roofline": b["roofline"],
+                            "gpu_launches": b["gpu_launches"], "clocks": b["clocks"]}
     return line
 
 

@@ -251,7 +251,8 @@ def gla_chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: 
                   force_exact: bool = False):
     """Gradients of L = sum <d_o, o> + <dhT, hT> through the chunked forward.
 
-    Inputs as for ``gla_chunk_fwd`` (per-channel gates ``[B,H,T,dk]``), with
+    Inputs as for ``gla_chunk_fwd`` (gates ``[B,H,T,dk]``, or ``[B,H,T]`` for one
+    gate per token and head; ``dlog_alpha`` then has the same shape), with
     ``d_o`` ``[B,H,T,dv]`` bf16 and ``dhT`` ``[B,H,dk,dv]`` fp32 or None (zero).
     Returns ``(dq, dk, dv, dlog_alpha, dh0)``: bf16, bf16, bf16, fp32, and fp32
     or None when ``need_dh0`` is False.  The states are recomputed on the GPU.
@@ -266,7 +267,8 @@ def gla_chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: 
     _need(q, "q", torch.bfloat16, (B, H, T, dk), dev)
     _need(k, "k", torch.bfloat16, (B, H, T, dk), dev)
     _need(v, "v", torch.bfloat16, (B, H, T, dv), dev)
-    _need(log_alpha, "log_alpha", torch.float32, (B, H, T, dk), dev)
+    per_head = log_alpha.dim() == 3
+    _need(log_alpha, "log_alpha", torch.float32, (B, H, T) if per_head else (B, H, T, dk), dev)
     _need(d_o, "d_o", torch.bfloat16, (B, H, T, dv), dev)
     if h0 is not None:
         _need(h0, "h0", torch.float32, (B, H, dk, dv), dev)
@@ -279,7 +281,7 @@ def gla_chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: 
     dvv = torch.empty_like(v)
     da = torch.empty_like(log_alpha)
     dh0 = torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev) if need_dh0 else None
-    opts = GlaChunkOptions(force_exact=1 if force_exact else 0)
+    opts = GlaChunkOptions(force_exact=1 if force_exact else 0, gate_per_head=1 if per_head else 0)
     ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
     with torch.cuda.device(dev):
         st = _lib.lib().gla_chunk_bwd_ex(
@@ -323,7 +325,7 @@ def gla_chunk(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: torc
               scale: float | None = None, h0: torch.Tensor | None = None):
     """Differentiable chunked GLA: ``(o, hT)`` with gradients through ``gla_chunk_bwd``.
 
-    Per-channel gates ``[B,H,T,dk]`` only.  The backward recomputes the states
+    Gates ``[B,H,T,dk]`` or ``[B,H,T]``.  The backward recomputes the states
     from the saved inputs; ``d_o`` is taken in bf16, ``dhT`` in fp32.
     """
     if scale is None:

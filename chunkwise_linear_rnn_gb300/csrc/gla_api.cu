@@ -672,16 +672,23 @@ int gla_chunk_bwd_ex(const void *q, const void *k, const void *v, const float *l
         return GLA_ERR_ARG;
     gla_chunk_options o_def = {};
     const gla_chunk_options &op = opts ? *opts : o_def;
-    if (op.gate_per_head != 0 || (op.force_exact != 0 && op.force_exact != 1)) return GLA_ERR_ARG;
+    if ((op.gate_per_head != 0 && op.gate_per_head != 1) ||
+        (op.force_exact != 0 && op.force_exact != 1))
+        return GLA_ERR_ARG;
     size_t st_b = 0, adj_b = 0, car_b = 0, dec_b = 0, par_b = 0;
     if (!bwd_layout(B, H, T, dk, dv, &st_b, &adj_b, &car_b, &dec_b, &par_b)) return GLA_ERR_ARG;
+    // one gate per head: the gate broadcast to every channel and its gradient, fp32 [BH, T, dk]
+    const size_t gate_b = op.gate_per_head
+                              ? ((sizeof(float) * static_cast<size_t>(B) * H * T * dk + 255) &
+                                 ~static_cast<size_t>(255))
+                              : 0;
 
     DeviceInfo *dev = nullptr;
     const int st = current_device(&dev);
     if (st != GLA_OK) return st;
     char *ws = nullptr;
-    if (cudaMallocAsync(reinterpret_cast<void **>(&ws), st_b + adj_b + car_b + dec_b + par_b,
-                        stream) !=
+    if (cudaMallocAsync(reinterpret_cast<void **>(&ws),
+                        st_b + adj_b + car_b + dec_b + par_b + 2 * gate_b, stream) !=
         cudaSuccess) {
         cudaGetLastError();
         return GLA_ERR_ALLOC;
@@ -717,7 +724,19 @@ int gla_chunk_bwd_ex(const void *q, const void *k, const void *v, const float *l
     p.dk = dk;
     p.dv = dv;
     p.force_exact = op.force_exact;
-    const int r = launch_chunk_bwd(p, stream) == 0 ? GLA_OK : GLA_ERR_LAUNCH;
+    int r = GLA_OK;
+    const long long rows = static_cast<long long>(B) * H * T;
+    if (op.gate_per_head) {
+        float *full = reinterpret_cast<float *>(ws + st_b + adj_b + car_b + dec_b + par_b);
+        float *gfull = reinterpret_cast<float *>(ws + st_b + adj_b + car_b + dec_b + par_b + gate_b);
+        if (launch_gate_broadcast(log_alpha, full, rows, dk, stream) != 0) r = GLA_ERR_LAUNCH;
+        p.log_alpha = full;
+        p.ga = gfull;
+    }
+    if (r == GLA_OK && launch_chunk_bwd(p, stream) != 0) r = GLA_ERR_LAUNCH;
+    if (r == GLA_OK && op.gate_per_head &&
+        launch_gate_sum(p.ga, grad_log_alpha, rows, dk, stream) != 0)
+        r = GLA_ERR_LAUNCH;
     cudaFreeAsync(ws, stream);
     return r;
 }

@@ -1139,6 +1139,35 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdLaunch p) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// One gate per token and head: the backward runs on the gate broadcast to
+// every key channel, and the head gate's gradient is the sum of the channel
+// gates' gradients (each channel's gate is the same input).
+template <int DK>
+__global__ void __launch_bounds__(256) bwd_gate_broadcast_kernel(const float *__restrict__ g,
+                                                                 float *__restrict__ full,
+                                                                 long long rows) {
+    const long long e = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;   // float4 index
+    if (e >= rows * (DK / 4)) return;
+    const float x = g[e / (DK / 4)];
+    reinterpret_cast<float4 *>(full)[e] = make_float4(x, x, x, x);
+}
+
+template <int DK>
+__global__ void __launch_bounds__(256) bwd_gate_sum_kernel(const float *__restrict__ full,
+                                                           float *__restrict__ g, long long rows) {
+    const long long r = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
+    if (r >= rows) return;
+    const float4 *src = reinterpret_cast<const float4 *>(full + r * DK);
+    float acc = 0.f;
+#pragma unroll 8
+    for (int m = 0; m < DK / 4; ++m) {
+        const float4 v = src[m];
+        acc += (v.x + v.y) + (v.z + v.w);
+    }
+    g[r] = acc;
+}
+
 template <int DK, int DV>
 int launch_bwd_dims(const BwdLaunch &p, cudaStream_t stream) {
     const size_t sum_bytes = SumSmem<DK, DV>::kBytes;
@@ -1175,6 +1204,21 @@ int launch_bwd_dims(const BwdLaunch &p, cudaStream_t stream) {
 
 int bwd_chunk_tokens() { return BC; }
 int bwd_value_tiles(int dv) { return dv / TW; }
+
+int launch_gate_broadcast(const float *g, float *full, long long rows, int dk, cudaStream_t stream) {
+    const long long n = rows * (dk / 4);
+    const unsigned blocks = static_cast<unsigned>((n + 255) / 256);
+    if (dk == 64) bwd_gate_broadcast_kernel<64><<<blocks, 256, 0, stream>>>(g, full, rows);
+    else bwd_gate_broadcast_kernel<128><<<blocks, 256, 0, stream>>>(g, full, rows);
+    return static_cast<int>(cudaGetLastError());
+}
+
+int launch_gate_sum(const float *full, float *g, long long rows, int dk, cudaStream_t stream) {
+    const unsigned blocks = static_cast<unsigned>((rows + 255) / 256);
+    if (dk == 64) bwd_gate_sum_kernel<64><<<blocks, 256, 0, stream>>>(full, g, rows);
+    else bwd_gate_sum_kernel<128><<<blocks, 256, 0, stream>>>(full, g, rows);
+    return static_cast<int>(cudaGetLastError());
+}
 
 int launch_chunk_bwd(const BwdLaunch &p, cudaStream_t stream) {
     switch (p.dk * 1000 + p.dv) {

@@ -108,6 +108,11 @@ struct BwdLaunch {
 int bwd_chunk_tokens();
 int bwd_value_tiles(int dv);
 
+// One gate per token and head: full[r][i] = g[r] for every key channel, and
+// g[r] = sum_i full[r][i] (rows = B * H * T).  Return cudaError_t values.
+int launch_gate_broadcast(const float *g, float *full, long long rows, int dk, cudaStream_t stream);
+int launch_gate_sum(const float *full, float *g, long long rows, int dk, cudaStream_t stream);
+
 // Enqueues the six backward kernels; returns a cudaError_t value.
 int launch_chunk_bwd(const BwdLaunch &p, cudaStream_t stream);
 

@@ -290,10 +290,13 @@ int gla_chunk_bwd(const void *q, const void *k, const void *v, const float *log_
                   float *grad_h0, int B, int H, int T, int dk, int dv, cudaStream_t stream);
 
 /*
- * gla_chunk_bwd with options: only `force_exact` applies (every chunk takes
- * each in-chunk decay factor as its own exponential, the path chunks whose
- * decay spans more than 2^120 always take); `gate_per_head` must be 0; the
- * other fields are ignored.  opts NULL = defaults.
+ * gla_chunk_bwd with options.  `force_exact`: every chunk takes each
+ * in-chunk decay factor as its own exponential (the path chunks whose decay
+ * spans more than 2^120 always take).  `gate_per_head` = 1: log_alpha and
+ * grad_log_alpha are fp32 [B, H, T], one gate per token and head used for
+ * every key channel; the gradient of a head gate is the sum of its channels'
+ * (two more launches and 2 * B * H * T * dk fp32 of scratch).  The other
+ * fields are ignored.  opts NULL = defaults.
  */
 int gla_chunk_bwd_ex(const void *q, const void *k, const void *v, const float *log_alpha,
                      float scale, const float *h0, const void *d_o, const float *dhT,

@@ -149,3 +149,33 @@ def test_argument_errors():
         gla.gla_chunk_bwd(q, k, v, a, d_o[..., :32].contiguous(), 0.1)
     with pytest.raises(TypeError):
         gla.gla_chunk_bwd(q, k, v, a, d_o.float(), 0.1)
+
+
+@pytest.mark.parametrize("dk,dv,T", [(64, 128, 300), (128, 256, 200), (128, 64, 65)])
+def test_one_gate_per_head(dk, dv, T):
+    """log_alpha [B,H,T]: one gate per token and head, used for every key channel.
+
+    The oracle runs on the gate broadcast over the channels; the head gate's
+    gradient is then the sum of the channel gates' gradients (chain rule)."""
+    q, k, v, a, s0, d_o, g = _inputs(1, 2, T, dk, dv, sigma_z=2.0, seed=11 + dk + T)
+    a1 = a[..., 0].contiguous()
+    a_full = a1[..., None].expand(-1, -1, -1, dk).contiguous()
+    scale = dk ** -0.5
+    got = _gpu(q, k, v, a1, s0, d_o, g, scale)
+    want = list(_oracle(q, k, v, a_full, s0, d_o, g, scale))
+    want[3] = want[3].sum(axis=-1)
+    assert got[3].shape == want[3].shape
+    _compare(got, want, f"gate per head dk={dk} dv={dv} T={T}")
+
+
+def test_differentiable_wrapper_with_one_gate_per_head():
+    q, k, v, a, s0, d_o, g = [None if t is None else t.to(DEV) for t in _inputs(1, 2, 130, 64, 64,
+                                                                               seed=12)]
+    a1 = a[..., 0].contiguous()
+    leaves = [t.clone().requires_grad_(True) for t in (q, k, v, a1, s0)]
+    o, hT = gla.gla_chunk(*leaves[:4], 0.125, leaves[4])
+    ((o.float() * d_o.float()).sum() + (hT * g).sum()).backward()
+    want = gla.gla_chunk_bwd(q, k, v, a1, d_o, 0.125, s0, g)
+    torch.cuda.synchronize()
+    for name, leaf, ref in zip(NAMES, leaves, want):
+        assert torch.equal(leaf.grad, ref), name
