@@ -24,7 +24,9 @@ GLA_ERR_ALLOC = 6
 GLA_ERR_SCRATCH = 7
 
 EXPORTED = ("gla_chunk_fwd", "gla_chunk_fwd_ex", "gla_chunk_fwd_plan", "gla_chunk_fwd_noalloc",
-            "gla_chunk_fwd_host", "gla_recurrent_step", "gla_status_string",
+            "gla_chunk_fwd_host", "gla_chunk_fwd_varlen", "gla_chunk_fwd_varlen_ex",
+            "gla_chunk_fwd_varlen_plan", "gla_chunk_bwd", "gla_chunk_bwd_ex",
+            "gla_chunk_bwd_plan", "gla_recurrent_step", "gla_status_string",
             "gla_last_device_status", "gla_version")
 
 

@@ -190,3 +190,48 @@ def test_python_binding_rejects_cpu_tensors():
     q = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         gla.gla_chunk_fwd(q, q, q, torch.zeros(1, 1, 4, 64))
+
+
+def _bwd(lib, **kw):
+    """gla_chunk_bwd_ex with fake aligned pointers; keyword overrides."""
+    a = dict(q=P, k=P, v=P, a=P, scale=0.125, h0=None, d_o=P, dhT=None, gq=P, gk=P, gv=P, ga=P,
+             gh0=None, B=1, H=1, T=16, dk=64, dv=64, opts=None)
+    a.update(kw)
+    return lib.gla_chunk_bwd_ex(a["q"], a["k"], a["v"], a["a"], a["scale"], a["h0"], a["d_o"],
+                                a["dhT"], a["gq"], a["gk"], a["gv"], a["ga"], a["gh0"], a["B"],
+                                a["H"], a["T"], a["dk"], a["dv"], a["opts"], None)
+
+
+@pytest.mark.parametrize("field", ["q", "k", "v", "a", "d_o", "gq", "gk", "gv", "ga"])
+def test_backward_rejects_null(lib, field):
+    assert _bwd(lib, **{field: None}) == _lib.GLA_ERR_ARG
+
+
+def test_backward_validates_on_the_host(lib):
+    assert _bwd(lib, T=0) == _lib.GLA_ERR_ARG
+    assert _bwd(lib, B=70000) == _lib.GLA_ERR_ARG            # B * H beyond the grid's y extent
+    assert _bwd(lib, dk=96) == _lib.GLA_ERR_SHAPE
+    assert _bwd(lib, dv=32) == _lib.GLA_ERR_SHAPE
+    assert _bwd(lib, q=P + 2) == _lib.GLA_ERR_ARG            # 16-byte alignment
+    assert _bwd(lib, gh0=P + 4) == _lib.GLA_ERR_ARG
+    assert _bwd(lib, opts=ctypes.byref(_lib.GlaChunkOptions(gate_per_head=2))) == _lib.GLA_ERR_ARG
+    assert _bwd(lib, opts=ctypes.byref(_lib.GlaChunkOptions(force_exact=3))) == _lib.GLA_ERR_ARG
+
+
+def test_backward_plan(lib):
+    import chunkwise_linear_rnn_gb300 as gla
+    p = gla.gla_chunk_bwd_plan(2, 16, 32768, 128, 256)
+    assert p["chunk"] == 64 and p["launches"] == 6
+    NC, BH = 512, 32
+    # chunk states (NC + 1 slots) and state gradients (NC slots), fp32 dk x dv each
+    assert p["scratch_bytes"] >= 4 * BH * (2 * NC + 1) * 128 * 256
+    with pytest.raises(gla.GlaError):
+        gla.gla_chunk_bwd_plan(1, 1, 0, 64, 64)
+
+
+def test_backward_without_gpu_reports_device_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _bwd(lib) == _lib.GLA_ERR_DEVICE
+    assert _bwd(lib, opts=ctypes.byref(_lib.GlaChunkOptions(gate_per_head=1))) == _lib.GLA_ERR_DEVICE
