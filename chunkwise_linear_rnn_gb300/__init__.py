@@ -24,7 +24,8 @@ from . import _lib
 from ._lib import GlaChunkOptions, GlaError, status_string  # noqa: F401
 
 __all__ = ["gla_chunk_fwd", "gla_chunk_fwd_varlen", "gla_chunk_fwd_varlen_plan",
-           "gla_chunk_fwd_plan", "gla_chunk_bwd", "gla_chunk_bwd_plan", "gla_chunk",
+           "gla_chunk_fwd_plan", "gla_chunk_bwd", "gla_chunk_bwd_plan", "gla_chunk_bwd_varlen",
+           "gla_chunk",
            "gla_recurrent_step", "gla_last_device_status", "GlaError", "status_string",
            "library_path"]
 
@@ -289,6 +290,56 @@ def gla_chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: 
             ptr(h0), d_o.data_ptr(), ptr(dhT), dq.data_ptr(), dkk.data_ptr(), dvv.data_ptr(),
             da.data_ptr(), ptr(dh0), B, H, T, dk, dv, ctypes.byref(opts), _stream(dev))
     _lib.check(st, "gla_chunk_bwd")
+    return dq, dkk, dvv, da, dh0
+
+
+def gla_chunk_bwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                         log_alpha: torch.Tensor, d_o: torch.Tensor, cu_seqlens,
+                         scale: float | None = None, h0: torch.Tensor | None = None,
+                         dhT: torch.Tensor | None = None, *, need_dh0: bool = True,
+                         force_exact: bool = False):
+    """Gradients of gla_chunk_fwd_varlen over a packed batch of sequences.
+
+    ``q``, ``k``, ``log_alpha`` ``[H, T_total, dk]``; ``v``, ``d_o``
+    ``[H, T_total, dv]``; ``h0``, ``dhT`` ``[N, H, dk, dv]`` or None (zero);
+    ``cu_seqlens`` a host sequence of ``N + 1`` ints.  Returns
+    ``(dq, dk, dv, dlog_alpha, dh0)`` shaped like their inputs (``dh0`` None
+    when ``need_dh0`` is False).
+    """
+    if q.dim() != 3:
+        raise ValueError("q must be [H, T_total, dk]")
+    H, T_total, dk = q.shape
+    dv = v.shape[-1]
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("q must be on a CUDA device")
+    cu = [int(x) for x in (cu_seqlens.tolist() if torch.is_tensor(cu_seqlens) else cu_seqlens)]
+    N = len(cu) - 1
+    if N < 1:
+        raise ValueError("cu_seqlens needs at least two entries")
+    _need(q, "q", torch.bfloat16, (H, T_total, dk), dev)
+    _need(k, "k", torch.bfloat16, (H, T_total, dk), dev)
+    _need(v, "v", torch.bfloat16, (H, T_total, dv), dev)
+    _need(log_alpha, "log_alpha", torch.float32, (H, T_total, dk), dev)
+    _need(d_o, "d_o", torch.bfloat16, (H, T_total, dv), dev)
+    if h0 is not None:
+        _need(h0, "h0", torch.float32, (N, H, dk, dv), dev)
+    if dhT is not None:
+        _need(dhT, "dhT", torch.float32, (N, H, dk, dv), dev)
+    if scale is None:
+        scale = dk ** -0.5
+    dq, dkk, dvv, da = (torch.empty_like(t) for t in (q, k, v, log_alpha))
+    dh0 = torch.empty(N, H, dk, dv, dtype=torch.float32, device=dev) if need_dh0 else None
+    opts = GlaChunkOptions(force_exact=1 if force_exact else 0)
+    cu_arr = (ctypes.c_int * len(cu))(*cu)
+    ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+    with torch.cuda.device(dev):
+        st = _lib.lib().gla_chunk_bwd_varlen_ex(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), log_alpha.data_ptr(), float(scale),
+            ptr(h0), d_o.data_ptr(), ptr(dhT), dq.data_ptr(), dkk.data_ptr(), dvv.data_ptr(),
+            da.data_ptr(), ptr(dh0), cu_arr, N, H, T_total, dk, dv, ctypes.byref(opts),
+            _stream(dev))
+    _lib.check(st, "gla_chunk_bwd_varlen")
     return dq, dkk, dvv, da, dh0
 
 

@@ -26,7 +26,8 @@ GLA_ERR_SCRATCH = 7
 EXPORTED = ("gla_chunk_fwd", "gla_chunk_fwd_ex", "gla_chunk_fwd_plan", "gla_chunk_fwd_noalloc",
             "gla_chunk_fwd_host", "gla_chunk_fwd_varlen", "gla_chunk_fwd_varlen_ex",
             "gla_chunk_fwd_varlen_plan", "gla_chunk_bwd", "gla_chunk_bwd_ex",
-            "gla_chunk_bwd_plan", "gla_recurrent_step", "gla_status_string",
+            "gla_chunk_bwd_plan", "gla_chunk_bwd_varlen", "gla_chunk_bwd_varlen_ex",
+            "gla_recurrent_step", "gla_status_string",
             "gla_last_device_status", "gla_version")
 
 
@@ -76,6 +77,11 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.gla_chunk_bwd_ex.argtypes = bwd + [ctypes.POINTER(GlaChunkOptions), vp]
     lib.gla_chunk_bwd_ex.restype = i
     lib.gla_chunk_bwd_plan.argtypes = [i, i, i, i, i, ip, ip, ctypes.POINTER(ctypes.c_ulong)]
+    bwdv = [vp, vp, vp, fp, f, fp, vp, fp, vp, vp, vp, fp, fp, ip, i, i, i, i, i]
+    lib.gla_chunk_bwd_varlen.argtypes = bwdv + [vp]
+    lib.gla_chunk_bwd_varlen.restype = i
+    lib.gla_chunk_bwd_varlen_ex.argtypes = bwdv + [ctypes.POINTER(GlaChunkOptions), vp]
+    lib.gla_chunk_bwd_varlen_ex.restype = i
     lib.gla_chunk_bwd_plan.restype = i
     lib.gla_recurrent_step.argtypes = [vp, vp, vp, fp, f, fp, vp, i, i, i, i, vp]
     lib.gla_recurrent_step.restype = i

@@ -633,6 +633,22 @@ bool bwd_layout(int B, int H, int T, int dk, int dv, size_t *states, size_t *adj
     return NC <= 0x7fffffffLL;
 }
 
+// Points the scratch fields of p into ws (laid out by bwd_layout for B, H, T).
+void bwd_bind_scratch(gla::BwdLaunch &p, char *ws, int B, int H, int T, int dk, int dv) {
+    size_t st_b = 0, adj_b = 0, car_b = 0, dec_b = 0, par_b = 0;
+    bwd_layout(B, H, T, dk, dv, &st_b, &adj_b, &car_b, &dec_b, &par_b);
+    p.states = reinterpret_cast<float *>(ws);
+    p.adjoints = reinterpret_cast<float *>(ws + st_b);
+    p.carry = reinterpret_cast<float *>(ws + st_b + adj_b);
+    p.decay = reinterpret_cast<float *>(ws + st_b + adj_b + car_b);
+    p.pq = reinterpret_cast<float *>(ws + st_b + adj_b + car_b + dec_b);
+    p.pk = p.pq + static_cast<size_t>(B) * H * T * dk;
+    p.pv = p.pk + static_cast<size_t>(B) * H * T * dk;
+    p.wide = reinterpret_cast<unsigned char *>(
+        ws + st_b + adj_b + car_b + dec_b +
+        ((sizeof(float) * static_cast<size_t>(B) * H * T * (2 * dk + dv) + 255) & ~static_cast<size_t>(255)));
+}
+
 int bwd_shape_ok(int B, int H, int T, int dk, int dv) {
     if (B <= 0 || H <= 0 || T <= 0) return GLA_ERR_ARG;
     if (static_cast<long long>(B) * H > 65535) return GLA_ERR_ARG;
@@ -706,16 +722,7 @@ int gla_chunk_bwd_ex(const void *q, const void *k, const void *v, const float *l
     p.gv = static_cast<__nv_bfloat16 *>(grad_v);
     p.ga = grad_log_alpha;
     p.gh0 = grad_h0;
-    p.states = reinterpret_cast<float *>(ws);
-    p.adjoints = reinterpret_cast<float *>(ws + st_b);
-    p.carry = reinterpret_cast<float *>(ws + st_b + adj_b);
-    p.decay = reinterpret_cast<float *>(ws + st_b + adj_b + car_b);
-    p.pq = reinterpret_cast<float *>(ws + st_b + adj_b + car_b + dec_b);
-    p.pk = p.pq + static_cast<size_t>(B) * H * T * dk;
-    p.pv = p.pk + static_cast<size_t>(B) * H * T * dk;
-    p.wide = reinterpret_cast<unsigned char *>(
-        ws + st_b + adj_b + car_b + dec_b +
-        ((sizeof(float) * static_cast<size_t>(B) * H * T * (2 * dk + dv) + 255) & ~static_cast<size_t>(255)));
+    bwd_bind_scratch(p, ws, B, H, T, dk, dv);
     p.status = dev->status;
     p.scale = scale;
     p.BH = B * H;
@@ -723,6 +730,8 @@ int gla_chunk_bwd_ex(const void *q, const void *k, const void *v, const float *l
     p.NC = (T + bwd_chunk_tokens() - 1) / bwd_chunk_tokens();
     p.dk = dk;
     p.dv = dv;
+    p.sk = static_cast<long long>(T) * dk;
+    p.sv = static_cast<long long>(T) * dv;
     p.force_exact = op.force_exact;
     int r = GLA_OK;
     const long long rows = static_cast<long long>(B) * H * T;
@@ -747,6 +756,100 @@ int gla_chunk_bwd(const void *q, const void *k, const void *v, const float *log_
                   float *grad_h0, int B, int H, int T, int dk, int dv, cudaStream_t stream) {
     return gla_chunk_bwd_ex(q, k, v, log_alpha, scale, h0, d_o, dhT, grad_q, grad_k, grad_v,
                             grad_log_alpha, grad_h0, B, H, T, dk, dv, nullptr, stream);
+}
+
+int gla_chunk_bwd_varlen_ex(const void *q, const void *k, const void *v, const float *log_alpha,
+                            float scale, const float *h0, const void *d_o, const float *dhT,
+                            void *grad_q, void *grad_k, void *grad_v, float *grad_log_alpha,
+                            float *grad_h0, const int *cu_seqlens, int N, int H, int T_total,
+                            int dk, int dv, const gla_chunk_options *opts, cudaStream_t stream) {
+    using namespace gla;
+    if (!q || !k || !v || !log_alpha || !d_o || !grad_q || !grad_k || !grad_v ||
+        !grad_log_alpha || !cu_seqlens)
+        return GLA_ERR_ARG;
+    if (N <= 0 || H <= 0 || T_total < 0 || H > 65535) return GLA_ERR_ARG;
+    if (!dk_ok(dk) || !dv_ok(dv)) return GLA_ERR_SHAPE;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(d_o) ||
+        !aligned16(grad_q) || !aligned16(grad_k) || !aligned16(grad_v) ||
+        !aligned16(log_alpha) || !aligned16(grad_log_alpha) || (h0 && !aligned16(h0)) ||
+        (dhT && !aligned16(dhT)) || (grad_h0 && !aligned16(grad_h0)))
+        return GLA_ERR_ARG;
+    gla_chunk_options o_def = {};
+    const gla_chunk_options &op = opts ? *opts : o_def;
+    if (op.gate_per_head != 0 || (op.force_exact != 0 && op.force_exact != 1)) return GLA_ERR_ARG;
+    if (cu_seqlens[0] != 0 || cu_seqlens[N] != T_total) return GLA_ERR_ARG;
+    int max_len = 0;
+    for (int n = 0; n < N; ++n) {
+        const int len = cu_seqlens[n + 1] - cu_seqlens[n];
+        if (len < 0) return GLA_ERR_ARG;
+        max_len = std::max(max_len, len);
+    }
+    DeviceInfo *dev = nullptr;
+    const int st = current_device(&dev);
+    if (st != GLA_OK) return st;
+    const size_t state = static_cast<size_t>(H) * dk * dv;   // one sequence's states, all heads
+    char *ws = nullptr;
+    if (max_len > 0) {
+        size_t a = 0, b = 0, c = 0, d = 0, e = 0;
+        if (!bwd_layout(1, H, max_len, dk, dv, &a, &b, &c, &d, &e)) return GLA_ERR_ARG;
+        if (cudaMallocAsync(reinterpret_cast<void **>(&ws), a + b + c + d + e, stream) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return GLA_ERR_ALLOC;
+        }
+    }
+    int r = GLA_OK;
+    for (int n = 0; n < N && r == GLA_OK; ++n) {
+        const int bos = cu_seqlens[n], len = cu_seqlens[n + 1] - bos;
+        if (len == 0) {   // nothing flows through: dh0 = dhT (zero without one)
+            if (grad_h0) {
+                const cudaError_t ce =
+                    dhT ? cudaMemcpyAsync(grad_h0 + n * state, dhT + n * state,
+                                          sizeof(float) * state, cudaMemcpyDeviceToDevice, stream)
+                        : cudaMemsetAsync(grad_h0 + n * state, 0, sizeof(float) * state, stream);
+                if (ce != cudaSuccess) r = GLA_ERR_LAUNCH;
+            }
+            continue;
+        }
+        const size_t ok_ = static_cast<size_t>(bos) * dk, ov = static_cast<size_t>(bos) * dv;
+        BwdLaunch p = {};
+        p.q = static_cast<const __nv_bfloat16 *>(q) + ok_;
+        p.k = static_cast<const __nv_bfloat16 *>(k) + ok_;
+        p.v = static_cast<const __nv_bfloat16 *>(v) + ov;
+        p.d_o = static_cast<const __nv_bfloat16 *>(d_o) + ov;
+        p.log_alpha = log_alpha + ok_;
+        p.h0 = h0 ? h0 + n * state : nullptr;
+        p.dhT = dhT ? dhT + n * state : nullptr;
+        p.gq = static_cast<__nv_bfloat16 *>(grad_q) + ok_;
+        p.gk = static_cast<__nv_bfloat16 *>(grad_k) + ok_;
+        p.gv = static_cast<__nv_bfloat16 *>(grad_v) + ov;
+        p.ga = grad_log_alpha + ok_;
+        p.gh0 = grad_h0 ? grad_h0 + n * state : nullptr;
+        bwd_bind_scratch(p, ws, 1, H, len, dk, dv);
+        p.status = dev->status;
+        p.scale = scale;
+        p.BH = H;
+        p.T = len;
+        p.NC = (len + bwd_chunk_tokens() - 1) / bwd_chunk_tokens();
+        p.dk = dk;
+        p.dv = dv;
+        p.sk = static_cast<long long>(T_total) * dk;   // head stride of the packed tensors
+        p.sv = static_cast<long long>(T_total) * dv;
+        p.force_exact = op.force_exact;
+        if (launch_chunk_bwd(p, stream) != 0) r = GLA_ERR_LAUNCH;
+    }
+    if (ws) cudaFreeAsync(ws, stream);
+    return r;
+}
+
+int gla_chunk_bwd_varlen(const void *q, const void *k, const void *v, const float *log_alpha,
+                         float scale, const float *h0, const void *d_o, const float *dhT,
+                         void *grad_q, void *grad_k, void *grad_v, float *grad_log_alpha,
+                         float *grad_h0, const int *cu_seqlens, int N, int H, int T_total, int dk,
+                         int dv, cudaStream_t stream) {
+    return gla_chunk_bwd_varlen_ex(q, k, v, log_alpha, scale, h0, d_o, dhT, grad_q, grad_k, grad_v,
+                                   grad_log_alpha, grad_h0, cu_seqlens, N, H, T_total, dk, dv,
+                                   nullptr, stream);
 }
 
 int gla_last_device_status(cudaStream_t stream) {

@@ -52,7 +52,7 @@ namespace gla {
 namespace {
 
 constexpr int BC = 64;          // tokens per backward chunk
-constexpr int TW = 32;          // value columns per state tile (bwd_states / bwd_adjoint)
+constexpr int TW = 32;          // value columns per log-gate carry group and per CUDA-core slice
 constexpr int NT = 256;         // threads per CTA
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kMaxSpan = 120.f;  // log2 units: larger in-chunk decay spans take the exact path
@@ -146,8 +146,8 @@ __global__ void __launch_bounds__(kSumThreads, 2) bwd_sums_kernel(BwdLaunch p) {
     const int u = blockIdx.x, bh = blockIdx.y, which = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5;
     const int t0 = u * BC, n = min(BC, p.T - t0);
-    const size_t rk = (static_cast<size_t>(bh) * p.T + t0) * DK;
-    const size_t rv = (static_cast<size_t>(bh) * p.T + t0) * DV;
+    const size_t rk = static_cast<size_t>(bh) * p.sk + static_cast<size_t>(t0) * DK;   // user key rows
+    const size_t rv = static_cast<size_t>(bh) * p.sv + static_cast<size_t>(t0) * DV;   // user value rows
 
     if (warp == 0) tmem_alloc(slot, DV);
     if (tid == 0) {
@@ -397,8 +397,10 @@ __global__ void __launch_bounds__(kInterThreads, 1) bwd_inter_kernel(BwdLaunch p
     const int u = blockIdx.x, bh = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5;
     const int t0 = u * BC, n = min(BC, p.T - t0);
-    const size_t rk = (static_cast<size_t>(bh) * p.T + t0) * DK;
-    const size_t rv = (static_cast<size_t>(bh) * p.T + t0) * DV;
+    const size_t rk = static_cast<size_t>(bh) * p.sk + static_cast<size_t>(t0) * DK;   // user key rows
+    const size_t rv = static_cast<size_t>(bh) * p.sv + static_cast<size_t>(t0) * DV;   // user value rows
+    const size_t xk = (static_cast<size_t>(bh) * p.T + t0) * DK;   // scratch partials, key side
+    const size_t xv = (static_cast<size_t>(bh) * p.T + t0) * DV;   // scratch partials, value side
 
     if (warp == 0) tmem_alloc(slot, L::kCols);
     if (tid == 0) {
@@ -531,7 +533,7 @@ __global__ void __launch_bounds__(kInterThreads, 1) bwd_inter_kernel(BwdLaunch p
             if (!ok) continue;
             if (part < 2) {
                 if (r >= DK) continue;
-                float *dst = (part == 0 ? p.pq : p.pk) + rk + r;
+                float *dst = (part == 0 ? p.pq : p.pk) + xk + r;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int t = tb + j;
@@ -544,7 +546,7 @@ __global__ void __launch_bounds__(kInterThreads, 1) bwd_inter_kernel(BwdLaunch p
             } else {
                 const int c = (part - 2) * SLAB + r;
                 if (c >= DV) continue;
-                float *dst = p.pv + rv + c;
+                float *dst = p.pv + xv + c;
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
                     if (tb + j < n) dst[static_cast<size_t>(tb + j) * DV] = __uint_as_float(v[j]);
@@ -608,8 +610,10 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
     const int u = blockIdx.x, bh = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int t0 = u * BC, n = min(BC, p.T - t0);
-    const size_t rk = (static_cast<size_t>(bh) * p.T + t0) * DK;
-    const size_t rv = (static_cast<size_t>(bh) * p.T + t0) * DV;
+    const size_t rk = static_cast<size_t>(bh) * p.sk + static_cast<size_t>(t0) * DK;   // user key rows
+    const size_t rv = static_cast<size_t>(bh) * p.sv + static_cast<size_t>(t0) * DV;   // user value rows
+    const size_t xk = (static_cast<size_t>(bh) * p.T + t0) * DK;   // scratch partials, key side
+    const size_t xv = (static_cast<size_t>(bh) * p.T + t0) * DV;   // scratch partials, value side
     const float s = p.scale;
 
     // loads first: q, k pairs and dO, V 16-byte groups; then the prefix sums
@@ -792,8 +796,9 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
                         float pr[4] = {0.f, 0.f, 0.f, 0.f};
                         if (row_ok) {
                             const size_t off = rk + static_cast<size_t>(t) * DK + i;
-                            const float4 pq4 = *reinterpret_cast<const float4 *>(p.pq + off);
-                            const float4 pk4 = *reinterpret_cast<const float4 *>(p.pk + off);
+                            const size_t xo = xk + static_cast<size_t>(t) * DK + i;
+                            const float4 pq4 = *reinterpret_cast<const float4 *>(p.pq + xo);
+                            const float4 pk4 = *reinterpret_cast<const float4 *>(p.pk + xo);
                             const uint2 qv = *reinterpret_cast<const uint2 *>(p.q + off);
                             const uint2 kv = *reinterpret_cast<const uint2 *>(p.k + off);
                             const float pqa[4] = {pq4.x, pq4.y, pq4.z, pq4.w};
@@ -835,7 +840,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
 #pragma unroll
                     for (int j = 0; j < 32; j += 4) {
                         const size_t off = rv + static_cast<size_t>(t) * DV + cb + j;
-                        const float4 pv4 = *reinterpret_cast<const float4 *>(p.pv + off);
+                        const float4 pv4 = *reinterpret_cast<const float4 *>(
+                            p.pv + xv + static_cast<size_t>(t) * DV + cb + j);
                         const uint32_t w0 = pack_bf16x2(__uint_as_float(rv_[j]) + pv4.x,
                                                         __uint_as_float(rv_[j + 1]) + pv4.y);
                         const uint32_t w1 = pack_bf16x2(__uint_as_float(rv_[j + 2]) + pv4.z,
@@ -892,8 +898,10 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdLaunch p) {
     if (!p.wide[static_cast<size_t>(bh) * p.NC + u]) return;   // done by the tensor-core kernel
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
     const int t0 = u * BC, n = min(BC, p.T - t0);
-    const size_t rk = (static_cast<size_t>(bh) * p.T + t0) * DK;   // first row, key tensors
-    const size_t rv = (static_cast<size_t>(bh) * p.T + t0) * DV;   // first row, value tensors
+    const size_t rk = static_cast<size_t>(bh) * p.sk + static_cast<size_t>(t0) * DK;   // user key rows
+    const size_t rv = static_cast<size_t>(bh) * p.sv + static_cast<size_t>(t0) * DV;   // user value rows
+    const size_t xk = (static_cast<size_t>(bh) * p.T + t0) * DK;   // scratch partials, key side
+    const size_t xv = (static_cast<size_t>(bh) * p.T + t0) * DV;   // scratch partials, value side
     const float s = p.scale;
 
     // the state terms of dq and dk (bwd_inter), fetched early for phase 2
@@ -903,7 +911,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdLaunch p) {
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
             const int t = 4 * ty + a;
-            const size_t off = rk + static_cast<size_t>(t) * DK + tx + 16 * b;
+            const size_t off = xk + static_cast<size_t>(t) * DK + tx + 16 * b;
             pq[a][b] = t < n ? p.pq[off] : 0.f;
             pk[a][b] = t < n ? p.pk[off] : 0.f;
         }
@@ -1091,7 +1099,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdLaunch p) {
 #pragma unroll
             for (int a = 0; a < 4; ++a) {
                 const int j = 4 * ty + a;
-                const size_t off = rv + static_cast<size_t>(j) * DV + c0 + tx;
+                const size_t off = xv + static_cast<size_t>(j) * DV + c0 + tx;
                 pvv[a][0] = j < n ? p.pv[off] : 0.f;
                 pvv[a][1] = j < n ? p.pv[off + 16] : 0.f;
             }

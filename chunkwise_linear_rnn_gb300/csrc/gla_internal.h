@@ -101,6 +101,10 @@ struct BwdLaunch {
     unsigned int *status;                    // device status word (bounded waits)
     float scale;
     int BH, T, NC, dk, dv;
+    // elements between consecutive (batch, head) rows of the caller's tensors:
+    // T * dk and T * dv for [BH, T, .] tensors; a packed sequence of a
+    // [H, T_total, .] batch is a strided view with T_total * dk / T_total * dv
+    long long sk, sv;
     int force_exact;
 };
 

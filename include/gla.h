@@ -312,6 +312,33 @@ int gla_chunk_bwd_ex(const void *q, const void *k, const void *v, const float *l
 int gla_chunk_bwd_plan(int B, int H, int T, int dk, int dv, int *chunk, int *launches,
                        unsigned long *scratch_bytes);
 
+/*
+ * gla_chunk_bwd_varlen — the backward of gla_chunk_fwd_varlen: gradients for
+ * a packed batch of N sequences of different lengths, each its own
+ * recurrence (layouts as for gla_chunk_fwd_varlen):
+ *   q, k, log_alpha, grad_q, grad_k, grad_log_alpha : [H, T_total, dk]
+ *   v, d_o, grad_v                                   : [H, T_total, dv]
+ *   h0, dhT, grad_h0                                 : [N, H, dk, dv] (each nullable)
+ *   cu_seqlens : HOST array of N + 1 ints, from 0 to T_total, nondecreasing.
+ * Each sequence runs the gla_chunk_bwd kernels on its rows (a strided view
+ * of the packed tensors), one after another on `stream`, with one scratch
+ * sized for the longest sequence; an empty sequence gets grad_h0 = dhT (zero
+ * without dhT).  Per-head gates are not supported here (GLA_ERR_ARG).
+ * Errors as for gla_chunk_bwd and gla_chunk_fwd_varlen.
+ */
+int gla_chunk_bwd_varlen(const void *q, const void *k, const void *v, const float *log_alpha,
+                         float scale, const float *h0, const void *d_o, const float *dhT,
+                         void *grad_q, void *grad_k, void *grad_v, float *grad_log_alpha,
+                         float *grad_h0, const int *cu_seqlens, int N, int H, int T_total, int dk,
+                         int dv, cudaStream_t stream);
+
+/* gla_chunk_bwd_varlen with options (force_exact only; opts may be NULL). */
+int gla_chunk_bwd_varlen_ex(const void *q, const void *k, const void *v, const float *log_alpha,
+                            float scale, const float *h0, const void *d_o, const float *dhT,
+                            void *grad_q, void *grad_k, void *grad_v, float *grad_log_alpha,
+                            float *grad_h0, const int *cu_seqlens, int N, int H, int T_total,
+                            int dk, int dv, const gla_chunk_options *opts, cudaStream_t stream);
+
 /* Static text for a status code (never NULL). */
 const char *gla_status_string(int status);
 
