@@ -395,6 +395,7 @@ __global__ void __launch_bounds__(kInterThreads, 1) bwd_inter_kernel(BwdLaunch p
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::kBar);
     uint32_t *slot = reinterpret_cast<uint32_t *>(sm + L::kSlot);
     const int u = blockIdx.x, bh = blockIdx.y;
+    if (!p.wide[static_cast<size_t>(bh) * p.NC + u]) return;   // done by bwd_intra
     const int tid = threadIdx.x, warp = tid >> 5;
     const int t0 = u * BC, n = min(BC, p.T - t0);
     const size_t rk = static_cast<size_t>(bh) * p.sk + static_cast<size_t>(t0) * DK;   // user key rows
@@ -612,8 +613,6 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
     const int t0 = u * BC, n = min(BC, p.T - t0);
     const size_t rk = static_cast<size_t>(bh) * p.sk + static_cast<size_t>(t0) * DK;   // user key rows
     const size_t rv = static_cast<size_t>(bh) * p.sv + static_cast<size_t>(t0) * DV;   // user value rows
-    const size_t xk = (static_cast<size_t>(bh) * p.T + t0) * DK;   // scratch partials, key side
-    const size_t xv = (static_cast<size_t>(bh) * p.T + t0) * DV;   // scratch partials, value side
     const float s = p.scale;
 
     // loads first: q, k pairs and dO, V 16-byte groups; then the prefix sums
@@ -706,14 +705,14 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
     bool ok = mbar_wait_bounded(bar, 0, p.status);
     tc_fence_after();
 
-    // epilogue 1: mask A and scale * M to j <= t, split into bf16 pairs, [t][j] tiles.
+    // epilogue 1: mask A and M to j <= t, split into bf16 pairs, [t][j] tiles.
     // Warp q (= warp % 4) holds rows 16 q .. 16 q + 15 in lanes 0-15; warps 0-3 take
     // A, warps 4-7 take M.
     {
         const int q4 = warp & 3, t = 16 * q4 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
         const int col = warp < 4 ? 0 : 64;
-        const float mult = warp < 4 ? 1.f : s;
+        const float mult = 1.f;
         uint8_t *th = sm + (warp < 4 ? L::kAh : L::kMh), *tl = sm + (warp < 4 ? L::kAl : L::kMl);
 #pragma unroll 1
         for (int jb = 0; jb < BC; jb += 32) {
@@ -772,6 +771,86 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
     }
     ok = mbar_wait_bounded(bar, 1, p.status) && ok;
     tc_fence_after();
+
+    // group 3: the state terms, accumulated onto dQ, dK and dV, 64 value
+    // columns at a time:  dQ += dO S~^T,  dK += V R~^T,  dV += Kh R~  with
+    // S~ = 2^r S_u and R~ = 2^(Gamma_C - r) R_u / scale (bf16 pairs, [dk][64]
+    // tiles), so that the epilogue's factors s 2^(Gamma - r), s 2^(r - Gamma)
+    // and s apply to both terms.  The slab tiles take the place of the Qh and
+    // A / M tiles, which the products above have finished reading.
+    {
+        constexpr uint32_t kSB = DK * 128;
+        uint8_t *tSh = sm + L::kQh, *tSl = tSh + kSB, *tRh = sm + L::kAh, *tRl = tRh + kSB;
+        constexpr int SPER = DK * 64 / 4 / NTI;
+        float4 sv[SPER], rr[SPER];
+        auto fetch = [&](int c0) {
+#pragma unroll
+            for (int m = 0; m < SPER; ++m) {
+                const int e = tid + m * NTI, i = e / 16, cl = (e % 16) * 4;
+                sv[m] = *reinterpret_cast<const float4 *>(
+                    p.states + slot_index<DK, DV>(bh, i, c0 + cl, u, p.NC + 1));
+                rr[m] = *reinterpret_cast<const float4 *>(
+                    p.adjoints + slot_index<DK, DV>(bh, i, c0 + cl, u, p.NC));
+            }
+        };
+        fetch(0);
+#pragma unroll 1
+        for (int sl = 0; sl < DV / 64; ++sl) {
+            const int c0 = sl * 64;
+#pragma unroll
+            for (int m = 0; m < SPER; ++m) {
+                const int e = tid + m * NTI, i = e / 16, cl = (e % 16) * 4;
+                const float fs = exp2f(sRef[i]), fr = exp2f(sGC[i] - sRef[i]) / s;
+                const uint32_t off = sw128_offset(i, cl, kSB);
+                uint32_t h0, l0, h1, l1;
+                split_pair(sv[m].x * fs, sv[m].y * fs, h0, l0);
+                split_pair(sv[m].z * fs, sv[m].w * fs, h1, l1);
+                *reinterpret_cast<uint2 *>(tSh + off) = make_uint2(h0, h1);
+                *reinterpret_cast<uint2 *>(tSl + off) = make_uint2(l0, l1);
+                split_pair(rr[m].x * fr, rr[m].y * fr, h0, l0);
+                split_pair(rr[m].z * fr, rr[m].w * fr, h1, l1);
+                *reinterpret_cast<uint2 *>(tRh + off) = make_uint2(h0, h1);
+                *reinterpret_cast<uint2 *>(tRl + off) = make_uint2(l0, l1);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+            if (sl + 1 < DV / 64) fetch(c0 + 64);   // the next slab in flight during the products
+            if (tid == 0) {
+                constexpr uint32_t id_qk3 = idesc_bf16(64, DK, false, false);   // [t][c] x [i][c]
+                constexpr uint32_t id_v3 = idesc_bf16(64, BC, false, true);     // Kh [t][i] x R~ [i][c]
+                const uint32_t aSh = smem_u32(tSh), aSl = smem_u32(tSl);
+                const uint32_t aRh = smem_u32(tRh), aRl = smem_u32(tRl);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint32_t o = kk * 32;
+                    const uint64_t ado = sw128_desc(a0 + L::kDo + sl * L::kBlk + o, 16, 1024);
+                    const uint64_t av = sw128_desc(a0 + L::kV + sl * L::kBlk + o, 16, 1024);
+                    mma_bf16_ss(tmem + 128, ado, sw128_desc(aSh + o, 16, 1024), id_qk3, 1u);
+                    mma_bf16_ss(tmem + 128, ado, sw128_desc(aSl + o, 16, 1024), id_qk3, 1u);
+                    mma_bf16_ss(tmem + 128 + DK, av, sw128_desc(aRh + o, 16, 1024), id_qk3, 1u);
+                    mma_bf16_ss(tmem + 128 + DK, av, sw128_desc(aRl + o, 16, 1024), id_qk3, 1u);
+                }
+                const uint32_t dcol = c0 < 128 ? static_cast<uint32_t>(c0)
+                                               : 128u + 2u * DK + static_cast<uint32_t>(c0 - 128);
+#pragma unroll
+                for (int kk = 0; kk < DK / 16; ++kk) {
+                    const uint32_t o = (kk >> 2) * L::kBlk + (kk & 3) * 32;
+                    const uint64_t kh = sw128_desc(a0 + L::kKh + o, 16, 1024);
+                    const uint64_t kl = sw128_desc(a0 + L::kKl + o, 16, 1024);
+                    const uint64_t rh = sw128_desc(aRh + kk * 2048, kSB, 1024);
+                    const uint64_t rl = sw128_desc(aRl + kk * 2048, kSB, 1024);
+                    mma_bf16_ss(tmem + dcol, kh, rh, id_v3, 1u);
+                    mma_bf16_ss(tmem + dcol, kl, rh, id_v3, 1u);
+                    mma_bf16_ss(tmem + dcol, kh, rl, id_v3, 1u);
+                }
+                mma_commit(bar);
+            }
+            ok = mbar_wait_bounded(bar, (2 + sl) & 1, p.status) && ok;
+            tc_fence_after();
+        }
+    }
     __syncthreads();   // every thread is past the tile reads; P may overwrite the q/k tiles
 
     // epilogue 2.  Warps 0-3: row t of dQ and dK (lanes 0-15), q dq - k dk into P.
@@ -796,13 +875,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
                         float pr[4] = {0.f, 0.f, 0.f, 0.f};
                         if (row_ok) {
                             const size_t off = rk + static_cast<size_t>(t) * DK + i;
-                            const size_t xo = xk + static_cast<size_t>(t) * DK + i;
-                            const float4 pq4 = *reinterpret_cast<const float4 *>(p.pq + xo);
-                            const float4 pk4 = *reinterpret_cast<const float4 *>(p.pk + xo);
                             const uint2 qv = *reinterpret_cast<const uint2 *>(p.q + off);
                             const uint2 kv = *reinterpret_cast<const uint2 *>(p.k + off);
-                            const float pqa[4] = {pq4.x, pq4.y, pq4.z, pq4.w};
-                            const float pka[4] = {pk4.x, pk4.y, pk4.z, pk4.w};
                             const float qa[4] = {__uint_as_float(qv.x << 16), __uint_as_float(qv.x & 0xffff0000u),
                                                  __uint_as_float(qv.y << 16), __uint_as_float(qv.y & 0xffff0000u)};
                             const float ka[4] = {__uint_as_float(kv.x << 16), __uint_as_float(kv.x & 0xffff0000u),
@@ -814,8 +888,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
 #pragma unroll
                                 for (int x = 0; x < 2; ++x) {
                                     const float d = gr[i + h + x] - sRef[i + h + x];
-                                    dqv[x] = s * exp2f(d) * __uint_as_float(rq[j + h + x]) + pqa[h + x];
-                                    dkv[x] = s * exp2f(-d) * __uint_as_float(rkk[j + h + x]) + pka[h + x];
+                                    dqv[x] = s * exp2f(d) * __uint_as_float(rq[j + h + x]);
+                                    dkv[x] = s * exp2f(-d) * __uint_as_float(rkk[j + h + x]);
                                     pr[h + x] = qa[h + x] * dqv[x] - ka[h + x] * dkv[x];
                                 }
                                 dqw[h / 2] = pack_bf16x2(dqv[0], dqv[1]);
@@ -840,12 +914,10 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
 #pragma unroll
                     for (int j = 0; j < 32; j += 4) {
                         const size_t off = rv + static_cast<size_t>(t) * DV + cb + j;
-                        const float4 pv4 = *reinterpret_cast<const float4 *>(
-                            p.pv + xv + static_cast<size_t>(t) * DV + cb + j);
-                        const uint32_t w0 = pack_bf16x2(__uint_as_float(rv_[j]) + pv4.x,
-                                                        __uint_as_float(rv_[j + 1]) + pv4.y);
-                        const uint32_t w1 = pack_bf16x2(__uint_as_float(rv_[j + 2]) + pv4.z,
-                                                        __uint_as_float(rv_[j + 3]) + pv4.w);
+                        const uint32_t w0 = pack_bf16x2(s * __uint_as_float(rv_[j]),
+                                                        s * __uint_as_float(rv_[j + 1]));
+                        const uint32_t w1 = pack_bf16x2(s * __uint_as_float(rv_[j + 2]),
+                                                        s * __uint_as_float(rv_[j + 3]));
                         *reinterpret_cast<uint2 *>(p.gv + off) = make_uint2(w0, w1);
                     }
                 }
@@ -1202,8 +1274,8 @@ int launch_bwd_dims(const BwdLaunch &p, cudaStream_t stream) {
     bwd_sums_kernel<DK, DV><<<dim3(p.NC, p.BH, 2), kSumThreads, sum_bytes, stream>>>(p);
     bwd_state_scan_kernel<DK, DV><<<scan_blocks, 256, 0, stream>>>(p);
     bwd_adjoint_scan_kernel<DK, DV><<<scan_blocks, 256, 0, stream>>>(p);
-    bwd_inter_kernel<DK, DV><<<dim3(p.NC, p.BH), kInterThreads, inter_bytes, stream>>>(p);
     bwd_intra_kernel<DK, DV><<<dim3(p.NC, p.BH), kIntraThreads, intra_bytes, stream>>>(p);
+    bwd_inter_kernel<DK, DV><<<dim3(p.NC, p.BH), kInterThreads, inter_bytes, stream>>>(p);
     bwd_grads_kernel<DK, DV><<<dim3(p.NC, p.BH), NT, grad_bytes, stream>>>(p);
     return static_cast<int>(cudaGetLastError());
 }
