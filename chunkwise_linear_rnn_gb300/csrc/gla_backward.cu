@@ -30,11 +30,12 @@
 //      gradient its outputs add, plus its total decay;
 //   2. bwd_state_scan:   S_u for u = 0 .. NC from those sums (elementwise);
 //   3. bwd_adjoint_scan: R_u, the log-gate carries rowsum(R_u * S_(u+1)), dh0;
-//   4. bwd_inter: every chunk's state terms of dq, dk, dv on the tensor cores;
-//   5. bwd_intra: every chunk's in-chunk terms on the tensor cores, plus the
-//      state terms, written as dq, dk, dv and dlog_alpha;
-//   6. bwd_grads: the same on CUDA cores in fp32, for the chunks that need
-//      exact decay factors (flagged by bwd_intra; the rest exit at once).
+//   4. bwd_intra: every chunk's in-chunk products on the tensor cores, with
+//      the state terms accumulated onto them in TMEM, written as dq, dk, dv
+//      and dlog_alpha;
+//   5. bwd_inter and 6. bwd_grads: the state terms (tensor cores) and the
+//      in-chunk terms (CUDA cores, fp32) for the chunks that need exact decay
+//      factors, flagged by bwd_intra; the other CTAs exit at once.
 // Inside a chunk the decay factor e^(Gamma_t - Gamma_j) (t >= j) is split
 // around a per-channel reference r = (Gamma_0 + Gamma_(C-1)) / 2, so both
 // halves stay within 2^+-60 when the chunk's decay spans at most 2^120; a
@@ -347,8 +348,8 @@ __global__ void __launch_bounds__(256, 2) bwd_adjoint_scan_kernel(BwdLaunch p) {
 }
 
 // ---------------------------------------------------------------------------
-// 3. the state terms of the gradients on the tensor cores, one CTA per
-//    (chunk, head), written as fp32 partial gradients:
+// 5. the state terms of the gradients on the tensor cores, one CTA per
+//    flagged (chunk, head), written as fp32 partial gradients for bwd_grads:
 //       pq = scale e^Gamma (dO S_u^T),  pk = e^(Gamma_C - Gamma) (V R_u^T),
 //       pv = (K e^(Gamma_C - Gamma)) R_u.
 //    Transposed so that every product has M = 128 (key channels or value
@@ -769,6 +770,21 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
         }
         mma_commit(bar);
     }
+    // the first state slab's loads fly while group 2 runs (group 3 below)
+    constexpr uint32_t kSB = DK * 128;
+    constexpr int SPER = DK * 64 / 4 / NTI;
+    float4 sv[SPER], rr[SPER];
+    auto fetch = [&](int c0) {
+#pragma unroll
+        for (int m = 0; m < SPER; ++m) {
+            const int e = tid + m * NTI, i = e / 16, cl = (e % 16) * 4;
+            sv[m] = *reinterpret_cast<const float4 *>(
+                p.states + slot_index<DK, DV>(bh, i, c0 + cl, u, p.NC + 1));
+            rr[m] = *reinterpret_cast<const float4 *>(
+                p.adjoints + slot_index<DK, DV>(bh, i, c0 + cl, u, p.NC));
+        }
+    };
+    fetch(0);
     ok = mbar_wait_bounded(bar, 1, p.status) && ok;
     tc_fence_after();
 
@@ -779,21 +795,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
     // and s apply to both terms.  The slab tiles take the place of the Qh and
     // A / M tiles, which the products above have finished reading.
     {
-        constexpr uint32_t kSB = DK * 128;
         uint8_t *tSh = sm + L::kQh, *tSl = tSh + kSB, *tRh = sm + L::kAh, *tRl = tRh + kSB;
-        constexpr int SPER = DK * 64 / 4 / NTI;
-        float4 sv[SPER], rr[SPER];
-        auto fetch = [&](int c0) {
-#pragma unroll
-            for (int m = 0; m < SPER; ++m) {
-                const int e = tid + m * NTI, i = e / 16, cl = (e % 16) * 4;
-                sv[m] = *reinterpret_cast<const float4 *>(
-                    p.states + slot_index<DK, DV>(bh, i, c0 + cl, u, p.NC + 1));
-                rr[m] = *reinterpret_cast<const float4 *>(
-                    p.adjoints + slot_index<DK, DV>(bh, i, c0 + cl, u, p.NC));
-            }
-        };
-        fetch(0);
 #pragma unroll 1
         for (int sl = 0; sl < DV / 64; ++sl) {
             const int c0 = sl * 64;
