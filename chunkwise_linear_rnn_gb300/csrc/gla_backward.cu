@@ -561,17 +561,20 @@ __global__ void __launch_bounds__(kInterThreads, 1) bwd_inter_kernel(BwdLaunch p
 }
 
 // ---------------------------------------------------------------------------
-// 4. the in-chunk terms on the tensor cores, one CTA per (chunk, head), for
-//    every chunk whose decay span allows the reference split (the others are
-//    flagged for the CUDA-core kernel below).  With M = 64 rows per product
-//    (row m of an M = 64 accumulator sits in TMEM lane 32 (m / 16) + m % 16):
+// 4. the gradients on the tensor cores, one CTA per (chunk, head), for every
+//    chunk whose decay span allows the reference split (the others are
+//    flagged for kernels 5 and 6).  With M = 64 rows per product (row m of an
+//    M = 64 accumulator sits in TMEM lane 32 (m / 16) + m % 16):
 //       A  = dO V^T                 (K = dv)      masked to j <= t
-//       M  = scale Qh Kh^T          (K = dk)      masked to j <= t
-//       dQ = A Kh,  dK = A^T Qh     (K = 64)      Qh = Q e^(Gamma - r), Kh = K e^(r - Gamma)
-//       dV = M^T dO                 (K = 64)
-//    Every fp32-valued operand (Qh, Kh, A, M) is a bf16 hi/lo pair; products
-//    of two pairs take the hi.hi, hi.lo and lo.hi terms.  The epilogue adds
-//    the state terms (bwd_inter), writes dq, dk, dv and takes dlog_alpha.
+//       M  = Qh Kh^T                (K = dk)      masked to j <= t
+//       dQ = A Kh + dO S~^T,  dK = A^T Qh + V R~^T,  dV = M^T dO + Kh R~
+//       with Qh = Q e^(Gamma - r), Kh = K e^(r - Gamma), S~ = 2^r S_u and
+//       R~ = 2^(Gamma_C - r) R_u / scale (the state terms, K = dv or dk,
+//       accumulated onto the in-chunk products in TMEM).
+//    Every fp32-valued operand (Qh, Kh, A, M, S~, R~) is a bf16 hi/lo pair;
+//    products of two pairs take the hi.hi, hi.lo and lo.hi terms.  The
+//    epilogue scales dQ by scale 2^(Gamma - r), dK by scale 2^(r - Gamma), dV
+//    by scale, writes dq, dk, dv and takes dlog_alpha.
 constexpr int kIntraThreads = 256;
 
 template <int DK, int DV>
@@ -940,7 +943,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
 }
 
 // ---------------------------------------------------------------------------
-// 5. per-chunk gradients on CUDA cores, for the chunks the tensor-core kernel
+// 6. per-chunk gradients on CUDA cores, for the chunks the tensor-core kernel
 //    leaves (decay span beyond the reference split, or force_exact).  Thread (ty, tx) = (tid / 16, tid % 16) owns rows
 //    4 ty .. 4 ty + 3 and columns tx, tx + 16, ... of every C x C, C x dk and
 //    C x 32 block it computes.
