@@ -1,4 +1,4 @@
-"""GB300-native gated linear attention (GLA) forward: chunked prefill and decode step.
+"""GB300-native gated linear attention (GLA): chunked prefill, its backward, and the decode step.
 
 The computation ("Gated Linear Attention (GLA): Mathematical Foundations, ..."
 (llms.blog), section "The Gated Recurrent Update"):

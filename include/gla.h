@@ -1,5 +1,6 @@
 /*
- * gla.h — C ABI of the GB300 (sm_103a) gated linear attention forward library.
+ * gla.h — C ABI of the GB300 (sm_103a) gated linear attention library: the
+ * chunked forward, its backward, and the decode step.
  *
  * The operation (from "Gated Linear Attention (GLA): Mathematical Foundations,
  * Data-Dependent Gating, Chunkwise Parallel Forms, and Sub-Quadratic Sequence
