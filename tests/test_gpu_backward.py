@@ -224,3 +224,21 @@ def test_packed_sequences(dk, dv, states):
             assert np.max(np.abs(got[3])) <= 1e-5, f"packed seq {n}: dlog_alpha not ~0"
             got[3], want = None, list(want)
         _compare(got, want, f"packed seq {n} (len {e - b}) dk={dk} dv={dv}")
+
+
+@pytest.mark.parametrize("name", ["medium", "very_long"])
+def test_full_size_other_workloads_sampled_heads(name):
+    """The medium (B8 H16 T2048 dk=dv=128) and very long (B1 H32 T262144 dk=dv=128)
+    workloads at full size on the GPU; one head of each checked against the oracle."""
+    from synth import CHUNK_CONFIGS
+    cfg = CHUNK_CONFIGS[name]
+    q, k, v, a, s0 = make_chunk_inputs(cfg.B, cfg.H, cfg.T, cfg.dk, cfg.dv, sigma_z=cfg.sigma_z,
+                                       tau=cfg.tau, sigma_h0=cfg.sigma_h0, seed=0, device=DEV)
+    d_o, g = make_backward_grads(cfg.B, cfg.H, cfg.T, cfg.dk, cfg.dv, seed=0, device=DEV)
+    out = gla.gla_chunk_bwd(q, k, v, a, d_o, cfg.scale, s0, g)
+    torch.cuda.synchronize()
+    b, h = cfg.B - 1, cfg.H - 1
+    sl = lambda t: None if t is None else t[b:b + 1, h:h + 1].cpu()  # noqa: E731
+    want = _oracle(sl(q), sl(k), sl(v), sl(a), sl(s0), sl(d_o), sl(g), cfg.scale)
+    got = [x[b:b + 1, h:h + 1].float().cpu().numpy() for x in out]
+    _compare(got, want, f"{name} workload head ({b},{h})")
