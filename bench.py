@@ -95,13 +95,13 @@ def chunk_bytes(cfg, n_states: int | None = None, gate_per_head: bool = False) -
     return cfg.tokens * per_token + state
 
 
-def bwd_bytes(cfg) -> int:
+def bwd_bytes(cfg, n_states: int | None = None) -> int:
     """Algorithmic bytes of one backward call: q, k, v, log alpha, d_o, h0 and dhT read
-    once; dq, dk, dv, dlog alpha and dh0 written once."""
+    once; dq, dk, dv, dlog alpha and dh0 written once (n_states = sequences x heads)."""
     per_token = 2 * cfg.dk * 2 + cfg.dv * 2 + cfg.dk * 4 + cfg.dv * 2 \
         + 2 * cfg.dk * 2 + cfg.dv * 2 + cfg.dk * 4
-    states = 3 * cfg.B * cfg.H * cfg.dk * cfg.dv * 4
-    return cfg.tokens * per_token + states
+    n = cfg.B * cfg.H if n_states is None else n_states
+    return cfg.tokens * per_token + 3 * n * cfg.dk * cfg.dv * 4
 
 
 def packed_lengths(total: int, n: int, seed: int) -> list:
@@ -438,14 +438,42 @@ def bwd_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_ki
     import torch
     from synth import make_backward_grads, make_config_inputs
     stream = torch.cuda.current_stream(dev)
-    q, k, v, a, h0 = make_config_inputs(cfg, seed=rank, device=dev)
-    d_o, dhT = make_backward_grads(cfg.B, cfg.H, cfg.T, cfg.dk, cfg.dv,
-                                   sigma_dhT=0.1 if h0 is not None else None, seed=rank,
-                                   device=dev)
     plan = gla.gla_chunk_bwd_plan(cfg.B, cfg.H, cfg.T, cfg.dk, cfg.dv)
+    packed = None
+    if args.varlen:
+        # the same tokens per head packed into --varlen sequences of mixed lengths
+        from synth import make_chunk_inputs
+        per_head = cfg.B * cfg.T
+        lens = packed_lengths(per_head, args.varlen, seed=1234 + rank)
+        cu = [0]
+        for m in lens:
+            cu.append(cu[-1] + m)
+        q, k, v, a, _ = make_chunk_inputs(1, cfg.H, per_head, cfg.dk, cfg.dv, sigma_z=cfg.sigma_z,
+                                          tau=cfg.tau, seed=rank, device=dev)
+        q, k, v, a = (t[0] for t in (q, k, v, a))
+        d_o, _ = make_backward_grads(1, cfg.H, per_head, cfg.dk, cfg.dv, seed=rank, device=dev)
+        d_o = d_o[0]
+        h0 = dhT = None
+        if cfg.sigma_h0 is not None:
+            g = torch.Generator(device=dev)
+            g.manual_seed(5678 + rank)
+            h0 = torch.randn(len(lens), cfg.H, cfg.dk, cfg.dv, generator=g, device=dev).mul_(0.1)
+            dhT = torch.randn(len(lens), cfg.H, cfg.dk, cfg.dv, generator=g, device=dev).mul_(0.1)
+        plan = dict(plan, launches=plan["launches"] * sum(1 for m in lens if m > 0))
+        srt = sorted(lens)
+        packed = {"sequences": len(lens), "min_len": srt[0], "median_len": srt[len(srt) // 2],
+                  "max_len": srt[-1], "lengths": "log-normal weights (sigma 1), seed 1234"}
 
-    def step():
-        return gla.gla_chunk_bwd(q, k, v, a, d_o, cfg.scale, h0, dhT)
+        def step():
+            return gla.gla_chunk_bwd_varlen(q, k, v, a, d_o, cu, cfg.scale, h0, dhT)
+    else:
+        q, k, v, a, h0 = make_config_inputs(cfg, seed=rank, device=dev)
+        d_o, dhT = make_backward_grads(cfg.B, cfg.H, cfg.T, cfg.dk, cfg.dv,
+                                       sigma_dhT=0.1 if h0 is not None else None, seed=rank,
+                                       device=dev)
+
+        def step():
+            return gla.gla_chunk_bwd(q, k, v, a, d_o, cfg.scale, h0, dhT)
 
     for _ in range(args.warmup):
         step()
@@ -467,12 +495,12 @@ def bwd_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_ki
     per_call_ms = statistics.mean(s0.elapsed_time(e0) for s0, e0 in ev)
     ms_per_step = total_ms / args.steps
     tokens_all = cfg.tokens * world
-    byts = bwd_bytes(cfg)
+    byts = bwd_bytes(cfg, None if packed is None else packed["sequences"] * cfg.H)
     achieved = byts / (per_call_ms / 1e3) / 1e9
 
     # end to end: pinned host inputs copied in and gradients copied out every call
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.varlen:
         host_in = [t.cpu().pin_memory() for t in (q, k, v, a, d_o, h0, dhT) if t is not None]
         dev_in = [torch.empty_like(t, device=dev) for t in host_in]
         outs = step()
@@ -513,7 +541,8 @@ def bwd_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_ki
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": cfg.name + "-backward", "B": cfg.B, "H": cfg.H, "T": cfg.T,
+        "config": {"workload": cfg.name + (f"-packed{args.varlen}" if args.varlen else "") +
+                   "-backward", "B": cfg.B, "H": cfg.H, "T": cfg.T,
                    "dk": cfg.dk, "dv": cfg.dv, "chunk": plan["chunk"], "replicas": world,
                    "l2": "inputs (%.2f GB) larger than L2; no flush" % (byts / 1e9)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
@@ -526,6 +555,8 @@ def bwd_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_ki
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if packed is not None:
+        line["config"]["packed"] = packed
     return line
 
 
