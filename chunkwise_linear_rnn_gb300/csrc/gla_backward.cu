@@ -944,7 +944,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
 
 // ---------------------------------------------------------------------------
 // 6. per-chunk gradients on CUDA cores, for the chunks the tensor-core kernel
-//    leaves (decay span beyond the reference split, or force_exact).  Thread (ty, tx) = (tid / 16, tid % 16) owns rows
+//    leaves (decay span beyond the reference split, or force_exact): every
+//    in-chunk decay factor e^(Gamma_t - Gamma_j) is its own exponential.  Thread (ty, tx) = (tid / 16, tid % 16) owns rows
 //    4 ty .. 4 ty + 3 and columns tx, tx + 16, ... of every C x C, C x dk and
 //    C x 32 block it computes.
 template <int DK>
@@ -955,7 +956,7 @@ struct GradSmem {
     static constexpr int kG = 0, kQ = kG + BC * LD, kK = kQ + BC * LD, kP = kK + BC * LD;
     static constexpr int kAM = kP + BC * LD;
     static constexpr int kDo = kAM + BC * LA, kV = kDo + BC * LS;
-    static constexpr int kRef = kV + BC * LS, kGC = kRef + DK, kCarry = kGC + DK;
+    static constexpr int kCarry = kV + BC * LS;
     static constexpr int kFloats = kCarry + DK;
     static constexpr size_t kBytes = sizeof(float) * kFloats;
 };
@@ -969,7 +970,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdLaunch p) {
     extern __shared__ float smem[];
     float *sG = smem + L::kG, *sQ = smem + L::kQ, *sK = smem + L::kK, *sP = smem + L::kP;
     float *sAM = smem + L::kAM, *sDo = smem + L::kDo, *sV = smem + L::kV;
-    float *sRef = smem + L::kRef, *sGC = smem + L::kGC, *sCarry = smem + L::kCarry;
+    float *sCarry = smem + L::kCarry;
 
     const int u = blockIdx.x, bh = blockIdx.y;
     if (!p.wide[static_cast<size_t>(bh) * p.NC + u]) return;   // done by the tensor-core kernel
@@ -993,23 +994,16 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdLaunch p) {
             pk[a][b] = t < n ? p.pk[off] : 0.f;
         }
 
-    // prefix sums, the reference and the path choice
+    // prefix sums and the log-gate carry
     load_prefix<DK, LD>(sG, p.log_alpha + rk, n);
-    int wide = 0;
     if (tid < DK) {
-        const float g0 = sG[tid], gl = sG[(BC - 1) * LD + tid];
-        sRef[tid] = 0.5f * (g0 + gl);
-        sGC[tid] = gl;
-        wide = (g0 - gl) > kMaxSpan;
         float c = 0.f;
         for (int x = 0; x < NTILE; ++x)
             c += p.carry[((static_cast<size_t>(bh) * p.NC + u) * NTILE + x) * DK + tid];
         sCarry[tid] = c;
     }
-    const bool exact = __syncthreads_or(wide) || p.force_exact;
-    if (!exact) return;   // done by the tensor-core kernel
 
-    // q and k: rescaled around the reference (fast path) or raw (exact path)
+    // q and k as they are: every decay factor below is its own exponential
     {
         constexpr int PER = BC * DK / 2 / NT;
         uint32_t qr[PER], kr[PER];
@@ -1025,11 +1019,8 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdLaunch p) {
             const int e = (tid + m * NT) * 2, t = e / DK, i = e % DK;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const float qq = __uint_as_float(h ? (qr[m] & 0xffff0000u) : (qr[m] << 16));
-                const float kk = __uint_as_float(h ? (kr[m] & 0xffff0000u) : (kr[m] << 16));
-                const float d = exact ? 0.f : sG[t * LD + i + h] - sRef[i + h];
-                sQ[t * LD + i + h] = qq * exp2f(d);
-                sK[t * LD + i + h] = kk * exp2f(-d);
+                sQ[t * LD + i + h] = __uint_as_float(h ? (qr[m] & 0xffff0000u) : (qr[m] << 16));
+                sK[t * LD + i + h] = __uint_as_float(h ? (kr[m] & 0xffff0000u) : (kr[m] << 16));
             }
         }
     }
@@ -1089,42 +1080,27 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdLaunch p) {
     for (int a = 0; a < 4; ++a) {
         const int t = 4 * ty + a;
         float iq[NB] = {}, ik[NB] = {};
-        if (!exact) {
-            for (int j = 0; j <= t; ++j) {
-                const float aij = sAM[t * LA + j];
+        for (int j = 0; j <= t; ++j) {
+            const float aij = sAM[t * LA + j];
 #pragma unroll
-                for (int b = 0; b < NB; ++b) iq[b] = fmaf(aij, sK[j * LD + tx + 16 * b], iq[b]);
+            for (int b = 0; b < NB; ++b) {
+                const int i = tx + 16 * b;
+                iq[b] = fmaf(aij * sK[j * LD + i], exp2f(sG[t * LD + i] - sG[j * LD + i]), iq[b]);
             }
-            for (int x = t; x < BC; ++x) {
-                const float axt = sAM[x * LA + t];
+        }
+        for (int x = t; x < BC; ++x) {
+            const float axt = sAM[x * LA + t];
 #pragma unroll
-                for (int b = 0; b < NB; ++b) ik[b] = fmaf(axt, sQ[x * LD + tx + 16 * b], ik[b]);
-            }
-        } else {
-            for (int j = 0; j <= t; ++j) {
-                const float aij = sAM[t * LA + j];
-#pragma unroll
-                for (int b = 0; b < NB; ++b) {
-                    const int i = tx + 16 * b;
-                    iq[b] = fmaf(aij * sK[j * LD + i], exp2f(sG[t * LD + i] - sG[j * LD + i]), iq[b]);
-                }
-            }
-            for (int x = t; x < BC; ++x) {
-                const float axt = sAM[x * LA + t];
-#pragma unroll
-                for (int b = 0; b < NB; ++b) {
-                    const int i = tx + 16 * b;
-                    ik[b] = fmaf(axt * sQ[x * LD + i], exp2f(sG[x * LD + i] - sG[t * LD + i]), ik[b]);
-                }
+            for (int b = 0; b < NB; ++b) {
+                const int i = tx + 16 * b;
+                ik[b] = fmaf(axt * sQ[x * LD + i], exp2f(sG[x * LD + i] - sG[t * LD + i]), ik[b]);
             }
         }
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
             const int i = tx + 16 * b;
-            const float g = sG[t * LD + i];
-            const float d = exact ? 0.f : g - sRef[i];
-            const float dq = s * exp2f(d) * iq[b] + pq[a][b];
-            const float dk = s * exp2f(-d) * ik[b] + pk[a][b];
+            const float dq = s * iq[b] + pq[a][b];
+            const float dk = s * ik[b] + pk[a][b];
             float pr = 0.f;
             if (t < n) {
                 const size_t off = rk + static_cast<size_t>(t) * DK + i;
@@ -1146,13 +1122,8 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdLaunch p) {
             const int j = tx + 16 * b;
             float m = 0.f;
             if (j <= t) {
-                if (!exact) {
-                    for (int i = 0; i < DK; ++i) m = fmaf(sQ[t * LD + i], sK[j * LD + i], m);
-                } else {
-                    for (int i = 0; i < DK; ++i)
-                        m = fmaf(sQ[t * LD + i] * sK[j * LD + i],
-                                 exp2f(sG[t * LD + i] - sG[j * LD + i]), m);
-                }
+                for (int i = 0; i < DK; ++i)
+                    m = fmaf(sQ[t * LD + i] * sK[j * LD + i], exp2f(sG[t * LD + i] - sG[j * LD + i]), m);
             }
             accA[a][b] = s * m;
         }
