@@ -945,9 +945,11 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
 // ---------------------------------------------------------------------------
 // 6. per-chunk gradients on CUDA cores, for the chunks the tensor-core kernel
 //    leaves (decay span beyond the reference split, or force_exact): every
-//    in-chunk decay factor e^(Gamma_t - Gamma_j) is its own exponential.  Thread (ty, tx) = (tid / 16, tid % 16) owns rows
-//    4 ty .. 4 ty + 3 and columns tx, tx + 16, ... of every C x C, C x dk and
-//    C x 32 block it computes.
+//    in-chunk decay factor e^(Gamma_t - Gamma_j) is its own exponential.
+//    Thread (ty, tx) = (tid / 16, tid % 16) owns rows 4 ty .. 4 ty + 3 and
+//    columns tx, tx + 16, ... of every C x C, C x dk and C x 32 block it
+//    computes.  (Kernels appear in this file in the order 1, 2, 5, 4, 6; the
+//    numbers are the launch order.)
 template <int DK>
 struct GradSmem {
     static constexpr int LD = DK + 1;      // odd strides: conflict-free column walks
