@@ -459,7 +459,6 @@ def bwd_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_ki
             g.manual_seed(5678 + rank)
             h0 = torch.randn(len(lens), cfg.H, cfg.dk, cfg.dv, generator=g, device=dev).mul_(0.1)
             dhT = torch.randn(len(lens), cfg.H, cfg.dk, cfg.dv, generator=g, device=dev).mul_(0.1)
-        plan = dict(plan, launches=plan["launches"] * sum(1 for m in lens if m > 0))
         srt = sorted(lens)
         packed = {"sequences": len(lens), "min_len": srt[0], "median_len": srt[len(srt) // 2],
                   "max_len": srt[-1], "lengths": "log-normal weights (sigma 1), seed 1234"}

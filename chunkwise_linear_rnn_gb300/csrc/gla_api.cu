@@ -615,101 +615,77 @@ int gla_recurrent_step(const void *q, const void *k, const void *v, const float 
 
 namespace {
 
-// Scratch of the chunkwise backward, in bytes: chunk-start states, state
-// gradients and per-tile log-gate carries, each 256-byte aligned.
-bool bwd_layout(int B, int H, int T, int dk, int dv, size_t *states, size_t *adjoints,
-                size_t *carry, size_t *decay, size_t *partials = nullptr) {
-    const long long BH = static_cast<long long>(B) * H;
-    const long long NC = (static_cast<long long>(T) + gla::bwd_chunk_tokens() - 1) /
-                         gla::bwd_chunk_tokens();
+// Scratch of the chunkwise backward for `units` (sequence, head) pairs whose
+// chunks number `chunks` in all, over `rows` rows of the caller's tensors:
+// chunk states (chunks + units slots) and state gradients (chunks slots) of
+// dk x dv fp32 each, per-chunk carries and decays, the partial gradients and
+// the path flags, each piece 256-byte aligned.
+struct BwdScratch {
+    size_t states, adjoints, carry, decay, partials, flags;
+    size_t total() const { return states + adjoints + carry + decay + partials + flags; }
+};
+
+BwdScratch bwd_layout(long long units, long long chunks, long long rows, int dk, int dv) {
     const auto al = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
-    *states = al(sizeof(float) * static_cast<size_t>(BH) * (NC + 1) * dk * dv);
-    *adjoints = al(sizeof(float) * static_cast<size_t>(BH) * NC * dk * dv);
-    *carry = al(sizeof(float) * static_cast<size_t>(BH) * NC * gla::bwd_value_tiles(dv) * dk);
-    *decay = al(sizeof(float) * static_cast<size_t>(BH) * NC * dk);
-    if (partials)
-        *partials = al(sizeof(float) * static_cast<size_t>(BH) * T * (2 * dk + dv)) +
-                    al(static_cast<size_t>(BH) * NC);   // + per-chunk path flags
-    return NC <= 0x7fffffffLL;
+    BwdScratch s;
+    s.states = al(sizeof(float) * static_cast<size_t>(chunks + units) * dk * dv);
+    s.adjoints = al(sizeof(float) * static_cast<size_t>(chunks) * dk * dv);
+    s.carry = al(sizeof(float) * static_cast<size_t>(chunks) * gla::bwd_value_tiles(dv) * dk);
+    s.decay = al(sizeof(float) * static_cast<size_t>(chunks) * dk);
+    s.partials = al(sizeof(float) * static_cast<size_t>(rows) * (2 * dk + dv));
+    s.flags = al(static_cast<size_t>(chunks));
+    return s;
 }
 
-// Points the scratch fields of p into ws (laid out by bwd_layout for B, H, T).
-void bwd_bind_scratch(gla::BwdLaunch &p, char *ws, int B, int H, int T, int dk, int dv) {
-    size_t st_b = 0, adj_b = 0, car_b = 0, dec_b = 0, par_b = 0;
-    bwd_layout(B, H, T, dk, dv, &st_b, &adj_b, &car_b, &dec_b, &par_b);
+// Points the scratch fields of p into ws, laid out as `s`.
+void bwd_bind_scratch(gla::BwdLaunch &p, char *ws, const BwdScratch &s, long long rows, int dk) {
     p.states = reinterpret_cast<float *>(ws);
-    p.adjoints = reinterpret_cast<float *>(ws + st_b);
-    p.carry = reinterpret_cast<float *>(ws + st_b + adj_b);
-    p.decay = reinterpret_cast<float *>(ws + st_b + adj_b + car_b);
-    p.pq = reinterpret_cast<float *>(ws + st_b + adj_b + car_b + dec_b);
-    p.pk = p.pq + static_cast<size_t>(B) * H * T * dk;
-    p.pv = p.pk + static_cast<size_t>(B) * H * T * dk;
-    p.wide = reinterpret_cast<unsigned char *>(
-        ws + st_b + adj_b + car_b + dec_b +
-        ((sizeof(float) * static_cast<size_t>(B) * H * T * (2 * dk + dv) + 255) & ~static_cast<size_t>(255)));
+    ws += s.states;
+    p.adjoints = reinterpret_cast<float *>(ws);
+    ws += s.adjoints;
+    p.carry = reinterpret_cast<float *>(ws);
+    ws += s.carry;
+    p.decay = reinterpret_cast<float *>(ws);
+    ws += s.decay;
+    p.pq = reinterpret_cast<float *>(ws);
+    p.pk = p.pq + static_cast<size_t>(rows) * dk;
+    p.pv = p.pk + static_cast<size_t>(rows) * dk;
+    ws += s.partials;
+    p.wide = reinterpret_cast<unsigned char *>(ws);
 }
+
+int bwd_chunks(int len) { return (len + gla::bwd_chunk_tokens() - 1) / gla::bwd_chunk_tokens(); }
 
 int bwd_shape_ok(int B, int H, int T, int dk, int dv) {
     if (B <= 0 || H <= 0 || T <= 0) return GLA_ERR_ARG;
-    if (static_cast<long long>(B) * H > 65535) return GLA_ERR_ARG;
+    if (H > 65535 || static_cast<long long>(B) * H > 0x7fffffffLL) return GLA_ERR_ARG;
+    if (static_cast<long long>(B) * bwd_chunks(T) > 0x7fffffffLL) return GLA_ERR_ARG;
     if (!gla::dk_ok(dk) || !gla::dv_ok(dv)) return GLA_ERR_SHAPE;
     return GLA_OK;
 }
 
-}  // namespace
-
-int gla_chunk_bwd_plan(int B, int H, int T, int dk, int dv, int *chunk, int *launches,
-                       unsigned long *scratch_bytes) {
-    const int st = bwd_shape_ok(B, H, T, dk, dv);
-    if (st != GLA_OK) return st;
-    size_t a = 0, b = 0, c = 0, d = 0, e = 0;
-    if (!bwd_layout(B, H, T, dk, dv, &a, &b, &c, &d, &e)) return GLA_ERR_ARG;
-    if (chunk) *chunk = gla::bwd_chunk_tokens();
-    if (launches) *launches = 6;
-    if (scratch_bytes) *scratch_bytes = static_cast<unsigned long>(a + b + c + d + e);
-    return GLA_OK;
+BwdScratch bwd_layout_fixed(int B, int H, int T, int dk, int dv) {
+    const long long units = static_cast<long long>(B) * H;
+    return bwd_layout(units, units * bwd_chunks(T), units * T, dk, dv);
 }
 
-int gla_chunk_bwd_ex(const void *q, const void *k, const void *v, const float *log_alpha,
-                     float scale, const float *h0, const void *d_o, const float *dhT,
-                     void *grad_q, void *grad_k, void *grad_v, float *grad_log_alpha,
-                     float *grad_h0, int B, int H, int T, int dk, int dv,
-                     const gla_chunk_options *opts, cudaStream_t stream) {
-    using namespace gla;
-    if (!q || !k || !v || !log_alpha || !d_o || !grad_q || !grad_k || !grad_v ||
-        !grad_log_alpha)
-        return GLA_ERR_ARG;
-    const int shape = bwd_shape_ok(B, H, T, dk, dv);
-    if (shape != GLA_OK) return shape;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(d_o) ||
-        !aligned16(grad_q) || !aligned16(grad_k) || !aligned16(grad_v) ||
-        !aligned16(log_alpha) || !aligned16(grad_log_alpha) || (h0 && !aligned16(h0)) ||
-        (dhT && !aligned16(dhT)) || (grad_h0 && !aligned16(grad_h0)))
-        return GLA_ERR_ARG;
-    gla_chunk_options o_def = {};
-    const gla_chunk_options &op = opts ? *opts : o_def;
-    if ((op.gate_per_head != 0 && op.gate_per_head != 1) ||
-        (op.force_exact != 0 && op.force_exact != 1))
-        return GLA_ERR_ARG;
-    size_t st_b = 0, adj_b = 0, car_b = 0, dec_b = 0, par_b = 0;
-    if (!bwd_layout(B, H, T, dk, dv, &st_b, &adj_b, &car_b, &dec_b, &par_b)) return GLA_ERR_ARG;
-    // one gate per head: the gate broadcast to every channel and its gradient, fp32 [BH, T, dk]
-    const size_t gate_b = op.gate_per_head
-                              ? ((sizeof(float) * static_cast<size_t>(B) * H * T * dk + 255) &
-                                 ~static_cast<size_t>(255))
-                              : 0;
+bool bwd_pointers_ok(const void *q, const void *k, const void *v, const float *log_alpha,
+                     const void *d_o, const void *grad_q, const void *grad_k, const void *grad_v,
+                     const float *grad_log_alpha, const float *h0, const float *dhT,
+                     const float *grad_h0) {
+    using gla::aligned16;
+    if (!q || !k || !v || !log_alpha || !d_o || !grad_q || !grad_k || !grad_v || !grad_log_alpha)
+        return false;
+    return aligned16(q) && aligned16(k) && aligned16(v) && aligned16(d_o) && aligned16(grad_q) &&
+           aligned16(grad_k) && aligned16(grad_v) && aligned16(log_alpha) &&
+           aligned16(grad_log_alpha) && (!h0 || aligned16(h0)) && (!dhT || aligned16(dhT)) &&
+           (!grad_h0 || aligned16(grad_h0));
+}
 
-    DeviceInfo *dev = nullptr;
-    const int st = current_device(&dev);
-    if (st != GLA_OK) return st;
-    char *ws = nullptr;
-    if (cudaMallocAsync(reinterpret_cast<void **>(&ws),
-                        st_b + adj_b + car_b + dec_b + par_b + 2 * gate_b, stream) !=
-        cudaSuccess) {
-        cudaGetLastError();
-        return GLA_ERR_ALLOC;
-    }
-    BwdLaunch p = {};
+void bwd_bind_tensors(gla::BwdLaunch &p, const void *q, const void *k, const void *v,
+                      const float *log_alpha, const float *h0, const void *d_o,
+                      const float *dhT, void *grad_q, void *grad_k, void *grad_v,
+                      float *grad_log_alpha, float *grad_h0) {
     p.q = static_cast<const __nv_bfloat16 *>(q);
     p.k = static_cast<const __nv_bfloat16 *>(k);
     p.v = static_cast<const __nv_bfloat16 *>(v);
@@ -722,22 +698,73 @@ int gla_chunk_bwd_ex(const void *q, const void *k, const void *v, const float *l
     p.gv = static_cast<__nv_bfloat16 *>(grad_v);
     p.ga = grad_log_alpha;
     p.gh0 = grad_h0;
-    bwd_bind_scratch(p, ws, B, H, T, dk, dv);
+}
+
+}  // namespace
+
+int gla_chunk_bwd_plan(int B, int H, int T, int dk, int dv, int *chunk, int *launches,
+                       unsigned long *scratch_bytes) {
+    const int st = bwd_shape_ok(B, H, T, dk, dv);
+    if (st != GLA_OK) return st;
+    if (chunk) *chunk = gla::bwd_chunk_tokens();
+    if (launches) *launches = 6;
+    if (scratch_bytes)
+        *scratch_bytes = static_cast<unsigned long>(bwd_layout_fixed(B, H, T, dk, dv).total());
+    return GLA_OK;
+}
+
+int gla_chunk_bwd_ex(const void *q, const void *k, const void *v, const float *log_alpha,
+                     float scale, const float *h0, const void *d_o, const float *dhT,
+                     void *grad_q, void *grad_k, void *grad_v, float *grad_log_alpha,
+                     float *grad_h0, int B, int H, int T, int dk, int dv,
+                     const gla_chunk_options *opts, cudaStream_t stream) {
+    using namespace gla;
+    if (!bwd_pointers_ok(q, k, v, log_alpha, d_o, grad_q, grad_k, grad_v, grad_log_alpha, h0,
+                         dhT, grad_h0))
+        return GLA_ERR_ARG;
+    const int shape = bwd_shape_ok(B, H, T, dk, dv);
+    if (shape != GLA_OK) return shape;
+    gla_chunk_options o_def = {};
+    const gla_chunk_options &op = opts ? *opts : o_def;
+    if ((op.gate_per_head != 0 && op.gate_per_head != 1) ||
+        (op.force_exact != 0 && op.force_exact != 1))
+        return GLA_ERR_ARG;
+    const BwdScratch sl = bwd_layout_fixed(B, H, T, dk, dv);
+    const long long rows = static_cast<long long>(B) * H * T;
+    // one gate per head: the gate broadcast to every channel and its gradient, fp32 [BH, T, dk]
+    const size_t gate_b = op.gate_per_head
+                              ? ((sizeof(float) * static_cast<size_t>(rows) * dk + 255) &
+                                 ~static_cast<size_t>(255))
+                              : 0;
+
+    DeviceInfo *dev = nullptr;
+    const int st = current_device(&dev);
+    if (st != GLA_OK) return st;
+    char *ws = nullptr;
+    if (cudaMallocAsync(reinterpret_cast<void **>(&ws), sl.total() + 2 * gate_b, stream) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return GLA_ERR_ALLOC;
+    }
+    BwdLaunch p = {};
+    bwd_bind_tensors(p, q, k, v, log_alpha, h0, d_o, dhT, grad_q, grad_k, grad_v,
+                     grad_log_alpha, grad_h0);
+    bwd_bind_scratch(p, ws, sl, rows, dk);
     p.status = dev->status;
     p.scale = scale;
-    p.BH = B * H;
+    p.seqs = nullptr;
+    p.N = B;
+    p.H = H;
     p.T = T;
-    p.NC = (T + bwd_chunk_tokens() - 1) / bwd_chunk_tokens();
+    p.NC = bwd_chunks(T);
+    p.chunks = static_cast<long long>(B) * p.NC;
     p.dk = dk;
     p.dv = dv;
-    p.sk = static_cast<long long>(T) * dk;
-    p.sv = static_cast<long long>(T) * dv;
     p.force_exact = op.force_exact;
     int r = GLA_OK;
-    const long long rows = static_cast<long long>(B) * H * T;
     if (op.gate_per_head) {
-        float *full = reinterpret_cast<float *>(ws + st_b + adj_b + car_b + dec_b + par_b);
-        float *gfull = reinterpret_cast<float *>(ws + st_b + adj_b + car_b + dec_b + par_b + gate_b);
+        float *full = reinterpret_cast<float *>(ws + sl.total());
+        float *gfull = reinterpret_cast<float *>(ws + sl.total() + gate_b);
         if (launch_gate_broadcast(log_alpha, full, rows, dk, stream) != 0) r = GLA_ERR_LAUNCH;
         p.log_alpha = full;
         p.ga = gfull;
@@ -764,81 +791,65 @@ int gla_chunk_bwd_varlen_ex(const void *q, const void *k, const void *v, const f
                             float *grad_h0, const int *cu_seqlens, int N, int H, int T_total,
                             int dk, int dv, const gla_chunk_options *opts, cudaStream_t stream) {
     using namespace gla;
-    if (!q || !k || !v || !log_alpha || !d_o || !grad_q || !grad_k || !grad_v ||
-        !grad_log_alpha || !cu_seqlens)
+    if (!bwd_pointers_ok(q, k, v, log_alpha, d_o, grad_q, grad_k, grad_v, grad_log_alpha, h0,
+                         dhT, grad_h0) || !cu_seqlens)
         return GLA_ERR_ARG;
-    if (N <= 0 || H <= 0 || T_total < 0 || H > 65535) return GLA_ERR_ARG;
+    if (N <= 0 || H <= 0 || T_total < 0 || H > 65535 ||
+        static_cast<long long>(N) * H > 0x7fffffffLL)
+        return GLA_ERR_ARG;
     if (!dk_ok(dk) || !dv_ok(dv)) return GLA_ERR_SHAPE;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(d_o) ||
-        !aligned16(grad_q) || !aligned16(grad_k) || !aligned16(grad_v) ||
-        !aligned16(log_alpha) || !aligned16(grad_log_alpha) || (h0 && !aligned16(h0)) ||
-        (dhT && !aligned16(dhT)) || (grad_h0 && !aligned16(grad_h0)))
-        return GLA_ERR_ARG;
     gla_chunk_options o_def = {};
     const gla_chunk_options &op = opts ? *opts : o_def;
     if (op.gate_per_head != 0 || (op.force_exact != 0 && op.force_exact != 1)) return GLA_ERR_ARG;
     if (cu_seqlens[0] != 0 || cu_seqlens[N] != T_total) return GLA_ERR_ARG;
-    int max_len = 0;
+    // the sequence table {first row, length, chunks, first chunk}, 64-token chunks
+    std::vector<int4> seqs(N);
+    long long chunks = 0;
     for (int n = 0; n < N; ++n) {
         const int len = cu_seqlens[n + 1] - cu_seqlens[n];
         if (len < 0) return GLA_ERR_ARG;
-        max_len = std::max(max_len, len);
+        seqs[n] = make_int4(cu_seqlens[n], len, bwd_chunks(len), static_cast<int>(chunks));
+        chunks += bwd_chunks(len);
+        if (chunks > 0x7fffffffLL) return GLA_ERR_ARG;
     }
     DeviceInfo *dev = nullptr;
     const int st = current_device(&dev);
     if (st != GLA_OK) return st;
-    const size_t state = static_cast<size_t>(H) * dk * dv;   // one sequence's states, all heads
+    const long long units = static_cast<long long>(N) * H, rows = static_cast<long long>(H) * T_total;
+    const BwdScratch sl = bwd_layout(units, chunks * H, rows, dk, dv);
+    const size_t table_b = (sizeof(int4) * static_cast<size_t>(N) + 255) & ~static_cast<size_t>(255);
     char *ws = nullptr;
-    if (max_len > 0) {
-        size_t a = 0, b = 0, c = 0, d = 0, e = 0;
-        if (!bwd_layout(1, H, max_len, dk, dv, &a, &b, &c, &d, &e)) return GLA_ERR_ARG;
-        if (cudaMallocAsync(reinterpret_cast<void **>(&ws), a + b + c + d + e, stream) !=
-            cudaSuccess) {
-            cudaGetLastError();
-            return GLA_ERR_ALLOC;
-        }
+    if (cudaMallocAsync(reinterpret_cast<void **>(&ws), table_b + sl.total(), stream) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return GLA_ERR_ALLOC;
     }
     int r = GLA_OK;
-    for (int n = 0; n < N && r == GLA_OK; ++n) {
-        const int bos = cu_seqlens[n], len = cu_seqlens[n + 1] - bos;
-        if (len == 0) {   // nothing flows through: dh0 = dhT (zero without one)
-            if (grad_h0) {
-                const cudaError_t ce =
-                    dhT ? cudaMemcpyAsync(grad_h0 + n * state, dhT + n * state,
-                                          sizeof(float) * state, cudaMemcpyDeviceToDevice, stream)
-                        : cudaMemsetAsync(grad_h0 + n * state, 0, sizeof(float) * state, stream);
-                if (ce != cudaSuccess) r = GLA_ERR_LAUNCH;
-            }
-            continue;
-        }
-        const size_t ok_ = static_cast<size_t>(bos) * dk, ov = static_cast<size_t>(bos) * dv;
+    // a copy from pageable memory has taken the host table by the time it returns
+    if (cudaMemcpyAsync(ws, seqs.data(), sizeof(int4) * static_cast<size_t>(N),
+                        cudaMemcpyHostToDevice, stream) != cudaSuccess) {
+        cudaGetLastError();
+        r = GLA_ERR_LAUNCH;
+    }
+    if (r == GLA_OK) {
         BwdLaunch p = {};
-        p.q = static_cast<const __nv_bfloat16 *>(q) + ok_;
-        p.k = static_cast<const __nv_bfloat16 *>(k) + ok_;
-        p.v = static_cast<const __nv_bfloat16 *>(v) + ov;
-        p.d_o = static_cast<const __nv_bfloat16 *>(d_o) + ov;
-        p.log_alpha = log_alpha + ok_;
-        p.h0 = h0 ? h0 + n * state : nullptr;
-        p.dhT = dhT ? dhT + n * state : nullptr;
-        p.gq = static_cast<__nv_bfloat16 *>(grad_q) + ok_;
-        p.gk = static_cast<__nv_bfloat16 *>(grad_k) + ok_;
-        p.gv = static_cast<__nv_bfloat16 *>(grad_v) + ov;
-        p.ga = grad_log_alpha + ok_;
-        p.gh0 = grad_h0 ? grad_h0 + n * state : nullptr;
-        bwd_bind_scratch(p, ws, 1, H, len, dk, dv);
+        bwd_bind_tensors(p, q, k, v, log_alpha, h0, d_o, dhT, grad_q, grad_k, grad_v,
+                         grad_log_alpha, grad_h0);
+        bwd_bind_scratch(p, ws + table_b, sl, rows, dk);
         p.status = dev->status;
         p.scale = scale;
-        p.BH = H;
-        p.T = len;
-        p.NC = (len + bwd_chunk_tokens() - 1) / bwd_chunk_tokens();
+        p.seqs = reinterpret_cast<const int4 *>(ws);
+        p.N = N;
+        p.H = H;
+        p.T = T_total;
+        p.NC = 0;
+        p.chunks = chunks;
         p.dk = dk;
         p.dv = dv;
-        p.sk = static_cast<long long>(T_total) * dk;   // head stride of the packed tensors
-        p.sv = static_cast<long long>(T_total) * dv;
         p.force_exact = op.force_exact;
         if (launch_chunk_bwd(p, stream) != 0) r = GLA_ERR_LAUNCH;
     }
-    if (ws) cudaFreeAsync(ws, stream);
+    cudaFreeAsync(ws, stream);
     return r;
 }
 

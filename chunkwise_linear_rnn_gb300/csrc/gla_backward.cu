@@ -69,13 +69,75 @@ __device__ __forceinline__ void split_pair(float x, float y, uint32_t &hi, uint3
     lo = pack_bf16x2(x - hx, y - hy);
 }
 
-// Per-chunk states and state gradients live in scratch as [BH][dk][dv/32]
-// [slots][32]: the 32-column groups of one row, chunk after chunk, so that a
-// scan over the chunks reads and writes whole consecutive lines.
+// One unit (sequence n, head h; index n H + h) of the work, and where its
+// pieces of scratch begin.  Chunk states and state gradients live as
+// [unit][dk][dv/32][slot][32]: the 32-column groups of one row, chunk after
+// chunk, so that a scan over the chunks reads and writes whole consecutive
+// lines; a unit has nch + 1 state slots and nch gradient slots.  Per-chunk
+// arrays (decay, carry, flags) hold a unit's nch chunks from `cbase` on.
+struct Unit {
+    int nch;             // chunks of the sequence
+    long long sbase;     // first state slot of the unit
+    long long rbase;     // first gradient slot (also `cbase`)
+};
+
+__device__ __forceinline__ Unit unit_at(const BwdLaunch &p, int unit) {
+    Unit w;
+    if (!p.seqs) {
+        w.nch = p.NC;
+        w.sbase = static_cast<long long>(unit) * (p.NC + 1);
+        w.rbase = static_cast<long long>(unit) * p.NC;
+    } else {
+        const int n = unit / p.H, h = unit % p.H;
+        const int4 sq = p.seqs[n];   // {first row, length, chunks, first chunk}
+        w.nch = sq.z;
+        w.sbase = static_cast<long long>(sq.w + n) * p.H + static_cast<long long>(h) * (sq.z + 1);
+        w.rbase = static_cast<long long>(sq.w) * p.H + static_cast<long long>(h) * sq.z;
+    }
+    return w;
+}
+
+// Chunk g (over all sequences) of head h.
+struct Chunk {
+    Unit w;
+    int unit;            // n H + h
+    int c;               // chunk within the sequence
+    int n;               // valid rows (<= BC)
+    long long row;       // its first row in the caller's tensors, in rows of dk / dv elements
+};
+
+__device__ __forceinline__ Chunk chunk_at(const BwdLaunch &p, long long g, int h) {
+    Chunk k;
+    if (!p.seqs) {
+        const int b = static_cast<int>(g / p.NC);
+        k.c = static_cast<int>(g % p.NC);
+        k.unit = b * p.H + h;
+        k.n = min(BC, p.T - k.c * BC);
+        k.row = static_cast<long long>(k.unit) * p.T + static_cast<long long>(k.c) * BC;
+    } else {
+        // the last sequence whose first chunk is <= g (empty ones share a first chunk
+        // with the sequence after them, which is then the one found)
+        int lo = 0, hi = p.N - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.seqs[mid].w <= g) lo = mid;
+            else hi = mid - 1;
+        }
+        const int4 sq = p.seqs[lo];
+        k.c = static_cast<int>(g - sq.w);
+        k.unit = lo * p.H + h;
+        k.n = min(BC, sq.y - k.c * BC);
+        k.row = static_cast<long long>(h) * p.T + sq.x + static_cast<long long>(k.c) * BC;
+    }
+    k.w = unit_at(p, k.unit);
+    return k;
+}
+
+// Float offset of (row i, column c) of slot u in a unit's states or gradients.
 template <int DK, int DV>
-__device__ __forceinline__ size_t slot_index(int bh, int i, int c, int u, int slots) {
-    return ((static_cast<size_t>(bh) * DK + i) * (DV / 32) + (c >> 5)) * slots * 32 +
-           static_cast<size_t>(u) * 32 + (c & 31);
+__device__ __forceinline__ size_t slot_index(long long base, int i, int c, int u, int slots) {
+    return static_cast<size_t>(base) * DK * DV +
+           ((static_cast<size_t>(i) * (DV / 32) + (c >> 5)) * slots + u) * 32 + (c & 31);
 }
 
 // Load one chunk of log-gates (log2 units, rows past the sequence end zero,
@@ -144,11 +206,11 @@ __global__ void __launch_bounds__(kSumThreads, 2) bwd_sums_kernel(BwdLaunch p) {
     float *sG = reinterpret_cast<float *>(sm + L::kG);
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::kBar);
     uint32_t *slot = reinterpret_cast<uint32_t *>(sm + L::kSlot);
-    const int u = blockIdx.x, bh = blockIdx.y, which = blockIdx.z;
+    const Chunk ck = chunk_at(p, blockIdx.x, blockIdx.y);
+    const int u = ck.c, n = ck.n, which = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int t0 = u * BC, n = min(BC, p.T - t0);
-    const size_t rk = static_cast<size_t>(bh) * p.sk + static_cast<size_t>(t0) * DK;   // user key rows
-    const size_t rv = static_cast<size_t>(bh) * p.sv + static_cast<size_t>(t0) * DV;   // user value rows
+    const size_t rk = static_cast<size_t>(ck.row) * DK;   // first row, key-side tensors
+    const size_t rv = static_cast<size_t>(ck.row) * DV;   // first row, value-side tensors
 
     if (warp == 0) tmem_alloc(slot, DV);
     if (tid == 0) {
@@ -223,8 +285,9 @@ __global__ void __launch_bounds__(kSumThreads, 2) bwd_sums_kernel(BwdLaunch p) {
     // Each 32-column group of a row is one 128-byte line of the scratch.
     const int i = 32 * (warp & 3) + (tid & 31);
     const float mult = which ? p.scale : 1.f;
-    const int slots = which ? p.NC : p.NC + 1;
-    float *dst = (which ? p.adjoints : p.states) + slot_index<DK, DV>(bh, i < DK ? i : 0, 0, u, slots);
+    const int slots = which ? ck.w.nch : ck.w.nch + 1;
+    float *dst = (which ? p.adjoints : p.states) +
+                 slot_index<DK, DV>(which ? ck.w.rbase : ck.w.sbase, i < DK ? i : 0, 0, u, slots);
     const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
     const int cbeg = warp < 4 ? 0 : DV / 2, cend = warp < 4 ? DV / 2 : DV;
 #pragma unroll 1
@@ -242,7 +305,7 @@ __global__ void __launch_bounds__(kSumThreads, 2) bwd_sums_kernel(BwdLaunch p) {
         }
     }
     if (which == 0 && warp < 4 && i < DK)
-        p.decay[(static_cast<size_t>(bh) * p.NC + u) * DK + i] = exp2f(sG[(BC - 1) * DK + i]);
+        p.decay[static_cast<size_t>(ck.w.rbase + u) * DK + i] = exp2f(sG[(BC - 1) * DK + i]);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, DV);
@@ -261,54 +324,56 @@ constexpr int kScanUnroll = 16;
 template <int DK, int DV>
 __global__ void __launch_bounds__(256, 3) bwd_state_scan_kernel(BwdLaunch p) {
     const size_t e = static_cast<size_t>(blockIdx.x) * 256 + threadIdx.x;
-    const int bh = static_cast<int>(e / (DK * DV));
+    const Unit w = unit_at(p, static_cast<int>(e / (DK * DV)));
+    const int NCu = w.nch;
     const int rem = static_cast<int>(e % (DK * DV)), i = rem / DV;
     constexpr size_t kM = 32;   // one slot step
-    float *buf = p.states + slot_index<DK, DV>(bh, i, rem % DV, 0, p.NC + 1);
-    const float *dec = p.decay + static_cast<size_t>(bh) * p.NC * DK + i;
+    float *buf = p.states + slot_index<DK, DV>(w.sbase, i, rem % DV, 0, NCu + 1);
+    const float *dec = p.decay + static_cast<size_t>(w.rbase) * DK + i;
     float S = p.h0 ? p.h0[e] : 0.f;
     float d[kScanUnroll], a[kScanUnroll];
     auto fetch = [&](int u0) {
 #pragma unroll
         for (int j = 0; j < kScanUnroll; ++j) {
-            if (u0 + j < p.NC) {
+            if (u0 + j < NCu) {
                 d[j] = buf[(u0 + j) * kM];
                 a[j] = dec[static_cast<size_t>(u0 + j) * DK];
             }
         }
     };
     fetch(0);
-    for (int u0 = 0; u0 < p.NC; u0 += kScanUnroll) {
+    for (int u0 = 0; u0 < NCu; u0 += kScanUnroll) {
         float dn[kScanUnroll], an[kScanUnroll];
 #pragma unroll
         for (int j = 0; j < kScanUnroll; ++j) {
             dn[j] = d[j];
             an[j] = a[j];
         }
-        if (u0 + kScanUnroll < p.NC) fetch(u0 + kScanUnroll);   // next group in flight
+        if (u0 + kScanUnroll < NCu) fetch(u0 + kScanUnroll);   // next group in flight
 #pragma unroll
         for (int j = 0; j < kScanUnroll; ++j) {
-            if (u0 + j < p.NC) {
+            if (u0 + j < NCu) {
                 buf[(u0 + j) * kM] = S;
                 S = fmaf(an[j], S, dn[j]);
             }
         }
     }
-    buf[static_cast<size_t>(p.NC) * kM] = S;
+    buf[static_cast<size_t>(NCu) * kM] = S;
 }
 
 template <int DK, int DV>
 __global__ void __launch_bounds__(256, 2) bwd_adjoint_scan_kernel(BwdLaunch p) {
     constexpr int NTILE = DV / TW;
     const size_t e = static_cast<size_t>(blockIdx.x) * 256 + threadIdx.x;
-    const int bh = static_cast<int>(e / (DK * DV));
+    const Unit w = unit_at(p, static_cast<int>(e / (DK * DV)));
+    const int NCu = w.nch;
     const int rem = static_cast<int>(e % (DK * DV)), i = rem / DV, c = rem % DV;
     const int lane = threadIdx.x & 31;
     constexpr size_t kM = 32;   // one slot step
-    float *buf = p.adjoints + slot_index<DK, DV>(bh, i, c, 0, p.NC);
-    const float *st = p.states + slot_index<DK, DV>(bh, i, c, 0, p.NC + 1);
-    const float *dec = p.decay + static_cast<size_t>(bh) * p.NC * DK + i;
-    float *carry = p.carry + static_cast<size_t>(bh) * p.NC * NTILE * DK + (c / TW) * DK + i;
+    float *buf = p.adjoints + slot_index<DK, DV>(w.rbase, i, c, 0, NCu);
+    const float *st = p.states + slot_index<DK, DV>(w.sbase, i, c, 0, NCu + 1);
+    const float *dec = p.decay + static_cast<size_t>(w.rbase) * DK + i;
+    float *carry = p.carry + static_cast<size_t>(w.rbase) * NTILE * DK + (c / TW) * DK + i;
     float R = p.dhT ? p.dhT[e] : 0.f;
     float d[kScanUnroll], a[kScanUnroll], sn[kScanUnroll];
     auto fetch = [&](int u0) {
@@ -321,8 +386,8 @@ __global__ void __launch_bounds__(256, 2) bwd_adjoint_scan_kernel(BwdLaunch p) {
             }
         }
     };
-    fetch(p.NC - 1);
-    for (int u0 = p.NC - 1; u0 >= 0; u0 -= kScanUnroll) {
+    fetch(NCu - 1);
+    for (int u0 = NCu - 1; u0 >= 0; u0 -= kScanUnroll) {
         float dc[kScanUnroll], ac[kScanUnroll], sc[kScanUnroll];
 #pragma unroll
         for (int j = 0; j < kScanUnroll; ++j) {
@@ -395,14 +460,13 @@ __global__ void __launch_bounds__(kInterThreads, 1) bwd_inter_kernel(BwdLaunch p
     float *sG = reinterpret_cast<float *>(sm + L::kG);
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::kBar);
     uint32_t *slot = reinterpret_cast<uint32_t *>(sm + L::kSlot);
-    const int u = blockIdx.x, bh = blockIdx.y;
-    if (!p.wide[static_cast<size_t>(bh) * p.NC + u]) return;   // done by bwd_intra
+    const Chunk ck = chunk_at(p, blockIdx.x, blockIdx.y);
+    const int u = ck.c, n = ck.n;
+    if (!p.wide[ck.w.rbase + u]) return;   // done by bwd_intra
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int t0 = u * BC, n = min(BC, p.T - t0);
-    const size_t rk = static_cast<size_t>(bh) * p.sk + static_cast<size_t>(t0) * DK;   // user key rows
-    const size_t rv = static_cast<size_t>(bh) * p.sv + static_cast<size_t>(t0) * DV;   // user value rows
-    const size_t xk = (static_cast<size_t>(bh) * p.T + t0) * DK;   // scratch partials, key side
-    const size_t xv = (static_cast<size_t>(bh) * p.T + t0) * DV;   // scratch partials, value side
+    // first rows of the caller's tensors; the partials use the same offsets
+    const size_t rk = static_cast<size_t>(ck.row) * DK, rv = static_cast<size_t>(ck.row) * DV;
+    const size_t xk = rk, xv = rv;
 
     if (warp == 0) tmem_alloc(slot, L::kCols);
     if (tid == 0) {
@@ -447,9 +511,9 @@ __global__ void __launch_bounds__(kInterThreads, 1) bwd_inter_kernel(BwdLaunch p
                 rr[m] = sv[m];
                 if (i < DK && cb + cl < DV) {
                     sv[m] = *reinterpret_cast<const float4 *>(
-                        p.states + slot_index<DK, DV>(bh, i, cb + cl, u, p.NC + 1));
+                        p.states + slot_index<DK, DV>(ck.w.sbase, i, cb + cl, u, ck.w.nch + 1));
                     rr[m] = *reinterpret_cast<const float4 *>(
-                        p.adjoints + slot_index<DK, DV>(bh, i, cb + cl, u, p.NC));
+                        p.adjoints + slot_index<DK, DV>(ck.w.rbase, i, cb + cl, u, ck.w.nch));
                 }
             }
 #pragma unroll
@@ -612,11 +676,11 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
     float *sRef = reinterpret_cast<float *>(sm + L::kRef), *sGC = sRef + DK, *sCarry = sGC + DK;
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::kBar);
     uint32_t *slot = reinterpret_cast<uint32_t *>(sm + L::kSlot);
-    const int u = blockIdx.x, bh = blockIdx.y;
+    const Chunk ck = chunk_at(p, blockIdx.x, blockIdx.y);
+    const int u = ck.c, n = ck.n;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int t0 = u * BC, n = min(BC, p.T - t0);
-    const size_t rk = static_cast<size_t>(bh) * p.sk + static_cast<size_t>(t0) * DK;   // user key rows
-    const size_t rv = static_cast<size_t>(bh) * p.sv + static_cast<size_t>(t0) * DV;   // user value rows
+    const size_t rk = static_cast<size_t>(ck.row) * DK;   // first row, key-side tensors
+    const size_t rv = static_cast<size_t>(ck.row) * DV;   // first row, value-side tensors
     const float s = p.scale;
 
     // loads first: q, k pairs and dO, V 16-byte groups; then the prefix sums
@@ -645,11 +709,11 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
         wide = (g0 - gl) > kMaxSpan;
         float c = 0.f;
         for (int x = 0; x < NTILE; ++x)
-            c += p.carry[((static_cast<size_t>(bh) * p.NC + u) * NTILE + x) * DK + tid];
+            c += p.carry[(static_cast<size_t>(ck.w.rbase + u) * NTILE + x) * DK + tid];
         sCarry[tid] = c;
     }
     const bool exact = __syncthreads_or(wide) || p.force_exact;
-    if (tid == 0) p.wide[static_cast<size_t>(bh) * p.NC + u] = exact ? 1 : 0;
+    if (tid == 0) p.wide[ck.w.rbase + u] = exact ? 1 : 0;
     if (exact) return;   // the CUDA-core kernel takes this chunk
 
     if (warp == 0) tmem_alloc(slot, L::kCols);
@@ -782,9 +846,9 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
         for (int m = 0; m < SPER; ++m) {
             const int e = tid + m * NTI, i = e / 16, cl = (e % 16) * 4;
             sv[m] = *reinterpret_cast<const float4 *>(
-                p.states + slot_index<DK, DV>(bh, i, c0 + cl, u, p.NC + 1));
+                p.states + slot_index<DK, DV>(ck.w.sbase, i, c0 + cl, u, ck.w.nch + 1));
             rr[m] = *reinterpret_cast<const float4 *>(
-                p.adjoints + slot_index<DK, DV>(bh, i, c0 + cl, u, p.NC));
+                p.adjoints + slot_index<DK, DV>(ck.w.rbase, i, c0 + cl, u, ck.w.nch));
         }
     };
     fetch(0);
@@ -974,14 +1038,13 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdLaunch p) {
     float *sAM = smem + L::kAM, *sDo = smem + L::kDo, *sV = smem + L::kV;
     float *sCarry = smem + L::kCarry;
 
-    const int u = blockIdx.x, bh = blockIdx.y;
-    if (!p.wide[static_cast<size_t>(bh) * p.NC + u]) return;   // done by the tensor-core kernel
+    const Chunk ck = chunk_at(p, blockIdx.x, blockIdx.y);
+    const int u = ck.c, n = ck.n;
+    if (!p.wide[ck.w.rbase + u]) return;   // done by the tensor-core kernel
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-    const int t0 = u * BC, n = min(BC, p.T - t0);
-    const size_t rk = static_cast<size_t>(bh) * p.sk + static_cast<size_t>(t0) * DK;   // user key rows
-    const size_t rv = static_cast<size_t>(bh) * p.sv + static_cast<size_t>(t0) * DV;   // user value rows
-    const size_t xk = (static_cast<size_t>(bh) * p.T + t0) * DK;   // scratch partials, key side
-    const size_t xv = (static_cast<size_t>(bh) * p.T + t0) * DV;   // scratch partials, value side
+    // first rows of the caller's tensors; the partials use the same offsets
+    const size_t rk = static_cast<size_t>(ck.row) * DK, rv = static_cast<size_t>(ck.row) * DV;
+    const size_t xk = rk, xv = rv;
     const float s = p.scale;
 
     // the state terms of dq and dk (bwd_inter), fetched early for phase 2
@@ -1001,7 +1064,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdLaunch p) {
     if (tid < DK) {
         float c = 0.f;
         for (int x = 0; x < NTILE; ++x)
-            c += p.carry[((static_cast<size_t>(bh) * p.NC + u) * NTILE + x) * DK + tid];
+            c += p.carry[(static_cast<size_t>(ck.w.rbase + u) * NTILE + x) * DK + tid];
         sCarry[tid] = c;
     }
 
@@ -1248,13 +1311,20 @@ int launch_bwd_dims(const BwdLaunch &p, cudaStream_t stream) {
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(grad_bytes));
     if (e != cudaSuccess) return static_cast<int>(e);
-    const unsigned scan_blocks = static_cast<unsigned>(static_cast<size_t>(p.BH) * DK * DV / 256);
-    bwd_sums_kernel<DK, DV><<<dim3(p.NC, p.BH, 2), kSumThreads, sum_bytes, stream>>>(p);
+    const unsigned scan_blocks =
+        static_cast<unsigned>(static_cast<size_t>(p.N) * p.H * DK * DV / 256);
+    const unsigned nchunks = static_cast<unsigned>(p.chunks);
+    if (nchunks == 0) {   // only empty sequences: dh0 = dhT (the scans walk no chunk)
+        bwd_state_scan_kernel<DK, DV><<<scan_blocks, 256, 0, stream>>>(p);
+        bwd_adjoint_scan_kernel<DK, DV><<<scan_blocks, 256, 0, stream>>>(p);
+        return static_cast<int>(cudaGetLastError());
+    }
+    bwd_sums_kernel<DK, DV><<<dim3(nchunks, p.H, 2), kSumThreads, sum_bytes, stream>>>(p);
     bwd_state_scan_kernel<DK, DV><<<scan_blocks, 256, 0, stream>>>(p);
     bwd_adjoint_scan_kernel<DK, DV><<<scan_blocks, 256, 0, stream>>>(p);
-    bwd_intra_kernel<DK, DV><<<dim3(p.NC, p.BH), kIntraThreads, intra_bytes, stream>>>(p);
-    bwd_inter_kernel<DK, DV><<<dim3(p.NC, p.BH), kInterThreads, inter_bytes, stream>>>(p);
-    bwd_grads_kernel<DK, DV><<<dim3(p.NC, p.BH), NT, grad_bytes, stream>>>(p);
+    bwd_intra_kernel<DK, DV><<<dim3(nchunks, p.H), kIntraThreads, intra_bytes, stream>>>(p);
+    bwd_inter_kernel<DK, DV><<<dim3(nchunks, p.H), kInterThreads, inter_bytes, stream>>>(p);
+    bwd_grads_kernel<DK, DV><<<dim3(nchunks, p.H), NT, grad_bytes, stream>>>(p);
     return static_cast<int>(cudaGetLastError());
 }
 

@@ -91,20 +91,24 @@ struct BwdLaunch {
     __nv_bfloat16 *gq, *gk, *gv;             // gradients of q, k, v
     float *ga;                               // gradient of log_alpha [BH, T, dk]
     float *gh0;                              // gradient of h0 [BH, dk, dv] or null
-    float *states;                           // scratch [BH, NC + 1, dk, dv]
-    float *adjoints;                         // scratch [BH, NC, dk, dv]
-    float *carry;                            // scratch [BH, NC, dv / 32, dk]
-    float *decay;                            // scratch [BH, NC, dk]: e^Gamma_C per chunk
-    float *pq, *pk;                          // scratch [BH, T, dk]: state terms of dq, dk
-    float *pv;                               // scratch [BH, T, dv]: state term of dv
-    unsigned char *wide;                     // scratch [BH, NC]: 1 = chunk left to the CUDA-core kernel
+    // Scratch.  Per unit, chunk states (nch + 1 slots) and state gradients
+    // (nch slots) of dk x dv fp32 each; per unit and chunk, the log-gate
+    // carry (dv / 32 x dk), the chunk decay (dk) and the path flag; partial
+    // gradients laid out like the caller's q / v rows.
+    float *states, *adjoints, *carry, *decay;
+    float *pq, *pk, *pv;
+    unsigned char *wide;                     // 1 = chunk left to the exact-path kernels
     unsigned int *status;                    // device status word (bounded waits)
     float scale;
-    int BH, T, NC, dk, dv;
-    // elements between consecutive (batch, head) rows of the caller's tensors:
-    // T * dk and T * dv for [BH, T, .] tensors; a packed sequence of a
-    // [H, T_total, .] batch is a strided view with T_total * dk / T_total * dv
-    long long sk, sv;
+    // Work: N sequences of H heads; unit n H + h indexes h0, dhT and dh0.
+    // Fixed length (seqs == null): the caller's tensors are [N, H, T, .] and
+    // every sequence has NC chunks.  Packed (seqs set): the tensors are
+    // [H, T, .] with T the packed length, and seqs[n] = {first row, length,
+    // chunks, first chunk} describes sequence n.  `chunks` counts the chunks
+    // of all sequences (one head).
+    const int4 *seqs;
+    int N, H, T, NC, dk, dv;
+    long long chunks;
     int force_exact;
 };
 

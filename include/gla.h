@@ -279,7 +279,7 @@ int gla_recurrent_step(const void *q, const void *k, const void *v, const float 
  * log-gate carries, NC = ceil(T / 64), taken stream-ordered (cudaMallocAsync) and released on
  * `stream` (GLA_ERR_ALLOC when the pool cannot supply it).
  *
- * Shapes as for gla_chunk_fwd, with B * H <= 65535; pointers 16-byte aligned.
+ * Shapes as for gla_chunk_fwd, with H <= 65535; pointers 16-byte aligned.
  * A bounded device wait that expires leaves the gradients unspecified and is
  * reported by gla_last_device_status (GLA_ERR_TIMEOUT).  Accuracy: each gradient matches the fp64 reverse-mode
  * differentiation of the recurrence to relative L2 error <= 1e-2 and max-abs
@@ -321,10 +321,10 @@ int gla_chunk_bwd_plan(int B, int H, int T, int dk, int dv, int *chunk, int *lau
  *   v, d_o, grad_v                                   : [H, T_total, dv]
  *   h0, dhT, grad_h0                                 : [N, H, dk, dv] (each nullable)
  *   cu_seqlens : HOST array of N + 1 ints, from 0 to T_total, nondecreasing.
- * Each sequence runs the gla_chunk_bwd kernels on its rows (a strided view
- * of the packed tensors), one after another on `stream`, with one scratch
- * sized for the longest sequence; an empty sequence gets grad_h0 = dhT (zero
- * without dhT).  Per-head gates are not supported here (GLA_ERR_ARG).
+ * One set of launches covers every chunk of every sequence (a table of the
+ * sequences goes up to stream-ordered scratch with the call); an empty
+ * sequence gets grad_h0 = dhT (zero without dhT).  Per-head gates are not
+ * supported here (GLA_ERR_ARG).
  * Errors as for gla_chunk_bwd and gla_chunk_fwd_varlen.
  */
 int gla_chunk_bwd_varlen(const void *q, const void *k, const void *v, const float *log_alpha,

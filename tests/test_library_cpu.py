@@ -209,7 +209,7 @@ def test_backward_rejects_null(lib, field):
 
 def test_backward_validates_on_the_host(lib):
     assert _bwd(lib, T=0) == _lib.GLA_ERR_ARG
-    assert _bwd(lib, B=70000) == _lib.GLA_ERR_ARG            # B * H beyond the grid's y extent
+    assert _bwd(lib, H=70000) == _lib.GLA_ERR_ARG            # H beyond the grid's y extent
     assert _bwd(lib, dk=96) == _lib.GLA_ERR_SHAPE
     assert _bwd(lib, dv=32) == _lib.GLA_ERR_SHAPE
     assert _bwd(lib, q=P + 2) == _lib.GLA_ERR_ARG            # 16-byte alignment
