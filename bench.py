@@ -56,15 +56,22 @@ def peaks():
 # one call) measured with ncu on the long workload at full size, with the
 # sources whose hash is given (profiles/chunk_fwd_B2-H16-T32768-dk128-dv256.md).
 # Any change to those sources makes the figure stale: it is then reported as null.
-MEASURED_TRAFFIC = {"workload": "B2-H16-T32768-dk128-dv256", "sources": "05733a8ea1fbb6ab",
-                    "bytes_per_call": 1615270144 + 507713536 + 35846656 + 256}
+MEASURED_TRAFFIC = {"workload": "B2-H16-T32768-dk128-dv256", "sources": "1444bf3a00d01fcc",
+                    "bytes_per_call": 1615176192 + 509176832 + 35845376 + 2560}
 TRAFFIC_SOURCES = ["gla_api.cu", "gla_chunk.cu", "gla_chunk_kernel.cuh", "gla_internal.h", "gla_ptx.cuh"]
 
 
-def kernel_sources_hash() -> str:
+# ncu DRAM bytes (read + write) of one gla_chunk_bwd call on the long workload,
+# all six launches, for the backward sources hashed in "sources"
+MEASURED_BWD_TRAFFIC = {"workload": "B2-H16-T32768-dk128-dv256", "sources": "8aba25f959ad8012",
+                        "bytes_per_call": 25807910912}
+BWD_TRAFFIC_SOURCES = ["gla_api.cu", "gla_backward.cu", "gla_internal.h", "gla_ptx.cuh"]
+
+
+def kernel_sources_hash(files=None) -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in TRAFFIC_SOURCES:
+    for f in (TRAFFIC_SOURCES if files is None else files):
         with open(os.path.join(ROOT, "chunkwise_linear_rnn_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -79,6 +86,17 @@ def measured_traffic(cfg):
     except OSError:
         return None
     return MEASURED_TRAFFIC["bytes_per_call"]
+
+
+def measured_bwd_traffic(cfg):
+    if cfg.name != MEASURED_BWD_TRAFFIC["workload"]:
+        return None
+    try:
+        if kernel_sources_hash(BWD_TRAFFIC_SOURCES) != MEASURED_BWD_TRAFFIC["sources"]:
+            return None
+    except OSError:
+        return None
+    return MEASURED_BWD_TRAFFIC["bytes_per_call"]
 
 
 def chunk_bytes(cfg, n_states: int | None = None, gate_per_head: bool = False) -> int:
@@ -545,7 +563,9 @@ def bwd_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_ki
                    "dk": cfg.dk, "dv": cfg.dv, "chunk": plan["chunk"], "replicas": world,
                    "l2": "inputs (%.2f GB) larger than L2; no flush" % (byts / 1e9)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / pk["hbm_gbs"], "traffic": None,
+                     "frac": achieved / pk["hbm_gbs"],
+                     "traffic": None if packed is not None else measured_bwd_traffic(cfg),
+                     "traffic_unit": "bytes per call",
                      "peak_kind": pk_kind, "kernel": "gla_chunk_bwd (whole call, %d launches)"
                      % plan["launches"], "algorithmic_bytes_per_launch": byts,
                      "scratch_bytes": plan["scratch_bytes"]},
