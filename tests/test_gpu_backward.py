@@ -242,3 +242,18 @@ def test_full_size_other_workloads_sampled_heads(name):
     want = _oracle(sl(q), sl(k), sl(v), sl(a), sl(s0), sl(d_o), sl(g), cfg.scale)
     got = [x[b:b + 1, h:h + 1].float().cpu().numpy() for x in out]
     _compare(got, want, f"{name} workload head ({b},{h})")
+
+
+def test_gates_of_one():
+    """log alpha = 0 (alpha = 1): causal linear attention with no decay at all."""
+    q, k, v, a, s0, d_o, g = _inputs(1, 2, 200, 64, 128, seed=13)
+    a = torch.zeros_like(a)
+    case = (q, k, v, a, s0, d_o, g)
+    _compare(_gpu(*case, 0.125), _oracle(*case, 0.125), "alpha = 1")
+
+
+def test_many_heads_one_token():
+    """B * H = 70,000 (beyond one grid dimension's 65,535) with T = 1."""
+    q, k, v, a, s0, d_o, g = _inputs(7000, 10, 1, 64, 64, seed=14)
+    case = (q, k, v, a, s0, d_o, g)
+    _compare(_gpu(*case, 0.125), _oracle(*case, 0.125), "B*H = 70000, T = 1")
