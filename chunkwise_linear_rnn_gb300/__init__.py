@@ -25,7 +25,7 @@ from ._lib import GlaChunkOptions, GlaError, status_string  # noqa: F401
 
 __all__ = ["gla_chunk_fwd", "gla_chunk_fwd_varlen", "gla_chunk_fwd_varlen_plan",
            "gla_chunk_fwd_plan", "gla_chunk_bwd", "gla_chunk_bwd_plan", "gla_chunk_bwd_varlen",
-           "gla_chunk",
+           "gla_chunk", "gla_chunk_varlen",
            "gla_recurrent_step", "gla_last_device_status", "GlaError", "status_string",
            "library_path"]
 
@@ -382,6 +382,38 @@ def gla_chunk(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: torc
     if scale is None:
         scale = q.shape[-1] ** -0.5
     return _GlaChunk.apply(q, k, v, log_alpha, h0, float(scale))
+
+
+class _GlaChunkVarlen(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, log_alpha, h0, cu, scale):
+        o, hT = gla_chunk_fwd_varlen(q, k, v, log_alpha, cu, scale, h0)
+        ctx.save_for_backward(q, k, v, log_alpha, h0)
+        ctx.cu, ctx.scale = cu, scale
+        return o, hT
+
+    @staticmethod
+    def backward(ctx, d_o, dhT):
+        q, k, v, log_alpha, h0 = ctx.saved_tensors
+        if d_o is None:
+            d_o = torch.zeros(*q.shape[:-1], v.shape[-1], dtype=torch.bfloat16, device=q.device)
+        d_o = d_o.to(torch.bfloat16).contiguous()
+        dhT = None if dhT is None else dhT.float().contiguous()
+        dq, dk, dv, da, dh0 = gla_chunk_bwd_varlen(
+            q, k, v, log_alpha, d_o, ctx.cu, ctx.scale, h0, dhT,
+            need_dh0=h0 is not None and ctx.needs_input_grad[4])
+        return dq, dk, dv, da, dh0, None, None
+
+
+def gla_chunk_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: torch.Tensor,
+                     cu_seqlens, scale: float | None = None, h0: torch.Tensor | None = None):
+    """Differentiable packed-batch GLA: ``(o, hT)`` of ``gla_chunk_fwd_varlen`` with gradients
+    through ``gla_chunk_bwd_varlen``.  ``q`` etc. are ``[H, T_total, .]``; ``h0`` is
+    ``[N, H, dk, dv]`` or None."""
+    if scale is None:
+        scale = q.shape[-1] ** -0.5
+    cu = [int(x) for x in (cu_seqlens.tolist() if torch.is_tensor(cu_seqlens) else cu_seqlens)]
+    return _GlaChunkVarlen.apply(q, k, v, log_alpha, h0, cu, float(scale))
 
 
 def gla_recurrent_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: torch.Tensor,

@@ -257,3 +257,16 @@ def test_many_heads_one_token():
     q, k, v, a, s0, d_o, g = _inputs(7000, 10, 1, 64, 64, seed=14)
     case = (q, k, v, a, s0, d_o, g)
     _compare(_gpu(*case, 0.125), _oracle(*case, 0.125), "B*H = 70000, T = 1")
+
+
+def test_differentiable_packed_wrapper_matches_the_c_call():
+    lens = [70, 0, 130, 5]
+    q, k, v, a, d_o, h0, dhT, cu = _packed_case(lens, 2, 64, 128, seed=15)
+    q, k, v, a, d_o, h0, dhT = (t.to(DEV) for t in (q, k, v, a, d_o, h0, dhT))
+    leaves = [t.clone().requires_grad_(True) for t in (q, k, v, a, h0)]
+    o, hT = gla.gla_chunk_varlen(*leaves[:4], cu, 0.125, leaves[4])
+    ((o.float() * d_o.float()).sum() + (hT * dhT).sum()).backward()
+    want = gla.gla_chunk_bwd_varlen(q, k, v, a, d_o, cu, 0.125, h0, dhT)
+    torch.cuda.synchronize()
+    for name, leaf, ref in zip(NAMES, leaves, want):
+        assert torch.equal(leaf.grad, ref), name
