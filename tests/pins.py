@@ -20,6 +20,11 @@ pages (or a textbook) state the same result:
   Recall Degradation Problem": S_i = gamma S_{i-1} + k_i^T v_i, whose parallel
   form is O = ((Q K^T) * D) V with D_{t,j} = gamma^(t-j) for t >= j.
 
+* ``chunk_form_backward``: the same chunk equations differentiated, in the
+  form the backward kernels evaluate (in-chunk products, state terms against
+  the chunk-start states and state gradients, the log-gate carry); pinned
+  against the oracle's reverse-mode backward.
+
 All take float arrays for one sequence: q, k, a=log_alpha [T, dk], v [T, dv],
 h0 [dk, dv] or None, and return o [T, dv] (times ``scale``) and, where the
 formulation yields one, the final state.
@@ -76,6 +81,50 @@ def chunk_form(q, k, v, a, scale, h0=None, C=64):
         GC = G[-1]
         S = np.exp(GC)[:, None] * S + (K * np.exp(GC[None, :] - G)).T @ V
     return scale * o, S
+
+
+def chunk_form_backward(q, k, v, a, scale, do, h0=None, dhT=None, C=64):
+    """Gradients of sum <do, o> + <dhT, hT> in chunk form (the equations the
+    backward kernels evaluate).  Per chunk u of C tokens, Gamma the in-chunk
+    inclusive prefix sums, S_u the state entering the chunk and R_u the
+    gradient of the state leaving it:
+        A  = tril(dO V^T),  lam_ij = exp(Gamma_i - Gamma_j) (i >= j)
+        dQ = scale [ e^Gamma (dO S_u^T) + sum_j A_ij K_j lam_ij ]
+        dK = e^(Gamma_C - Gamma) (V R_u^T) + scale sum_i A_ij Q_i lam_ij
+        dV = (K e^(Gamma_C - Gamma)) R_u + scale M^T dO,  M_ij = sum_d Q K lam
+        dlog_alpha_t = rowsum(R_u * S_(u+1)) + sum_(tau >= t in chunk) (q dq - k dk)
+        R_(u-1) = e^Gamma_C R_u + scale (Q e^Gamma)^T dO,  R_last = dhT,  dh0 = R_(-1)
+    Returns (dq, dk, dv, dlog_alpha, dh0)."""
+    q, k, v, a, do = _d(q), _d(k), _d(v), _d(a), _d(do)
+    T, dk = q.shape
+    dv = v.shape[1]
+    starts = list(range(0, T, C))
+    # forward: the state entering every chunk, and the one leaving the last
+    S = [np.zeros((dk, dv)) if h0 is None else _d(h0).copy()]
+    for u0 in starts:
+        sl = slice(u0, min(u0 + C, T))
+        G = np.cumsum(a[sl], axis=0)
+        S.append(np.exp(G[-1])[:, None] * S[-1] + (k[sl] * np.exp(G[-1][None, :] - G)).T @ v[sl])
+    dq, dkk, dvv, da = (np.zeros_like(x) for x in (q, k, v, a))
+    R = np.zeros((dk, dv)) if dhT is None else _d(dhT).copy()
+    for u in reversed(range(len(starts))):
+        sl = slice(starts[u], min(starts[u] + C, T))
+        Q, K, V, DO = q[sl], k[sl], v[sl], do[sl]
+        n = Q.shape[0]
+        G = np.cumsum(a[sl], axis=0)
+        causal = np.tril(np.ones((n, n), dtype=bool))
+        lam = np.exp(np.where(causal[:, :, None], G[:, None, :] - G[None, :, :], -np.inf))
+        A = np.where(causal, DO @ V.T, 0.0)
+        M = np.einsum("id,jd,ijd->ij", Q, K, lam)
+        dQ = scale * (np.exp(G) * (DO @ S[u].T) + np.einsum("ij,jd,ijd->id", A, K, lam))
+        dK = np.exp(G[-1][None, :] - G) * (V @ R.T) + scale * np.einsum("ij,id,ijd->jd", A, Q, lam)
+        dV = (K * np.exp(G[-1][None, :] - G)) @ R + scale * M.T @ DO
+        carry = np.sum(R * S[u + 1], axis=1)
+        P = Q * dQ - K * dK
+        da[sl] = carry[None, :] + np.flip(np.cumsum(np.flip(P, axis=0), axis=0), axis=0)
+        dq[sl], dkk[sl], dvv[sl] = dQ, dK, dV
+        R = np.exp(G[-1])[:, None] * R + scale * (Q * np.exp(G)).T @ DO
+    return dq, dkk, dvv, da, R
 
 
 def causal_linear_attention(q, k, v, scale, h0=None):

@@ -14,6 +14,8 @@ something else:
   log-gates of every token from t on, so
   dL/dlog_alpha_t = sum_{tau >= t} (q_tau * dq_tau - k_tau * dk_tau)
                     + rowsum(dhT * hT);
+* the chunk-form gradient equations (``pins.chunk_form_backward``, the form
+  the backward kernels evaluate) at every chunk length from 1 to T;
 * independence from the checkpoint spacing and the thread count.
 
 ``test_backward_mutants_are_rejected`` plants plausible mistakes in a copy of
@@ -173,8 +175,23 @@ def pin_no_states(orc: Orc):
         assert _rel(g_none[i][0], want[i]) <= 1e-10, name
 
 
+def pin_chunk_form(orc: Orc):
+    """The chunk-form gradient equations (every chunk length, incl. 1 and T) equal the
+    reverse-mode gradients."""
+    import pins
+    q, k, v, a, do, h0, dhT = _case(10, 2, 29, 5, 4, spread=2.0, tau=3.0)
+    scale = 0.45
+    grads = orc.bwd(q, k, v, a, scale, do, h0, dhT)
+    for C in (1, 4, 7, 29, 64):
+        for n in range(2):
+            want = pins.chunk_form_backward(q[n], k[n], v[n], a[n], scale, do[n], h0[n], dhT[n], C)
+            for i, name in enumerate(NAMES):
+                err = _rel(grads[i][n], want[i])
+                assert err <= 1e-10, f"C={C} head {n} {name}: rel err {err:.2e}"
+
+
 BWD_PINS = [pin_directional_differences, pin_entrywise_differences, pin_dual_form_autograd,
-            pin_log_gate_identity, pin_no_states]
+            pin_log_gate_identity, pin_no_states, pin_chunk_form]
 
 
 @pytest.mark.parametrize("pin", BWD_PINS, ids=[p.__name__ for p in BWD_PINS])
