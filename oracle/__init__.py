@@ -22,6 +22,9 @@ mutants of this file that each of those pins must reject.  The backward is
 pinned by ``tests/test_oracle_bwd_pins.py``: central differences of the
 forward, autograd through the dual attention form, the log-gate identity and
 mutants of the backward.
+
+``gdn_oracle`` (its own C file, ``gdn_oracle.c``) is the fp64 token loop of
+the gated delta rule (row F4), pinned by ``tests/test_oracle_gdn_pins.py``.
 """
 
 from .gla_oracle import (  # noqa: F401

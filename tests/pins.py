@@ -25,6 +25,10 @@ pages (or a textbook) state the same result:
   the chunk-start states and state gradients, the log-gate carry); pinned
   against the oracle's reverse-mode backward.
 
+* ``gdn_chunk_form``: the gated delta rule's four-step chunk algorithm
+  (KK^T-based lower-triangular inverse, W and U, the chunk recurrence, the
+  output), derived from the token recurrence; pins the GDN oracle.
+
 All take float arrays for one sequence: q, k, a=log_alpha [T, dk], v [T, dv],
 h0 [dk, dv] or None, and return o [T, dv] (times ``scale``) and, where the
 formulation yields one, the final state.
@@ -155,3 +159,35 @@ def rel_err(x, ref):
     x, ref = _d(x), _d(ref)
     den = np.linalg.norm(ref)
     return float(np.linalg.norm(x - ref) / (den if den > 0 else 1.0))
+
+
+def gdn_chunk_form(q, k, v, g, beta, scale, h0=None, C=64):
+    """The gated delta rule by its chunk algorithm ("Qwen Team Releases FlashQLA
+    ...", the four steps of the GDN prefill): per chunk, with gamma_t the
+    in-chunk product of the gates and Delta the per-token write errors,
+      1. T = (I + L)^-1, L strictly lower, L_ti = beta_t (gamma_t/gamma_i) k_t.k_i;
+      2. U = T diag(beta) V,  W = T diag(beta) diag(gamma) K;
+      3. S_C = gamma_C S_0 + (diag(gamma_C/gamma) K)^T (U - W S_0);
+      4. O = scale [diag(gamma) Q S_0 + tril(Q K^T * gamma_t/gamma_i) (U - W S_0)].
+    Returns (o [T, dv], hT [dk, dv])."""
+    q, k, v, g, beta = _d(q), _d(k), _d(v), _d(g), _d(beta)
+    T, dk = q.shape
+    dv = v.shape[1]
+    S = np.zeros((dk, dv)) if h0 is None else _d(h0).copy()
+    o = np.zeros((T, dv))
+    for u0 in range(0, T, C):
+        sl = slice(u0, min(u0 + C, T))
+        Q, K, V, b = q[sl], k[sl], v[sl], beta[sl]
+        n = Q.shape[0]
+        G = np.cumsum(g[sl])                                   # log gamma_t
+        low = np.tril(np.ones((n, n), dtype=bool))
+        ratio = np.exp(np.where(low, G[:, None] - G[None, :], -np.inf))   # gamma_t / gamma_i, i <= t
+        L = np.where(np.tril(np.ones((n, n), dtype=bool), -1), b[:, None] * ratio * (K @ K.T), 0.0)
+        Tm = np.linalg.inv(np.eye(n) + L)
+        U = Tm @ (b[:, None] * V)
+        W = Tm @ (b[:, None] * np.exp(G)[:, None] * K)
+        D = U - W @ S
+        o[sl] = scale * (np.exp(G)[:, None] * (Q @ S) + ((Q @ K.T) * ratio) @ D)
+        S = np.exp(G[-1]) * S + (K * np.exp(G[-1] - G)[:, None]).T @ D
+    return o, S
+
