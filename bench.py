@@ -33,6 +33,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "GLA chunk-fwd tokens/s (B·H·T) and % roofline; decode steps/s and HBM GB/s"
 BWD_METRIC = "GLA chunk-bwd tokens/s (B·H·T): gradients of q, k, v, log_alpha and h0"
+GDN_METRIC = "Gated DeltaNet forward tokens/s (B·H·T)"
+# fp32 FMA peak of the SM array: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz (max SM clock)
+FP32_SIMT_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -68,6 +71,14 @@ MEASURED_BWD_TRAFFIC = {"workload": "B2-H16-T32768-dk128-dv256", "sources": "8ab
 BWD_TRAFFIC_SOURCES = ["gla_api.cu", "gla_backward.cu", "gla_internal.h", "gla_ptx.cuh"]
 
 
+# ncu DRAM bytes (read + write) of one gla_gdn_fwd launch, captured at B=1, H=8 of
+# the long shape (T=32768, dk=128, dv=256) and scaled by the heads a launch
+# covers (traffic per head is fixed: every head streams its own rows once)
+MEASURED_GDN_TRAFFIC = {"T": 32768, "dk": 128, "dv": 256, "heads": 8, "sources": "ef91c872e7aeb93f",
+                        "bytes_per_launch": 272358144 + 110092032}
+GDN_TRAFFIC_SOURCES = ["gla_gdn.cu"]
+
+
 def kernel_sources_hash(files=None) -> str:
     import hashlib
     h = hashlib.sha256()
@@ -97,6 +108,18 @@ def measured_bwd_traffic(cfg):
     except OSError:
         return None
     return MEASURED_BWD_TRAFFIC["bytes_per_call"]
+
+
+def measured_gdn_traffic(cfg):
+    m = MEASURED_GDN_TRAFFIC
+    if (cfg.T, cfg.dk, cfg.dv) != (m["T"], m["dk"], m["dv"]):
+        return None
+    try:
+        if kernel_sources_hash(GDN_TRAFFIC_SOURCES) != m["sources"]:
+            return None
+    except OSError:
+        return None
+    return m["bytes_per_launch"] * cfg.B * cfg.H // m["heads"]
 
 
 def chunk_bytes(cfg, n_states: int | None = None, gate_per_head: bool = False) -> int:
@@ -271,6 +294,8 @@ def run_ours(args, rank, world, local_rank):
     line = None
     if args.only == "bwd":
         return bwd_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_kind)
+    if args.only == "gdn":
+        return gdn_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_kind)
     if args.only != "decode":
         line = chunk_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_kind)
     else:
@@ -579,6 +604,137 @@ def bwd_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_ki
     return line
 
 
+def gdn_flops(cfg) -> int:
+    """Per token, head and value column: k.S, the rank-1 update and q.S, dk FMAs each."""
+    return 6 * cfg.B * cfg.H * cfg.T * cfg.dk * cfg.dv
+
+
+def gdn_bytes(cfg) -> int:
+    """q, k, v, o in bf16; g, beta in fp32; h0 and hT in fp32."""
+    tok = cfg.B * cfg.H * cfg.T
+    return tok * (2 * cfg.dk * 2 + 2 * cfg.dv * 2 + 2 * 4) + 2 * cfg.B * cfg.H * cfg.dk * cfg.dv * 4
+
+
+def gdn_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_kind):
+    """The gated delta rule forward (gla_gdn_fwd, token-recurrent) on the workload's shape."""
+    import torch
+    from synth import make_gdn_inputs
+    stream = torch.cuda.current_stream(dev)
+    q, k, v, g, b, h0 = make_gdn_inputs(cfg.B, cfg.H, cfg.T, cfg.dk, cfg.dv, sigma_h0=0.1,
+                                        seed=rank, device=dev)
+
+    def step():
+        return gla.gla_gdn_fwd(q, k, v, g, b, cfg.scale, h0)
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    with ClockSampler(dev.index) as clk:
+        barrier()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for s0, e0 in ev:
+            s0.record(stream)
+            step()
+            e0.record(stream)
+        t_end.record(stream)
+        barrier()
+    ms_per_step = max_over_ranks(t_start.elapsed_time(t_end)) / args.steps
+    per_call_ms = statistics.mean(s0.elapsed_time(e0) for s0, e0 in ev)
+    tokens_all = cfg.tokens * world
+    flops, byts = gdn_flops(cfg), gdn_bytes(cfg)
+    achieved = flops / (per_call_ms / 1e3) / 1e12
+
+    e2e = None
+    if not args.no_e2e:
+        host_in = [t.cpu().pin_memory() for t in (q, k, v, g, b, h0)]
+        dev_in = [torch.empty_like(t, device=dev) for t in host_in]
+        outs = step()
+        host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
+
+        def e2e_step():
+            for hsrc, dst in zip(host_in, dev_in):
+                dst.copy_(hsrc, non_blocking=True)
+            res = gla.gla_gdn_fwd(*dev_in[:5], cfg.scale, dev_in[5])
+            for src, hdst in zip(res, host_out):
+                hdst.copy_(src, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        x0 = torch.cuda.Event(enable_timing=True)
+        x1 = torch.cuda.Event(enable_timing=True)
+        n_e2e = max(2, min(args.steps, 5))
+        x0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        x1.record(stream)
+        barrier()
+        e2e_ms = max_over_ranks(x0.elapsed_time(x1)) / n_e2e
+        e2e = {"value": tokens_all / (e2e_ms / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in host_in)),
+               "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in host_out)),
+               "ms_per_step": e2e_ms, "api": "gla_gdn_fwd with pinned-host copies"}
+        del host_in, dev_in, host_out, outs
+    del q, k, v, g, b, h0
+    torch.cuda.empty_cache()
+    line = {
+        "metric": GDN_METRIC,
+        "value": tokens_all / (ms_per_step / 1e3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": cfg.name + "-gated-delta-rule", "B": cfg.B, "H": cfg.H,
+                   "T": cfg.T, "dk": cfg.dk, "dv": cfg.dv, "replicas": world,
+                   "l2": "inputs (%.2f GB) larger than L2; no flush" % (byts / 1e9)},
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_SIMT_TFLOPS,
+                     "unit": "TFLOP/s", "frac": achieved / FP32_SIMT_TFLOPS,
+                     "traffic": measured_gdn_traffic(cfg), "traffic_unit": "DRAM bytes per launch",
+                     "peak_kind": "derived: 152 SMs x 128 fp32 FMA lanes x 2 x 2070 MHz",
+                     "kernel": "gdn_recurrent_kernel (token-recurrent, one launch)",
+                     "algorithmic_flops_per_launch": flops,
+                     "hbm_gbs": byts / (per_call_ms / 1e3) / 1e9,
+                     "hbm_frac": byts / (per_call_ms / 1e3) / 1e9 / pk["hbm_gbs"],
+                     "hbm_peak_kind": pk_kind},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    return line
+
+
+def gdn_oracle_sample(cfg, target_s: float, threads: int) -> dict:
+    """Time the fp64 gated-delta-rule oracle on whole heads and a prefix of tokens."""
+    from oracle import gdn_oracle
+    from synth import make_gdn_inputs
+    gdn_oracle.build()
+
+    def inputs(heads, T):
+        q, k, v, g, b, h0 = make_gdn_inputs(1, heads, T, cfg.dk, cfg.dv, sigma_h0=0.1, seed=0)
+        return [q.float().numpy(), k.float().numpy(), v.float().numpy(), g.numpy(), b.numpy(),
+                h0.double().numpy()]
+
+    def run(ins):
+        t0 = time.perf_counter()
+        gdn_oracle.forward(*ins[:5], cfg.scale, ins[5], nthreads=threads)
+        return time.perf_counter() - t0
+
+    heads = max(1, min(cfg.B * cfg.H, threads))
+    probe = inputs(heads, min(cfg.T, 256))
+    run(probe)
+    per_token = run(probe) / (heads * probe[0].shape[-2])
+    T = int(min(cfg.T, max(256, target_s / per_token / heads)))
+    dt = run(inputs(heads, T))
+    return {"value": heads * T / dt, "unit": "tokens/s", "cores": min(threads, heads),
+            "kind": "oracle", "seconds": dt,
+            "sample": f"{heads} heads x {T} tokens of {cfg.name} (dk={cfg.dk}, dv={cfg.dv}), "
+                      f"fp64 gated-delta-rule recurrence, {dt:.1f} s"}
+
+
 def decode_leg(args, world, rank, dev, gla, barrier, max_over_ranks, pk):
     """Decode steps at B=256, H=32, dk=dv=128 (secondary numbers on the same JSON line)."""
     import torch
@@ -696,6 +852,24 @@ def run_reference(args):
     cfg = chunk_config(args)
     threads = host_threads()
     per_step_s = max(0.5, min(args.ref_seconds, 150.0 / max(1, args.steps + args.warmup)))
+    if args.only == "gdn":
+        per = [gdn_oracle_sample(cfg, per_step_s, threads) for _ in range(args.warmup + args.steps)]
+        per = per[args.warmup:]
+        value = statistics.median(p["value"] for p in per)
+        base = dict(per[-1], value=value)
+        return {
+            "impl": "reference", "metric": GDN_METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * statistics.median(p["seconds"] for p in per),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": cfg.name + "-gated-delta-rule", "B": cfg.B, "H": cfg.H,
+                       "T": cfg.T, "dk": cfg.dk, "dv": cfg.dv},
+            "cpu_baseline": base,
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0,
+        }
     sample = OracleSample(cfg, per_step_s, threads, backward=args.only == "bwd")
     for _ in range(args.warmup):
         sample.run()
@@ -727,9 +901,10 @@ def main():
     ap.add_argument("--workload", default="long", choices=["small", "medium", "long", "very_long"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--decode-steps", type=int, default=256)
-    ap.add_argument("--only", default="both", choices=["both", "chunk", "decode", "bwd"],
-                    help="run only the chunked forward, only the decode step, or only the "
-                         "chunkwise backward (its own JSON line)")
+    ap.add_argument("--only", default="both", choices=["both", "chunk", "decode", "bwd", "gdn"],
+                    help="run only the chunked forward, only the decode step, only the "
+                         "chunkwise backward, or only the gated delta rule forward (the last "
+                         "two on their own JSON line)")
     ap.add_argument("--no-decode", action="store_true", help="same as --only chunk")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's B")
     ap.add_argument("--heads", type=int, default=0, help="override the workload's H")
@@ -760,7 +935,10 @@ def main():
 
     line = run_ours(args, rank, world, local_rank)
     if rank == 0:
-        if not args.no_cpu_baseline:
+        if not args.no_cpu_baseline and args.only == "gdn":
+            line["cpu_baseline"] = gdn_oracle_sample(chunk_config(args), args.ref_seconds,
+                                                     host_threads())
+        elif not args.no_cpu_baseline:
             line["cpu_baseline"] = oracle_sample(chunk_config(args), args.ref_seconds,
                                                  host_threads(), backward=args.only == "bwd")
         print(json.dumps(line), flush=True)

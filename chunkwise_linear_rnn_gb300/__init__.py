@@ -25,7 +25,7 @@ from ._lib import GlaChunkOptions, GlaError, status_string  # noqa: F401
 
 __all__ = ["gla_chunk_fwd", "gla_chunk_fwd_varlen", "gla_chunk_fwd_varlen_plan",
            "gla_chunk_fwd_plan", "gla_chunk_bwd", "gla_chunk_bwd_plan", "gla_chunk_bwd_varlen",
-           "gla_chunk", "gla_chunk_varlen",
+           "gla_chunk", "gla_chunk_varlen", "gla_gdn_fwd",
            "gla_recurrent_step", "gla_last_device_status", "GlaError", "status_string",
            "library_path"]
 
@@ -414,6 +414,42 @@ def gla_chunk_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alph
         scale = q.shape[-1] ** -0.5
     cu = [int(x) for x in (cu_seqlens.tolist() if torch.is_tensor(cu_seqlens) else cu_seqlens)]
     return _GlaChunkVarlen.apply(q, k, v, log_alpha, h0, cu, float(scale))
+
+
+def gla_gdn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                beta: torch.Tensor, scale: float | None = None, h0: torch.Tensor | None = None,
+                output_final_state: bool = True):
+    """Gated delta rule (Gated DeltaNet) forward: ``(o, hT)``.
+
+    q, k ``[B,H,T,dk]`` bf16 (k as given: normalise it first); v ``[B,H,T,dv]``
+    bf16; g (log alpha) and beta ``[B,H,T]`` fp32; h0 ``[B,H,dk,dv]`` fp32 or None.
+    """
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, T, dk]")
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("q must be on a CUDA device")
+    _need(q, "q", torch.bfloat16, (B, H, T, dk), dev)
+    _need(k, "k", torch.bfloat16, (B, H, T, dk), dev)
+    _need(v, "v", torch.bfloat16, (B, H, T, dv), dev)
+    _need(g, "g", torch.float32, (B, H, T), dev)
+    _need(beta, "beta", torch.float32, (B, H, T), dev)
+    if h0 is not None:
+        _need(h0, "h0", torch.float32, (B, H, dk, dv), dev)
+    if scale is None:
+        scale = dk ** -0.5
+    o = torch.empty(B, H, T, dv, dtype=torch.bfloat16, device=dev)
+    hT = torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev) if output_final_state else None
+    with torch.cuda.device(dev):
+        st = _lib.lib().gla_gdn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(),
+                                    beta.data_ptr(), float(scale),
+                                    None if h0 is None else h0.data_ptr(), o.data_ptr(),
+                                    None if hT is None else hT.data_ptr(), B, H, T, dk, dv,
+                                    _stream(dev))
+    _lib.check(st, "gla_gdn_fwd")
+    return o, hT
 
 
 def gla_recurrent_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: torch.Tensor,

@@ -340,6 +340,27 @@ int gla_chunk_bwd_varlen_ex(const void *q, const void *k, const void *v, const f
                             float *grad_h0, const int *cu_seqlens, int N, int H, int T_total,
                             int dk, int dv, const gla_chunk_options *opts, cudaStream_t stream);
 
+/*
+ * gla_gdn_fwd — the gated delta rule (Gated DeltaNet), forward, per (batch,
+ * head), with S in R^{dk x dv} and row vectors:
+ *     S_t = alpha_t (I - beta_t k_t^T k_t) S_{t-1} + beta_t k_t^T v_t,
+ *     o_t = scale * q_t S_t,
+ * from the FlashQLA page ("Qwen Team Releases FlashQLA for High-Performance
+ * Linear Attention", "Core Technical Principles": scalar alpha, beta in
+ * (0, 1), L2-normalised keys), in the standard gated-delta-rule reading.
+ *   q, k    bf16 [B, H, T, dk] (k as given: the caller normalises it)
+ *   v, o    bf16 [B, H, T, dv]
+ *   g       fp32 [B, H, T]     log alpha (finite, <= 0)
+ *   beta    fp32 [B, H, T]     in [0, 1]
+ *   h0, hT  fp32 [B, H, dk, dv] (nullable; zero initial state / not written)
+ * Token-recurrent: the exact recurrence, one step per token, the state in
+ * registers.  Shapes: dk in {64, 128}, dv in {64, 128, 256}, B * H <= 65535.
+ * Pointers need their element alignment.  Errors as for gla_chunk_fwd.
+ */
+int gla_gdn_fwd(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                float scale, const float *h0, void *o, float *hT, int B, int H, int T, int dk,
+                int dv, cudaStream_t stream);
+
 /* Static text for a status code (never NULL). */
 const char *gla_status_string(int status);
 

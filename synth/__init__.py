@@ -15,4 +15,5 @@ from .gla_inputs import (  # noqa: F401
     make_chunk_inputs,
     make_config_inputs,
     make_decode_inputs,
+    make_gdn_inputs,
 )

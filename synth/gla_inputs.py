@@ -143,3 +143,28 @@ def make_decode_inputs(B: int, H: int, dk: int, dv: int, steps: int, *, sigma_z:
     log_alpha = F.logsigmoid(z).div_(tau)
     del z
     return h0, q, k, v, log_alpha
+
+
+def make_gdn_inputs(B: int, H: int, T: int, dk: int, dv: int, *, sigma_z: float = 1.0,
+                    tau: float = 16.0, sigma_h0: float | None = None, seed: int = 0,
+                    device="cpu"):
+    """Draw (q, k, v, g, beta, h0) for the gated delta rule: one generator seeded
+    with ``seed``; draw order z, z_beta, q, k, v, h0; g = logsigmoid(z) / tau
+    [B,H,T] fp32; beta = sigmoid(z_beta) [B,H,T] fp32; q, v ~ N(0, 1) and k ~ N(0, 1)
+    normalised to unit L2 norm per token, all rounded to bf16; h0 ~ N(0, sigma_h0^2)."""
+    gen = _gen(seed, device)
+    z = torch.randn(B, H, T, generator=gen, device=device, dtype=torch.float32)
+    if sigma_z != 1.0:
+        z.mul_(sigma_z)
+    zb = torch.randn(B, H, T, generator=gen, device=device, dtype=torch.float32)
+    q = torch.randn(B, H, T, dk, generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+    k = torch.randn(B, H, T, dk, generator=gen, device=device, dtype=torch.float32)
+    k = (k / k.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+    v = torch.randn(B, H, T, dv, generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+    g = F.logsigmoid(z).div_(tau)
+    beta = torch.sigmoid(zb)
+    h0 = None
+    if sigma_h0 is not None:
+        h0 = torch.randn(B, H, dk, dv, generator=gen, device=device, dtype=torch.float32).mul_(sigma_h0)
+    return q, k, v, g, beta, h0
+

@@ -2,7 +2,8 @@
 
 ``bench.py --impl reference`` times the fp64 oracle on the host, so it runs
 without a GPU; its line must carry the keys the contract names, for the
-forward and for the backward (``--only bwd``)."""
+forward, for the backward (``--only bwd``) and for the gated delta rule
+(``--only gdn``)."""
 
 from __future__ import annotations
 
@@ -31,7 +32,7 @@ def _run(*extra):
     return json.loads(lines[0])
 
 
-@pytest.mark.parametrize("only", ["both", "bwd"])
+@pytest.mark.parametrize("only", ["both", "bwd", "gdn"])
 def test_reference_line_keeps_the_contract(only):
     line = _run("--only", only)
     assert KEYS <= set(line), sorted(KEYS - set(line))
@@ -41,3 +42,5 @@ def test_reference_line_keeps_the_contract(only):
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
     assert line["config"]["workload"].startswith("B1-H2-T256-dk64-dv64")
     assert ("chunk-bwd" in line["metric"]) == (only == "bwd")
+    assert ("Gated DeltaNet" in line["metric"]) == (only == "gdn")
+    assert line["ms_per_step"] > 0
