@@ -12,7 +12,9 @@
 // and do the same for q S[:, c].  The CTA's four warps cover adjacent columns
 // of one head and share its per-token q, k, v tile and gates, staged in shared
 // memory 32 tokens at a time; each 32-row part of a staged q or k row is padded
-// by four words so that the lanes of one column read different banks.
+// by four words so that the lanes of one column read different banks.  The
+// next round's tokens are loaded into registers (16-byte loads) while the
+// current round computes, so the staging barrier never waits on HBM.
 //
 // This is the first CUDA path of the workload: exact recurrence, no chunking,
 // so it is bound by the per-token chain, not by HBM; the chunked form (the
@@ -38,6 +40,53 @@ struct GdnTile {
     static constexpr int kRow = kParts * (kRows + kPad);      // padded words per staged row
 };
 
+// One round of staged tokens in flight, held in registers: this thread's
+// 16-byte pieces of the q, k and v tiles and (threads < kTok) one token's gates.
+template <int DK>
+struct GdnRound {
+    static constexpr int kQ = kTok * DK / 8 / (kWarps * 32);                // q or k pieces
+    static constexpr int kV = kTok * GdnTile<DK>::kCols / 8 / (kWarps * 32);  // v pieces
+    uint4 q[kQ], k[kQ], v[kV];
+    float g, b;
+};
+
+__device__ __forceinline__ void bf16x8_to_f32(uint4 u, float *f) {
+    const unsigned w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {   // little-endian: the lower half holds the even element
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+// Loads tokens [t0, t0 + kTok) of one head (zeros past T).
+template <int DK>
+__device__ __forceinline__ void gdn_load_round(GdnRound<DK> &r, const __nv_bfloat16 *q,
+                                               const __nv_bfloat16 *k, const __nv_bfloat16 *v,
+                                               const float *g, const float *beta, size_t rk,
+                                               size_t rv, size_t rg, int c0, int t0, int T,
+                                               int dv) {
+    constexpr int NC = GdnTile<DK>::kCols;
+    const int n = min(kTok, T - t0);
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int j = 0; j < GdnRound<DK>::kQ; ++j) {
+        const int i = threadIdx.x + j * kWarps * 32, t = i / (DK / 8), d0 = (i % (DK / 8)) * 8;
+        const size_t off = rk + static_cast<size_t>(t0 + t) * DK + d0;
+        r.q[j] = t < n ? *reinterpret_cast<const uint4 *>(q + off) : zero;
+        r.k[j] = t < n ? *reinterpret_cast<const uint4 *>(k + off) : zero;
+    }
+#pragma unroll
+    for (int j = 0; j < GdnRound<DK>::kV; ++j) {
+        const int i = threadIdx.x + j * kWarps * 32, t = i / (NC / 8), j0 = (i % (NC / 8)) * 8;
+        r.v[j] = t < n ? *reinterpret_cast<const uint4 *>(v + rv + static_cast<size_t>(t0 + t) * dv + c0 + j0)
+                       : zero;
+    }
+    const bool gate = threadIdx.x < n;
+    r.g = gate ? g[rg + t0 + threadIdx.x] : 0.f;
+    r.b = gate ? beta[rg + t0 + threadIdx.x] : 0.f;
+}
+
 template <int DK>
 __global__ void __launch_bounds__(kWarps * 32) gdn_recurrent_kernel(
     const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
@@ -48,7 +97,8 @@ __global__ void __launch_bounds__(kWarps * 32) gdn_recurrent_kernel(
     constexpr int P = Tile::kParts, NC = Tile::kCols, ROW = Tile::kRow;
     __shared__ __align__(16) float sq[kTok][ROW];
     __shared__ __align__(16) float sk[kTok][ROW];
-    __shared__ float sv[kTok][NC], sa[kTok], sb[kTok];
+    __shared__ __align__(16) float sv[kTok][NC];
+    __shared__ float sa[kTok], sb[kTok];
     const int bh = blockIdx.y;
     const int cl = threadIdx.x / P, part = threadIdx.x % P;   // local column, row part
     const int c0 = blockIdx.x * NC, c = c0 + cl;              // c < dv: dv is a multiple of NC
@@ -60,25 +110,39 @@ __global__ void __launch_bounds__(kWarps * 32) gdn_recurrent_kernel(
     for (int d = 0; d < kRows; ++d)
         S[d] = h0 ? h0[(static_cast<size_t>(bh) * DK + r0 + d) * dv + c] : 0.f;
 
+    const size_t rg = static_cast<size_t>(bh) * T;
+    GdnRound<DK> next;
+    gdn_load_round<DK>(next, q, k, v, g, beta, rk, rv, rg, c0, 0, T, dv);
     for (int t0 = 0; t0 < T; t0 += kTok) {
         const int n = min(kTok, T - t0);
         __syncthreads();   // the previous round is done with the staged tokens
-        for (int e = threadIdx.x; e < kTok * DK; e += blockDim.x) {
-            const int t = e / DK, d = e % DK, w = (d / kRows) * (kRows + kPad) + d % kRows;
-            const size_t off = rk + static_cast<size_t>(t0 + t) * DK + d;
-            sq[t][w] = t < n ? __bfloat162float(q[off]) : 0.f;
-            sk[t][w] = t < n ? __bfloat162float(k[off]) : 0.f;
+#pragma unroll
+        for (int j = 0; j < GdnRound<DK>::kQ; ++j) {
+            const int i = threadIdx.x + j * kWarps * 32, t = i / (DK / 8), d0 = (i % (DK / 8)) * 8;
+            const int w = (d0 / kRows) * (kRows + kPad) + d0 % kRows;   // 8 words in one part
+            float f[8];
+            bf16x8_to_f32(next.q[j], f);
+            *reinterpret_cast<float4 *>(&sq[t][w]) = make_float4(f[0], f[1], f[2], f[3]);
+            *reinterpret_cast<float4 *>(&sq[t][w + 4]) = make_float4(f[4], f[5], f[6], f[7]);
+            bf16x8_to_f32(next.k[j], f);
+            *reinterpret_cast<float4 *>(&sk[t][w]) = make_float4(f[0], f[1], f[2], f[3]);
+            *reinterpret_cast<float4 *>(&sk[t][w + 4]) = make_float4(f[4], f[5], f[6], f[7]);
         }
-        for (int e = threadIdx.x; e < kTok * NC; e += blockDim.x) {
-            const int t = e / NC, j = e % NC;
-            sv[t][j] = t < n ? __bfloat162float(v[rv + static_cast<size_t>(t0 + t) * dv + c0 + j]) : 0.f;
+#pragma unroll
+        for (int j = 0; j < GdnRound<DK>::kV; ++j) {
+            const int i = threadIdx.x + j * kWarps * 32, t = i / (NC / 8), j0 = (i % (NC / 8)) * 8;
+            float f[8];
+            bf16x8_to_f32(next.v[j], f);
+            *reinterpret_cast<float4 *>(&sv[t][j0]) = make_float4(f[0], f[1], f[2], f[3]);
+            *reinterpret_cast<float4 *>(&sv[t][j0 + 4]) = make_float4(f[4], f[5], f[6], f[7]);
         }
         if (threadIdx.x < kTok) {
-            const int t = threadIdx.x;
-            sa[t] = t < n ? expf(g[static_cast<size_t>(bh) * T + t0 + t]) : 1.f;
-            sb[t] = t < n ? beta[static_cast<size_t>(bh) * T + t0 + t] : 0.f;
+            sa[threadIdx.x] = expf(next.g);   // e^0 = 1 past T
+            sb[threadIdx.x] = next.b;
         }
         __syncthreads();
+        if (t0 + kTok < T)   // the next round's loads stay in flight while this one computes
+            gdn_load_round<DK>(next, q, k, v, g, beta, rk, rv, rg, c0, t0 + kTok, T, dv);
         for (int t = 0; t < n; ++t) {
             const float *kt = &sk[t][w0], *qt = &sq[t][w0];
             float ks0 = 0.f, ks1 = 0.f, ks2 = 0.f, ks3 = 0.f;   // this part of k S[:, c]
@@ -130,7 +194,7 @@ extern "C" int gla_gdn_fwd(const void *q, const void *k, const void *v, const fl
     if (B <= 0 || H <= 0 || T <= 0 || H > 65535 || static_cast<long long>(B) * H > 65535)
         return GLA_ERR_ARG;
     if (!(dk == 64 || dk == 128) || !(dv == 64 || dv == 128 || dv == 256)) return GLA_ERR_SHAPE;
-    if (misaligned(q, 2) || misaligned(k, 2) || misaligned(v, 2) || misaligned(o, 2) ||
+    if (misaligned(q, 16) || misaligned(k, 16) || misaligned(v, 16) || misaligned(o, 2) ||
         misaligned(g, 4) || misaligned(beta, 4) || (h0 && misaligned(h0, 4)) ||
         (hT && misaligned(hT, 4)))
         return GLA_ERR_ARG;

@@ -355,7 +355,9 @@ int gla_chunk_bwd_varlen_ex(const void *q, const void *k, const void *v, const f
  *   h0, hT  fp32 [B, H, dk, dv] (nullable; zero initial state / not written)
  * Token-recurrent: the exact recurrence, one step per token, the state in
  * registers.  Shapes: dk in {64, 128}, dv in {64, 128, 256}, B * H <= 65535.
- * Pointers need their element alignment.  Errors as for gla_chunk_fwd.
+ * q, k and v must be 16-byte aligned (the next 32 tokens are fetched in
+ * 16-byte pieces while the current ones compute; GLA_ERR_ARG otherwise); the
+ * other pointers need their element alignment.  Errors as for gla_chunk_fwd.
  */
 int gla_gdn_fwd(const void *q, const void *k, const void *v, const float *g, const float *beta,
                 float scale, const float *h0, void *o, float *hT, int B, int H, int T, int dk,

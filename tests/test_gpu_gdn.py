@@ -99,6 +99,12 @@ def test_bad_arguments_are_rejected():
                         dev(g), dev(b))
     with pytest.raises(Exception):
         gla.gla_gdn_fwd(dev(q), dev(k), dev(v), dev(g).double(), dev(b))
+    # q one element off a 16-byte boundary: refused on the host, nothing launched
+    flat = torch.empty(q.numel() + 8, dtype=torch.bfloat16, device=DEV)
+    q_off = flat[1:1 + q.numel()].view(q.shape)
+    q_off.copy_(dev(q))
+    with pytest.raises(Exception):
+        gla.gla_gdn_fwd(q_off, dev(k), dev(v), dev(g), dev(b))
 
 
 def test_long_workload_sampled_heads():

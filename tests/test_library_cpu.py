@@ -235,3 +235,25 @@ def test_backward_without_gpu_reports_device_error(lib):
         pytest.skip("a GPU is present")
     assert _bwd(lib) == _lib.GLA_ERR_DEVICE
     assert _bwd(lib, opts=ctypes.byref(_lib.GlaChunkOptions(gate_per_head=1))) == _lib.GLA_ERR_DEVICE
+
+
+def _gdn(lib, **kw):
+    """gla_gdn_fwd with fake aligned pointers; keyword overrides."""
+    a = dict(q=P, k=P, v=P, g=P, beta=P, scale=0.125, h0=None, o=P, hT=None, B=1, H=1, T=16,
+             dk=64, dv=64)
+    a.update(kw)
+    return lib.gla_gdn_fwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["scale"], a["h0"], a["o"],
+                           a["hT"], a["B"], a["H"], a["T"], a["dk"], a["dv"], None)
+
+
+def test_gated_delta_rule_validates_before_the_device(lib):
+    for field in ("q", "k", "v", "g", "beta", "o"):
+        assert _gdn(lib, **{field: None}) == _lib.GLA_ERR_ARG
+    for field in ("q", "k", "v"):   # fetched in 16-byte pieces
+        assert _gdn(lib, **{field: P + 8}) == _lib.GLA_ERR_ARG
+    assert _gdn(lib, o=P + 2) == _lib.GLA_ERR_DEVICE   # o needs element alignment only
+    assert _gdn(lib, T=0) == _lib.GLA_ERR_ARG
+    assert _gdn(lib, B=300, H=300) == _lib.GLA_ERR_ARG
+    assert _gdn(lib, dk=96) == _lib.GLA_ERR_SHAPE
+    assert _gdn(lib, dv=48) == _lib.GLA_ERR_SHAPE
+    assert _gdn(lib) == _lib.GLA_ERR_DEVICE   # valid arguments, no GPU here
