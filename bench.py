@@ -313,6 +313,20 @@ def run_ours(args, rank, world, local_rank):
                             "ms_per_step": b["ms_per_step"], "steps": b["steps"],
                             "workload": b["config"]["workload"], "roofline": b["roofline"],
                             "gpu_launches": b["gpu_launches"], "clocks": b["clocks"]}
+        # the gated delta rule forward on the same shape, likewise secondary; its failure
+        # is reported in place and never costs the primary line
+        gargs = _ap.Namespace(**vars(args))
+        gargs.steps, gargs.warmup, gargs.no_e2e = min(args.steps, 10), max(args.warmup, 3), True
+        try:
+            gd = gdn_leg(gargs, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_kind)
+            line["gated_delta_rule"] = {
+                "metric": gd["metric"], "value": gd["value"], "unit": gd["unit"],
+                "ms_per_step": gd["ms_per_step"], "steps": gd["steps"],
+                "workload": gd["config"]["workload"], "roofline": gd["roofline"],
+                "gpu_launches": gd["gpu_launches"], "clocks": gd["clocks"]}
+        except Exception as exc:  # noqa: BLE001
+            log(f"gated delta rule leg failed: {exc!r}")
+            line["gated_delta_rule"] = {"error": repr(exc)[:300]}
     return line
 
 
