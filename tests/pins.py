@@ -191,3 +191,61 @@ def gdn_chunk_form(q, k, v, g, beta, scale, h0=None, C=64):
         S = np.exp(G[-1]) * S + (K * np.exp(G[-1] - G)[:, None]).T @ D
     return o, S
 
+
+
+def gdn_chunk_transition(k, g, beta, C=64):
+    """Per chunk of the gated delta rule, the matrix M with S_C = M S_0 + K~^T U:
+    M = gamma_C I - K~^T W, K~ = diag(gamma_C/gamma) K (step 3 of the four-step
+    chunk algorithm, regrouped around S_0).  Returns the list over chunks."""
+    k, g, beta = _d(k), _d(g), _d(beta)
+    T, dk = k.shape
+    Ms = []
+    for u0 in range(0, T, C):
+        sl = slice(u0, min(u0 + C, T))
+        K, b = k[sl], beta[sl]
+        n = K.shape[0]
+        G = np.cumsum(g[sl])
+        low = np.tril(np.ones((n, n), dtype=bool))
+        ratio = np.exp(np.where(low, G[:, None] - G[None, :], -np.inf))
+        L = np.where(np.tril(np.ones((n, n), dtype=bool), -1), b[:, None] * ratio * (K @ K.T), 0.0)
+        Tm = np.linalg.inv(np.eye(n) + L)
+        W = Tm @ (b[:, None] * np.exp(G)[:, None] * K)
+        Kt = K * np.exp(G[-1] - G)[:, None]
+        Ms.append(np.exp(G[-1]) * np.eye(dk) - Kt.T @ W)
+    return Ms
+
+
+def gdn_segment_form(q, k, v, g, beta, scale, h0=None, C=64, seg_chunks=2):
+    """The gated delta rule with the sequence split into segments of seg_chunks
+    chunks ("Qwen Team Releases FlashQLA ...", "Core Technical Principles": the
+    error of a state started from a wrong initial value evolves by a dk x dk
+    matrix per chunk, and those matrices associate).  Pass 1: every segment
+    runs from a zero state to its end state S*_s, and the product M_s of its
+    chunks' transition matrices is formed.  Pass 2, serial over segments:
+    start_{s+1} = M_s start_s + S*_s from start_0 = h0.  Pass 3: every segment
+    runs again from its true start (the state is computed twice, as the page
+    says).  Returns (o [T, dv], hT [dk, dv])."""
+    q, k, v, g, beta = _d(q), _d(k), _d(v), _d(g), _d(beta)
+    T, dk = q.shape
+    dv = v.shape[1]
+    span = C * seg_chunks
+    bounds = [(s0, min(s0 + span, T)) for s0 in range(0, T, span)]
+    Ms = gdn_chunk_transition(k, g, beta, C)
+    ends, prods = [], []
+    for si, (a, b_) in enumerate(bounds):
+        _, s_star = gdn_chunk_form(q[a:b_], k[a:b_], v[a:b_], g[a:b_], beta[a:b_], scale, None, C)
+        ends.append(s_star)
+        P = np.eye(dk)
+        for c in range(a // C, (b_ + C - 1) // C):
+            P = Ms[c] @ P
+        prods.append(P)
+    start = np.zeros((dk, dv)) if h0 is None else _d(h0).copy()
+    starts = []
+    for P, s_star in zip(prods, ends):
+        starts.append(start)
+        start = P @ start + s_star
+    o = np.zeros((T, dv))
+    hT = None
+    for (a, b_), s0 in zip(bounds, starts):
+        o[a:b_], hT = gdn_chunk_form(q[a:b_], k[a:b_], v[a:b_], g[a:b_], beta[a:b_], scale, s0, C)
+    return o, hT

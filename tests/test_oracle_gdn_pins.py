@@ -8,8 +8,10 @@ of the same page (``pins.gdn_chunk_form``) at every chunk length, the
 decay-only closed form (beta = 0), the delta rule's defining overwrite
 (alpha = beta = 1, unit key: reading with the written key returns the
 written value), the vanishing-gate limit (only the current write survives),
-linearity in (v, h0), and the contraction bound that unit keys and gates in
-(0, 1] give.  ``test_gdn_mutants_are_rejected`` plants
+linearity in (v, h0), the contraction bound that unit keys and gates in
+(0, 1] give, the page's sequence-parallel correction (segments from zero
+state, corrected by products of per-chunk dk x dk transition matrices) and
+its sliding-window bound.  ``test_gdn_mutants_are_rejected`` plants
 mistakes in a copy of the oracle.
 """
 
@@ -119,8 +121,43 @@ def pin_vanishing_gate(orc: Orc):
     assert np.max(np.abs(hT - want_h)) <= 1e-9
 
 
+def pin_segment_correction(orc: Orc):
+    """Segments started from zero and corrected by the products of their chunks'
+    dk x dk transition matrices (the page's sequence-parallel scheme) give the
+    loop's outputs and final state, for segment and chunk lengths on and off
+    the sequence length."""
+    q, k, v, g, b, s0 = _case(11, 2, 45, 6, 5)
+    o, hT = orc.fwd(q, k, v, g, b, 0.5, s0)
+    for C, seg in ((1, 7), (4, 1), (4, 3), (8, 2), (16, 1), (64, 1)):
+        for n in range(2):
+            o_ref, s_ref = pins.gdn_segment_form(q[n], k[n], v[n], g[n], b[n], 0.5, s0[n], C, seg)
+            assert _rel(o[n], o_ref) <= 1e-10, f"C={C} seg={seg} head {n} o"
+            assert _rel(hT[n], s_ref) <= 1e-10, f"C={C} seg={seg} head {n} hT"
+
+
+def pin_sliding_window(orc: Orc):
+    """Each step maps a state difference D to alpha_t (I - beta_t k_t^T k_t) D,
+    whose norm is at most alpha_t |D| for unit keys and beta in [0, 1]: a state
+    rebuilt from zero over the last w tokens differs from the true one by at
+    most (product of alpha over the window) x |true state before the window|
+    (the sliding-window property of the same page)."""
+    q, k, v, g, b, s0 = _case(12, 3, 90, 6, 5, g_spread=1.0, tau=3.0)
+    p = 80
+    for w in (1, 5, 20, 40):
+        _, s_true = orc.fwd(q[:, :p], k[:, :p], v[:, :p], g[:, :p], b[:, :p], 1.0, s0)
+        _, s_before = orc.fwd(q[:, :p - w], k[:, :p - w], v[:, :p - w], g[:, :p - w],
+                              b[:, :p - w], 1.0, s0)
+        _, s_win = orc.fwd(q[:, p - w:p], k[:, p - w:p], v[:, p - w:p], g[:, p - w:p],
+                           b[:, p - w:p], 1.0, None)
+        decay = np.exp(np.sum(g[:, p - w:p].astype(np.float64), axis=1))
+        err = np.linalg.norm(s_true - s_win, axis=(1, 2))
+        bound = decay * np.linalg.norm(s_before, axis=(1, 2))
+        assert np.all(err <= bound * (1 + 1e-9) + 1e-12), (w, err, bound)
+        assert np.all(err >= 0.01 * bound) or w > 20   # the bound is not vacuous at short windows
+
+
 GDN_PINS = [pin_chunk_form, pin_decay_only, pin_overwrite, pin_linearity, pin_contraction,
-            pin_vanishing_gate]
+            pin_vanishing_gate, pin_segment_correction, pin_sliding_window]
 
 
 @pytest.mark.parametrize("pin", GDN_PINS, ids=[p.__name__ for p in GDN_PINS])
