@@ -353,6 +353,8 @@ int gla_chunk_bwd_varlen_ex(const void *q, const void *k, const void *v, const f
  *   g       fp32 [B, H, T]     log alpha (finite, <= 0)
  *   beta    fp32 [B, H, T]     in [0, 1]
  *   h0, hT  fp32 [B, H, dk, dv] (nullable; zero initial state / not written)
+ * No output may overlap an input (hT must not alias h0).  The call is
+ * asynchronous on `stream`; the caller owns every buffer.
  * Token-recurrent: the exact recurrence, one step per token, the state in
  * registers.  Shapes: dk in {64, 128}, dv in {64, 128, 256}, B * H <= 65535.
  * q, k and v must be 16-byte aligned (the next 32 tokens are fetched in
