@@ -3,7 +3,8 @@
 The oracle is the token loop S_t = alpha_t (I - beta_t k_t^T k_t) S_{t-1} +
 beta_t k_t^T v_t, o_t = scale q_t S_t ("Qwen Team Releases FlashQLA ...",
 "Core Technical Principles", in the standard gated-delta-rule reading).
-Each check compares it with something else: the four-step chunk algorithm
+Each check compares it with something else: two cases worked by hand
+(tests/golden/gdn_hand_examples.json), the four-step chunk algorithm
 of the same page (``pins.gdn_chunk_form``) at every chunk length, the
 decay-only closed form (beta = 0), the delta rule's defining overwrite
 (alpha = beta = 1, unit key: reading with the written key returns the
@@ -18,6 +19,8 @@ mistakes in a copy of the oracle.
 from __future__ import annotations
 
 import ctypes
+import json
+import os
 import shutil
 
 import numpy as np
@@ -25,6 +28,9 @@ import pytest
 
 from oracle import gdn_oracle as gd
 import pins
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                      "gdn_hand_examples.json")
 
 
 def _case(seed, BH, T, dk, dv, *, g_spread=1.0, tau=4.0, h0=True):
@@ -51,6 +57,24 @@ class Orc:
 def _rel(x, ref):
     x, ref = np.asarray(x, np.float64), np.asarray(ref, np.float64)
     return float(np.linalg.norm(x - ref) / max(np.linalg.norm(ref), 1e-300))
+
+
+def pin_hand_examples(orc: Orc):
+    """Cases worked by hand (tests/golden/gdn_hand_examples.json, derivations included)."""
+    with open(GOLDEN) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        q = np.asarray(c["q"], np.float32)[None]
+        k = np.asarray(c["k"], np.float32)[None]
+        v = np.asarray(c["v"], np.float32)[None]
+        g = np.log(np.asarray(c["alpha"], np.float64)).astype(np.float32)[None]
+        b = np.asarray(c["beta"], np.float32)[None]
+        h0 = None if c["h0"] is None else np.asarray(c["h0"], np.float64)[None]
+        o, hT = orc.fwd(q, k, v, g, b, c["scale"], h0)
+        np.testing.assert_allclose(o[0], np.asarray(c["o"]), rtol=1e-6, atol=1e-6,
+                                   err_msg=c["name"] + " o")
+        np.testing.assert_allclose(hT[0], np.asarray(c["hT"]), rtol=1e-6, atol=1e-6,
+                                   err_msg=c["name"] + " hT")
 
 
 def pin_chunk_form(orc: Orc):
@@ -156,7 +180,7 @@ def pin_sliding_window(orc: Orc):
         assert np.all(err >= 0.01 * bound) or w > 20   # the bound is not vacuous at short windows
 
 
-GDN_PINS = [pin_chunk_form, pin_decay_only, pin_overwrite, pin_linearity, pin_contraction,
+GDN_PINS = [pin_hand_examples, pin_chunk_form, pin_decay_only, pin_overwrite, pin_linearity, pin_contraction,
             pin_vanishing_gate, pin_segment_correction, pin_sliding_window]
 
 
