@@ -740,13 +740,19 @@ def gdn_oracle_sample(cfg, target_s: float, threads: int) -> dict:
     heads = max(1, min(cfg.B * cfg.H, threads))
     probe = inputs(heads, min(cfg.T, 256))
     run(probe)
-    per_token = run(probe) / (heads * probe[0].shape[-2])
-    T = int(min(cfg.T, max(256, target_s / per_token / heads)))
-    dt = run(inputs(heads, T))
-    return {"value": heads * T / dt, "unit": "tokens/s", "cores": min(threads, heads),
+    # host-seconds per token with every thread busy
+    per_token = run(probe) / (heads * probe[0].shape[-2]) * min(heads, threads) / threads
+    budget = target_s / per_token                        # tokens that fill target_s
+    T = int(min(cfg.T, max(256, budget / heads)))
+    if T == cfg.T:                                       # whole sequences: widen to more heads
+        heads = int(min(cfg.B * cfg.H, max(heads, budget / T)))
+    repeat = max(1, int(budget / (heads * T))) if (heads == cfg.B * cfg.H and T == cfg.T) else 1
+    ins = inputs(heads, T)
+    dt = sum(run(ins) for _ in range(repeat))
+    return {"value": repeat * heads * T / dt, "unit": "tokens/s", "cores": min(threads, heads),
             "kind": "oracle", "seconds": dt,
-            "sample": f"{heads} heads x {T} tokens of {cfg.name} (dk={cfg.dk}, dv={cfg.dv}), "
-                      f"fp64 gated-delta-rule recurrence, {dt:.1f} s"}
+            "sample": f"{repeat} x {heads} heads x {T} tokens of {cfg.name} (dk={cfg.dk}, "
+                      f"dv={cfg.dv}), fp64 gated-delta-rule recurrence, {dt:.1f} s"}
 
 
 def decode_leg(args, world, rank, dev, gla, barrier, max_over_ranks, pk):
