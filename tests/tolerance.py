@@ -32,8 +32,9 @@ def half_ulp_bf16(x) -> np.ndarray:
     return np.where(ax > 0, np.exp2(e - 8.0), 0.0)
 
 
-def errors(x, ref, bf16_output: bool = False):
-    """Returns (relative L2 error, max excess abs error, RMS of ref)."""
+def error_report(x, ref, bf16_output: bool = False) -> dict:
+    """Relative L2 error, the plain max abs error, the max abs error beyond the
+    output rounding allowance, and the RMS of ref."""
     x = np.asarray(x, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert x.shape == ref.shape, (x.shape, ref.shape)
@@ -41,19 +42,35 @@ def errors(x, ref, bf16_output: bool = False):
     nref = np.linalg.norm(ref)
     rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
     rel = float(np.linalg.norm(diff) / nref) if nref > 0 else float(np.linalg.norm(diff))
+    plain = float(np.max(diff)) if diff.size else 0.0
     if bf16_output:
         diff = diff - half_ulp_bf16(np.maximum(np.abs(x), np.abs(ref)))
-    maxabs = float(np.max(diff)) if diff.size else 0.0
-    return rel, maxabs, rms
+    excess = float(np.max(diff)) if diff.size else 0.0
+    return {"rel_l2": rel, "max_abs": plain, "max_abs_excess": excess, "rms": rms}
+
+
+def errors(x, ref, bf16_output: bool = False):
+    """Returns (relative L2 error, max excess abs error, RMS of ref)."""
+    r = error_report(x, ref, bf16_output)
+    return r["rel_l2"], r["max_abs_excess"], r["rms"]
+
+
+# Every comparison made in this process, for the run's closing summary: the plain
+# max abs error is reported beside the one the bar applies to.
+RECORDS: list = []
 
 
 def assert_close(x, ref, what: str = "", bf16_output: bool = False) -> dict:
     xa = np.asarray(x, dtype=np.float64)
     assert np.all(np.isfinite(xa)), f"{what}: non-finite values"
-    rel, maxabs, rms = errors(xa, ref, bf16_output)
-    assert rel <= REL_L2, f"{what}: relative L2 error {rel:.3e} > {REL_L2}"
+    r = error_report(xa, ref, bf16_output)
+    rel, maxabs, rms = r["rel_l2"], r["max_abs_excess"], r["rms"]
+    RECORDS.append(dict(r, what=what, bf16_output=bf16_output))
+    plain = (f"plain max abs {r['max_abs']:.3e} = {r['max_abs'] / rms:.3e} RMS"
+             if rms > 0 else f"plain max abs {r['max_abs']:.3e}")
+    assert rel <= REL_L2, f"{what}: relative L2 error {rel:.3e} > {REL_L2} ({plain})"
     bound = MAX_ABS_OVER_RMS * rms
     assert maxabs <= bound or (rms == 0.0 and maxabs <= 0.0), (
         f"{what}: max abs error beyond the output rounding {maxabs:.3e} > "
-        f"{MAX_ABS_OVER_RMS} * RMS ({bound:.3e})")
-    return {"rel_l2": rel, "max_abs_excess": maxabs, "rms": rms}
+        f"{MAX_ABS_OVER_RMS} * RMS ({bound:.3e}); {plain}")
+    return r
