@@ -56,9 +56,9 @@ def peaks():
 # --------------------------------------------------------------------------- workloads
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum, both launches of
-# one call) measured with ncu on the long workload at full size, with the
-# sources whose hash is given (profiles/chunk_fwd_B2-H16-T32768-dk128-dv256.md).
-# Any change to those sources makes the figure stale: it is then reported as null.
+# one call) measured with ncu on the long workload (B2 H16 T32768 dk128 dv256)
+# at full size, with the kernel sources whose hash is given.  Any change to
+# those sources makes the figure stale: it is then reported as null.
 MEASURED_TRAFFIC = {"workload": "B2-H16-T32768-dk128-dv256", "sources": "1444bf3a00d01fcc",
                     "bytes_per_call": 1615176192 + 509176832 + 35845376 + 2560}
 TRAFFIC_SOURCES = ["gla_api.cu", "gla_chunk.cu", "gla_chunk_kernel.cuh", "gla_internal.h", "gla_ptx.cuh"]
@@ -77,6 +77,14 @@ BWD_TRAFFIC_SOURCES = ["gla_api.cu", "gla_backward.cu", "gla_internal.h", "gla_p
 MEASURED_GDN_TRAFFIC = {"T": 32768, "dk": 128, "dv": 256, "heads": 8, "sources": "ef91c872e7aeb93f",
                         "bytes_per_launch": 272358144 + 110092032}
 GDN_TRAFFIC_SOURCES = ["gla_gdn.cu"]
+
+
+# ncu DRAM bytes (read + write) of one decode step at B=256 H=32 dk=dv=128 (the 5th
+# launch of a run: 6.715 TB/s x 152.93 us), for the decode source hashed in "sources".
+# Part of the state is still in L2 from the previous step, so DRAM moves 0.95x the
+# algorithmic bytes.
+MEASURED_DECODE_TRAFFIC = {"sources": "96841f7d24f0df73", "bytes_per_step": 1026925000}
+DECODE_TRAFFIC_SOURCES = ["gla_decode.cu"]
 
 
 def kernel_sources_hash(files=None) -> str:
@@ -154,9 +162,36 @@ def packed_lengths(total: int, n: int, seed: int) -> list:
     return [int(x) for x in lens]
 
 
-def chunk_flops(cfg, C: int = 64) -> int:
+# tokens per chunk of the chunked forward kernel
+KERNEL_CHUNK = 128
+
+
+def chunk_flops(cfg, C: int = KERNEL_CHUNK) -> int:
     """Algorithmic flops (causal entries only) at chunk size C, as counted for the roofline."""
     return cfg.tokens * ((C + 1) * (cfg.dk + cfg.dv) + 4 * cfg.dk * cfg.dv)
+
+
+def roofline(byts: int, flops: int, seconds: float, pk: dict, pk_kind: str,
+             tensor_peak_key: str = "bf16_tflops") -> dict:
+    """Roofline of one launch: the slower of its bytes at the HBM peak and its flops at
+    the bf16 tensor peak binds; `frac` = roofline time / measured time, and `achieved`
+    is the binding quantity's rate.  Both fractions are returned."""
+    hbm_gbs = byts / seconds / 1e9
+    tflops = flops / seconds / 1e12
+    t_hbm = byts / (pk["hbm_gbs"] * 1e9)
+    t_tc = flops / (pk[tensor_peak_key] * 1e12)
+    out = {"peak_kind": pk_kind, "algorithmic_bytes_per_launch": int(byts),
+           "flops_per_launch": int(flops), "hbm_frac": hbm_gbs / pk["hbm_gbs"],
+           "tensor_frac": tflops / pk[tensor_peak_key], "tensor_peak_tflops": pk[tensor_peak_key],
+           "tensor_peak_key": tensor_peak_key}
+    if t_hbm >= t_tc:
+        out.update({"bound": "hbm", "achieved": hbm_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                    "frac": hbm_gbs / pk["hbm_gbs"]})
+    else:
+        out.update({"bound": "tensor", "achieved": tflops, "peak": pk[tensor_peak_key],
+                    "unit": "TFLOP/s", "frac": tflops / pk[tensor_peak_key]})
+    # the order the contract lists the keys in
+    return {k: out[k] for k in ("bound", "achieved", "peak", "unit", "frac")} | out
 
 
 def decode_bytes(cfg) -> int:
@@ -301,6 +336,20 @@ def run_ours(args, rank, world, local_rank):
     else:
         line = {"metric": METRIC, "value": None, "unit": "tokens/s", "n_gpus": world,
                 "steps": 0, "warmup": args.warmup, "note": "chunked forward skipped (--only decode)"}
+    if (args.only == "both" and args.workload == "long" and not args.varlen
+            and args.gate == "channel" and not (args.batch or args.heads)):
+        # the other prefill workloads of the same kernel, secondary numbers on the line
+        import argparse as _ap
+        for wl, steps in (("medium", 100), ("very_long", 20)):
+            wargs = _ap.Namespace(**vars(args))
+            wargs.workload, wargs.no_e2e = wl, True
+            wargs.steps, wargs.warmup = min(args.steps, steps), max(args.warmup, 3)
+            w = chunk_leg(wargs, chunk_config(wargs), world, rank, dev, gla, barrier,
+                          max_over_ranks, pk, pk_kind)
+            line[wl] = {"metric": w["metric"], "value": w["value"], "unit": w["unit"],
+                        "ms_per_step": w["ms_per_step"], "steps": w["steps"],
+                        "workload": w["config"]["workload"], "roofline": w["roofline"],
+                        "gpu_launches": w["gpu_launches"], "clocks": w["clocks"]}
     if args.only != "chunk":
         line["decode"] = decode_leg(args, world, rank, dev, gla, barrier, max_over_ranks, pk)
     if args.only == "both" and not args.varlen and args.gate == "channel":
@@ -471,15 +520,10 @@ def chunk_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_
                    "B": cfg.B, "H": cfg.H, "T": cfg.T, "dk": cfg.dk,
                    "dv": cfg.dv, "chunk": 128, "replicas": world,
                    "l2": "inputs (%.2f GB) larger than L2; no flush" % (byts / 1e9)},
-        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": pk["hbm_gbs"],
-                     "unit": "GB/s", "frac": achieved_gbs / pk["hbm_gbs"],
-                     "traffic": None if (args.varlen or args.gate == "head") else measured_traffic(cfg),
-                     "traffic_unit": "bytes per call",
-                     "peak_kind": pk_kind, "kernel": "chunk_fwd_kernel",
-                     "algorithmic_bytes_per_launch": byts,
-                     "flops_per_launch": chunk_flops(cfg),
-                     "tensor_frac": chunk_flops(cfg) / (per_launch_ms / 1e3) / 1e12 /
-                     pk["bf16_tflops"]},
+        "roofline": roofline(byts, chunk_flops(cfg), per_launch_ms / 1e3, pk, pk_kind) | {
+            "traffic": None if (args.varlen or args.gate == "head") else measured_traffic(cfg),
+            "traffic_unit": "bytes per call", "kernel": "chunk_fwd_kernel",
+            "flops_chunk": KERNEL_CHUNK},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
@@ -780,9 +824,21 @@ def decode_leg(args, world, rank, dev, gla, barrier, max_over_ranks, pk):
     dms = max_over_ranks(d0.elapsed_time(d1)) / nsteps
     dbytes = decode_bytes(dc)
     dgbs = dbytes / (dms / 1e3) / 1e9
+    # DRAM bytes per step as ncu measured them (null once the kernel source changed):
+    # the algorithmic rate can read above the copy peak because part of the state hits
+    # in L2; the DRAM rate cannot
+    try:
+        fresh = kernel_sources_hash(DECODE_TRAFFIC_SOURCES) == MEASURED_DECODE_TRAFFIC["sources"]
+    except OSError:
+        fresh = False
+    traffic = MEASURED_DECODE_TRAFFIC["bytes_per_step"] if fresh else None
     decode = {"workload": dc.name, "steps_per_s": 1e3 / dms, "replicas": world,
               "ms_per_step": dms, "hbm_gbs": dgbs, "bytes_per_step": dbytes,
               "frac_of_hbm_peak": dgbs / pk["hbm_gbs"], "timed_steps": nsteps,
+              "traffic": traffic, "traffic_unit": "DRAM bytes per step (ncu)",
+              "dram_gbs": None if traffic is None else traffic / (dms / 1e3) / 1e9,
+              "dram_frac_of_hbm_peak": None if traffic is None
+              else traffic / (dms / 1e3) / 1e9 / pk["hbm_gbs"],
               "gpu_launches": nsteps}
     del dh0, dqs, dks, dvs, das, h, do
     torch.cuda.empty_cache()
@@ -920,7 +976,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="long", choices=["small", "medium", "long", "very_long"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--decode-steps", type=int, default=256)
+    ap.add_argument("--decode-steps", type=int, default=1024)
     ap.add_argument("--only", default="both", choices=["both", "chunk", "decode", "bwd", "gdn"],
                     help="run only the chunked forward, only the decode step, only the "
                          "chunkwise backward, or only the gated delta rule forward (the last "

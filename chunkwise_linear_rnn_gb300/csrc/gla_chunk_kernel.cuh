@@ -26,6 +26,11 @@
 // that changes is below e^-30 ~ 9e-14 of the state, under fp32 resolution.
 // Masked score entries are selected away, never multiplied by zero.
 //
+// A CTA pair folds the read-out scale into Qh (scale Q e^Gamma): both of an
+// output's products then arrive scaled, and the epilogue of the TMEM warps,
+// on the pair's critical path, only rounds.  A single CTA, whose preparation
+// is the longer path, scales in the epilogue.
+//
 // Precision.  bf16 operands carry 8 significant bits; the two roundings that
 // dominate the output error are removed by splitting the operand into a bf16
 // pair x = hi + lo: the rescaled keys Kh (score and state products) and the
@@ -361,7 +366,7 @@ __device__ __forceinline__ void zero_p_block(uint32_t taddr) {
 // `n` counts items; `last_flags` go to the chunk's last item; gtot0/gtot1
 // return the chunk's clamped Gamma at its end for the thread's channels (valid
 // in the last token part).  Returns false if a bounded wait expired.
-template <int DK, bool PACKED, bool SCALAR, typename BeforeEmptyWait>
+template <int DK, bool PACKED, bool SCALAR, bool FOLD, typename BeforeEmptyWait>
 __device__ __forceinline__ bool sub_chunk_items(const KParams &p, int bh, int t0, int lc,
                                                 bool store, int last_flags, int pt, uint8_t *sQ,
                                                 uint8_t *sK,
@@ -460,7 +465,8 @@ __device__ __forceinline__ bool sub_chunk_items(const KParams &p, int bh, int t0
             if (i >= sa && i < sb && t < T) {
                 const float2 qf = unpack_bf16x2(qb[static_cast<size_t>(t) * kStride]);
                 const float2 kf = unpack_bf16x2(kb[static_cast<size_t>(t) * kStride]);
-                qv = bf16x2_bits(qf.x * __expf(c0 - r0), qf.y * __expf(c1 - r1));
+                const float qs = FOLD ? p.scale : 1.f;
+                qv = bf16x2_bits(qf.x * qs * __expf(c0 - r0), qf.y * qs * __expf(c1 - r1));
                 split_pair(kf.x * __expf(r0 - c0), kf.y * __expf(r1 - c1), hi, lo);
             }
             *reinterpret_cast<uint32_t *>(sQ + off) = qv;
@@ -651,7 +657,7 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
                 const float2 kf =
                     unpack_bf16x2(in ? *reinterpret_cast<const uint32_t *>(sRawK + off) : 0u);
                 const float g0 = o0 + av[e].x, g1 = o1 + av[e].y;
-                rq[e] = bf16x2_bits(qf.x * ex2f(g0), qf.y * ex2f(g1));
+                rq[e] = bf16x2_bits(qf.x * p.scale * ex2f(g0), qf.y * p.scale * ex2f(g1));
                 split_pair(kf.x * ex2f(-g0), kf.y * ex2f(-g1), rh[e], rl[e]);
             }
             gc0 = o0 + c0;                       // Gamma log2 e at the chunk end (last part)
@@ -740,7 +746,7 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
             // channels, computed by each CTA of the pair on its own
             if (n > 0) ok &= mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status);
             float gt0 = 0.f, gt1 = 0.f;
-            ok &= sub_chunk_items<DK, PACKED, SCALAR>(p, bh, t0, lc, store, piece_end, pt, sQ, sK, sKlo, sG, sItem,
+            ok &= sub_chunk_items<DK, PACKED, SCALAR, true>(p, bh, t0, lc, store, piece_end, pt, sQ, sK, sKlo, sG, sItem,
                                       bars, n, gt0, gt1, [] {});
             if (pt < DK) {
                 // the chunk's clamped decay of channel pt, summed in token order
@@ -1050,7 +1056,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             }
             // ---- sub-chunk rescaling (chunks whose decay exceeds the bound)
             float gtot0 = 0.f, gtot1 = 0.f;
-            ok = sub_chunk_items<DK, PACKED, SCALAR>(p, bh, t0, lc, store, piece_end, pt, sQ, sK, sKlo, sG, sItem,
+            ok = sub_chunk_items<DK, PACKED, SCALAR, false>(p, bh, t0, lc, store, piece_end, pt, sQ, sK, sKlo, sG, sItem,
                                      bars, n, gtot0, gtot1, [] {});
             if (last_part) {
                 gseg0 += gtot0;
@@ -1513,6 +1519,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                 if (kStageInS && (it.flags & kItemLast) && lane == 0)
                     mbar_arrive(&bars[kBarVEmpty0 + it.lc % VS]);
                 {
+                    // a CTA pair folds the read-out scale into Qh
+                    const float osc = PAIR ? 1.f : p.scale;
                     const uint32_t tO = tmem + lane_base + (ob ? TM::kO1 : TM::kO0);
                     const int t = it.t0 + i;
                     const bool st = store_item && !staged && i >= it.r0 && i < it.r1 && t < sq.len;
@@ -1531,10 +1539,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
 #pragma unroll
                             for (int j = 0; j < 32; j += 8) {
                                 uint4 pk;
-                                pk.x = pack_bf16x2(p.scale * __uint_as_float(r[j]), p.scale * __uint_as_float(r[j + 1]));
-                                pk.y = pack_bf16x2(p.scale * __uint_as_float(r[j + 2]), p.scale * __uint_as_float(r[j + 3]));
-                                pk.z = pack_bf16x2(p.scale * __uint_as_float(r[j + 4]), p.scale * __uint_as_float(r[j + 5]));
-                                pk.w = pack_bf16x2(p.scale * __uint_as_float(r[j + 6]), p.scale * __uint_as_float(r[j + 7]));
+                                pk.x = pack_bf16x2(osc * __uint_as_float(r[j]), osc * __uint_as_float(r[j + 1]));
+                                pk.y = pack_bf16x2(osc * __uint_as_float(r[j + 2]), osc * __uint_as_float(r[j + 3]));
+                                pk.z = pack_bf16x2(osc * __uint_as_float(r[j + 4]), osc * __uint_as_float(r[j + 5]));
+                                pk.w = pack_bf16x2(osc * __uint_as_float(r[j + 6]), osc * __uint_as_float(r[j + 7]));
                                 if (staged)
                                     *reinterpret_cast<uint4 *>(sStage + sw128_offset(i, cc + j, kBlk)) = pk;
                                 else if (st)

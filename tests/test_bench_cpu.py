@@ -44,3 +44,31 @@ def test_reference_line_keeps_the_contract(only):
     assert ("chunk-bwd" in line["metric"]) == (only == "bwd")
     assert ("Gated DeltaNet" in line["metric"]) == (only == "gdn")
     assert line["ms_per_step"] > 0
+
+
+def test_roofline_binds_on_the_slower_roof():
+    """The roofline's bound is whichever of bytes / HBM peak and flops / tensor peak
+    takes longer, and its fraction is that roof's time over the measured time."""
+    sys.path.insert(0, ROOT)
+    import bench
+    pk = {"hbm_gbs": 1000.0, "bf16_tflops": 100.0}
+    # 1 GB at 1000 GB/s = 1 ms; 50 GFLOP at 100 TF/s = 0.5 ms: HBM binds
+    r = bench.roofline(10**9, 5 * 10**10, 2e-3, pk, "test")
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert abs(r["frac"] - 0.5) < 1e-12 and abs(r["achieved"] - 500.0) < 1e-9
+    assert abs(r["tensor_frac"] - 0.25) < 1e-12
+    # 200 GFLOP = 2 ms against 1 ms of bytes: the tensor roof binds
+    r = bench.roofline(10**9, 2 * 10**11, 4e-3, pk, "test")
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert abs(r["frac"] - 0.5) < 1e-12 and abs(r["hbm_frac"] - 0.25) < 1e-12
+    assert list(r)[:5] == ["bound", "achieved", "peak", "unit", "frac"]
+
+
+def test_chunk_flops_use_the_kernel_chunk():
+    sys.path.insert(0, ROOT)
+    import bench
+    from synth import CHUNK_CONFIGS
+    cfg = CHUNK_CONFIGS["long"]
+    per_token = (bench.KERNEL_CHUNK + 1) * (cfg.dk + cfg.dv) + 4 * cfg.dk * cfg.dv
+    assert bench.KERNEL_CHUNK == 128
+    assert bench.chunk_flops(cfg) == cfg.tokens * per_token
