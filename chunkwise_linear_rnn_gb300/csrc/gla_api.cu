@@ -276,6 +276,9 @@ int chunk_fwd_with_scratch(const void *q, const void *k, const void *v, const fl
     p.NS = 0;
     p.gate_per_head = op.gate_per_head;
     p.force_exact = op.force_exact ? 1 : 0;
+    // two segments per sequence, each range one whole segment: the first
+    // segment's CTA pair corrects the second segment's window itself
+    p.fuse = (pl.pair && pl.seg_max == 2 && pl.NC % pl.L == 0 && pl.NC / pl.L == 2) ? 1 : 0;
     p.status = dev->status;
     return launch_chunk_fwd(p, stream) == 0 ? GLA_OK : GLA_ERR_LAUNCH;
 }

@@ -71,6 +71,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "gla_internal.h"
@@ -99,6 +100,9 @@ constexpr int kItemLast = 1;      // last item of its chunk: releases the chunk'
 constexpr int kItemStore = 2;     // store this item's output rows
 constexpr int kItemEnd = 4;       // end of the item stream
 constexpr int kItemPieceEnd = 8;  // last item of a piece (FULL pass): its end state is stored
+// with kItemPieceEnd: the state is stored and kept, because the CTA goes on
+// into the next segment's decay window with it (two-segment plans)
+constexpr int kItemKeep = 16;
 
 constexpr int kModeFull = 0, kModeCorrect = 1;
 
@@ -198,6 +202,10 @@ struct KParams {
     const int4 *seqs;
     int NS, H;
     int mode, force_sub;
+    // Two-segment plans (CTA pairs): the CTA of a sequence's first segment,
+    // whose start state is exact, goes on through the second segment's decay
+    // window, storing its outputs, in place of the correction pass.
+    int fuse;
     long long n_units;   // CTAs (clusters) per tile column in this launch
     unsigned int *status;
 };
@@ -551,15 +559,25 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
 
     // the pieces of this CTA's range, one after another: the current piece is
     // chunks [c, c_end) of sequence bh (the rest is recomputed at piece ends)
-    int bh, c, c_end;
+    int bh, c, c_end, seg_cur;
     bool closed;
     {
         const Piece pc = piece_at<PACKED>(p, g_begin, g_end);
         bh = pc.u;
         c = pc.c0;
         c_end = pc.c1;
+        seg_cur = pc.seg;
         closed = p.mode == kModeFull && pc.seg == 0;
     }
+    // correction semantics (every output stored, stop once the window has
+    // closed): the correction pass, or a first segment's CTA going on into
+    // the second segment's window
+    bool corr = p.mode == kModeCorrect;
+    // whether the current piece, a first segment whose start state is exact,
+    // is followed by the second segment's window in this CTA
+    auto continues = [&]() {
+        return p.fuse != 0 && !corr && seg_cur == 0 && nseg_of<PACKED>(p, bh) == 2;
+    };
     float gseg = 0.f;                            // threads pt < DK: channel pt
     int n = 0;                                   // items published
     int nx = 0;                                  // operand exchanges made
@@ -668,7 +686,9 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
             int nc = -1, nbh = bh;
             if (c + 1 < c_end) {
                 nc = c + 1;
-            } else if (p.mode == kModeFull) {
+            } else if (continues()) {
+                nc = c + 1;                      // the second segment's first chunk
+            } else if (p.mode == kModeFull && !corr) {
                 const long long gn = seq_of<PACKED>(p, bh).a + c_end, ge = full_range_end(p);
                 if (gn < ge) {
                     const Piece next = piece_at<PACKED>(p, gn, ge);
@@ -697,10 +717,13 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
         const bool win = !closed && pt < DK && gseg > -kWindowCut;
         const bool any_win = bar_or(1, kPrepThreads, win);
         if (!closed && !any_win) closed = true;
-        if (!have || (p.mode == kModeCorrect && closed)) break;
-        const bool store = p.mode == kModeCorrect || closed;
-        // the FULL pass stores the state at the end of every piece
-        const int piece_end = (p.mode == kModeFull && c + 1 == c_end) ? kItemPieceEnd : 0;
+        if (!have || (corr && closed)) break;
+        const bool store = corr || closed;
+        // the FULL pass stores the state at the end of every piece (and keeps
+        // it when the CTA goes on into the next segment's window)
+        const int piece_end = (p.mode == kModeFull && !corr && c + 1 == c_end)
+                                  ? (kItemPieceEnd | (continues() ? kItemKeep : 0))
+                                  : 0;
         // ---- both CTAs' verdicts: one branch for all threads, even for one
         // whose wait expired
         ok &= mbar_wait_bounded(&bars[kBarVerd0 + (lc & 1)], (lc >> 1) & 1, p.status);
@@ -774,12 +797,22 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
                 const int seg = static_cast<int>((a + c_end - 1) / p.L - a / p.L);
                 p.ws_decay[(static_cast<size_t>(seg) * BHn + bh) * DK + pt] = gseg;
             }
+            if (piece_end & kItemKeep) {
+                // on into the second segment's window, with the exact state
+                corr = true;
+                seg_cur = 1;
+                c_end = seq_of<PACKED>(p, bh).nch;
+                gseg = 0.f;
+                closed = false;
+                continue;
+            }
             const long long gn = a + c_end, ge = full_range_end(p);
             if (gn >= ge) break;
             const Piece next = piece_at<PACKED>(p, gn, ge);
             bh = next.u;
             c = next.c0;
             c_end = next.c1;
+            seg_cur = next.seg;
             gseg = 0.f;
             closed = next.seg == 0;
         }
@@ -1459,6 +1492,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             const bool staged = store_item && it.r0 == 0 && it.r1 == kChunk &&
                                 (!PACKED || it.t0 + kChunk <= sq.len);
             const bool piece_end = (it.flags & kItemPieceEnd) != 0;
+            const bool keep = (it.flags & kItemKeep) != 0;
             auto state_step = [&]() -> bool {
                 if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarSDone], n & 1, p.status)))
                     return false;
@@ -1478,7 +1512,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
 #pragma unroll
                         for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * f);
                         tmem_st32(tS + c0, r);
-                        if (piece_end) continue;   // the next piece starts afresh
+                        if (piece_end && !keep) continue;   // the next piece starts afresh
 #pragma unroll
                         for (int j = 0; j < 32; j += 8) {
                             uint4 pk;
@@ -1500,9 +1534,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                     done.u = it.bh;
                     done.seg = static_cast<int>((a + cl) / p.L - a / p.L);
                     store_state(done);
-                    const long long gn = a + cl + 1, ge = full_range_end(p);
-                    if (gn < ge) load_state(piece_at<PACKED>(p, gn, ge));
-                    return true;
+                    if (!keep) {
+                        const long long gn = a + cl + 1, ge = full_range_end(p);
+                        if (gn < ge) load_state(piece_at<PACKED>(p, gn, ge));
+                        return true;
+                    }
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -1594,6 +1630,28 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
     if constexpr (PAIR) cluster_sync_all();
 }
 
+// Final states of a two-segment plan whose correction ran inside the FULL pass:
+// hT = diag(e^G_1) S*_0 + S*_1 per (sequence, key row), where S*_0 is the
+// exact state at the end of the first segment, and S*_1 and G_1 are the second
+// segment's end state from a zero start and its total log-decay.  One thread
+// per four value columns.
+__global__ void __launch_bounds__(256) two_segment_states_kernel(const float *__restrict__ ws_state,
+                                                                 const float *__restrict__ ws_decay,
+                                                                 float *__restrict__ hT, long long BH,
+                                                                 int dk, int dv) {
+    const long long quads = BH * dk * (dv / 4);
+    for (long long q = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; q < quads;
+         q += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long row = q / (dv / 4);           // (sequence, key row)
+        const float e = __expf(ws_decay[BH * dk + row]);
+        const float4 s0 = reinterpret_cast<const float4 *>(ws_state)[q];
+        const float4 s1 = reinterpret_cast<const float4 *>(ws_state + BH * dk * dv)[q];
+        reinterpret_cast<float4 *>(hT)[q] =
+            make_float4(fmaf(e, s0.x, s1.x), fmaf(e, s0.y, s1.y), fmaf(e, s0.z, s1.z),
+                        fmaf(e, s0.w, s1.w));
+    }
+}
+
 template <int DK, int DVT, bool PAIR, bool PACKED, bool SCALAR>
 int launch_tiles(const ChunkLaunch &c, cudaStream_t stream) {
     using L = Smem<DK, DVT, PAIR>;
@@ -1633,6 +1691,7 @@ int launch_tiles(const ChunkLaunch &c, cudaStream_t stream) {
     p.seg_max = c.seg_max;
     p.force_sub = c.force_exact;
     p.status = c.status;
+    p.fuse = c.fuse;
     const int n_dvt = c.dv / DVT;
     // `count` CTAs (clusters) per tile column; the index is blockIdx.y +
     // blockIdx.z * gridDim.y, so that any count fits the grid's limits
@@ -1661,6 +1720,16 @@ int launch_tiles(const ChunkLaunch &c, cudaStream_t stream) {
     // segment >= 1), those past a sequence's segment count leave at once
     cudaError_t e = launch(kModeFull, c.W);
     if (e != cudaSuccess || c.seg_max == 1) return static_cast<int>(e);
+    if (c.fuse) {
+        // the windows were corrected in the FULL pass; only hT remains
+        if (!c.hT) return 0;
+        const long long quads = static_cast<long long>(c.B) * c.H * DK * (c.dv / 4);
+        const int blocks = static_cast<int>(std::min<long long>((quads + 255) / 256, 4096));
+        two_segment_states_kernel<<<blocks, 256, 0, stream>>>(c.ws_state, c.ws_decay, c.hT,
+                                                               static_cast<long long>(c.B) * c.H,
+                                                               DK, c.dv);
+        return static_cast<int>(cudaGetLastError());
+    }
     return static_cast<int>(
         launch(kModeCorrect, static_cast<long long>(c.B) * c.H * (c.seg_max - 1)));
 }

@@ -39,6 +39,10 @@ struct ChunkLaunch {
     int NS;
     int gate_per_head;        // 1: log_alpha is [BH, T], one gate per token (fixed length only)
     int force_exact;          // process every chunk in rescaled sub-chunks
+    // two-segment plan of CTA pairs whose ranges are whole segments: the first
+    // segment's CTA corrects the second segment's window itself, and a small
+    // kernel forms hT (no correction pass)
+    int fuse;
     unsigned int *status;     // device status word
 };
 
