@@ -24,6 +24,7 @@ GLA_ERR_ALLOC = 6
 GLA_ERR_SCRATCH = 7
 
 EXPORTED = ("gla_chunk_fwd", "gla_chunk_fwd_ex", "gla_chunk_fwd_plan", "gla_chunk_fwd_noalloc",
+            "gla_chunk_fwd_debug",
             "gla_chunk_fwd_host", "gla_chunk_fwd_varlen", "gla_chunk_fwd_varlen_ex",
             "gla_chunk_fwd_varlen_plan", "gla_chunk_bwd", "gla_chunk_bwd_ex",
             "gla_chunk_bwd_plan", "gla_chunk_bwd_varlen", "gla_chunk_bwd_varlen_ex",
@@ -35,6 +36,12 @@ class GlaChunkOptions(ctypes.Structure):
     _fields_ = [("segments", ctypes.c_int), ("dv_tile", ctypes.c_int),
                 ("force_exact", ctypes.c_int), ("cta_pair", ctypes.c_int),
                 ("gate_per_head", ctypes.c_int), ("reserved", ctypes.c_int * 3)]
+
+
+class GlaChunkDebug(ctypes.Structure):
+    """gla_chunk_debug (include/gla.h): test instrumentation of the chunked forward."""
+    _fields_ = [("gamma", ctypes.c_void_p), ("block_len", ctypes.c_void_p),
+                ("wait_limit_us", ctypes.c_uint), ("withhold_v", ctypes.c_int)]
 
 
 class GlaError(RuntimeError):
@@ -57,6 +64,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.gla_chunk_fwd_noalloc.argtypes = [vp, vp, vp, fp, f, fp, vp, fp, i, i, i, i, i,
                                           ctypes.POINTER(GlaChunkOptions), vp]
     lib.gla_chunk_fwd_noalloc.restype = i
+    lib.gla_chunk_fwd_debug.argtypes = [vp, vp, vp, fp, f, fp, vp, fp, i, i, i, i, i,
+                                        ctypes.POINTER(GlaChunkOptions),
+                                        ctypes.POINTER(GlaChunkDebug), vp]
+    lib.gla_chunk_fwd_debug.restype = i
     lib.gla_chunk_fwd_host.argtypes = [vp, vp, vp, fp, f, fp, vp, fp, i, i, i, i, i, vp]
     lib.gla_chunk_fwd_host.restype = i
     ip = ctypes.POINTER(ctypes.c_int)

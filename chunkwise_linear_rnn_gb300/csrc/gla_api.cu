@@ -204,7 +204,7 @@ bool dv_ok(int dv) { return dv == 64 || dv == 128 || dv == 256; }
 int chunk_fwd_with_scratch(const void *q, const void *k, const void *v, const float *log_alpha,
                            float scale, const float *h0, void *o, float *hT, int B, int H, int T,
                            int dk, int dv, const gla_chunk_options *opts, cudaStream_t stream,
-                           void *scratch, size_t scratch_bytes) {
+                           void *scratch, size_t scratch_bytes, const gla_chunk_debug *dbg) {
     if (!q || !k || !v || !log_alpha || !o) return GLA_ERR_ARG;
     if (B <= 0 || H <= 0 || T <= 0) return GLA_ERR_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_alpha) ||
@@ -216,6 +216,7 @@ int chunk_fwd_with_scratch(const void *q, const void *k, const void *v, const fl
     if (!options_ok(dv, op)) return GLA_ERR_ARG;
     if (static_cast<long long>(B) * H > 0x7fffffffLL) return GLA_ERR_ARG;
     if (scratch && !aligned16(scratch)) return GLA_ERR_ARG;
+    if (dbg && (dbg->withhold_v < 0 || (dbg->gamma && !aligned16(dbg->gamma)))) return GLA_ERR_ARG;
 
     DeviceInfo *dev = nullptr;
     int st = current_device(&dev);
@@ -280,6 +281,12 @@ int chunk_fwd_with_scratch(const void *q, const void *k, const void *v, const fl
     // segment's CTA pair corrects the second segment's window itself
     p.fuse = (pl.pair && pl.seg_max == 2 && pl.NC % pl.L == 0 && pl.NC / pl.L == 2) ? 1 : 0;
     p.status = dev->status;
+    if (dbg) {
+        p.wait_ns = static_cast<unsigned long long>(dbg->wait_limit_us) * 1000ull;
+        p.dbg_gamma = dbg->gamma;
+        p.dbg_blk = dbg->block_len;
+        p.withhold_v = dbg->withhold_v;
+    }
     return launch_chunk_fwd(p, stream) == 0 ? GLA_OK : GLA_ERR_LAUNCH;
 }
 
@@ -488,6 +495,14 @@ const char *gla_status_string(int status) {
 int gla_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *log_alpha,
                      float scale, const float *h0, void *o, float *hT, int B, int H, int T,
                      int dk, int dv, const gla_chunk_options *opts, cudaStream_t stream) {
+    return gla_chunk_fwd_debug(q, k, v, log_alpha, scale, h0, o, hT, B, H, T, dk, dv, opts,
+                               nullptr, stream);
+}
+
+int gla_chunk_fwd_debug(const void *q, const void *k, const void *v, const float *log_alpha,
+                        float scale, const float *h0, void *o, float *hT, int B, int H, int T,
+                        int dk, int dv, const gla_chunk_options *opts, const gla_chunk_debug *dbg,
+                        cudaStream_t stream) {
     using namespace gla;
     if (!q || !k || !v || !log_alpha || !o) return GLA_ERR_ARG;
     if (B <= 0 || H <= 0 || T <= 0) return GLA_ERR_ARG;
@@ -514,7 +529,7 @@ int gla_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *l
         }
     }
     const int r = chunk_fwd_with_scratch(q, k, v, log_alpha, scale, h0, o, hT, B, H, T, dk, dv,
-                                         &op, stream, ws, ws_bytes);
+                                         &op, stream, ws, ws_bytes, dbg);
     if (ws) cudaFreeAsync(ws, stream);
     return r;
 }

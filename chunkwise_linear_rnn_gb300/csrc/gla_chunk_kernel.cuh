@@ -123,11 +123,11 @@ enum Bar {
     kBarQkFull = 0, kBarQkEmpty, kBarItem0, kBarItem1, kBarPFull, kBarPSplit, kBarSDone, kBarSReady,
     kBarOFull0, kBarOFull1, kBarOFree0, kBarOFree1, kBarVFull0, kBarVFull1, kBarVEmpty0,
     kBarVEmpty1, kBarAFull, kBarQkRaw, kBarReq, kBarXchg0, kBarXchg1, kBarVerd0, kBarVerd1,
-    kNumBars
+    kBarDrain, kNumBars
 };
 // arrival counts, in enum order (a CTA pair doubles kBarQkEmpty: both MMAs commit to it)
 __device__ constexpr uint32_t kBarCounts[kNumBars] = {kPrepWarps, 1, 1, 1, 1, 4, 1, 4, 1, 1, 4, 4,
-                                                      1, 1, 4, 4, 1, 1, 1, 1, 1, 1, 1};
+                                                      1, 1, 4, 4, 1, 1, 1, 1, 1, 1, 1, 1};
 
 template <int DK, int DVT, bool PAIR>
 struct Smem {
@@ -208,6 +208,16 @@ struct KParams {
     int fuse;
     long long n_units;   // CTAs (clusters) per tile column in this launch
     unsigned int *status;
+    unsigned long long wait_ns;   // limit of every bounded wait
+    // Test instrumentation (null / 0 in production): the in-chunk prefix sums
+    // of log_alpha the preparation used ([rows][DK] fp32, natural-log units,
+    // relative to the reference of the token's block), the block length of
+    // every chunk (by global chunk index), and a value tile the TMA thread
+    // withholds (n > 0: the n-th chunk each CTA of the FULL pass serves gets
+    // no V load, so that the waits for it expire).
+    float *dbg_gamma;
+    int *dbg_blk;
+    int withhold_v;
 };
 
 // Where sequence u lives: tensor head z, token rows [y0, y0 + len), nch
@@ -366,6 +376,17 @@ __device__ __forceinline__ void zero_p_block(uint32_t taddr) {
     tmem_st16(taddr + 16, z);
 }
 
+// Test instrumentation: the in-chunk prefix sums of token t (of sequence u)
+// for channels ch and ch + 1, given in log2 units, stored in natural-log units.
+template <bool PACKED>
+__device__ __forceinline__ void dbg_gamma_pair(const KParams &p, int u, int t, int ch, float g0,
+                                               float g1, int dk) {
+    const Seq sq = seq_of<PACKED>(p, u);
+    if (t >= sq.len) return;
+    const size_t row = static_cast<size_t>(sq.z) * p.T + sq.y0 + t;
+    *reinterpret_cast<float2 *>(p.dbg_gamma + row * dk + ch) = make_float2(g0 * kLn2, g1 * kLn2);
+}
+
 // Sub-chunk rescaling of one chunk (prep threads): the largest power-of-two
 // block length cs whose every block keeps |Gamma - r_block| <= kExpBound
 // (clamped gates); each block becomes one item, written to the operand tiles
@@ -375,8 +396,9 @@ __device__ __forceinline__ void zero_p_block(uint32_t taddr) {
 // return the chunk's clamped Gamma at its end for the thread's channels (valid
 // in the last token part).  Returns false if a bounded wait expired.
 template <int DK, bool PACKED, bool SCALAR, bool FOLD, typename BeforeEmptyWait>
-__device__ __forceinline__ bool sub_chunk_items(const KParams &p, int bh, int t0, int lc,
-                                                bool store, int last_flags, int pt, uint8_t *sQ,
+__device__ __forceinline__ bool sub_chunk_items(const KParams &p, int dbg_block, int bh, int t0,
+                                                int lc, bool store, int last_flags, int pt,
+                                                uint8_t *sQ,
                                                 uint8_t *sK,
                                                 uint8_t *sKlo, float *sG, ItemInfo *sItem,
                                                 uint64_t *bars, int &n, float &gtot0,
@@ -441,13 +463,15 @@ __device__ __forceinline__ bool sub_chunk_items(const KParams &p, int bh, int t0
     }
     // cs == 1 always satisfies the bound: a single clamped gate is within it.
     const int n_sub = kChunk / cs;
+    const bool dbg = p.dbg_gamma != nullptr && (dbg_block == -1 || (ch >> 6) == dbg_block);
+    if (p.dbg_blk != nullptr && dbg_block != -2 && pt == 0) p.dbg_blk[sq.a + t0 / kChunk] = cs;
     bool ok = true;
     for (int sidx = 0; sidx < n_sub; ++sidx) {
         const int sa = sidx * cs, sb = sa + cs;
         bool okw = true;
         if (sidx > 0) {
             before_empty_wait();
-            okw = mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status);
+            okw = mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status, p.wait_ns);
         }
         ok = !bar_or(4, kPrepThreads, !okw);
         if (!ok) break;
@@ -471,6 +495,9 @@ __device__ __forceinline__ bool sub_chunk_items(const KParams &p, int bh, int t0
             const uint32_t off = sw128_offset(i, ch, kBlk);
             uint32_t hi = 0u, lo = 0u, qv = 0u;
             if (i >= sa && i < sb && t < T) {
+                if (dbg)
+                    *reinterpret_cast<float2 *>(p.dbg_gamma + (row0 + t) * DK + ch) =
+                        make_float2(c0 - r0, c1 - r1);
                 const float2 qf = unpack_bf16x2(qb[static_cast<size_t>(t) * kStride]);
                 const float2 kf = unpack_bf16x2(kb[static_cast<size_t>(t) * kStride]);
                 const float qs = FOLD ? p.scale : 1.f;
@@ -605,7 +632,7 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
             // ---- phase A: prefix sums of this thread's part (log2 units) in
             // registers; the part total goes to the A tile's last row of the part
             if (pt == 0) mbar_arrive_expect_tx(&bars[kBarVerd0 + (lc & 1)], 4u);
-            ok &= mbar_wait_bounded(&bars[kBarAFull], lc & 1, p.status);
+            ok &= mbar_wait_bounded(&bars[kBarAFull], lc & 1, p.status, p.wait_ns);
             spec = false;
             // rows past the sequence end (the tail of a packed sequence) count
             // as gate 0 and operands 0
@@ -664,7 +691,7 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
             }
             // ---- phase B into registers (values of a chunk that broke the
             // bound are computed but never used)
-            ok &= mbar_wait_bounded(&bars[kBarQkRaw], lc & 1, p.status);
+            ok &= mbar_wait_bounded(&bars[kBarQkRaw], lc & 1, p.status, p.wait_ns);
 #pragma unroll
             for (int e = 0; e < TP; ++e) {
                 const int i = part * TP + e;
@@ -677,6 +704,7 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
                 const float g0 = o0 + av[e].x, g1 = o1 + av[e].y;
                 rq[e] = bf16x2_bits(qf.x * p.scale * ex2f(g0), qf.y * p.scale * ex2f(g1));
                 split_pair(kf.x * ex2f(-g0), kf.y * ex2f(-g1), rh[e], rl[e]);
+                if (p.dbg_gamma != nullptr) dbg_gamma_pair<PACKED>(p, bh, t0 + i, ch, g0, g1, DK);
             }
             gc0 = o0 + c0;                       // Gamma log2 e at the chunk end (last part)
             gc1 = o1 + c1;
@@ -709,7 +737,7 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
         // ---- segment decay through chunk c-1 (the previous exchange's factors)
         if (pend) {
             const int x = nx - 1;
-            ok &= mbar_wait_bounded(&bars[kBarXchg0 + (x & 1)], (x >> 1) & 1, p.status);
+            ok &= mbar_wait_bounded(&bars[kBarXchg0 + (x & 1)], (x >> 1) & 1, p.status, p.wait_ns);
             if (pt < DK) gseg += __logf(sG[((n - 1) & 1) * DK + pt]);
             pend = false;
         }
@@ -726,13 +754,13 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
                                   : 0;
         // ---- both CTAs' verdicts: one branch for all threads, even for one
         // whose wait expired
-        ok &= mbar_wait_bounded(&bars[kBarVerd0 + (lc & 1)], (lc >> 1) & 1, p.status);
+        ok &= mbar_wait_bounded(&bars[kBarVerd0 + (lc & 1)], (lc >> 1) & 1, p.status, p.wait_ns);
         const bool bad = bar_or(2, kPrepThreads, bad_here || sVerd[lc & 1] != 0u);
         prepped_last = false;
         ++used;
         if (!bad) {
             // ---- both CTAs' MMAs are done with the previous item's tiles
-            if (n > 0) ok &= mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status);
+            if (n > 0) ok &= mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status, p.wait_ns);
 #pragma unroll
             for (int e = 0; e < TP; ++e) {
                 const uint32_t off = sw128_offset(part * TP + e, ch, kBlk);
@@ -747,6 +775,7 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
             fence_proxy_async_smem();
             named_barrier(5, kPrepThreads);
             if (pt == 0) {
+                if (p.dbg_blk != nullptr && rank == 0) p.dbg_blk[seq_of<PACKED>(p, bh).a + c] = kChunk;
                 sItem[n & 1] = ItemInfo{t0, 0, kChunk,
                                         kItemLast | (store ? kItemStore : 0) | piece_end, lc, nx,
                                         bh, 0};
@@ -767,9 +796,9 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
         } else {
             // ---- a chunk whose decay breaks the bound: sub-chunk items over all
             // channels, computed by each CTA of the pair on its own
-            if (n > 0) ok &= mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status);
+            if (n > 0) ok &= mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status, p.wait_ns);
             float gt0 = 0.f, gt1 = 0.f;
-            ok &= sub_chunk_items<DK, PACKED, SCALAR, true>(p, bh, t0, lc, store, piece_end, pt, sQ, sK, sKlo, sG, sItem,
+            ok &= sub_chunk_items<DK, PACKED, SCALAR, true>(p, static_cast<int>(rank), bh, t0, lc, store, piece_end, pt, sQ, sK, sKlo, sG, sItem,
                                       bars, n, gt0, gt1, [] {});
             if (pt < DK) {
                 // the chunk's clamped decay of channel pt, summed in token order
@@ -788,7 +817,7 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
             // ---- end of a FULL-pass piece: its decay, then the next piece
             if (pend) {
                 const int x = nx - 1;
-                ok &= mbar_wait_bounded(&bars[kBarXchg0 + (x & 1)], (x >> 1) & 1, p.status);
+                ok &= mbar_wait_bounded(&bars[kBarXchg0 + (x & 1)], (x >> 1) & 1, p.status, p.wait_ns);
                 if (pt < DK) gseg += __logf(sG[((n - 1) & 1) * DK + pt]);
                 pend = false;
             }
@@ -820,22 +849,22 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
     // ---- end of the item stream and of the load requests
     if (pend) {
         const int x = nx - 1;
-        ok &= mbar_wait_bounded(&bars[kBarXchg0 + (x & 1)], (x >> 1) & 1, p.status);
+        ok &= mbar_wait_bounded(&bars[kBarXchg0 + (x & 1)], (x >> 1) & 1, p.status, p.wait_ns);
         if (pt < DK) gseg += __logf(sG[((n - 1) & 1) * DK + pt]);
     }
     // the peer's verdict for a chunk prepared here but not used has to land
     // before this CTA may exit
-    if (prepped_last) ok &= mbar_wait_bounded(&bars[kBarVerd0 + (lc_last & 1)], (lc_last >> 1) & 1, p.status);
+    if (prepped_last) ok &= mbar_wait_bounded(&bars[kBarVerd0 + (lc_last & 1)], (lc_last >> 1) & 1, p.status, p.wait_ns);
     // the request mailbox holds one request: the end may be posted only once
     // the TMA thread has taken the last one (its A tile has landed)
-    if (spec) ok &= mbar_wait_bounded(&bars[kBarAFull], (lc_last + 1) & 1, p.status);
+    if (spec) ok &= mbar_wait_bounded(&bars[kBarAFull], (lc_last + 1) & 1, p.status, p.wait_ns);
     named_barrier(5, kPrepThreads);
     if (pt == 0) {
         // the count of chunks used, so that no V load waits for a tile never freed
         sReq[0] = ChunkReq{used, 0, 1, 0};
         mbar_arrive(&bars[kBarReq]);
     }
-    if (n > 0 && !mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status)) ok = false;
+    if (n > 0 && !mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status, p.wait_ns)) ok = false;
     if (pt == 0) sItem[n & 1] = ItemInfo{0, 0, 0, kItemEnd, 0, -1, 0, 0};
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars[kBarQkFull]);
@@ -960,7 +989,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             // ---- phase A (needs only the A tile, which arrives early): the
             // local prefix sum of this thread's part, written in place of A.
             constexpr int kB = 8;
-            bool okw = mbar_wait_bounded(&bars[kBarAFull], lc & 1, p.status);
+            bool okw = mbar_wait_bounded(&bars[kBarAFull], lc & 1, p.status, p.wait_ns);
             ok = !bar_or(4, kPrepThreads, !okw);   // one verdict for all prep threads
             if (!ok) break;
             float c0 = 0.f, c1 = 0.f;
@@ -1019,7 +1048,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             const bool bad = bar_or(2, kPrepThreads,
                                     fmaxf(-fminf(gmin, 0.f), fmaxf(gmax, 0.f)) > kExpBound2 ||
                                         p.force_sub != 0);
-            okw = mbar_wait_bounded(&bars[kBarQkRaw], lc & 1, p.status);
+            okw = mbar_wait_bounded(&bars[kBarQkRaw], lc & 1, p.status, p.wait_ns);
             ok = !bar_or(4, kPrepThreads, !okw);
             if (!ok) break;
             if (!bad) {
@@ -1066,6 +1095,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                     for (int e = 0; e < kB; ++e) {
                         const int i = i0 + e;
                         const float g0 = o0 + ca[e].x, g1 = o1 + ca[e].y;
+                        if (p.dbg_gamma != nullptr && dv_tile == 0)
+                            dbg_gamma_pair<PACKED>(p, bh, t0 + i, ch, g0, g1, DK);
                         const float2 qf = unpack_bf16x2(cq[e]), kf = unpack_bf16x2(ck[e]);
                         const uint32_t off = sw128_offset(i, ch, kBlk);
                         *reinterpret_cast<uint32_t *>(sQ + off) =
@@ -1077,6 +1108,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                     }
                 }
                 if (pt == 0) {
+                    if (p.dbg_blk != nullptr && dv_tile == 0) p.dbg_blk[seq_of<PACKED>(p, bh).a + c] = kChunk;
                     sItem[n & 1] = ItemInfo{t0, 0, kChunk,
                                             kItemLast | (store ? kItemStore : 0) | piece_end, lc,
                                             -1, bh, 0};
@@ -1089,7 +1121,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             }
             // ---- sub-chunk rescaling (chunks whose decay exceeds the bound)
             float gtot0 = 0.f, gtot1 = 0.f;
-            ok = sub_chunk_items<DK, PACKED, SCALAR, false>(p, bh, t0, lc, store, piece_end, pt, sQ, sK, sKlo, sG, sItem,
+            ok = sub_chunk_items<DK, PACKED, SCALAR, false>(p, dv_tile == 0 ? -1 : -2, bh, t0, lc, store, piece_end, pt, sQ, sK, sKlo, sG, sItem,
                                      bars, n, gtot0, gtot1, [] {});
             if (last_part) {
                 gseg0 += gtot0;
@@ -1109,7 +1141,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             sReq[0] = ChunkReq{0, n, 1, 0};
             mbar_arrive(&bars[kBarReq]);
         }
-        if (n > 0 && !mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status)) ok = false;
+        if (n > 0 && !mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status, p.wait_ns)) ok = false;
         if (pt == 0) sItem[n & 1] = ItemInfo{0, 0, 0, kItemEnd, 0, -1, 0, 0};
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kBarQkFull]);
@@ -1122,6 +1154,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
         // its slot (also the output staging tile with two slots) is free.
         if (lane == 0) {
             int n_req = 0, n_qk = 0, n_v = 0;   // chunks requested / Q,K issued / V issued
+            int withheld = -1;                  // the V tile a test withholds, if any
             int n_use = 0;                      // chunks used (known at the end request)
             bool req_end = false;
             // per requested chunk: tensor row and tensor head of its first token
@@ -1200,11 +1233,17 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                     const int t0 = t0s[n_v & 3], bh = bhs[n_v & 3];
                     const int slot = n_v % VS;
                     uint8_t *dst = sV + slot * L::kVBytes;
-                    mbar_arrive_expect_tx(&bars[kBarVFull0 + slot], L::kVBytes);
+                    if (p.mode == kModeFull && n_v + 1 == p.withhold_v) {
+                        // test instrumentation: this tile is never loaded (and
+                        // its barrier never armed), so its waiters time out
+                        withheld = n_v;
+                    } else {
+                        mbar_arrive_expect_tx(&bars[kBarVFull0 + slot], L::kVBytes);
 #pragma unroll
-                    for (int nb = 0; nb < DVT / 64; ++nb)
-                        tma_load_3d(dst + nb * kBlk, &p.tm_v, &bars[kBarVFull0 + slot], dv0 + nb * 64,
-                                    t0, bh);
+                        for (int nb = 0; nb < DVT / 64; ++nb)
+                            tma_load_3d(dst + nb * kBlk, &p.tm_v, &bars[kBarVFull0 + slot],
+                                        dv0 + nb * 64, t0, bh);
+                    }
                     ++n_v;
                     progress = true;
                 }
@@ -1215,7 +1254,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                     const unsigned long long now = global_timer_ns();
                     if (idle_since == 0) {
                         idle_since = now;
-                    } else if (now - idle_since > kWaitLimitNs) {
+                    } else if (now - idle_since > p.wait_ns) {
                         atomicOr(p.status, kStatusTimeout);
                         break;
                     }
@@ -1225,11 +1264,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             // loads issued for chunks that were never used must land before exit
             // (the last phase of each barrier; no later phase follows)
             if (n_req > 0) {
-                mbar_wait_bounded(&bars[kBarAFull], (n_req - 1) & 1, p.status);
-                if (PAIR) mbar_wait_bounded(&bars[kBarQkRaw], (n_req - 1) & 1, p.status);
+                mbar_wait_bounded(&bars[kBarAFull], (n_req - 1) & 1, p.status, p.wait_ns);
+                if (PAIR) mbar_wait_bounded(&bars[kBarQkRaw], (n_req - 1) & 1, p.status, p.wait_ns);
             }
             for (int j = n_v - VS < 0 ? 0 : n_v - VS; j < n_v; ++j)
-                mbar_wait_bounded(&bars[kBarVFull0 + j % VS], (j / VS) & 1, p.status);
+                if (j != withheld)
+                    mbar_wait_bounded(&bars[kBarVFull0 + j % VS], (j / VS) & 1, p.status, p.wait_ns);
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
@@ -1241,7 +1281,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aKlo = smem_u32(sKlo);
             const uint32_t aV0 = smem_u32(sV), aS = smem_u32(sS);
             for (int n = 0;; ++n) {
-                if (!mbar_wait_bounded(&bars[kBarQkFull], n & 1, p.status)) break;
+                if (!mbar_wait_bounded(&bars[kBarQkFull], n & 1, p.status, p.wait_ns)) break;
                 const ItemInfo it = sItem[n & 1];
                 mbar_arrive(&bars[kBarItem0 + (n & 1)]);
                 if (it.flags & kItemEnd) break;
@@ -1264,7 +1304,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                 };
                 // a CTA pair's item: the peer's half of the operand tiles first
                 if (PAIR && it.xi >= 0) {
-                    if (!mbar_wait_bounded(&bars[kBarXchg0 + (it.xi & 1)], (it.xi >> 1) & 1, p.status))
+                    if (!mbar_wait_bounded(&bars[kBarXchg0 + (it.xi & 1)], (it.xi >> 1) & 1, p.status, p.wait_ns))
                         break;
                     tc_fence_after();
                 }
@@ -1274,8 +1314,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                 // O = Qh S_prev: needs this O buffer drained and the previous
                 // state scaled and copied
                 bool okw = true;
-                if (n >= 2) okw &= mbar_wait_bounded(&bars[kBarOFree0 + ob], ((n >> 1) + 1) & 1, p.status);
-                okw &= mbar_wait_bounded(&bars[kBarSReady], n & 1, p.status);
+                if (n >= 2) okw &= mbar_wait_bounded(&bars[kBarOFree0 + ob], ((n >> 1) + 1) & 1, p.status, p.wait_ns);
+                okw &= mbar_wait_bounded(&bars[kBarSReady], n & 1, p.status, p.wait_ns);
                 if (!okw) break;
                 tc_fence_after();
 #pragma unroll
@@ -1285,7 +1325,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                                 sw128_desc(aS + ks * 2048, L::kSBlk, 1024), id_ov, ks > 0);
                 }
                 // S += (Kh_hi + Kh_lo)^T V
-                if (!mbar_wait_bounded(&bars[kBarVFull0 + it.lc % VS], (it.lc / VS) & 1, p.status))
+                if (!mbar_wait_bounded(&bars[kBarVFull0 + it.lc % VS], (it.lc / VS) & 1, p.status, p.wait_ns))
                     break;
                 tc_fence_after();
 #pragma unroll
@@ -1301,7 +1341,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                 else
                     mma_commit(&bars[kBarQkEmpty]);
                 // O += (P_hi + P_lo) V, P from TMEM
-                if (!mbar_wait_bounded(&bars[kBarPSplit], n & 1, p.status)) break;
+                if (!mbar_wait_bounded(&bars[kBarPSplit], n & 1, p.status, p.wait_ns)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < kChunk / 16; ++ks) {
@@ -1312,6 +1352,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                 }
                 mma_commit(&bars[kBarOFull0 + ob]);
             }
+            // every product issued here is complete before TMEM is freed (a
+            // stream that ended on an expired wait may leave some in flight)
+            mma_commit(&bars[kBarDrain]);
+            mbar_wait_bounded(&bars[kBarDrain], 0, p.status, p.wait_ns);
         }
         __syncwarp();
     } else {
@@ -1433,14 +1477,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             // (one barrier per item parity, so that the MMA issuer may run up
             // to two items ahead of these warps)
             if (!__all_sync(0xffffffffu,
-                            mbar_wait_bounded(&bars[kBarItem0 + (n & 1)], (n >> 1) & 1, p.status)))
+                            mbar_wait_bounded(&bars[kBarItem0 + (n & 1)], (n >> 1) & 1, p.status, p.wait_ns)))
                 break;
             const ItemInfo it = sItem[n & 1];
             if (it.flags & kItemEnd) break;
             const int ob = n & 1;
             // ---- causal mask of P (row i), split into the TMEM A operand of P V
             {
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarPFull], n & 1, p.status)))
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarPFull], n & 1, p.status, p.wait_ns)))
                     break;
                 tc_fence_after();
                 // This warp's rows are 32 wq .. 32 wq + 31: column blocks past
@@ -1494,12 +1538,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             const bool piece_end = (it.flags & kItemPieceEnd) != 0;
             const bool keep = (it.flags & kItemKeep) != 0;
             auto state_step = [&]() -> bool {
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarSDone], n & 1, p.status)))
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarSDone], n & 1, p.status, p.wait_ns)))
                     return false;
                 // a CTA pair's item: the peer's half of the state factors
                 if (it.xi >= 0 &&
                     !__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarXchg0 + (it.xi & 1)],
-                                                               (it.xi >> 1) & 1, p.status)))
+                                                               (it.xi >> 1) & 1, p.status, p.wait_ns)))
                     return false;
                 tc_fence_after();
                 if (has_state_row) {
@@ -1548,7 +1592,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             };
             auto output_step = [&]() -> bool {
                 if (!__all_sync(0xffffffffu,
-                                mbar_wait_bounded(&bars[kBarOFull0 + ob], (n >> 1) & 1, p.status)))
+                                mbar_wait_bounded(&bars[kBarOFull0 + ob], (n >> 1) & 1, p.status, p.wait_ns)))
                     return false;
                 tc_fence_after();
                 // staged in the state copy: the V tile is free now
@@ -1692,6 +1736,10 @@ int launch_tiles(const ChunkLaunch &c, cudaStream_t stream) {
     p.force_sub = c.force_exact;
     p.status = c.status;
     p.fuse = c.fuse;
+    p.wait_ns = c.wait_ns ? c.wait_ns : kWaitLimitNs;
+    p.dbg_gamma = c.dbg_gamma;
+    p.dbg_blk = c.dbg_blk;
+    p.withhold_v = c.withhold_v;
     const int n_dvt = c.dv / DVT;
     // `count` CTAs (clusters) per tile column; the index is blockIdx.y +
     // blockIdx.z * gridDim.y, so that any count fits the grid's limits

@@ -44,6 +44,11 @@ struct ChunkLaunch {
     // kernel forms hT (no correction pass)
     int fuse;
     unsigned int *status;     // device status word
+    // test instrumentation (gla_chunk_fwd_debug; zero / null otherwise)
+    unsigned long long wait_ns;   // bounded-wait limit (0 = the default, 2 s)
+    float *dbg_gamma;         // [rows, dk] in-chunk prefix sums the preparation used, or null
+    int *dbg_blk;             // block length of every chunk (global chunk index), or null
+    int withhold_v;           // n > 0: each FULL-pass CTA withholds its n-th value tile
 };
 
 // Returns a cudaError_t value (0 on success).
@@ -64,10 +69,12 @@ int chunk_fwd_max_resident(int dk, int dv_tile, int pair);
 // allocated (`scratch_bytes` bytes of device memory, 16-byte aligned; may be
 // null when the plan needs none).  Returns a GLA status; GLA_ERR_SCRATCH when
 // the launch plan needs more scratch than given.
+// `dbg`: test instrumentation (gla_chunk_fwd_debug), or null.
 int chunk_fwd_with_scratch(const void *q, const void *k, const void *v, const float *log_alpha,
                            float scale, const float *h0, void *o, float *hT, int B, int H, int T,
                            int dk, int dv, const gla_chunk_options *opts, cudaStream_t stream,
-                           void *scratch, size_t scratch_bytes);
+                           void *scratch, size_t scratch_bytes,
+                           const gla_chunk_debug *dbg = nullptr);
 
 // The chunked forward over a packed variable-length batch (see
 // gla_chunk_fwd_varlen_ex).  Returns a GLA status.

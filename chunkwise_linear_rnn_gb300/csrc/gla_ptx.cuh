@@ -85,16 +85,18 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
 }
 
 // Wait for the phase with the given parity to complete.  Returns false (and
-// raises the timeout bit in *status) if it did not within kWaitLimitNs.
-// Waiting threads sleep in the barrier unit rather than spin, leaving issue
-// slots to the warps that share their scheduler.
+// raises the timeout bit in *status) if it did not within limit_ns
+// (kWaitLimitNs unless a test shortens it).  Waiting threads sleep in the
+// barrier unit rather than spin, leaving issue slots to the warps that share
+// their scheduler.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
-                                                  unsigned int *status) {
+                                                  unsigned int *status,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_timer_ns();
     while (true) {
         if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
+        if (global_timer_ns() - t0 > limit_ns) {
             atomicOr(status, kStatusTimeout);
             return false;
         }

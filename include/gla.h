@@ -169,6 +169,47 @@ int gla_chunk_fwd_plan(int B, int H, int T, int dk, int dv, const gla_chunk_opti
                        int *n_segments, int *dv_tile, int *launches, unsigned long *scratch_bytes);
 
 /*
+ * gla_chunk_fwd_debug — gla_chunk_fwd_ex with test instrumentation.  Not for
+ * production use: the library's own tests call it to look inside the chunked
+ * forward.  With dbg == NULL, or every field zero, it is gla_chunk_fwd_ex.
+ *
+ *   gamma         : nullable, device [B, H, T, dk] fp32, written: for every
+ *                   token and key channel, the in-chunk prefix sum of
+ *                   log_alpha that the preparation rescaled Q and K with (the
+ *                   GLA page's "Cumulative Decay Representation"), in
+ *                   natural-log units, relative to the reference of the
+ *                   token's block: the chunk start when the chunk is one
+ *                   block, else the start of its rescaled sub-chunk, whose
+ *                   gates are clamped to [-30, 30].
+ *   block_len     : nullable, device [B * H * ceil(T / 128)] int32, written:
+ *                   the block length each chunk was processed with (128: one
+ *                   block; less: the rescaled sub-chunk length).  Index
+ *                   (b * H + h) * ceil(T / 128) + chunk.
+ *   wait_limit_us : 0 = the production limit of every bounded device wait
+ *                   (2 s); else that limit in microseconds.
+ *   withhold_v    : 0 = off; n > 0: in the first launch every CTA's loader
+ *                   never loads, nor announces, the value tile of the n-th
+ *                   chunk it serves, so that the waits for it expire.  This
+ *                   makes a timeout on purpose with no copy or product in
+ *                   flight on the withheld barrier: the waiting threads give
+ *                   up, the CTA frees its TMEM and returns.  The call returns
+ *                   GLA_OK (it was enqueued); gla_last_device_status then
+ *                   reports GLA_ERR_TIMEOUT, and the outputs are undefined.
+ *
+ * Returns as gla_chunk_fwd_ex, and GLA_ERR_ARG for a negative withhold_v.
+ */
+typedef struct gla_chunk_debug {
+    float *gamma;
+    int *block_len;
+    unsigned int wait_limit_us;
+    int withhold_v;
+} gla_chunk_debug;
+int gla_chunk_fwd_debug(const void *q, const void *k, const void *v, const float *log_alpha,
+                        float scale, const float *h0, void *o, float *hT, int B, int H, int T,
+                        int dk, int dv, const gla_chunk_options *opts, const gla_chunk_debug *dbg,
+                        cudaStream_t stream);
+
+/*
  * gla_chunk_fwd_noalloc — gla_chunk_fwd_ex that allocates no device memory.
  *
  * The pages describe no counterpart: this is a service to callers that cannot
