@@ -667,6 +667,14 @@ def gdn_flops(cfg) -> int:
     return 6 * cfg.B * cfg.H * cfg.T * cfg.dk * cfg.dv
 
 
+def gdn_chunk_flops(cfg, C: int = 64) -> int:
+    """Tensor-core flops of the chunk algorithm (chunk C), per token: K K^T, W = T(beta gamma K)
+    and Q K^T (2 C dk each), U = T(beta V) and P D (2 C dv each), W S, Q S and K~^T D
+    (2 dk dv each)."""
+    return cfg.B * cfg.H * cfg.T * (3 * 2 * C * cfg.dk + 2 * 2 * C * cfg.dv
+                                    + 3 * 2 * cfg.dk * cfg.dv)
+
+
 def gdn_bytes(cfg) -> int:
     """q, k, v, o in bf16; g, beta in fp32; h0 and hT in fp32."""
     tok = cfg.B * cfg.H * cfg.T
@@ -674,15 +682,17 @@ def gdn_bytes(cfg) -> int:
 
 
 def gdn_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_kind):
-    """The gated delta rule forward (gla_gdn_fwd, token-recurrent) on the workload's shape."""
+    """The gated delta rule forward on the workload's shape: by chunks on the tensor cores
+    (gla_gdn_chunk_fwd, dk = 128) unless --gdn-impl token, or dk != 128 (gla_gdn_fwd)."""
     import torch
     from synth import make_gdn_inputs
     stream = torch.cuda.current_stream(dev)
+    chunked = args.gdn_impl == "chunk" and cfg.dk == 128
     q, k, v, g, b, h0 = make_gdn_inputs(cfg.B, cfg.H, cfg.T, cfg.dk, cfg.dv, sigma_h0=0.1,
                                         seed=rank, device=dev)
 
     def step():
-        return gla.gla_gdn_fwd(q, k, v, g, b, cfg.scale, h0)
+        return gla.gla_gdn_fwd(q, k, v, g, b, cfg.scale, h0, chunked=chunked)
 
     for _ in range(args.warmup):
         step()
@@ -716,7 +726,7 @@ def gdn_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_ki
         def e2e_step():
             for hsrc, dst in zip(host_in, dev_in):
                 dst.copy_(hsrc, non_blocking=True)
-            res = gla.gla_gdn_fwd(*dev_in[:5], cfg.scale, dev_in[5])
+            res = gla.gla_gdn_fwd(*dev_in[:5], cfg.scale, dev_in[5], chunked=chunked)
             for src, hdst in zip(res, host_out):
                 hdst.copy_(src, non_blocking=True)
 
@@ -735,7 +745,8 @@ def gdn_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_ki
         e2e = {"value": tokens_all / (e2e_ms / 1e3), "unit": "tokens/s",
                "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in host_in)),
                "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in host_out)),
-               "ms_per_step": e2e_ms, "api": "gla_gdn_fwd with pinned-host copies"}
+               "ms_per_step": e2e_ms,
+               "api": ("gla_gdn_chunk_fwd" if chunked else "gla_gdn_fwd") + " with pinned-host copies"}
         del host_in, dev_in, host_out, outs
     del q, k, v, g, b, h0
     torch.cuda.empty_cache()
@@ -748,7 +759,12 @@ def gdn_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_ki
         "config": {"workload": cfg.name + "-gated-delta-rule", "B": cfg.B, "H": cfg.H,
                    "T": cfg.T, "dk": cfg.dk, "dv": cfg.dv, "replicas": world,
                    "l2": "inputs (%.2f GB) larger than L2; no flush" % (byts / 1e9)},
-        "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_SIMT_TFLOPS,
+        "roofline": (roofline(byts, gdn_chunk_flops(cfg), per_call_ms / 1e3, pk, pk_kind) | {
+            "traffic": None, "traffic_unit": "DRAM bytes per call",
+            "kernel": "gdn_wy_kernel + gdn_seq_kernel (chunked, two launches)",
+            "note": "algorithmic bytes count the contract's inputs and outputs once; the WY "
+                    "pre-pass scratch (W, U) is extra traffic"}) if chunked else
+        {"bound": "alu", "achieved": achieved, "peak": FP32_SIMT_TFLOPS,
                      "unit": "TFLOP/s", "frac": achieved / FP32_SIMT_TFLOPS,
                      "traffic": measured_gdn_traffic(cfg), "traffic_unit": "DRAM bytes per launch",
                      "peak_kind": "derived: 152 SMs x 128 fp32 FMA lanes x 2 x 2070 MHz",
@@ -757,7 +773,7 @@ def gdn_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_ki
                      "hbm_gbs": byts / (per_call_ms / 1e3) / 1e9,
                      "hbm_frac": byts / (per_call_ms / 1e3) / 1e9 / pk["hbm_gbs"],
                      "hbm_peak_kind": pk_kind},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (2 if chunked else 1),
         "clocks": clk.summary(),
     }
     if e2e is not None:
@@ -985,6 +1001,9 @@ def main():
     ap.add_argument("--batch", type=int, default=0, help="override the workload's B")
     ap.add_argument("--heads", type=int, default=0, help="override the workload's H")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--gdn-impl", default="chunk", choices=["chunk", "token"],
+                    help="gated delta rule leg: the chunk algorithm on the tensor cores "
+                         "(gla_gdn_chunk_fwd, dk = 128) or the token recurrence (gla_gdn_fwd)")
     ap.add_argument("--gate", default="channel", choices=["channel", "head"],
                     help="log_alpha per key channel [B,H,T,dk] (the workloads') or per head "
                          "[B,H,T] (no e2e leg)")

@@ -418,11 +418,13 @@ def gla_chunk_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alph
 
 def gla_gdn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
                 beta: torch.Tensor, scale: float | None = None, h0: torch.Tensor | None = None,
-                output_final_state: bool = True):
+                output_final_state: bool = True, chunked: bool = False):
     """Gated delta rule (Gated DeltaNet) forward: ``(o, hT)``.
 
     q, k ``[B,H,T,dk]`` bf16 (k as given: normalise it first); v ``[B,H,T,dv]``
     bf16; g (log alpha) and beta ``[B,H,T]`` fp32; h0 ``[B,H,dk,dv]`` fp32 or None.
+    ``chunked=True`` calls gla_gdn_chunk_fwd (the chunk algorithm on the tensor
+    cores, dk = 128), else gla_gdn_fwd (token-recurrent).
     """
     if q.dim() != 4:
         raise ValueError("q must be [B, H, T, dk]")
@@ -443,12 +445,11 @@ def gla_gdn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tens
     o = torch.empty(B, H, T, dv, dtype=torch.bfloat16, device=dev)
     hT = torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev) if output_final_state else None
     with torch.cuda.device(dev):
-        st = _lib.lib().gla_gdn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(),
-                                    beta.data_ptr(), float(scale),
-                                    None if h0 is None else h0.data_ptr(), o.data_ptr(),
-                                    None if hT is None else hT.data_ptr(), B, H, T, dk, dv,
-                                    _stream(dev))
-    _lib.check(st, "gla_gdn_fwd")
+        fn = _lib.lib().gla_gdn_chunk_fwd if chunked else _lib.lib().gla_gdn_fwd
+        st = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(), beta.data_ptr(),
+                float(scale), None if h0 is None else h0.data_ptr(), o.data_ptr(),
+                None if hT is None else hT.data_ptr(), B, H, T, dk, dv, _stream(dev))
+    _lib.check(st, "gla_gdn_chunk_fwd" if chunked else "gla_gdn_fwd")
     return o, hT
 
 

@@ -28,7 +28,7 @@ EXPORTED = ("gla_chunk_fwd", "gla_chunk_fwd_ex", "gla_chunk_fwd_plan", "gla_chun
             "gla_chunk_fwd_host", "gla_chunk_fwd_varlen", "gla_chunk_fwd_varlen_ex",
             "gla_chunk_fwd_varlen_plan", "gla_chunk_bwd", "gla_chunk_bwd_ex",
             "gla_chunk_bwd_plan", "gla_chunk_bwd_varlen", "gla_chunk_bwd_varlen_ex",
-            "gla_gdn_fwd", "gla_recurrent_step", "gla_status_string",
+            "gla_gdn_fwd", "gla_gdn_chunk_fwd", "gla_recurrent_step", "gla_status_string",
             "gla_last_device_status", "gla_version")
 
 
@@ -96,6 +96,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.gla_chunk_bwd_plan.restype = i
     lib.gla_gdn_fwd.argtypes = [vp, vp, vp, fp, fp, f, fp, vp, fp, i, i, i, i, i, vp]
     lib.gla_gdn_fwd.restype = i
+    lib.gla_gdn_chunk_fwd.argtypes = [vp, vp, vp, fp, fp, f, fp, vp, fp, i, i, i, i, i, vp]
+    lib.gla_gdn_chunk_fwd.restype = i
     lib.gla_recurrent_step.argtypes = [vp, vp, vp, fp, f, fp, vp, i, i, i, i, vp]
     lib.gla_recurrent_step.restype = i
     lib.gla_status_string.argtypes = [i]

@@ -881,6 +881,51 @@ int gla_chunk_bwd_varlen(const void *q, const void *k, const void *v, const floa
                                    nullptr, stream);
 }
 
+int gla_gdn_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
+                      const float *beta, float scale, const float *h0, void *o, float *hT, int B,
+                      int H, int T, int dk, int dv, cudaStream_t stream) {
+    using namespace gla;
+    if (!q || !k || !v || !g || !beta || !o) return GLA_ERR_ARG;
+    if (B <= 0 || H <= 0 || T <= 0) return GLA_ERR_ARG;
+    if (dk != 128 || !dv_ok(dv)) return GLA_ERR_SHAPE;
+    if (static_cast<long long>(B) * H > 65535) return GLA_ERR_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+        (hT && !aligned16(hT)) || (reinterpret_cast<uintptr_t>(g) & 3u) ||
+        (reinterpret_cast<uintptr_t>(beta) & 3u) || (h0 && (reinterpret_cast<uintptr_t>(h0) & 3u)))
+        return GLA_ERR_ARG;
+    DeviceInfo *dev = nullptr;
+    const int st = current_device(&dev);
+    if (st != GLA_OK) return st;
+    const long long BH = static_cast<long long>(B) * H;
+    const size_t bytes = gdn_chunk_scratch_bytes(BH, T, dk);
+    void *ws = nullptr;
+    if (cudaMallocAsync(&ws, bytes, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return GLA_ERR_ALLOC;
+    }
+    const size_t rows = static_cast<size_t>(BH) * ((T + 63) / 64) * 64;
+    GdnChunkLaunch p = {};
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.g = g;
+    p.beta = beta;
+    p.scale = scale;
+    p.h0 = h0;
+    p.o = o;
+    p.hT = hT;
+    p.BH = static_cast<int>(BH);
+    p.T = T;
+    p.dk = dk;
+    p.dv = dv;
+    p.W = static_cast<__nv_bfloat16 *>(ws);
+    p.Tm = reinterpret_cast<__nv_bfloat16 *>(static_cast<char *>(ws) + rows * dk * 2);
+    p.status = dev->status;
+    const int r = launch_gdn_chunk(p, stream);
+    cudaFreeAsync(ws, stream);
+    return r == 0 ? GLA_OK : GLA_ERR_LAUNCH;
+}
+
 int gla_last_device_status(cudaStream_t stream) {
     using namespace gla;
     DeviceInfo *dev = nullptr;

@@ -1,0 +1,609 @@
+// gla_gdn_chunk.cu — the gated delta rule (Gated DeltaNet) forward by chunks on
+// the tensor cores: the four-step chunk algorithm of "Qwen Team Releases
+// FlashQLA for High-Performance Linear Attention" (todayforai.com), "Core
+// Technical Principles", in the standard gated-delta-rule reading
+//     S_t = alpha_t (I - beta_t k_t^T k_t) S_{t-1} + beta_t k_t^T v_t,
+//     o_t = scale q_t S_t,
+// with chunks of C = 64 tokens, gamma_t the in-chunk product of the gates
+// (G = log2 gamma, prefix sums in log2 units) and the chunk's write errors D:
+//   1. T = (I + L)^-1, L strictly lower, L_ti = beta_t (gamma_t / gamma_i) k_t.k_i;
+//   2. W = T diag(beta gamma) K,  U = T diag(beta) V;
+//   3. S_C = gamma_C S_0 + (diag(gamma_C / gamma) K)^T D,  D = U - W S_0;
+//   4. O = scale (diag(gamma) Q S_0 + tril(Q K^T gamma_t / gamma_i) D).
+//
+// Two kernels, split as the page splits its operators (an inversion operator,
+// then one fused operator for the rest):
+//   gdn_wy_kernel   one CTA per (chunk, head), two CTAs per SM: step 1 and W.
+//                   K K^T on the tensor cores; the unit lower triangular
+//                   inverse by 16 x 16 blocks (the four diagonal blocks by
+//                   substitution, one column per thread, then the
+//                   off-diagonal blocks level by level as small products);
+//                   T (bf16) and W = T diag(beta gamma) K (bf16) to scratch,
+//                   2 dk + 128 bytes per token.
+//   gdn_seq_kernel  one CTA per (head, 64-column value tile), chunks in order,
+//                   the state's 128 key rows in the registers of warps 0-3
+//                   (one row per thread): U = T (beta V) for the tile and
+//                   steps 3-4 as tensor-core products W S, Q S, Q K^T, U, then
+//                   P D and K~^T D (K~ = K gamma_C/gamma).
+//
+// Precision: bf16 operands with fp32 accumulation; the products whose operand
+// rounding would enter every later state (beta K, beta V, S in Q S, P, D, K~)
+// use bf16 hi/lo pairs (16 significant bits); T and W S stay single bf16
+// (their error enters through D once per chunk).  o is rounded once to bf16;
+// the state and hT are fp32.
+//
+// Every mbarrier wait is bounded (the library's limit); an expired wait sets
+// the status word and the CTA stops at the next chunk boundary.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "gla.h"
+#include "gla_internal.h"
+#include "gla_ptx.cuh"
+
+namespace gla {
+namespace {
+
+constexpr int C = 64;             // tokens per chunk
+constexpr int NT = 256;           // threads per CTA (both kernels)
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ void split_pair(float x, float y, uint32_t &hi, uint32_t &lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x - hf.x, y - hf.y);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float x, float y) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// Inclusive prefix sum of one chunk's log-gates in log2 units (rows past n
+// are zero, so the sum stays flat there) and the chunk's beta; warp 0.
+__device__ __forceinline__ void chunk_gates(float *sG, float *sB, const float *g, const float *beta,
+                                            size_t r0, int n) {
+    if (threadIdx.x < 32) {
+        const int l = threadIdx.x;
+        float a = l < n ? g[r0 + l] * kLog2e : 0.f, b = l + 32 < n ? g[r0 + l + 32] * kLog2e : 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float ya = __shfl_up_sync(0xffffffffu, a, o), yb = __shfl_up_sync(0xffffffffu, b, o);
+            if (l >= o) { a += ya; b += yb; }
+        }
+        b += __shfl_sync(0xffffffffu, a, 31);
+        sG[l] = a;
+        sG[l + 32] = b;
+        sB[l] = l < n ? beta[r0 + l] : 0.f;
+        sB[l + 32] = l + 32 < n ? beta[r0 + l + 32] : 0.f;
+    }
+}
+
+// ------------------------------------------------------------------ WY pre-pass
+template <int DK>
+struct WySmem {
+    static constexpr uint32_t kBlk = C * 128;                    // 64 rows x 64 bf16
+    static constexpr uint32_t kK = 0;                            // K [t][c] K-major, DK/64 blocks
+    static constexpr uint32_t kBKh = kK + (DK / 64) * kBlk;      // beta 2^G K [i][c] MN-major
+    static constexpr uint32_t kBKl = kBKh + (DK / 64) * kBlk;
+    static constexpr uint32_t kT = kBKl + (DK / 64) * kBlk;      // T [t][i] K-major, bf16
+    static constexpr uint32_t kL = kT + kBlk;                    // fp32 [64][65]: L, then T
+    static constexpr uint32_t kTf = kL + C * 65 * 4;
+    static constexpr uint32_t kX = kTf + C * 65 * 4;             // blocked inverse scratch [3][16][17]
+    static constexpr uint32_t kG = kX + 3 * 16 * 17 * 4;
+    static constexpr uint32_t kBeta = kG + C * 4;
+    static constexpr uint32_t kBar = kBeta + C * 4;
+    static constexpr uint32_t kSlot = kBar + 16;
+    static constexpr uint32_t kBytes = kSlot + 16 + 1024;
+    static_assert(kBytes <= 113 * 1024, "two CTAs per SM");
+};
+
+
+// T = (I + L)^-1 for strictly lower L (64 x 64, row stride 65), by blocks of
+// 16: the four diagonal blocks by substitution (threads 0-63, one column
+// each), then level by level T_ba = -T_bb sum_{m=a}^{b-1} L_bm T_ma, one
+// thread per element of a 16 x 16 block.  Needs NT == 256.
+__device__ __forceinline__ void invert_unit_lower_blocked(const float *sL, float *sTf, float *sX) {
+    static_assert(NT == 256, "one thread per element of a 16 x 16 block");
+    const int tid = threadIdx.x;
+    for (int e = tid; e < C * 65; e += NT) sTf[e] = 0.f;
+    __syncthreads();
+    if (tid < C) {
+        const int o = (tid >> 4) * 16, j = tid & 15;
+        for (int i = j; i < 16; ++i) {
+            float acc = 0.f;
+            for (int m = j; m < i; ++m) acc = fmaf(sL[(o + i) * 65 + o + m], sTf[(o + m) * 65 + o + j], acc);
+            sTf[(o + i) * 65 + o + j] = i == j ? 1.f : -acc;
+        }
+    }
+    __syncthreads();
+    const int r = tid >> 4, c = tid & 15;
+    for (int lev = 1; lev < 4; ++lev) {
+        for (int a = 0; a + lev < 4; ++a) {
+            const int b = a + lev;
+            float acc = 0.f;
+            for (int m = a * 16; m < b * 16; ++m) acc = fmaf(sL[(b * 16 + r) * 65 + m], sTf[m * 65 + a * 16 + c], acc);
+            sX[a * 272 + r * 17 + c] = acc;
+        }
+        __syncthreads();
+        for (int a = 0; a + lev < 4; ++a) {
+            const int b = a + lev;
+            float acc = 0.f;
+            for (int m = 0; m < 16; ++m) acc = fmaf(sTf[(b * 16 + r) * 65 + b * 16 + m], sX[a * 272 + m * 17 + c], acc);
+            sTf[(b * 16 + r) * 65 + a * 16 + c] = -acc;
+        }
+        __syncthreads();
+    }
+}
+
+// Grid (chunks per head, B*H).  W: [BH][nch*C][DK] bf16, U: [BH][nch*C][DV] fp32.
+template <int DK>
+__global__ void __launch_bounds__(NT, 2) gdn_wy_kernel(
+    const __nv_bfloat16 *__restrict__ k, const float *__restrict__ g,
+    const float *__restrict__ beta, __nv_bfloat16 *__restrict__ Wout,
+    __nv_bfloat16 *__restrict__ Tout, int T, unsigned int *status) {
+    using L = WySmem<DK>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    float *sL = reinterpret_cast<float *>(sm + L::kL), *sTf = reinterpret_cast<float *>(sm + L::kTf);
+    float *sG = reinterpret_cast<float *>(sm + L::kG), *sB = reinterpret_cast<float *>(sm + L::kBeta);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::kBar);
+    uint32_t *slot = reinterpret_cast<uint32_t *>(sm + L::kSlot);
+    const int u = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nch = (T + C - 1) / C, t0 = u * C, n = min(C, T - t0);
+    const size_t rg = static_cast<size_t>(bh) * T + t0;
+    const size_t rk = rg * DK;
+    const size_t orow = (static_cast<size_t>(bh) * nch + u) * C;   // first scratch row
+
+    if (warp == 0) tmem_alloc(slot, 256);
+    if (tid == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        fence_mbar_init();
+    }
+    chunk_gates(sG, sB, g, beta, rg, n);
+    // K as bf16 [t][c] K-major (exact input)
+    constexpr int KPER = C * DK / 8 / NT;
+    uint4 kraw[KPER];
+#pragma unroll
+    for (int m = 0; m < KPER; ++m) {
+        const int e = tid + m * NT, t = e / (DK / 8), c = (e % (DK / 8)) * 8;
+        kraw[m] = t < n ? *reinterpret_cast<const uint4 *>(k + rk + static_cast<size_t>(t) * DK + c)
+                        : make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4 *>(sm + L::kK + sw128_offset(t, c, L::kBlk)) = kraw[m];
+    }
+    __syncthreads();   // sG, sB
+    // beta 2^G K as a hi/lo pair, [i][c] (rows = tokens = K of the product)
+#pragma unroll
+    for (int m = 0; m < KPER; ++m) {
+        const int e = tid + m * NT, t = e / (DK / 8), c = (e % (DK / 8)) * 8;
+        const float f = sB[t] * exp2f(sG[t]);
+        const uint32_t w[4] = {kraw[m].x, kraw[m].y, kraw[m].z, kraw[m].w};
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            split_pair(__uint_as_float(w[j] << 16) * f, __uint_as_float(w[j] & 0xffff0000u) * f, hi[j], lo[j]);
+        const uint32_t off = sw128_offset(t, c, L::kBlk);
+        *reinterpret_cast<uint4 *>(sm + L::kBKh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4 *>(sm + L::kBKl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *slot, a0 = smem_u32(sm);
+
+    // K K^T: M = 64 (t), N = 64 (i), K = DK; both operands K-major
+    if (tid == 0) {
+        constexpr uint32_t id = idesc_bf16(64, C, false, false);
+#pragma unroll
+        for (int kk = 0; kk < DK / 16; ++kk) {
+            const uint32_t o = (kk >> 2) * L::kBlk + (kk & 3) * 32;
+            const uint64_t d = sw128_desc(a0 + L::kK + o, 16, 1024);
+            mma_bf16_ss(tmem, d, d, id, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bar[0]);
+    }
+    bool ok = mbar_wait_bounded(&bar[0], 0, status);
+    tc_fence_after();
+    // L_ti = beta_t 2^(G_t - G_i) (k_t . k_i) for i < t; rows t = 16 q + lane (lanes 0-15)
+    if (warp < 4) {
+        const int t = 16 * warp + lane;
+        uint32_t r[32];
+#pragma unroll 1
+        for (int ib = 0; ib < C; ib += 32) {
+            tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + ib, r);
+            tmem_wait_ld();
+            if (lane < 16) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int i = ib + j;
+                    sL[t * 65 + i] = (ok && i < t) ? sB[t] * exp2f(sG[t] - sG[i]) * __uint_as_float(r[j]) : 0.f;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    invert_unit_lower_blocked(sL, sTf, reinterpret_cast<float *>(sm + L::kX));
+    // T as a single bf16 K-major tile [t][i], and row-major to the scratch
+    __nv_bfloat16 *tdst = Tout + orow * C;
+    for (int e = tid; e < C * C / 2; e += NT) {
+        const int t = e / (C / 2), i = (e % (C / 2)) * 2;
+        const uint32_t w = pack_bf16(sTf[t * 65 + i], sTf[t * 65 + i + 1]);
+        *reinterpret_cast<uint32_t *>(sm + L::kT + sw128_offset(t, i, L::kBlk)) = w;
+        if (ok) *reinterpret_cast<uint32_t *>(tdst + t * C + i) = w;
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // W = T (beta 2^G K): M = 64, N = DK, K = 64
+    if (tid == 0) {
+        constexpr uint32_t idw = idesc_bf16(64, DK, false, true);
+#pragma unroll
+        for (int kk = 0; kk < C / 16; ++kk) {
+            const uint64_t at = sw128_desc(a0 + L::kT + kk * 32, 16, 1024);
+            const uint32_t om = kk * 2048;
+            mma_bf16_ss(tmem + 64, at, sw128_desc(a0 + L::kBKh + om, L::kBlk, 1024), idw, kk > 0 ? 1u : 0u);
+            mma_bf16_ss(tmem + 64, at, sw128_desc(a0 + L::kBKl + om, L::kBlk, 1024), idw, 1u);
+        }
+        mma_commit(&bar[1]);
+    }
+    ok = mbar_wait_bounded(&bar[1], 0, status) && ok;
+    tc_fence_after();
+    // epilogue: warps 0-3 store W (bf16); row t = 16 q + lane
+    if (warp < 4) {
+        const int t = 16 * warp + lane;
+        const uint32_t lo_ = static_cast<uint32_t>(32 * warp) << 16;
+        uint32_t r[32];
+#pragma unroll 1
+        for (int cb = 0; cb < DK; cb += 32) {
+            tmem_ld32(tmem + lo_ + 64 + cb, r);
+            tmem_wait_ld();
+            if (lane < 16 && ok) {
+                __nv_bfloat16 *dst = Wout + (orow + t) * DK + cb;
+#pragma unroll
+                for (int j = 0; j < 32; j += 8)
+                    *reinterpret_cast<uint4 *>(dst + j) = make_uint4(
+                        pack_bf16(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
+                        pack_bf16(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])),
+                        pack_bf16(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5])),
+                        pack_bf16(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7])));
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+// ------------------------------------------------------------------ sequential chunk kernel
+struct SeqSmem {
+    static constexpr int DK = 128;
+    static constexpr uint32_t kBlk = C * 128;       // 64 rows x 64 bf16
+    static constexpr uint32_t kSBlk = DK * 128;     // 128 rows x 64 bf16
+    static constexpr uint32_t kQ = 0;               // Q [t][c] K-major (2 blocks)
+    static constexpr uint32_t kK = kQ + 2 * kBlk;   // K [i][c] K-major (B of Q K^T)
+    static constexpr uint32_t kW = kK + 2 * kBlk;   // W [t][c] K-major
+    static constexpr uint32_t kKth = kW + 2 * kBlk; // K~ [t][c], read MN-major (A of K~^T D)
+    static constexpr uint32_t kKtl = kKth + 2 * kBlk;
+    static constexpr uint32_t kSh = kKtl + 2 * kBlk;   // S [i][c] MN-major (B), hi and lo
+    static constexpr uint32_t kSl = kSh + kSBlk;
+    static constexpr uint32_t kPh = kSl + kSBlk;    // P [t][i] K-major, hi and lo
+    static constexpr uint32_t kPl = kPh + kBlk;
+    static constexpr uint32_t kDh = kPl + kBlk;     // D [t][c] MN-major (B), hi and lo
+    static constexpr uint32_t kDl = kDh + kBlk;
+    static constexpr uint32_t kT = kDl + kBlk;      // T [t][i] K-major (A of U = T beta V)
+    static constexpr uint32_t kBVh = kT + kBlk;     // beta V [i][c] MN-major (B), hi and lo
+    static constexpr uint32_t kBVl = kBVh + kBlk;
+    static constexpr uint32_t kG = kBVl + kBlk;
+    static constexpr uint32_t kBeta = kG + C * 4;
+    static constexpr uint32_t kBar = kBeta + C * 4;
+    static constexpr uint32_t kSlot = kBar + 16;
+    static constexpr uint32_t kBytes = kSlot + 16 + 1024;
+};
+
+// Grid (DV / 64, B*H); dk = 128.  W and T from gdn_wy_kernel.
+template <int DV>
+__global__ void __launch_bounds__(NT, 1) gdn_seq_kernel(
+    const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+    const __nv_bfloat16 *__restrict__ v, const float *__restrict__ g,
+    const float *__restrict__ beta, const __nv_bfloat16 *__restrict__ W,
+    const __nv_bfloat16 *__restrict__ Tg, float scale,
+    const float *__restrict__ h0, __nv_bfloat16 *__restrict__ o, float *__restrict__ hT, int T,
+    unsigned int *status) {
+    using L = SeqSmem;
+    constexpr int DK = L::DK;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    float *sG = reinterpret_cast<float *>(sm + L::kG), *sB = reinterpret_cast<float *>(sm + L::kBeta);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::kBar);
+    uint32_t *slot = reinterpret_cast<uint32_t *>(sm + L::kSlot);
+    const int c0 = blockIdx.x * 64, bh = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nch = (T + C - 1) / C;
+    const int q4 = warp & 3;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
+
+    if (warp == 0) tmem_alloc(slot, 512);
+    if (tid == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        fence_mbar_init();
+    }
+    // warps 0-3: thread = key row i, the 64 columns of this tile
+    float S[64];
+    const int i_row = tid;   // meaningful for tid < 128
+    if (warp < 4) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+            S[c] = h0 ? h0[(static_cast<size_t>(bh) * DK + i_row) * DV + c0 + c] : 0.f;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *slot, a0 = smem_u32(sm);
+    bool ok = true;
+
+#pragma unroll 1
+    for (int u = 0; u < nch; ++u) {
+        const int t0 = u * C, n = min(C, T - t0);
+        const size_t rg = static_cast<size_t>(bh) * T + t0;
+        const size_t orow = (static_cast<size_t>(bh) * nch + u) * C;
+        chunk_gates(sG, sB, g, beta, rg, n);
+        __syncthreads();   // sG
+        const float GC = sG[C - 1];
+        // Q, K, W as bf16 tiles; K~ = K 2^(G_C - G_t) as a hi/lo pair
+        constexpr int PER = C * DK / 8 / NT;
+#pragma unroll
+        for (int m = 0; m < PER; ++m) {
+            const int e = tid + m * NT, t = e / (DK / 8), c = (e % (DK / 8)) * 8;
+            const size_t off = (rg + t) * DK + c;
+            const uint4 zq = make_uint4(0u, 0u, 0u, 0u);
+            const uint4 rq = t < n ? *reinterpret_cast<const uint4 *>(q + off) : zq;
+            const uint4 rk = t < n ? *reinterpret_cast<const uint4 *>(k + off) : zq;
+            const uint4 rw = *reinterpret_cast<const uint4 *>(W + (orow + t) * DK + c);
+            const uint32_t so = sw128_offset(t, c, L::kBlk);
+            *reinterpret_cast<uint4 *>(sm + L::kQ + so) = rq;
+            *reinterpret_cast<uint4 *>(sm + L::kK + so) = rk;
+            *reinterpret_cast<uint4 *>(sm + L::kW + so) = rw;
+            const float f = exp2f(GC - sG[t]);
+            const uint32_t w4[4] = {rk.x, rk.y, rk.z, rk.w};
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                split_pair(__uint_as_float(w4[j] << 16) * f, __uint_as_float(w4[j] & 0xffff0000u) * f, hi[j], lo[j]);
+            *reinterpret_cast<uint4 *>(sm + L::kKth + so) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4 *>(sm + L::kKtl + so) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+        // T (bf16, K-major [t][i]) and beta V of this tile's 64 columns as a hi/lo pair
+        {
+            const int e = tid, t = e / 8 + 32 * 0, i8 = (e % 8) * 8;
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                const int tt = t + 32 * m;
+                const uint4 w = *reinterpret_cast<const uint4 *>(Tg + (orow + tt) * C + i8);
+                *reinterpret_cast<uint4 *>(sm + L::kT + sw128_offset(tt, i8, L::kBlk)) = w;
+                const uint4 zv = make_uint4(0u, 0u, 0u, 0u);
+                const uint4 rv = tt < n ? *reinterpret_cast<const uint4 *>(v + (rg + tt) * DV + c0 + i8) : zv;
+                const float fb = sB[tt];
+                const uint32_t w4[4] = {rv.x, rv.y, rv.z, rv.w};
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    split_pair(__uint_as_float(w4[j] << 16) * fb, __uint_as_float(w4[j] & 0xffff0000u) * fb, hi[j], lo[j]);
+                const uint32_t so = sw128_offset(tt, i8, L::kBlk);
+                *reinterpret_cast<uint4 *>(sm + L::kBVh + so) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4 *>(sm + L::kBVl + so) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+        }
+        // the state entering the chunk, as a hi/lo pair [i][c]
+        if (warp < 4) {
+#pragma unroll
+            for (int c = 0; c < 64; c += 8) {
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) split_pair(S[c + 2 * j], S[c + 2 * j + 1], hi[j], lo[j]);
+                const uint32_t so = sw128_offset(i_row, c, L::kSBlk);
+                *reinterpret_cast<uint4 *>(sm + L::kSh + so) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4 *>(sm + L::kSl + so) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        // group A: W S (TMEM 0), Q S (64), Q K^T (128); M = 64 tokens, K = 128 channels
+        if (tid == 0) {
+            constexpr uint32_t id_s = idesc_bf16(64, 64, false, true);    // A [t][c] K-major, S [c][j] MN-major
+            constexpr uint32_t id_p = idesc_bf16(64, C, false, false);    // Q [t][c], K [i][c]
+#pragma unroll
+            for (int kk = 0; kk < DK / 16; ++kk) {
+                const uint32_t ok_ = (kk >> 2) * L::kBlk + (kk & 3) * 32;
+                const uint32_t om = kk * 2048;
+                const uint64_t sh = sw128_desc(a0 + L::kSh + om, L::kSBlk, 1024);
+                const uint64_t sl = sw128_desc(a0 + L::kSl + om, L::kSBlk, 1024);
+                const uint64_t aq = sw128_desc(a0 + L::kQ + ok_, 16, 1024);
+                mma_bf16_ss(tmem, sw128_desc(a0 + L::kW + ok_, 16, 1024), sh, id_s, kk > 0 ? 1u : 0u);
+                mma_bf16_ss(tmem + 64, aq, sh, id_s, kk > 0 ? 1u : 0u);
+                mma_bf16_ss(tmem + 64, aq, sl, id_s, 1u);
+                mma_bf16_ss(tmem + 128, aq, sw128_desc(a0 + L::kK + ok_, 16, 1024), id_p, kk > 0 ? 1u : 0u);
+            }
+            // U = T (beta V): M = 64 tokens, N = 64 columns, K = 64 tokens
+            constexpr uint32_t id_u = idesc_bf16(64, 64, false, true);
+#pragma unroll
+            for (int kk = 0; kk < C / 16; ++kk) {
+                const uint64_t at = sw128_desc(a0 + L::kT + kk * 32, 16, 1024);
+                const uint32_t om = kk * 2048;
+                mma_bf16_ss(tmem + 320, at, sw128_desc(a0 + L::kBVh + om, L::kBlk, 1024), id_u,
+                            kk > 0 ? 1u : 0u);
+                mma_bf16_ss(tmem + 320, at, sw128_desc(a0 + L::kBVl + om, L::kBlk, 1024), id_u, 1u);
+            }
+            mma_commit(&bar[0]);
+        }
+        ok = mbar_wait_bounded(&bar[0], u & 1, status) && ok;
+        tc_fence_after();
+        // epilogue A: warps 4-7 form D = U - W S (rows t = 16 q4 + lane, lanes 0-15),
+        // warps 0-3 form P = tril(Q K^T 2^(G_t - G_i)); both as hi/lo pairs
+        {
+            const int t = 16 * q4 + lane;
+            uint32_t r[32];
+#pragma unroll 1
+            for (int cb = 0; cb < 64; cb += 32) {
+                uint32_t ru[32];
+                tmem_ld32(tmem + lane_off + (warp < 4 ? 128 : 0) + cb, r);
+                if (warp >= 4) tmem_ld32(tmem + lane_off + 320 + cb, ru);
+                tmem_wait_ld();
+                if (lane < 16) {
+                    if (warp >= 4) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 8) {
+                            float d[8];
+#pragma unroll
+                            for (int x = 0; x < 8; ++x)
+                                d[x] = __uint_as_float(ru[j + x]) - __uint_as_float(r[j + x]);
+                            uint32_t hi[4], lo[4];
+#pragma unroll
+                            for (int x = 0; x < 4; ++x) split_pair(d[2 * x], d[2 * x + 1], hi[x], lo[x]);
+                            const uint32_t so = sw128_offset(t, cb + j, L::kBlk);
+                            *reinterpret_cast<uint4 *>(sm + L::kDh + so) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                            *reinterpret_cast<uint4 *>(sm + L::kDl + so) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                        }
+                    } else {
+                        const float Gt = sG[t];
+#pragma unroll
+                        for (int j = 0; j < 32; j += 2) {
+                            const int i = cb + j;
+                            const float x0 = i <= t ? __uint_as_float(r[j]) * exp2f(Gt - sG[i]) : 0.f;
+                            const float x1 = i + 1 <= t ? __uint_as_float(r[j + 1]) * exp2f(Gt - sG[i + 1]) : 0.f;
+                            uint32_t hi, lo;
+                            split_pair(x0, x1, hi, lo);
+                            const uint32_t so = sw128_offset(t, i, L::kBlk);
+                            *reinterpret_cast<uint32_t *>(sm + L::kPh + so) = hi;
+                            *reinterpret_cast<uint32_t *>(sm + L::kPl + so) = lo;
+                        }
+                    }
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        // group B: P D (TMEM 192; M = 64, K = 64 tokens) and K~^T D (TMEM 256; M = 128 channels)
+        if (tid == 0) {
+            constexpr uint32_t id_pd = idesc_bf16(64, 64, false, true);   // P [t][i] K-major, D [i][c] MN-major
+            constexpr uint32_t id_kd = idesc_bf16(128, 64, true, true);   // K~ [i][c] MN-major, D [i][c] MN-major
+#pragma unroll
+            for (int kk = 0; kk < C / 16; ++kk) {
+                const uint32_t om = kk * 2048;
+                const uint64_t dh = sw128_desc(a0 + L::kDh + om, L::kBlk, 1024);
+                const uint64_t dl = sw128_desc(a0 + L::kDl + om, L::kBlk, 1024);
+                const uint64_t ph = sw128_desc(a0 + L::kPh + kk * 32, 16, 1024);
+                const uint64_t pl = sw128_desc(a0 + L::kPl + kk * 32, 16, 1024);
+                mma_bf16_ss(tmem + 192, ph, dh, id_pd, kk > 0 ? 1u : 0u);
+                mma_bf16_ss(tmem + 192, pl, dh, id_pd, 1u);
+                mma_bf16_ss(tmem + 192, ph, dl, id_pd, 1u);
+                const uint64_t kh = sw128_desc(a0 + L::kKth + om, L::kBlk, 1024);
+                const uint64_t kl = sw128_desc(a0 + L::kKtl + om, L::kBlk, 1024);
+                mma_bf16_ss(tmem + 256, kh, dh, id_kd, kk > 0 ? 1u : 0u);
+                mma_bf16_ss(tmem + 256, kl, dh, id_kd, 1u);
+                mma_bf16_ss(tmem + 256, kh, dl, id_kd, 1u);
+            }
+            mma_commit(&bar[1]);
+        }
+        ok = mbar_wait_bounded(&bar[1], u & 1, status) && ok;
+        tc_fence_after();
+        // epilogue B: warps 4-7 write o_t = scale (2^G_t QS_t + PD_t);
+        // warps 0-3 update their state rows S_i = 2^G_C S_i + (K~^T D)_i
+        if (warp >= 4) {
+            const int t = 16 * q4 + lane;
+            const float f = lane < 16 ? exp2f(sG[t]) : 0.f;
+            uint32_t a[32], b[32];
+#pragma unroll 1
+            for (int cb = 0; cb < 64; cb += 32) {
+                tmem_ld32(tmem + lane_off + 64 + cb, a);
+                tmem_ld32(tmem + lane_off + 192 + cb, b);
+                tmem_wait_ld();
+                if (lane < 16 && t < n && ok) {
+                    __nv_bfloat16 *dst = o + (rg + t) * DV + c0 + cb;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 8) {
+                        float x[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            x[e] = scale * fmaf(f, __uint_as_float(a[j + e]), __uint_as_float(b[j + e]));
+                        *reinterpret_cast<uint4 *>(dst + j) =
+                            make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]),
+                                       pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+                    }
+                }
+            }
+        } else {
+            const float fc = exp2f(GC);
+            uint32_t r[32];
+#pragma unroll
+            for (int cb = 0; cb < 64; cb += 32) {
+                tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 256 + cb, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) S[cb + j] = fmaf(fc, S[cb + j], __uint_as_float(r[j]));
+            }
+        }
+        tc_fence_before();
+        ok = __syncthreads_and(ok) != 0;   // one verdict for the whole CTA; also ends the chunk
+        tc_fence_after();
+        if (!ok) break;
+    }
+    if (warp < 4 && hT && ok) {
+#pragma unroll
+        for (int c = 0; c < 64; c += 4)
+            *reinterpret_cast<float4 *>(hT + (static_cast<size_t>(bh) * DK + i_row) * DV + c0 + c) =
+                make_float4(S[c], S[c + 1], S[c + 2], S[c + 3]);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// ------------------------------------------------------------------ launch
+template <int DV>
+int launch_dv(const GdnChunkLaunch &p, cudaStream_t stream) {
+    static bool attr_set = false;   // per instantiation, per process
+    const int s1 = static_cast<int>(WySmem<128>::kBytes);
+    const int s2 = static_cast<int>(SeqSmem::kBytes);
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(gdn_wy_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 s1) != cudaSuccess ||
+            cudaFuncSetAttribute(gdn_seq_kernel<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 s2) != cudaSuccess)
+            return static_cast<int>(cudaGetLastError());
+        attr_set = true;
+    }
+    const int nch = (p.T + C - 1) / C;
+    const dim3 g1(static_cast<unsigned>(nch), static_cast<unsigned>(p.BH));
+    const dim3 g2(DV / 64, static_cast<unsigned>(p.BH));
+    const auto *qb = static_cast<const __nv_bfloat16 *>(p.q);
+    const auto *kb = static_cast<const __nv_bfloat16 *>(p.k);
+    const auto *vb = static_cast<const __nv_bfloat16 *>(p.v);
+    gdn_wy_kernel<128><<<g1, NT, s1, stream>>>(kb, p.g, p.beta, p.W, p.Tm, p.T, p.status);
+    gdn_seq_kernel<DV><<<g2, NT, s2, stream>>>(qb, kb, vb, p.g, p.beta, p.W, p.Tm, p.scale, p.h0,
+                                               static_cast<__nv_bfloat16 *>(p.o), p.hT, p.T,
+                                               p.status);
+    return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace
+
+int launch_gdn_chunk(const GdnChunkLaunch &p, cudaStream_t stream) {
+    if (p.dv == 64) return launch_dv<64>(p, stream);
+    if (p.dv == 128) return launch_dv<128>(p, stream);
+    return launch_dv<256>(p, stream);
+}
+
+}  // namespace gla

@@ -135,4 +135,29 @@ int launch_gate_sum(const float *full, float *g, long long rows, int dk, cudaStr
 // Enqueues the six backward kernels; returns a cudaError_t value.
 int launch_chunk_bwd(const BwdLaunch &p, cudaStream_t stream);
 
+// The gated delta rule forward by chunks (gla_gdn_chunk.cu): dk = 128.
+struct GdnChunkLaunch {
+    const void *q, *k, *v;         // bf16 [BH, T, dk] / [BH, T, dv]
+    const float *g, *beta;         // fp32 [BH, T]
+    float scale;
+    const float *h0;               // [BH, dk, dv] or null (zero state)
+    void *o;                       // bf16 [BH, T, dv]
+    float *hT;                     // [BH, dk, dv] or null
+    int BH, T, dk, dv;
+    // scratch of the pre-pass, rows = BH * ceil(T / 64) * 64:
+    // W bf16 [rows, dk] and the chunks' inverses T bf16 [rows, 64]
+    __nv_bfloat16 *W;
+    __nv_bfloat16 *Tm;
+    unsigned int *status;          // device status word (bounded waits)
+};
+
+// Bytes of pre-pass scratch for these sizes (W and T).
+inline size_t gdn_chunk_scratch_bytes(long long BH, int T, int dk) {
+    const long long rows = BH * ((T + 63) / 64) * 64;
+    return static_cast<size_t>(rows) * (static_cast<size_t>(dk) * 2 + 64 * 2);
+}
+
+// Enqueues the WY pre-pass and the sequential chunk kernel; returns a cudaError_t value.
+int launch_gdn_chunk(const GdnChunkLaunch &p, cudaStream_t stream);
+
 }  // namespace gla

@@ -1,4 +1,5 @@
-"""GPU parity of gla_gdn_fwd (the gated delta rule, token-recurrent) against the fp64 oracle.
+"""GPU parity of gla_gdn_fwd (the gated delta rule, token-recurrent) and gla_gdn_chunk_fwd
+(the same rule by chunks on the tensor cores) against the fp64 oracle.
 
 The oracle walks the same recurrence in double on the exact bf16/fp32 input
 values; the CUDA path keeps each state column in fp32 registers split over
@@ -118,3 +119,64 @@ def test_long_workload_sampled_heads():
                              b[n, h].cpu().numpy(), dk ** -0.5, h0[n, h].double().cpu().numpy())
         assert_close(o[n, h].float().cpu().numpy(), ro, f"long ({n},{h}) o", bf16_output=True)
         assert_close(hT[n, h].cpu().numpy(), rhT, f"long ({n},{h}) hT")
+
+
+# ---- gla_gdn_chunk_fwd: the same recurrence by the four-step chunk algorithm on
+# the tensor cores (64-token chunks, dk = 128), against the same oracle.
+
+@pytest.mark.parametrize("dv", [64, 128, 256])
+@pytest.mark.parametrize("T", [1, 37, 63, 64, 65, 200, 1000])
+def test_chunked_matches_oracle(dv, T):
+    case = make_gdn_inputs(1, 3, T, 128, dv, sigma_h0=0.1, seed=T + dv)
+    _check(case, 128 ** -0.5, f"chunked T={T} dv={dv}", chunked=True)
+
+
+def test_chunked_without_states_and_with_several_batches():
+    q, k, v, g, b, _ = make_gdn_inputs(3, 2, 300, 128, 128, seed=21)
+    o, hT = _gpu(q, k, v, g, b, None, 0.1, output_final_state=False, chunked=True)
+    assert hT is None
+    ro, _ = _oracle(q, k, v, g, b, None, 0.1)
+    assert_close(o, ro, "chunked no h0 o", bf16_output=True)
+
+
+def test_chunked_strong_forgetting_full_writes_and_beta_zero():
+    q, k, v, g, b, h0 = make_gdn_inputs(1, 2, 260, 128, 256, tau=1.0, sigma_z=3.0, sigma_h0=1.0,
+                                        seed=23)
+    _check((q, k, v, g, b, h0), 128 ** -0.5, "chunked tau=1", chunked=True)
+    _check((q, k, v, g, torch.ones_like(b), h0), 128 ** -0.5, "chunked beta=1", chunked=True)
+    # beta = 0 on the default gates: the state only decays (the gates above would take it
+    # below the fp32 range within these 260 tokens)
+    q, k, v, g, b, h0 = make_gdn_inputs(1, 2, 260, 128, 128, sigma_h0=1.0, seed=24)
+    o, hT, ro, rhT = _check((q, k, v, g, torch.zeros_like(b), h0), 128 ** -0.5,
+                            "chunked beta=0", chunked=True)
+    decay = np.exp(g.double().numpy().sum(axis=-1))[..., None, None]
+    np.testing.assert_allclose(hT, decay * h0.double().numpy(), rtol=1e-4, atol=1e-7)
+
+
+def test_chunked_agrees_with_the_token_recurrent_kernel():
+    case = make_gdn_inputs(2, 2, 500, 128, 128, sigma_h0=0.1, seed=25)
+    o_c, h_c = _gpu(*case, 128 ** -0.5, chunked=True)
+    o_t, h_t = _gpu(*case, 128 ** -0.5)
+    assert_close(o_c, o_t.astype(np.float64), "chunked vs token o", bf16_output=True)
+    assert_close(h_c, h_t.astype(np.float64), "chunked vs token hT")
+
+
+def test_chunked_rejects_other_key_widths():
+    q, k, v, g, b, h0 = make_gdn_inputs(1, 1, 8, 64, 64, seed=0)
+    dev = lambda t: t.to(DEV)  # noqa: E731
+    with pytest.raises(Exception):
+        gla.gla_gdn_fwd(dev(q), dev(k), dev(v), dev(g), dev(b), chunked=True)
+
+
+def test_chunked_long_workload_sampled_heads():
+    B, H, T, dk, dv = 2, 16, 32768, 128, 256
+    q, k, v, g, b, h0 = make_gdn_inputs(B, H, T, dk, dv, sigma_h0=0.1, seed=7, device=DEV)
+    o, hT = gla.gla_gdn_fwd(q, k, v, g, b, dk ** -0.5, h0, chunked=True)
+    torch.cuda.synchronize()
+    for n, h in ((0, 0), (1, 13)):
+        ro, rhT = gd.forward(q[n, h].float().cpu().numpy(), k[n, h].float().cpu().numpy(),
+                             v[n, h].float().cpu().numpy(), g[n, h].cpu().numpy(),
+                             b[n, h].cpu().numpy(), dk ** -0.5, h0[n, h].double().cpu().numpy())
+        assert_close(o[n, h].float().cpu().numpy(), ro, f"chunked long ({n},{h}) o",
+                     bf16_output=True)
+        assert_close(hT[n, h].cpu().numpy(), rhT, f"chunked long ({n},{h}) hT")
