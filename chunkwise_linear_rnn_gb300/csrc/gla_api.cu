@@ -897,6 +897,8 @@ int gla_gdn_chunk_fwd(const void *q, const void *k, const void *v, const float *
     const int st = current_device(&dev);
     if (st != GLA_OK) return st;
     const long long BH = static_cast<long long>(B) * H;
+    // the scratch rows are addressed by 32-bit TMA coordinates
+    if (BH * ((T + 63) / 64) * 64 > 0x7fffffffLL) return GLA_ERR_ARG;
     const size_t bytes = gdn_chunk_scratch_bytes(BH, T, dk);
     void *ws = nullptr;
     if (cudaMallocAsync(&ws, bytes, stream) != cudaSuccess) {
@@ -921,7 +923,25 @@ int gla_gdn_chunk_fwd(const void *q, const void *k, const void *v, const float *
     p.W = static_cast<__nv_bfloat16 *>(ws);
     p.Tm = reinterpret_cast<__nv_bfloat16 *>(static_cast<char *>(ws) + rows * dk * 2);
     p.status = dev->status;
-    const int r = launch_gdn_chunk(p, stream);
+    EncodeTiledFn enc = nullptr;
+    int r = encode_fn(&enc);
+    if (r == GLA_OK &&
+        (!make_map(enc, &p.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dk, T, p.BH, 64, 64,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+         !make_map(enc, &p.tm_k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dk, T, p.BH, 64, 64,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+         !make_map(enc, &p.tm_v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dv, T, p.BH, 64, 64,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+         !make_map(enc, &p.tm_w, p.W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dk,
+                   static_cast<int>(rows), 1, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+         !make_map(enc, &p.tm_t, p.Tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64,
+                   static_cast<int>(rows), 1, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)))
+        r = GLA_ERR_LAUNCH;
+    if (r != GLA_OK) {
+        cudaFreeAsync(ws, stream);
+        return r;
+    }
+    r = launch_gdn_chunk(p, stream);
     cudaFreeAsync(ws, stream);
     return r == 0 ? GLA_OK : GLA_ERR_LAUNCH;
 }

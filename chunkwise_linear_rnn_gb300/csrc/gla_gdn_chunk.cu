@@ -301,28 +301,110 @@ struct SeqSmem {
     static constexpr uint32_t kT = kDl + kBlk;      // T [t][i] K-major (A of U = T beta V)
     static constexpr uint32_t kBVh = kT + kBlk;     // beta V [i][c] MN-major (B), hi and lo
     static constexpr uint32_t kBVl = kBVh + kBlk;
-    static constexpr uint32_t kG = kBVl + kBlk;
+    static constexpr uint32_t kVr = kBVl + kBlk;    // V of this tile as loaded, [t][c]
+    static constexpr uint32_t kG = kVr + kBlk;
     static constexpr uint32_t kBeta = kG + C * 4;
-    static constexpr uint32_t kBar = kBeta + C * 4;
-    static constexpr uint32_t kSlot = kBar + 16;
+    static constexpr uint32_t kE = kBeta + C * 4;   // 2^-G per token (the scores' column factors)
+    static constexpr uint32_t kBar = kE + C * 4;    // the kernel's mbarriers (SeqBar)
+    static constexpr uint32_t kSlot = kBar + 64;
     static constexpr uint32_t kBytes = kSlot + 16 + 1024;
+    static constexpr uint32_t kLoadBytes = 2 * kBlk * 3 + 2 * kBlk;   // Q, K, W; T, V
 };
 
-// Grid (DV / 64, B*H); dk = 128.  W and T from gdn_wy_kernel.
-template <int DV>
-__global__ void __launch_bounds__(NT, 1) gdn_seq_kernel(
-    const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
-    const __nv_bfloat16 *__restrict__ v, const float *__restrict__ g,
-    const float *__restrict__ beta, const __nv_bfloat16 *__restrict__ W,
-    const __nv_bfloat16 *__restrict__ Tg, float scale,
-    const float *__restrict__ h0, __nv_bfloat16 *__restrict__ o, float *__restrict__ hT, int T,
-    unsigned int *status) {
+// The sequential kernel's operands: tensor maps of q, k, v ([BH, T, .] as
+// (channel, token, head)), W ([rows, 128]) and T ([rows, 64]), 64 x 64 boxes
+// with the 128-byte swizzle; rows past T load as zeros.
+struct SeqParams {
+    CUtensorMap tm_q, tm_k, tm_v, tm_w, tm_t;
+    const float *g, *beta, *h0;
+    __nv_bfloat16 *o;
+    float *hT;
+    float scale;
+    int T;
+    unsigned int *status;
+};
+
+// One chunk's gates into registers (warp 0: lane l holds tokens l and l + 32;
+// rows past n read as zero).
+__device__ __forceinline__ void gates_load(const float *g, const float *beta, size_t r0, int n,
+                                           float (&gr)[4]) {
+    const int l = threadIdx.x & 31;
+    gr[0] = l < n ? g[r0 + l] : 0.f;
+    gr[1] = l + 32 < n ? g[r0 + l + 32] : 0.f;
+    gr[2] = l < n ? beta[r0 + l] : 0.f;
+    gr[3] = l + 32 < n ? beta[r0 + l + 32] : 0.f;
+}
+
+// Inclusive prefix sum (log2 units) of the loaded gates and the betas into the
+// shared tables; warp 0.
+__device__ __forceinline__ void gates_scan(const float (&gr)[4], float *sG, float *sB) {
+    const int l = threadIdx.x & 31;
+    float a = gr[0] * kLog2e, b = gr[1] * kLog2e;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float ya = __shfl_up_sync(0xffffffffu, a, o), yb = __shfl_up_sync(0xffffffffu, b, o);
+        if (l >= o) { a += ya; b += yb; }
+    }
+    b += __shfl_sync(0xffffffffu, a, 31);
+    sG[l] = a;
+    sG[l + 32] = b;
+    sB[l] = gr[2];
+    sB[l + 32] = gr[3];
+}
+
+// The TMA loads of chunk u of head bh: Q, K and W (two 64-channel blocks
+// each), T, and the tile's 64 columns of V; one thread.
+__device__ __forceinline__ void chunk_loads(const SeqParams &p, uint8_t *sm, uint64_t *bar, int u,
+                                            int bh, int c0, int nch) {
     using L = SeqSmem;
+    const int t0 = u * C;
+    const int orow = (bh * nch + u) * C;
+    fence_proxy_async_smem();   // the previous chunk's generic reads of these tiles are done
+    mbar_arrive_expect_tx(bar, L::kLoadBytes);
+#pragma unroll
+    for (int kb = 0; kb < 2; ++kb) {
+        tma_load_3d(sm + L::kQ + kb * L::kBlk, &p.tm_q, bar, kb * 64, t0, bh);
+        tma_load_3d(sm + L::kK + kb * L::kBlk, &p.tm_k, bar, kb * 64, t0, bh);
+        tma_load_3d(sm + L::kW + kb * L::kBlk, &p.tm_w, bar, kb * 64, orow, 0);
+    }
+    tma_load_3d(sm + L::kT, &p.tm_t, bar, 0, orow, 0);
+    tma_load_3d(sm + L::kVr, &p.tm_v, bar, c0, t0, bh);
+}
+
+// Grid (DV / 64, B*H); dk = 128.  W and T from gdn_wy_kernel.  288 threads:
+//   warps 0-3 "state": thread i holds key row i of the state (this tile's 64
+//     columns, fp32 registers); they write its bf16 hi/lo copy, form the
+//     masked scores P from Q K^T while the state chain runs, then apply the
+//     state update from K~^T D;
+//   warps 4-7 "token": the write errors D = U - W S, then the outputs;
+//   warp 8 "issue": lane 0 issues every product and the TMA loads; the warp
+//     loads the next chunk's gates.
+// Per chunk: U, W S (commit A1); Q K^T, Q S (commit A2); once A2 is done the
+// next chunk's Q, K, W, T and V load into the tiles it read; K~^T D once D is
+// written (commit B1); P D once P is written (commit B2).  Only the state
+// chain W S -> D -> K~^T D -> S is serial; the scores, P D and the outputs
+// run beside it.
+constexpr int NTS = 288;
+enum SeqBar { kSbA1 = 0, kSbA2, kSbB1, kSbB2, kSbD, kSbP, kSbLd, kSbDrain, kSbCount };
+static_assert(kSbCount * 8 <= 64, "mbarrier space of SeqSmem");
+
+template <int DV>
+__global__ void __launch_bounds__(NTS, 1) gdn_seq_kernel(const __grid_constant__ SeqParams p) {
+    using L = SeqSmem;
+    const float *__restrict__ g = p.g;
+    const float *__restrict__ beta = p.beta;
+    const float *__restrict__ h0 = p.h0;
+    __nv_bfloat16 *__restrict__ o = p.o;
+    float *__restrict__ hT = p.hT;
+    const float scale = p.scale;
+    const int T = p.T;
+    unsigned int *status = p.status;
     constexpr int DK = L::DK;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     float *sG = reinterpret_cast<float *>(sm + L::kG), *sB = reinterpret_cast<float *>(sm + L::kBeta);
+    float *sE = reinterpret_cast<float *>(sm + L::kE);
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::kBar);
     uint32_t *slot = reinterpret_cast<uint32_t *>(sm + L::kSlot);
     const int c0 = blockIdx.x * 64, bh = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -332,9 +414,13 @@ __global__ void __launch_bounds__(NT, 1) gdn_seq_kernel(
 
     if (warp == 0) tmem_alloc(slot, 512);
     if (tid == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
+        for (int i = 0; i < kSbCount; ++i) mbar_init(&bar[i], (i == kSbD || i == kSbP) ? 4u : 1u);
         fence_mbar_init();
+        prefetch_tensormap(&p.tm_q);
+        prefetch_tensormap(&p.tm_k);
+        prefetch_tensormap(&p.tm_v);
+        prefetch_tensormap(&p.tm_w);
+        prefetch_tensormap(&p.tm_t);
     }
     // warps 0-3: thread = key row i, the 64 columns of this tile
     float S[64];
@@ -349,184 +435,193 @@ __global__ void __launch_bounds__(NT, 1) gdn_seq_kernel(
     tc_fence_after();
     const uint32_t tmem = *slot, a0 = smem_u32(sm);
     bool ok = true;
+    // the state entering a chunk as a hi/lo pair [i][c] (the B operand of W S
+    // and Q S): written here for the first chunk, then by the state warps right
+    // after each update, once both products of the chunk have read it
+    auto state_copy = [&]() {
+#pragma unroll
+        for (int c = 0; c < 64; c += 8) {
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) split_pair(S[c + 2 * j], S[c + 2 * j + 1], hi[j], lo[j]);
+            const uint32_t so = sw128_offset(i_row, c, L::kSBlk);
+            *reinterpret_cast<uint4 *>(sm + L::kSh + so) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4 *>(sm + L::kSl + so) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+    };
+    if (warp < 4) state_copy();
+    float gr[4];   // warp 8: the next chunk's gates
+    int loads = 0;  // warp 8 lane 0: chunk loads issued
+    if (warp == 8) {
+        gates_load(g, beta, static_cast<size_t>(bh) * T, min(C, T), gr);
+        if (lane == 0) {
+            chunk_loads(p, sm, &bar[kSbLd], 0, bh, c0, nch);
+            loads = 1;
+        }
+    }
 
 #pragma unroll 1
     for (int u = 0; u < nch; ++u) {
         const int t0 = u * C, n = min(C, T - t0);
         const size_t rg = static_cast<size_t>(bh) * T + t0;
-        const size_t orow = (static_cast<size_t>(bh) * nch + u) * C;
-        chunk_gates(sG, sB, g, beta, rg, n);
-        __syncthreads();   // sG
+        const uint32_t ph = static_cast<uint32_t>(u & 1);
+        if (warp == 8) gates_scan(gr, sG, sB);
+        ok = mbar_wait_bounded(&bar[kSbLd], ph, status) && ok;   // this chunk's tiles
+        __syncthreads();   // sG, sB
         const float GC = sG[C - 1];
-        // Q, K, W as bf16 tiles; K~ = K 2^(G_C - G_t) as a hi/lo pair
-        constexpr int PER = C * DK / 8 / NT;
+        if (warp < 8) {
+            // K~ = K 2^(G_C - G_t) and beta V of this tile as hi/lo pairs, from
+            // the loaded tiles (same swizzled layout); warps 0-7
+            constexpr int PER = C * DK / 8 / 256;
 #pragma unroll
-        for (int m = 0; m < PER; ++m) {
-            const int e = tid + m * NT, t = e / (DK / 8), c = (e % (DK / 8)) * 8;
-            const size_t off = (rg + t) * DK + c;
-            const uint4 zq = make_uint4(0u, 0u, 0u, 0u);
-            const uint4 rq = t < n ? *reinterpret_cast<const uint4 *>(q + off) : zq;
-            const uint4 rk = t < n ? *reinterpret_cast<const uint4 *>(k + off) : zq;
-            const uint4 rw = *reinterpret_cast<const uint4 *>(W + (orow + t) * DK + c);
-            const uint32_t so = sw128_offset(t, c, L::kBlk);
-            *reinterpret_cast<uint4 *>(sm + L::kQ + so) = rq;
-            *reinterpret_cast<uint4 *>(sm + L::kK + so) = rk;
-            *reinterpret_cast<uint4 *>(sm + L::kW + so) = rw;
-            const float f = exp2f(GC - sG[t]);
-            const uint32_t w4[4] = {rk.x, rk.y, rk.z, rk.w};
-            uint32_t hi[4], lo[4];
+            for (int m = 0; m < PER; ++m) {
+                const int e = tid + m * 256, t = e / (DK / 8), c = (e % (DK / 8)) * 8;
+                const uint32_t so = sw128_offset(t, c, L::kBlk);
+                const uint4 rk = *reinterpret_cast<const uint4 *>(sm + L::kK + so);
+                const float f = ex2f(GC - sG[t]);
+                const uint32_t w4[4] = {rk.x, rk.y, rk.z, rk.w};
+                uint32_t hi[4], lo[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                split_pair(__uint_as_float(w4[j] << 16) * f, __uint_as_float(w4[j] & 0xffff0000u) * f, hi[j], lo[j]);
-            *reinterpret_cast<uint4 *>(sm + L::kKth + so) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4 *>(sm + L::kKtl + so) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        }
-        // T (bf16, K-major [t][i]) and beta V of this tile's 64 columns as a hi/lo pair
-        {
-            const int e = tid, t = e / 8 + 32 * 0, i8 = (e % 8) * 8;
+                for (int j = 0; j < 4; ++j)
+                    split_pair(__uint_as_float(w4[j] << 16) * f, __uint_as_float(w4[j] & 0xffff0000u) * f, hi[j], lo[j]);
+                *reinterpret_cast<uint4 *>(sm + L::kKth + so) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4 *>(sm + L::kKtl + so) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
-                const int tt = t + 32 * m;
-                const uint4 w = *reinterpret_cast<const uint4 *>(Tg + (orow + tt) * C + i8);
-                *reinterpret_cast<uint4 *>(sm + L::kT + sw128_offset(tt, i8, L::kBlk)) = w;
-                const uint4 zv = make_uint4(0u, 0u, 0u, 0u);
-                const uint4 rv = tt < n ? *reinterpret_cast<const uint4 *>(v + (rg + tt) * DV + c0 + i8) : zv;
-                const float fb = sB[tt];
+                const int e = tid + m * 256, t = e / 8, c = (e % 8) * 8;
+                const uint32_t so = sw128_offset(t, c, L::kBlk);
+                const uint4 rv = *reinterpret_cast<const uint4 *>(sm + L::kVr + so);
+                const float fb = sB[t];
                 const uint32_t w4[4] = {rv.x, rv.y, rv.z, rv.w};
                 uint32_t hi[4], lo[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                     split_pair(__uint_as_float(w4[j] << 16) * fb, __uint_as_float(w4[j] & 0xffff0000u) * fb, hi[j], lo[j]);
-                const uint32_t so = sw128_offset(tt, i8, L::kBlk);
                 *reinterpret_cast<uint4 *>(sm + L::kBVh + so) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
                 *reinterpret_cast<uint4 *>(sm + L::kBVl + so) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
         }
-        // the state entering the chunk, as a hi/lo pair [i][c]
-        if (warp < 4) {
-#pragma unroll
-            for (int c = 0; c < 64; c += 8) {
-                uint32_t hi[4], lo[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) split_pair(S[c + 2 * j], S[c + 2 * j + 1], hi[j], lo[j]);
-                const uint32_t so = sw128_offset(i_row, c, L::kSBlk);
-                *reinterpret_cast<uint4 *>(sm + L::kSh + so) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4 *>(sm + L::kSl + so) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-            }
-        }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        // group A: W S (TMEM 0), Q S (64), Q K^T (128); M = 64 tokens, K = 128 channels
-        if (tid == 0) {
-            constexpr uint32_t id_s = idesc_bf16(64, 64, false, true);    // A [t][c] K-major, S [c][j] MN-major
-            constexpr uint32_t id_p = idesc_bf16(64, C, false, false);    // Q [t][c], K [i][c]
+        if (warp == 8) {
+            // ======================================================= issue warp
+            if (lane == 0) {
+                constexpr uint32_t id_s = idesc_bf16(64, 64, false, true);    // A [t][c] K-major, S [c][j] MN-major
+                constexpr uint32_t id_p = idesc_bf16(64, C, false, false);    // Q [t][c], K [i][c]
+                constexpr uint32_t id_u = idesc_bf16(64, 64, false, true);    // T [t][i], beta V [i][c]
+                // A1: U = T (beta V) (TMEM 320) and W S (TMEM 0), the state chain's first step
 #pragma unroll
-            for (int kk = 0; kk < DK / 16; ++kk) {
-                const uint32_t ok_ = (kk >> 2) * L::kBlk + (kk & 3) * 32;
-                const uint32_t om = kk * 2048;
-                const uint64_t sh = sw128_desc(a0 + L::kSh + om, L::kSBlk, 1024);
-                const uint64_t sl = sw128_desc(a0 + L::kSl + om, L::kSBlk, 1024);
-                const uint64_t aq = sw128_desc(a0 + L::kQ + ok_, 16, 1024);
-                mma_bf16_ss(tmem, sw128_desc(a0 + L::kW + ok_, 16, 1024), sh, id_s, kk > 0 ? 1u : 0u);
-                mma_bf16_ss(tmem + 64, aq, sh, id_s, kk > 0 ? 1u : 0u);
-                mma_bf16_ss(tmem + 64, aq, sl, id_s, 1u);
-                mma_bf16_ss(tmem + 128, aq, sw128_desc(a0 + L::kK + ok_, 16, 1024), id_p, kk > 0 ? 1u : 0u);
-            }
-            // U = T (beta V): M = 64 tokens, N = 64 columns, K = 64 tokens
-            constexpr uint32_t id_u = idesc_bf16(64, 64, false, true);
+                for (int kk = 0; kk < C / 16; ++kk) {
+                    const uint64_t at = sw128_desc(a0 + L::kT + kk * 32, 16, 1024);
+                    const uint32_t om = kk * 2048;
+                    mma_bf16_ss(tmem + 320, at, sw128_desc(a0 + L::kBVh + om, L::kBlk, 1024), id_u,
+                                kk > 0 ? 1u : 0u);
+                    mma_bf16_ss(tmem + 320, at, sw128_desc(a0 + L::kBVl + om, L::kBlk, 1024), id_u, 1u);
+                }
 #pragma unroll
-            for (int kk = 0; kk < C / 16; ++kk) {
-                const uint64_t at = sw128_desc(a0 + L::kT + kk * 32, 16, 1024);
-                const uint32_t om = kk * 2048;
-                mma_bf16_ss(tmem + 320, at, sw128_desc(a0 + L::kBVh + om, L::kBlk, 1024), id_u,
-                            kk > 0 ? 1u : 0u);
-                mma_bf16_ss(tmem + 320, at, sw128_desc(a0 + L::kBVl + om, L::kBlk, 1024), id_u, 1u);
+                for (int kk = 0; kk < DK / 16; ++kk) {
+                    const uint32_t ok_ = (kk >> 2) * L::kBlk + (kk & 3) * 32;
+                    mma_bf16_ss(tmem, sw128_desc(a0 + L::kW + ok_, 16, 1024),
+                                sw128_desc(a0 + L::kSh + kk * 2048, L::kSBlk, 1024), id_s,
+                                kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&bar[kSbA1]);
+                // A2: Q K^T (TMEM 128) and Q S (TMEM 64)
+#pragma unroll
+                for (int kk = 0; kk < DK / 16; ++kk) {
+                    const uint32_t ok_ = (kk >> 2) * L::kBlk + (kk & 3) * 32;
+                    const uint32_t om = kk * 2048;
+                    const uint64_t aq = sw128_desc(a0 + L::kQ + ok_, 16, 1024);
+                    mma_bf16_ss(tmem + 128, aq, sw128_desc(a0 + L::kK + ok_, 16, 1024), id_p,
+                                kk > 0 ? 1u : 0u);
+                    mma_bf16_ss(tmem + 64, aq, sw128_desc(a0 + L::kSh + om, L::kSBlk, 1024), id_s,
+                                kk > 0 ? 1u : 0u);
+                    mma_bf16_ss(tmem + 64, aq, sw128_desc(a0 + L::kSl + om, L::kSBlk, 1024), id_s, 1u);
+                }
+                mma_commit(&bar[kSbA2]);
+                // Q, K, W, T and V are read once A2 is done: the next chunk's
+                // operands load into them
+                ok = mbar_wait_bounded(&bar[kSbA2], ph, status) && ok;
+                if (u + 1 < nch) {
+                    chunk_loads(p, sm, &bar[kSbLd], u + 1, bh, c0, nch);
+                    loads = u + 2;
+                }
+                // B1: K~^T D (TMEM 256; M = 128 channels) once D is written
+                constexpr uint32_t id_kd = idesc_bf16(128, 64, true, true);   // K~ [i][c] MN-major, D [i][c] MN-major
+                ok = mbar_wait_bounded(&bar[kSbD], ph, status) && ok;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < C / 16; ++kk) {
+                    const uint32_t om = kk * 2048;
+                    const uint64_t dh = sw128_desc(a0 + L::kDh + om, L::kBlk, 1024);
+                    const uint64_t dl = sw128_desc(a0 + L::kDl + om, L::kBlk, 1024);
+                    const uint64_t kh = sw128_desc(a0 + L::kKth + om, L::kBlk, 1024);
+                    const uint64_t kl = sw128_desc(a0 + L::kKtl + om, L::kBlk, 1024);
+                    mma_bf16_ss(tmem + 256, kh, dh, id_kd, kk > 0 ? 1u : 0u);
+                    mma_bf16_ss(tmem + 256, kl, dh, id_kd, 1u);
+                    mma_bf16_ss(tmem + 256, kh, dl, id_kd, 1u);
+                }
+                mma_commit(&bar[kSbB1]);
+                // B2: P D (TMEM 192; M = 64, K = 64 tokens) once P is written
+                constexpr uint32_t id_pd = idesc_bf16(64, 64, false, true);   // P [t][i] K-major, D [i][c] MN-major
+                ok = mbar_wait_bounded(&bar[kSbP], ph, status) && ok;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < C / 16; ++kk) {
+                    const uint32_t om = kk * 2048;
+                    const uint64_t dh = sw128_desc(a0 + L::kDh + om, L::kBlk, 1024);
+                    const uint64_t dl = sw128_desc(a0 + L::kDl + om, L::kBlk, 1024);
+                    const uint64_t phd = sw128_desc(a0 + L::kPh + kk * 32, 16, 1024);
+                    const uint64_t pld = sw128_desc(a0 + L::kPl + kk * 32, 16, 1024);
+                    mma_bf16_ss(tmem + 192, phd, dh, id_pd, kk > 0 ? 1u : 0u);
+                    mma_bf16_ss(tmem + 192, pld, dh, id_pd, 1u);
+                    mma_bf16_ss(tmem + 192, phd, dl, id_pd, 1u);
+                }
+                mma_commit(&bar[kSbB2]);
             }
-            mma_commit(&bar[0]);
-        }
-        ok = mbar_wait_bounded(&bar[0], u & 1, status) && ok;
-        tc_fence_after();
-        // epilogue A: warps 4-7 form D = U - W S (rows t = 16 q4 + lane, lanes 0-15),
-        // warps 0-3 form P = tril(Q K^T 2^(G_t - G_i)); both as hi/lo pairs
-        {
-            const int t = 16 * q4 + lane;
-            uint32_t r[32];
+            __syncwarp();
+            if (u + 1 < nch) gates_load(g, beta, rg + C, min(C, T - t0 - C), gr);
+        } else if (warp >= 4) {
+            // ======================================================= token warps
+            const int t = 16 * q4 + lane;   // rows t in lanes 0-15 of each quarter (M = 64)
+            // D = U - W S as a hi/lo pair [t][c]
+            ok = mbar_wait_bounded(&bar[kSbA1], ph, status) && ok;
+            tc_fence_after();
 #pragma unroll 1
             for (int cb = 0; cb < 64; cb += 32) {
-                uint32_t ru[32];
-                tmem_ld32(tmem + lane_off + (warp < 4 ? 128 : 0) + cb, r);
-                if (warp >= 4) tmem_ld32(tmem + lane_off + 320 + cb, ru);
+                uint32_t r[32], ru[32];
+                tmem_ld32(tmem + lane_off + cb, r);
+                tmem_ld32(tmem + lane_off + 320 + cb, ru);
                 tmem_wait_ld();
                 if (lane < 16) {
-                    if (warp >= 4) {
 #pragma unroll
-                        for (int j = 0; j < 32; j += 8) {
-                            float d[8];
+                    for (int j = 0; j < 32; j += 8) {
+                        float d[8];
 #pragma unroll
-                            for (int x = 0; x < 8; ++x)
-                                d[x] = __uint_as_float(ru[j + x]) - __uint_as_float(r[j + x]);
-                            uint32_t hi[4], lo[4];
+                        for (int x = 0; x < 8; ++x) d[x] = __uint_as_float(ru[j + x]) - __uint_as_float(r[j + x]);
+                        uint32_t hi[4], lo[4];
 #pragma unroll
-                            for (int x = 0; x < 4; ++x) split_pair(d[2 * x], d[2 * x + 1], hi[x], lo[x]);
-                            const uint32_t so = sw128_offset(t, cb + j, L::kBlk);
-                            *reinterpret_cast<uint4 *>(sm + L::kDh + so) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                            *reinterpret_cast<uint4 *>(sm + L::kDl + so) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                        }
-                    } else {
-                        const float Gt = sG[t];
-#pragma unroll
-                        for (int j = 0; j < 32; j += 2) {
-                            const int i = cb + j;
-                            const float x0 = i <= t ? __uint_as_float(r[j]) * exp2f(Gt - sG[i]) : 0.f;
-                            const float x1 = i + 1 <= t ? __uint_as_float(r[j + 1]) * exp2f(Gt - sG[i + 1]) : 0.f;
-                            uint32_t hi, lo;
-                            split_pair(x0, x1, hi, lo);
-                            const uint32_t so = sw128_offset(t, i, L::kBlk);
-                            *reinterpret_cast<uint32_t *>(sm + L::kPh + so) = hi;
-                            *reinterpret_cast<uint32_t *>(sm + L::kPl + so) = lo;
-                        }
+                        for (int x = 0; x < 4; ++x) split_pair(d[2 * x], d[2 * x + 1], hi[x], lo[x]);
+                        const uint32_t so = sw128_offset(t, cb + j, L::kBlk);
+                        *reinterpret_cast<uint4 *>(sm + L::kDh + so) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                        *reinterpret_cast<uint4 *>(sm + L::kDl + so) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                     }
                 }
             }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        // group B: P D (TMEM 192; M = 64, K = 64 tokens) and K~^T D (TMEM 256; M = 128 channels)
-        if (tid == 0) {
-            constexpr uint32_t id_pd = idesc_bf16(64, 64, false, true);   // P [t][i] K-major, D [i][c] MN-major
-            constexpr uint32_t id_kd = idesc_bf16(128, 64, true, true);   // K~ [i][c] MN-major, D [i][c] MN-major
-#pragma unroll
-            for (int kk = 0; kk < C / 16; ++kk) {
-                const uint32_t om = kk * 2048;
-                const uint64_t dh = sw128_desc(a0 + L::kDh + om, L::kBlk, 1024);
-                const uint64_t dl = sw128_desc(a0 + L::kDl + om, L::kBlk, 1024);
-                const uint64_t ph = sw128_desc(a0 + L::kPh + kk * 32, 16, 1024);
-                const uint64_t pl = sw128_desc(a0 + L::kPl + kk * 32, 16, 1024);
-                mma_bf16_ss(tmem + 192, ph, dh, id_pd, kk > 0 ? 1u : 0u);
-                mma_bf16_ss(tmem + 192, pl, dh, id_pd, 1u);
-                mma_bf16_ss(tmem + 192, ph, dl, id_pd, 1u);
-                const uint64_t kh = sw128_desc(a0 + L::kKth + om, L::kBlk, 1024);
-                const uint64_t kl = sw128_desc(a0 + L::kKtl + om, L::kBlk, 1024);
-                mma_bf16_ss(tmem + 256, kh, dh, id_kd, kk > 0 ? 1u : 0u);
-                mma_bf16_ss(tmem + 256, kl, dh, id_kd, 1u);
-                mma_bf16_ss(tmem + 256, kh, dl, id_kd, 1u);
-            }
-            mma_commit(&bar[1]);
-        }
-        ok = mbar_wait_bounded(&bar[1], u & 1, status) && ok;
-        tc_fence_after();
-        // epilogue B: warps 4-7 write o_t = scale (2^G_t QS_t + PD_t);
-        // warps 0-3 update their state rows S_i = 2^G_C S_i + (K~^T D)_i
-        if (warp >= 4) {
-            const int t = 16 * q4 + lane;
-            const float f = lane < 16 ? exp2f(sG[t]) : 0.f;
-            uint32_t a[32], b[32];
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[kSbD]);
+            // o_t = scale (2^G_t QS_t + PD_t) once P D is done (Q S came before it)
+            ok = mbar_wait_bounded(&bar[kSbB2], ph, status) && ok;
+            tc_fence_after();
+            const float f = lane < 16 ? ex2f(sG[t]) : 0.f;
 #pragma unroll 1
             for (int cb = 0; cb < 64; cb += 32) {
+                uint32_t a[32], b[32];
                 tmem_ld32(tmem + lane_off + 64 + cb, a);
                 tmem_ld32(tmem + lane_off + 192 + cb, b);
                 tmem_wait_ld();
@@ -545,7 +640,64 @@ __global__ void __launch_bounds__(NT, 1) gdn_seq_kernel(
                 }
             }
         } else {
-            const float fc = exp2f(GC);
+            // ======================================================= state warps
+            // P = tril(Q K^T 2^(G_t - G_i)) as a hi/lo pair [t][i] (rows t in lanes
+            // 0-15 of each quarter), while the state chain runs
+            {
+                const int t = 16 * q4 + lane;
+                // 2^(G_t - G_i) = 2^G_t 2^-G_i: one exponential per row and a
+                // column table, while the chunk's total decay keeps 2^-G_i
+                // within 2^60 (G falls monotonically over the chunk); else one
+                // exponential per element
+                const bool split_exp = GC >= -60.f;
+                if (split_exp && lane < 16) sE[t] = ex2f(-sG[t]);   // (rows = columns here)
+                ok = mbar_wait_bounded(&bar[kSbA2], ph, status) && ok;
+                tc_fence_after();
+                named_barrier(1, 128);   // the column table of the state warps
+                const float Gt = lane < 16 ? sG[t] : 0.f;
+                const float et = ex2f(Gt);
+                // one 32-column block of scores: the decay factor of column i
+                // from the table or by its own exponential
+                // (eight consecutive columns of the row are one 16-byte piece of
+                // the swizzled tile: one store each for hi and lo)
+                auto p_block = [&](const uint32_t(&r)[32], int cb, auto factor) {
+#pragma unroll
+                    for (int j8 = 0; j8 < 32; j8 += 8) {
+                        uint32_t hi[4], lo[4];
+#pragma unroll
+                        for (int x = 0; x < 4; ++x) {
+                            const int i = cb + j8 + 2 * x;
+                            const float x0 = i <= t ? __uint_as_float(r[j8 + 2 * x]) * factor(i) : 0.f;
+                            const float x1 =
+                                i + 1 <= t ? __uint_as_float(r[j8 + 2 * x + 1]) * factor(i + 1) : 0.f;
+                            split_pair(x0, x1, hi[x], lo[x]);
+                        }
+                        const uint32_t so = sw128_offset(t, cb + j8, L::kBlk);
+                        *reinterpret_cast<uint4 *>(sm + L::kPh + so) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                        *reinterpret_cast<uint4 *>(sm + L::kPl + so) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    }
+                };
+#pragma unroll 1
+                for (int cb = 0; cb < 64; cb += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lane_off + 128 + cb, r);
+                    tmem_wait_ld();
+                    if (lane < 16) {
+                        if (split_exp)
+                            p_block(r, cb, [&](int i) { return et * sE[i]; });
+                        else
+                            p_block(r, cb, [&](int i) { return ex2f(Gt - sG[i]); });
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[kSbP]);
+            }
+            // S_i = 2^G_C S_i + (K~^T D)_i (lane = key row, M = 128)
+            ok = mbar_wait_bounded(&bar[kSbB1], ph, status) && ok;
+            tc_fence_after();
+            const float fc = ex2f(GC);
             uint32_t r[32];
 #pragma unroll
             for (int cb = 0; cb < 64; cb += 32) {
@@ -554,6 +706,8 @@ __global__ void __launch_bounds__(NT, 1) gdn_seq_kernel(
 #pragma unroll
                 for (int j = 0; j < 32; ++j) S[cb + j] = fmaf(fc, S[cb + j], __uint_as_float(r[j]));
             }
+            // W S and Q S (A1, A2) are done: the copy for the next chunk
+            if (u + 1 < nch) state_copy();
         }
         tc_fence_before();
         ok = __syncthreads_and(ok) != 0;   // one verdict for the whole CTA; also ends the chunk
@@ -565,6 +719,14 @@ __global__ void __launch_bounds__(NT, 1) gdn_seq_kernel(
         for (int c = 0; c < 64; c += 4)
             *reinterpret_cast<float4 *>(hT + (static_cast<size_t>(bh) * DK + i_row) * DV + c0 + c) =
                 make_float4(S[c], S[c + 1], S[c + 2], S[c + 3]);
+    }
+    // every product issued here completes, and every chunk load lands, before
+    // TMEM and shared memory are given up (a stream ended by an expired wait
+    // may leave some in flight)
+    if (warp == 8 && lane == 0) {
+        mma_commit(&bar[kSbDrain]);
+        mbar_wait_bounded(&bar[kSbDrain], 0, status);
+        if (loads > 0) mbar_wait_bounded(&bar[kSbLd], static_cast<uint32_t>((loads - 1) & 1), status);
     }
     tc_fence_before();
     __syncthreads();
@@ -588,13 +750,23 @@ int launch_dv(const GdnChunkLaunch &p, cudaStream_t stream) {
     const int nch = (p.T + C - 1) / C;
     const dim3 g1(static_cast<unsigned>(nch), static_cast<unsigned>(p.BH));
     const dim3 g2(DV / 64, static_cast<unsigned>(p.BH));
-    const auto *qb = static_cast<const __nv_bfloat16 *>(p.q);
     const auto *kb = static_cast<const __nv_bfloat16 *>(p.k);
-    const auto *vb = static_cast<const __nv_bfloat16 *>(p.v);
     gdn_wy_kernel<128><<<g1, NT, s1, stream>>>(kb, p.g, p.beta, p.W, p.Tm, p.T, p.status);
-    gdn_seq_kernel<DV><<<g2, NT, s2, stream>>>(qb, kb, vb, p.g, p.beta, p.W, p.Tm, p.scale, p.h0,
-                                               static_cast<__nv_bfloat16 *>(p.o), p.hT, p.T,
-                                               p.status);
+    SeqParams sp;
+    sp.tm_q = p.tm_q;
+    sp.tm_k = p.tm_k;
+    sp.tm_v = p.tm_v;
+    sp.tm_w = p.tm_w;
+    sp.tm_t = p.tm_t;
+    sp.g = p.g;
+    sp.beta = p.beta;
+    sp.h0 = p.h0;
+    sp.o = static_cast<__nv_bfloat16 *>(p.o);
+    sp.hT = p.hT;
+    sp.scale = p.scale;
+    sp.T = p.T;
+    sp.status = p.status;
+    gdn_seq_kernel<DV><<<g2, NTS, s2, stream>>>(sp);
     return static_cast<int>(cudaGetLastError());
 }
 

@@ -148,6 +148,9 @@ struct GdnChunkLaunch {
     // W bf16 [rows, dk] and the chunks' inverses T bf16 [rows, 64]
     __nv_bfloat16 *W;
     __nv_bfloat16 *Tm;
+    // tensor maps, 64 x 64 boxes, 128-byte swizzle: q, k (128, T, BH), v (dv, T, BH),
+    // W (128, rows, 1), T (64, rows, 1)
+    CUtensorMap tm_q, tm_k, tm_v, tm_w, tm_t;
     unsigned int *status;          // device status word (bounded waits)
 };
 
