@@ -230,13 +230,17 @@ __global__ void __launch_bounds__(NT, 2) gdn_wy_kernel(
     }
     __syncthreads();
     invert_unit_lower_blocked(sL, sTf, reinterpret_cast<float *>(sm + L::kX));
-    // T as a single bf16 K-major tile [t][i], and row-major to the scratch
+    // T as a single bf16 K-major tile [t][i] (for W), and (T - I) diag(beta)
+    // row-major to the scratch: U = T diag(beta) V is taken as beta_t v_t
+    // (exact, in fp32 where D is formed) plus (T - I) diag(beta) V
     __nv_bfloat16 *tdst = Tout + orow * C;
     for (int e = tid; e < C * C / 2; e += NT) {
         const int t = e / (C / 2), i = (e % (C / 2)) * 2;
-        const uint32_t w = pack_bf16(sTf[t * 65 + i], sTf[t * 65 + i + 1]);
-        *reinterpret_cast<uint32_t *>(sm + L::kT + sw128_offset(t, i, L::kBlk)) = w;
-        if (ok) *reinterpret_cast<uint32_t *>(tdst + t * C + i) = w;
+        const float x0 = sTf[t * 65 + i], x1 = sTf[t * 65 + i + 1];
+        *reinterpret_cast<uint32_t *>(sm + L::kT + sw128_offset(t, i, L::kBlk)) = pack_bf16(x0, x1);
+        if (ok)
+            *reinterpret_cast<uint32_t *>(tdst + t * C + i) =
+                pack_bf16(i == t ? 0.f : x0 * sB[i], i + 1 == t ? 0.f : x1 * sB[i + 1]);
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -287,33 +291,34 @@ struct SeqSmem {
     static constexpr int DK = 128;
     static constexpr uint32_t kBlk = C * 128;       // 64 rows x 64 bf16
     static constexpr uint32_t kSBlk = DK * 128;     // 128 rows x 64 bf16
+    // the loaded operands of one chunk (a stage; two stages, chunk u in u & 1)
     static constexpr uint32_t kQ = 0;               // Q [t][c] K-major (2 blocks)
-    static constexpr uint32_t kK = kQ + 2 * kBlk;   // K [i][c] K-major (B of Q K^T)
+    static constexpr uint32_t kK = kQ + 2 * kBlk;   // K [t][c]: B of Q K^T (K-major), A of K^T D' (MN-major)
     static constexpr uint32_t kW = kK + 2 * kBlk;   // W [t][c] K-major
-    static constexpr uint32_t kKth = kW + 2 * kBlk; // K~ [t][c], read MN-major (A of K~^T D)
-    static constexpr uint32_t kKtl = kKth + 2 * kBlk;
-    static constexpr uint32_t kSh = kKtl + 2 * kBlk;   // S [i][c] MN-major (B), hi and lo
+    static constexpr uint32_t kT = kW + 2 * kBlk;   // (T - I) diag(beta) [t][i] K-major
+    static constexpr uint32_t kV = kT + kBlk;       // V of this tile [i][c]: B of U (MN-major)
+    static constexpr uint32_t kStage = kV + kBlk;
+    static constexpr uint32_t kSh = 2 * kStage;     // S [i][c] MN-major (B), hi and lo
     static constexpr uint32_t kSl = kSh + kSBlk;
     static constexpr uint32_t kPh = kSl + kSBlk;    // P [t][i] K-major, hi and lo
     static constexpr uint32_t kPl = kPh + kBlk;
-    static constexpr uint32_t kDh = kPl + kBlk;     // D [t][c] MN-major (B), hi and lo
+    static constexpr uint32_t kDh = kPl + kBlk;     // D [t][c] MN-major (B of P D), hi and lo
     static constexpr uint32_t kDl = kDh + kBlk;
-    static constexpr uint32_t kT = kDl + kBlk;      // T [t][i] K-major (A of U = T beta V)
-    static constexpr uint32_t kBVh = kT + kBlk;     // beta V [i][c] MN-major (B), hi and lo
-    static constexpr uint32_t kBVl = kBVh + kBlk;
-    static constexpr uint32_t kVr = kBVl + kBlk;    // V of this tile as loaded, [t][c]
-    static constexpr uint32_t kG = kVr + kBlk;
-    static constexpr uint32_t kBeta = kG + C * 4;
-    static constexpr uint32_t kE = kBeta + C * 4;   // 2^-G per token (the scores' column factors)
+    static constexpr uint32_t kEh = kDl + kBlk;     // D' = diag(2^(G_C - G)) D (B of K^T D'), hi and lo
+    static constexpr uint32_t kEl = kEh + kBlk;
+    static constexpr uint32_t kG = kEl + kBlk;      // G of chunk u in [u & 1]
+    static constexpr uint32_t kBeta = kG + 2 * C * 4;   // beta of chunk u in [u & 1]
+    static constexpr uint32_t kE = kBeta + 2 * C * 4;   // 2^-G per token (the scores' column factors)
     static constexpr uint32_t kBar = kE + C * 4;    // the kernel's mbarriers (SeqBar)
-    static constexpr uint32_t kSlot = kBar + 64;
+    static constexpr uint32_t kSlot = kBar + 128;
     static constexpr uint32_t kBytes = kSlot + 16 + 1024;
-    static constexpr uint32_t kLoadBytes = 2 * kBlk * 3 + 2 * kBlk;   // Q, K, W; T, V
+    static constexpr uint32_t kLoadBytes = kStage;
 };
+static_assert(SeqSmem::kBytes <= 227 * 1024, "shared memory of one CTA");
 
 // The sequential kernel's operands: tensor maps of q, k, v ([BH, T, .] as
-// (channel, token, head)), W ([rows, 128]) and T ([rows, 64]), 64 x 64 boxes
-// with the 128-byte swizzle; rows past T load as zeros.
+// (channel, token, head)), W ([rows, 128]) and (T - I) diag(beta) ([rows, 64]),
+// 64 x 64 boxes with the 128-byte swizzle; rows past T load as zeros.
 struct SeqParams {
     CUtensorMap tm_q, tm_k, tm_v, tm_w, tm_t;
     const float *g, *beta, *h0;
@@ -324,22 +329,14 @@ struct SeqParams {
     unsigned int *status;
 };
 
-// One chunk's gates into registers (warp 0: lane l holds tokens l and l + 32;
-// rows past n read as zero).
-__device__ __forceinline__ void gates_load(const float *g, const float *beta, size_t r0, int n,
-                                           float (&gr)[4]) {
+// Inclusive prefix sum (log2 units) of one chunk's log-gates into sG and its
+// betas into sB (rows past n are zero, so the sum stays flat there); one warp.
+__device__ __forceinline__ void gates_scan(const float *g, const float *beta, size_t r0, int n,
+                                           float *sG, float *sB) {
     const int l = threadIdx.x & 31;
-    gr[0] = l < n ? g[r0 + l] : 0.f;
-    gr[1] = l + 32 < n ? g[r0 + l + 32] : 0.f;
-    gr[2] = l < n ? beta[r0 + l] : 0.f;
-    gr[3] = l + 32 < n ? beta[r0 + l + 32] : 0.f;
-}
-
-// Inclusive prefix sum (log2 units) of the loaded gates and the betas into the
-// shared tables; warp 0.
-__device__ __forceinline__ void gates_scan(const float (&gr)[4], float *sG, float *sB) {
-    const int l = threadIdx.x & 31;
-    float a = gr[0] * kLog2e, b = gr[1] * kLog2e;
+    sB[l] = l < n ? beta[r0 + l] : 0.f;
+    sB[l + 32] = l + 32 < n ? beta[r0 + l + 32] : 0.f;
+    float a = l < n ? g[r0 + l] * kLog2e : 0.f, b = l + 32 < n ? g[r0 + l + 32] * kLog2e : 0.f;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const float ya = __shfl_up_sync(0xffffffffu, a, o), yb = __shfl_up_sync(0xffffffffu, b, o);
@@ -348,45 +345,51 @@ __device__ __forceinline__ void gates_scan(const float (&gr)[4], float *sG, floa
     b += __shfl_sync(0xffffffffu, a, 31);
     sG[l] = a;
     sG[l + 32] = b;
-    sB[l] = gr[2];
-    sB[l + 32] = gr[3];
 }
 
-// The TMA loads of chunk u of head bh: Q, K and W (two 64-channel blocks
-// each), T, and the tile's 64 columns of V; one thread.
+// The TMA loads of chunk u of head bh into stage u & 1: Q, K and W (two
+// 64-channel blocks each), (T - I) diag(beta), and the tile's 64 columns of V; one
+// thread.
 __device__ __forceinline__ void chunk_loads(const SeqParams &p, uint8_t *sm, uint64_t *bar, int u,
                                             int bh, int c0, int nch) {
     using L = SeqSmem;
+    uint8_t *st = sm + (u & 1) * L::kStage;
     const int t0 = u * C;
     const int orow = (bh * nch + u) * C;
-    fence_proxy_async_smem();   // the previous chunk's generic reads of these tiles are done
     mbar_arrive_expect_tx(bar, L::kLoadBytes);
 #pragma unroll
     for (int kb = 0; kb < 2; ++kb) {
-        tma_load_3d(sm + L::kQ + kb * L::kBlk, &p.tm_q, bar, kb * 64, t0, bh);
-        tma_load_3d(sm + L::kK + kb * L::kBlk, &p.tm_k, bar, kb * 64, t0, bh);
-        tma_load_3d(sm + L::kW + kb * L::kBlk, &p.tm_w, bar, kb * 64, orow, 0);
+        tma_load_3d(st + L::kQ + kb * L::kBlk, &p.tm_q, bar, kb * 64, t0, bh);
+        tma_load_3d(st + L::kK + kb * L::kBlk, &p.tm_k, bar, kb * 64, t0, bh);
+        tma_load_3d(st + L::kW + kb * L::kBlk, &p.tm_w, bar, kb * 64, orow, 0);
     }
-    tma_load_3d(sm + L::kT, &p.tm_t, bar, 0, orow, 0);
-    tma_load_3d(sm + L::kVr, &p.tm_v, bar, c0, t0, bh);
+    tma_load_3d(st + L::kT, &p.tm_t, bar, 0, orow, 0);
+    tma_load_3d(st + L::kV, &p.tm_v, bar, c0, t0, bh);
 }
 
-// Grid (DV / 64, B*H); dk = 128.  W and T from gdn_wy_kernel.  288 threads:
+// Grid (DV / 64, B*H); dk = 128.  W and (T - I) diag(beta) from gdn_wy_kernel.
+// 320 threads:
 //   warps 0-3 "state": thread i holds key row i of the state (this tile's 64
-//     columns, fp32 registers); they write its bf16 hi/lo copy, form the
-//     masked scores P from Q K^T while the state chain runs, then apply the
-//     state update from K~^T D;
-//   warps 4-7 "token": the write errors D = U - W S, then the outputs;
-//   warp 8 "issue": lane 0 issues every product and the TMA loads; the warp
-//     loads the next chunk's gates.
-// Per chunk: U, W S (commit A1); Q K^T, Q S (commit A2); once A2 is done the
-// next chunk's Q, K, W, T and V load into the tiles it read; K~^T D once D is
-// written (commit B1); P D once P is written (commit B2).  Only the state
-// chain W S -> D -> K~^T D -> S is serial; the scores, P D and the outputs
-// run beside it.
-constexpr int NTS = 288;
-enum SeqBar { kSbA1 = 0, kSbA2, kSbB1, kSbB2, kSbD, kSbP, kSbLd, kSbDrain, kSbCount };
-static_assert(kSbCount * 8 <= 64, "mbarrier space of SeqSmem");
+//     columns, fp32 registers); they form the masked scores P from Q K^T
+//     while the state chain runs, then apply the state update from K^T D'
+//     and write the updated state's bf16 hi/lo copy;
+//   warps 4-7 "token": the write errors D = U - W S (and D' = D scaled by
+//     the decay to the chunk's end), then the outputs;
+//   warp 8 "issue": lane 0 issues every product;
+//   warp 9 "load": lane 0 issues the next chunk's TMA loads into the other
+//     stage as the chunk begins; the warp scans the next chunk's gates.
+// Per chunk: (T - I) diag(beta) V and W S (commit A1), Q K^T (commit QK),
+// Q S (commit A2); K^T D' once D is written (commit B1); P D once P is
+// written (commit B2).  Only the state chain W S -> D -> K^T D' -> S is
+// serial; the scores, P D and the outputs run beside it.  beta rides on T
+// (its exact diagonal term beta_t v_t is added in fp32 where D is formed) and
+// the decay to the chunk's end on D', so the raw bf16 tiles of K and V are
+// the operands as loaded.  The M = 64 products (token rows in lanes 0-15 of each
+// lane quarter) are read with the half-split TMEM load, so that all 32
+// threads of a warp take part in their epilogues.
+constexpr int NTS = 320;
+enum SeqBar { kSbQK = 0, kSbA1, kSbA2, kSbB1, kSbB2, kSbD, kSbP, kSbLd0, kSbLd1, kSbDrain, kSbCount };
+static_assert(kSbCount * 8 <= 128, "mbarrier space of SeqSmem");
 
 template <int DV>
 __global__ void __launch_bounds__(NTS, 1) gdn_seq_kernel(const __grid_constant__ SeqParams p) {
@@ -403,7 +406,7 @@ __global__ void __launch_bounds__(NTS, 1) gdn_seq_kernel(const __grid_constant__
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    float *sG = reinterpret_cast<float *>(sm + L::kG), *sB = reinterpret_cast<float *>(sm + L::kBeta);
+    float *sGb = reinterpret_cast<float *>(sm + L::kG), *sBb = reinterpret_cast<float *>(sm + L::kBeta);
     float *sE = reinterpret_cast<float *>(sm + L::kE);
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::kBar);
     uint32_t *slot = reinterpret_cast<uint32_t *>(sm + L::kSlot);
@@ -450,119 +453,97 @@ __global__ void __launch_bounds__(NTS, 1) gdn_seq_kernel(const __grid_constant__
         }
     };
     if (warp < 4) state_copy();
-    float gr[4];   // warp 8: the next chunk's gates
-    int loads = 0;  // warp 8 lane 0: chunk loads issued
-    if (warp == 8) {
-        gates_load(g, beta, static_cast<size_t>(bh) * T, min(C, T), gr);
+    int loads = 0;  // warp 9 lane 0: chunks whose loads are issued
+    if (warp == 9) {
+        gates_scan(g, beta, static_cast<size_t>(bh) * T, min(C, T), sGb, sBb);
         if (lane == 0) {
-            chunk_loads(p, sm, &bar[kSbLd], 0, bh, c0, nch);
+            chunk_loads(p, sm, &bar[kSbLd0], 0, bh, c0, nch);
             loads = 1;
         }
     }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();   // the state copy and the first chunk's gates
+    tc_fence_after();
 
 #pragma unroll 1
     for (int u = 0; u < nch; ++u) {
         const int t0 = u * C, n = min(C, T - t0);
         const size_t rg = static_cast<size_t>(bh) * T + t0;
         const uint32_t ph = static_cast<uint32_t>(u & 1);
-        if (warp == 8) gates_scan(gr, sG, sB);
-        ok = mbar_wait_bounded(&bar[kSbLd], ph, status) && ok;   // this chunk's tiles
-        __syncthreads();   // sG, sB
+        const float *sG = sGb + (u & 1) * C;
         const float GC = sG[C - 1];
-        if (warp < 8) {
-            // K~ = K 2^(G_C - G_t) and beta V of this tile as hi/lo pairs, from
-            // the loaded tiles (same swizzled layout); warps 0-7
-            constexpr int PER = C * DK / 8 / 256;
-#pragma unroll
-            for (int m = 0; m < PER; ++m) {
-                const int e = tid + m * 256, t = e / (DK / 8), c = (e % (DK / 8)) * 8;
-                const uint32_t so = sw128_offset(t, c, L::kBlk);
-                const uint4 rk = *reinterpret_cast<const uint4 *>(sm + L::kK + so);
-                const float f = ex2f(GC - sG[t]);
-                const uint32_t w4[4] = {rk.x, rk.y, rk.z, rk.w};
-                uint32_t hi[4], lo[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    split_pair(__uint_as_float(w4[j] << 16) * f, __uint_as_float(w4[j] & 0xffff0000u) * f, hi[j], lo[j]);
-                *reinterpret_cast<uint4 *>(sm + L::kKth + so) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4 *>(sm + L::kKtl + so) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        const uint32_t st = a0 + (u & 1) * L::kStage;   // this chunk's stage
+        // 2^(G_t - G_i) = 2^G_t 2^-G_i for the scores: one exponential per row
+        // and a column table, while the chunk's total decay keeps 2^-G_i within
+        // 2^60 (G falls monotonically over the chunk); else one exponential
+        // per element
+        const bool split_exp = GC >= -60.f;
+        if (warp == 9) {
+            // ======================================================= load warp
+            // the next chunk's operands into the other stage (every read of
+            // it ended with the previous chunk), and its gates
+            if (u + 1 < nch) {
+                if (lane == 0) {
+                    chunk_loads(p, sm, &bar[kSbLd0 + ((u + 1) & 1)], u + 1, bh, c0, nch);
+                    loads = u + 2;
+                }
+                __syncwarp();
+                gates_scan(g, beta, rg + C, min(C, T - t0 - C), sGb + ((u + 1) & 1) * C,
+                           sBb + ((u + 1) & 1) * C);
             }
-#pragma unroll
-            for (int m = 0; m < 2; ++m) {
-                const int e = tid + m * 256, t = e / 8, c = (e % 8) * 8;
-                const uint32_t so = sw128_offset(t, c, L::kBlk);
-                const uint4 rv = *reinterpret_cast<const uint4 *>(sm + L::kVr + so);
-                const float fb = sB[t];
-                const uint32_t w4[4] = {rv.x, rv.y, rv.z, rv.w};
-                uint32_t hi[4], lo[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    split_pair(__uint_as_float(w4[j] << 16) * fb, __uint_as_float(w4[j] & 0xffff0000u) * fb, hi[j], lo[j]);
-                *reinterpret_cast<uint4 *>(sm + L::kBVh + so) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4 *>(sm + L::kBVl + so) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (warp == 8) {
+        } else if (warp == 8) {
             // ======================================================= issue warp
             if (lane == 0) {
+                ok = mbar_wait_bounded(&bar[kSbLd0 + (u & 1)], static_cast<uint32_t>((u >> 1) & 1),
+                                       status) && ok;
+                tc_fence_after();
                 constexpr uint32_t id_s = idesc_bf16(64, 64, false, true);    // A [t][c] K-major, S [c][j] MN-major
                 constexpr uint32_t id_p = idesc_bf16(64, C, false, false);    // Q [t][c], K [i][c]
-                constexpr uint32_t id_u = idesc_bf16(64, 64, false, true);    // T [t][i], beta V [i][c]
-                // A1: U = T (beta V) (TMEM 320) and W S (TMEM 0), the state chain's first step
+                constexpr uint32_t id_u = idesc_bf16(64, 64, false, true);    // T [t][i], V [i][c]
+                // A1: (T - I) diag(beta) V (TMEM 320) and W S (TMEM 0), the state chain's first step
 #pragma unroll
-                for (int kk = 0; kk < C / 16; ++kk) {
-                    const uint64_t at = sw128_desc(a0 + L::kT + kk * 32, 16, 1024);
-                    const uint32_t om = kk * 2048;
-                    mma_bf16_ss(tmem + 320, at, sw128_desc(a0 + L::kBVh + om, L::kBlk, 1024), id_u,
-                                kk > 0 ? 1u : 0u);
-                    mma_bf16_ss(tmem + 320, at, sw128_desc(a0 + L::kBVl + om, L::kBlk, 1024), id_u, 1u);
-                }
+                for (int kk = 0; kk < C / 16; ++kk)
+                    mma_bf16_ss(tmem + 320, sw128_desc(st + L::kT + kk * 32, 16, 1024),
+                                sw128_desc(st + L::kV + kk * 2048, L::kBlk, 1024), id_u, kk > 0 ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; ++kk) {
                     const uint32_t ok_ = (kk >> 2) * L::kBlk + (kk & 3) * 32;
-                    mma_bf16_ss(tmem, sw128_desc(a0 + L::kW + ok_, 16, 1024),
+                    mma_bf16_ss(tmem, sw128_desc(st + L::kW + ok_, 16, 1024),
                                 sw128_desc(a0 + L::kSh + kk * 2048, L::kSBlk, 1024), id_s,
                                 kk > 0 ? 1u : 0u);
                 }
                 mma_commit(&bar[kSbA1]);
-                // A2: Q K^T (TMEM 128) and Q S (TMEM 64)
+                // Q K^T (TMEM 128)
+#pragma unroll
+                for (int kk = 0; kk < DK / 16; ++kk) {
+                    const uint32_t ok_ = (kk >> 2) * L::kBlk + (kk & 3) * 32;
+                    mma_bf16_ss(tmem + 128, sw128_desc(st + L::kQ + ok_, 16, 1024),
+                                sw128_desc(st + L::kK + ok_, 16, 1024), id_p, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&bar[kSbQK]);
+                // A2: Q S (TMEM 64)
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; ++kk) {
                     const uint32_t ok_ = (kk >> 2) * L::kBlk + (kk & 3) * 32;
                     const uint32_t om = kk * 2048;
-                    const uint64_t aq = sw128_desc(a0 + L::kQ + ok_, 16, 1024);
-                    mma_bf16_ss(tmem + 128, aq, sw128_desc(a0 + L::kK + ok_, 16, 1024), id_p,
-                                kk > 0 ? 1u : 0u);
+                    const uint64_t aq = sw128_desc(st + L::kQ + ok_, 16, 1024);
                     mma_bf16_ss(tmem + 64, aq, sw128_desc(a0 + L::kSh + om, L::kSBlk, 1024), id_s,
                                 kk > 0 ? 1u : 0u);
                     mma_bf16_ss(tmem + 64, aq, sw128_desc(a0 + L::kSl + om, L::kSBlk, 1024), id_s, 1u);
                 }
                 mma_commit(&bar[kSbA2]);
-                // Q, K, W, T and V are read once A2 is done: the next chunk's
-                // operands load into them
-                ok = mbar_wait_bounded(&bar[kSbA2], ph, status) && ok;
-                if (u + 1 < nch) {
-                    chunk_loads(p, sm, &bar[kSbLd], u + 1, bh, c0, nch);
-                    loads = u + 2;
-                }
-                // B1: K~^T D (TMEM 256; M = 128 channels) once D is written
-                constexpr uint32_t id_kd = idesc_bf16(128, 64, true, true);   // K~ [i][c] MN-major, D [i][c] MN-major
+                // B1: K^T D' (TMEM 256; M = 128 channels) once D' is written
+                constexpr uint32_t id_kd = idesc_bf16(128, 64, true, true);   // K [t][c] MN-major, D' [t][c] MN-major
                 ok = mbar_wait_bounded(&bar[kSbD], ph, status) && ok;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < C / 16; ++kk) {
                     const uint32_t om = kk * 2048;
-                    const uint64_t dh = sw128_desc(a0 + L::kDh + om, L::kBlk, 1024);
-                    const uint64_t dl = sw128_desc(a0 + L::kDl + om, L::kBlk, 1024);
-                    const uint64_t kh = sw128_desc(a0 + L::kKth + om, L::kBlk, 1024);
-                    const uint64_t kl = sw128_desc(a0 + L::kKtl + om, L::kBlk, 1024);
-                    mma_bf16_ss(tmem + 256, kh, dh, id_kd, kk > 0 ? 1u : 0u);
-                    mma_bf16_ss(tmem + 256, kl, dh, id_kd, 1u);
-                    mma_bf16_ss(tmem + 256, kh, dl, id_kd, 1u);
+                    const uint64_t kd = sw128_desc(st + L::kK + om, L::kBlk, 1024);
+                    mma_bf16_ss(tmem + 256, kd, sw128_desc(a0 + L::kEh + om, L::kBlk, 1024), id_kd,
+                                kk > 0 ? 1u : 0u);
+                    mma_bf16_ss(tmem + 256, kd, sw128_desc(a0 + L::kEl + om, L::kBlk, 1024), id_kd, 1u);
                 }
                 mma_commit(&bar[kSbB1]);
                 // B2: P D (TMEM 192; M = 64, K = 64 tokens) once P is written
@@ -583,32 +564,48 @@ __global__ void __launch_bounds__(NTS, 1) gdn_seq_kernel(const __grid_constant__
                 mma_commit(&bar[kSbB2]);
             }
             __syncwarp();
-            if (u + 1 < nch) gates_load(g, beta, rg + C, min(C, T - t0 - C), gr);
         } else if (warp >= 4) {
             // ======================================================= token warps
-            const int t = 16 * q4 + lane;   // rows t in lanes 0-15 of each quarter (M = 64)
-            // D = U - W S as a hi/lo pair [t][c]
+            // thread: row t (lanes 0-15 of the quarter) and a 16-column half
+            // of each 32-column block
+            const int t = 16 * q4 + (lane & 15), hc = (lane >> 4) * 16;
+            const float fe = ex2f(GC - sG[t]);   // decay from token t to the chunk's end (<= 1)
+            const float bt = sBb[(u & 1) * C + t];
+            // D = beta_t v_t + ((T - I) diag(beta) V)_t - (W S)_t and
+            // D' = 2^(G_C - G_t) D, each as a hi/lo pair [t][c]
+            // (the V tile is read here too: its load is complete before A1 is)
+            ok = mbar_wait_bounded(&bar[kSbLd0 + (u & 1)], static_cast<uint32_t>((u >> 1) & 1), status) && ok;
             ok = mbar_wait_bounded(&bar[kSbA1], ph, status) && ok;
             tc_fence_after();
 #pragma unroll 1
             for (int cb = 0; cb < 64; cb += 32) {
-                uint32_t r[32], ru[32];
-                tmem_ld32(tmem + lane_off + cb, r);
-                tmem_ld32(tmem + lane_off + 320 + cb, ru);
+                uint32_t r[16], ru[16];
+                tmem_ld16x2<16>(tmem + lane_off + cb, r);
+                tmem_ld16x2<16>(tmem + lane_off + 320 + cb, ru);
                 tmem_wait_ld();
-                if (lane < 16) {
 #pragma unroll
-                    for (int j = 0; j < 32; j += 8) {
-                        float d[8];
+                for (int j = 0; j < 16; j += 8) {
+                    const uint32_t so = sw128_offset(t, cb + hc + j, L::kBlk);
+                    const uint4 vr = *reinterpret_cast<const uint4 *>(sm + (u & 1) * L::kStage + L::kV + so);
+                    const uint32_t v4[4] = {vr.x, vr.y, vr.z, vr.w};
+                    float d[8];
 #pragma unroll
-                        for (int x = 0; x < 8; ++x) d[x] = __uint_as_float(ru[j + x]) - __uint_as_float(r[j + x]);
-                        uint32_t hi[4], lo[4];
-#pragma unroll
-                        for (int x = 0; x < 4; ++x) split_pair(d[2 * x], d[2 * x + 1], hi[x], lo[x]);
-                        const uint32_t so = sw128_offset(t, cb + j, L::kBlk);
-                        *reinterpret_cast<uint4 *>(sm + L::kDh + so) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                        *reinterpret_cast<uint4 *>(sm + L::kDl + so) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    for (int x = 0; x < 4; ++x) {
+                        d[2 * x] = fmaf(bt, __uint_as_float(v4[x] << 16),
+                                        __uint_as_float(ru[j + 2 * x]) - __uint_as_float(r[j + 2 * x]));
+                        d[2 * x + 1] = fmaf(bt, __uint_as_float(v4[x] & 0xffff0000u),
+                                            __uint_as_float(ru[j + 2 * x + 1]) - __uint_as_float(r[j + 2 * x + 1]));
                     }
+                    uint32_t hi[4], lo[4], ehi[4], elo[4];
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {
+                        split_pair(d[2 * x], d[2 * x + 1], hi[x], lo[x]);
+                        split_pair(fe * d[2 * x], fe * d[2 * x + 1], ehi[x], elo[x]);
+                    }
+                    *reinterpret_cast<uint4 *>(sm + L::kDh + so) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4 *>(sm + L::kDl + so) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    *reinterpret_cast<uint4 *>(sm + L::kEh + so) = make_uint4(ehi[0], ehi[1], ehi[2], ehi[3]);
+                    *reinterpret_cast<uint4 *>(sm + L::kEl + so) = make_uint4(elo[0], elo[1], elo[2], elo[3]);
                 }
             }
             fence_proxy_async_smem();
@@ -618,21 +615,21 @@ __global__ void __launch_bounds__(NTS, 1) gdn_seq_kernel(const __grid_constant__
             // o_t = scale (2^G_t QS_t + PD_t) once P D is done (Q S came before it)
             ok = mbar_wait_bounded(&bar[kSbB2], ph, status) && ok;
             tc_fence_after();
-            const float f = lane < 16 ? ex2f(sG[t]) : 0.f;
+            const float f = scale * ex2f(sG[t]);
 #pragma unroll 1
             for (int cb = 0; cb < 64; cb += 32) {
-                uint32_t a[32], b[32];
-                tmem_ld32(tmem + lane_off + 64 + cb, a);
-                tmem_ld32(tmem + lane_off + 192 + cb, b);
+                uint32_t a[16], b[16];
+                tmem_ld16x2<16>(tmem + lane_off + 64 + cb, a);
+                tmem_ld16x2<16>(tmem + lane_off + 192 + cb, b);
                 tmem_wait_ld();
-                if (lane < 16 && t < n && ok) {
-                    __nv_bfloat16 *dst = o + (rg + t) * DV + c0 + cb;
+                if (t < n && ok) {
+                    __nv_bfloat16 *dst = o + (rg + t) * DV + c0 + cb + hc;
 #pragma unroll
-                    for (int j = 0; j < 32; j += 8) {
+                    for (int j = 0; j < 16; j += 8) {
                         float x[8];
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
-                            x[e] = scale * fmaf(f, __uint_as_float(a[j + e]), __uint_as_float(b[j + e]));
+                            x[e] = fmaf(f, __uint_as_float(a[j + e]), scale * __uint_as_float(b[j + e]));
                         *reinterpret_cast<uint4 *>(dst + j) =
                             make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]),
                                        pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
@@ -641,60 +638,53 @@ __global__ void __launch_bounds__(NTS, 1) gdn_seq_kernel(const __grid_constant__
             }
         } else {
             // ======================================================= state warps
-            // P = tril(Q K^T 2^(G_t - G_i)) as a hi/lo pair [t][i] (rows t in lanes
-            // 0-15 of each quarter), while the state chain runs
+            // P = tril(Q K^T 2^(G_t - G_i)) as a hi/lo pair [t][i] while the
+            // state chain runs; thread: row t, a 16-column half of each block
             {
-                const int t = 16 * q4 + lane;
-                // 2^(G_t - G_i) = 2^G_t 2^-G_i: one exponential per row and a
-                // column table, while the chunk's total decay keeps 2^-G_i
-                // within 2^60 (G falls monotonically over the chunk); else one
-                // exponential per element
-                const bool split_exp = GC >= -60.f;
-                if (split_exp && lane < 16) sE[t] = ex2f(-sG[t]);   // (rows = columns here)
-                ok = mbar_wait_bounded(&bar[kSbA2], ph, status) && ok;
-                tc_fence_after();
+                if (split_exp && lane < 16) sE[16 * q4 + lane] = ex2f(-sG[16 * q4 + lane]);
                 named_barrier(1, 128);   // the column table of the state warps
-                const float Gt = lane < 16 ? sG[t] : 0.f;
+                const int t = 16 * q4 + (lane & 15), hc = (lane >> 4) * 16;
+                const float Gt = sG[t];
                 const float et = ex2f(Gt);
-                // one 32-column block of scores: the decay factor of column i
-                // from the table or by its own exponential
-                // (eight consecutive columns of the row are one 16-byte piece of
-                // the swizzled tile: one store each for hi and lo)
-                auto p_block = [&](const uint32_t(&r)[32], int cb, auto factor) {
+                // 16 scores of row t from column i0 on; the decay factor of
+                // column i from the table or by its own exponential (eight
+                // consecutive columns are one 16-byte piece of the swizzled
+                // tile: one store each for hi and lo)
+                auto p_block = [&](const uint32_t(&r)[16], int i0, auto factor) {
 #pragma unroll
-                    for (int j8 = 0; j8 < 32; j8 += 8) {
+                    for (int j8 = 0; j8 < 16; j8 += 8) {
                         uint32_t hi[4], lo[4];
 #pragma unroll
                         for (int x = 0; x < 4; ++x) {
-                            const int i = cb + j8 + 2 * x;
+                            const int i = i0 + j8 + 2 * x;
                             const float x0 = i <= t ? __uint_as_float(r[j8 + 2 * x]) * factor(i) : 0.f;
                             const float x1 =
                                 i + 1 <= t ? __uint_as_float(r[j8 + 2 * x + 1]) * factor(i + 1) : 0.f;
                             split_pair(x0, x1, hi[x], lo[x]);
                         }
-                        const uint32_t so = sw128_offset(t, cb + j8, L::kBlk);
+                        const uint32_t so = sw128_offset(t, i0 + j8, L::kBlk);
                         *reinterpret_cast<uint4 *>(sm + L::kPh + so) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
                         *reinterpret_cast<uint4 *>(sm + L::kPl + so) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                     }
                 };
+                ok = mbar_wait_bounded(&bar[kSbQK], ph, status) && ok;
+                tc_fence_after();
 #pragma unroll 1
                 for (int cb = 0; cb < 64; cb += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(tmem + lane_off + 128 + cb, r);
+                    uint32_t r[16];
+                    tmem_ld16x2<16>(tmem + lane_off + 128 + cb, r);
                     tmem_wait_ld();
-                    if (lane < 16) {
-                        if (split_exp)
-                            p_block(r, cb, [&](int i) { return et * sE[i]; });
-                        else
-                            p_block(r, cb, [&](int i) { return ex2f(Gt - sG[i]); });
-                    }
+                    if (split_exp)
+                        p_block(r, cb + hc, [&](int i) { return et * sE[i]; });
+                    else
+                        p_block(r, cb + hc, [&](int i) { return ex2f(Gt - sG[i]); });
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar[kSbP]);
             }
-            // S_i = 2^G_C S_i + (K~^T D)_i (lane = key row, M = 128)
+            // S_i = 2^G_C S_i + (K^T D')_i (lane = key row, M = 128)
             ok = mbar_wait_bounded(&bar[kSbB1], ph, status) && ok;
             tc_fence_after();
             const float fc = ex2f(GC);
@@ -708,6 +698,7 @@ __global__ void __launch_bounds__(NTS, 1) gdn_seq_kernel(const __grid_constant__
             }
             // W S and Q S (A1, A2) are done: the copy for the next chunk
             if (u + 1 < nch) state_copy();
+            fence_proxy_async_smem();
         }
         tc_fence_before();
         ok = __syncthreads_and(ok) != 0;   // one verdict for the whole CTA; also ends the chunk
@@ -726,7 +717,10 @@ __global__ void __launch_bounds__(NTS, 1) gdn_seq_kernel(const __grid_constant__
     if (warp == 8 && lane == 0) {
         mma_commit(&bar[kSbDrain]);
         mbar_wait_bounded(&bar[kSbDrain], 0, status);
-        if (loads > 0) mbar_wait_bounded(&bar[kSbLd], static_cast<uint32_t>((loads - 1) & 1), status);
+    }
+    if (warp == 9 && lane == 0) {
+        for (int c = max(0, loads - 2); c < loads; ++c)
+            mbar_wait_bounded(&bar[kSbLd0 + (c & 1)], static_cast<uint32_t>((c >> 1) & 1), status);
     }
     tc_fence_before();
     __syncthreads();
