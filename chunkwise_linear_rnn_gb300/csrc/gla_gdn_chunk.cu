@@ -388,7 +388,7 @@ __device__ __forceinline__ void chunk_loads(const SeqParams &p, uint8_t *sm, uin
 // lane quarter) are read with the half-split TMEM load, so that all 32
 // threads of a warp take part in their epilogues.
 constexpr int NTS = 320;
-enum SeqBar { kSbQK = 0, kSbA1, kSbA2, kSbB1, kSbB2, kSbD, kSbP, kSbLd0, kSbLd1, kSbDrain, kSbCount };
+enum SeqBar { kSbA1 = 0, kSbQK, kSbA2, kSbB1, kSbB2, kSbD, kSbP, kSbLd0, kSbLd1, kSbDrain, kSbDrain2, kSbCount };
 static_assert(kSbCount * 8 <= 128, "mbarrier space of SeqSmem");
 
 template <int DV>
@@ -481,85 +481,89 @@ __global__ void __launch_bounds__(NTS, 1) gdn_seq_kernel(const __grid_constant__
         const bool split_exp = GC >= -60.f;
         if (warp == 9) {
             // ======================================================= load warp
-            // the next chunk's operands into the other stage (every read of
-            // it ended with the previous chunk), and its gates
-            if (u + 1 < nch) {
-                if (lane == 0) {
+            // lane 0 issues the products of the output side, Q K^T (TMEM
+            // 256-319) and Q [Sh|Sl] (TMEM 128-255), beside the issue warp's
+            // state chain; then the next chunk's operands into the other
+            // stage (every read of it ended with the previous chunk); the
+            // warp scans the next chunk's gates
+            if (lane == 0) {
+                ok = mbar_wait_bounded(&bar[kSbLd0 + (u & 1)], static_cast<uint32_t>((u >> 1) & 1),
+                                       status) && ok;
+                tc_fence_after();
+                constexpr uint32_t id_p = idesc_bf16(64, C, false, false);     // Q [t][c], K [i][c]
+                constexpr uint32_t id_s2 = idesc_bf16(64, 128, false, true);   // Q [t][c], [Sh|Sl] MN-major
+#pragma unroll
+                for (int kk = 0; kk < DK / 16; ++kk) {
+                    const uint32_t ok_ = (kk >> 2) * L::kBlk + (kk & 3) * 32;
+                    mma_bf16_ss(tmem + 256, sw128_desc(st + L::kQ + ok_, 16, 1024),
+                                sw128_desc(st + L::kK + ok_, 16, 1024), id_p, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&bar[kSbQK]);
+#pragma unroll
+                for (int kk = 0; kk < DK / 16; ++kk) {
+                    const uint32_t ok_ = (kk >> 2) * L::kBlk + (kk & 3) * 32;
+                    mma_bf16_ss(tmem + 128, sw128_desc(st + L::kQ + ok_, 16, 1024),
+                                sw128_desc(a0 + L::kSh + kk * 2048, L::kSBlk, 1024), id_s2,
+                                kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&bar[kSbA2]);
+                if (u + 1 < nch) {
                     chunk_loads(p, sm, &bar[kSbLd0 + ((u + 1) & 1)], u + 1, bh, c0, nch);
                     loads = u + 2;
                 }
-                __syncwarp();
+            }
+            __syncwarp();
+            if (u + 1 < nch)
                 gates_scan(g, beta, rg + C, min(C, T - t0 - C), sGb + ((u + 1) & 1) * C,
                            sBb + ((u + 1) & 1) * C);
-            }
         } else if (warp == 8) {
             // ======================================================= issue warp
             if (lane == 0) {
                 ok = mbar_wait_bounded(&bar[kSbLd0 + (u & 1)], static_cast<uint32_t>((u >> 1) & 1),
                                        status) && ok;
                 tc_fence_after();
-                constexpr uint32_t id_s = idesc_bf16(64, 64, false, true);    // A [t][c] K-major, S [c][j] MN-major
-                constexpr uint32_t id_p = idesc_bf16(64, C, false, false);    // Q [t][c], K [i][c]
                 constexpr uint32_t id_u = idesc_bf16(64, 64, false, true);    // T [t][i], V [i][c]
-                // A1: (T - I) diag(beta) V (TMEM 320) and W S (TMEM 0), the state chain's first step
-#pragma unroll
-                for (int kk = 0; kk < C / 16; ++kk)
-                    mma_bf16_ss(tmem + 320, sw128_desc(st + L::kT + kk * 32, 16, 1024),
-                                sw128_desc(st + L::kV + kk * 2048, L::kBlk, 1024), id_u, kk > 0 ? 1u : 0u);
+                // TMEM columns: W [Sh|Sl] 0-127, Q [Sh|Sl] 128-255, Q K^T
+                // 256-319, (T - I) diag(beta) V 320-383, K^T [D'h|D'l] 384-511
+                // (M = 128); once D is formed, Ph [Dh|Dl] into 0-127 and Pl Dh
+                // into 320-383.  A split operand's hi and lo halves sit side by
+                // side as one N = 128 operand (their sum is taken where the
+                // product is read): one instruction per 16-deep step for both.
+                constexpr uint32_t id_s2 = idesc_bf16(64, 128, false, true);   // A [t][c] K-major, [Sh|Sl] MN-major
+                // A1: W S and (T - I) diag(beta) V, the state chain's first step
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; ++kk) {
                     const uint32_t ok_ = (kk >> 2) * L::kBlk + (kk & 3) * 32;
+                    const uint32_t acc = kk > 0 ? 1u : 0u;
                     mma_bf16_ss(tmem, sw128_desc(st + L::kW + ok_, 16, 1024),
-                                sw128_desc(a0 + L::kSh + kk * 2048, L::kSBlk, 1024), id_s,
-                                kk > 0 ? 1u : 0u);
+                                sw128_desc(a0 + L::kSh + kk * 2048, L::kSBlk, 1024), id_s2, acc);
+                    if (kk < C / 16)
+                        mma_bf16_ss(tmem + 320, sw128_desc(st + L::kT + kk * 32, 16, 1024),
+                                    sw128_desc(st + L::kV + kk * 2048, L::kBlk, 1024), id_u, acc);
                 }
                 mma_commit(&bar[kSbA1]);
-                // Q K^T (TMEM 128)
-#pragma unroll
-                for (int kk = 0; kk < DK / 16; ++kk) {
-                    const uint32_t ok_ = (kk >> 2) * L::kBlk + (kk & 3) * 32;
-                    mma_bf16_ss(tmem + 128, sw128_desc(st + L::kQ + ok_, 16, 1024),
-                                sw128_desc(st + L::kK + ok_, 16, 1024), id_p, kk > 0 ? 1u : 0u);
-                }
-                mma_commit(&bar[kSbQK]);
-                // A2: Q S (TMEM 64)
-#pragma unroll
-                for (int kk = 0; kk < DK / 16; ++kk) {
-                    const uint32_t ok_ = (kk >> 2) * L::kBlk + (kk & 3) * 32;
-                    const uint32_t om = kk * 2048;
-                    const uint64_t aq = sw128_desc(st + L::kQ + ok_, 16, 1024);
-                    mma_bf16_ss(tmem + 64, aq, sw128_desc(a0 + L::kSh + om, L::kSBlk, 1024), id_s,
-                                kk > 0 ? 1u : 0u);
-                    mma_bf16_ss(tmem + 64, aq, sw128_desc(a0 + L::kSl + om, L::kSBlk, 1024), id_s, 1u);
-                }
-                mma_commit(&bar[kSbA2]);
-                // B1: K^T D' (TMEM 256; M = 128 channels) once D' is written
-                constexpr uint32_t id_kd = idesc_bf16(128, 64, true, true);   // K [t][c] MN-major, D' [t][c] MN-major
+                // B1: K^T D' (M = 128 channels) once D' is written
+                constexpr uint32_t id_kd = idesc_bf16(128, 128, true, true);   // K [t][c] MN-major, [D'h|D'l] MN-major
                 ok = mbar_wait_bounded(&bar[kSbD], ph, status) && ok;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < C / 16; ++kk) {
-                    const uint32_t om = kk * 2048;
-                    const uint64_t kd = sw128_desc(st + L::kK + om, L::kBlk, 1024);
-                    mma_bf16_ss(tmem + 256, kd, sw128_desc(a0 + L::kEh + om, L::kBlk, 1024), id_kd,
+                for (int kk = 0; kk < C / 16; ++kk)
+                    mma_bf16_ss(tmem + 384, sw128_desc(st + L::kK + kk * 2048, L::kBlk, 1024),
+                                sw128_desc(a0 + L::kEh + kk * 2048, L::kBlk, 1024), id_kd,
                                 kk > 0 ? 1u : 0u);
-                    mma_bf16_ss(tmem + 256, kd, sw128_desc(a0 + L::kEl + om, L::kBlk, 1024), id_kd, 1u);
-                }
                 mma_commit(&bar[kSbB1]);
-                // B2: P D (TMEM 192; M = 64, K = 64 tokens) once P is written
-                constexpr uint32_t id_pd = idesc_bf16(64, 64, false, true);   // P [t][i] K-major, D [i][c] MN-major
+                // B2: P D (K = 64 tokens) once P is written; W S and U were
+                // read into D by then
+                constexpr uint32_t id_pd2 = idesc_bf16(64, 128, false, true);  // P [t][i] K-major, [Dh|Dl] MN-major
+                constexpr uint32_t id_pd = idesc_bf16(64, 64, false, true);
                 ok = mbar_wait_bounded(&bar[kSbP], ph, status) && ok;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < C / 16; ++kk) {
-                    const uint32_t om = kk * 2048;
-                    const uint64_t dh = sw128_desc(a0 + L::kDh + om, L::kBlk, 1024);
-                    const uint64_t dl = sw128_desc(a0 + L::kDl + om, L::kBlk, 1024);
-                    const uint64_t phd = sw128_desc(a0 + L::kPh + kk * 32, 16, 1024);
-                    const uint64_t pld = sw128_desc(a0 + L::kPl + kk * 32, 16, 1024);
-                    mma_bf16_ss(tmem + 192, phd, dh, id_pd, kk > 0 ? 1u : 0u);
-                    mma_bf16_ss(tmem + 192, pld, dh, id_pd, 1u);
-                    mma_bf16_ss(tmem + 192, phd, dl, id_pd, 1u);
+                    const uint64_t dh = sw128_desc(a0 + L::kDh + kk * 2048, L::kBlk, 1024);
+                    const uint32_t acc = kk > 0 ? 1u : 0u;
+                    mma_bf16_ss(tmem, sw128_desc(a0 + L::kPh + kk * 32, 16, 1024), dh, id_pd2, acc);
+                    mma_bf16_ss(tmem + 320, sw128_desc(a0 + L::kPl + kk * 32, 16, 1024), dh, id_pd, acc);
                 }
                 mma_commit(&bar[kSbB2]);
             }
@@ -579,10 +583,13 @@ __global__ void __launch_bounds__(NTS, 1) gdn_seq_kernel(const __grid_constant__
             tc_fence_after();
 #pragma unroll 1
             for (int cb = 0; cb < 64; cb += 32) {
-                uint32_t r[16], ru[16];
+                uint32_t r[16], rl[16], ru[16];
                 tmem_ld16x2<16>(tmem + lane_off + cb, r);
+                tmem_ld16x2<16>(tmem + lane_off + 64 + cb, rl);
                 tmem_ld16x2<16>(tmem + lane_off + 320 + cb, ru);
                 tmem_wait_ld();
+#pragma unroll
+                for (int x = 0; x < 16; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) + __uint_as_float(rl[x]));
 #pragma unroll
                 for (int j = 0; j < 16; j += 8) {
                     const uint32_t so = sw128_offset(t, cb + hc + j, L::kBlk);
@@ -612,16 +619,22 @@ __global__ void __launch_bounds__(NTS, 1) gdn_seq_kernel(const __grid_constant__
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[kSbD]);
-            // o_t = scale (2^G_t QS_t + PD_t) once P D is done (Q S came before it)
+            // o_t = scale (2^G_t QS_t + PD_t) once Q S and P D are done
+            ok = mbar_wait_bounded(&bar[kSbA2], ph, status) && ok;
             ok = mbar_wait_bounded(&bar[kSbB2], ph, status) && ok;
             tc_fence_after();
             const float f = scale * ex2f(sG[t]);
 #pragma unroll 1
             for (int cb = 0; cb < 64; cb += 32) {
-                uint32_t a[16], b[16];
-                tmem_ld16x2<16>(tmem + lane_off + 64 + cb, a);
-                tmem_ld16x2<16>(tmem + lane_off + 192 + cb, b);
+                uint32_t a[16], a2[16], b[16], b2[16], b3[16];
+                tmem_ld16x2<16>(tmem + lane_off + 128 + cb, a);
+                tmem_ld16x2<16>(tmem + lane_off + 192 + cb, a2);
+                tmem_ld16x2<16>(tmem + lane_off + cb, b);
+                tmem_ld16x2<16>(tmem + lane_off + 64 + cb, b2);
+                tmem_ld16x2<16>(tmem + lane_off + 320 + cb, b3);
                 tmem_wait_ld();
+#pragma unroll
+                for (int x = 0; x < 16; ++x) b2[x] = __float_as_uint(__uint_as_float(b2[x]) + __uint_as_float(b3[x]));
                 if (t < n && ok) {
                     __nv_bfloat16 *dst = o + (rg + t) * DV + c0 + cb + hc;
 #pragma unroll
@@ -629,7 +642,8 @@ __global__ void __launch_bounds__(NTS, 1) gdn_seq_kernel(const __grid_constant__
                         float x[8];
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
-                            x[e] = fmaf(f, __uint_as_float(a[j + e]), scale * __uint_as_float(b[j + e]));
+                            x[e] = fmaf(f, __uint_as_float(a[j + e]) + __uint_as_float(a2[j + e]),
+                                        scale * (__uint_as_float(b[j + e]) + __uint_as_float(b2[j + e])));
                         *reinterpret_cast<uint4 *>(dst + j) =
                             make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]),
                                        pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
@@ -672,7 +686,7 @@ __global__ void __launch_bounds__(NTS, 1) gdn_seq_kernel(const __grid_constant__
 #pragma unroll 1
                 for (int cb = 0; cb < 64; cb += 32) {
                     uint32_t r[16];
-                    tmem_ld16x2<16>(tmem + lane_off + 128 + cb, r);
+                    tmem_ld16x2<16>(tmem + lane_off + 256 + cb, r);
                     tmem_wait_ld();
                     if (split_exp)
                         p_block(r, cb + hc, [&](int i) { return et * sE[i]; });
@@ -688,15 +702,19 @@ __global__ void __launch_bounds__(NTS, 1) gdn_seq_kernel(const __grid_constant__
             ok = mbar_wait_bounded(&bar[kSbB1], ph, status) && ok;
             tc_fence_after();
             const float fc = ex2f(GC);
-            uint32_t r[32];
 #pragma unroll
             for (int cb = 0; cb < 64; cb += 32) {
-                tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 256 + cb, r);
+                uint32_t r[32], r2[32];
+                tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 384 + cb, r);
+                tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 448 + cb, r2);
                 tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) S[cb + j] = fmaf(fc, S[cb + j], __uint_as_float(r[j]));
+                for (int j = 0; j < 32; ++j)
+                    S[cb + j] = fmaf(fc, S[cb + j], __uint_as_float(r[j]) + __uint_as_float(r2[j]));
             }
-            // W S and Q S (A1, A2) are done: the copy for the next chunk
+            // W S (before K^T D') and Q S are done reading the copy: the
+            // copy for the next chunk
+            ok = mbar_wait_bounded(&bar[kSbA2], ph, status) && ok;
             if (u + 1 < nch) state_copy();
             fence_proxy_async_smem();
         }
@@ -719,6 +737,8 @@ __global__ void __launch_bounds__(NTS, 1) gdn_seq_kernel(const __grid_constant__
         mbar_wait_bounded(&bar[kSbDrain], 0, status);
     }
     if (warp == 9 && lane == 0) {
+        mma_commit(&bar[kSbDrain2]);
+        mbar_wait_bounded(&bar[kSbDrain2], 0, status);
         for (int c = max(0, loads - 2); c < loads; ++c)
             mbar_wait_bounded(&bar[kSbLd0 + (c & 1)], static_cast<uint32_t>((c >> 1) & 1), status);
     }
