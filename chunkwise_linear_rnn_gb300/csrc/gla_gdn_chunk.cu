@@ -84,74 +84,123 @@ __device__ __forceinline__ void chunk_gates(float *sG, float *sB, const float *g
 }
 
 // ------------------------------------------------------------------ WY pre-pass
-template <int DK>
 struct WySmem {
+    static constexpr int DK = 128;
+    static constexpr int LS = 68;                                // fp32 row stride (16-byte rows)
     static constexpr uint32_t kBlk = C * 128;                    // 64 rows x 64 bf16
-    static constexpr uint32_t kK = 0;                            // K [t][c] K-major, DK/64 blocks
-    static constexpr uint32_t kBKh = kK + (DK / 64) * kBlk;      // beta 2^G K [i][c] MN-major
-    static constexpr uint32_t kBKl = kBKh + (DK / 64) * kBlk;
-    static constexpr uint32_t kT = kBKl + (DK / 64) * kBlk;      // T [t][i] K-major, bf16
-    static constexpr uint32_t kL = kT + kBlk;                    // fp32 [64][65]: L, then T
-    static constexpr uint32_t kTf = kL + C * 65 * 4;
-    static constexpr uint32_t kX = kTf + C * 65 * 4;             // blocked inverse scratch [3][16][17]
-    static constexpr uint32_t kG = kX + 3 * 16 * 17 * 4;
+    static constexpr uint32_t kK = 0;                            // K [t][c] (2 channel blocks)
+    static constexpr uint32_t kTh = kK + 2 * kBlk;               // T diag(beta gamma) [t][i] K-major, hi
+    static constexpr uint32_t kTl = kTh + kBlk;                  // and lo
+    static constexpr uint32_t kL = kTl + kBlk;                   // fp32 [64][LS]: L
+    static constexpr uint32_t kTf = kL + C * LS * 4;             // fp32 [64][LS]: T
+    static constexpr uint32_t kX = kTf + C * LS * 4;             // level products [3][16][16]
+    static constexpr uint32_t kG = kX + 3 * 16 * 16 * 4;
     static constexpr uint32_t kBeta = kG + C * 4;
-    static constexpr uint32_t kBar = kBeta + C * 4;
+    static constexpr uint32_t kE = kBeta + C * 4;                // 2^-G per token
+    static constexpr uint32_t kBar = kE + C * 4;
     static constexpr uint32_t kSlot = kBar + 16;
     static constexpr uint32_t kBytes = kSlot + 16 + 1024;
-    static_assert(kBytes <= 113 * 1024, "two CTAs per SM");
+    static_assert(kBytes <= 75 * 1024, "three CTAs per SM");
 };
 
-
-// T = (I + L)^-1 for strictly lower L (64 x 64, row stride 65), by blocks of
-// 16: the four diagonal blocks by substitution (threads 0-63, one column
-// each), then level by level T_ba = -T_bb sum_{m=a}^{b-1} L_bm T_ma, one
-// thread per element of a 16 x 16 block.  Needs NT == 256.
+// T = (I + L)^-1 for strictly lower L (64 x 64 fp32, row stride LS), by blocks
+// of 16.  The four diagonal blocks by substitution, one column per thread
+// (threads 0-63), in registers; then level by level
+//     T_ba = -T_bb sum_{m=a}^{b-1} L_bm T_ma   (b = a + lev),
+// first X_a = sum_m L_bm T_ma, then -T_bb X_a, a thread per row and four
+// columns of a 16 x 16 block.  Only the blocks on and below the diagonal of
+// sTf are written.  Needs NT == 256.
 __device__ __forceinline__ void invert_unit_lower_blocked(const float *sL, float *sTf, float *sX) {
-    static_assert(NT == 256, "one thread per element of a 16 x 16 block");
+    static_assert(NT == 256, "64 threads per 16 x 16 block, up to three blocks");
+    constexpr int LS = WySmem::LS;
     const int tid = threadIdx.x;
-    for (int e = tid; e < C * 65; e += NT) sTf[e] = 0.f;
-    __syncthreads();
     if (tid < C) {
         const int o = (tid >> 4) * 16, j = tid & 15;
-        for (int i = j; i < 16; ++i) {
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = i == j ? 1.f : 0.f;
+#pragma unroll
+        for (int i = 1; i < 16; ++i) {
+            const float *row = sL + (o + i) * LS + o;
             float acc = 0.f;
-            for (int m = j; m < i; ++m) acc = fmaf(sL[(o + i) * 65 + o + m], sTf[(o + m) * 65 + o + j], acc);
-            sTf[(o + i) * 65 + o + j] = i == j ? 1.f : -acc;
+#pragma unroll
+            for (int m4 = 0; m4 < i; m4 += 4) {
+                const float4 l4 = *reinterpret_cast<const float4 *>(row + m4);
+                acc = fmaf(l4.x, x[m4], acc);
+                if (m4 + 1 < i) acc = fmaf(l4.y, x[m4 + 1], acc);
+                if (m4 + 2 < i) acc = fmaf(l4.z, x[m4 + 2], acc);
+                if (m4 + 3 < i) acc = fmaf(l4.w, x[m4 + 3], acc);
+            }
+            if (i > j) x[i] = -acc;
         }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) sTf[(o + i) * LS + o + j] = x[i];
     }
     __syncthreads();
-    const int r = tid >> 4, c = tid & 15;
+    const int blk = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
     for (int lev = 1; lev < 4; ++lev) {
-        for (int a = 0; a + lev < 4; ++a) {
-            const int b = a + lev;
-            float acc = 0.f;
-            for (int m = a * 16; m < b * 16; ++m) acc = fmaf(sL[(b * 16 + r) * 65 + m], sTf[m * 65 + a * 16 + c], acc);
-            sX[a * 272 + r * 17 + c] = acc;
+        const int a = blk, b = a + lev;
+        if (b < 4) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            const float *lrow = sL + (b * 16 + r) * LS;
+            for (int m = a * 16; m < b * 16; m += 4) {
+                const float4 l4 = *reinterpret_cast<const float4 *>(lrow + m);
+                const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float4 t4 = *reinterpret_cast<const float4 *>(sTf + (m + e) * LS + a * 16 + c4);
+                    acc.x = fmaf(lv[e], t4.x, acc.x);
+                    acc.y = fmaf(lv[e], t4.y, acc.y);
+                    acc.z = fmaf(lv[e], t4.z, acc.z);
+                    acc.w = fmaf(lv[e], t4.w, acc.w);
+                }
+            }
+            *reinterpret_cast<float4 *>(sX + a * 256 + r * 16 + c4) = acc;
         }
         __syncthreads();
-        for (int a = 0; a + lev < 4; ++a) {
-            const int b = a + lev;
-            float acc = 0.f;
-            for (int m = 0; m < 16; ++m) acc = fmaf(sTf[(b * 16 + r) * 65 + b * 16 + m], sX[a * 272 + m * 17 + c], acc);
-            sTf[(b * 16 + r) * 65 + a * 16 + c] = -acc;
+        if (b < 4) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            const float *trow = sTf + (b * 16 + r) * LS + b * 16;
+#pragma unroll
+            for (int m = 0; m < 16; m += 4) {
+                const float4 t4 = *reinterpret_cast<const float4 *>(trow + m);
+                const float tv[4] = {t4.x, t4.y, t4.z, t4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float4 x4 = *reinterpret_cast<const float4 *>(sX + a * 256 + (m + e) * 16 + c4);
+                    acc.x = fmaf(tv[e], x4.x, acc.x);
+                    acc.y = fmaf(tv[e], x4.y, acc.y);
+                    acc.z = fmaf(tv[e], x4.z, acc.z);
+                    acc.w = fmaf(tv[e], x4.w, acc.w);
+                }
+            }
+            *reinterpret_cast<float4 *>(sTf + (b * 16 + r) * LS + a * 16 + c4) =
+                make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
         }
         __syncthreads();
     }
 }
 
-// Grid (chunks per head, B*H).  W: [BH][nch*C][DK] bf16, U: [BH][nch*C][DV] fp32.
+// Grid (chunks per head, B*H), three CTAs per SM.  Per chunk: L from K K^T
+// (tensor cores), T = (I + L)^-1, then
+//   Tout = (T - I) diag(beta) (bf16, [BH][nch*C][64]): the off-diagonal part
+//          of T diag(beta), for U = beta v + (T - I) diag(beta) V;
+//   Wout = T diag(beta gamma) K (bf16, [BH][nch*C][DK]), from T diag(beta
+//          gamma) as a hi/lo pair times the raw K tile (tensor cores).
 template <int DK>
-__global__ void __launch_bounds__(NT, 2) gdn_wy_kernel(
+__global__ void __launch_bounds__(NT, 3) gdn_wy_kernel(
     const __nv_bfloat16 *__restrict__ k, const float *__restrict__ g,
     const float *__restrict__ beta, __nv_bfloat16 *__restrict__ Wout,
     __nv_bfloat16 *__restrict__ Tout, int T, unsigned int *status) {
-    using L = WySmem<DK>;
+    static_assert(DK == WySmem::DK, "dk = 128");
+    using L = WySmem;
+    constexpr int LS = L::LS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     float *sL = reinterpret_cast<float *>(sm + L::kL), *sTf = reinterpret_cast<float *>(sm + L::kTf);
     float *sG = reinterpret_cast<float *>(sm + L::kG), *sB = reinterpret_cast<float *>(sm + L::kBeta);
+    float *sE = reinterpret_cast<float *>(sm + L::kE);
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::kBar);
     uint32_t *slot = reinterpret_cast<uint32_t *>(sm + L::kSlot);
     const int u = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -167,30 +216,14 @@ __global__ void __launch_bounds__(NT, 2) gdn_wy_kernel(
         fence_mbar_init();
     }
     chunk_gates(sG, sB, g, beta, rg, n);
-    // K as bf16 [t][c] K-major (exact input)
+    // K as bf16 [t][c] K-major (exact input; rows past n zero)
     constexpr int KPER = C * DK / 8 / NT;
-    uint4 kraw[KPER];
 #pragma unroll
     for (int m = 0; m < KPER; ++m) {
         const int e = tid + m * NT, t = e / (DK / 8), c = (e % (DK / 8)) * 8;
-        kraw[m] = t < n ? *reinterpret_cast<const uint4 *>(k + rk + static_cast<size_t>(t) * DK + c)
-                        : make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4 *>(sm + L::kK + sw128_offset(t, c, L::kBlk)) = kraw[m];
-    }
-    __syncthreads();   // sG, sB
-    // beta 2^G K as a hi/lo pair, [i][c] (rows = tokens = K of the product)
-#pragma unroll
-    for (int m = 0; m < KPER; ++m) {
-        const int e = tid + m * NT, t = e / (DK / 8), c = (e % (DK / 8)) * 8;
-        const float f = sB[t] * exp2f(sG[t]);
-        const uint32_t w[4] = {kraw[m].x, kraw[m].y, kraw[m].z, kraw[m].w};
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            split_pair(__uint_as_float(w[j] << 16) * f, __uint_as_float(w[j] & 0xffff0000u) * f, hi[j], lo[j]);
-        const uint32_t off = sw128_offset(t, c, L::kBlk);
-        *reinterpret_cast<uint4 *>(sm + L::kBKh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4 *>(sm + L::kBKl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        const uint4 kr = t < n ? *reinterpret_cast<const uint4 *>(k + rk + static_cast<size_t>(t) * DK + c)
+                               : make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4 *>(sm + L::kK + sw128_offset(t, c, L::kBlk)) = kr;
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -209,70 +242,89 @@ __global__ void __launch_bounds__(NT, 2) gdn_wy_kernel(
         }
         mma_commit(&bar[0]);
     }
+    // 2^(G_t - G_i) = 2^G_t 2^-G_i while the chunk's total decay keeps 2^-G_i
+    // within 2^60 (G falls over the chunk); else one exponential per element
+    const bool split_exp = sG[C - 1] >= -60.f;
+    if (split_exp && tid < C) sE[tid] = exp2f(-sG[tid]);
     bool ok = mbar_wait_bounded(&bar[0], 0, status);
     tc_fence_after();
-    // L_ti = beta_t 2^(G_t - G_i) (k_t . k_i) for i < t; rows t = 16 q + lane (lanes 0-15)
+    __syncthreads();   // sE
+    // L_ti = beta_t 2^(G_t - G_i) (k_t . k_i) for i < t: warps 0-3, row
+    // t = 16 q + (lane & 15), 16 columns per half-split load
     if (warp < 4) {
-        const int t = 16 * warp + lane;
-        uint32_t r[32];
+        const int t = 16 * warp + (lane & 15), hc = (lane >> 4) * 16;
+        const float Gt = sG[t], bt = sB[t], rt = bt * exp2f(Gt);
 #pragma unroll 1
         for (int ib = 0; ib < C; ib += 32) {
-            tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + ib, r);
+            uint32_t r[16];
+            tmem_ld16x2<16>(tmem + (static_cast<uint32_t>(32 * warp) << 16) + ib, r);
             tmem_wait_ld();
-            if (lane < 16) {
+            float v[16];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int i = ib + j;
-                    sL[t * 65 + i] = (ok && i < t) ? sB[t] * exp2f(sG[t] - sG[i]) * __uint_as_float(r[j]) : 0.f;
-                }
+            for (int j = 0; j < 16; ++j) {
+                const int i = ib + hc + j;
+                const float f = split_exp ? rt * sE[i] : bt * exp2f(Gt - sG[i]);
+                v[j] = (ok && i < t) ? f * __uint_as_float(r[j]) : 0.f;
             }
+#pragma unroll
+            for (int j = 0; j < 16; j += 4)
+                *reinterpret_cast<float4 *>(sL + t * LS + ib + hc + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
         }
     }
     __syncthreads();
     invert_unit_lower_blocked(sL, sTf, reinterpret_cast<float *>(sm + L::kX));
-    // T as a single bf16 K-major tile [t][i] (for W), and (T - I) diag(beta)
-    // row-major to the scratch: U = T diag(beta) V is taken as beta_t v_t
-    // (exact, in fp32 where D is formed) plus (T - I) diag(beta) V
+    // T diag(beta gamma) as a hi/lo pair, K-major [t][i] (A of W), and
+    // (T - I) diag(beta) row-major to the scratch
     __nv_bfloat16 *tdst = Tout + orow * C;
-    for (int e = tid; e < C * C / 2; e += NT) {
-        const int t = e / (C / 2), i = (e % (C / 2)) * 2;
-        const float x0 = sTf[t * 65 + i], x1 = sTf[t * 65 + i + 1];
-        *reinterpret_cast<uint32_t *>(sm + L::kT + sw128_offset(t, i, L::kBlk)) = pack_bf16(x0, x1);
-        if (ok)
-            *reinterpret_cast<uint32_t *>(tdst + t * C + i) =
-                pack_bf16(i == t ? 0.f : x0 * sB[i], i + 1 == t ? 0.f : x1 * sB[i + 1]);
+#pragma unroll
+    for (int m = 0; m < C * C / 8 / NT; ++m) {
+        const int e = tid + m * NT, t = e / (C / 8), i0 = (e % (C / 8)) * 8;
+        uint32_t hi[4], lo[4], tb[4];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            const int i = i0 + 2 * x;
+            // blocks above the diagonal were never written: zero there
+            const bool low0 = (i >> 4) <= (t >> 4), low1 = ((i + 1) >> 4) <= (t >> 4);
+            const float x0 = low0 ? sTf[t * LS + i] : 0.f, x1 = low1 ? sTf[t * LS + i + 1] : 0.f;
+            split_pair(x0 * sB[i] * exp2f(sG[i]), x1 * sB[i + 1] * exp2f(sG[i + 1]), hi[x], lo[x]);
+            tb[x] = pack_bf16(i == t ? 0.f : x0 * sB[i], i + 1 == t ? 0.f : x1 * sB[i + 1]);
+        }
+        const uint32_t off = sw128_offset(t, i0, L::kBlk);
+        *reinterpret_cast<uint4 *>(sm + L::kTh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4 *>(sm + L::kTl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        if (ok) *reinterpret_cast<uint4 *>(tdst + t * C + i0) = make_uint4(tb[0], tb[1], tb[2], tb[3]);
     }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // W = T (beta 2^G K): M = 64, N = DK, K = 64
+    // W = (T diag(beta gamma)) K: M = 64, N = DK (two 64-channel blocks of
+    // the K tile, MN-major), K = 64 tokens; hi and lo of the left factor
     if (tid == 0) {
         constexpr uint32_t idw = idesc_bf16(64, DK, false, true);
 #pragma unroll
         for (int kk = 0; kk < C / 16; ++kk) {
-            const uint64_t at = sw128_desc(a0 + L::kT + kk * 32, 16, 1024);
-            const uint32_t om = kk * 2048;
-            mma_bf16_ss(tmem + 64, at, sw128_desc(a0 + L::kBKh + om, L::kBlk, 1024), idw, kk > 0 ? 1u : 0u);
-            mma_bf16_ss(tmem + 64, at, sw128_desc(a0 + L::kBKl + om, L::kBlk, 1024), idw, 1u);
+            const uint64_t bk = sw128_desc(a0 + L::kK + kk * 2048, L::kBlk, 1024);
+            mma_bf16_ss(tmem + 64, sw128_desc(a0 + L::kTh + kk * 32, 16, 1024), bk, idw, kk > 0 ? 1u : 0u);
+            mma_bf16_ss(tmem + 64, sw128_desc(a0 + L::kTl + kk * 32, 16, 1024), bk, idw, 1u);
         }
         mma_commit(&bar[1]);
     }
     ok = mbar_wait_bounded(&bar[1], 0, status) && ok;
     tc_fence_after();
-    // epilogue: warps 0-3 store W (bf16); row t = 16 q + lane
+    // epilogue: warps 0-3 store W (bf16), row t, 16 columns per half-split load
     if (warp < 4) {
-        const int t = 16 * warp + lane;
+        const int t = 16 * warp + (lane & 15), hc = (lane >> 4) * 16;
         const uint32_t lo_ = static_cast<uint32_t>(32 * warp) << 16;
-        uint32_t r[32];
 #pragma unroll 1
         for (int cb = 0; cb < DK; cb += 32) {
-            tmem_ld32(tmem + lo_ + 64 + cb, r);
+            uint32_t r[16];
+            tmem_ld16x2<16>(tmem + lo_ + 64 + cb, r);
             tmem_wait_ld();
-            if (lane < 16 && ok) {
-                __nv_bfloat16 *dst = Wout + (orow + t) * DK + cb;
+            if (ok) {
+                __nv_bfloat16 *dst = Wout + (orow + t) * DK + cb + hc;
 #pragma unroll
-                for (int j = 0; j < 32; j += 8)
+                for (int j = 0; j < 16; j += 8)
                     *reinterpret_cast<uint4 *>(dst + j) = make_uint4(
                         pack_bf16(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
                         pack_bf16(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])),
@@ -751,7 +803,7 @@ __global__ void __launch_bounds__(NTS, 1) gdn_seq_kernel(const __grid_constant__
 template <int DV>
 int launch_dv(const GdnChunkLaunch &p, cudaStream_t stream) {
     static bool attr_set = false;   // per instantiation, per process
-    const int s1 = static_cast<int>(WySmem<128>::kBytes);
+    const int s1 = static_cast<int>(WySmem::kBytes);
     const int s2 = static_cast<int>(SeqSmem::kBytes);
     if (!attr_set) {
         if (cudaFuncSetAttribute(gdn_wy_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
