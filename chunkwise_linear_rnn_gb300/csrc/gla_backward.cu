@@ -774,31 +774,32 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
     tc_fence_after();
 
     // epilogue 1: mask A and M to j <= t, split into bf16 pairs, [t][j] tiles.
-    // Warp q (= warp % 4) holds rows 16 q .. 16 q + 15 in lanes 0-15; warps 0-3 take
-    // A, warps 4-7 take M.
+    // Warp q (= warp % 4) holds rows 16 q .. 16 q + 15 in lanes 0-15 of its
+    // quarter, read with the half-split load: thread = row t and 16 columns of
+    // each 32-column block.  Warps 0-3 take A, warps 4-7 take M.
     {
-        const int q4 = warp & 3, t = 16 * q4 + lane;
+        const int q4 = warp & 3, t = 16 * q4 + (lane & 15), hc = (lane >> 4) * 16;
         const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
         const int col = warp < 4 ? 0 : 64;
-        const float mult = 1.f;
         uint8_t *th = sm + (warp < 4 ? L::kAh : L::kMh), *tl = sm + (warp < 4 ? L::kAl : L::kMl);
 #pragma unroll 1
         for (int jb = 0; jb < BC; jb += 32) {
-            uint32_t r[32];
-            tmem_ld32(tmem + lane_off + col + jb, r);
+            uint32_t r[16];
+            tmem_ld16x2<16>(tmem + lane_off + col + jb, r);
             tmem_wait_ld();
-            if (lane < 16) {
 #pragma unroll
-                for (int j = 0; j < 32; j += 2) {
-                    const int jj = jb + j;
-                    const float x0 = (jj <= t) ? __uint_as_float(r[j]) * mult : 0.f;
-                    const float x1 = (jj + 1 <= t) ? __uint_as_float(r[j + 1]) * mult : 0.f;
-                    uint32_t hi, lo;
-                    split_pair(x0, x1, hi, lo);
-                    const uint32_t off = sw128_offset(t, jj, L::kBlk);
-                    *reinterpret_cast<uint32_t *>(th + off) = hi;
-                    *reinterpret_cast<uint32_t *>(tl + off) = lo;
+            for (int j8 = 0; j8 < 16; j8 += 8) {
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    const int jj = jb + hc + j8 + 2 * x;
+                    const float x0 = (jj <= t) ? __uint_as_float(r[j8 + 2 * x]) : 0.f;
+                    const float x1 = (jj + 1 <= t) ? __uint_as_float(r[j8 + 2 * x + 1]) : 0.f;
+                    split_pair(x0, x1, hi[x], lo[x]);
                 }
+                const uint32_t off = sw128_offset(t, jb + hc + j8, L::kBlk);
+                *reinterpret_cast<uint4 *>(th + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4 *>(tl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
         }
     }
@@ -922,25 +923,26 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
     }
     __syncthreads();   // every thread is past the tile reads; P may overwrite the q/k tiles
 
-    // epilogue 2.  Warps 0-3: row t of dQ and dK (lanes 0-15), q dq - k dk into P.
-    // Warps 4-7: row j of dV.
+    // epilogue 2.  Warps 0-3: row t of dQ and dK, q dq - k dk into P.  Warps
+    // 4-7: row j of dV.  Thread = row t and 16 columns of each 32-column block
+    // (half-split loads, as in epilogue 1).
     float *sP = reinterpret_cast<float *>(sm + L::kQh);
     {
-        const int q4 = warp & 3, t = 16 * q4 + lane;
+        const int q4 = warp & 3, t = 16 * q4 + (lane & 15), hc = (lane >> 4) * 16;
         const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
-        const bool row_ok = ok && lane < 16 && t < n;
+        const bool row_ok = ok && t < n;
         if (warp < 4) {
             const float *gr = sG + t * LG;
 #pragma unroll 1
             for (int ib = 0; ib < DK; ib += 32) {
-                uint32_t rq[32], rkk[32];
-                tmem_ld32(tmem + lane_off + 128 + ib, rq);
-                tmem_ld32(tmem + lane_off + 128 + DK + ib, rkk);
+                uint32_t rq[16], rkk[16];
+                tmem_ld16x2<16>(tmem + lane_off + 128 + ib, rq);
+                tmem_ld16x2<16>(tmem + lane_off + 128 + DK + ib, rkk);
                 tmem_wait_ld();
-                if (lane < 16) {
+                {
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
-                        const int i = ib + j;
+                    for (int j = 0; j < 16; j += 4) {
+                        const int i = ib + hc + j;
                         float pr[4] = {0.f, 0.f, 0.f, 0.f};
                         if (row_ok) {
                             const size_t off = rk + static_cast<size_t>(t) * DK + i;
@@ -976,13 +978,13 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
 #pragma unroll 1
             for (int cb = 0; cb < DV; cb += 32) {
                 const uint32_t dcol = cb < 128 ? static_cast<uint32_t>(cb) : 128u + 2u * DK + (cb - 128);
-                uint32_t rv_[32];
-                tmem_ld32(tmem + lane_off + dcol, rv_);
+                uint32_t rv_[16];
+                tmem_ld16x2<16>(tmem + lane_off + dcol, rv_);
                 tmem_wait_ld();
                 if (row_ok) {
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
-                        const size_t off = rv + static_cast<size_t>(t) * DV + cb + j;
+                    for (int j = 0; j < 16; j += 4) {
+                        const size_t off = rv + static_cast<size_t>(t) * DV + cb + hc + j;
                         const uint32_t w0 = pack_bf16x2(s * __uint_as_float(rv_[j]),
                                                         s * __uint_as_float(rv_[j + 1]));
                         const uint32_t w1 = pack_bf16x2(s * __uint_as_float(rv_[j + 2]),
