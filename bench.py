@@ -59,8 +59,8 @@ def peaks():
 # one call) measured with ncu on the long workload (B2 H16 T32768 dk128 dv256)
 # at full size, with the kernel sources whose hash is given.  Any change to
 # those sources makes the figure stale: it is then reported as null.
-MEASURED_TRAFFIC = {"workload": "B2-H16-T32768-dk128-dv256", "sources": "1444bf3a00d01fcc",
-                    "bytes_per_call": 1615176192 + 509176832 + 35845376 + 2560}
+MEASURED_TRAFFIC = {"workload": "B2-H16-T32768-dk128-dv256", "sources": "cb518f4eacba22d7",
+                    "bytes_per_call": 1642675968 + 514746368}
 TRAFFIC_SOURCES = ["gla_api.cu", "gla_chunk.cu", "gla_chunk_kernel.cuh", "gla_internal.h", "gla_ptx.cuh"]
 
 
@@ -69,6 +69,16 @@ TRAFFIC_SOURCES = ["gla_api.cu", "gla_chunk.cu", "gla_chunk_kernel.cuh", "gla_in
 MEASURED_BWD_TRAFFIC = {"workload": "B2-H16-T32768-dk128-dv256", "sources": "8aba25f959ad8012",
                         "bytes_per_call": 25807910912}
 BWD_TRAFFIC_SOURCES = ["gla_api.cu", "gla_backward.cu", "gla_internal.h", "gla_ptx.cuh"]
+
+
+# ncu DRAM bytes (read + write) of one gla_gdn_chunk_fwd call (the WY pre-pass and
+# the sequential kernel) at the long shape B=2 H=16 T=32768 dk=128 dv=256, for the
+# sources hashed in "sources"; scaled by the heads a call covers (every head
+# streams its own rows and scratch once)
+MEASURED_GDN_CHUNK_TRAFFIC = {"T": 32768, "dk": 128, "dv": 256, "heads": 32,
+                              "sources": "ec01fba213eed766",
+                              "bytes_per_call": 277143296 + 347051264 + 1489058048 + 512030976}
+GDN_CHUNK_TRAFFIC_SOURCES = ["gla_gdn_chunk.cu", "gla_api.cu", "gla_internal.h", "gla_ptx.cuh"]
 
 
 # ncu DRAM bytes (read + write) of one gla_gdn_fwd launch, captured at B=1, H=8 of
@@ -128,6 +138,18 @@ def measured_gdn_traffic(cfg):
     except OSError:
         return None
     return m["bytes_per_launch"] * cfg.B * cfg.H // m["heads"]
+
+
+def measured_gdn_chunk_traffic(cfg):
+    m = MEASURED_GDN_CHUNK_TRAFFIC
+    if (cfg.T, cfg.dk, cfg.dv) != (m["T"], m["dk"], m["dv"]):
+        return None
+    try:
+        if kernel_sources_hash(GDN_CHUNK_TRAFFIC_SOURCES) != m["sources"]:
+            return None
+    except OSError:
+        return None
+    return m["bytes_per_call"] * cfg.B * cfg.H // m["heads"]
 
 
 def chunk_bytes(cfg, n_states: int | None = None, gate_per_head: bool = False) -> int:
@@ -760,10 +782,11 @@ def gdn_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_ki
                    "T": cfg.T, "dk": cfg.dk, "dv": cfg.dv, "replicas": world,
                    "l2": "inputs (%.2f GB) larger than L2; no flush" % (byts / 1e9)},
         "roofline": (roofline(byts, gdn_chunk_flops(cfg), per_call_ms / 1e3, pk, pk_kind) | {
-            "traffic": None, "traffic_unit": "DRAM bytes per call",
+            "traffic": measured_gdn_chunk_traffic(cfg), "traffic_unit": "DRAM bytes per call",
             "kernel": "gdn_wy_kernel + gdn_seq_kernel (chunked, two launches)",
             "note": "algorithmic bytes count the contract's inputs and outputs once; the WY "
-                    "pre-pass scratch (W, U) is extra traffic"}) if chunked else
+                    "pre-pass scratch (W and (T - I) diag(beta), written once and read by "
+                    "each value-column tile) is extra traffic"}) if chunked else
         {"bound": "alu", "achieved": achieved, "peak": FP32_SIMT_TFLOPS,
                      "unit": "TFLOP/s", "frac": achieved / FP32_SIMT_TFLOPS,
                      "traffic": measured_gdn_traffic(cfg), "traffic_unit": "DRAM bytes per launch",
