@@ -65,9 +65,12 @@ TRAFFIC_SOURCES = ["gla_api.cu", "gla_chunk.cu", "gla_chunk_kernel.cuh", "gla_in
 
 
 # ncu DRAM bytes (read + write) of one gla_chunk_bwd call on the long workload,
-# all six launches, for the backward sources hashed in "sources"
-MEASURED_BWD_TRAFFIC = {"workload": "B2-H16-T32768-dk128-dv256", "sources": "8aba25f959ad8012",
-                        "bytes_per_call": 25807910912}
+# all six launches, for the backward sources hashed in "sources": captured at
+# B=1 H=4 (2,048 chunks) and scaled by the chunks of the long workload (16,384;
+# every chunk's inputs, states and gradients move once per launch)
+MEASURED_BWD_TRAFFIC = {"workload": "B2-H16-T32768-dk128-dv256", "sources": "5ebca0514955477d",
+                        "bytes_per_call": 8 * (821_060_096 + 474_234_112 + 768_632_576
+                                               + 998_441_728 + 67_840 + 67_840)}
 BWD_TRAFFIC_SOURCES = ["gla_api.cu", "gla_backward.cu", "gla_internal.h", "gla_ptx.cuh"]
 
 
