@@ -55,23 +55,25 @@ def peaks():
 
 # --------------------------------------------------------------------------- workloads
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum, both launches of
-# one call) measured with ncu on the long workload (B2 H16 T32768 dk128 dv256)
-# at full size, with the kernel sources whose hash is given.  Any change to
-# those sources makes the figure stale: it is then reported as null.
-MEASURED_TRAFFIC = {"workload": "B2-H16-T32768-dk128-dv256", "sources": "cb518f4eacba22d7",
-                    "bytes_per_call": 1642675968 + 514746368}
-TRAFFIC_SOURCES = ["gla_api.cu", "gla_chunk.cu", "gla_chunk_kernel.cuh", "gla_internal.h", "gla_ptx.cuh"]
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the chunked
+# forward kernel's launch in one call (the FULL pass with the fused correction;
+# the small hT combine that follows it is not counted), measured with ncu on the
+# long workload (B2 H16 T32768 dk128 dv256) at full size, with the kernel
+# sources whose hash is given.  Any change to those sources makes the figure
+# stale: it is then reported as null.
+MEASURED_TRAFFIC = {"workload": "B2-H16-T32768-dk128-dv256", "sources": "25308919e11d6600",
+                    "bytes_per_call": 1642691328 + 514783232}
+TRAFFIC_SOURCES = ["gla_chunk.cu", "gla_chunk_kernel.cuh", "gla_ptx.cuh"]
 
 
 # ncu DRAM bytes (read + write) of one gla_chunk_bwd call on the long workload,
 # all six launches, for the backward sources hashed in "sources": captured at
 # B=1 H=4 (2,048 chunks) and scaled by the chunks of the long workload (16,384;
 # every chunk's inputs, states and gradients move once per launch)
-MEASURED_BWD_TRAFFIC = {"workload": "B2-H16-T32768-dk128-dv256", "sources": "5ebca0514955477d",
+MEASURED_BWD_TRAFFIC = {"workload": "B2-H16-T32768-dk128-dv256", "sources": "19637c16dfd6a354",
                         "bytes_per_call": 8 * (821_060_096 + 474_234_112 + 768_632_576
                                                + 998_441_728 + 67_840 + 67_840)}
-BWD_TRAFFIC_SOURCES = ["gla_api.cu", "gla_backward.cu", "gla_internal.h", "gla_ptx.cuh"]
+BWD_TRAFFIC_SOURCES = ["gla_backward.cu", "gla_ptx.cuh"]
 
 
 # ncu DRAM bytes (read + write) of one gla_gdn_chunk_fwd call (the WY pre-pass and
@@ -79,9 +81,9 @@ BWD_TRAFFIC_SOURCES = ["gla_api.cu", "gla_backward.cu", "gla_internal.h", "gla_p
 # sources hashed in "sources"; scaled by the heads a call covers (every head
 # streams its own rows and scratch once)
 MEASURED_GDN_CHUNK_TRAFFIC = {"T": 32768, "dk": 128, "dv": 256, "heads": 32,
-                              "sources": "ec01fba213eed766",
+                              "sources": "3a910b4716c3b498",
                               "bytes_per_call": 277143296 + 347051264 + 1489058048 + 512030976}
-GDN_CHUNK_TRAFFIC_SOURCES = ["gla_gdn_chunk.cu", "gla_api.cu", "gla_internal.h", "gla_ptx.cuh"]
+GDN_CHUNK_TRAFFIC_SOURCES = ["gla_gdn_chunk.cu", "gla_ptx.cuh"]
 
 
 # ncu DRAM bytes (read + write) of one gla_gdn_fwd launch, captured at B=1, H=8 of

@@ -26,7 +26,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgla.so")
 SOURCES = ["gla_api.cu", "gla_chunk.cu", "gla_chunk_packed.cu", "gla_chunk_scalar.cu",
            "gla_decode.cu", "gla_noalloc.cu", "gla_host.cu", "gla_backward.cu", "gla_gdn.cu",
-           "gla_gdn_chunk.cu"]
+           "gla_gdn_chunk.cu", "gla_chunk_debug.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-I", INCLUDE, "-I", CSRC]

@@ -217,6 +217,8 @@ int chunk_fwd_with_scratch(const void *q, const void *k, const void *v, const fl
     if (static_cast<long long>(B) * H > 0x7fffffffLL) return GLA_ERR_ARG;
     if (scratch && !aligned16(scratch)) return GLA_ERR_ARG;
     if (dbg && (dbg->withhold_v < 0 || (dbg->gamma && !aligned16(dbg->gamma)))) return GLA_ERR_ARG;
+    // the instrumented kernel build covers one gate per key channel only
+    if (dbg && opts && opts->gate_per_head) return GLA_ERR_ARG;
 
     DeviceInfo *dev = nullptr;
     int st = current_device(&dev);
@@ -282,6 +284,7 @@ int chunk_fwd_with_scratch(const void *q, const void *k, const void *v, const fl
     p.fuse = (pl.pair && pl.seg_max == 2 && pl.NC % pl.L == 0 && pl.NC / pl.L == 2) ? 1 : 0;
     p.status = dev->status;
     if (dbg) {
+        p.debug = 1;
         p.wait_ns = static_cast<unsigned long long>(dbg->wait_limit_us) * 1000ull;
         p.dbg_gamma = dbg->gamma;
         p.dbg_blk = dbg->block_len;

@@ -39,6 +39,7 @@ int chunk_fwd_max_resident(int dk, int dv_tile, int pair) {
 }
 
 int launch_chunk_fwd(const ChunkLaunch &p, cudaStream_t stream) {
+    if (p.debug) return launch_chunk_fwd_debug(p, stream);
     if (p.seqs) return launch_chunk_fwd_packed(p, stream);
     if (p.gate_per_head) return launch_chunk_fwd_scalar(p, stream);
     if (p.dk == 64) {

@@ -378,6 +378,14 @@ __device__ __forceinline__ void zero_p_block(uint32_t taddr) {
 
 // Test instrumentation: the in-chunk prefix sums of token t (of sequence u)
 // for channels ch and ch + 1, given in log2 units, stored in natural-log units.
+// The limit of every bounded wait: the library's, or (instrumented builds
+// only) the caller's shorter one.
+template <bool DBG>
+__device__ __forceinline__ unsigned long long wait_limit(const KParams &p) {
+    if constexpr (DBG) return p.wait_ns;
+    return kWaitLimitNs;
+}
+
 template <bool PACKED>
 __device__ __forceinline__ void dbg_gamma_pair(const KParams &p, int u, int t, int ch, float g0,
                                                float g1, int dk) {
@@ -395,7 +403,7 @@ __device__ __forceinline__ void dbg_gamma_pair(const KParams &p, int u, int t, i
 // `n` counts items; `last_flags` go to the chunk's last item; gtot0/gtot1
 // return the chunk's clamped Gamma at its end for the thread's channels (valid
 // in the last token part).  Returns false if a bounded wait expired.
-template <int DK, bool PACKED, bool SCALAR, bool FOLD, typename BeforeEmptyWait>
+template <int DK, bool PACKED, bool SCALAR, bool FOLD, bool DBG, typename BeforeEmptyWait>
 __device__ __forceinline__ bool sub_chunk_items(const KParams &p, int dbg_block, int bh, int t0,
                                                 int lc, bool store, int last_flags, int pt,
                                                 uint8_t *sQ,
@@ -463,15 +471,15 @@ __device__ __forceinline__ bool sub_chunk_items(const KParams &p, int dbg_block,
     }
     // cs == 1 always satisfies the bound: a single clamped gate is within it.
     const int n_sub = kChunk / cs;
-    const bool dbg = p.dbg_gamma != nullptr && (dbg_block == -1 || (ch >> 6) == dbg_block);
-    if (p.dbg_blk != nullptr && dbg_block != -2 && pt == 0) p.dbg_blk[sq.a + t0 / kChunk] = cs;
+    const bool dbg = DBG && p.dbg_gamma != nullptr && (dbg_block == -1 || (ch >> 6) == dbg_block);
+    if (DBG && p.dbg_blk != nullptr && dbg_block != -2 && pt == 0) p.dbg_blk[sq.a + t0 / kChunk] = cs;
     bool ok = true;
     for (int sidx = 0; sidx < n_sub; ++sidx) {
         const int sa = sidx * cs, sb = sa + cs;
         bool okw = true;
         if (sidx > 0) {
             before_empty_wait();
-            okw = mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status, p.wait_ns);
+            okw = mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status, wait_limit<DBG>(p));
         }
         ok = !bar_or(4, kPrepThreads, !okw);
         if (!ok) break;
@@ -553,7 +561,7 @@ __device__ __forceinline__ bool sub_chunk_items(const KParams &p, int dbg_block,
 // Threads pt < DK keep the decay since the segment start of channel pt; both
 // CTAs compute it from identical bits (the exchanged factor table, or the raw
 // gates), so their window decisions agree.
-template <int DK, int DVT, bool PACKED, bool SCALAR>
+template <int DK, int DVT, bool PACKED, bool SCALAR, bool DBG>
 __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint32_t rank,
                                           long long g_begin, long long g_end, size_t BHn,
                                           int dv_tile) {
@@ -632,7 +640,7 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
             // ---- phase A: prefix sums of this thread's part (log2 units) in
             // registers; the part total goes to the A tile's last row of the part
             if (pt == 0) mbar_arrive_expect_tx(&bars[kBarVerd0 + (lc & 1)], 4u);
-            ok &= mbar_wait_bounded(&bars[kBarAFull], lc & 1, p.status, p.wait_ns);
+            ok &= mbar_wait_bounded(&bars[kBarAFull], lc & 1, p.status, wait_limit<DBG>(p));
             spec = false;
             // rows past the sequence end (the tail of a packed sequence) count
             // as gate 0 and operands 0
@@ -691,7 +699,7 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
             }
             // ---- phase B into registers (values of a chunk that broke the
             // bound are computed but never used)
-            ok &= mbar_wait_bounded(&bars[kBarQkRaw], lc & 1, p.status, p.wait_ns);
+            ok &= mbar_wait_bounded(&bars[kBarQkRaw], lc & 1, p.status, wait_limit<DBG>(p));
 #pragma unroll
             for (int e = 0; e < TP; ++e) {
                 const int i = part * TP + e;
@@ -704,7 +712,7 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
                 const float g0 = o0 + av[e].x, g1 = o1 + av[e].y;
                 rq[e] = bf16x2_bits(qf.x * p.scale * ex2f(g0), qf.y * p.scale * ex2f(g1));
                 split_pair(kf.x * ex2f(-g0), kf.y * ex2f(-g1), rh[e], rl[e]);
-                if (p.dbg_gamma != nullptr) dbg_gamma_pair<PACKED>(p, bh, t0 + i, ch, g0, g1, DK);
+                if (DBG && p.dbg_gamma != nullptr) dbg_gamma_pair<PACKED>(p, bh, t0 + i, ch, g0, g1, DK);
             }
             gc0 = o0 + c0;                       // Gamma log2 e at the chunk end (last part)
             gc1 = o1 + c1;
@@ -737,7 +745,7 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
         // ---- segment decay through chunk c-1 (the previous exchange's factors)
         if (pend) {
             const int x = nx - 1;
-            ok &= mbar_wait_bounded(&bars[kBarXchg0 + (x & 1)], (x >> 1) & 1, p.status, p.wait_ns);
+            ok &= mbar_wait_bounded(&bars[kBarXchg0 + (x & 1)], (x >> 1) & 1, p.status, wait_limit<DBG>(p));
             if (pt < DK) gseg += __logf(sG[((n - 1) & 1) * DK + pt]);
             pend = false;
         }
@@ -754,13 +762,13 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
                                   : 0;
         // ---- both CTAs' verdicts: one branch for all threads, even for one
         // whose wait expired
-        ok &= mbar_wait_bounded(&bars[kBarVerd0 + (lc & 1)], (lc >> 1) & 1, p.status, p.wait_ns);
+        ok &= mbar_wait_bounded(&bars[kBarVerd0 + (lc & 1)], (lc >> 1) & 1, p.status, wait_limit<DBG>(p));
         const bool bad = bar_or(2, kPrepThreads, bad_here || sVerd[lc & 1] != 0u);
         prepped_last = false;
         ++used;
         if (!bad) {
             // ---- both CTAs' MMAs are done with the previous item's tiles
-            if (n > 0) ok &= mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status, p.wait_ns);
+            if (n > 0) ok &= mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status, wait_limit<DBG>(p));
 #pragma unroll
             for (int e = 0; e < TP; ++e) {
                 const uint32_t off = sw128_offset(part * TP + e, ch, kBlk);
@@ -775,7 +783,7 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
             fence_proxy_async_smem();
             named_barrier(5, kPrepThreads);
             if (pt == 0) {
-                if (p.dbg_blk != nullptr && rank == 0) p.dbg_blk[seq_of<PACKED>(p, bh).a + c] = kChunk;
+                if (DBG && p.dbg_blk != nullptr && rank == 0) p.dbg_blk[seq_of<PACKED>(p, bh).a + c] = kChunk;
                 sItem[n & 1] = ItemInfo{t0, 0, kChunk,
                                         kItemLast | (store ? kItemStore : 0) | piece_end, lc, nx,
                                         bh, 0};
@@ -796,9 +804,9 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
         } else {
             // ---- a chunk whose decay breaks the bound: sub-chunk items over all
             // channels, computed by each CTA of the pair on its own
-            if (n > 0) ok &= mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status, p.wait_ns);
+            if (n > 0) ok &= mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status, wait_limit<DBG>(p));
             float gt0 = 0.f, gt1 = 0.f;
-            ok &= sub_chunk_items<DK, PACKED, SCALAR, true>(p, static_cast<int>(rank), bh, t0, lc, store, piece_end, pt, sQ, sK, sKlo, sG, sItem,
+            ok &= sub_chunk_items<DK, PACKED, SCALAR, true, DBG>(p, static_cast<int>(rank), bh, t0, lc, store, piece_end, pt, sQ, sK, sKlo, sG, sItem,
                                       bars, n, gt0, gt1, [] {});
             if (pt < DK) {
                 // the chunk's clamped decay of channel pt, summed in token order
@@ -817,7 +825,7 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
             // ---- end of a FULL-pass piece: its decay, then the next piece
             if (pend) {
                 const int x = nx - 1;
-                ok &= mbar_wait_bounded(&bars[kBarXchg0 + (x & 1)], (x >> 1) & 1, p.status, p.wait_ns);
+                ok &= mbar_wait_bounded(&bars[kBarXchg0 + (x & 1)], (x >> 1) & 1, p.status, wait_limit<DBG>(p));
                 if (pt < DK) gseg += __logf(sG[((n - 1) & 1) * DK + pt]);
                 pend = false;
             }
@@ -849,28 +857,28 @@ __device__ __forceinline__ void prep_pair(const KParams &p, uint8_t *smem, uint3
     // ---- end of the item stream and of the load requests
     if (pend) {
         const int x = nx - 1;
-        ok &= mbar_wait_bounded(&bars[kBarXchg0 + (x & 1)], (x >> 1) & 1, p.status, p.wait_ns);
+        ok &= mbar_wait_bounded(&bars[kBarXchg0 + (x & 1)], (x >> 1) & 1, p.status, wait_limit<DBG>(p));
         if (pt < DK) gseg += __logf(sG[((n - 1) & 1) * DK + pt]);
     }
     // the peer's verdict for a chunk prepared here but not used has to land
     // before this CTA may exit
-    if (prepped_last) ok &= mbar_wait_bounded(&bars[kBarVerd0 + (lc_last & 1)], (lc_last >> 1) & 1, p.status, p.wait_ns);
+    if (prepped_last) ok &= mbar_wait_bounded(&bars[kBarVerd0 + (lc_last & 1)], (lc_last >> 1) & 1, p.status, wait_limit<DBG>(p));
     // the request mailbox holds one request: the end may be posted only once
     // the TMA thread has taken the last one (its A tile has landed)
-    if (spec) ok &= mbar_wait_bounded(&bars[kBarAFull], (lc_last + 1) & 1, p.status, p.wait_ns);
+    if (spec) ok &= mbar_wait_bounded(&bars[kBarAFull], (lc_last + 1) & 1, p.status, wait_limit<DBG>(p));
     named_barrier(5, kPrepThreads);
     if (pt == 0) {
         // the count of chunks used, so that no V load waits for a tile never freed
         sReq[0] = ChunkReq{used, 0, 1, 0};
         mbar_arrive(&bars[kBarReq]);
     }
-    if (n > 0 && !mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status, p.wait_ns)) ok = false;
+    if (n > 0 && !mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status, wait_limit<DBG>(p))) ok = false;
     if (pt == 0) sItem[n & 1] = ItemInfo{0, 0, 0, kItemEnd, 0, -1, 0, 0};
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars[kBarQkFull]);
 }
 
-template <int DK, int DVT, bool PAIR, bool PACKED, bool SCALAR>
+template <int DK, int DVT, bool PAIR, bool PACKED, bool SCALAR, bool DBG = false>
 __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_constant__ KParams p) {
     using L = Smem<DK, DVT, PAIR>;
     using TM = Tmem<DVT>;
@@ -943,7 +951,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
 
     if (warp < kPrepWarps && PAIR) {
         if constexpr (PAIR) {
-            prep_pair<DK, DVT, PACKED, SCALAR>(p, smem, rank, g_begin, g_end, BHn, dv_tile);
+            prep_pair<DK, DVT, PACKED, SCALAR, DBG>(p, smem, rank, g_begin, g_end, BHn, dv_tile);
         }
     } else if (warp < kPrepWarps) {
         // =========================================================== prep warps
@@ -989,7 +997,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             // ---- phase A (needs only the A tile, which arrives early): the
             // local prefix sum of this thread's part, written in place of A.
             constexpr int kB = 8;
-            bool okw = mbar_wait_bounded(&bars[kBarAFull], lc & 1, p.status, p.wait_ns);
+            bool okw = mbar_wait_bounded(&bars[kBarAFull], lc & 1, p.status, wait_limit<DBG>(p));
             ok = !bar_or(4, kPrepThreads, !okw);   // one verdict for all prep threads
             if (!ok) break;
             float c0 = 0.f, c1 = 0.f;
@@ -1048,7 +1056,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             const bool bad = bar_or(2, kPrepThreads,
                                     fmaxf(-fminf(gmin, 0.f), fmaxf(gmax, 0.f)) > kExpBound2 ||
                                         p.force_sub != 0);
-            okw = mbar_wait_bounded(&bars[kBarQkRaw], lc & 1, p.status, p.wait_ns);
+            okw = mbar_wait_bounded(&bars[kBarQkRaw], lc & 1, p.status, wait_limit<DBG>(p));
             ok = !bar_or(4, kPrepThreads, !okw);
             if (!ok) break;
             if (!bad) {
@@ -1095,7 +1103,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                     for (int e = 0; e < kB; ++e) {
                         const int i = i0 + e;
                         const float g0 = o0 + ca[e].x, g1 = o1 + ca[e].y;
-                        if (p.dbg_gamma != nullptr && dv_tile == 0)
+                        if (DBG && p.dbg_gamma != nullptr && dv_tile == 0)
                             dbg_gamma_pair<PACKED>(p, bh, t0 + i, ch, g0, g1, DK);
                         const float2 qf = unpack_bf16x2(cq[e]), kf = unpack_bf16x2(ck[e]);
                         const uint32_t off = sw128_offset(i, ch, kBlk);
@@ -1108,7 +1116,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                     }
                 }
                 if (pt == 0) {
-                    if (p.dbg_blk != nullptr && dv_tile == 0) p.dbg_blk[seq_of<PACKED>(p, bh).a + c] = kChunk;
+                    if (DBG && p.dbg_blk != nullptr && dv_tile == 0) p.dbg_blk[seq_of<PACKED>(p, bh).a + c] = kChunk;
                     sItem[n & 1] = ItemInfo{t0, 0, kChunk,
                                             kItemLast | (store ? kItemStore : 0) | piece_end, lc,
                                             -1, bh, 0};
@@ -1121,7 +1129,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             }
             // ---- sub-chunk rescaling (chunks whose decay exceeds the bound)
             float gtot0 = 0.f, gtot1 = 0.f;
-            ok = sub_chunk_items<DK, PACKED, SCALAR, false>(p, dv_tile == 0 ? -1 : -2, bh, t0, lc, store, piece_end, pt, sQ, sK, sKlo, sG, sItem,
+            ok = sub_chunk_items<DK, PACKED, SCALAR, false, DBG>(p, dv_tile == 0 ? -1 : -2, bh, t0, lc, store, piece_end, pt, sQ, sK, sKlo, sG, sItem,
                                      bars, n, gtot0, gtot1, [] {});
             if (last_part) {
                 gseg0 += gtot0;
@@ -1141,7 +1149,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             sReq[0] = ChunkReq{0, n, 1, 0};
             mbar_arrive(&bars[kBarReq]);
         }
-        if (n > 0 && !mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status, p.wait_ns)) ok = false;
+        if (n > 0 && !mbar_wait_bounded(&bars[kBarQkEmpty], (n - 1) & 1, p.status, wait_limit<DBG>(p))) ok = false;
         if (pt == 0) sItem[n & 1] = ItemInfo{0, 0, 0, kItemEnd, 0, -1, 0, 0};
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kBarQkFull]);
@@ -1233,7 +1241,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                     const int t0 = t0s[n_v & 3], bh = bhs[n_v & 3];
                     const int slot = n_v % VS;
                     uint8_t *dst = sV + slot * L::kVBytes;
-                    if (p.mode == kModeFull && n_v + 1 == p.withhold_v) {
+                    if (DBG && p.mode == kModeFull && n_v + 1 == p.withhold_v) {
                         // test instrumentation: this tile is never loaded (and
                         // its barrier never armed), so its waiters time out
                         withheld = n_v;
@@ -1254,7 +1262,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                     const unsigned long long now = global_timer_ns();
                     if (idle_since == 0) {
                         idle_since = now;
-                    } else if (now - idle_since > p.wait_ns) {
+                    } else if (now - idle_since > wait_limit<DBG>(p)) {
                         atomicOr(p.status, kStatusTimeout);
                         break;
                     }
@@ -1264,12 +1272,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             // loads issued for chunks that were never used must land before exit
             // (the last phase of each barrier; no later phase follows)
             if (n_req > 0) {
-                mbar_wait_bounded(&bars[kBarAFull], (n_req - 1) & 1, p.status, p.wait_ns);
-                if (PAIR) mbar_wait_bounded(&bars[kBarQkRaw], (n_req - 1) & 1, p.status, p.wait_ns);
+                mbar_wait_bounded(&bars[kBarAFull], (n_req - 1) & 1, p.status, wait_limit<DBG>(p));
+                if (PAIR) mbar_wait_bounded(&bars[kBarQkRaw], (n_req - 1) & 1, p.status, wait_limit<DBG>(p));
             }
             for (int j = n_v - VS < 0 ? 0 : n_v - VS; j < n_v; ++j)
                 if (j != withheld)
-                    mbar_wait_bounded(&bars[kBarVFull0 + j % VS], (j / VS) & 1, p.status, p.wait_ns);
+                    mbar_wait_bounded(&bars[kBarVFull0 + j % VS], (j / VS) & 1, p.status, wait_limit<DBG>(p));
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
@@ -1281,7 +1289,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aKlo = smem_u32(sKlo);
             const uint32_t aV0 = smem_u32(sV), aS = smem_u32(sS);
             for (int n = 0;; ++n) {
-                if (!mbar_wait_bounded(&bars[kBarQkFull], n & 1, p.status, p.wait_ns)) break;
+                if (!mbar_wait_bounded(&bars[kBarQkFull], n & 1, p.status, wait_limit<DBG>(p))) break;
                 const ItemInfo it = sItem[n & 1];
                 mbar_arrive(&bars[kBarItem0 + (n & 1)]);
                 if (it.flags & kItemEnd) break;
@@ -1304,7 +1312,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                 };
                 // a CTA pair's item: the peer's half of the operand tiles first
                 if (PAIR && it.xi >= 0) {
-                    if (!mbar_wait_bounded(&bars[kBarXchg0 + (it.xi & 1)], (it.xi >> 1) & 1, p.status, p.wait_ns))
+                    if (!mbar_wait_bounded(&bars[kBarXchg0 + (it.xi & 1)], (it.xi >> 1) & 1, p.status, wait_limit<DBG>(p)))
                         break;
                     tc_fence_after();
                 }
@@ -1314,8 +1322,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                 // O = Qh S_prev: needs this O buffer drained and the previous
                 // state scaled and copied
                 bool okw = true;
-                if (n >= 2) okw &= mbar_wait_bounded(&bars[kBarOFree0 + ob], ((n >> 1) + 1) & 1, p.status, p.wait_ns);
-                okw &= mbar_wait_bounded(&bars[kBarSReady], n & 1, p.status, p.wait_ns);
+                if (n >= 2) okw &= mbar_wait_bounded(&bars[kBarOFree0 + ob], ((n >> 1) + 1) & 1, p.status, wait_limit<DBG>(p));
+                okw &= mbar_wait_bounded(&bars[kBarSReady], n & 1, p.status, wait_limit<DBG>(p));
                 if (!okw) break;
                 tc_fence_after();
 #pragma unroll
@@ -1325,7 +1333,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                                 sw128_desc(aS + ks * 2048, L::kSBlk, 1024), id_ov, ks > 0);
                 }
                 // S += (Kh_hi + Kh_lo)^T V
-                if (!mbar_wait_bounded(&bars[kBarVFull0 + it.lc % VS], (it.lc / VS) & 1, p.status, p.wait_ns))
+                if (!mbar_wait_bounded(&bars[kBarVFull0 + it.lc % VS], (it.lc / VS) & 1, p.status, wait_limit<DBG>(p)))
                     break;
                 tc_fence_after();
 #pragma unroll
@@ -1341,7 +1349,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
                 else
                     mma_commit(&bars[kBarQkEmpty]);
                 // O += (P_hi + P_lo) V, P from TMEM
-                if (!mbar_wait_bounded(&bars[kBarPSplit], n & 1, p.status, p.wait_ns)) break;
+                if (!mbar_wait_bounded(&bars[kBarPSplit], n & 1, p.status, wait_limit<DBG>(p))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < kChunk / 16; ++ks) {
@@ -1355,7 +1363,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             // every product issued here is complete before TMEM is freed (a
             // stream that ended on an expired wait may leave some in flight)
             mma_commit(&bars[kBarDrain]);
-            mbar_wait_bounded(&bars[kBarDrain], 0, p.status, p.wait_ns);
+            mbar_wait_bounded(&bars[kBarDrain], 0, p.status, wait_limit<DBG>(p));
         }
         __syncwarp();
     } else {
@@ -1477,14 +1485,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             // (one barrier per item parity, so that the MMA issuer may run up
             // to two items ahead of these warps)
             if (!__all_sync(0xffffffffu,
-                            mbar_wait_bounded(&bars[kBarItem0 + (n & 1)], (n >> 1) & 1, p.status, p.wait_ns)))
+                            mbar_wait_bounded(&bars[kBarItem0 + (n & 1)], (n >> 1) & 1, p.status, wait_limit<DBG>(p))))
                 break;
             const ItemInfo it = sItem[n & 1];
             if (it.flags & kItemEnd) break;
             const int ob = n & 1;
             // ---- causal mask of P (row i), split into the TMEM A operand of P V
             {
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarPFull], n & 1, p.status, p.wait_ns)))
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarPFull], n & 1, p.status, wait_limit<DBG>(p))))
                     break;
                 tc_fence_after();
                 // This warp's rows are 32 wq .. 32 wq + 31: column blocks past
@@ -1538,12 +1546,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             const bool piece_end = (it.flags & kItemPieceEnd) != 0;
             const bool keep = (it.flags & kItemKeep) != 0;
             auto state_step = [&]() -> bool {
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarSDone], n & 1, p.status, p.wait_ns)))
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarSDone], n & 1, p.status, wait_limit<DBG>(p))))
                     return false;
                 // a CTA pair's item: the peer's half of the state factors
                 if (it.xi >= 0 &&
                     !__all_sync(0xffffffffu, mbar_wait_bounded(&bars[kBarXchg0 + (it.xi & 1)],
-                                                               (it.xi >> 1) & 1, p.status, p.wait_ns)))
+                                                               (it.xi >> 1) & 1, p.status, wait_limit<DBG>(p))))
                     return false;
                 tc_fence_after();
                 if (has_state_row) {
@@ -1592,7 +1600,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fwd_kernel(const __grid_con
             };
             auto output_step = [&]() -> bool {
                 if (!__all_sync(0xffffffffu,
-                                mbar_wait_bounded(&bars[kBarOFull0 + ob], (n >> 1) & 1, p.status, p.wait_ns)))
+                                mbar_wait_bounded(&bars[kBarOFull0 + ob], (n >> 1) & 1, p.status, wait_limit<DBG>(p))))
                     return false;
                 tc_fence_after();
                 // staged in the state copy: the V tile is free now
@@ -1696,10 +1704,10 @@ __global__ void __launch_bounds__(256) two_segment_states_kernel(const float *__
     }
 }
 
-template <int DK, int DVT, bool PAIR, bool PACKED, bool SCALAR>
+template <int DK, int DVT, bool PAIR, bool PACKED, bool SCALAR, bool DBG = false>
 int launch_tiles(const ChunkLaunch &c, cudaStream_t stream) {
     using L = Smem<DK, DVT, PAIR>;
-    auto kern = chunk_fwd_kernel<DK, DVT, PAIR, PACKED, SCALAR>;
+    auto kern = chunk_fwd_kernel<DK, DVT, PAIR, PACKED, SCALAR, DBG>;
     static bool attr_set = false;  // per instantiation, per process
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -44,7 +44,10 @@ struct ChunkLaunch {
     // kernel forms hT (no correction pass)
     int fuse;
     unsigned int *status;     // device status word
-    // test instrumentation (gla_chunk_fwd_debug; zero / null otherwise)
+    // test instrumentation (gla_chunk_fwd_debug; zero / null otherwise).  A
+    // call with `debug` set runs the instrumented kernel build, which alone
+    // reads the fields below; production calls run a build without them.
+    int debug;
     unsigned long long wait_ns;   // bounded-wait limit (0 = the default, 2 s)
     float *dbg_gamma;         // [rows, dk] in-chunk prefix sums the preparation used, or null
     int *dbg_blk;             // block length of every chunk (global chunk index), or null
@@ -53,6 +56,10 @@ struct ChunkLaunch {
 
 // Returns a cudaError_t value (0 on success).
 int launch_chunk_fwd(const ChunkLaunch &p, cudaStream_t stream);
+
+// launch_chunk_fwd with the instrumented kernel build (p.debug set; fixed-length
+// batches, one gate per key channel); gla_chunk_debug.cu.
+int launch_chunk_fwd_debug(const ChunkLaunch &p, cudaStream_t stream);
 
 // launch_chunk_fwd for a packed batch (p.seqs set); gla_chunk_packed.cu.
 int launch_chunk_fwd_packed(const ChunkLaunch &p, cudaStream_t stream);

@@ -196,7 +196,12 @@ int gla_chunk_fwd_plan(int B, int H, int T, int dk, int dv, const gla_chunk_opti
  *                   GLA_OK (it was enqueued); gla_last_device_status then
  *                   reports GLA_ERR_TIMEOUT, and the outputs are undefined.
  *
- * Returns as gla_chunk_fwd_ex, and GLA_ERR_ARG for a negative withhold_v.
+ * With dbg non-NULL the call runs an instrumented build of the kernel (the
+ * production entry points run a build without any of this); it covers one
+ * gate per key channel, so opts->gate_per_head must be 0.
+ *
+ * Returns as gla_chunk_fwd_ex, and GLA_ERR_ARG for a negative withhold_v or
+ * gate_per_head set.
  */
 typedef struct gla_chunk_debug {
     float *gamma;
