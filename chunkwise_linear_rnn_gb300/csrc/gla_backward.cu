@@ -163,10 +163,19 @@ __device__ __forceinline__ void load_prefix(float *sG, const float *__restrict__
     }
     __syncthreads();
     if (threadIdx.x < DK) {
+        // 16 rows' loads in flight at a time, then their running sums (the
+        // same order of additions as one row at a time)
         float acc = 0.f;
-        for (int t = 0; t < BC; ++t) {
-            acc += sG[t * LD + threadIdx.x];
-            sG[t * LD + threadIdx.x] = acc;
+#pragma unroll
+        for (int t0 = 0; t0 < BC; t0 += 16) {
+            float x[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) x[j] = sG[(t0 + j) * LD + threadIdx.x];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                acc += x[j];
+                sG[(t0 + j) * LD + threadIdx.x] = acc;
+            }
         }
     }
     __syncthreads();
@@ -998,12 +1007,23 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, L::kCols);
-    // dlog_alpha = carry + reverse in-chunk sum of q dq - k dk
+    // dlog_alpha = carry + reverse in-chunk sum of q dq - k dk (16 rows' loads
+    // in flight at a time; rows past n hold zeros and are not stored)
     if (tid < DK) {
         float acc = sCarry[tid];
-        for (int t = n - 1; t >= 0; --t) {
-            acc += sP[t * LP + tid];
-            p.ga[rk + static_cast<size_t>(t) * DK + tid] = acc;
+#pragma unroll
+        for (int t1 = BC; t1 > 0; t1 -= 16) {
+            float x[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) x[j] = sP[(t1 - 1 - j) * LP + tid];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int t = t1 - 1 - j;
+                if (t < n) {
+                    acc += x[j];
+                    p.ga[rk + static_cast<size_t>(t) * DK + tid] = acc;
+                }
+            }
         }
     }
 }
