@@ -143,15 +143,22 @@ __device__ __forceinline__ size_t slot_index(long long base, int i, int c, int u
 // Load one chunk of log-gates (log2 units, rows past the sequence end zero,
 // so the prefix sum stays flat there) and take the inclusive prefix sum per
 // channel.  sG is [BC][LD].  All loads are issued before the first use.
-template <int DK, int LD, int NTH = NT>
-__device__ __forceinline__ void load_prefix(float *sG, const float *__restrict__ la, int n) {
+// prefix_issue loads this thread's share into registers; prefix_finish stores
+// it (log2 units) and scans.
+template <int DK, int NTH>
+__device__ __forceinline__ void prefix_issue(float4 (&r)[BC * DK / 4 / NTH], const float *__restrict__ la,
+                                             int n) {
     constexpr int PER = BC * DK / 4 / NTH;
-    float4 r[PER];
 #pragma unroll
     for (int m = 0; m < PER; ++m) {
         const int e = (threadIdx.x + m * NTH) * 4, t = e / DK;
         r[m] = t < n ? *reinterpret_cast<const float4 *>(la + e) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+}
+
+template <int DK, int LD, int NTH>
+__device__ __forceinline__ void prefix_finish(float *sG, const float4 (&r)[BC * DK / 4 / NTH]) {
+    constexpr int PER = BC * DK / 4 / NTH;
 #pragma unroll
     for (int m = 0; m < PER; ++m) {
         const int e = (threadIdx.x + m * NTH) * 4, t = e / DK, i = e % DK;
@@ -179,6 +186,13 @@ __device__ __forceinline__ void load_prefix(float *sG, const float *__restrict__
         }
     }
     __syncthreads();
+}
+
+template <int DK, int LD, int NTH = NT>
+__device__ __forceinline__ void load_prefix(float *sG, const float *__restrict__ la, int n) {
+    float4 r[BC * DK / 4 / NTH];
+    prefix_issue<DK, NTH>(r, la, n);
+    prefix_finish<DK, LD, NTH>(sG, r);
 }
 
 // ---------------------------------------------------------------------------
@@ -692,7 +706,14 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
     const size_t rv = static_cast<size_t>(ck.row) * DV;   // first row, value-side tensors
     const float s = p.scale;
 
-    // loads first: q, k pairs and dO, V 16-byte groups; then the prefix sums
+    // loads first: the gates and the log-gate carries (the prefix sums need them
+    // first), then q, k pairs and dO, V 16-byte groups; then the prefix sums
+    float4 gr[BC * DK / 4 / NTI];
+    prefix_issue<DK, NTI>(gr, p.log_alpha + rk, n);
+    float cr[NTILE];
+#pragma unroll
+    for (int x = 0; x < NTILE; ++x)
+        cr[x] = tid < DK ? p.carry[(static_cast<size_t>(ck.w.rbase + u) * NTILE + x) * DK + tid] : 0.f;
     constexpr int QPER = BC * DK / 2 / NTI, VPER = BC * DV / 8 / NTI;
     uint32_t qr[QPER], kr[QPER];
     uint4 dor[VPER], vr[VPER];
@@ -709,7 +730,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
         dor[m] = t < n ? *reinterpret_cast<const uint4 *>(p.d_o + off) : make_uint4(0u, 0u, 0u, 0u);
         vr[m] = t < n ? *reinterpret_cast<const uint4 *>(p.v + off) : make_uint4(0u, 0u, 0u, 0u);
     }
-    load_prefix<DK, LG, NTI>(sG, p.log_alpha + rk, n);
+    prefix_finish<DK, LG, NTI>(sG, gr);
     int wide = 0;
     if (tid < DK) {
         const float g0 = sG[tid], gl = sG[(BC - 1) * LG + tid];
@@ -717,8 +738,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
         sGC[tid] = gl;
         wide = (g0 - gl) > kMaxSpan;
         float c = 0.f;
-        for (int x = 0; x < NTILE; ++x)
-            c += p.carry[(static_cast<size_t>(ck.w.rbase + u) * NTILE + x) * DK + tid];
+#pragma unroll
+        for (int x = 0; x < NTILE; ++x) c += cr[x];
         sCarry[tid] = c;
     }
     const bool exact = __syncthreads_or(wide) || p.force_exact;
@@ -941,46 +962,56 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
         const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
         const bool row_ok = ok && t < n;
         if (warp < 4) {
-            const float *gr = sG + t * LG;
-#pragma unroll 1
-            for (int ib = 0; ib < DK; ib += 32) {
+            const float *grow = sG + t * LG;
+            // this thread's 64 columns of q and k (16 per 32-column block), in
+            // one batch of loads
+            uint4 qv4[DK / 32][2], kv4[DK / 32][2];
+#pragma unroll
+            for (int b = 0; b < DK / 32; ++b)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const size_t off = rk + static_cast<size_t>(t) * DK + b * 32 + hc + h * 8;
+                    qv4[b][h] = row_ok ? *reinterpret_cast<const uint4 *>(p.q + off) : make_uint4(0u, 0u, 0u, 0u);
+                    kv4[b][h] = row_ok ? *reinterpret_cast<const uint4 *>(p.k + off) : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+            for (int b = 0; b < DK / 32; ++b) {
+                const int ib = b * 32;
                 uint32_t rq[16], rkk[16];
                 tmem_ld16x2<16>(tmem + lane_off + 128 + ib, rq);
                 tmem_ld16x2<16>(tmem + lane_off + 128 + DK + ib, rkk);
                 tmem_wait_ld();
-                {
 #pragma unroll
-                    for (int j = 0; j < 16; j += 4) {
-                        const int i = ib + hc + j;
-                        float pr[4] = {0.f, 0.f, 0.f, 0.f};
-                        if (row_ok) {
-                            const size_t off = rk + static_cast<size_t>(t) * DK + i;
-                            const uint2 qv = *reinterpret_cast<const uint2 *>(p.q + off);
-                            const uint2 kv = *reinterpret_cast<const uint2 *>(p.k + off);
-                            const float qa[4] = {__uint_as_float(qv.x << 16), __uint_as_float(qv.x & 0xffff0000u),
-                                                 __uint_as_float(qv.y << 16), __uint_as_float(qv.y & 0xffff0000u)};
-                            const float ka[4] = {__uint_as_float(kv.x << 16), __uint_as_float(kv.x & 0xffff0000u),
-                                                 __uint_as_float(kv.y << 16), __uint_as_float(kv.y & 0xffff0000u)};
-                            uint32_t dqw[2], dkw[2];
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t qw[4] = {qv4[b][h].x, qv4[b][h].y, qv4[b][h].z, qv4[b][h].w};
+                    const uint32_t kw[4] = {kv4[b][h].x, kv4[b][h].y, kv4[b][h].z, kv4[b][h].w};
+                    uint32_t dqw[4], dkw[4];
+                    float pr[8];
 #pragma unroll
-                            for (int h = 0; h < 4; h += 2) {
-                                float dqv[2], dkv[2];
+                    for (int x = 0; x < 8; x += 2) {
+                        const int j = h * 8 + x, i = ib + hc + j;
+                        float dqv[2], dkv[2];
 #pragma unroll
-                                for (int x = 0; x < 2; ++x) {
-                                    const float d = gr[i + h + x] - sRef[i + h + x];
-                                    dqv[x] = s * exp2f(d) * __uint_as_float(rq[j + h + x]);
-                                    dkv[x] = s * exp2f(-d) * __uint_as_float(rkk[j + h + x]);
-                                    pr[h + x] = qa[h + x] * dqv[x] - ka[h + x] * dkv[x];
-                                }
-                                dqw[h / 2] = pack_bf16x2(dqv[0], dqv[1]);
-                                dkw[h / 2] = pack_bf16x2(dkv[0], dkv[1]);
-                            }
-                            *reinterpret_cast<uint2 *>(p.gq + off) = make_uint2(dqw[0], dqw[1]);
-                            *reinterpret_cast<uint2 *>(p.gk + off) = make_uint2(dkw[0], dkw[1]);
+                        for (int y = 0; y < 2; ++y) {
+                            const float d = grow[i + y] - sRef[i + y];
+                            dqv[y] = s * exp2f(d) * __uint_as_float(rq[j + y]);
+                            dkv[y] = s * exp2f(-d) * __uint_as_float(rkk[j + y]);
                         }
-#pragma unroll
-                        for (int x = 0; x < 4; ++x) sP[t * LP + i + x] = pr[x];
+                        const float q0 = __uint_as_float(qw[x / 2] << 16), q1 = __uint_as_float(qw[x / 2] & 0xffff0000u);
+                        const float k0 = __uint_as_float(kw[x / 2] << 16), k1 = __uint_as_float(kw[x / 2] & 0xffff0000u);
+                        pr[x] = q0 * dqv[0] - k0 * dkv[0];
+                        pr[x + 1] = q1 * dqv[1] - k1 * dkv[1];
+                        dqw[x / 2] = pack_bf16x2(dqv[0], dqv[1]);
+                        dkw[x / 2] = pack_bf16x2(dkv[0], dkv[1]);
                     }
+                    const int i0 = ib + hc + h * 8;
+                    if (row_ok) {
+                        const size_t off = rk + static_cast<size_t>(t) * DK + i0;
+                        *reinterpret_cast<uint4 *>(p.gq + off) = make_uint4(dqw[0], dqw[1], dqw[2], dqw[3]);
+                        *reinterpret_cast<uint4 *>(p.gk + off) = make_uint4(dkw[0], dkw[1], dkw[2], dkw[3]);
+                    }
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) sP[t * LP + i0 + x] = row_ok ? pr[x] : 0.f;
                 }
             }
         } else {
