@@ -679,10 +679,14 @@ struct IntraSmem {
     static constexpr uint32_t kSlot = kBar + 16;
     static constexpr uint32_t kBytes = kSlot + 16 + 1024;
     static constexpr int LP = DK + 1;                       // q dq - k dk, fp32 [BC][LP], over Qh..Kl
+    // the gradient epilogue's raw q and k rows, bf16 [BC][DK] each, over the
+    // dO, V and A/M tiles (free once the state products are done)
+    static constexpr uint32_t kQr = kDo, kKr = kQr + BC * DK * 2;
     // TMEM columns used: A, M / dV first half [0, 128), dQ, dK, then dV's second half
     static constexpr uint32_t kUsed = 128 + 2 * DK + (DV > 128 ? 128 : 0);
     static constexpr uint32_t kCols = kUsed <= 256 ? 256 : 512;
     static_assert(BC * LP * 4 <= 4 * (DK / 64) * kBlk, "P fits over the q/k tiles");
+    static_assert(kKr + BC * DK * 2 <= kMl + kBlk, "raw q, k fit over the dO, V and A/M tiles");
 };
 
 // Columns: A [0, 64), M [64, 128) first; then dV over [0, 128) (+ [2 dk + 128, ...) for
@@ -749,6 +753,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
     if (warp == 0) tmem_alloc(slot, L::kCols);
     if (tid == 0) {
         mbar_init(bar, 1);
+        mbar_init(bar + 1, 1);   // the raw q, k rows of the epilogue
         fence_mbar_init();
     }
     // Qh, Kh (hi/lo) as [t][i] tiles; dO, V as [t][c] tiles
@@ -951,6 +956,14 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
             tc_fence_after();
         }
     }
+    // every state product is done: the chunk's raw q and k rows load over the
+    // dO, V and A/M tiles for the gradient epilogue, while the epilogue starts
+    if (tid == 0) {
+        const uint32_t bytes = static_cast<uint32_t>(n) * DK * 2;
+        mbar_arrive_expect_tx(bar + 1, 2 * bytes);
+        bulk_load(sm + L::kQr, p.q + rk, bytes, bar + 1);
+        bulk_load(sm + L::kKr, p.k + rk, bytes, bar + 1);
+    }
     __syncthreads();   // every thread is past the tile reads; P may overwrite the q/k tiles
 
     // epilogue 2.  Warps 0-3: row t of dQ and dK, q dq - k dk into P.  Warps
@@ -963,17 +976,10 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
         const bool row_ok = ok && t < n;
         if (warp < 4) {
             const float *grow = sG + t * LG;
-            // this thread's 64 columns of q and k (16 per 32-column block), in
-            // one batch of loads
-            uint4 qv4[DK / 32][2], kv4[DK / 32][2];
-#pragma unroll
-            for (int b = 0; b < DK / 32; ++b)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const size_t off = rk + static_cast<size_t>(t) * DK + b * 32 + hc + h * 8;
-                    qv4[b][h] = row_ok ? *reinterpret_cast<const uint4 *>(p.q + off) : make_uint4(0u, 0u, 0u, 0u);
-                    kv4[b][h] = row_ok ? *reinterpret_cast<const uint4 *>(p.k + off) : make_uint4(0u, 0u, 0u, 0u);
-                }
+            // this thread's q and k columns from the rows loaded above (rows
+            // past n were not loaded; their results are not used)
+            const bool qk_ok = mbar_wait_bounded(bar + 1, 0, p.status);
+            const uint8_t *qrow = sm + L::kQr + t * DK * 2, *krow = sm + L::kKr + t * DK * 2;
 #pragma unroll
             for (int b = 0; b < DK / 32; ++b) {
                 const int ib = b * 32;
@@ -983,8 +989,10 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
                 tmem_wait_ld();
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const uint32_t qw[4] = {qv4[b][h].x, qv4[b][h].y, qv4[b][h].z, qv4[b][h].w};
-                    const uint32_t kw[4] = {kv4[b][h].x, kv4[b][h].y, kv4[b][h].z, kv4[b][h].w};
+                    const uint4 q4 = *reinterpret_cast<const uint4 *>(qrow + (b * 32 + hc + h * 8) * 2);
+                    const uint4 k4 = *reinterpret_cast<const uint4 *>(krow + (b * 32 + hc + h * 8) * 2);
+                    const uint32_t qw[4] = {q4.x, q4.y, q4.z, q4.w};
+                    const uint32_t kw[4] = {k4.x, k4.y, k4.z, k4.w};
                     uint32_t dqw[4], dkw[4];
                     float pr[8];
 #pragma unroll
@@ -1005,13 +1013,13 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
                         dkw[x / 2] = pack_bf16x2(dkv[0], dkv[1]);
                     }
                     const int i0 = ib + hc + h * 8;
-                    if (row_ok) {
+                    if (row_ok && qk_ok) {
                         const size_t off = rk + static_cast<size_t>(t) * DK + i0;
                         *reinterpret_cast<uint4 *>(p.gq + off) = make_uint4(dqw[0], dqw[1], dqw[2], dqw[3]);
                         *reinterpret_cast<uint4 *>(p.gk + off) = make_uint4(dkw[0], dkw[1], dkw[2], dkw[3]);
                     }
 #pragma unroll
-                    for (int x = 0; x < 8; ++x) sP[t * LP + i0 + x] = row_ok ? pr[x] : 0.f;
+                    for (int x = 0; x < 8; ++x) sP[t * LP + i0 + x] = row_ok && qk_ok ? pr[x] : 0.f;
                 }
             }
         } else {

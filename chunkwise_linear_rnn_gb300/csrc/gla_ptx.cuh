@@ -189,6 +189,16 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, const vo
         : "memory");
 }
 
+// Copy `bytes` (a multiple of 16; both addresses 16-byte aligned) from global
+// to this CTA's shared memory; completes as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Store one 32-bit word into another CTA's shared memory (dst and bar are
 // shared::cluster addresses); completes as 4 transaction bytes on its mbarrier.
 __device__ __forceinline__ void st_async_to_peer(uint32_t dst_cluster, uint32_t value,
