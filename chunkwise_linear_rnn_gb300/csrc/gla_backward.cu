@@ -980,7 +980,9 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
             // past n were not loaded; their results are not used)
             const bool qk_ok = mbar_wait_bounded(bar + 1, 0, p.status);
             const uint8_t *qrow = sm + L::kQr + t * DK * 2, *krow = sm + L::kKr + t * DK * 2;
-#pragma unroll
+            // rolled loops: this code runs once per CTA, so a small body that
+            // stays in the instruction cache beats unrolled straight-line code
+#pragma unroll 1
             for (int b = 0; b < DK / 32; ++b) {
                 const int ib = b * 32;
                 uint32_t rq[16], rkk[16];
