@@ -517,6 +517,10 @@ int gla_chunk_fwd_debug(const void *q, const void *k, const void *v, const float
     const gla_chunk_options &op = opts ? *opts : o_def;
     if (!options_ok(dv, op)) return GLA_ERR_ARG;
     if (static_cast<long long>(B) * H > 0x7fffffffLL) return GLA_ERR_ARG;
+    // the instrumentation's own arguments; its kernel build covers one gate per
+    // key channel only
+    if (dbg && (dbg->withhold_v < 0 || (dbg->gamma && !aligned16(dbg->gamma)) || op.gate_per_head))
+        return GLA_ERR_ARG;
 
     DeviceInfo *dev = nullptr;
     const int st = current_device(&dev);
@@ -896,12 +900,12 @@ int gla_gdn_chunk_fwd(const void *q, const void *k, const void *v, const float *
         (hT && !aligned16(hT)) || (reinterpret_cast<uintptr_t>(g) & 3u) ||
         (reinterpret_cast<uintptr_t>(beta) & 3u) || (h0 && (reinterpret_cast<uintptr_t>(h0) & 3u)))
         return GLA_ERR_ARG;
+    const long long BH = static_cast<long long>(B) * H;
+    // the scratch rows are addressed by 32-bit TMA coordinates
+    if (BH * ((static_cast<long long>(T) + 63) / 64) * 64 > 0x7fffffffLL) return GLA_ERR_ARG;
     DeviceInfo *dev = nullptr;
     const int st = current_device(&dev);
     if (st != GLA_OK) return st;
-    const long long BH = static_cast<long long>(B) * H;
-    // the scratch rows are addressed by 32-bit TMA coordinates
-    if (BH * ((T + 63) / 64) * 64 > 0x7fffffffLL) return GLA_ERR_ARG;
     const size_t bytes = gdn_chunk_scratch_bytes(BH, T, dk);
     void *ws = nullptr;
     if (cudaMallocAsync(&ws, bytes, stream) != cudaSuccess) {

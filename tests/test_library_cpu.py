@@ -257,3 +257,40 @@ def test_gated_delta_rule_validates_before_the_device(lib):
     assert _gdn(lib, dk=96) == _lib.GLA_ERR_SHAPE
     assert _gdn(lib, dv=48) == _lib.GLA_ERR_SHAPE
     assert _gdn(lib) == _lib.GLA_ERR_DEVICE   # valid arguments, no GPU here
+
+
+def _gdn_chunk(lib, **kw):
+    """gla_gdn_chunk_fwd with fake aligned pointers; keyword overrides."""
+    a = dict(q=P, k=P, v=P, g=P, beta=P, scale=0.125, h0=None, o=P, hT=None, B=1, H=1, T=16,
+             dk=128, dv=64)
+    a.update(kw)
+    return lib.gla_gdn_chunk_fwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["scale"], a["h0"],
+                                 a["o"], a["hT"], a["B"], a["H"], a["T"], a["dk"], a["dv"], None)
+
+
+def test_chunked_gated_delta_rule_validates_before_the_device(lib):
+    for field in ("q", "k", "v", "g", "beta", "o"):
+        assert _gdn_chunk(lib, **{field: None}) == _lib.GLA_ERR_ARG
+    for field in ("q", "k", "v", "o", "hT"):   # TMA tiles and 16-byte stores
+        assert _gdn_chunk(lib, **{field: P + 8}) == _lib.GLA_ERR_ARG
+    for field in ("g", "beta", "h0"):          # fp32, read as words
+        assert _gdn_chunk(lib, **{field: P + 2}) == _lib.GLA_ERR_ARG
+    assert _gdn_chunk(lib, T=0) == _lib.GLA_ERR_ARG
+    assert _gdn_chunk(lib, B=300, H=300) == _lib.GLA_ERR_ARG
+    assert _gdn_chunk(lib, dk=64) == _lib.GLA_ERR_SHAPE    # the chunked form is dk = 128 only
+    assert _gdn_chunk(lib, dv=48) == _lib.GLA_ERR_SHAPE
+    # more scratch rows than 32-bit tensor-map coordinates address
+    assert _gdn_chunk(lib, H=2, T=2 ** 30 + 1) == _lib.GLA_ERR_ARG
+    assert _gdn_chunk(lib) == _lib.GLA_ERR_DEVICE        # valid arguments, no GPU here
+
+
+def test_debug_entry_validates_before_the_device(lib):
+    def dbg_call(dbg, opts=None):
+        return lib.gla_chunk_fwd_debug(P, P, P, P, 0.125, None, P, None, 1, 1, 16, 64, 64,
+                                       None if opts is None else ctypes.byref(opts),
+                                       ctypes.byref(dbg), None)
+    assert dbg_call(_lib.GlaChunkDebug(withhold_v=-1)) == _lib.GLA_ERR_ARG
+    assert dbg_call(_lib.GlaChunkDebug(gamma=P + 4)) == _lib.GLA_ERR_ARG
+    # the instrumented kernel build covers one gate per key channel only
+    assert dbg_call(_lib.GlaChunkDebug(), _lib.GlaChunkOptions(gate_per_head=1)) == _lib.GLA_ERR_ARG
+    assert dbg_call(_lib.GlaChunkDebug(wait_limit_us=5, withhold_v=1)) == _lib.GLA_ERR_DEVICE
