@@ -93,8 +93,8 @@ struct WySmem {
     static constexpr uint32_t kTl = kTh + kBlk;                  // and lo
     static constexpr uint32_t kL = kTl + kBlk;                   // fp32 [64][LS]: L
     static constexpr uint32_t kTf = kL + C * LS * 4;             // fp32 [64][LS]: T
-    static constexpr uint32_t kX = kTf + C * LS * 4;             // level products [3][16][16]
-    static constexpr uint32_t kG = kX + 3 * 16 * 16 * 4;
+    static constexpr uint32_t kX = kTf + C * LS * 4;             // merge products, up to [32][32]
+    static constexpr uint32_t kG = kX + 32 * 32 * 4;
     static constexpr uint32_t kBeta = kG + C * 4;
     static constexpr uint32_t kE = kBeta + C * 4;                // 2^-G per token
     static constexpr uint32_t kBar = kE + C * 4;
@@ -103,80 +103,127 @@ struct WySmem {
     static_assert(kBytes <= 75 * 1024, "three CTAs per SM");
 };
 
-// T = (I + L)^-1 for strictly lower L (64 x 64 fp32, row stride LS), by blocks
-// of 16.  The four diagonal blocks by substitution, one column per thread
-// (threads 0-63), in registers; then level by level
-//     T_ba = -T_bb sum_{m=a}^{b-1} L_bm T_ma   (b = a + lev),
-// first X_a = sum_m L_bm T_ma, then -T_bb X_a, a thread per row and four
-// columns of a 16 x 16 block.  Only the blocks on and below the diagonal of
+// The diagonal 16 x 16 block o..o+15 of T = (I + L)^-1 by substitution:
+// column j per thread (lanes 0-15 of the warp whose TMEM quarter holds those
+// rows of L), in registers; x_i = -sum_{m<i} L_im x_m below the unit diagonal.
+__device__ __forceinline__ void invert_diagonal_block(const float *sL, float *sTf, int o, int j) {
+    constexpr int LS = WySmem::LS;
+    float x[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = i == j ? 1.f : 0.f;
+#pragma unroll
+    for (int i = 1; i < 16; ++i) {
+        const float *row = sL + (o + i) * LS + o;
+        float acc = 0.f;
+#pragma unroll
+        for (int m4 = 0; m4 < i; m4 += 4) {
+            const float4 l4 = *reinterpret_cast<const float4 *>(row + m4);
+            acc = fmaf(l4.x, x[m4], acc);
+            if (m4 + 1 < i) acc = fmaf(l4.y, x[m4 + 1], acc);
+            if (m4 + 2 < i) acc = fmaf(l4.z, x[m4 + 2], acc);
+            if (m4 + 3 < i) acc = fmaf(l4.w, x[m4 + 3], acc);
+        }
+        if (i > j) x[i] = -acc;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) sTf[(o + i) * LS + o + j] = x[i];
+}
+
+// The rest of T = (I + L)^-1 (64 x 64 fp32, row stride LS) once its four
+// diagonal 16 x 16 blocks are in sTf: merge pairs of blocks, then the halves,
+// each as T_ba = -T_bb (L_ba T_aa) with T_aa, T_bb lower triangular (inverse
+// of a block lower-triangular matrix).  Four output columns per thread,
+// 16-byte shared-memory loads.  Only the blocks on and below the diagonal of
 // sTf are written.  Needs NT == 256.
-__device__ __forceinline__ void invert_unit_lower_blocked(const float *sL, float *sTf, float *sX) {
-    static_assert(NT == 256, "64 threads per 16 x 16 block, up to three blocks");
+__device__ __forceinline__ void merge_inverse_blocks(const float *sL, float *sTf, float *sX) {
+    static_assert(NT == 256, "four-column strips of a 32 x 32 block per thread");
     constexpr int LS = WySmem::LS;
     const int tid = threadIdx.x;
-    if (tid < C) {
-        const int o = (tid >> 4) * 16, j = tid & 15;
-        float x[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) x[i] = i == j ? 1.f : 0.f;
-#pragma unroll
-        for (int i = 1; i < 16; ++i) {
-            const float *row = sL + (o + i) * LS + o;
-            float acc = 0.f;
-#pragma unroll
-            for (int m4 = 0; m4 < i; m4 += 4) {
-                const float4 l4 = *reinterpret_cast<const float4 *>(row + m4);
-                acc = fmaf(l4.x, x[m4], acc);
-                if (m4 + 1 < i) acc = fmaf(l4.y, x[m4 + 1], acc);
-                if (m4 + 2 < i) acc = fmaf(l4.z, x[m4 + 2], acc);
-                if (m4 + 3 < i) acc = fmaf(l4.w, x[m4 + 3], acc);
-            }
-            if (i > j) x[i] = -acc;
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) sTf[(o + i) * LS + o + j] = x[i];
-    }
-    __syncthreads();
-    const int blk = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
-    for (int lev = 1; lev < 4; ++lev) {
-        const int a = blk, b = a + lev;
-        if (b < 4) {
+    // 16 x 16 merges: (rows 16-31, cols 0-15) and (rows 48-63, cols 32-47);
+    // threads 0-127: block p = tid / 64, row r, columns c4..c4+3
+    {
+        const int pb = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
+        const int a = 32 * pb, bb = a + 16;   // T_aa at (a, a), T_bb at (bb, bb)
+        if (tid < 128) {
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            const float *lrow = sL + (b * 16 + r) * LS;
-            for (int m = a * 16; m < b * 16; m += 4) {
+            const float *lrow = sL + (bb + r) * LS + a;
+#pragma unroll
+            for (int m = 0; m < 16; m += 4) {
                 const float4 l4 = *reinterpret_cast<const float4 *>(lrow + m);
                 const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float4 t4 = *reinterpret_cast<const float4 *>(sTf + (m + e) * LS + a * 16 + c4);
+                    const float4 t4 = *reinterpret_cast<const float4 *>(sTf + (a + m + e) * LS + a + c4);
                     acc.x = fmaf(lv[e], t4.x, acc.x);
                     acc.y = fmaf(lv[e], t4.y, acc.y);
                     acc.z = fmaf(lv[e], t4.z, acc.z);
                     acc.w = fmaf(lv[e], t4.w, acc.w);
                 }
             }
-            *reinterpret_cast<float4 *>(sX + a * 256 + r * 16 + c4) = acc;
+            *reinterpret_cast<float4 *>(sX + pb * 256 + r * 16 + c4) = acc;
         }
         __syncthreads();
-        if (b < 4) {
+        if (tid < 128) {
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            const float *trow = sTf + (b * 16 + r) * LS + b * 16;
+            const float *trow = sTf + (bb + r) * LS + bb;
 #pragma unroll
             for (int m = 0; m < 16; m += 4) {
                 const float4 t4 = *reinterpret_cast<const float4 *>(trow + m);
                 const float tv[4] = {t4.x, t4.y, t4.z, t4.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float4 x4 = *reinterpret_cast<const float4 *>(sX + a * 256 + (m + e) * 16 + c4);
+                    const float4 x4 = *reinterpret_cast<const float4 *>(sX + pb * 256 + (m + e) * 16 + c4);
                     acc.x = fmaf(tv[e], x4.x, acc.x);
                     acc.y = fmaf(tv[e], x4.y, acc.y);
                     acc.z = fmaf(tv[e], x4.z, acc.z);
                     acc.w = fmaf(tv[e], x4.w, acc.w);
                 }
             }
-            *reinterpret_cast<float4 *>(sTf + (b * 16 + r) * LS + a * 16 + c4) =
+            *reinterpret_cast<float4 *>(sTf + (bb + r) * LS + a + c4) =
                 make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
         }
+        __syncthreads();
+    }
+    // 32 x 32 merge: rows 32-63, cols 0-31; thread = row r, columns c4..c4+3.
+    // T_A (rows, cols 0-31) and T_B (rows, cols 32-63) are lower triangular,
+    // so X = L_BA T_A sums m >= c and T_B X sums m <= r; the loops still run
+    // over all 32 (the zero entries above the diagonal blocks were never
+    // written, so they are skipped by block: m-blocks of 16 below c's block
+    // and above r's block contribute nothing).
+    {
+        const int r = tid >> 3, c4 = (tid & 7) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float *lrow = sL + (32 + r) * LS;
+        for (int m = (c4 >> 4) * 16; m < 32; m += 4) {
+            const float4 l4 = *reinterpret_cast<const float4 *>(lrow + m);
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float4 t4 = *reinterpret_cast<const float4 *>(sTf + (m + e) * LS + c4);
+                acc.x = fmaf(lv[e], t4.x, acc.x);
+                acc.y = fmaf(lv[e], t4.y, acc.y);
+                acc.z = fmaf(lv[e], t4.z, acc.z);
+                acc.w = fmaf(lv[e], t4.w, acc.w);
+            }
+        }
+        *reinterpret_cast<float4 *>(sX + r * 32 + c4) = acc;
+        __syncthreads();
+        acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float *trow = sTf + (32 + r) * LS + 32;
+        const int mend = (r >> 4) * 16 + 16;
+        for (int m = 0; m < mend; m += 4) {
+            const float4 t4 = *reinterpret_cast<const float4 *>(trow + m);
+            const float tv[4] = {t4.x, t4.y, t4.z, t4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float4 x4 = *reinterpret_cast<const float4 *>(sX + (m + e) * 32 + c4);
+                acc.x = fmaf(tv[e], x4.x, acc.x);
+                acc.y = fmaf(tv[e], x4.y, acc.y);
+                acc.z = fmaf(tv[e], x4.z, acc.z);
+                acc.w = fmaf(tv[e], x4.w, acc.w);
+            }
+        }
+        *reinterpret_cast<float4 *>(sTf + (32 + r) * LS + c4) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
         __syncthreads();
     }
 }
@@ -209,7 +256,7 @@ __global__ void __launch_bounds__(NT, 3) gdn_wy_kernel(
     const size_t rk = rg * DK;
     const size_t orow = (static_cast<size_t>(bh) * nch + u) * C;   // first scratch row
 
-    if (warp == 0) tmem_alloc(slot, 256);
+    if (warp == 0) tmem_alloc(slot, 128);   // K K^T, then W over it: four CTAs' worth per SM
     if (tid == 0) {
         mbar_init(&bar[0], 1);
         mbar_init(&bar[1], 1);
@@ -250,7 +297,8 @@ __global__ void __launch_bounds__(NT, 3) gdn_wy_kernel(
     tc_fence_after();
     __syncthreads();   // sE
     // L_ti = beta_t 2^(G_t - G_i) (k_t . k_i) for i < t: warps 0-3, row
-    // t = 16 q + (lane & 15), 16 columns per half-split load
+    // t = 16 q + (lane & 15), 16 columns per half-split load; then each of
+    // these warps inverts the diagonal block of its own 16 rows
     if (warp < 4) {
         const int t = 16 * warp + (lane & 15), hc = (lane >> 4) * 16;
         const float Gt = sG[t], bt = sB[t], rt = bt * exp2f(Gt);
@@ -270,9 +318,12 @@ __global__ void __launch_bounds__(NT, 3) gdn_wy_kernel(
             for (int j = 0; j < 16; j += 4)
                 *reinterpret_cast<float4 *>(sL + t * LS + ib + hc + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
         }
+        __syncwarp();
+        if (lane < 16) invert_diagonal_block(sL, sTf, 16 * warp, lane);
     }
+    tc_fence_before();   // K K^T is read: W may take its columns
     __syncthreads();
-    invert_unit_lower_blocked(sL, sTf, reinterpret_cast<float *>(sm + L::kX));
+    merge_inverse_blocks(sL, sTf, reinterpret_cast<float *>(sm + L::kX));
     // T diag(beta gamma) as a hi/lo pair, K-major [t][i] (A of W), and
     // (T - I) diag(beta) row-major to the scratch
     __nv_bfloat16 *tdst = Tout + orow * C;
@@ -305,8 +356,8 @@ __global__ void __launch_bounds__(NT, 3) gdn_wy_kernel(
 #pragma unroll
         for (int kk = 0; kk < C / 16; ++kk) {
             const uint64_t bk = sw128_desc(a0 + L::kK + kk * 2048, L::kBlk, 1024);
-            mma_bf16_ss(tmem + 64, sw128_desc(a0 + L::kTh + kk * 32, 16, 1024), bk, idw, kk > 0 ? 1u : 0u);
-            mma_bf16_ss(tmem + 64, sw128_desc(a0 + L::kTl + kk * 32, 16, 1024), bk, idw, 1u);
+            mma_bf16_ss(tmem, sw128_desc(a0 + L::kTh + kk * 32, 16, 1024), bk, idw, kk > 0 ? 1u : 0u);
+            mma_bf16_ss(tmem, sw128_desc(a0 + L::kTl + kk * 32, 16, 1024), bk, idw, 1u);
         }
         mma_commit(&bar[1]);
     }
@@ -319,7 +370,7 @@ __global__ void __launch_bounds__(NT, 3) gdn_wy_kernel(
 #pragma unroll 1
         for (int cb = 0; cb < DK; cb += 32) {
             uint32_t r[16];
-            tmem_ld16x2<16>(tmem + lo_ + 64 + cb, r);
+            tmem_ld16x2<16>(tmem + lo_ + cb, r);
             tmem_wait_ld();
             if (ok) {
                 __nv_bfloat16 *dst = Wout + (orow + t) * DK + cb + hc;
@@ -335,7 +386,7 @@ __global__ void __launch_bounds__(NT, 3) gdn_wy_kernel(
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
 // ------------------------------------------------------------------ sequential chunk kernel
