@@ -69,3 +69,23 @@ def test_reference_arm_other_ranks_exit_without_output():
                          env=env, capture_output=True, text=True, timeout=300)
     assert res.returncode == 0, res.stderr[-2000:]
     assert res.stdout.strip() == ""
+
+
+def test_torchrun_two_ranks_reference_arm_prints_one_line():
+    """The N > 1 launch of bench.py (torchrun, two local ranks, rendezvous on
+    127.0.0.1): rank 0 alone times the oracle on the host cores and prints the
+    one JSON line (n_gpus 0: no GPU in that arm), rank 1 exits at once, and
+    both exit 0.  Runs here without a GPU."""
+    import json
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
+           "--master-addr=127.0.0.1", f"--master-port={port}", os.path.join(ROOT, "bench.py"),
+           "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "0",
+           "--workload", "small", "--ref-seconds", "0.5", "--only", "chunk"]
+    res = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert res.returncode == 0, res.stderr[-3000:]
+    lines = [ln for ln in res.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, res.stdout[-2000:]
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference" and rec["steps"] == 1 and rec["n_gpus"] == 0
+    assert rec["value"] > 0 and rec["cpu_baseline"]["kind"] == "oracle"
