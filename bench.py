@@ -61,8 +61,8 @@ def peaks():
 # long workload (B2 H16 T32768 dk128 dv256) at full size, with the kernel
 # sources whose hash is given.  Any change to those sources makes the figure
 # stale: it is then reported as null.
-MEASURED_TRAFFIC = {"workload": "B2-H16-T32768-dk128-dv256", "sources": "25308919e11d6600",
-                    "bytes_per_call": 1642691328 + 514783232}
+MEASURED_TRAFFIC = {"workload": "B2-H16-T32768-dk128-dv256", "sources": "2061b6c4cb81ba29",
+                    "bytes_per_call": 1642785280 + 515365120}
 TRAFFIC_SOURCES = ["gla_chunk.cu", "gla_chunk_kernel.cuh", "gla_ptx.cuh"]
 
 
@@ -70,9 +70,9 @@ TRAFFIC_SOURCES = ["gla_chunk.cu", "gla_chunk_kernel.cuh", "gla_ptx.cuh"]
 # all six launches, for the backward sources hashed in "sources": captured at
 # B=1 H=4 (2,048 chunks) and scaled by the chunks of the long workload (16,384;
 # every chunk's inputs, states and gradients move once per launch)
-MEASURED_BWD_TRAFFIC = {"workload": "B2-H16-T32768-dk128-dv256", "sources": "19637c16dfd6a354",
-                        "bytes_per_call": 8 * (821_060_096 + 474_234_112 + 768_632_576
-                                               + 998_441_728 + 67_840 + 67_840)}
+MEASURED_BWD_TRAFFIC = {"workload": "B2-H16-T32768-dk128-dv256", "sources": "99c98ecd177a2657",
+                        "bytes_per_call": 8 * (820_990_976 + 474_674_432 + 768_330_240
+                                               + 994_709_760 + 135_424)}
 BWD_TRAFFIC_SOURCES = ["gla_backward.cu", "gla_ptx.cuh"]
 
 
@@ -81,8 +81,8 @@ BWD_TRAFFIC_SOURCES = ["gla_backward.cu", "gla_ptx.cuh"]
 # sources hashed in "sources"; scaled by the heads a call covers (every head
 # streams its own rows and scratch once)
 MEASURED_GDN_CHUNK_TRAFFIC = {"T": 32768, "dk": 128, "dv": 256, "heads": 32,
-                              "sources": "3a910b4716c3b498",
-                              "bytes_per_call": 277143296 + 347051264 + 1489058048 + 512030976}
+                              "sources": "c5948dbd13bc0e9b",
+                              "bytes_per_call": 277083136 + 347115008 + 1489071616 + 512064768}
 GDN_CHUNK_TRAFFIC_SOURCES = ["gla_gdn_chunk.cu", "gla_ptx.cuh"]
 
 
