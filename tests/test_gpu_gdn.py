@@ -153,6 +153,17 @@ def test_chunked_strong_forgetting_full_writes_and_beta_zero():
     np.testing.assert_allclose(hT, decay * h0.double().numpy(), rtol=1e-4, atol=1e-7)
 
 
+def test_chunked_more_sequential_ctas_than_sms():
+    # B*H = 64 heads at dv = 256: 256 sequential-kernel CTAs (one per head and
+    # 64-column tile, one per SM) run in two waves; the WY pre-pass has 1,280
+    # CTAs; a ragged last chunk
+    q, k, v, g, b, h0 = make_gdn_inputs(4, 16, 300, 128, 256, sigma_h0=0.1, seed=26)
+    o, hT = _gpu(q, k, v, g, b, h0, 128 ** -0.5, chunked=True)
+    ro, rhT = _oracle(q, k, v, g, b, h0, 128 ** -0.5)
+    assert_close(o, ro, "chunked 64 heads o", bf16_output=True)
+    assert_close(hT, rhT, "chunked 64 heads hT")
+
+
 def test_chunked_agrees_with_the_token_recurrent_kernel():
     case = make_gdn_inputs(2, 2, 500, 128, 128, sigma_h0=0.1, seed=25)
     o_c, h_c = _gpu(*case, 128 ** -0.5, chunked=True)
