@@ -13,24 +13,26 @@
 //
 // Two kernels, split as the page splits its operators (an inversion operator,
 // then one fused operator for the rest):
-//   gdn_wy_kernel   one CTA per (chunk, head), two CTAs per SM: step 1 and W.
+//   gdn_wy_kernel   one CTA per (chunk, head), three CTAs per SM: step 1 and W.
 //                   K K^T on the tensor cores; the unit lower triangular
-//                   inverse by 16 x 16 blocks (the four diagonal blocks by
-//                   substitution, one column per thread, then the
-//                   off-diagonal blocks level by level as small products);
-//                   T (bf16) and W = T diag(beta gamma) K (bf16) to scratch,
-//                   2 dk + 128 bytes per token.
+//                   inverse by 16 x 16 blocks (each diagonal block by
+//                   substitution in the warp that formed its rows of L, then
+//                   two merge levels of small products); to scratch, bf16,
+//                   2 dk + 128 bytes per token: W = (T diag(beta gamma)) K and
+//                   (T - I) diag(beta), the off-diagonal part of U's factor.
 //   gdn_seq_kernel  one CTA per (head, 64-column value tile), chunks in order,
 //                   the state's 128 key rows in the registers of warps 0-3
-//                   (one row per thread): U = T (beta V) for the tile and
-//                   steps 3-4 as tensor-core products W S, Q S, Q K^T, U, then
-//                   P D and K~^T D (K~ = K gamma_C/gamma).
+//                   (one row per thread); each chunk's operands loaded by TMA
+//                   one chunk ahead into the other of two stages; steps 3-4 as
+//                   tensor-core products W S, (T - I) diag(beta) V, Q K^T, Q S,
+//                   K^T D' and P D, with D' = diag(gamma_C / gamma) D.
 //
-// Precision: bf16 operands with fp32 accumulation; the products whose operand
-// rounding would enter every later state (beta K, beta V, S in Q S, P, D, K~)
-// use bf16 hi/lo pairs (16 significant bits); T and W S stay single bf16
-// (their error enters through D once per chunk).  o is rounded once to bf16;
-// the state and hT are fp32.
+// Precision: bf16 operands with fp32 accumulation.  The operands whose
+// rounding would enter every later state (T diag(beta gamma) in W, S, D, D',
+// P) are bf16 hi/lo pairs (16 significant bits); the stored W and
+// (T - I) diag(beta) are single bf16, and U's diagonal term beta_t v_t is
+// added exactly in fp32.  K and V enter as the exact bf16 inputs.  o is
+// rounded once to bf16; the state and hT are fp32.
 //
 // Every mbarrier wait is bounded (the library's limit); an expired wait sets
 // the status word and the CTA stops at the next chunk boundary.
