@@ -421,13 +421,16 @@ int gla_gdn_fwd(const void *q, const void *k, const void *v, const float *g, con
  *   2. W = T diag(beta gamma) K and U = T diag(beta) V;
  *   3. S_end = gamma_C S + (diag(gamma_C / gamma) K)^T (U - W S);
  *   4. O = scale (diag(gamma) Q S + tril(Q K^T gamma_t / gamma_i) (U - W S)).
- * Step 1 and W run for all chunks at once and leave T and W in stream-ordered
- * scratch (cudaMallocAsync / cudaFreeAsync on `stream`):
- * ceil(T / 64) * 64 * B * H * (2 dk + 128) bytes.  U and steps 3-4 run as each
- * head's chunks are walked in order with the state on chip.  dk = 128 only (GLA_ERR_SHAPE
- * otherwise); dv in {64, 128, 256}; B * H <= 65535.  q, k, v, o and hT must be
- * 16-byte aligned, g, beta and h0 4-byte aligned (GLA_ERR_ARG otherwise).
- * hT may alias h0.  GLA_ERR_ALLOC if the scratch cannot be allocated.
+ * Step 1 and W run for all chunks at once and leave W and (T - I) diag(beta)
+ * (bf16) in stream-ordered scratch (cudaMallocAsync / cudaFreeAsync on
+ * `stream`): ceil(T / 64) * 64 * B * H * (2 dk + 128) bytes.  U and steps 3-4
+ * run as each head's chunks are walked in order with the state on chip.
+ * dk = 128 only (GLA_ERR_SHAPE otherwise); dv in {64, 128, 256};
+ * B * H <= 65535 and B * H * ceil(T / 64) * 64 < 2^31 (the scratch rows'
+ * tensor-map coordinates).  q, k, v, o and hT must be 16-byte aligned, g, beta
+ * and h0 4-byte aligned.  GLA_ERR_ARG for a violated bound or alignment, found
+ * on the host before any device call.  hT may alias h0.  GLA_ERR_ALLOC if the
+ * scratch cannot be allocated.
  */
 int gla_gdn_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
                       const float *beta, float scale, const float *h0, void *o, float *hT, int B,
