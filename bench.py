@@ -81,7 +81,7 @@ BWD_TRAFFIC_SOURCES = ["gla_backward.cu", "gla_ptx.cuh"]
 # sources hashed in "sources"; scaled by the heads a call covers (every head
 # streams its own rows and scratch once)
 MEASURED_GDN_CHUNK_TRAFFIC = {"T": 32768, "dk": 128, "dv": 256, "heads": 32,
-                              "sources": "c5948dbd13bc0e9b",
+                              "sources": "314d585fa2cf92a6",
                               "bytes_per_call": 277083136 + 347115008 + 1489071616 + 512064768}
 GDN_CHUNK_TRAFFIC_SOURCES = ["gla_gdn_chunk.cu", "gla_ptx.cuh"]
 
