@@ -781,7 +781,10 @@ def gdn_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_ki
         "metric": GDN_METRIC,
         "value": tokens_all / (ms_per_step / 1e3), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        # chunked: bf16 tensor-core products (hi/lo pairs) with fp32 accumulation;
+        # token recurrence: fp32 on the CUDA cores
+        "dtype": "bf16" if chunked else "f32",
         "data": "synthetic",
         "config": {"workload": cfg.name + "-gated-delta-rule", "B": cfg.B, "H": cfg.H,
                    "T": cfg.T, "dk": cfg.dk, "dv": cfg.dv, "replicas": world,
