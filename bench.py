@@ -666,7 +666,9 @@ def bwd_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_ki
         "metric": BWD_METRIC,
         "value": tokens_all / (ms_per_step / 1e3), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        # bf16 tensor-core products (hi/lo pairs), fp32 accumulation and scans
+        "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": cfg.name + (f"-packed{args.varlen}" if args.varlen else "") +
                    "-backward", "B": cfg.B, "H": cfg.H, "T": cfg.T,
