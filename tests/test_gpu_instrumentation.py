@@ -1,5 +1,10 @@
 """Looking inside the chunked forward through gla_chunk_fwd_debug (C ABI).
 
+gla_chunk_fwd_debug runs the instrumented build of the forward kernel: the
+same template with its test hooks compiled in (the production entry points
+run the build without them).  The outputs of every instrumented call are
+still checked against the oracle.
+
 1. The in-chunk prefix sums (GLA page, "Cumulative Decay Representation"): the
    preparation stage's Gamma, dumped by the kernel, against an fp64 cumulative
    sum of the same fp32 gates, and the block length each chunk took against
