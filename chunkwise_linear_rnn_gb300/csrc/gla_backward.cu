@@ -899,13 +899,21 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
     // A / M tiles, which the products above have finished reading.
     {
         uint8_t *tSh = sm + L::kQh, *tSl = tSh + kSB, *tRh = sm + L::kAh, *tRl = tRh + kSB;
+        // each row's two factors, the same for every slab
+        float fsv[SPER], frv[SPER];
+#pragma unroll
+        for (int m = 0; m < SPER; ++m) {
+            const int i = (tid + m * NTI) / 16;
+            fsv[m] = exp2f(sRef[i]);
+            frv[m] = exp2f(sGC[i] - sRef[i]) / s;
+        }
 #pragma unroll 1
         for (int sl = 0; sl < DV / 64; ++sl) {
             const int c0 = sl * 64;
 #pragma unroll
             for (int m = 0; m < SPER; ++m) {
                 const int e = tid + m * NTI, i = e / 16, cl = (e % 16) * 4;
-                const float fs = exp2f(sRef[i]), fr = exp2f(sGC[i] - sRef[i]) / s;
+                const float fs = fsv[m], fr = frv[m];
                 const uint32_t off = sw128_offset(i, cl, kSB);
                 uint32_t h0, l0, h1, l1;
                 split_pair(sv[m].x * fs, sv[m].y * fs, h0, l0);
