@@ -240,7 +240,10 @@ __global__ void __launch_bounds__(kSumThreads, 2) bwd_sums_kernel(BwdLaunch p) {
         mbar_init(bar, 1);
         fence_mbar_init();
     }
-    // issue the key-side and value-side loads first; they land during the prefix sums
+    // the gates first (the prefix sums need them first), then the key-side and
+    // value-side loads, which land during the prefix sums
+    float4 gr[BC * DK / 4 / NTS];
+    prefix_issue<DK, NTS>(gr, p.log_alpha + rk, n);
     const __nv_bfloat16 *asrc = which ? p.q : p.k;
     const __nv_bfloat16 *bsrc = which ? p.d_o : p.v;
     constexpr int APER = BC * 64 / NTS;           // channel pairs per thread
@@ -260,7 +263,7 @@ __global__ void __launch_bounds__(kSumThreads, 2) bwd_sums_kernel(BwdLaunch p) {
         braw[m] = t < n ? *reinterpret_cast<const uint4 *>(bsrc + rv + static_cast<size_t>(t) * DV + c)
                         : make_uint4(0u, 0u, 0u, 0u);
     }
-    load_prefix<DK, DK, NTS>(sG, p.log_alpha + rk, n);
+    prefix_finish<DK, DK, NTS>(sG, gr);
 
     // A: rows = tokens, columns = key channels, scaled and split
 #pragma unroll
