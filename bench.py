@@ -70,9 +70,9 @@ TRAFFIC_SOURCES = ["gla_chunk.cu", "gla_chunk_kernel.cuh", "gla_ptx.cuh"]
 # all six launches, for the backward sources hashed in "sources": captured at
 # B=1 H=4 (2,048 chunks) and scaled by the chunks of the long workload (16,384;
 # every chunk's inputs, states and gradients move once per launch)
-MEASURED_BWD_TRAFFIC = {"workload": "B2-H16-T32768-dk128-dv256", "sources": "99c98ecd177a2657",
-                        "bytes_per_call": 8 * (820_990_976 + 474_674_432 + 768_330_240
-                                               + 994_709_760 + 135_424)}
+MEASURED_BWD_TRAFFIC = {"workload": "B2-H16-T32768-dk128-dv256", "sources": "87c4734e2d005a15",
+                        "bytes_per_call": 8 * (821_586_432 + 474_372_352 + 768_244_480
+                                               + 994_942_976 + 135_424)}
 BWD_TRAFFIC_SOURCES = ["gla_backward.cu", "gla_ptx.cuh"]
 
 
