@@ -336,6 +336,19 @@ class Ranks:
         return float(t.item())
 
 
+def replica_inputs(cfg, rank: int, device):
+    """Rank `rank`'s replica of a fixed-length workload: the seeded synthetic
+    inputs drawn with seed = rank, so that each rank works on its own shard
+    (a distinct draw of the same distribution) and no data crosses ranks."""
+    from synth import make_config_inputs
+    return make_config_inputs(cfg, seed=rank, device=device)
+
+
+def job_tokens(cfg, world: int) -> int:
+    """Tokens the whole job processes per step: every rank's replica."""
+    return cfg.tokens * world
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import __graft_entry__ as ge
@@ -420,7 +433,7 @@ def chunk_config(args):
 
 def chunk_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_kind):
     import torch
-    from synth import make_chunk_inputs, make_config_inputs
+    from synth import make_chunk_inputs
     stream = torch.cuda.current_stream(dev)
     n_states = None
     packed = None
@@ -455,7 +468,7 @@ def chunk_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_
 
         launches_per_step = gla.gla_chunk_fwd_varlen_plan(cu, cfg.H, cfg.dk, cfg.dv)["launches"]
     else:
-        q, k, v, a, h0 = make_config_inputs(cfg, seed=rank, device=dev)
+        q, k, v, a, h0 = replica_inputs(cfg, rank, dev)
         if args.gate == "head":
             a = a[..., 0].contiguous()   # one gate per token and head (its first channel's draw)
         o = torch.empty(cfg.B, cfg.H, cfg.T, cfg.dv, dtype=torch.bfloat16, device=dev)
@@ -486,7 +499,7 @@ def chunk_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_
     if gla.gla_last_device_status(dev) != 0:
         raise RuntimeError("device status word reports an expired wait during the benchmark")
     ms_per_step = total_ms / args.steps
-    tokens_all = cfg.tokens * world
+    tokens_all = job_tokens(cfg, world)
     value = tokens_all / (ms_per_step / 1e3)
     byts = chunk_bytes(cfg, n_states, gate_per_head=args.gate == "head")
     achieved_gbs = byts / (per_launch_ms / 1e3) / 1e9
@@ -564,7 +577,7 @@ def chunk_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_
 def bwd_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_kind):
     """The chunkwise backward (gla_chunk_bwd) on the workload, its own JSON line."""
     import torch
-    from synth import make_backward_grads, make_config_inputs
+    from synth import make_backward_grads
     stream = torch.cuda.current_stream(dev)
     plan = gla.gla_chunk_bwd_plan(cfg.B, cfg.H, cfg.T, cfg.dk, cfg.dv)
     packed = None
@@ -594,7 +607,7 @@ def bwd_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_ki
         def step():
             return gla.gla_chunk_bwd_varlen(q, k, v, a, d_o, cu, cfg.scale, h0, dhT)
     else:
-        q, k, v, a, h0 = make_config_inputs(cfg, seed=rank, device=dev)
+        q, k, v, a, h0 = replica_inputs(cfg, rank, dev)
         d_o, dhT = make_backward_grads(cfg.B, cfg.H, cfg.T, cfg.dk, cfg.dv,
                                        sigma_dhT=0.1 if h0 is not None else None, seed=rank,
                                        device=dev)
@@ -621,7 +634,7 @@ def bwd_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_ki
     total_ms = max_over_ranks(t_start.elapsed_time(t_end))
     per_call_ms = statistics.mean(s0.elapsed_time(e0) for s0, e0 in ev)
     ms_per_step = total_ms / args.steps
-    tokens_all = cfg.tokens * world
+    tokens_all = job_tokens(cfg, world)
     byts = bwd_bytes(cfg, None if packed is None else packed["sequences"] * cfg.H)
     achieved = byts / (per_call_ms / 1e3) / 1e9
 
@@ -741,7 +754,7 @@ def gdn_leg(args, cfg, world, rank, dev, gla, barrier, max_over_ranks, pk, pk_ki
         barrier()
     ms_per_step = max_over_ranks(t_start.elapsed_time(t_end)) / args.steps
     per_call_ms = statistics.mean(s0.elapsed_time(e0) for s0, e0 in ev)
-    tokens_all = cfg.tokens * world
+    tokens_all = job_tokens(cfg, world)
     flops, byts = gdn_flops(cfg), gdn_bytes(cfg)
     achieved = flops / (per_call_ms / 1e3) / 1e12
 

@@ -2,7 +2,9 @@
 
 Two gloo ranks exercise the rank helpers the GPU run uses over NCCL: the
 barrier, and the maximum over ranks that turns per-rank times into the job's
-time.  The reference arm's ranks other than 0 exit at once, without output.
+time.  Each rank's replica is its own shard of seeded inputs, and its result
+(computed here on the oracle) is what one process gets alone.  The reference
+arm's ranks other than 0 exit at once, without output.
 """
 
 from __future__ import annotations
@@ -89,3 +91,59 @@ def test_torchrun_two_ranks_reference_arm_prints_one_line():
     rec = json.loads(lines[0])
     assert rec["impl"] == "reference" and rec["steps"] == 1 and rec["n_gpus"] == 0
     assert rec["value"] > 0 and rec["cpu_baseline"]["kind"] == "oracle"
+
+
+def _shard_main(rank: int, world: int, port: int, out):
+    import numpy as np
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench
+    from oracle import gla_oracle
+    from synth import CHUNK_CONFIGS
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
+                            world_size=world)
+    try:
+        cfg = CHUNK_CONFIGS["small"]
+        q, k, v, a, h0 = bench.replica_inputs(cfg, rank, "cpu")
+        o, hT = gla_oracle.forward_torch(q, k, v, a, cfg.scale, h0, nthreads=1)
+        tokens = [None] * world
+        dist.all_gather_object(tokens, int(q.shape[0] * q.shape[1] * q.shape[2]))
+        out.put((rank, np.asarray(o), np.asarray(hT), tokens, bench.job_tokens(cfg, world)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_replica_shards_are_independent_workloads():
+    """Two gloo ranks, each with its replica of the small workload, computed on
+    the oracle: the ranks hold distinct shards, each rank's result is what one
+    process computes alone on that rank's inputs (no data crosses ranks), and
+    the job's token count is the sum over the ranks' shards."""
+    import numpy as np
+    sys.path.insert(0, ROOT)
+    import bench
+    from oracle import gla_oracle
+    from synth import CHUNK_CONFIGS
+    gla_oracle.build()   # once, before the ranks load it
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_shard_main, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    got = {}
+    for _ in range(world):
+        r, o, hT, tokens, job = q.get(timeout=300)
+        got[r] = (o, hT, tokens, job)
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    cfg = CHUNK_CONFIGS["small"]
+    for r in range(world):
+        qi, ki, vi, ai, h0 = bench.replica_inputs(cfg, r, "cpu")
+        o, hT = gla_oracle.forward_torch(qi, ki, vi, ai, cfg.scale, h0, nthreads=1)
+        np.testing.assert_array_equal(got[r][0], o)
+        np.testing.assert_array_equal(got[r][1], hT)
+        assert got[r][2] == [cfg.tokens] * world
+        assert got[r][3] == sum(got[r][2])
+    assert not np.allclose(got[0][0], got[1][0])
