@@ -70,9 +70,9 @@ TRAFFIC_SOURCES = ["gla_chunk.cu", "gla_chunk_kernel.cuh", "gla_ptx.cuh"]
 # all six launches, for the backward sources hashed in "sources": captured at
 # B=1 H=4 (2,048 chunks) and scaled by the chunks of the long workload (16,384;
 # every chunk's inputs, states and gradients move once per launch)
-MEASURED_BWD_TRAFFIC = {"workload": "B2-H16-T32768-dk128-dv256", "sources": "87c4734e2d005a15",
-                        "bytes_per_call": 8 * (821_586_432 + 474_372_352 + 768_244_480
-                                               + 994_942_976 + 135_424)}
+MEASURED_BWD_TRAFFIC = {"workload": "B2-H16-T32768-dk128-dv256", "sources": "9f9241ee65f9a264",
+                        "bytes_per_call": 8 * (818_819_584 + 474_715_392 + 768_919_296
+                                               + 994_489_088 + 134_400)}
 BWD_TRAFFIC_SOURCES = ["gla_backward.cu", "gla_ptx.cuh"]
 
 

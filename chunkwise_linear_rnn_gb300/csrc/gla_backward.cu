@@ -71,10 +71,11 @@ __device__ __forceinline__ void split_pair(float x, float y, uint32_t &hi, uint3
 
 // One unit (sequence n, head h; index n H + h) of the work, and where its
 // pieces of scratch begin.  Chunk states and state gradients live as
-// [unit][dk][dv/32][slot][32]: the 32-column groups of one row, chunk after
-// chunk, so that a scan over the chunks reads and writes whole consecutive
-// lines; a unit has nch + 1 state slots and nch gradient slots.  Per-chunk
-// arrays (decay, carry, flags) hold a unit's nch chunks from `cbase` on.
+// [unit][slot][dk][dv]: each chunk's dk x dv block in one piece, so that the
+// chunk sums write, and the in-chunk kernel reads, whole contiguous blocks
+// (the scans step one block per chunk); a unit has nch + 1 state slots and
+// nch gradient slots.  Per-chunk arrays (decay, carry, flags) hold a unit's
+// nch chunks from `cbase` on.
 struct Unit {
     int nch;             // chunks of the sequence
     long long sbase;     // first state slot of the unit
@@ -133,11 +134,11 @@ __device__ __forceinline__ Chunk chunk_at(const BwdLaunch &p, long long g, int h
     return k;
 }
 
-// Float offset of (row i, column c) of slot u in a unit's states or gradients.
+// Float offset of (row i, column c) of slot u of a unit whose slots begin at
+// slot `base` of the states or gradients.
 template <int DK, int DV>
-__device__ __forceinline__ size_t slot_index(long long base, int i, int c, int u, int slots) {
-    return static_cast<size_t>(base) * DK * DV +
-           ((static_cast<size_t>(i) * (DV / 32) + (c >> 5)) * slots + u) * 32 + (c & 31);
+__device__ __forceinline__ size_t slot_index(long long base, int i, int c, int u) {
+    return ((static_cast<size_t>(base) + u) * DK + i) * DV + c;
 }
 
 // Load one chunk of log-gates (log2 units, rows past the sequence end zero,
@@ -196,150 +197,290 @@ __device__ __forceinline__ void load_prefix(float *sG, const float *__restrict__
 }
 
 // ---------------------------------------------------------------------------
-// 1. chunk sums on the tensor cores.  CTA (u, bh, which): which = 0 gives the
-//    state a chunk adds from a zero start, dS_u = (K e^(Gamma_C - Gamma))^T V;
-//    which = 1 the state gradient its outputs add, dR_u = scale (Q e^Gamma)^T dO.
+// 1. chunk sums on the tensor cores.  Work item (which, chunk, head), the
+//    chunk index fastest: which = 0 gives the state a chunk adds from a zero
+//    start, dS_u = (K e^(Gamma_C - Gamma))^T V; which = 1 the state gradient
+//    its outputs add, dR_u = scale (Q e^Gamma)^T dO.
 //    M = 128 key channels (zero rows past dk), N = dv, K = the chunk's tokens.
 //    The key-side operand is split into a bf16 pair (hi + lo, 16 significant
 //    bits) because these sums accumulate over the whole sequence; V and dO
 //    are bf16 inputs, exact.  Operand tiles are 128-byte swizzled, 64
 //    channels (or value columns) per block, read MN-major.
-constexpr int kSumThreads = 256;
+//    Persistent CTAs, item after item (CTA c takes items c, c + grid, ...),
+//    so that loads, products and stores of neighbouring items overlap:
+//      - the load warp's first thread stages an item's raw rows (log-gates,
+//        key-side rows, value-side rows; only the chunk's valid rows) by bulk
+//        copies into one of two staging buffers, as soon as the compute warps
+//        are done with the item that used the buffer before;
+//      - the 8 compute warps take the item's prefix sums in place, form the
+//        operand tiles, release the staging buffer, issue the products into
+//        one of two TMEM accumulators, and then store the previous item's
+//        sums while these products run.
+constexpr int kSumThreads = 256;                  // compute threads
+constexpr int kSumLoadWarp = kSumThreads / 32;    // the warp after them
+constexpr int kSumAllThreads = kSumThreads + 32;
 
 template <int DK, int DV>
 struct SumSmem {
     static constexpr uint32_t kBlk = BC * 128;              // one 64-column block of a tile
-    static constexpr uint32_t kA = 0;                       // A hi: two blocks (128 channels)
+    static constexpr uint32_t kGBytes = BC * DK * 4;        // staged log-gates, then prefix sums
+    static constexpr uint32_t kABytes = BC * DK * 2;        // staged key-side rows
+    static constexpr uint32_t kBBytes = BC * DV * 2;        // staged value-side rows
+    static constexpr uint32_t kStage = kGBytes + kABytes + kBBytes;
+    static constexpr uint32_t kSt = 0;                      // two staging buffers
+    static constexpr uint32_t kA = 2 * kStage;              // A hi: two blocks (128 channels)
     static constexpr uint32_t kAlo = kA + 2 * kBlk;
     static constexpr uint32_t kB = kAlo + 2 * kBlk;         // B: DV / 64 blocks
-    static constexpr uint32_t kG = kB + (DV / 64) * kBlk;   // fp32 prefix sums [BC][DK]
-    static constexpr uint32_t kBar = kG + BC * DK * 4;
-    static constexpr uint32_t kSlot = kBar + 8;
-    static constexpr uint32_t kBytes = kSlot + 8 + 1024;    // + alignment slack
+    static constexpr uint32_t kBar = kB + (DV / 64) * kBlk;  // full[2], empty[2], done[2], drain
+    static constexpr uint32_t kSlot = kBar + 8 * 8;
+    static constexpr uint32_t kBytes = kSlot + 16 + 1024;   // + alignment slack
+    static_assert(kStage % 1024 == 0, "operand tiles stay 1024-byte aligned");
+    static_assert(kStage >= 8 * 32 * 32 * 4, "a staging buffer holds the 8 warps' store blocks");
+    static_assert(kBytes <= 232448, "shared memory budget exceeded");
 };
 
+// Item w of the chunk sums: chunk fastest, then head, then which.
+struct SumItem {
+    long long g;   // chunk over all sequences (one head)
+    int h, which;
+};
+
+__device__ __forceinline__ SumItem sum_item(const BwdLaunch &p, long long w) {
+    SumItem it;
+    it.g = w % p.chunks;
+    const long long r = w / p.chunks;
+    it.h = static_cast<int>(r % p.H);
+    it.which = static_cast<int>(r / p.H);
+    return it;
+}
+
+// AND of `pred` over the `n` threads of named barrier `id`.
+__device__ __forceinline__ bool bar_and(int id, int n, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(pred ? 1u : 0u), "r"(id), "r"(n)
+        : "memory");
+    return r != 0u;
+}
+
 template <int DK, int DV>
-__global__ void __launch_bounds__(kSumThreads, 2) bwd_sums_kernel(BwdLaunch p) {
+__global__ void __launch_bounds__(kSumAllThreads, 1) bwd_sums_kernel(BwdLaunch p, long long items) {
     constexpr int NTS = kSumThreads;
     using L = SumSmem<DK, DV>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *sA = sm + L::kA, *sAlo = sm + L::kAlo, *sB = sm + L::kB;
-    float *sG = reinterpret_cast<float *>(sm + L::kG);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::kBar);
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + L::kBar);
+    uint64_t *empty = full + 2, *done = full + 4, *drain = full + 6;
     uint32_t *slot = reinterpret_cast<uint32_t *>(sm + L::kSlot);
-    const Chunk ck = chunk_at(p, blockIdx.x, blockIdx.y);
-    const int u = ck.c, n = ck.n, which = blockIdx.z;
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const size_t rk = static_cast<size_t>(ck.row) * DK;   // first row, key-side tensors
-    const size_t rv = static_cast<size_t>(ck.row) * DV;   // first row, value-side tensors
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const long long first = blockIdx.x, stride = gridDim.x;
+    const int nitems = first < items ? static_cast<int>((items - 1 - first) / stride + 1) : 0;
 
-    if (warp == 0) tmem_alloc(slot, DV);
+    if (warp == 0) tmem_alloc(slot, 2 * DV);   // two accumulators of DV columns
     if (tid == 0) {
-        mbar_init(bar, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&full[b], 1);
+            mbar_init(&empty[b], NTS / 32);
+            mbar_init(&done[b], 1);
+        }
+        mbar_init(drain, 1);
         fence_mbar_init();
     }
-    // the gates first (the prefix sums need them first), then the key-side and
-    // value-side loads, which land during the prefix sums
-    float4 gr[BC * DK / 4 / NTS];
-    prefix_issue<DK, NTS>(gr, p.log_alpha + rk, n);
-    const __nv_bfloat16 *asrc = which ? p.q : p.k;
-    const __nv_bfloat16 *bsrc = which ? p.d_o : p.v;
-    constexpr int APER = BC * 64 / NTS;           // channel pairs per thread
-    constexpr int BPER = BC * DV / 8 / NTS;       // 16-byte value groups per thread
-    uint32_t araw[APER];
-    uint4 braw[BPER];
-#pragma unroll
-    for (int m = 0; m < APER; ++m) {
-        const int e = tid + m * NTS, t = e >> 6, i = (e & 63) * 2;
-        araw[m] = (t < n && i < DK)
-                      ? *reinterpret_cast<const uint32_t *>(asrc + rk + static_cast<size_t>(t) * DK + i)
-                      : 0u;
-    }
-#pragma unroll
-    for (int m = 0; m < BPER; ++m) {
-        const int e = tid + m * NTS, t = e / (DV / 8), c = (e % (DV / 8)) * 8;
-        braw[m] = t < n ? *reinterpret_cast<const uint4 *>(bsrc + rv + static_cast<size_t>(t) * DV + c)
-                        : make_uint4(0u, 0u, 0u, 0u);
-    }
-    prefix_finish<DK, DK, NTS>(sG, gr);
-
-    // A: rows = tokens, columns = key channels, scaled and split
-#pragma unroll
-    for (int m = 0; m < APER; ++m) {
-        const int e = tid + m * NTS, t = e >> 6, i = (e & 63) * 2;
-        uint32_t hi = 0u, lo = 0u;
-        if (t < n && i < DK) {
-            const float f0 = __uint_as_float(araw[m] << 16), f1 = __uint_as_float(araw[m] & 0xffff0000u);
-            const float g0 = sG[t * DK + i], g1 = sG[t * DK + i + 1];
-            const float e0 = which ? exp2f(g0) : exp2f(sG[(BC - 1) * DK + i] - g0);
-            const float e1 = which ? exp2f(g1) : exp2f(sG[(BC - 1) * DK + i + 1] - g1);
-            split_pair(f0 * e0, f1 * e1, hi, lo);
-        }
-        const uint32_t off = sw128_offset(t, i, L::kBlk);
-        *reinterpret_cast<uint32_t *>(sA + off) = hi;
-        *reinterpret_cast<uint32_t *>(sAlo + off) = lo;
-    }
-    // B: rows = tokens, columns = value columns (bf16 copied as is)
-#pragma unroll
-    for (int m = 0; m < BPER; ++m) {
-        const int e = tid + m * NTS, t = e / (DV / 8), c = (e % (DV / 8)) * 8;
-        *reinterpret_cast<uint4 *>(sB + sw128_offset(t, c, L::kBlk)) = braw[m];
-    }
-    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *slot;
-    if (tid == 0) {
-        constexpr uint32_t id = idesc_bf16(128, DV, true, true);
-        const uint32_t aA = smem_u32(sA), aAlo = smem_u32(sAlo), aB = smem_u32(sB);
-#pragma unroll
-        for (int ks = 0; ks < BC / 16; ++ks) {
-            const uint64_t db = sw128_desc(aB + ks * 2048, L::kBlk, 1024);
-            mma_bf16_ss(tmem, sw128_desc(aA + ks * 2048, L::kBlk, 1024), db, id, ks > 0);
-            mma_bf16_ss(tmem, sw128_desc(aAlo + ks * 2048, L::kBlk, 1024), db, id, 1);
-        }
-        mma_commit(bar);
-    }
-    const bool ok = mbar_wait_bounded(bar, 0, p.status);
-    tc_fence_after();
 
-    // epilogue: thread = key channel = TMEM lane (32 (warp % 4) + lane); warps
-    // 0-3 store the first half of the value columns, warps 4-7 the second.
-    // Each 32-column group of a row is one 128-byte line of the scratch.
-    const int i = 32 * (warp & 3) + (tid & 31);
-    const float mult = which ? p.scale : 1.f;
-    const int slots = which ? ck.w.nch : ck.w.nch + 1;
-    float *dst = (which ? p.adjoints : p.states) +
-                 slot_index<DK, DV>(which ? ck.w.rbase : ck.w.sbase, i < DK ? i : 0, 0, u, slots);
-    const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-    const int cbeg = warp < 4 ? 0 : DV / 2, cend = warp < 4 ? DV / 2 : DV;
+    if (warp == kSumLoadWarp) {
+        // ================================================= load warp
+        int issued = 0;
+        if (lane == 0) {
+            for (int kk = 0; kk < nitems; ++kk) {
+                const int s = kk & 1;
+                // the compute warps are done with item kk - 2, which used this buffer
+                if (kk >= 2 && !mbar_wait_bounded(&empty[s], ((kk - 2) >> 1) & 1, p.status)) break;
+                const SumItem it = sum_item(p, first + kk * stride);
+                const Chunk ck = chunk_at(p, it.g, it.h);
+                const uint32_t n = static_cast<uint32_t>(ck.n);
+                const size_t rk = static_cast<size_t>(ck.row) * DK;
+                const size_t rv = static_cast<size_t>(ck.row) * DV;
+                uint8_t *st = sm + L::kSt + s * L::kStage;
+                mbar_arrive_expect_tx(&full[s], n * (DK * 4 + DK * 2 + DV * 2));
+                bulk_load(st, p.log_alpha + rk, n * DK * 4, &full[s]);
+                bulk_load(st + L::kGBytes, (it.which ? p.q : p.k) + rk, n * DK * 2, &full[s]);
+                bulk_load(st + L::kGBytes + L::kABytes, (it.which ? p.d_o : p.v) + rv, n * DV * 2,
+                          &full[s]);
+                issued = kk + 1;
+            }
+            // every copy issued here lands before the shared memory is given up
+            for (int c = issued > 2 ? issued - 2 : 0; c < issued; ++c)
+                mbar_wait_bounded(&full[c & 1], (c >> 1) & 1, p.status);
+        }
+        __syncwarp();
+    } else {
+        // ================================================= compute warps
+        bool ok = true;
+        // the stores of item j's sums from TMEM accumulator j & 1.  A warp
+        // reads key channels 32 (warp % 4) .. + 31 (its TMEM lanes, one row per
+        // thread), warps 0-3 the first half of the value columns, warps 4-7 the
+        // second, 32 columns at a time; each 32 x 32 block goes through the
+        // warp's 4 KB of `xbuf` (16-byte pieces XOR-swizzled by row, so that
+        // neither side has bank conflicts), and 8 threads then store one row's
+        // 128 bytes: every store instruction writes 4 whole lines.
+        auto store_sums = [&](int j, uint8_t *xbuf) {
+            const SumItem it = sum_item(p, first + j * stride);
+            const Chunk ck = chunk_at(p, it.g, it.h);
+            const float mult = it.which ? p.scale : 1.f;
+            float *dst = it.which ? p.adjoints : p.states;
+            const long long base = it.which ? ck.w.rbase : ck.w.sbase;
+            float *xw = reinterpret_cast<float *>(xbuf) + warp * 1024;
+            const int i0 = 32 * (warp & 3);
+            const uint32_t taddr = tmem + (j & 1) * DV + (static_cast<uint32_t>(i0) << 16);
+            const int cbeg = warp < 4 ? 0 : DV / 2, cend = warp < 4 ? DV / 2 : DV;
 #pragma unroll 1
-    for (int c0 = cbeg; c0 < cend; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(taddr + c0, r);
-        tmem_wait_ld();
-        if (ok && i < DK) {
-            float *row = dst + static_cast<size_t>(c0 >> 5) * slots * 32;
+            for (int c0 = cbeg; c0 < cend; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld32(taddr + c0, r);
+                tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; j += 4)
-                *reinterpret_cast<float4 *>(row + j) =
-                    make_float4(__uint_as_float(r[j]) * mult, __uint_as_float(r[j + 1]) * mult,
-                                __uint_as_float(r[j + 2]) * mult, __uint_as_float(r[j + 3]) * mult);
+                for (int x = 0; x < 8; ++x)
+                    *reinterpret_cast<float4 *>(xw + lane * 32 + ((x ^ (lane & 7)) << 2)) =
+                        make_float4(__uint_as_float(r[4 * x]) * mult, __uint_as_float(r[4 * x + 1]) * mult,
+                                    __uint_as_float(r[4 * x + 2]) * mult, __uint_as_float(r[4 * x + 3]) * mult);
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int rr = 4 * k + (lane >> 3), x = lane & 7;
+                    const float4 v = *reinterpret_cast<const float4 *>(xw + rr * 32 + ((x ^ (rr & 7)) << 2));
+                    if (ok && i0 + rr < DK)
+                        *reinterpret_cast<float4 *>(dst + slot_index<DK, DV>(base, i0 + rr, c0 + 4 * x, ck.c)) = v;
+                }
+                __syncwarp();
+            }
+        };
+        int kk = 0;
+#pragma unroll 1
+        for (; kk < nitems; ++kk) {
+            const int s = kk & 1;
+            const SumItem it = sum_item(p, first + kk * stride);
+            const Chunk ck = chunk_at(p, it.g, it.h);
+            const int n = ck.n, which = it.which;
+            uint8_t *st = sm + L::kSt + s * L::kStage;
+            float *sG = reinterpret_cast<float *>(st);
+            const uint8_t *sa = st + L::kGBytes, *sb = st + L::kGBytes + L::kABytes;
+            ok = mbar_wait_bounded(&full[s], (kk >> 1) & 1, p.status) && ok;
+            ok = bar_and(1, NTS, ok);   // one verdict for the compute warps
+            if (!ok) break;
+            // inclusive prefix sums of the log-gates (log2 units), in place, one
+            // channel per thread; rows past the chunk's valid ones count as zero
+            if (tid < DK) {
+                float acc = 0.f;
+#pragma unroll
+                for (int t0 = 0; t0 < BC; t0 += 16) {
+                    float x[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        x[j] = t0 + j < n ? sG[(t0 + j) * DK + tid] * kLog2e : 0.f;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        acc += x[j];
+                        sG[(t0 + j) * DK + tid] = acc;
+                    }
+                }
+            }
+            // the operand tiles are free once item kk - 1's products are done
+            if (kk >= 1) ok = mbar_wait_bounded(&done[(kk - 1) & 1], ((kk - 1) >> 1) & 1, p.status) && ok;
+            named_barrier(1, NTS);   // the prefix sums
+            tc_fence_after();
+            // A: rows = tokens, columns = key channels, scaled and split
+            constexpr int APER = BC * 64 / NTS;           // channel pairs per thread
+#pragma unroll
+            for (int m = 0; m < APER; ++m) {
+                const int e = tid + m * NTS, t = e >> 6, i = (e & 63) * 2;
+                uint32_t hi = 0u, lo = 0u;
+                if (t < n && i < DK) {
+                    const uint32_t a = *reinterpret_cast<const uint32_t *>(sa + (t * DK + i) * 2);
+                    const float f0 = __uint_as_float(a << 16), f1 = __uint_as_float(a & 0xffff0000u);
+                    const float g0 = sG[t * DK + i], g1 = sG[t * DK + i + 1];
+                    const float e0 = which ? exp2f(g0) : exp2f(sG[(BC - 1) * DK + i] - g0);
+                    const float e1 = which ? exp2f(g1) : exp2f(sG[(BC - 1) * DK + i + 1] - g1);
+                    split_pair(f0 * e0, f1 * e1, hi, lo);
+                }
+                const uint32_t off = sw128_offset(t, i, L::kBlk);
+                *reinterpret_cast<uint32_t *>(sA + off) = hi;
+                *reinterpret_cast<uint32_t *>(sAlo + off) = lo;
+            }
+            // B: rows = tokens, columns = value columns (bf16 copied as is)
+            constexpr int BPER = BC * DV / 8 / NTS;       // 16-byte value groups per thread
+#pragma unroll
+            for (int m = 0; m < BPER; ++m) {
+                const int e = tid + m * NTS, t = e / (DV / 8), c = (e % (DV / 8)) * 8;
+                const uint4 b = t < n ? *reinterpret_cast<const uint4 *>(sb + (t * DV + c) * 2)
+                                      : make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4 *>(sB + sw128_offset(t, c, L::kBlk)) = b;
+            }
+            if (which == 0 && warp < 4) {
+                const int i = 32 * warp + lane;
+                if (i < DK) p.decay[static_cast<size_t>(ck.w.rbase + ck.c) * DK + i] = exp2f(sG[(BC - 1) * DK + i]);
+            }
+            fence_proxy_async_smem();   // the tiles, before the tensor core reads them
+            tc_fence_before();
+            ok = bar_and(1, NTS, ok);   // the tiles, and the previous item's verdict
+            tc_fence_after();
+            if (!ok) break;
+            if (tid == 0) {
+                constexpr uint32_t id = idesc_bf16(128, DV, true, true);
+                const uint32_t aA = smem_u32(sA), aAlo = smem_u32(sAlo), aB = smem_u32(sB);
+                const uint32_t acc = tmem + s * DV;
+#pragma unroll
+                for (int ks = 0; ks < BC / 16; ++ks) {
+                    const uint64_t db = sw128_desc(aB + ks * 2048, L::kBlk, 1024);
+                    mma_bf16_ss(acc, sw128_desc(aA + ks * 2048, L::kBlk, 1024), db, id, ks > 0);
+                    mma_bf16_ss(acc, sw128_desc(aAlo + ks * 2048, L::kBlk, 1024), db, id, 1);
+                }
+                mma_commit(&done[s]);
+            }
+            // the previous item's sums, while these products run, through this
+            // item's staging buffer (every warp is done reading it: the barrier
+            // above); then the buffer goes back to the load warp, the generic
+            // writes to it ordered before the next bulk copy into it
+            if (kk >= 1) store_sums(kk - 1, st);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+            tc_fence_before();
+        }
+        // the last item's sums (after a full run of the loop)
+        if (ok && kk == nitems && nitems > 0) {
+            ok = mbar_wait_bounded(&done[(nitems - 1) & 1], ((nitems - 1) >> 1) & 1, p.status);
+            tc_fence_after();
+            store_sums(nitems - 1, sm + L::kSt + ((nitems - 1) & 1) * L::kStage);
+        }
+        // every product issued here completes before TMEM is given up
+        if (tid == 0) {
+            mma_commit(drain);
+            mbar_wait_bounded(drain, 0, p.status);
         }
     }
-    if (which == 0 && warp < 4 && i < DK)
-        p.decay[static_cast<size_t>(ck.w.rbase + u) * DK + i] = exp2f(sG[(BC - 1) * DK + i]);
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, DV);
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 2 * DV);
+    }
 }
 
 // ---------------------------------------------------------------------------
 // 2. scans over the chunks, one thread per state element (bh, i, c), value
-//    columns fastest so that a warp covers 32 columns of one row.
+//    columns fastest so that a warp covers 32 columns of one row (one
+//    128-byte line of each chunk's block; the next chunk's is a block on).
 //    States:    slot u holds dS_u on entry and S_u on exit, slot NC gets hT:
 //               S_(u+1) = e^Gamma_C(u) S_u + dS_u, S_0 = h0.
 //    Gradients: slot u holds dR_u on entry and R_u on exit, dh0 = R_(-1):
@@ -353,8 +494,8 @@ __global__ void __launch_bounds__(256, 3) bwd_state_scan_kernel(BwdLaunch p) {
     const Unit w = unit_at(p, static_cast<int>(e / (DK * DV)));
     const int NCu = w.nch;
     const int rem = static_cast<int>(e % (DK * DV)), i = rem / DV;
-    constexpr size_t kM = 32;   // one slot step
-    float *buf = p.states + slot_index<DK, DV>(w.sbase, i, rem % DV, 0, NCu + 1);
+    constexpr size_t kM = static_cast<size_t>(DK) * DV;   // one slot step
+    float *buf = p.states + slot_index<DK, DV>(w.sbase, i, rem % DV, 0);
     const float *dec = p.decay + static_cast<size_t>(w.rbase) * DK + i;
     float S = p.h0 ? p.h0[e] : 0.f;
     float d[kScanUnroll], a[kScanUnroll];
@@ -395,9 +536,9 @@ __global__ void __launch_bounds__(256, 2) bwd_adjoint_scan_kernel(BwdLaunch p) {
     const int NCu = w.nch;
     const int rem = static_cast<int>(e % (DK * DV)), i = rem / DV, c = rem % DV;
     const int lane = threadIdx.x & 31;
-    constexpr size_t kM = 32;   // one slot step
-    float *buf = p.adjoints + slot_index<DK, DV>(w.rbase, i, c, 0, NCu);
-    const float *st = p.states + slot_index<DK, DV>(w.sbase, i, c, 0, NCu + 1);
+    constexpr size_t kM = static_cast<size_t>(DK) * DV;   // one slot step
+    float *buf = p.adjoints + slot_index<DK, DV>(w.rbase, i, c, 0);
+    const float *st = p.states + slot_index<DK, DV>(w.sbase, i, c, 0);
     const float *dec = p.decay + static_cast<size_t>(w.rbase) * DK + i;
     float *carry = p.carry + static_cast<size_t>(w.rbase) * NTILE * DK + (c / TW) * DK + i;
     float R = p.dhT ? p.dhT[e] : 0.f;
@@ -537,9 +678,9 @@ __global__ void __launch_bounds__(kInterThreads, 1) bwd_inter_kernel(BwdLaunch p
                 rr[m] = sv[m];
                 if (i < DK && cb + cl < DV) {
                     sv[m] = *reinterpret_cast<const float4 *>(
-                        p.states + slot_index<DK, DV>(ck.w.sbase, i, cb + cl, u, ck.w.nch + 1));
+                        p.states + slot_index<DK, DV>(ck.w.sbase, i, cb + cl, u));
                     rr[m] = *reinterpret_cast<const float4 *>(
-                        p.adjoints + slot_index<DK, DV>(ck.w.rbase, i, cb + cl, u, ck.w.nch));
+                        p.adjoints + slot_index<DK, DV>(ck.w.rbase, i, cb + cl, u));
                 }
             }
 #pragma unroll
@@ -885,9 +1026,9 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
         for (int m = 0; m < SPER; ++m) {
             const int e = tid + m * NTI, i = e / 16, cl = (e % 16) * 4;
             sv[m] = *reinterpret_cast<const float4 *>(
-                p.states + slot_index<DK, DV>(ck.w.sbase, i, c0 + cl, u, ck.w.nch + 1));
+                p.states + slot_index<DK, DV>(ck.w.sbase, i, c0 + cl, u));
             rr[m] = *reinterpret_cast<const float4 *>(
-                p.adjoints + slot_index<DK, DV>(ck.w.rbase, i, c0 + cl, u, ck.w.nch));
+                p.adjoints + slot_index<DK, DV>(ck.w.rbase, i, c0 + cl, u));
         }
     };
     fetch(0);
@@ -1393,7 +1534,18 @@ int launch_bwd_dims(const BwdLaunch &p, cudaStream_t stream) {
         bwd_adjoint_scan_kernel<DK, DV><<<scan_blocks, 256, 0, stream>>>(p);
         return static_cast<int>(cudaGetLastError());
     }
-    bwd_sums_kernel<DK, DV><<<dim3(nchunks, p.H, 2), kSumThreads, sum_bytes, stream>>>(p);
+    // chunk sums: persistent CTAs, as many as fit on the GPU at once
+    const long long items = 2LL * p.chunks * p.H;
+    int dev = 0, sms = 0, per_sm = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bwd_sums_kernel<DK, DV>,
+                                                          kSumAllThreads, sum_bytes);
+    if (e != cudaSuccess) return static_cast<int>(e);
+    const long long slots = static_cast<long long>(sms) * (per_sm > 0 ? per_sm : 1);
+    const unsigned sum_grid = static_cast<unsigned>(items < slots ? items : slots);
+    bwd_sums_kernel<DK, DV><<<sum_grid, kSumAllThreads, sum_bytes, stream>>>(p, items);
     bwd_state_scan_kernel<DK, DV><<<scan_blocks, 256, 0, stream>>>(p);
     bwd_adjoint_scan_kernel<DK, DV><<<scan_blocks, 256, 0, stream>>>(p);
     bwd_intra_kernel<DK, DV><<<dim3(nchunks, p.H), kIntraThreads, intra_bytes, stream>>>(p);
