@@ -831,6 +831,17 @@ struct IntraSmem {
     static constexpr uint32_t kCols = kUsed <= 256 ? 256 : 512;
     static_assert(BC * LP * 4 <= 4 * (DK / 64) * kBlk, "P fits over the q/k tiles");
     static_assert(kKr + BC * DK * 2 <= kMl + kBlk, "raw q, k fit over the dO, V and A/M tiles");
+    // epilogue 2's staging rows (bf16 dq, dk and dv): dq and dk after the raw
+    // rows where the dO, V and A/M tiles have room, dv after them or else past
+    // P in the q/k tiles; without room for dq and dk (dk 128 with dv 64) those
+    // two are stored from the rows' own threads
+    static constexpr uint32_t kRawEnd = kKr + BC * DK * 2;
+    static constexpr bool kStageQK = kRawEnd + 2 * BC * DK * 2 <= kMl + kBlk;
+    static constexpr uint32_t kXqk = kRawEnd;
+    static constexpr uint32_t kAfterQK = kStageQK ? kRawEnd + 2 * BC * DK * 2 : kRawEnd;
+    static constexpr uint32_t kPEnd = (kQh + BC * LP * 4 + 15) & ~15u;
+    static constexpr uint32_t kXv = kAfterQK + BC * DV * 2 <= kMl + kBlk ? kAfterQK : kPEnd;
+    static_assert(kXv != kPEnd || kPEnd + BC * DV * 2 <= kDo, "the dv rows of epilogue 2 have room");
 };
 
 // Columns: A [0, 64), M [64, 128) first; then dV over [0, 128) (+ [2 dk + 128, ...) for
@@ -1120,12 +1131,19 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
 
     // epilogue 2.  Warps 0-3: row t of dQ and dK, q dq - k dk into P.  Warps
     // 4-7: row j of dV.  Thread = row t and 16 columns of each 32-column block
-    // (half-split loads, as in epilogue 1).
+    // (half-split loads, as in epilogue 1).  The bf16 rows go through shared
+    // memory (the V and A/M tiles, free by now; each warp its own 16 rows,
+    // 16-byte pieces XOR-swizzled by row), so that each warp then stores
+    // whole rows: a store instruction writes 512 contiguous bytes.
     float *sP = reinterpret_cast<float *>(sm + L::kQh);
     {
-        const int q4 = warp & 3, t = 16 * q4 + (lane & 15), hc = (lane >> 4) * 16;
+        const int q4 = warp & 3, r16 = lane & 15, t = 16 * q4 + r16, hc = (lane >> 4) * 16;
         const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
         const bool row_ok = ok && t < n;
+        // the warp's staging rows and the offset of row r's 16-byte piece c
+        uint8_t *xq = sm + L::kXqk + q4 * (2 * 16 * DK * 2), *xk = xq + 16 * DK * 2;
+        uint8_t *xv = sm + L::kXv + q4 * (16 * DV * 2);
+        auto piece = [](int r, int c, int row_bytes) { return r * row_bytes + ((c ^ (r & 7)) << 4); };
         if (warp < 4) {
             const float *grow = sG + t * LG;
             // this thread's q and k columns from the rows loaded above (rows
@@ -1167,13 +1185,29 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
                         dkw[x / 2] = pack_bf16x2(dkv[0], dkv[1]);
                     }
                     const int i0 = ib + hc + h * 8;
-                    if (row_ok && qk_ok) {
+                    if constexpr (L::kStageQK) {
+                        *reinterpret_cast<uint4 *>(xq + piece(r16, i0 >> 3, DK * 2)) =
+                            make_uint4(dqw[0], dqw[1], dqw[2], dqw[3]);
+                        *reinterpret_cast<uint4 *>(xk + piece(r16, i0 >> 3, DK * 2)) =
+                            make_uint4(dkw[0], dkw[1], dkw[2], dkw[3]);
+                    } else if (row_ok && qk_ok) {
                         const size_t off = rk + static_cast<size_t>(t) * DK + i0;
                         *reinterpret_cast<uint4 *>(p.gq + off) = make_uint4(dqw[0], dqw[1], dqw[2], dqw[3]);
                         *reinterpret_cast<uint4 *>(p.gk + off) = make_uint4(dkw[0], dkw[1], dkw[2], dkw[3]);
                     }
 #pragma unroll
                     for (int x = 0; x < 8; ++x) sP[t * LP + i0 + x] = row_ok && qk_ok ? pr[x] : 0.f;
+                }
+            }
+            __syncwarp();
+            const bool wok = __all_sync(0xffffffffu, ok && qk_ok);
+#pragma unroll
+            for (int m = 0; m < (L::kStageQK ? 16 * DK / 8 / 32 : 0); ++m) {
+                const int e = lane + 32 * m, r = e / (DK / 8), c = e % (DK / 8);
+                if (wok && 16 * q4 + r < n) {
+                    const size_t off = rk + static_cast<size_t>(16 * q4 + r) * DK + c * 8;
+                    *reinterpret_cast<uint4 *>(p.gq + off) = *reinterpret_cast<const uint4 *>(xq + piece(r, c, DK * 2));
+                    *reinterpret_cast<uint4 *>(p.gk + off) = *reinterpret_cast<const uint4 *>(xk + piece(r, c, DK * 2));
                 }
             }
         } else {
@@ -1183,17 +1217,24 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_intra_kernel(BwdLaunch p
                 uint32_t rv_[16];
                 tmem_ld16x2<16>(tmem + lane_off + dcol, rv_);
                 tmem_wait_ld();
-                if (row_ok) {
 #pragma unroll
-                    for (int j = 0; j < 16; j += 4) {
-                        const size_t off = rv + static_cast<size_t>(t) * DV + cb + hc + j;
-                        const uint32_t w0 = pack_bf16x2(s * __uint_as_float(rv_[j]),
-                                                        s * __uint_as_float(rv_[j + 1]));
-                        const uint32_t w1 = pack_bf16x2(s * __uint_as_float(rv_[j + 2]),
-                                                        s * __uint_as_float(rv_[j + 3]));
-                        *reinterpret_cast<uint2 *>(p.gv + off) = make_uint2(w0, w1);
-                    }
+                for (int j = 0; j < 16; j += 8) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int x = 0; x < 4; ++x)
+                        w[x] = pack_bf16x2(s * __uint_as_float(rv_[j + 2 * x]), s * __uint_as_float(rv_[j + 2 * x + 1]));
+                    *reinterpret_cast<uint4 *>(xv + piece(r16, (cb + hc + j) >> 3, DV * 2)) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
                 }
+            }
+            __syncwarp();
+            const bool wok = __all_sync(0xffffffffu, ok);
+#pragma unroll
+            for (int m = 0; m < 16 * DV / 8 / 32; ++m) {
+                const int e = lane + 32 * m, r = e / (DV / 8), c = e % (DV / 8);
+                if (wok && 16 * q4 + r < n)
+                    *reinterpret_cast<uint4 *>(p.gv + rv + static_cast<size_t>(16 * q4 + r) * DV + c * 8) =
+                        *reinterpret_cast<const uint4 *>(xv + piece(r, c, DV * 2));
             }
         }
     }
