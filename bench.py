@@ -70,9 +70,9 @@ TRAFFIC_SOURCES = ["gla_chunk.cu", "gla_chunk_kernel.cuh", "gla_ptx.cuh"]
 # all six launches, for the backward sources hashed in "sources": captured at
 # B=1 H=4 (2,048 chunks) and scaled by the chunks of the long workload (16,384;
 # every chunk's inputs, states and gradients move once per launch)
-MEASURED_BWD_TRAFFIC = {"workload": "B2-H16-T32768-dk128-dv256", "sources": "9f9241ee65f9a264",
-                        "bytes_per_call": 8 * (818_819_584 + 474_715_392 + 768_919_296
-                                               + 994_489_088 + 134_400)}
+MEASURED_BWD_TRAFFIC = {"workload": "B2-H16-T32768-dk128-dv256", "sources": "78ecd605f9e52d28",
+                        "bytes_per_call": 8 * (810_661_632 + 474_801_408 + 769_031_680
+                                               + 994_191_360 + 134_400)}
 BWD_TRAFFIC_SOURCES = ["gla_backward.cu", "gla_ptx.cuh"]
 
 
